@@ -1,0 +1,410 @@
+/*
+ * sv_oracle.c -- CPU oracle for the speculative-decoding verify-and-sample step.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE (tests, smoke check and the bench's
+ * cpu_baseline/reference leg only).  Plain, single-threaded, double precision,
+ * written for a reader to check against the pages by eye.  Nothing here is
+ * blocked, fused or reordered for speed.
+ *
+ * Sources (page title, section):
+ *  [A1]  "Fast Inference from Transformers via Speculative Decoding"
+ *        (intuitivepapers.ai), "The loop: draft, verify in one pass, keep a
+ *        prefix", Algorithm 1: walk drafts left to right, accept x_i w.p.
+ *        min(1, p_i(x_i)/q_i(x_i)), stop at the first rejection, then one token
+ *        from the residual or, after a clean sweep, from p_{gamma+1}.
+ *  [A2]  same page, "Speculative sampling: the accept/reject rule": residual
+ *        p'(x) = max(0, p(x)-q(x)) / (1-beta), beta = sum_x min(p,q)
+ *        (Appendix A.1).
+ *  [A3]  same page, the paragraph on the distributions being "already adjusted":
+ *        temperature rescales the logits before the softmax; argmax is the
+ *        one-hot limit.
+ *  [B1]  "Speculative Decoding" (course notes), "The algorithm": u ~ U(0,1),
+ *        accept iff u <= min(1, p/q); "Exactness": residual normaliser.
+ *  [C1]  lihaoran.work essay, "What does unchanged output mean?": greedy mode
+ *        keeps the prefix matching the target's own selection.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - temperature: s = z * fl32(1/T) for target and draft rows alike;
+ *  - the accept comparison is "<=", with IEEE p/q (p/0 = inf accepts, 0/0 rejects);
+ *  - "sample" = Gumbel-max argmax(log w_v + g_v), g = -log(-log u), ties to the
+ *    lowest index, u from Philox4x32-10 with the documented counter layout;
+ *  - an all-zero residual (possible only by rounding) falls back to p_n;
+ *  - an empty row (no finite logit) emits token 0 and sets ZERO_MASS.
+ */
+#include "sv_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x32-10, from the SC'11 paper "Parallel random numbers: as easy as   */
+/* 1, 2, 3": two 32x32->64 multiplies per round, the high halves xored with   */
+/* the other two counter words and the round key, a Weyl-sequence key bump    */
+/* between rounds, ten rounds.                                                */
+/* ------------------------------------------------------------------------ */
+#define PHILOX_M0 0xD2511F53u
+#define PHILOX_M1 0xCD9E8D57u
+#define PHILOX_W0 0x9E3779B9u
+#define PHILOX_W1 0xBB67AE85u
+
+void svo_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += PHILOX_W0;
+      k1 += PHILOX_W1;
+    }
+    uint64_t prod0 = (uint64_t)PHILOX_M0 * (uint64_t)x0;
+    uint64_t prod1 = (uint64_t)PHILOX_M1 * (uint64_t)x2;
+    uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+    uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+    uint32_t y0 = hi1 ^ x1 ^ k0;
+    uint32_t y1 = lo1;
+    uint32_t y2 = hi0 ^ x3 ^ k1;
+    uint32_t y3 = lo0;
+    x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+  }
+  out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+double svo_uniform(uint64_t seed, uint32_t tag, uint32_t pos, uint32_t b,
+                   uint64_t round, uint32_t c0, int lane) {
+  uint32_t ctr[4] = {c0, (tag << 24) | (pos & 0xFFFFFFu), b, (uint32_t)round};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  svo_philox4x32_10(ctr, key, out);
+  uint32_t x = out[lane & 3];
+  /* 23 random bits -> odd multiple of 2^-24: strictly inside (0, 1). */
+  return (2.0 * (double)(x >> 9) + 1.0) * 0x1p-24;
+}
+
+void svo_uniform_row(uint64_t seed, uint32_t tag, uint32_t pos, uint32_t b, uint64_t round,
+                     int64_t v0, int64_t n, double* out) {
+  for (int64_t j = 0; j < n; ++j) {
+    int64_t v = v0 + j;
+    out[j] = svo_uniform(seed, tag, pos, b, round, (uint32_t)(v >> 2), (int)(v & 3));
+  }
+}
+
+/* Gumbel noise for vocabulary entry v at a draw position (tag 1). */
+static double gumbel(uint64_t seed, uint32_t pos, uint32_t b, uint64_t round, int64_t v) {
+  double u = svo_uniform(seed, 1u, pos, b, round, (uint32_t)(v >> 2), (int)(v & 3));
+  return -log(-log(u));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Probability-level pieces ([A2], [B1]).                                     */
+/* ------------------------------------------------------------------------ */
+
+/* Accepted mass per token, min(p, q); returns beta = its sum. */
+double svo_accept_mass(const double* p, const double* q, int64_t V, double* out_min) {
+  double beta = 0.0;
+  for (int64_t v = 0; v < V; ++v) {
+    double m = p[v] < q[v] ? p[v] : q[v];
+    if (out_min) out_min[v] = m;
+    beta += m;
+  }
+  return beta;
+}
+
+/* Residual distribution max(0, p - q) normalised by its sum; returns the sum
+ * (the rejection probability 1 - beta).  A zero sum is not normalised. */
+double svo_residual(const double* p, const double* q, int64_t V, double* out_resid) {
+  double mass = 0.0;
+  for (int64_t v = 0; v < V; ++v) {
+    double r = p[v] - q[v];
+    r = r > 0.0 ? r : 0.0;
+    if (out_resid) out_resid[v] = r;
+    mass += r;
+  }
+  if (out_resid && mass > 0.0)
+    for (int64_t v = 0; v < V; ++v) out_resid[v] /= mass;
+  return mass;
+}
+
+/* Max-subtracted softmax; returns S = sum_v exp(s_v - max). */
+double svo_softmax(const double* s, int64_t V, double* p) {
+  double m = -INFINITY;
+  for (int64_t v = 0; v < V; ++v)
+    if (s[v] > m) m = s[v];
+  if (m == -INFINITY) { /* no finite entry */
+    if (p) for (int64_t v = 0; v < V; ++v) p[v] = 0.0;
+    return 0.0;
+  }
+  double S = 0.0;
+  for (int64_t v = 0; v < V; ++v) S += exp(s[v] - m);
+  if (p) for (int64_t v = 0; v < V; ++v) p[v] = exp(s[v] - m) / S;
+  return S;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Logit rows.                                                               */
+/* ------------------------------------------------------------------------ */
+static double logit_at(const void* base, int dtype, int64_t idx) {
+  if (dtype == SVO_F32) return (double)((const float*)base)[idx];
+  uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+typedef struct {
+  double* s;  /* scaled logits s_v = z_v * invT          */
+  double m;   /* max_v s_v                                */
+  double S;   /* sum_v exp(s_v - m), 0 if no finite entry */
+} row_t;
+
+/* Temperature then softmax statistics of one row ([A3]). */
+static void load_row(row_t* r, const void* base, int dtype, int64_t off, int64_t V, double invT) {
+  for (int64_t v = 0; v < V; ++v) r->s[v] = logit_at(base, dtype, off + v) * invT;
+  double m = -INFINITY;
+  for (int64_t v = 0; v < V; ++v)
+    if (r->s[v] > m) m = r->s[v];
+  double S = 0.0;
+  if (m != -INFINITY)
+    for (int64_t v = 0; v < V; ++v) S += exp(r->s[v] - m);
+  r->m = m;
+  r->S = S;
+}
+
+static double prob(const row_t* r, int64_t v) {
+  if (!(r->S > 0.0)) return 0.0;
+  return exp(r->s[v] - r->m) / r->S;
+}
+
+static int row_nonfinite(const row_t* r) { return !isfinite(r->S) || isnan(r->m) || r->m == INFINITY; }
+
+/* Gumbel-max over the entries whose log-weight lw(v) is finite:
+ * argmax_v lw(v) + g_v, ties to the lowest v.  Returns -1 if there is no
+ * candidate; *gap = top1 - top2 key (inf with a single candidate). */
+typedef double (*logw_fn)(const void* ctx, int64_t v);
+
+static int64_t gumbel_argmax(logw_fn lw, const void* ctx, int64_t V, uint64_t seed, uint32_t pos,
+                             uint32_t b, uint64_t round, double* gap) {
+  int64_t best = -1;
+  double k1 = -INFINITY, k2 = -INFINITY;
+  for (int64_t v = 0; v < V; ++v) {
+    double w = lw(ctx, v);
+    if (!(w > -INFINITY) || w == INFINITY) continue; /* excludes -inf, NaN, +inf */
+    double key = w + gumbel(seed, pos, b, round, v);
+    if (best < 0 || key > k1) {
+      k2 = k1;
+      k1 = key;
+      best = v;
+    } else if (key > k2) {
+      k2 = key;
+    }
+  }
+  if (gap) *gap = best < 0 ? NAN : k1 - k2;
+  return best;
+}
+
+static double logw_scaled_logit(const void* ctx, int64_t v) { return ((const row_t*)ctx)->s[v]; }
+
+typedef struct {
+  const row_t* t;
+  const row_t* d;
+} pair_t;
+
+/* log max(0, p - q) with p, q the normalised target/draft probabilities. */
+static double logw_residual(const void* ctx, int64_t v) {
+  const pair_t* pr = (const pair_t*)ctx;
+  double r = prob(pr->t, v) - prob(pr->d, v);
+  return r > 0.0 ? log(r) : -INFINITY;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The verify step ([A1], [B1]).                                             */
+/* ------------------------------------------------------------------------ */
+int svo_spec_verify(const void* zt, const void* zd, const int32_t* xt,
+                    int B, int gamma, int64_t V, int dtype,
+                    float temperature, const float* row_temperature,
+                    uint64_t seed, uint64_t round,
+                    int32_t* tokens, int32_t* counts,
+                    double* p_at, double* q_at, double* ratio_out, double* u_out,
+                    double* beta_out, double* gumbel_gap, double* resid_mass,
+                    uint8_t* flags) {
+  if (B < 0 || gamma < 1 || gamma > 64 || V < 1 || (dtype != SVO_F32 && dtype != SVO_BF16))
+    return -1;
+  if (B == 0) return 0;
+  if (!zt || !zd || !xt || !tokens || !counts) return -1;
+
+  const int R = 2 * gamma + 1; /* rows 0..gamma: target, gamma+1..2gamma: draft */
+  row_t* rows = (row_t*)calloc((size_t)R, sizeof(row_t));
+  if (!rows) return -1;
+  for (int r = 0; r < R; ++r) {
+    rows[r].s = (double*)malloc((size_t)V * sizeof(double));
+    if (!rows[r].s) {
+      for (int k = 0; k < r; ++k) free(rows[k].s);
+      free(rows);
+      return -1;
+    }
+  }
+
+  for (int b = 0; b < B; ++b) {
+    float T = row_temperature ? row_temperature[b] : temperature;
+    /* Both sides use the single-precision reciprocal of T as the scale. */
+    float invT_f = 1.0f / T;
+    double invT = (double)invT_f;
+    uint8_t flag = 0;
+
+    for (int i = 0; i <= gamma; ++i)
+      load_row(&rows[i], zt, dtype, ((int64_t)b * (gamma + 1) + i) * V, V, invT);
+    for (int i = 0; i < gamma; ++i)
+      load_row(&rows[gamma + 1 + i], zd, dtype, ((int64_t)b * gamma + i) * V, V, invT);
+    for (int r = 0; r < R; ++r) {
+      if (rows[r].m == -INFINITY) flag |= SVO_FLAG_ZERO_MASS;
+      if (row_nonfinite(&rows[r])) flag |= SVO_FLAG_NONFINITE;
+    }
+
+    /* p(x~_i), q(x~_i) and the ratio for every draft position. */
+    double P[64], Q[64], RATIO[64], U[64];
+    for (int i = 0; i < gamma; ++i) {
+      int32_t x = xt[(int64_t)b * gamma + i];
+      const row_t* rt = &rows[i];
+      const row_t* rd = &rows[gamma + 1 + i];
+      if (x < 0 || (int64_t)x >= V) {
+        flag |= SVO_FLAG_BAD_TOKEN;
+        P[i] = 0.0;
+        Q[i] = 0.0;
+      } else {
+        P[i] = prob(rt, x);
+        Q[i] = prob(rd, x);
+      }
+      RATIO[i] = P[i] / Q[i]; /* IEEE: p/0 = inf, 0/0 = NaN (rejects) */
+      U[i] = svo_uniform(seed, 0u, (uint32_t)i, (uint32_t)b, round, 0u, 0);
+      if (p_at) p_at[(int64_t)b * gamma + i] = P[i];
+      if (q_at) q_at[(int64_t)b * gamma + i] = Q[i];
+      if (ratio_out) ratio_out[(int64_t)b * gamma + i] = RATIO[i];
+      if (u_out) u_out[(int64_t)b * gamma + i] = U[i];
+    }
+
+    /* Left-to-right test, stop at the first rejection. */
+    int n = gamma;
+    for (int i = 0; i < gamma; ++i) {
+      if (!(Q[i] > 0.0)) flag |= SVO_FLAG_NONFINITE; /* tested position with q(x~)=0 */
+      if (U[i] <= RATIO[i]) continue;
+      n = i;
+      break;
+    }
+
+    /* The target's own token. */
+    int64_t t;
+    double gap = NAN, rmass = NAN;
+    if (n == gamma) {
+      /* Clean sweep: bonus token from p_gamma. */
+      t = gumbel_argmax(logw_scaled_logit, &rows[gamma], V, seed, (uint32_t)gamma, (uint32_t)b,
+                        round, &gap);
+      if (t < 0) { t = 0; flag |= SVO_FLAG_ZERO_MASS; }
+    } else {
+      /* Rejection at n: residual max(0, p_n - q_n). */
+      pair_t pr = {&rows[n], &rows[gamma + 1 + n]};
+      rmass = 0.0;
+      for (int64_t v = 0; v < V; ++v) {
+        double r = prob(pr.t, v) - prob(pr.d, v);
+        if (r > 0.0) rmass += r;
+      }
+      t = gumbel_argmax(logw_residual, &pr, V, seed, (uint32_t)n, (uint32_t)b, round, &gap);
+      if (t < 0) {
+        /* Residual empty in floating point: sample p_n itself. */
+        flag |= SVO_FLAG_RESIDUAL_FALLBACK;
+        t = gumbel_argmax(logw_scaled_logit, &rows[n], V, seed, (uint32_t)n, (uint32_t)b, round,
+                          &gap);
+        if (t < 0) { t = 0; flag |= SVO_FLAG_ZERO_MASS; }
+      }
+    }
+
+    /* Emit x~_0..x~_{n-1}, t, then -1 padding. */
+    int32_t* out = tokens + (int64_t)b * (gamma + 1);
+    for (int i = 0; i < n; ++i) out[i] = xt[(int64_t)b * gamma + i];
+    out[n] = (int32_t)t;
+    for (int i = n + 1; i <= gamma; ++i) out[i] = -1;
+    counts[b] = n;
+
+    if (beta_out) {
+      for (int i = 0; i < gamma; ++i) {
+        double beta = 0.0;
+        for (int64_t v = 0; v < V; ++v) {
+          double pv = prob(&rows[i], v), qv = prob(&rows[gamma + 1 + i], v);
+          beta += pv < qv ? pv : qv;
+        }
+        beta_out[(int64_t)b * gamma + i] = beta;
+      }
+    }
+    if (gumbel_gap) gumbel_gap[b] = gap;
+    if (resid_mass) resid_mass[b] = rmass;
+    if (flags) flags[b] = flag;
+  }
+
+  for (int r = 0; r < R; ++r) free(rows[r].s);
+  free(rows);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Greedy verify ([C1]; argmax is the one-hot limit of [A3]).  NaN counts as  */
+/* -inf; ties (including an all -inf row) go to the lowest index.            */
+/* ------------------------------------------------------------------------ */
+int svo_spec_verify_greedy(const void* zt, const int32_t* xt, int B, int gamma,
+                           int64_t V, int dtype, int32_t* tokens, int32_t* counts) {
+  if (B < 0 || gamma < 1 || gamma > 64 || V < 1 || (dtype != SVO_F32 && dtype != SVO_BF16))
+    return -1;
+  if (B == 0) return 0;
+  if (!zt || !xt || !tokens || !counts) return -1;
+  int32_t tgt[65];
+  for (int b = 0; b < B; ++b) {
+    for (int i = 0; i <= gamma; ++i) {
+      int64_t off = ((int64_t)b * (gamma + 1) + i) * V;
+      double best = -INFINITY;
+      int64_t arg = 0;
+      for (int64_t v = 0; v < V; ++v) {
+        double z = logit_at(zt, dtype, off + v);
+        if (isnan(z)) z = -INFINITY;
+        if (z > best) {
+          best = z;
+          arg = v;
+        }
+      }
+      tgt[i] = (int32_t)arg;
+    }
+    int n = gamma;
+    for (int i = 0; i < gamma; ++i) {
+      if (xt[(int64_t)b * gamma + i] != tgt[i]) {
+        n = i;
+        break;
+      }
+    }
+    int32_t* out = tokens + (int64_t)b * (gamma + 1);
+    for (int i = 0; i < n; ++i) out[i] = xt[(int64_t)b * gamma + i];
+    out[n] = tgt[n];
+    for (int i = n + 1; i <= gamma; ++i) out[i] = -1;
+    counts[b] = n;
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* LM head reference: the target pass's final projection, logits = h W.      */
+/* ------------------------------------------------------------------------ */
+static double bf16_to_double(uint16_t h) {
+  uint32_t bits = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+void svo_lmhead_logits(const uint16_t* h, const uint16_t* W, int M, int H, int64_t V,
+                       const int64_t* cols, int64_t ncols, float* out) {
+  int64_t nc = cols ? ncols : V;
+  for (int m = 0; m < M; ++m) {
+    for (int64_t j = 0; j < nc; ++j) {
+      int64_t v = cols ? cols[j] : j;
+      double acc = 0.0;
+      for (int k = 0; k < H; ++k)
+        acc += bf16_to_double(h[(int64_t)m * H + k]) * bf16_to_double(W[(int64_t)k * V + v]);
+      out[(int64_t)m * nc + j] = (float)acc;
+    }
+  }
+}
