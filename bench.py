@@ -1,0 +1,382 @@
+#!/usr/bin/env python3
+"""Benchmark of the verify-and-sample step on GB300.
+
+One step = one call of spec_verify (softmax sweep over all 2*gamma+1 logit rows,
+accept test, residual/bonus draw) on one round of the sample_b64 workload:
+B=64, gamma=4, V=128256, bf16 logits, T=0.8, draft noise sigma=1 (Zipf(1.1)
+target bias).  Metric: verify rounds per second (whole job, all GPUs); the
+line also carries verified positions/s (B*gamma per round).
+
+Timing: W untimed warm-up steps, then K steps between a barrier +
+cuda.synchronize() on both sides, CUDA events on the launching stream, max over
+ranks.  Inputs rotate through enough sets to exceed 4x the L2 size, so no step
+reads logits the previous step left in L2.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+For N > 1 (torchrun) every rank runs an independent replica on its own GPU
+(batch rows are independent; there is no exchange step): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "spec_verify rounds/s & positions/s at B=64,γ=4,V=128256; HBM GB/s % of peak"
+UNIT = "rounds/s"
+WORKLOAD = dict(workload="sample_b64", B=64, gamma=4, V=128256, dtype="bf16", temperature=0.8,
+                sigma=1.0, target="N(0,2^2)+Zipf(1.1) bias", draft="target+N(0,sigma^2)")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sigma", type=float, default=1.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif args.impl == "ours":
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline / reference arm: the oracle, timed on the host cores.
+# ----------------------------------------------------------------------------
+def oracle_rounds_per_s(w_np, budget_s: float, rows_per_step: int = 1, max_steps=None):
+    """Runs the single-threaded oracle on batch rows of the workload, one or more
+    rows per step, until the time budget is used; returns (rounds/s, rows, steps, s)."""
+    import oracle
+    zt, zd, xt, T, B = w_np
+    done_rows = steps = 0
+    t0 = time.perf_counter()
+    while True:
+        rows = [(steps * rows_per_step + k) % B for k in range(rows_per_step)]
+        rnd = (steps * rows_per_step) // B
+        oracle.spec_verify(zt, zd, xt, temperature=T, seed=0, rnd=rnd, rows=rows, threads=1)
+        done_rows += len(rows)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps is not None and steps >= max_steps):
+            break
+    return (done_rows / B) / el, done_rows, steps, el
+
+
+def workload_numpy(sigma):
+    import torch
+    from speculative_decoding_verification_21_gb300 import workloads as wl
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = wl.sample_b64(sigma=sigma, device=dev)
+    return (wl.to_oracle(w.zt), wl.to_oracle(w.zd), w.xt.cpu().numpy(), w.temperature, w.B)
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        barrier(world)
+        return
+    w_np = workload_numpy(args.sigma)
+    # warm-up steps (untimed), then timed steps bounded by --ref-seconds
+    oracle_rounds_per_s(w_np, 0.0, max_steps=max(1, min(args.warmup, 3)))
+    val, rows, steps, el = oracle_rounds_per_s(w_np, args.ref_seconds, max_steps=args.steps)
+    sample = (f"{steps} steps of one batch row each ({rows} of the B=64 rows, "
+              f"{rows / 64:.2f} rounds) of sample_b64 sigma={args.sigma:g}, "
+              f"single-threaded, {el:.1f} s")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": steps, "steps_requested": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * el / steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(WORKLOAD, sigma=args.sigma),
+            "positions_per_s": val * 64 * 4,
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+# ----------------------------------------------------------------------------
+# Our arm.
+# ----------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import speculative_decoding_verification_21_gb300 as sv
+    from speculative_decoding_verification_21_gb300 import _lib
+    from speculative_decoding_verification_21_gb300 import workloads as wl
+
+    world, rank, local = dist_setup(args)
+    L = sv.load(build_if_missing=False)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2**20)
+    B, gamma, V = 64, 4, 128256
+
+    # input sets: rotate through >= 4x L2 of logits
+    base = wl.sample_b64(sigma=args.sigma, seed=1003 + 17 * rank, device=dev)
+    set_bytes = base.logit_bytes
+    nsets = max(2, -(-4 * l2 // set_bytes))
+    sets = [base] + [wl.sample_b64(sigma=args.sigma, seed=1003 + 17 * rank + 1000 * k, device=dev)
+                     for k in range(1, nsets)]
+    stream = torch.cuda.current_stream(dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    counts = torch.empty((B,), dtype=torch.int32, device=dev)
+    flags = torch.empty((B,), dtype=torch.uint8, device=dev)
+    ws = sv.alloc_workspace(B, gamma, V, 0, device=dev)
+    P = ctypes.c_void_p
+    argsets = []
+    for s in sets:
+        argsets.append((P(s.zt.data_ptr()), P(s.zd.data_ptr()), P(s.xt.data_ptr()), B, gamma, V,
+                        1, ctypes.c_float(s.temperature), None))
+    tail = (P(tokens.data_ptr()), P(counts.data_ptr()), None, None, None, P(flags.data_ptr()),
+            P(ws.data_ptr()), ctypes.c_size_t(ws.numel()), sh)
+    fn = L.spec_verify
+
+    def step(i):
+        a = argsets[i % nsets]
+        rc = fn(*a, 0, i, *tail)
+        if rc != 0:
+            raise RuntimeError(f"spec_verify failed: {sv.status_string(rc)}")
+
+    # per-kernel events on a subset of the timed steps
+    EVERY = 16
+    n_ev = args.steps // EVERY + 1
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
+    for es in evsets:  # materialise the underlying cudaEvent_t before taking handles
+        for e in es:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+    evptrs = [(ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in es])
+              for es in evsets]
+    assert all(e.cuda_event for es in evsets for e in es)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        k = 0
+        for i in range(args.steps):
+            if i % EVERY == 0:
+                L.sv_set_timing_events(ctypes.cast(evptrs[k], ctypes.c_void_p), 4)
+                step(args.warmup + i)
+                L.sv_set_timing_events(None, 0)
+                k += 1
+            else:
+                step(args.warmup + i)
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = start.elapsed_time(stop)
+    ms = max_over_ranks(ms, world)
+    kern = {"k_sweep": [], "k_decide": [], "k_draw": []}
+    for es in evsets[:k]:
+        kern["k_sweep"].append(es[0].elapsed_time(es[1]))
+        kern["k_decide"].append(es[1].elapsed_time(es[2]))
+        kern["k_draw"].append(es[2].elapsed_time(es[3]))
+    kavg = {n: (sum(v) / len(v) if v else None) for n, v in kern.items()}
+
+    rounds_per_s = world * args.steps / (ms / 1000.0)
+    hbm, peak_kind = peaks()
+    sweep_bytes = B * (2 * gamma + 1) * V * 2
+    sweep_gbs = sweep_bytes / (kavg["k_sweep"] / 1000.0) / 1e9
+
+    # end-to-end through the C ABI with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hz = [(s.zt.cpu().pin_memory(), s.zd.cpu().pin_memory(), s.xt.cpu().pin_memory())
+              for s in sets[:2]]
+        dzt, dzd, dxt = torch.empty_like(base.zt), torch.empty_like(base.zd), torch.empty_like(
+            base.xt)
+        htok = torch.empty((B, gamma + 1), dtype=torch.int32).pin_memory()
+        hcnt = torch.empty((B,), dtype=torch.int32).pin_memory()
+        e2e_steps = max(20, min(400, args.steps // 50))
+
+        def e2e_step(i):
+            z1, z2, x = hz[i % len(hz)]
+            dzt.copy_(z1, non_blocking=True)
+            dzd.copy_(z2, non_blocking=True)
+            dxt.copy_(x, non_blocking=True)
+            rc = fn(P(dzt.data_ptr()), P(dzd.data_ptr()), P(dxt.data_ptr()), B, gamma, V, 1,
+                    ctypes.c_float(base.temperature), None, 0, i, *tail)
+            if rc != 0:
+                raise RuntimeError(sv.status_string(rc))
+            htok.copy_(tokens, non_blocking=True)
+            hcnt.copy_(counts, non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        ems = max_over_ranks(s0.elapsed_time(s1), world)
+        h2d = base.logit_bytes + base.xt.numel() * 4
+        d2h = tokens.numel() * 4 + counts.numel() * 4
+        e2e = {"value": world * e2e_steps / (ems / 1000.0), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        w_np = (wl.to_oracle(base.zt), wl.to_oracle(base.zd), base.xt.cpu().numpy(),
+                base.temperature, B)
+        val, rows, steps_done, el = oracle_rounds_per_s(w_np, args.cpu_seconds)
+        cpu = {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{rows} batch rows ({rows / B:.2f} rounds) of this workload, "
+                         f"single-threaded, {el:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": rounds_per_s, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": dict(WORKLOAD, sigma=args.sigma, l2_policy=(
+                f"inputs rotate over {nsets} sets of {set_bytes / 1e6:.1f} MB "
+                f"(>= 4x L2 {l2 / 2**20:.0f} MiB)"), parallelism=f"replicas x{world}"),
+            "positions_per_s": rounds_per_s * B * gamma,
+            "step_effective_gbs": world * sweep_bytes * args.steps / (ms / 1000.0) / 1e9 / world,
+            "roofline": {"bound": "hbm", "kernel": "k_sweep", "achieved": sweep_gbs,
+                         "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": sweep_gbs / hbm, "frac_of_8TBs": sweep_gbs / 8000.0,
+                         "traffic": None, "algorithmic_bytes": sweep_bytes},
+            "kernel_ms": kavg,
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk.summary(),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

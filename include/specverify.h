@@ -1,0 +1,171 @@
+/*
+ * specverify.h -- C ABI of libspecverify, the verify-and-sample step of
+ * speculative decoding on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (one call = one round, for a batch of B independent rows):
+ *   "Fast Inference from Transformers via Speculative Decoding"
+ *   (intuitivepapers.ai), section "The loop: draft, verify in one pass, keep a
+ *   prefix", Algorithm 1 steps 3-4, and the course notes "Speculative Decoding",
+ *   section "The algorithm":
+ *     - p_i = softmax(target_logits[b][i] / T), q_i = softmax(draft_logits[b][i] / T)
+ *       (temperature applied to both, "already adjusted" distributions);
+ *     - walk i = 0..gamma-1, accept draft x_i iff u_i <= min(1, p_i(x_i)/q_i(x_i)),
+ *       stop at the first rejection; n = number accepted;
+ *     - if n < gamma emit one token from max(0, p_n - q_n) (normalised), else one
+ *       token from p_gamma (the bonus token);
+ *     - output x_0..x_{n-1}, then that token.
+ *   Greedy mode (lihaoran.work essay, "What does unchanged output mean?"): keep
+ *   the longest prefix where the draft equals the target argmax, then append the
+ *   target argmax at the stop position.
+ *
+ * Randomness (no state): Philox4x32-10 (Salmon et al., SC'11), key = (lo32(seed),
+ * hi32(seed)), counter = (c0, (tag<<24)|position, b, lo32(round)); tag 0 is the
+ * acceptance uniform (c0 = 0, lane 0), tag 1 the Gumbel noise of vocabulary entry
+ * v (c0 = v>>2, lane v&3); u = (2*(x>>9)+1)*2^-24 in (0,1).  Sampling is Gumbel-max
+ * argmax_v(log w_v - log(-log u_v)) with ties to the lowest index.  Same inputs and
+ * (seed, round) give the same outputs on any stream, launch shape or GPU.
+ *
+ * Conventions for every entry point:
+ *   - All array arguments are DEVICE pointers, row-major and contiguous; the caller
+ *     owns every buffer.  The library never allocates or frees device memory and
+ *     keeps no state between calls except a per-device SM-count cache.
+ *   - Work is queued on `cuda_stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and the call returns at once.  The return value reports only errors the host
+ *     can see: bad arguments, misalignment, a too-small workspace, a launch failure.
+ *     Data-dependent conditions are reported per batch row in `out_flags`.
+ *   - Logit pointers must be 16-byte aligned; int32/float outputs 4-byte aligned;
+ *     the workspace 256-byte aligned.
+ *   - Workspace: at least sv_workspace_bytes(...) bytes of device memory owned by
+ *     the caller; no initial contents are needed (each call zeroes the counters it
+ *     uses before using them).  Calls that may run concurrently on the GPU need
+ *     separate workspaces; calls queued one after another may share one.
+ *   - Limits: 1 <= gamma <= 32, 1 <= V < 2^31, B >= 0 (B == 0 is a no-op).
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_ARG = -1,         /* null required pointer, size out of range, temperature <= 0 */
+  SV_ERR_DTYPE = -2,       /* dtype not SV_F32 / SV_BF16                                  */
+  SV_ERR_ALIGN = -3,       /* pointer misaligned (see conventions)                       */
+  SV_ERR_WORKSPACE = -4,   /* workspace null or smaller than sv_workspace_bytes()        */
+  SV_ERR_CUDA = -5,        /* a CUDA runtime call or kernel launch failed                */
+  SV_ERR_UNSUPPORTED = -6  /* device is not sm_103 or shape outside the fused kernel's set */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* Per-batch-row flags written to out_flags[b] (bitwise OR). */
+enum {
+  SV_FLAG_ZERO_MASS = 1,         /* a logit row of this batch row has no finite entry; an
+                                    empty draw emits token 0                              */
+  SV_FLAG_NONFINITE = 2,         /* a softmax normaliser is NaN/inf (NaN or +inf logits, bad
+                                    per-row temperature) or q(x_i) == 0 at a tested i;
+                                    outputs of the row are then in range but unspecified  */
+  SV_FLAG_RESIDUAL_FALLBACK = 4, /* max(0, p_n - q_n) had no positive entry in floating
+                                    point; the token was drawn from p_n                   */
+  SV_FLAG_TIMEOUT = 8,           /* reserved: a bounded device-side wait gave up           */
+  SV_FLAG_BAD_TOKEN = 16         /* a draft token outside [0, V): treated as p = q = 0    */
+};
+
+enum { SV_MODE_SAMPLE = 0, SV_MODE_GREEDY = 1, SV_MODE_LMHEAD = 2 };
+
+/* Bytes of workspace a call with these sizes needs (0 for B == 0).  `mode` is one
+ * of SV_MODE_*.  For SV_MODE_LMHEAD, V and the hidden sizes of spec_lmhead_verify
+ * do not change the answer beyond V. */
+size_t sv_workspace_bytes(int B, int gamma, int64_t V, int mode);
+
+/* Zero `bytes` of workspace on `cuda_stream` (a cudaMemsetAsync).  Not required
+ * by the entry points; provided for callers that want a known initial state. */
+int sv_workspace_init(void* workspace, size_t bytes, void* cuda_stream);
+
+/*
+ * spec_verify -- sampling verify (Algorithm 1, steps 3-4).
+ *   target_logits   [B][gamma+1][V]  dtype (fp32, or bf16 bit patterns)
+ *   draft_logits    [B][gamma][V]    dtype
+ *   draft_tokens    [B][gamma]       int32; a token outside [0,V) counts as p=q=0
+ *   temperature     used when row_temperature == NULL; must be > 0 and finite
+ *   row_temperature [B] float or NULL; applies to all 2*gamma+1 rows of batch row b
+ *   seed, round     RNG key and round number (see header comment)
+ * Outputs (device):
+ *   out_tokens      [B][gamma+1] int32: x_0..x_{n-1}, the emitted token, then -1
+ *   out_counts      [B] int32: n, accepted drafts, 0..gamma
+ *   out_p_at_draft  [B][gamma] float or NULL: p_i(x_i) for every i (not only tested)
+ *   out_q_at_draft  [B][gamma] float or NULL: q_i(x_i)
+ *   out_alpha       [B] float or NULL: (1/gamma) sum_i sum_v min(p_i, q_i) -- the
+ *                   overlap of "Fast Inference ...", section "The acceptance rate is
+ *                   the overlap of p and q"; costs one extra pass over 2*gamma rows
+ *   out_flags       [B] uint8 or NULL: SV_FLAG_* bits
+ *   workspace       >= sv_workspace_bytes(B, gamma, V, SV_MODE_SAMPLE), see conventions
+ */
+int spec_verify(const void* target_logits, const void* draft_logits,
+                const int32_t* draft_tokens, int B, int gamma, int64_t V, int dtype,
+                float temperature, const float* row_temperature, uint64_t seed,
+                uint64_t round, int32_t* out_tokens, int32_t* out_counts,
+                float* out_p_at_draft, float* out_q_at_draft, float* out_alpha,
+                uint8_t* out_flags, void* workspace, size_t workspace_bytes,
+                void* cuda_stream);
+
+/*
+ * spec_verify_greedy -- greedy verify.  Reads only the target logits.
+ *   t_i = argmax_v target_logits[b][i][v] on the raw values (exact comparison; NaN
+ *   counts as -inf; ties, including an all -inf row, go to the lowest index);
+ *   n = first i with draft_tokens[b][i] != t_i, else gamma;
+ *   out_tokens[b] = x_0..x_{n-1}, t_n, -1...; out_counts[b] = n.
+ *   workspace >= sv_workspace_bytes(B, gamma, V, SV_MODE_GREEDY).
+ */
+int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B,
+                       int gamma, int64_t V, int dtype, int32_t* out_tokens,
+                       int32_t* out_counts, void* workspace, size_t workspace_bytes,
+                       void* cuda_stream);
+
+/*
+ * spec_lmhead_verify -- fused target/draft LM heads + sampling verify.  The logits
+ * are the final projection of the two models' passes ("Fast Inference ...",
+ * section "The loop ...", steps 1-2: one target pass over gamma+1 positions, the
+ * draft distributions q_i), computed on the tensor cores and consumed by the
+ * verify sweep without being written to HBM.
+ *   h_target  [B*(gamma+1)][Ht] bf16 (row b*(gamma+1)+i = position i of batch row b)
+ *   W_target  [Ht][V]           bf16
+ *   h_draft   [B*gamma][Hd]     bf16
+ *   W_draft   [Hd][V]           bf16
+ *   then as spec_verify (temperature scalar only).
+ *   debug_logits: NULL in production; else [B*(2*gamma+1)][V] float receives the
+ *   logits the kernel used (target rows of batch row b first, then its draft rows),
+ *   so that decisions can be checked on identical logits.
+ * Returns SV_ERR_UNSUPPORTED for hidden sizes that are not multiples of 64 or
+ * B*(gamma+1) > 256.
+ */
+int spec_lmhead_verify(const void* h_target, const void* W_target, int Ht,
+                       const void* h_draft, const void* W_draft, int Hd,
+                       const int32_t* draft_tokens, int B, int gamma, int64_t V,
+                       float temperature, uint64_t seed, uint64_t round,
+                       int32_t* out_tokens, int32_t* out_counts, float* out_p_at_draft,
+                       float* out_q_at_draft, uint8_t* out_flags, float* debug_logits,
+                       void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Profiling aid (not thread-safe): when `events` is non-NULL, following calls
+ * of spec_verify record events[0] on their stream before the first kernel and
+ * events[k] after the k-th of their kernels (the softmax sweep, the decision,
+ * the draw; n >= 4).  NULL switches recording off.  The events are cudaEvent_t
+ * created by the caller; they change no result. */
+int sv_set_timing_events(void* const* events, int n);
+
+/* Human-readable name of a status code. */
+const char* sv_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int sv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECVERIFY_H */

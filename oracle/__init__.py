@@ -75,6 +75,9 @@ def lib():
                                           ctypes.c_int, ctypes.c_float, P, ctypes.c_uint64,
                                           ctypes.c_uint64, P, P, P, P, P, P, P, P, P, P]
             L.svo_spec_verify.restype = ctypes.c_int
+            L.svo_spec_verify_rows.argtypes = L.svo_spec_verify.argtypes + [ctypes.c_int,
+                                                                            ctypes.c_int]
+            L.svo_spec_verify_rows.restype = ctypes.c_int
             L.svo_spec_verify_greedy.argtypes = [P, P, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_int64, ctypes.c_int, P, P]
             L.svo_spec_verify_greedy.restype = ctypes.c_int
@@ -138,9 +141,13 @@ def _dtype_code(a: np.ndarray) -> int:
 
 
 def spec_verify(zt, zd, xt, temperature=1.0, row_temperature=None, seed=0, rnd=0,
-                want_beta=False):
+                want_beta=False, rows=None, threads=1):
     """Sampling verify.  zt [B,g+1,V], zd [B,g,V] (float32 or bf16 bits as uint16),
-    xt [B,g] int32.  Returns a dict of numpy arrays."""
+    xt [B,g] int32.  Returns a dict of numpy arrays.
+
+    rows: optional list of batch-row indices to compute (others left zero);
+    threads: run disjoint row ranges in that many Python threads (each a plain
+    single-threaded oracle call; ctypes releases the GIL)."""
     zt = np.ascontiguousarray(zt)
     zd = np.ascontiguousarray(zd)
     xt = np.ascontiguousarray(xt, dtype=np.int32)
@@ -153,13 +160,29 @@ def spec_verify(zt, zd, xt, temperature=1.0, row_temperature=None, seed=0, rnd=0
         p=np.zeros((B, g)), q=np.zeros((B, g)), ratio=np.zeros((B, g)), u=np.zeros((B, g)),
         beta=np.zeros((B, g)) if want_beta else None, gap=np.zeros(B), resid_mass=np.zeros(B),
         flags=np.zeros(B, np.uint8))
-    rc = lib().svo_spec_verify(
-        _ptr(zt), _ptr(zd), _ptr(xt), B, g, V, _dtype_code(zt), float(temperature), _ptr(rowT),
-        int(seed), int(rnd), _ptr(out["tokens"]), _ptr(out["counts"]), _ptr(out["p"]),
-        _ptr(out["q"]), _ptr(out["ratio"]), _ptr(out["u"]), _ptr(out["beta"]), _ptr(out["gap"]),
-        _ptr(out["resid_mass"]), _ptr(out["flags"]))
-    if rc != 0:
-        raise ValueError(f"oracle spec_verify rejected its arguments (rc={rc})")
+    L = lib()
+
+    def run(b0, b1):
+        rc = L.svo_spec_verify_rows(
+            _ptr(zt), _ptr(zd), _ptr(xt), B, g, V, _dtype_code(zt), float(temperature),
+            _ptr(rowT), int(seed) & (2**64 - 1), int(rnd) & (2**64 - 1), _ptr(out["tokens"]),
+            _ptr(out["counts"]), _ptr(out["p"]), _ptr(out["q"]), _ptr(out["ratio"]),
+            _ptr(out["u"]), _ptr(out["beta"]), _ptr(out["gap"]), _ptr(out["resid_mass"]),
+            _ptr(out["flags"]), int(b0), int(b1))
+        if rc != 0:
+            raise ValueError(f"oracle spec_verify rejected its arguments (rc={rc})")
+
+    ranges = [(b, b + 1) for b in rows] if rows is not None else [(0, B)]
+    if threads > 1 and rows is None and B > 1:
+        step = -(-B // threads)
+        ranges = [(b, min(B, b + step)) for b in range(0, B, step)]
+    if threads > 1 and len(ranges) > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda r: run(*r), ranges))
+    else:
+        for r in ranges:
+            run(*r)
     if want_beta:
         out["alpha"] = out["beta"].mean(axis=1)
     return out

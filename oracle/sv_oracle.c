@@ -226,9 +226,23 @@ int svo_spec_verify(const void* zt, const void* zd, const int32_t* xt,
                     double* p_at, double* q_at, double* ratio_out, double* u_out,
                     double* beta_out, double* gumbel_gap, double* resid_mass,
                     uint8_t* flags) {
+  return svo_spec_verify_rows(zt, zd, xt, B, gamma, V, dtype, temperature, row_temperature, seed,
+                              round, tokens, counts, p_at, q_at, ratio_out, u_out, beta_out,
+                              gumbel_gap, resid_mass, flags, 0, B);
+}
+
+int svo_spec_verify_rows(const void* zt, const void* zd, const int32_t* xt,
+                         int B, int gamma, int64_t V, int dtype,
+                         float temperature, const float* row_temperature,
+                         uint64_t seed, uint64_t round,
+                         int32_t* tokens, int32_t* counts,
+                         double* p_at, double* q_at, double* ratio_out, double* u_out,
+                         double* beta_out, double* gumbel_gap, double* resid_mass,
+                         uint8_t* flags, int b_begin, int b_end) {
   if (B < 0 || gamma < 1 || gamma > 64 || V < 1 || (dtype != SVO_F32 && dtype != SVO_BF16))
     return -1;
-  if (B == 0) return 0;
+  if (b_begin < 0 || b_end > B || b_begin > b_end) return -1;
+  if (B == 0 || b_begin == b_end) return 0;
   if (!zt || !zd || !xt || !tokens || !counts) return -1;
 
   const int R = 2 * gamma + 1; /* rows 0..gamma: target, gamma+1..2gamma: draft */
@@ -243,7 +257,7 @@ int svo_spec_verify(const void* zt, const void* zd, const int32_t* xt,
     }
   }
 
-  for (int b = 0; b < B; ++b) {
+  for (int b = b_begin; b < b_end; ++b) {
     float T = row_temperature ? row_temperature[b] : temperature;
     /* Both sides use the single-precision reciprocal of T as the scale. */
     float invT_f = 1.0f / T;

@@ -71,6 +71,17 @@ int svo_spec_verify(const void* zt, const void* zd, const int32_t* xt,
                     double* beta, double* gumbel_gap, double* resid_mass,
                     uint8_t* flags);
 
+/* Same, for batch rows [b_begin, b_end) only (rows keep their global index b in
+ * the RNG counters; other rows of the outputs are left untouched). */
+int svo_spec_verify_rows(const void* zt, const void* zd, const int32_t* xt,
+                         int B, int gamma, int64_t V, int dtype,
+                         float temperature, const float* row_temperature,
+                         uint64_t seed, uint64_t round,
+                         int32_t* tokens, int32_t* counts,
+                         double* p_at, double* q_at, double* ratio, double* u_acc,
+                         double* beta, double* gumbel_gap, double* resid_mass,
+                         uint8_t* flags, int b_begin, int b_end);
+
 /* Greedy verify on raw target logits. */
 int svo_spec_verify_greedy(const void* zt, const int32_t* xt, int B, int gamma,
                            int64_t V, int dtype, int32_t* tokens, int32_t* counts);

@@ -1,0 +1,230 @@
+// sv_device.cuh -- device-side building blocks of libspecverify (sm_103a).
+//
+// Philox4x32-10 and the uniform/Gumbel mapping, logit loads, and the small
+// reductions every kernel uses.  Written for the GPU path only; the CPU oracle
+// has its own independent implementations.
+#pragma once
+
+#include <cstdint>
+#include <limits>
+
+#include <cuda_runtime.h>
+
+#include "specverify.h"
+
+namespace sv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kInf = std::numeric_limits<float>::infinity();
+
+// --------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+// as 1, 2, 3", SC'11): per round, two 32x32->64-bit products of counter words
+// 0 and 2 with the round multipliers; the high halves are xored with counter
+// words 1 and 3 and the round key; the key advances by the Weyl constants.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Counter for tag/position/batch row/round; c0 selects the vocabulary block.
+__device__ __forceinline__ uint4 sv_counter(uint32_t c0, uint32_t tag, uint32_t pos, uint32_t b,
+                                            uint64_t round) {
+  return make_uint4(c0, (tag << 24) | (pos & 0xFFFFFFu), b, (uint32_t)round);
+}
+
+// 23 random bits -> odd multiple of 2^-24, strictly inside (0,1); exact in fp32.
+__device__ __forceinline__ float sv_u01(uint32_t x) {
+  return __uint2float_rn(2u * (x >> 9) + 1u) * 0x1p-24f;
+}
+
+// E = -ln(u) for u = sv_u01(x), to ~1e-5 relative at worst.  Near u = 1 the
+// logarithm is taken from w = 1 - u (exact in fp32) with the series
+// -ln(1-w) = w + w^2/2 + w^3/3 + ...; elsewhere from the hardware log2.
+__device__ __forceinline__ float sv_neglog_u(uint32_t x) {
+  const uint32_t k = 2u * (x >> 9) + 1u;            // u = k * 2^-24
+  const float u = __uint2float_rn(k) * 0x1p-24f;
+  const float w = __uint2float_rn(16777216u - k) * 0x1p-24f;  // 1 - u, exact
+  const float series = w * fmaf(w, fmaf(w, 1.0f / 3.0f, 0.5f), 1.0f);
+  const float viaLog = -__log2f(u) * kLn2;
+  return (w < 0x1p-8f) ? series : viaLog;
+}
+
+// Exact-ish double version used where a decision is refined (same definition).
+__device__ __forceinline__ double sv_neglog_u_f64(uint32_t x) {
+  const double u = (2.0 * (double)(x >> 9) + 1.0) * 0x1p-24;
+  return -log(u);
+}
+
+// --------------------------------------------------------------------------
+// Fast exp2 (MUFU.EX2, flush-to-zero below 2^-126).
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// --------------------------------------------------------------------------
+// Logit access.  bf16 values are carried as raw bits; widening to fp32 is a
+// shift (low half) or a mask (high half).
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <int DT>
+__device__ __forceinline__ float load_logit(const void* base, int64_t idx);
+template <>
+__device__ __forceinline__ float load_logit<SV_F32>(const void* base, int64_t idx) {
+  return __ldg(reinterpret_cast<const float*>(base) + idx);
+}
+template <>
+__device__ __forceinline__ float load_logit<SV_BF16>(const void* base, int64_t idx) {
+  const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(base) + idx);
+  return __uint_as_float((uint32_t)h << 16);
+}
+
+// Streaming 16-byte load that does not allocate in L1 (data is read once per SM).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Elements per 16-byte vector.
+template <int DT>
+struct VecInfo;
+template <>
+struct VecInfo<SV_F32> {
+  static constexpr int kElems = 4;
+};
+template <>
+struct VecInfo<SV_BF16> {
+  static constexpr int kElems = 8;
+};
+
+// Unpack a 16-byte vector into fp32 values.
+template <int DT>
+__device__ __forceinline__ void unpack(const uint4& v, float* f);
+template <>
+__device__ __forceinline__ void unpack<SV_F32>(const uint4& v, float* f) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
+}
+template <>
+__device__ __forceinline__ void unpack<SV_BF16>(const uint4& v, float* f) {
+  f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+  f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+  f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+  f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+// Max over a vector, NaN ignored (fmaxf semantics).
+template <int DT>
+__device__ __forceinline__ float vmax(const uint4& v);
+template <>
+__device__ __forceinline__ float vmax<SV_F32>(const uint4& v) {
+  return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+               fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+}
+template <>
+__device__ __forceinline__ float vmax<SV_BF16>(const uint4& v) {
+  // packed bf16x2 max (NaN-ignoring), then the two halves
+  uint32_t a, b, c;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x), "r"(v.y));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z), "r"(v.w));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(a), "r"(b));
+  return fmaxf(bf16lo(c), bf16hi(c));
+}
+
+// --------------------------------------------------------------------------
+// (max, sum) pairs of the online softmax: S is a sum of 2^(y - m).
+// --------------------------------------------------------------------------
+struct MS {
+  float m;
+  float s;
+};
+
+__device__ __forceinline__ MS ms_combine(MS a, MS b) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -kInf) return MS{-kInf, 0.0f};
+  const float sa = (a.m == -kInf) ? 0.0f : a.s * ex2(a.m - m);
+  const float sb = (b.m == -kInf) ? 0.0f : b.s * ex2(b.m - m);
+  return MS{m, sa + sb};
+}
+
+__device__ __forceinline__ MS warp_reduce_ms(MS v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MS w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
+    v = ms_combine(v, w);
+  }
+  return v;
+}
+
+// (key, index) with "larger key wins, lower index wins ties".
+struct KI {
+  float k;
+  int i;
+};
+
+__device__ __forceinline__ bool ki_better(KI a, KI b) {
+  return (a.k > b.k) || (a.k == b.k && (unsigned)a.i < (unsigned)b.i);
+}
+
+// Top-2 of (key, index) pairs.
+struct Top2 {
+  KI a, b;
+};
+
+__device__ __forceinline__ Top2 top2_insert(Top2 t, KI x) {
+  if (ki_better(x, t.a)) {
+    t.b = t.a;
+    t.a = x;
+  } else if (ki_better(x, t.b)) {
+    t.b = x;
+  }
+  return t;
+}
+
+__device__ __forceinline__ Top2 top2_merge(Top2 t, Top2 o) {
+  t = top2_insert(t, o.a);
+  return top2_insert(t, o.b);
+}
+
+__device__ __forceinline__ Top2 warp_reduce_top2(Top2 t) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Top2 w;
+    w.a.k = __shfl_xor_sync(0xffffffffu, t.a.k, o);
+    w.a.i = __shfl_xor_sync(0xffffffffu, t.a.i, o);
+    w.b.k = __shfl_xor_sync(0xffffffffu, t.b.k, o);
+    w.b.i = __shfl_xor_sync(0xffffffffu, t.b.i, o);
+    t = top2_merge(t, w);
+  }
+  return t;
+}
+
+__device__ __forceinline__ KI warp_reduce_ki(KI t) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    KI w{__shfl_xor_sync(0xffffffffu, t.k, o), __shfl_xor_sync(0xffffffffu, t.i, o)};
+    if (ki_better(w, t)) t = w;
+  }
+  return t;
+}
+
+}  // namespace sv

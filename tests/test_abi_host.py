@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every entry point its header declares, size the
+workspace, and reject bad arguments with the documented status before any
+kernel is queued.  Pointer arguments here are fake non-null addresses: a
+validating call returns before touching them.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_21_gb300 as sv
+from speculative_decoding_verification_21_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = sv.load()
+    names = declared_functions()
+    assert "spec_verify" in names and "spec_verify_greedy" in names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in specverify.h but not exported"
+    assert set(_lib.EXPORTS) <= set(names)
+
+
+def test_version_and_status_strings():
+    L = sv.load()
+    assert L.sv_version() >= 100
+    for st in (0, -1, -2, -3, -4, -5, -6):
+        assert sv.status_string(st).startswith("SV_")
+
+
+def test_workspace_sizes():
+    assert sv.workspace_bytes(0, 4, 1000, 0) == 0
+    a = sv.workspace_bytes(64, 4, 128256, 0)
+    b = sv.workspace_bytes(128, 4, 128256, 0)
+    assert 0 < a < b and a % 256 == 0
+    assert sv.workspace_bytes(64, 5, 32000, 1) > 0
+    assert sv.workspace_bytes(1, 0, 10, 0) == 0       # gamma out of range
+    assert sv.workspace_bytes(1, 33, 10, 0) == 0
+    assert sv.workspace_bytes(1, 4, 0, 0) == 0
+    assert sv.workspace_bytes(1, 4, 2**31, 0) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced
+FAKE_MIS = ctypes.c_void_p(0x10008)  # 8-byte aligned only
+
+
+def _sv(L, zt=FAKE, zd=FAKE, xt=FAKE, B=2, g=2, V=64, dt=0, T=1.0, rowT=None, tok=FAKE,
+        cnt=FAKE, ws=FAKE, wsb=1 << 20):
+    return L.spec_verify(zt, zd, xt, B, g, V, dt, T, rowT, 0, 0, tok, cnt, None, None, None,
+                         None, ws, wsb, None)
+
+
+def test_spec_verify_argument_errors():
+    L = sv.load()
+    assert _sv(L, g=0) == -1
+    assert _sv(L, g=33) == -1
+    assert _sv(L, V=0) == -1
+    assert _sv(L, B=-1) == -1
+    assert _sv(L, dt=7) == -2
+    assert _sv(L, T=0.0) == -1
+    assert _sv(L, T=-1.0) == -1
+    assert _sv(L, T=float("nan")) == -1
+    assert _sv(L, zt=None) == -1
+    assert _sv(L, tok=None) == -1
+    assert _sv(L, zt=FAKE_MIS) == -3
+    assert _sv(L, zd=FAKE_MIS) == -3
+    assert _sv(L, ws=None) == -4
+    assert _sv(L, wsb=16) == -4
+    assert _sv(L, ws=ctypes.c_void_p(0x10010)) == -3
+    assert _sv(L, B=0) == 0  # no-op, nothing queued
+
+
+def test_greedy_argument_errors():
+    L = sv.load()
+    g = lambda **k: L.spec_verify_greedy(k.get("zt", FAKE), FAKE, k.get("B", 2), k.get("g", 2),
+                                         k.get("V", 64), k.get("dt", 1), FAKE, FAKE,
+                                         k.get("ws", FAKE), k.get("wsb", 1 << 20), None)
+    assert g(g=0) == -1
+    assert g(dt=3) == -2
+    assert g(zt=FAKE_MIS) == -3
+    assert g(wsb=8) == -4
+    assert g(B=0) == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    zt = torch.zeros(1, 2, 8)
+    zd = torch.zeros(1, 1, 8)
+    xt = torch.zeros(1, 1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        sv.spec_verify(zt, zd, xt)
