@@ -115,6 +115,31 @@ int spec_verify(const void* target_logits, const void* draft_logits,
                 void* cuda_stream);
 
 /*
+ * spec_verify_noalloc -- spec_verify for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for the deployment.
+ * Some callers are handed only their input and output buffers (a plugin inside
+ * another runtime, code that must not call into an allocator on the hot path, a
+ * pool that may not grow).  This call takes the same arguments as spec_verify minus
+ * the workspace and gives the same results.  Its scratch memory is one static 4 MiB
+ * device array inside the library, held by every GPU that loads the library until
+ * the process exits.
+ *   - Sizes with sv_workspace_bytes(B, gamma, V, SV_MODE_SAMPLE) > 4 MiB (4194304
+ *     bytes) are rejected with SV_ERR_WORKSPACE before anything is queued.
+ *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device (with that device current) looks up the array's
+ *     device address and caches it; make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents; the
+ *     kernels clear the counters that must start at zero.  Calls that overlap on
+ *     the GPU (different streams or host threads) race on it: serialise them.
+ */
+int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
+                        const int32_t* draft_tokens, int B, int gamma, int64_t V, int dtype,
+                        float temperature, const float* row_temperature, uint64_t seed,
+                        uint64_t round, int32_t* out_tokens, int32_t* out_counts,
+                        float* out_p_at_draft, float* out_q_at_draft, float* out_alpha,
+                        uint8_t* out_flags, void* cuda_stream);
+
+/*
  * spec_verify_greedy -- greedy verify.  Reads only the target logits.
  *   t_i = argmax_v target_logits[b][i][v] on the raw values (exact comparison; NaN
  *   counts as -inf; ties, including an all -inf row, go to the lowest index);
