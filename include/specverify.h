@@ -128,9 +128,10 @@ int spec_verify(const void* target_logits, const void* draft_logits,
  *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device (with that device current) looks up the array's
  *     device address and caches it; make that first call before any stream capture.
- *   - All calls share the one array and it keeps the last call's contents; the
- *     kernels clear the counters that must start at zero.  Calls that overlap on
- *     the GPU (different streams or host threads) race on it: serialise them.
+ *   - All calls share the one array and it keeps the last call's contents; each
+ *     call first resets, on its stream, the counters and markers it relies on.
+ *     Calls that overlap on the GPU (different streams or host threads) race on
+ *     it: serialise them.
  */
 int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
                         const int32_t* draft_tokens, int B, int gamma, int64_t V, int dtype,

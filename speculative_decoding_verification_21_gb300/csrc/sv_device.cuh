@@ -47,13 +47,14 @@ __device__ __forceinline__ float sv_u01(uint32_t x) {
   return __uint2float_rn(2u * (x >> 9) + 1u) * 0x1p-24f;
 }
 
-// E = -ln(u) for u = sv_u01(x), to ~1e-5 relative at worst.  Near u = 1 the
-// logarithm is taken from w = 1 - u (exact in fp32) with the series
-// -ln(1-w) = w + w^2/2 + w^3/3 + ...; elsewhere from the hardware log2.
+// E = -ln(u) for u = sv_u01(x), to ~1e-5 relative at worst.  u is built from
+// the bits directly: 1 + m 2^-23 is exact in fp32 and subtracting 1 - 2^-24 is
+// exact, giving (2m+1) 2^-24.  Near u = 1 the logarithm is taken from
+// w = 1 - u (exact) with the series -ln(1-w) = w + w^2/2 + w^3/3 + ...;
+// elsewhere from the hardware log2.
 __device__ __forceinline__ float sv_neglog_u(uint32_t x) {
-  const uint32_t k = 2u * (x >> 9) + 1u;            // u = k * 2^-24
-  const float u = __uint2float_rn(k) * 0x1p-24f;
-  const float w = __uint2float_rn(16777216u - k) * 0x1p-24f;  // 1 - u, exact
+  const float u = __uint_as_float(0x3f800000u | (x >> 9)) - 0x1.fffffep-1f;
+  const float w = 1.0f - u;
   const float series = w * fmaf(w, fmaf(w, 1.0f / 3.0f, 0.5f), 1.0f);
   const float viaLog = -__log2f(u) * kLn2;
   return (w < 0x1p-8f) ? series : viaLog;
@@ -172,6 +173,18 @@ __device__ __forceinline__ MS warp_reduce_ms(MS v) {
     MS w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
     v = ms_combine(v, w);
   }
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ double warp_sum_f64(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 

@@ -20,9 +20,9 @@
 //     array's device address (cudaGetSymbolAddress) and caches it; make that
 //     first call before any stream capture;
 //   - every call shares the one array, which keeps whatever the last call left
-//     in it.  The counters that must start at zero are cleared by the kernels
-//     themselves at the start of each call.  Calls that overlap on the GPU
-//     (other streams, other host threads) race on the array: serialise them.
+//     in it.  Each call first resets, on its stream, the counters and markers
+//     it relies on.  Calls that overlap on the GPU (other streams, other host
+//     threads) race on the array: serialise them.
 #include <cuda_runtime.h>
 
 #include <cstdint>

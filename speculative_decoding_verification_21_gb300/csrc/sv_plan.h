@@ -14,19 +14,40 @@ namespace sv {
 
 constexpr int kThreads = 256;          // threads per CTA for the streaming kernels
 constexpr int64_t kChunkSweep = 8192;  // logits per CTA in the softmax/argmax sweeps
-constexpr int64_t kChunkDraw = 4096;   // vocabulary entries per CTA in the draw pass
+constexpr int64_t kChunkDraw = 8192;   // vocabulary entries per CTA in the draw pass
 constexpr size_t kAlign = 256;
+
+// Persistent bulk-copy sweep: warps per CTA, pipeline stages per warp, bytes per chunk.
+constexpr int kSweepWarps = 8;
+constexpr int kSweepStages = 3;
+constexpr int kSweepChunkBytes = 4096;
+
+SV_HD inline size_t sweep_smem_bytes() {
+  return (size_t)kSweepWarps * kSweepStages * kSweepChunkBytes +
+         (size_t)kSweepWarps * kSweepStages * sizeof(uint64_t);
+}
+// Logits per bulk-copy chunk for a dtype (0 = fp32, 1 = bf16).
+SV_HD inline int64_t tma_chunk_elems(int dtype) { return kSweepChunkBytes / (dtype == 0 ? 4 : 2); }
+// The bulk-copy sweep needs every row to start on a 16-byte boundary.
+SV_HD inline bool use_tma_sweep(int dtype, int64_t V) {
+  return (V * (dtype == 0 ? 4 : 2)) % 16 == 0;
+}
 
 SV_HD inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 SV_HD inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Per-row softmax statistics after the split combine: max (scaled, log2 units)
-// and the sum of 2^(y - max) in double.
+// Per-row softmax statistics after the chunk combine: max (scaled, log2 units),
+// row condition bits, and the sum of 2^(y - max) in double.
 struct RowStat {
   float mc;
-  float pad;
+  int bits;  // kRowNaN | kRowTimeout
   double s;
 };
+constexpr int kRowNaN = 1, kRowTimeout = 2;
+
+// Counters start at zero; an add's old value tells the caller it was the n-th
+// (last) arrival when old + 1 == n.
+SV_HD inline bool is_last(uint32_t old, uint32_t n) { return old + 1u == n; }
 
 // What the draw pass must do for one batch row.
 enum DrawMode : int { kDrawDone = 0, kDrawSampleRow = 1, kDrawResidual = 2 };
@@ -39,17 +60,18 @@ struct DrawState {
   float mct;     // target row n: scaled max
   float mcd;     // draft row n: scaled max (residual only)
   float K;       // (mct + log2 St) - (mcd + log2 Sd), log2 of q/p offset
-  int pad;
+  int flags;     // SV_FLAG_* gathered by the decision
   double st;     // target row n: sum
   double sd;     // draft row n: sum (residual only)
 };
 
 struct SamplePlan {
   int R1 = 0;          // logit rows per batch row, 2*gamma+1
-  int nsplit1 = 0;     // CTAs per row in the sweep
+  int nsplit1 = 0;     // 8192-logit chunks per row (generic sweep, overlap pass)
   int nsplit3 = 0;     // CTAs per batch row in the draw pass
-  size_t off_cnt = 0, off_part1 = 0, off_rowstat = 0, off_state = 0, off_part3 = 0,
-         off_alpha = 0, total = 0;
+  // counters: [B] draw CTAs, [B] overlap CTAs (zeroed by the finish kernel)
+  size_t off_cnt = 0, cnt_bytes = 0, off_part1 = 0, off_rowstat = 0, off_state = 0,
+         off_part3 = 0, off_alpha = 0, total = 0;
 };
 
 inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
@@ -58,10 +80,13 @@ inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
   p.R1 = 2 * gamma + 1;
   p.nsplit1 = (int)ceil_div(V, kChunkSweep);
   p.nsplit3 = (int)ceil_div(V, kChunkDraw);
+  // per-(row, chunk) partials: enough for the smaller bulk-copy chunks of fp32
+  const int64_t nch_max = ceil_div(V, tma_chunk_elems(0));
   size_t o = 0;
-  p.off_cnt = o;      o = align_up(o + sizeof(uint32_t) * 2 * (size_t)B);
-  p.off_part1 = o;    o = align_up(o + 8 * (size_t)B * p.R1 * p.nsplit1);
+  p.cnt_bytes = sizeof(uint32_t) * 2 * (size_t)B;  // draw and overlap CTA counters
+  p.off_cnt = o;      o = align_up(o + p.cnt_bytes);
   p.off_rowstat = o;  o = align_up(o + sizeof(RowStat) * (size_t)B * p.R1);
+  p.off_part1 = o;    o = align_up(o + 8 * (size_t)B * p.R1 * (size_t)nch_max);
   p.off_state = o;    o = align_up(o + sizeof(DrawState) * (size_t)B);
   p.off_part3 = o;    o = align_up(o + 16 * (size_t)B * p.nsplit3);
   p.off_alpha = o;    o = align_up(o + sizeof(float) * (size_t)B * gamma * p.nsplit1);

@@ -3,37 +3,42 @@
 // One round for B independent batch rows, after Algorithm 1 of "Fast Inference
 // from Transformers via Speculative Decoding" (section "The loop: draft, verify
 // in one pass, keep a prefix") and the course notes "Speculative Decoding"
-// ("The algorithm"):
+// ("The algorithm").  Two kernels per call (three with the optional overlap):
 //
-//   k_sweep   every CTA streams one chunk of one of the 2*gamma+1 logit rows of
-//             a batch row with 16-byte loads and keeps an online (max, sum of
-//             2^(y - max)) with y = z * T^-1 * log2 e; one partial per CTA.
-//   k_decide  one CTA per batch row: combines the partials (double), gathers
-//             p(x_i), q(x_i), draws u_i, accepts iff u_i <= p/q, finds the first
-//             rejection with a warp ballot, writes the accepted prefix, and sets
-//             up the draw of the target's own token.
-//   k_draw    Gumbel-max over the bonus row p_gamma or the residual
-//             max(0, p_n - q_n), in the exponential-race form argmax w_v / E_v
-//             (E_v = -ln u_v), which has the same argmax as log w_v + g_v; the
-//             last CTA of a batch row merges the per-CTA top-2 and, when the two
-//             best fp32 keys are within 2^-10 of each other, re-decides between
+//   sweep     online softmax statistics of every chunk of all 2*gamma+1 logit
+//             rows: max and sum of 2^(y - max), y = z * T^-1 * log2 e.
+//             k_sweep_tma (rows whose byte length is a multiple of 16): a
+//             persistent kernel; every warp streams 4 KB chunks, interleaved
+//             across warps in batch-row order, through a 3-stage bulk-copy (TMA)
+//             pipeline in shared memory.  k_sweep (any shape): one CTA per
+//             8192-logit chunk with 16-byte vector loads.  In both, the warp
+//             that finishes the last chunk of a row combines the row, and the
+//             one that finishes the last row of a batch row makes the decision:
+//             p(x_i), q(x_i), u_i, accept iff u_i <= p/q, first rejection by a
+//             warp ballot, the accepted prefix, and the set-up of the draw.
+//   k_draw    the target's own token -- bonus row p_gamma or residual
+//             max(0, p_n - q_n) -- as a Gumbel-max in the exponential-race form
+//             argmax w_v / E_v (E_v = -ln u_v, the same argmax as log w_v + g_v),
+//             split over CTAs; the last CTA of a batch row merges their top-2
+//             keys and, when the best two are within 2^-10, re-decides between
 //             them in double with the oracle-level definition.
-//   k_alpha   optional overlap sum_v min(p_i, q_i), "The acceptance rate is the
-//             overlap of p and q".
+//   k_alpha   optional overlap sum_v min(p_i, q_i) ("The acceptance rate is the
+//             overlap of p and q").
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "specverify.h"
 #include "sv_device.cuh"
 #include "sv_plan.h"
+#include "sv_tma.cuh"
 
 namespace sv {
 
 __device__ __forceinline__ float inv_temperature(float T) { return 1.0f / T; }
 __device__ __forceinline__ float log2_scale(float invT) { return invT * kLog2e; }
-
 __device__ __forceinline__ bool temperature_ok(float T) { return T > 0.0f && T < kInf; }
 
 // Row k of batch row b: target rows k = 0..gamma, draft rows k = gamma+1..2gamma.
@@ -46,16 +51,249 @@ __device__ __forceinline__ const char* row_ptr(const void* zt, const void* zd, i
   return reinterpret_cast<const char*>(zd) + (((int64_t)b * gamma + (k - gamma - 1)) * V) * kBytes;
 }
 
+// Sum of 2^(y - my) over one lane's vectors, my = max of its raw logits times c.
+template <int DT>
+__device__ __forceinline__ MS ms_of_vectors(const uint4* v, int nv, float c) {
+  float m = -kInf;
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    if (u < nv) m = fmaxf(m, vmax<DT>(v[u]));
+  if (!(m > -kInf)) return MS{-kInf, 0.0f};
+  const float mc = m * c;
+  float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    if (u < nv) {
+      float f[VecInfo<DT>::kElems];
+      unpack<DT>(v[u], f);
+#pragma unroll
+      for (int e = 0; e < VecInfo<DT>::kElems; e += 2) {
+        s0 += ex2(fmaf(f[e], c, -mc));
+        s1 += ex2(fmaf(f[e + 1], c, -mc));
+      }
+    }
+  }
+  return MS{mc, s0 + s1};
+}
+
+// --------------------------------------------------------------------------
+// Row combine and decision (k_finish).
+// --------------------------------------------------------------------------
+struct SweepCtx {
+  const void* zt;
+  const void* zd;
+  const int32_t* xt;
+  int B, gamma;
+  int64_t V;
+  float temperature;
+  const float* row_T;
+  uint64_t seed, round;
+  int nch;               // chunk partials per logit row
+  float2* part;          // [B][R1][nch]
+  RowStat* rowstat;      // [B][R1]
+  DrawState* state;      // [B]
+  int32_t* out_tokens;
+  int32_t* out_counts;
+  float* out_p;
+  float* out_q;
+  uint8_t* out_flags;
+};
+
+// Row statistics of row r from its chunk partials (one warp, all loads of a
+// lane in flight together), kept by lane 0 and written to rowstat[r].
+__device__ __forceinline__ RowStat combine_row(const float2* pr, int nch, RowStat* out) {
+  const int lane = threadIdx.x & 31;
+  float m = -kInf, s = 0.0f;
+  int bits = 0;
+#pragma unroll 4
+  for (int j = lane; j < nch; j += 32) {
+    const float2 p = __ldcg(pr + j);
+    if (p.x != p.x) bits |= kRowNaN;
+    if (p.y < 0.0f) bits |= kRowTimeout;
+    if (p.x > m) {
+      s = (m == -kInf) ? 0.0f : s * exp2f(m - p.x);
+      m = p.x;
+    }
+    if (p.x > -kInf) s += p.y * exp2f(p.x - m);
+  }
+  const float M = warp_max(m);
+  float sl = (m > -kInf) ? s * exp2f(m - M) : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, o);
+  bits = __reduce_or_sync(0xffffffffu, bits);
+  RowStat rs;
+  rs.mc = M;
+  rs.bits = bits;
+  rs.s = (bits & kRowNaN) ? CUDART_NAN : (double)sl;
+  if (lane == 0 && out) *out = rs;
+  return rs;
+}
+
+// log2 of the unnormalised probability, e = z c - mc, carried in two floats:
+// z c = ph + pl exactly (FMA residual) and ph - mc by TwoSum, so e = hi + lo
+// to about 2^-48 relative.
+struct Exp2 {
+  float hi, lo;
+};
+__device__ __forceinline__ Exp2 exponent_at(float z, float c, float mc) {
+  const float ph = z * c;
+  const float pl = fmaf(z, c, -ph);
+  const float a = ph - mc;
+  const float bv = a - ph;
+  const float err = (ph - (a - bv)) + (-mc - bv);
+  return Exp2{a, err + pl};
+}
+// p(x) from its exponent and the row sum (0 for a -inf logit or an empty row).
+__device__ __forceinline__ float prob_from(float z, const Exp2& e, const RowStat& r) {
+  if (!(r.s > 0.0)) return (r.s == 0.0) ? 0.0f : (float)r.s;  // NaN stays NaN
+  if (z == -kInf) return 0.0f;
+  return exp2f(e.hi) * fmaf(e.lo, kLn2, 1.0f) / (float)r.s;
+}
+
+// The decision for batch row b (one warp): accept test, prefix, draw set-up.
+// srs[k] holds the statistics of row k of the batch row.
+template <int DT>
+__device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs) {
+  const int lane = threadIdx.x & 31;
+  const int gamma = x.gamma;
+  const int64_t V = x.V;
+  const int R1 = 2 * gamma + 1;
+  const float T = x.row_T ? __ldg(x.row_T + b) : x.temperature;
+  const float invT = inv_temperature(T);
+  const float c = log2_scale(invT);
+
+  int fl = 0;
+  for (int k = lane; k < R1; k += 32) {
+    const RowStat v = srs[k];
+    if (v.mc == -kInf) fl |= SV_FLAG_ZERO_MASS;
+    if (!(v.s < CUDART_INF) || v.mc == kInf || !temperature_ok(T)) fl |= SV_FLAG_NONFINITE;
+    if (v.bits & kRowTimeout) fl |= SV_FLAG_TIMEOUT | SV_FLAG_NONFINITE;
+  }
+  bool accept = false, bad = false, qzero = false;
+  double P = 0.0, Q = 0.0;
+  if (lane < gamma) {
+    const int32_t xi = __ldg(x.xt + (int64_t)b * gamma + lane);
+    bad = (xi < 0 || (int64_t)xi >= V);
+    float ratio = CUDART_NAN_F;  // a bad token: p = q = 0, rejected
+    if (!bad) {
+      const float zx = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, lane, gamma, V), xi);
+      const float zy = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + lane, gamma, V), xi);
+      const RowStat rt = srs[lane], rd = srs[gamma + 1 + lane];
+      const Exp2 ep = exponent_at(zx, c, rt.mc), eq = exponent_at(zy, c, rd.mc);
+      P = prob_from(zx, ep, rt);
+      Q = prob_from(zy, eq, rd);
+      // p/q from the exponent difference (no underflow of p and q themselves);
+      // q = 0 with p > 0 gives inf (accept), p = q = 0 gives NaN (reject)
+      const bool p0 = !(rt.s > 0.0) || zx == -kInf, q0 = !(rd.s > 0.0) || zy == -kInf;
+      if (rt.s != rt.s || rd.s != rd.s) {
+        ratio = CUDART_NAN_F;
+      } else if (p0 || q0) {
+        ratio = p0 ? (q0 ? CUDART_NAN_F : 0.0f) : kInf;
+      } else {
+        const float d = (ep.hi - eq.hi) + (ep.lo - eq.lo);
+        ratio = exp2f(d) * (float)(rd.s / rt.s);
+      }
+      qzero = q0 || !(rd.s == rd.s);
+    } else {
+      qzero = true;
+    }
+    const uint4 rnd = philox4x32_10(sv_counter(0u, 0u, (uint32_t)lane, (uint32_t)b, x.round),
+                                    (uint32_t)x.seed, (uint32_t)(x.seed >> 32));
+    accept = (sv_u01(rnd.x) <= ratio);
+    if (x.out_p) x.out_p[(int64_t)b * gamma + lane] = (float)P;
+    if (x.out_q) x.out_q[(int64_t)b * gamma + lane] = (float)Q;
+  }
+  const unsigned rej = ~__ballot_sync(0xffffffffu, accept);
+  const int n = (rej == 0u) ? 32 : min(__ffs((int)rej) - 1, gamma);
+  // flags: bad tokens anywhere, q(x) = 0 at a tested position (i <= n, i < gamma)
+  if (__ballot_sync(0xffffffffu, bad)) fl |= SV_FLAG_BAD_TOKEN;
+  if (__ballot_sync(0xffffffffu, lane < gamma && lane <= n && qzero)) fl |= SV_FLAG_NONFINITE;
+  fl = __reduce_or_sync(0xffffffffu, fl);
+  int32_t* tok = x.out_tokens + (int64_t)b * (gamma + 1);
+  for (int i = lane; i <= gamma; i += 32) {
+    if (i < n) tok[i] = __ldg(x.xt + (int64_t)b * gamma + i);
+    else if (i > n) tok[i] = -1;
+  }
+  if (lane == 0) {
+    // set up the draw of the target's own token
+    const float mct = srs[n].mc;
+    const double St = srs[n].s;
+    DrawState st{};
+    st.pos = n;
+    st.c = c;
+    st.invT = invT;
+    const bool t_ok = (St > 0.0) && (St < 1e308) && (mct < kInf);
+    if (n == gamma) {
+      if (t_ok) {
+        st.mode = kDrawSampleRow;
+        st.mct = mct;
+        st.st = St;
+      } else {
+        st.mode = kDrawDone;
+      }
+    } else {
+      const float mcd = srs[gamma + 1 + n].mc;
+      const double Sd = srs[gamma + 1 + n].s;
+      const bool d_nonfinite = !(Sd < 1e308) || mcd == kInf;
+      if (!t_ok || d_nonfinite) {
+        // p_n has no mass (or a row is not finite): the residual and its fallback
+        // are empty; token 0
+        st.mode = kDrawDone;
+        if (St == 0.0) fl |= SV_FLAG_RESIDUAL_FALLBACK;
+      } else if (Sd == 0.0) {
+        st.mode = kDrawSampleRow;  // q_n has no mass: max(0, p_n - q_n) = p_n
+        st.mct = mct;
+        st.st = St;
+      } else {
+        st.mode = kDrawResidual;
+        st.mct = mct;
+        st.st = St;
+        st.mcd = mcd;
+        st.sd = Sd;
+        st.K = (mct - mcd) + (log2f((float)St) - log2f((float)Sd));
+      }
+    }
+    st.flags = fl;
+    x.state[b] = st;
+    x.out_counts[b] = n;
+    if (st.mode == kDrawDone) {
+      tok[n] = 0;
+      if (x.out_flags) x.out_flags[b] = (uint8_t)fl;
+    }
+  }
+}
+
+// One CTA per batch row: row statistics (one warp per row), then the decision.
+template <int DT>
+__global__ void __launch_bounds__(1024) k_finish(SweepCtx x, uint32_t* __restrict__ counters) {
+  const int b = blockIdx.x;
+  const int R1 = 2 * x.gamma + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ RowStat srs[65];
+  if (threadIdx.x == 0) {  // counters of the draw and overlap kernels that follow
+    counters[b] = 0u;
+    counters[x.B + b] = 0u;
+  }
+  for (int k = warp; k < R1; k += (int)(blockDim.x >> 5)) {
+    const RowStat rs = combine_row(x.part + ((int64_t)b * R1 + k) * x.nch, x.nch,
+                                   x.rowstat + (int64_t)b * R1 + k);
+    if (lane == 0) srs[k] = rs;
+  }
+  __syncthreads();
+  if (warp == 0) decide_batch_row<DT>(x, b, srs);
+}
+
+// --------------------------------------------------------------------------
+// Generic sweep (any V): one CTA per (row, 8192-logit chunk).
+// --------------------------------------------------------------------------
 // Visit elements [lo, hi) of a row: an unaligned head as scalars, then 16-byte
-// vectors, then the tail.  Every thread sees its own elements in increasing
-// index order.  `row` must be a row start; `f_vec(v0, vec)` / `f_one(v, z)`.
+// vectors, then the tail.
 template <int DT, int UNROLL, class FV, class FS>
 __device__ __forceinline__ void for_each_in_chunk(const char* row, int64_t lo, int64_t hi,
                                                   FV&& f_vec, FS&& f_one) {
   constexpr int VE = VecInfo<DT>::kElems;
   constexpr int kBytes = (DT == SV_F32) ? 4 : 2;
   const int tid = threadIdx.x;
-  // first element at or after lo whose address is 16-byte aligned
   const uintptr_t addr_lo = reinterpret_cast<uintptr_t>(row) + lo * kBytes;
   const int64_t head = (int64_t)(((16 - (addr_lo & 15)) & 15) / kBytes);
   int64_t a0 = lo + head;
@@ -80,24 +318,18 @@ __device__ __forceinline__ void for_each_in_chunk(const char* row, int64_t lo, i
   for (int64_t v = a1 + tid; v < hi; v += blockDim.x) f_one(v, load_logit<DT>(row, v));
 }
 
-// --------------------------------------------------------------------------
-// k_sweep: online softmax statistics per (row, chunk).
-// --------------------------------------------------------------------------
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 4)
-k_sweep(const void* __restrict__ zt, const void* __restrict__ zd, int gamma, int64_t V,
-        float temperature, const float* __restrict__ row_T, int nsplit,
-        float2* __restrict__ part) {
-  const int R1 = 2 * gamma + 1;
-  const int64_t item = blockIdx.x;  // (row, split) flattened: rows are B*R1
-  const int64_t r = item / nsplit;
-  const int split = (int)(item - r * nsplit);
+__global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
+  const int R1 = 2 * x.gamma + 1;
+  const int64_t item = blockIdx.x;  // (row, chunk) flattened, rows in batch-row order
+  const int64_t r = item / x.nch;
+  const int split = (int)(item - r * x.nch);
   const int b = (int)(r / R1), k = (int)(r - (int64_t)b * R1);
-  const float T = row_T ? __ldg(row_T + b) : temperature;
+  const float T = x.row_T ? __ldg(x.row_T + b) : x.temperature;
   const float c = log2_scale(inv_temperature(T));
-  const char* row = row_ptr<DT>(zt, zd, b, k, gamma, V);
+  const char* row = row_ptr<DT>(x.zt, x.zd, b, k, x.gamma, x.V);
   const int64_t lo = (int64_t)split * kChunkSweep;
-  const int64_t hi = min(V, lo + kChunkSweep);
+  const int64_t hi = min(x.V, lo + kChunkSweep);
 
   float zmax = -kInf, mc = -kInf, s = 0.0f;
   auto raise_max = [&](float m) {
@@ -134,235 +366,370 @@ k_sweep(const void* __restrict__ zt, const void* __restrict__ zd, int gamma, int
   if (warp == 0) {
     v = (lane < (int)(blockDim.x >> 5)) ? sm[lane] : MS{-kInf, 0.0f};
     v = warp_reduce_ms(v);
-    if (lane == 0) part[item] = make_float2(v.m, v.s);
+    if (lane == 0) x.part[item] = make_float2(v.m, v.s);
   }
 }
 
+// Per-lane online (max, sum) update with a chunk maximum m of raw logits.
+__device__ __forceinline__ void lane_raise_max(float m, float c, float& zmax, float& mc,
+                                               float& sacc) {
+  if (m > zmax) {
+    const float mcn = m * c;
+    sacc = (zmax == -kInf) ? 0.0f : sacc * ex2(mc - mcn);
+    mc = mcn;
+    zmax = m;
+  }
+}
+
+// One full 4 KB chunk in shared memory: each lane takes 8 of its 256 vectors.
+// The maximum is a packed tree over the raw words, then one exp2 per logit.
+template <int DT>
+__device__ __forceinline__ void chunk_update_full(const uint4* sv, int lane, float c, float& zmax,
+                                                  float& mc, float& sacc) {
+  uint4 v[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) v[u] = sv[lane + 32 * u];
+  float m;
+  if constexpr (DT == SV_BF16) {
+    uint32_t a[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      uint32_t p, q;
+      asm("max.bf16x2 %0, %1, %2;" : "=r"(p) : "r"(v[u].x), "r"(v[u].y));
+      asm("max.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(v[u].z), "r"(v[u].w));
+      asm("max.bf16x2 %0, %1, %2;" : "=r"(a[u]) : "r"(p), "r"(q));
+    }
+#pragma unroll
+    for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+      for (int u = 0; u < k; ++u) asm("max.bf16x2 %0, %1, %2;" : "=r"(a[u]) : "r"(a[u]), "r"(a[u + k]));
+    m = fmaxf(bf16lo(a[0]), bf16hi(a[0]));
+  } else {
+    float a[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      a[u] = fmaxf(fmaxf(__uint_as_float(v[u].x), __uint_as_float(v[u].y)),
+                   fmaxf(__uint_as_float(v[u].z), __uint_as_float(v[u].w)));
+#pragma unroll
+    for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+      for (int u = 0; u < k; ++u) a[u] = fmaxf(a[u], a[u + k]);
+    m = a[0];
+  }
+  lane_raise_max(m, c, zmax, mc, sacc);
+  if (!(zmax > -kInf)) return;
+  const float nm = -mc;
+  float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if constexpr (DT == SV_BF16) {
+        s0 += ex2(fmaf(bf16lo(w[q]), c, nm));
+        s1 += ex2(fmaf(bf16hi(w[q]), c, nm));
+      } else {
+        if (q & 1) s1 += ex2(fmaf(__uint_as_float(w[q]), c, nm));
+        else s0 += ex2(fmaf(__uint_as_float(w[q]), c, nm));
+      }
+    }
+    if (u & 1) { s2 += s0; s3 += s1; s0 = 0.0f; s1 = 0.0f; }
+  }
+  sacc += (s0 + s1) + (s2 + s3);
+}
+
 // --------------------------------------------------------------------------
-// k_decide: one CTA (128 threads) per batch row.
+// TMA sweep (rows a multiple of 16 bytes long): persistent, per-warp pipelines.
+// Chunk c of the [b][row][chunk] order goes to warp c mod W, so the whole GPU
+// walks memory in address order; each chunk leaves one (max, sum) partial.
 // --------------------------------------------------------------------------
 template <int DT>
-__global__ void __launch_bounds__(128)
-k_decide(const void* __restrict__ zt, const void* __restrict__ zd,
-         const int32_t* __restrict__ xt, int gamma, int64_t V, float temperature,
-         const float* __restrict__ row_T, uint64_t seed, uint64_t round, int nsplit,
-         const float2* __restrict__ part, RowStat* __restrict__ rowstat,
-         DrawState* __restrict__ state, uint32_t* __restrict__ counters, int B,
-         int32_t* __restrict__ out_tokens, int32_t* __restrict__ out_counts,
-         float* __restrict__ out_p, float* __restrict__ out_q, uint8_t* __restrict__ out_flags) {
-  const int b = blockIdx.x;
+__global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
+  constexpr int kBytes = (DT == SV_F32) ? 4 : 2;
+  constexpr int CH = kSweepChunkBytes / kBytes;  // logits per chunk
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* stage0 = smem + (size_t)warp * kSweepStages * kSweepChunkBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kSweepWarps * kSweepStages *
+                                                          kSweepChunkBytes) +
+                   warp * kSweepStages;
+  const int gamma = x.gamma;
+  const int64_t V = x.V;
+  const int nch = x.nch;
   const int R1 = 2 * gamma + 1;
-  const int tid = threadIdx.x;
-  // the draw and overlap kernels that follow count their CTAs here: start at zero
-  // whatever an earlier call (of any shape) left in this part of the workspace
-  if (tid == 0) {
-    counters[b] = 0u;
-    counters[B + b] = 0u;
-  }
-  __shared__ float s_mc[65];
-  __shared__ double s_s[65];
-  __shared__ int s_flag;
-  if (tid == 0) s_flag = 0;
-  const float T = row_T ? __ldg(row_T + b) : temperature;
-  const float invT = inv_temperature(T);
-  const float c = log2_scale(invT);
-  __syncthreads();
+  const int64_t NC = (int64_t)x.B * R1 * nch;
+  const int64_t W = (int64_t)gridDim.x * kSweepWarps;
+  const int64_t w = (int64_t)blockIdx.x * kSweepWarps + warp;
+  const int count = (w < NC) ? (int)((NC - w + W - 1) / W) : 0;  // chunks w, w+W, ...
+  const uint32_t tail_bytes = (uint32_t)((V - (int64_t)(nch - 1) * CH) * kBytes);
 
-  // 1. combine the split partials of every row (double sum)
-  for (int k = tid; k < R1; k += blockDim.x) {
-    const float2* pr = part + ((int64_t)b * R1 + k) * nsplit;
-    float m = -kInf;
-    bool nan_m = false;
-    for (int j = 0; j < nsplit; ++j) {
-      const float mj = pr[j].x;
-      nan_m |= (mj != mj);
-      m = fmaxf(m, mj);
-    }
-    double s = 0.0;
-    if (m > -kInf) {
-      for (int j = 0; j < nsplit; ++j) {
-        const float2 pj = pr[j];
-        if (pj.x > -kInf) s += (double)pj.y * exp2((double)pj.x - (double)m);
-        else if (pj.y != 0.0f) s += (double)pj.y;  // NaN/inf propagate
-      }
-    }
-    if (nan_m) s = CUDART_NAN;
-    s_mc[k] = m;
-    s_s[k] = s;
-    rowstat[(int64_t)b * R1 + k] = RowStat{m, 0.0f, s};
-    int f = 0;
-    if (m == -kInf) f |= SV_FLAG_ZERO_MASS;
-    if (!(s < CUDART_INF) || m == kInf || !temperature_ok(T)) f |= SV_FLAG_NONFINITE;
-    if (f) atomicOr(&s_flag, f);
+  if (lane == 0) {
+    for (int s = 0; s < kSweepStages; ++s) mbar_init(bars + s, 1);
+    fence_mbar_init();
   }
-  __syncthreads();
+  __syncwarp();
 
-  // 2. accept test on warp 0, one lane per draft position
-  if (tid < 32) {
-    const int lane = tid;
-    bool accept = false;
-    double P = 0.0, Q = 0.0;
-    int bad = 0;
-    if (lane < gamma) {
-      const int32_t x = __ldg(xt + (int64_t)b * gamma + lane);
-      if (x < 0 || (int64_t)x >= V) {
-        bad = 1;
+  auto src_of = [&](int64_t cidx, uint32_t& bytes, int64_t& r) -> const char* {
+    r = cidx / nch;
+    const int j = (int)(cidx - r * nch);
+    const int b = (int)(r / R1);
+    bytes = (j == nch - 1) ? tail_bytes : (uint32_t)kSweepChunkBytes;
+    return row_ptr<DT>(x.zt, x.zd, b, (int)(r - (int64_t)b * R1), gamma, V) +
+           (size_t)j * kSweepChunkBytes;
+  };
+  auto issue = [&](int s, int64_t cidx) {  // lane 0 only
+    uint32_t bytes;
+    int64_t r;
+    const char* src = src_of(cidx, bytes, r);
+    mbar_arrive_expect_tx(bars + s, bytes);
+    bulk_g2s(stage0 + (size_t)s * kSweepChunkBytes, src, bytes, bars + s);
+  };
+
+  if (lane == 0)
+    for (int s = 0; s < kSweepStages && s < count; ++s) issue(s, w + (int64_t)s * W);
+
+  bool dead = false;  // a bounded wait ran out: stop loading, mark what is left
+  int issued = count < kSweepStages ? count : kSweepStages;  // chunks issued so far
+
+  for (int t = 0; t < count; ++t) {
+    const int s = t % kSweepStages;
+    const uint32_t parity = (uint32_t)((t / kSweepStages) & 1);
+    const int64_t cidx = w + (int64_t)t * W;
+    uint32_t bytes;
+    int64_t r;
+    src_of(cidx, bytes, r);
+    float2 res;
+    if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait_bounded(bars + s, parity));
+    if (!dead) {
+      const int b = (int)(r / R1);
+      const float T = x.row_T ? __ldg(x.row_T + b) : x.temperature;
+      const float c = log2_scale(inv_temperature(T));
+      const uint4* sv = reinterpret_cast<const uint4*>(stage0 + (size_t)s * kSweepChunkBytes);
+      float zmax = -kInf, mc = -kInf, sacc = 0.0f;
+      if (bytes == (uint32_t)kSweepChunkBytes) {
+        chunk_update_full<DT>(sv, lane, c, zmax, mc, sacc);
       } else {
-        const double cd = (double)c;
-        const double zx = (double)load_logit<DT>(row_ptr<DT>(zt, zd, b, lane, gamma, V), x);
-        const double zy =
-            (double)load_logit<DT>(row_ptr<DT>(zt, zd, b, gamma + 1 + lane, gamma, V), x);
-        const double St = s_s[lane], Sd = s_s[gamma + 1 + lane];
-        P = (St > 0.0) ? exp2(zx * cd - (double)s_mc[lane]) / St : (St == 0.0 ? 0.0 : St);
-        Q = (Sd > 0.0) ? exp2(zy * cd - (double)s_mc[gamma + 1 + lane]) / Sd
-                       : (Sd == 0.0 ? 0.0 : Sd);
-      }
-      const double ratio = P / Q;  // IEEE: p/0 = inf (accept), 0/0 = NaN (reject)
-      const uint4 rnd = philox4x32_10(sv_counter(0u, 0u, (uint32_t)lane, (uint32_t)b, round),
-                                      (uint32_t)seed, (uint32_t)(seed >> 32));
-      const double u = (double)sv_u01(rnd.x);
-      accept = (u <= ratio);
-      if (out_p) out_p[(int64_t)b * gamma + lane] = (float)P;
-      if (out_q) out_q[(int64_t)b * gamma + lane] = (float)Q;
-    }
-    const unsigned mask = __ballot_sync(0xffffffffu, accept);
-    const unsigned rej = ~mask;
-    const int n = (rej == 0u) ? 32 : min(__ffs((int)rej) - 1, gamma);
-    // flags: bad tokens anywhere, q(x)=0 at a tested position (i <= n, i < gamma)
-    const unsigned badm = __ballot_sync(0xffffffffu, bad);
-    const unsigned qz = __ballot_sync(0xffffffffu, lane < gamma && lane <= n && !(Q > 0.0));
-    if (lane == 0) {
-      int f = s_flag;
-      if (badm) f |= SV_FLAG_BAD_TOKEN;
-      if (qz) f |= SV_FLAG_NONFINITE;
-      s_flag = f;
-    }
-    __syncwarp();
-    int32_t* tok = out_tokens + (int64_t)b * (gamma + 1);
-    for (int i = lane; i <= gamma; i += 32) {
-      if (i < n) tok[i] = __ldg(xt + (int64_t)b * gamma + i);
-      else if (i > n) tok[i] = -1;
-    }
-    if (lane == 0) {
-      out_counts[b] = n;
-      // 3. set up the draw of the target's own token
-      DrawState st{};
-      st.pos = n;
-      st.c = c;
-      st.invT = invT;
-      int f = s_flag;
-      const float mct = s_mc[n];
-      const double St = s_s[n];
-      const bool t_ok = (St > 0.0) && (St < 1e308) && (mct < kInf);
-      if (n == gamma) {
-        if (!t_ok) {
-          st.mode = kDrawDone;
-          tok[n] = 0;
-        } else {
-          st.mode = kDrawSampleRow;
-          st.mct = mct;
-          st.st = St;
-        }
-      } else {
-        const float mcd = s_mc[gamma + 1 + n];
-        const double Sd = s_s[gamma + 1 + n];
-        const bool d_nonfinite = !(Sd < 1e308) || mcd == kInf;
-        if (!t_ok || d_nonfinite) {
-          // p_n has no mass (or the row is not finite): the residual is empty and
-          // so is its fallback; emit token 0
-          st.mode = kDrawDone;
-          tok[n] = 0;
-          if (St == 0.0) f |= SV_FLAG_RESIDUAL_FALLBACK;
-        } else if (Sd == 0.0) {
-          // q_n has no mass: max(0, p_n - q_n) = p_n
-          st.mode = kDrawSampleRow;
-          st.mct = mct;
-          st.st = St;
-        } else {
-          st.mode = kDrawResidual;
-          st.mct = mct;
-          st.st = St;
-          st.mcd = mcd;
-          st.sd = Sd;
-          st.K = (float)(((double)mct + log2(St)) - ((double)mcd + log2(Sd)));
+        const int nvec = (int)(bytes / 16);
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (lane + 32 * u < nvec) v[u] = sv[lane + 32 * u];
+        const int nv = (nvec - lane + 31) >> 5;
+        float m = -kInf;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (u < nv) m = fmaxf(m, vmax<DT>(v[u]));
+        lane_raise_max(m, c, zmax, mc, sacc);
+        if (zmax > -kInf) {
+          float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (u < nv) {
+              float f[VecInfo<DT>::kElems];
+              unpack<DT>(v[u], f);
+#pragma unroll
+              for (int e = 0; e < VecInfo<DT>::kElems; e += 2) {
+                s0 += ex2(fmaf(f[e], c, -mc));
+                s1 += ex2(fmaf(f[e + 1], c, -mc));
+              }
+            }
+          }
+          sacc += s0 + s1;
         }
       }
-      state[b] = st;
-      if (out_flags) out_flags[b] = (uint8_t)f;
+      const MS ms = warp_reduce_ms(MS{mc, sacc});
+      res = make_float2(ms.m, ms.s);
+      __syncwarp();
+      if (t + kSweepStages < count) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          issue(s, cidx + (int64_t)kSweepStages * W);
+        }
+        issued = t + kSweepStages + 1;
+      }
+    } else {
+      res = make_float2(CUDART_NAN_F, -1.0f);  // timed-out chunk: flagged downstream
     }
+    if (lane == 0) x.part[cidx] = res;  // chunk order = [b][row][chunk]
+  }
+  if (dead && lane == 0) {
+    // let copies still in flight land before the CTA's shared memory is released:
+    // the last chunk issued into each stage, at its phase
+    for (int t = (issued > kSweepStages ? issued - kSweepStages : 0); t < issued; ++t)
+      mbar_wait_bounded(bars + (t % kSweepStages), (uint32_t)((t / kSweepStages) & 1), 1u << 16);
   }
 }
 
 // --------------------------------------------------------------------------
-// k_draw: Gumbel-max of the target's own token.
+// Draw of the target's own token.
 // --------------------------------------------------------------------------
 struct DrawArgs {
   const void* zt;
   const void* zd;
-  int gamma;
+  int B, gamma;
   int64_t V;
   uint64_t seed, round;
-  int nsplit;
-  const DrawState* state;
-  Top2* part;
-  uint32_t* counter;
+  const DrawState* state;  // [B]
+  uint32_t* counter;       // [B] CTAs done per batch row
+  Top2* part3;             // [B][nsplit3]
+  int nsplit3;
   int32_t* out_tokens;
   uint8_t* out_flags;
 };
 
-// Keys of one 4-entry Philox group v = 4g .. 4g+3 (entries >= V skipped).
-template <int DT, bool RESID>
-__device__ __forceinline__ void draw_group(const char* rt, const char* rd, int64_t g, int64_t V,
-                                           bool vec_ok, const DrawState& st, uint32_t b,
-                                           uint64_t seed, uint64_t round, KI& best) {
-  const int64_t v0 = 4 * g;
-  float ztv[4], zdv[4];
-  if (vec_ok && v0 + 3 < V) {
-    if (DT == SV_F32) {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(rt) + g);
-      ztv[0] = a.x; ztv[1] = a.y; ztv[2] = a.z; ztv[3] = a.w;
-      if (RESID) {
-        const float4 d = __ldg(reinterpret_cast<const float4*>(rd) + g);
-        zdv[0] = d.x; zdv[1] = d.y; zdv[2] = d.z; zdv[3] = d.w;
-      }
-    } else {
-      const uint2 a = __ldg(reinterpret_cast<const uint2*>(rt) + g);
-      ztv[0] = bf16lo(a.x); ztv[1] = bf16hi(a.x); ztv[2] = bf16lo(a.y); ztv[3] = bf16hi(a.y);
-      if (RESID) {
-        const uint2 d = __ldg(reinterpret_cast<const uint2*>(rd) + g);
-        zdv[0] = bf16lo(d.x); zdv[1] = bf16hi(d.x); zdv[2] = bf16lo(d.y); zdv[3] = bf16hi(d.y);
-      }
-    }
-  } else {
+// -log2(u) for u = sv_u01(x): the exponential variate E of the race, in log2
+// units (a common scale factor of all keys, so the argmax is unchanged).  Near
+// u = 1 it comes from w = 1 - u (exact) and -log2(1-w) = (w + w^2/2 + ...)/ln 2,
+// truncated after w^2 (relative error < w^2/3 < 2^-17.5 for w < 2^-8).
+__device__ __forceinline__ float neglog2_u(uint32_t x) {
+  const float u = __uint_as_float(0x3f800000u | (x >> 9)) - 0x1.fffffep-1f;
+  const float w = 1.0f - u;
+  const float series = w * fmaf(w, 0.5f * kLog2e, kLog2e);
+  return (w < 0x1p-8f) ? series : -__log2f(u);
+}
+
+// Philox4x32-10 with the ten round keys precomputed (the key schedule depends
+// only on the seed).
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
+  PhiloxKeys k;
+  uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int64_t v = v0 + e;
-      ztv[e] = (v < V) ? load_logit<DT>(rt, v) : -kInf;
-      if (RESID) zdv[e] = (v < V) ? load_logit<DT>(rd, v) : 0.0f;
-    }
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = a;
+    k.k1[r] = b;
+    a += 0x9E3779B9u;
+    b += 0xBB67AE85u;
   }
-  const uint4 rnd = philox4x32_10(sv_counter((uint32_t)g, 1u, (uint32_t)st.pos, b, round),
-                                  (uint32_t)seed, (uint32_t)(seed >> 32));
+  return k;
+}
+__device__ __forceinline__ uint4 philox_rk(uint4 c, const PhiloxKeys& k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k.k0[r], lo1, hi0 ^ c.w ^ k.k1[r], lo0);
+  }
+  return c;
+}
+
+// Keys of one 4-entry Philox group v = v0 .. v0+3 from already loaded logits;
+// the running best is kept as a fraction num/den and compared by cross-products.
+template <bool RESID>
+__device__ __forceinline__ void draw_keys(const float* ztv, const float* zdv, int v0,
+                                          const DrawState& st, uint4 rnd, float& bn, float& bd,
+                                          int& bi) {
   const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    float key;
-    bool cand;
     const float et = ex2(fmaf(ztv[e], st.c, -st.mct));
+    float wgt;
+    bool cand;
     if (RESID) {
-      // log2(q/p) for this entry; p > q iff x < 0
+      // x = log2(q/p) for this entry; p > q iff x < 0; weight p - q = p (1 - 2^x)
       const float x = fmaf(zdv[e] - ztv[e], st.c, st.K);
       cand = x < 0.0f;
-      key = __fdividef(et * -expm1f(x * kLn2), sv_neglog_u(rr[e]));
+      const float y = x * kLn2;
+      // 1 - 2^x: Taylor series of -expm1(y) near 0, 1 - 2^x directly elsewhere
+      const float ser = -y * fmaf(y, fmaf(y, fmaf(y, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
+      const float om = (x > -0.125f) ? ser : 1.0f - ex2(x);
+      wgt = et * om;
     } else {
       cand = ztv[e] > -kInf;
-      key = __fdividef(et, sv_neglog_u(rr[e]));
+      wgt = et;
     }
-    if (cand && key > best.k) {
-      best.k = key;
-      best.i = (int)(v0 + e);
+    const float E = neglog2_u(rr[e]);
+    if (cand && wgt * bd > bn * E) {
+      bn = wgt;
+      bd = E;
+      bi = v0 + e;
     }
   }
+}
+
+// Raw 4-entry group of a row (bf16: 8 bytes, fp32: 16 bytes) and its widening.
+template <int DT>
+struct Group;
+template <>
+struct Group<SV_BF16> {
+  uint2 v;
+};
+template <>
+struct Group<SV_F32> {
+  float4 v;
+};
+
+template <int DT>
+__device__ __forceinline__ Group<DT> load_group(const char* row, int g, int V, bool vec_ok,
+                                                float pad) {
+  Group<DT> out;
+  const int v0 = 4 * g;
+  if (vec_ok && v0 + 3 < V) {
+    if constexpr (DT == SV_F32)
+      out.v = __ldg(reinterpret_cast<const float4*>(row) + g);
+    else
+      out.v = __ldg(reinterpret_cast<const uint2*>(row) + g);
+  } else {
+    float f[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) f[e] = (v0 + e < V) ? load_logit<DT>(row, v0 + e) : pad;
+    if constexpr (DT == SV_F32) {
+      out.v = make_float4(f[0], f[1], f[2], f[3]);
+    } else {
+      // re-pack as bf16 bits (the values are bf16-exact)
+      out.v.x = (__float_as_uint(f[0]) >> 16) | (__float_as_uint(f[1]) & 0xFFFF0000u);
+      out.v.y = (__float_as_uint(f[2]) >> 16) | (__float_as_uint(f[3]) & 0xFFFF0000u);
+    }
+  }
+  return out;
+}
+
+template <int DT>
+__device__ __forceinline__ void widen(const Group<DT>& g, float* f) {
+  if constexpr (DT == SV_F32) {
+    f[0] = g.v.x; f[1] = g.v.y; f[2] = g.v.z; f[3] = g.v.w;
+  } else {
+    f[0] = bf16lo(g.v.x); f[1] = bf16hi(g.v.x); f[2] = bf16lo(g.v.y); f[3] = bf16hi(g.v.y);
+  }
+}
+
+// This thread's best key over groups [g0, g1); all loads of a step in flight together.
+template <int DT, bool RESID>
+__device__ __forceinline__ KI draw_range(const char* rt, const char* rd, int g0, int g1, int V,
+                                         bool vec_ok, const DrawState& st, uint32_t b,
+                                         const PhiloxKeys& pk, uint64_t round) {
+  float bn = -1.0f, bd = 1.0f;
+  int bi = -1;
+  constexpr int U = (DT == SV_F32) ? 4 : 8;
+  const int stride = (int)blockDim.x;
+  for (int g = g0 + (int)threadIdx.x; g < g1; g += U * stride) {
+    Group<DT> gt[U], gd[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int gg = g + u * stride;
+      if (gg < g1) {
+        gt[u] = load_group<DT>(rt, gg, V, vec_ok, -kInf);
+        if (RESID) gd[u] = load_group<DT>(rd, gg, V, vec_ok, 0.0f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int gg = g + u * stride;
+      if (gg < g1) {
+        float zt4[4], zd4[4];
+        widen<DT>(gt[u], zt4);
+        if (RESID) widen<DT>(gd[u], zd4);
+        const uint4 rnd = philox_rk(sv_counter((uint32_t)gg, 1u, (uint32_t)st.pos, b, round), pk);
+        draw_keys<RESID>(zt4, zd4, 4 * gg, st, rnd, bn, bd, bi);
+      }
+    }
+  }
+  KI r;
+  r.i = bi;
+  r.k = (bi >= 0) ? bn / bd : -kInf;
+  return r;
 }
 
 // Double-precision key with the oracle-level definition, for the refinement.
@@ -371,8 +738,8 @@ __device__ double draw_key_f64(const char* rt, const char* rd, int64_t v, const 
                                bool resid, uint32_t b, uint64_t seed, uint64_t round) {
   const uint4 rnd = philox4x32_10(sv_counter((uint32_t)(v >> 2), 1u, (uint32_t)st.pos, b, round),
                                   (uint32_t)seed, (uint32_t)(seed >> 32));
-  const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
-  const double lnE = log(sv_neglog_u_f64(rr[v & 3]));
+  const uint32_t lanes[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+  const double lnE = log(sv_neglog_u_f64(lanes[v & 3]));
   const double zt = (double)load_logit<DT>(rt, v);
   if (!resid) return zt * (double)st.invT - lnE;
   const double zd = (double)load_logit<DT>(rd, v);
@@ -380,16 +747,6 @@ __device__ double draw_key_f64(const char* rt, const char* rd, int64_t v, const 
   const double Q = exp2(zd * (double)st.c - (double)st.mcd) / st.sd;
   const double r = P - Q;
   return (r > 0.0) ? log(r) - lnE : -CUDART_INF;
-}
-
-template <int DT, bool RESID>
-__device__ __forceinline__ KI draw_range(const char* rt, const char* rd, int64_t g0, int64_t g1,
-                                         int64_t V, bool vec_ok, const DrawState& st, uint32_t b,
-                                         uint64_t seed, uint64_t round) {
-  KI best{-kInf, -1};
-  for (int64_t g = g0 + threadIdx.x; g < g1; g += blockDim.x)
-    draw_group<DT, RESID>(rt, rd, g, V, vec_ok, st, b, seed, round, best);
-  return best;
 }
 
 __device__ __forceinline__ Top2 block_top2(KI mine) {
@@ -421,41 +778,42 @@ __device__ int refine(const Top2& t, const char* rt, const char* rd, const DrawS
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads) k_draw(DrawArgs a) {
-  const int b = (int)(blockIdx.x / (unsigned)a.nsplit);
-  const int split = (int)(blockIdx.x - (unsigned)b * (unsigned)a.nsplit);
-  const DrawState st = a.state[b];
-  if (st.mode == kDrawDone) return;
-  const bool resid = (st.mode == kDrawResidual);
+  const int b = (int)(blockIdx.x / (unsigned)a.nsplit3);
+  const int split = (int)(blockIdx.x - (unsigned)b * (unsigned)a.nsplit3);
   const int gamma = a.gamma;
   const int64_t V = a.V;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const DrawState st = a.state[b];
+  if (st.mode == kDrawDone) return;
+
+  const bool resid = (st.mode == kDrawResidual);
   const char* rt = row_ptr<DT>(a.zt, a.zd, b, st.pos, gamma, V);
   const char* rd = resid ? row_ptr<DT>(a.zt, a.zd, b, gamma + 1 + st.pos, gamma, V) : nullptr;
-  // 4-entry groups are vector-loadable when rows start on a group boundary
-  const bool vec_ok = (V % 4) == 0;
-  const int64_t ngroups = ceil_div(V, 4);
-  const int64_t gpc = kChunkDraw / 4;
-  const int64_t g0 = (int64_t)split * gpc, g1 = min(ngroups, g0 + gpc);
-
-  KI mine = resid ? draw_range<DT, true>(rt, rd, g0, g1, V, vec_ok, st, b, a.seed, a.round)
-                  : draw_range<DT, false>(rt, rd, g0, g1, V, vec_ok, st, b, a.seed, a.round);
+  const bool vec_ok = (V % 4) == 0;  // 4-entry groups start 4-entry aligned in every row
+  const int Vi = (int)V;             // V < 2^31
+  const int ngroups = (int)ceil_div(V, 4);
+  const int gpc = (int)(kChunkDraw / 4);
+  const int g0 = split * gpc, g1 = min(ngroups, g0 + gpc);
+  const PhiloxKeys pk = philox_keys(a.seed);
+  KI mine = resid ? draw_range<DT, true>(rt, rd, g0, g1, Vi, vec_ok, st, b, pk, a.round)
+                  : draw_range<DT, false>(rt, rd, g0, g1, Vi, vec_ok, st, b, pk, a.round);
   Top2 t = block_top2(mine);
 
   __shared__ bool s_last;
-  if (threadIdx.x == 0) {
-    a.part[(int64_t)b * a.nsplit + split] = t;
+  if (tid == 0) {
+    a.part3[(int64_t)b * a.nsplit3 + split] = t;
     __threadfence();
-    const uint32_t prev = atomicAdd(a.counter + b, 1u);
-    s_last = (prev == (uint32_t)a.nsplit - 1);
+    s_last = is_last(atomicAdd(a.counter + b, 1u), (uint32_t)a.nsplit3);
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
 
-  // last CTA of batch row b: merge the per-CTA top-2
+  // last CTA of batch row b: merge the per-CTA top-2 and decide
   Top2 m{KI{-kInf, -1}, KI{-kInf, -1}};
-  for (int j = threadIdx.x; j < a.nsplit; j += blockDim.x) {
-    // other CTAs' partials: read through L2 (never cached in this SM's L1)
-    const float4 raw = __ldcg(reinterpret_cast<const float4*>(a.part + (int64_t)b * a.nsplit + j));
+  for (int j = tid; j < a.nsplit3; j += blockDim.x) {
+    const float4 raw =
+        __ldcg(reinterpret_cast<const float4*>(a.part3 + (int64_t)b * a.nsplit3 + j));
     Top2 p;
     p.a.k = raw.x;
     p.a.i = __float_as_int(raw.y);
@@ -465,39 +823,38 @@ __global__ void __launch_bounds__(kThreads) k_draw(DrawArgs a) {
   }
   __shared__ Top2 sm2[kThreads / 32];
   m = warp_reduce_top2(m);
-  if ((threadIdx.x & 31) == 0) sm2[threadIdx.x >> 5] = m;
+  if (lane == 0) sm2[warp] = m;
   __syncthreads();
   __shared__ int s_tok;
   __shared__ int s_fallback;
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     Top2 r{KI{-kInf, -1}, KI{-kInf, -1}};
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r = top2_merge(r, sm2[w]);
-    const int tok = refine<DT>(r, rt, rd, st, resid, (uint32_t)b, a.seed, a.round);
-    s_tok = tok;
-    s_fallback = (tok < 0 && resid) ? 1 : 0;
-    a.counter[b] = 0u;  // leave the workspace ready for the next call
+    const int tk = refine<DT>(r, rt, rd, st, resid, (uint32_t)b, a.seed, a.round);
+    s_tok = tk;
+    s_fallback = (tk < 0 && resid) ? 1 : 0;
   }
   __syncthreads();
   if (s_fallback) {
     // the residual had no positive entry in floating point: draw from p_n itself
     DrawState sp = st;
     sp.mode = kDrawSampleRow;
-    KI f = draw_range<DT, false>(rt, nullptr, 0, ngroups, V, vec_ok, sp, b, a.seed, a.round);
+    KI f = draw_range<DT, false>(rt, nullptr, 0, ngroups, Vi, vec_ok, sp, b, pk, a.round);
     Top2 tf = block_top2(f);
-    if (threadIdx.x == 0) s_tok = refine<DT>(tf, rt, nullptr, sp, false, (uint32_t)b, a.seed,
-                                             a.round);
+    if (tid == 0)
+      s_tok = refine<DT>(tf, rt, nullptr, sp, false, (uint32_t)b, a.seed, a.round);
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    int tok = s_tok;
-    uint8_t fl = 0;
+  if (tid == 0) {
+    int tk = s_tok;
+    int fl = st.flags;
     if (s_fallback) fl |= SV_FLAG_RESIDUAL_FALLBACK;
-    if (tok < 0) {
-      tok = 0;
+    if (tk < 0) {
+      tk = 0;
       fl |= SV_FLAG_ZERO_MASS;
     }
-    a.out_tokens[(int64_t)b * (gamma + 1) + st.pos] = tok;
-    if (a.out_flags && fl) a.out_flags[b] |= fl;
+    a.out_tokens[(int64_t)b * (gamma + 1) + st.pos] = tk;
+    if (a.out_flags) a.out_flags[b] = (uint8_t)fl;
   }
 }
 
@@ -541,8 +898,7 @@ k_alpha(const void* __restrict__ zt, const void* __restrict__ zd, int gamma, int
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += sm[w];
     part[((int64_t)b * gamma + i) * nsplit + split] = s;
     __threadfence();
-    const uint32_t prev = atomicAdd(counter + b, 1u);
-    s_last = (prev == (uint32_t)(gamma * nsplit) - 1);
+    s_last = is_last(atomicAdd(counter + b, 1u), (uint32_t)(gamma * nsplit));
   }
   __syncthreads();
   if (!s_last || threadIdx.x != 0) return;
@@ -551,11 +907,10 @@ k_alpha(const void* __restrict__ zt, const void* __restrict__ zd, int gamma, int
   const float* pp = part + (int64_t)b * gamma * nsplit;
   for (int j = 0; j < gamma * nsplit; ++j) tot += (double)__ldcg(pp + j);
   out_alpha[b] = (float)(tot / gamma);
-  counter[b] = 0u;
 }
 
 // --------------------------------------------------------------------------
-// Host-side launcher.
+// Host side.
 // --------------------------------------------------------------------------
 static cudaEvent_t g_events[4] = {nullptr, nullptr, nullptr, nullptr};
 
@@ -567,6 +922,43 @@ static inline void mark(int i, cudaStream_t s) {
   if (g_events[i]) cudaEventRecord(g_events[i], s);
 }
 
+// Per-device launch facts for the persistent sweep, looked up once per device.
+struct DeviceInfo {
+  int sms = 0;
+  int sweep_ctas_per_sm[2] = {0, 0};  // by dtype
+  bool ready = false;
+};
+static std::mutex g_dev_mu;
+static DeviceInfo g_dev[64];
+
+static cudaError_t device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int smem = (int)sweep_smem_bytes();
+    e = cudaFuncSetAttribute(k_sweep_tma<SV_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_sweep_tma<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sweep_ctas_per_sm[SV_F32],
+                                                      k_sweep_tma<SV_F32>, kSweepWarps * 32, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sweep_ctas_per_sm[SV_BF16],
+                                                      k_sweep_tma<SV_BF16>, kSweepWarps * 32, smem);
+    if (e != cudaSuccess) return e;
+    d.ready = true;
+  }
+  *out = &d;
+  return cudaSuccess;
+}
+
 template <int DT>
 static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t* xt, int B,
                                    int gamma, int64_t V, float temperature, const float* row_T,
@@ -575,28 +967,48 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
                                    float* out_alpha, uint8_t* out_flags, char* ws,
                                    const SamplePlan& pl, cudaStream_t stream) {
   const int R1 = pl.R1;
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + pl.off_cnt);
   float2* part1 = reinterpret_cast<float2*>(ws + pl.off_part1);
   RowStat* rowstat = reinterpret_cast<RowStat*>(ws + pl.off_rowstat);
   DrawState* state = reinterpret_cast<DrawState*>(ws + pl.off_state);
   Top2* part3 = reinterpret_cast<Top2*>(ws + pl.off_part3);
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + pl.off_cnt);
   float* apart = reinterpret_cast<float*>(ws + pl.off_alpha);
-
-  const unsigned g1 = (unsigned)((int64_t)pl.nsplit1 * B * R1);
+  uint32_t* draw_cnt = cnt;
+  uint32_t* alpha_cnt = cnt + B;
+  bool tma = use_tma_sweep(DT, V);
+  DeviceInfo* di = nullptr;
+  if (tma) {
+    const cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    tma = di->sweep_ctas_per_sm[DT] > 0;
+  }
+  const int nch = (int)(tma ? ceil_div(V, tma_chunk_elems(DT)) : ceil_div(V, kChunkSweep));
+  SweepCtx sx{zt, zd, xt, B, gamma, V, temperature, row_T, seed, round, nch, part1, rowstat,
+              state, out_tokens, out_counts, out_p, out_q, out_flags};
   mark(0, stream);
-  k_sweep<DT><<<g1, kThreads, 0, stream>>>(zt, zd, gamma, V, temperature, row_T, pl.nsplit1,
-                                            part1);
+  if (tma) {
+    // one resident wave of warps, chunks dealt round-robin
+    const int64_t nc = (int64_t)B * R1 * nch;
+    const int64_t full = (int64_t)di->sms * di->sweep_ctas_per_sm[DT];
+    const int64_t need = ceil_div(nc, kSweepWarps);
+    const int64_t g = full < need ? full : need;
+    k_sweep_tma<DT><<<(unsigned)(g < 1 ? 1 : g), kSweepWarps * 32, sweep_smem_bytes(), stream>>>(
+        sx);
+  } else {
+    k_sweep<DT><<<(unsigned)((int64_t)nch * B * R1), kThreads, 0, stream>>>(sx);
+  }
   mark(1, stream);
-  k_decide<DT><<<B, 128, 0, stream>>>(zt, zd, xt, gamma, V, temperature, row_T, seed, round,
-                                       pl.nsplit1, part1, rowstat, state, cnt, B, out_tokens,
-                                       out_counts, out_p, out_q, out_flags);
+  const int fw = R1 < 32 ? R1 : 32;  // one warp per row
+  k_finish<DT><<<(unsigned)B, 32 * fw, 0, stream>>>(sx, cnt);
   mark(2, stream);
-  DrawArgs da{zt, zd, gamma, V, seed, round, pl.nsplit3, state, part3, cnt, out_tokens, out_flags};
+  DrawArgs da{zt, zd, B, gamma, V, seed, round, state, draw_cnt, part3, pl.nsplit3, out_tokens,
+              out_flags};
   k_draw<DT><<<(unsigned)((int64_t)pl.nsplit3 * B), kThreads, 0, stream>>>(da);
   mark(3, stream);
   if (out_alpha) {
-    k_alpha<DT><<<(unsigned)((int64_t)pl.nsplit1 * gamma * B), kThreads, 0, stream>>>(
-        zt, zd, gamma, V, temperature, row_T, pl.nsplit1, rowstat, apart, cnt + B, out_alpha);
+    const int ns = (int)ceil_div(V, kChunkSweep);
+    k_alpha<DT><<<(unsigned)((int64_t)ns * gamma * B), kThreads, 0, stream>>>(
+        zt, zd, gamma, V, temperature, row_T, ns, rowstat, apart, alpha_cnt, out_alpha);
   }
   return cudaGetLastError();
 }
