@@ -83,7 +83,7 @@ inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
   // per-(row, chunk) partials: enough for the smaller bulk-copy chunks of fp32
   const int64_t nch_max = ceil_div(V, tma_chunk_elems(0));
   size_t o = 0;
-  p.cnt_bytes = sizeof(uint32_t) * 2 * (size_t)B;  // draw and overlap CTA counters
+  p.cnt_bytes = sizeof(uint32_t) * (2 * (size_t)B + 1);  // draw, overlap, draw work
   p.off_cnt = o;      o = align_up(o + p.cnt_bytes);
   p.off_rowstat = o;  o = align_up(o + sizeof(RowStat) * (size_t)B * p.R1);
   p.off_part1 = o;    o = align_up(o + 8 * (size_t)B * p.R1 * (size_t)nch_max);

@@ -152,8 +152,15 @@ __device__ __forceinline__ float prob_from(float z, const Exp2& e, const RowStat
 
 // The decision for batch row b (one warp): accept test, prefix, draw set-up.
 // srs[k] holds the statistics of row k of the batch row.
+// Draft token i of a batch row and the two logits at it.
+struct DraftAt {
+  int32_t x;
+  float zt, zd;
+};
+
 template <int DT>
-__device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs) {
+__device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
+                                 const DraftAt* sda) {
   const int lane = threadIdx.x & 31;
   const int gamma = x.gamma;
   const int64_t V = x.V;
@@ -171,13 +178,15 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs) {
   }
   bool accept = false, bad = false, qzero = false;
   double P = 0.0, Q = 0.0;
+  int32_t xi = 0;
   if (lane < gamma) {
-    const int32_t xi = __ldg(x.xt + (int64_t)b * gamma + lane);
+    const DraftAt da = sda[lane];
+    xi = da.x;
     bad = (xi < 0 || (int64_t)xi >= V);
     float ratio = CUDART_NAN_F;  // a bad token: p = q = 0, rejected
     if (!bad) {
-      const float zx = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, lane, gamma, V), xi);
-      const float zy = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + lane, gamma, V), xi);
+      const float zx = da.zt;
+      const float zy = da.zd;
       const RowStat rt = srs[lane], rd = srs[gamma + 1 + lane];
       const Exp2 ep = exponent_at(zx, c, rt.mc), eq = exponent_at(zy, c, rd.mc);
       P = prob_from(zx, ep, rt);
@@ -210,10 +219,9 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs) {
   if (__ballot_sync(0xffffffffu, lane < gamma && lane <= n && qzero)) fl |= SV_FLAG_NONFINITE;
   fl = __reduce_or_sync(0xffffffffu, fl);
   int32_t* tok = x.out_tokens + (int64_t)b * (gamma + 1);
-  for (int i = lane; i <= gamma; i += 32) {
-    if (i < n) tok[i] = __ldg(x.xt + (int64_t)b * gamma + i);
-    else if (i > n) tok[i] = -1;
-  }
+  if (lane < n) tok[lane] = xi;  // n <= gamma <= 32
+  for (int i = lane; i <= gamma; i += 32)
+    if (i > n) tok[i] = -1;
   if (lane == 0) {
     // set up the draw of the target's own token
     const float mct = srs[n].mc;
@@ -263,24 +271,46 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs) {
   }
 }
 
-// One CTA per batch row: row statistics (one warp per row), then the decision.
+// One CTA per batch row: row statistics (one warp per row) while one more warp
+// fetches the draft tokens and their target/draft logits, then the decision.
 template <int DT>
 __global__ void __launch_bounds__(1024) k_finish(SweepCtx x, uint32_t* __restrict__ counters) {
   const int b = blockIdx.x;
-  const int R1 = 2 * x.gamma + 1;
+  const int gamma = x.gamma;
+  const int R1 = 2 * gamma + 1;
+  const int nrw = (int)(blockDim.x >> 5) - 1;  // row warps; the last warp prefetches
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ RowStat srs[65];
+  __shared__ DraftAt sda[32];
+  pdl_launch_dependents();
+  if (warp == nrw) {
+    // independent of the sweep: read before waiting for it
+    if (lane < gamma) {
+      DraftAt d;
+      d.x = __ldg(x.xt + (int64_t)b * gamma + lane);
+      d.zt = d.zd = 0.0f;
+      if (d.x >= 0 && (int64_t)d.x < x.V) {
+        d.zt = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, lane, gamma, x.V), d.x);
+        d.zd = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + lane, gamma, x.V), d.x);
+      }
+      sda[lane] = d;
+    }
+  }
+  pdl_wait();  // the sweep's partials
   if (threadIdx.x == 0) {  // counters of the draw and overlap kernels that follow
     counters[b] = 0u;
     counters[x.B + b] = 0u;
+    if (b == 0) counters[2 * x.B] = 0u;  // the draw's work counter
   }
-  for (int k = warp; k < R1; k += (int)(blockDim.x >> 5)) {
-    const RowStat rs = combine_row(x.part + ((int64_t)b * R1 + k) * x.nch, x.nch,
-                                   x.rowstat + (int64_t)b * R1 + k);
-    if (lane == 0) srs[k] = rs;
+  if (warp < nrw) {
+    for (int k = warp; k < R1; k += nrw) {
+      const RowStat rs = combine_row(x.part + ((int64_t)b * R1 + k) * x.nch, x.nch,
+                                     x.rowstat + (int64_t)b * R1 + k);
+      if (lane == 0) srs[k] = rs;
+    }
   }
   __syncthreads();
-  if (warp == 0) decide_batch_row<DT>(x, b, srs);
+  if (warp == 0) decide_batch_row<DT>(x, b, srs, sda);
 }
 
 // --------------------------------------------------------------------------
@@ -320,6 +350,7 @@ __device__ __forceinline__ void for_each_in_chunk(const char* row, int64_t lo, i
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
+  pdl_launch_dependents();
   const int R1 = 2 * x.gamma + 1;
   const int64_t item = blockIdx.x;  // (row, chunk) flattened, rows in batch-row order
   const int64_t r = item / x.nch;
@@ -443,8 +474,42 @@ __device__ __forceinline__ void chunk_update_full(const uint4* sv, int lane, flo
 // Chunk c of the [b][row][chunk] order goes to warp c mod W, so the whole GPU
 // walks memory in address order; each chunk leaves one (max, sum) partial.
 // --------------------------------------------------------------------------
+// Position of a chunk: batch row b, row k of it, chunk j of the row, advanced
+// by a fixed stride without divisions.
+struct ChunkPos {
+  int b, k, j;
+};
+struct ChunkStep {
+  int db, dk, dj;  // stride W = ((db * R1) + dk) * nch + dj chunks
+};
+__device__ __forceinline__ void advance(ChunkPos& p, const ChunkStep& d, int R1, int nch) {
+  p.j += d.dj;
+  int carry_k = 0;
+  if (p.j >= nch) {
+    p.j -= nch;
+    carry_k = 1;
+  }
+  p.k += d.dk + carry_k;
+  int carry_b = 0;
+  if (p.k >= R1) {
+    p.k -= R1;
+    carry_b = 1;
+  }
+  p.b += d.db + carry_b;
+}
+
+// Warp max of m, then one rescale per lane and a warp sum.
+__device__ __forceinline__ MS warp_reduce_ms_fast(MS v) {
+  const float M = warp_max(v.m);
+  float s = (v.m > -kInf) ? v.s * ex2(v.m - M) : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return MS{M, (M > -kInf) ? s : 0.0f};
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
+  pdl_launch_dependents();  // the finish kernel may be scheduled now; it waits for us
   constexpr int kBytes = (DT == SV_F32) ? 4 : 2;
   constexpr int CH = kSweepChunkBytes / kBytes;  // logits per chunk
   extern __shared__ __align__(128) unsigned char smem[];
@@ -462,6 +527,7 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
   const int64_t w = (int64_t)blockIdx.x * kSweepWarps + warp;
   const int count = (w < NC) ? (int)((NC - w + W - 1) / W) : 0;  // chunks w, w+W, ...
   const uint32_t tail_bytes = (uint32_t)((V - (int64_t)(nch - 1) * CH) * kBytes);
+  const size_t row_bytes = (size_t)V * kBytes;
 
   if (lane == 0) {
     for (int s = 0; s < kSweepStages; ++s) mbar_init(bars + s, 1);
@@ -469,47 +535,62 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
   }
   __syncwarp();
 
-  auto src_of = [&](int64_t cidx, uint32_t& bytes, int64_t& r) -> const char* {
-    r = cidx / nch;
-    const int j = (int)(cidx - r * nch);
-    const int b = (int)(r / R1);
-    bytes = (j == nch - 1) ? tail_bytes : (uint32_t)kSweepChunkBytes;
-    return row_ptr<DT>(x.zt, x.zd, b, (int)(r - (int64_t)b * R1), gamma, V) +
-           (size_t)j * kSweepChunkBytes;
+  auto pos_of = [&](int64_t cidx) {
+    ChunkPos p;
+    const int64_t r = cidx / nch;
+    p.j = (int)(cidx - r * nch);
+    p.b = (int)(r / R1);
+    p.k = (int)(r - (int64_t)p.b * R1);
+    return p;
   };
-  auto issue = [&](int s, int64_t cidx) {  // lane 0 only
-    uint32_t bytes;
-    int64_t r;
-    const char* src = src_of(cidx, bytes, r);
+  ChunkStep step;
+  {
+    const int64_t r = W / nch;
+    step.dj = (int)(W - r * nch);
+    step.db = (int)(r / R1);
+    step.dk = (int)(r - (int64_t)step.db * R1);
+  }
+  auto src_of = [&](const ChunkPos& p) -> const char* {
+    const char* row = (p.k <= gamma)
+        ? reinterpret_cast<const char*>(x.zt) + ((size_t)p.b * (gamma + 1) + p.k) * row_bytes
+        : reinterpret_cast<const char*>(x.zd) + ((size_t)p.b * gamma + (p.k - gamma - 1)) * row_bytes;
+    return row + (size_t)p.j * kSweepChunkBytes;
+  };
+  auto issue = [&](int s, const ChunkPos& p) {  // lane 0 only
+    const uint32_t bytes = (p.j == nch - 1) ? tail_bytes : (uint32_t)kSweepChunkBytes;
     mbar_arrive_expect_tx(bars + s, bytes);
-    bulk_g2s(stage0 + (size_t)s * kSweepChunkBytes, src, bytes, bars + s);
+    bulk_g2s(stage0 + (size_t)s * kSweepChunkBytes, src_of(p), bytes, bars + s);
   };
 
-  if (lane == 0)
-    for (int s = 0; s < kSweepStages && s < count; ++s) issue(s, w + (int64_t)s * W);
+  ChunkPos pi = pos_of(w);  // next chunk to issue
+  for (int s = 0; s < kSweepStages && s < count; ++s) {
+    if (lane == 0) issue(s, pi);
+    advance(pi, step, R1, nch);
+  }
 
   bool dead = false;  // a bounded wait ran out: stop loading, mark what is left
   int issued = count < kSweepStages ? count : kSweepStages;  // chunks issued so far
-
-  for (int t = 0; t < count; ++t) {
+  ChunkPos pc = pos_of(w);  // chunk being computed
+  int64_t cidx = w;
+  int cur_b = -1;
+  float c = 0.0f;
+  for (int t = 0; t < count; ++t, cidx += W, advance(pc, step, R1, nch)) {
     const int s = t % kSweepStages;
     const uint32_t parity = (uint32_t)((t / kSweepStages) & 1);
-    const int64_t cidx = w + (int64_t)t * W;
-    uint32_t bytes;
-    int64_t r;
-    src_of(cidx, bytes, r);
     float2 res;
     if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait_bounded(bars + s, parity));
     if (!dead) {
-      const int b = (int)(r / R1);
-      const float T = x.row_T ? __ldg(x.row_T + b) : x.temperature;
-      const float c = log2_scale(inv_temperature(T));
+      if (pc.b != cur_b) {
+        cur_b = pc.b;
+        const float T = x.row_T ? __ldg(x.row_T + cur_b) : x.temperature;
+        c = log2_scale(inv_temperature(T));
+      }
       const uint4* sv = reinterpret_cast<const uint4*>(stage0 + (size_t)s * kSweepChunkBytes);
       float zmax = -kInf, mc = -kInf, sacc = 0.0f;
-      if (bytes == (uint32_t)kSweepChunkBytes) {
+      if (pc.j != nch - 1) {
         chunk_update_full<DT>(sv, lane, c, zmax, mc, sacc);
       } else {
-        const int nvec = (int)(bytes / 16);
+        const int nvec = (int)(tail_bytes / 16);
         uint4 v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
@@ -537,16 +618,17 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
           sacc += s0 + s1;
         }
       }
-      const MS ms = warp_reduce_ms(MS{mc, sacc});
-      res = make_float2(ms.m, ms.s);
       __syncwarp();
       if (t + kSweepStages < count) {
         if (lane == 0) {
           fence_proxy_async_smem();
-          issue(s, cidx + (int64_t)kSweepStages * W);
+          issue(s, pi);
         }
+        advance(pi, step, R1, nch);
         issued = t + kSweepStages + 1;
       }
+      const MS ms = warp_reduce_ms_fast(MS{mc, sacc});
+      res = make_float2(ms.m, ms.s);
     } else {
       res = make_float2(CUDART_NAN_F, -1.0f);  // timed-out chunk: flagged downstream
     }
@@ -571,8 +653,9 @@ struct DrawArgs {
   uint64_t seed, round;
   const DrawState* state;  // [B]
   uint32_t* counter;       // [B] CTAs done per batch row
+  uint32_t* work;          // unused by the CTA-per-chunk draw
   Top2* part3;             // [B][nsplit3]
-  int nsplit3;
+  int nsplit3;             // CTAs per batch row
   int32_t* out_tokens;
   uint8_t* out_flags;
 };
@@ -783,6 +866,7 @@ __global__ void __launch_bounds__(kThreads) k_draw(DrawArgs a) {
   const int gamma = a.gamma;
   const int64_t V = a.V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();  // the decision's draw states and zeroed counters
   const DrawState st = a.state[b];
   if (st.mode == kDrawDone) return;
 
@@ -953,10 +1037,30 @@ static cudaError_t device_info(DeviceInfo** out) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sweep_ctas_per_sm[SV_BF16],
                                                       k_sweep_tma<SV_BF16>, kSweepWarps * 32, smem);
     if (e != cudaSuccess) return e;
+
     d.ready = true;
   }
   *out = &d;
   return cudaSuccess;
+}
+
+// Launch with programmatic stream serialisation: the kernel may start while the
+// previous one on the stream drains, and waits for it with griddepcontrol.wait.
+// Without event markers only: an event recorded between the two would order them.
+template <class... KArgs, class... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <int DT>
@@ -998,12 +1102,15 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
     k_sweep<DT><<<(unsigned)((int64_t)nch * B * R1), kThreads, 0, stream>>>(sx);
   }
   mark(1, stream);
-  const int fw = R1 < 32 ? R1 : 32;  // one warp per row
-  k_finish<DT><<<(unsigned)B, 32 * fw, 0, stream>>>(sx, cnt);
+  const int fw = (R1 < 31 ? R1 : 31) + 1;  // one warp per row, one prefetching
+  cudaError_t e = launch_pdl(k_finish<DT>, dim3((unsigned)B), dim3(32 * fw), stream, sx, cnt);
+  if (e != cudaSuccess) return e;
   mark(2, stream);
-  DrawArgs da{zt, zd, B, gamma, V, seed, round, state, draw_cnt, part3, pl.nsplit3, out_tokens,
-              out_flags};
-  k_draw<DT><<<(unsigned)((int64_t)pl.nsplit3 * B), kThreads, 0, stream>>>(da);
+  DrawArgs da{zt, zd, B, gamma, V, seed, round, state, draw_cnt, cnt + 2 * B, part3, pl.nsplit3,
+              out_tokens, out_flags};
+  e = launch_pdl(k_draw<DT>, dim3((unsigned)((int64_t)pl.nsplit3 * B)), dim3(kThreads), stream,
+                 da);
+  if (e != cudaSuccess) return e;
   mark(3, stream);
   if (out_alpha) {
     const int ns = (int)ceil_div(V, kChunkSweep);

@@ -72,4 +72,12 @@ __device__ __forceinline__ uint32_t atom_add_acqrel_gpu(uint32_t* p, uint32_t v)
   return old;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream launch
+// early / wait here until the previous kernel has completed and its writes are
+// visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace sv
