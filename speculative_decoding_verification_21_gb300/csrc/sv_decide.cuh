@@ -1,0 +1,226 @@
+// sv_decide.cuh -- the decision of one round for one batch row (accept test,
+// prefix, set-up of the draw), shared by the logits path and the fused LM-head
+// path, plus the row-combine of chunk partials.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <cstdint>
+
+#include "specverify.h"
+#include "sv_device.cuh"
+#include "sv_plan.h"
+
+namespace sv {
+
+__device__ __forceinline__ float inv_temperature(float T) { return 1.0f / T; }
+__device__ __forceinline__ float log2_scale(float invT) { return invT * kLog2e; }
+__device__ __forceinline__ bool temperature_ok(float T) { return T > 0.0f && T < kInf; }
+
+// Row k of batch row b: target rows k = 0..gamma, draft rows k = gamma+1..2gamma.
+template <int DT>
+__device__ __forceinline__ const char* row_ptr(const void* zt, const void* zd, int b, int k,
+                                               int gamma, int64_t V) {
+  constexpr int kBytes = (DT == SV_F32) ? 4 : 2;
+  if (k <= gamma)
+    return reinterpret_cast<const char*>(zt) + (((int64_t)b * (gamma + 1) + k) * V) * kBytes;
+  return reinterpret_cast<const char*>(zd) + (((int64_t)b * gamma + (k - gamma - 1)) * V) * kBytes;
+}
+
+// --------------------------------------------------------------------------
+// Row combine and decision (k_finish).
+// --------------------------------------------------------------------------
+struct SweepCtx {
+  const void* zt;
+  const void* zd;
+  const int32_t* xt;
+  int B, gamma;
+  int64_t V;
+  float temperature;
+  const float* row_T;
+  uint64_t seed, round;
+  int nch;               // chunk partials per logit row
+  float2* part;          // [B][R1][nch]
+  RowStat* rowstat;      // [B][R1]
+  DrawState* state;      // [B]
+  int32_t* out_tokens;
+  int32_t* out_counts;
+  float* out_p;
+  float* out_q;
+  uint8_t* out_flags;
+};
+
+// Row statistics of row r from its chunk partials (one warp, all loads of a
+// lane in flight together), kept by lane 0 and written to rowstat[r].
+__device__ __forceinline__ RowStat combine_row(const float2* pr, int nch, RowStat* out) {
+  const int lane = threadIdx.x & 31;
+  float m = -kInf, s = 0.0f;
+  int bits = 0;
+#pragma unroll 4
+  for (int j = lane; j < nch; j += 32) {
+    const float2 p = __ldcg(pr + j);
+    if (p.x != p.x) bits |= kRowNaN;
+    if (p.y < 0.0f) bits |= kRowTimeout;
+    if (p.x > m) {
+      s = (m == -kInf) ? 0.0f : s * exp2f(m - p.x);
+      m = p.x;
+    }
+    if (p.x > -kInf) s += p.y * exp2f(p.x - m);
+  }
+  const float M = warp_max(m);
+  float sl = (m > -kInf) ? s * exp2f(m - M) : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, o);
+  bits = __reduce_or_sync(0xffffffffu, bits);
+  RowStat rs;
+  rs.mc = M;
+  rs.bits = bits;
+  rs.s = (bits & kRowNaN) ? CUDART_NAN : (double)sl;
+  if (lane == 0 && out) *out = rs;
+  return rs;
+}
+
+// log2 of the unnormalised probability, e = z c - mc, carried in two floats:
+// z c = ph + pl exactly (FMA residual) and ph - mc by TwoSum, so e = hi + lo
+// to about 2^-48 relative.
+struct Exp2 {
+  float hi, lo;
+};
+__device__ __forceinline__ Exp2 exponent_at(float z, float c, float mc) {
+  const float ph = z * c;
+  const float pl = fmaf(z, c, -ph);
+  const float a = ph - mc;
+  const float bv = a - ph;
+  const float err = (ph - (a - bv)) + (-mc - bv);
+  return Exp2{a, err + pl};
+}
+// p(x) from its exponent and the row sum (0 for a -inf logit or an empty row).
+__device__ __forceinline__ float prob_from(float z, const Exp2& e, const RowStat& r) {
+  if (!(r.s > 0.0)) return (r.s == 0.0) ? 0.0f : (float)r.s;  // NaN stays NaN
+  if (z == -kInf) return 0.0f;
+  return exp2f(e.hi) * fmaf(e.lo, kLn2, 1.0f) / (float)r.s;
+}
+
+// The decision for batch row b (one warp): accept test, prefix, draw set-up.
+// srs[k] holds the statistics of row k of the batch row.
+// Draft token i of a batch row and the two logits at it.
+struct DraftAt {
+  int32_t x;
+  float zt, zd;
+};
+
+template <int DT>
+__device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
+                                 const DraftAt* sda) {
+  const int lane = threadIdx.x & 31;
+  const int gamma = x.gamma;
+  const int64_t V = x.V;
+  const int R1 = 2 * gamma + 1;
+  const float T = x.row_T ? __ldg(x.row_T + b) : x.temperature;
+  const float invT = inv_temperature(T);
+  const float c = log2_scale(invT);
+
+  int fl = 0;
+  for (int k = lane; k < R1; k += 32) {
+    const RowStat v = srs[k];
+    if (v.mc == -kInf) fl |= SV_FLAG_ZERO_MASS;
+    if (!(v.s < CUDART_INF) || v.mc == kInf || !temperature_ok(T)) fl |= SV_FLAG_NONFINITE;
+    if (v.bits & kRowTimeout) fl |= SV_FLAG_TIMEOUT | SV_FLAG_NONFINITE;
+  }
+  bool accept = false, bad = false, qzero = false;
+  double P = 0.0, Q = 0.0;
+  int32_t xi = 0;
+  if (lane < gamma) {
+    const DraftAt da = sda[lane];
+    xi = da.x;
+    bad = (xi < 0 || (int64_t)xi >= V);
+    float ratio = CUDART_NAN_F;  // a bad token: p = q = 0, rejected
+    if (!bad) {
+      const float zx = da.zt;
+      const float zy = da.zd;
+      const RowStat rt = srs[lane], rd = srs[gamma + 1 + lane];
+      const Exp2 ep = exponent_at(zx, c, rt.mc), eq = exponent_at(zy, c, rd.mc);
+      P = prob_from(zx, ep, rt);
+      Q = prob_from(zy, eq, rd);
+      // p/q from the exponent difference (no underflow of p and q themselves);
+      // q = 0 with p > 0 gives inf (accept), p = q = 0 gives NaN (reject)
+      const bool p0 = !(rt.s > 0.0) || zx == -kInf, q0 = !(rd.s > 0.0) || zy == -kInf;
+      if (rt.s != rt.s || rd.s != rd.s) {
+        ratio = CUDART_NAN_F;
+      } else if (p0 || q0) {
+        ratio = p0 ? (q0 ? CUDART_NAN_F : 0.0f) : kInf;
+      } else {
+        const float d = (ep.hi - eq.hi) + (ep.lo - eq.lo);
+        ratio = exp2f(d) * (float)(rd.s / rt.s);
+      }
+      qzero = q0 || !(rd.s == rd.s);
+    } else {
+      qzero = true;
+    }
+    const uint4 rnd = philox4x32_10(sv_counter(0u, 0u, (uint32_t)lane, (uint32_t)b, x.round),
+                                    (uint32_t)x.seed, (uint32_t)(x.seed >> 32));
+    accept = (sv_u01(rnd.x) <= ratio);
+    if (x.out_p) x.out_p[(int64_t)b * gamma + lane] = (float)P;
+    if (x.out_q) x.out_q[(int64_t)b * gamma + lane] = (float)Q;
+  }
+  const unsigned rej = ~__ballot_sync(0xffffffffu, accept);
+  const int n = (rej == 0u) ? 32 : min(__ffs((int)rej) - 1, gamma);
+  // flags: bad tokens anywhere, q(x) = 0 at a tested position (i <= n, i < gamma)
+  if (__ballot_sync(0xffffffffu, bad)) fl |= SV_FLAG_BAD_TOKEN;
+  if (__ballot_sync(0xffffffffu, lane < gamma && lane <= n && qzero)) fl |= SV_FLAG_NONFINITE;
+  fl = __reduce_or_sync(0xffffffffu, fl);
+  int32_t* tok = x.out_tokens + (int64_t)b * (gamma + 1);
+  if (lane < n) tok[lane] = xi;  // n <= gamma <= 32
+  for (int i = lane; i <= gamma; i += 32)
+    if (i > n) tok[i] = -1;
+  if (lane == 0) {
+    // set up the draw of the target's own token
+    const float mct = srs[n].mc;
+    const double St = srs[n].s;
+    DrawState st{};
+    st.pos = n;
+    st.c = c;
+    st.invT = invT;
+    const bool t_ok = (St > 0.0) && (St < 1e308) && (mct < kInf);
+    if (n == gamma) {
+      if (t_ok) {
+        st.mode = kDrawSampleRow;
+        st.mct = mct;
+        st.st = St;
+      } else {
+        st.mode = kDrawDone;
+      }
+    } else {
+      const float mcd = srs[gamma + 1 + n].mc;
+      const double Sd = srs[gamma + 1 + n].s;
+      const bool d_nonfinite = !(Sd < 1e308) || mcd == kInf;
+      if (!t_ok || d_nonfinite) {
+        // p_n has no mass (or a row is not finite): the residual and its fallback
+        // are empty; token 0
+        st.mode = kDrawDone;
+        if (St == 0.0) fl |= SV_FLAG_RESIDUAL_FALLBACK;
+      } else if (Sd == 0.0) {
+        st.mode = kDrawSampleRow;  // q_n has no mass: max(0, p_n - q_n) = p_n
+        st.mct = mct;
+        st.st = St;
+      } else {
+        st.mode = kDrawResidual;
+        st.mct = mct;
+        st.st = St;
+        st.mcd = mcd;
+        st.sd = Sd;
+        st.K = (mct - mcd) + (log2f((float)St) - log2f((float)Sd));
+      }
+    }
+    st.flags = fl;
+    x.state[b] = st;
+    x.out_counts[b] = n;
+    if (st.mode == kDrawDone) {
+      tok[n] = 0;
+      if (x.out_flags) x.out_flags[b] = (uint8_t)fl;
+    }
+  }
+}
+
+}  // namespace sv

@@ -240,4 +240,42 @@ __device__ __forceinline__ KI warp_reduce_ki(KI t) {
   return t;
 }
 
+// -log2(u) for u = sv_u01(x): the exponential variate E of the race, in log2
+// units (a common scale factor of all keys, so the argmax is unchanged).  Near
+// u = 1 it comes from w = 1 - u (exact) and -log2(1-w) = (w + w^2/2 + ...)/ln 2,
+// truncated after w^2 (relative error < w^2/3 < 2^-17.5 for w < 2^-8).
+__device__ __forceinline__ float neglog2_u(uint32_t x) {
+  const float u = __uint_as_float(0x3f800000u | (x >> 9)) - 0x1.fffffep-1f;
+  const float w = 1.0f - u;
+  const float series = w * fmaf(w, 0.5f * kLog2e, kLog2e);
+  return (w < 0x1p-8f) ? series : -__log2f(u);
+}
+
+// Philox4x32-10 with the ten round keys precomputed (the key schedule depends
+// only on the seed).
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
+  PhiloxKeys k;
+  uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = a;
+    k.k1[r] = b;
+    a += 0x9E3779B9u;
+    b += 0xBB67AE85u;
+  }
+  return k;
+}
+__device__ __forceinline__ uint4 philox_rk(uint4 c, const PhiloxKeys& k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k.k0[r], lo1, hi0 ^ c.w ^ k.k1[r], lo0);
+  }
+  return c;
+}
+
 }  // namespace sv
