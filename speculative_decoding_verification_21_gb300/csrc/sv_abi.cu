@@ -9,6 +9,7 @@
 
 #include "specverify.h"
 #include "sv_plan.h"
+#include "sv_launch.h"
 
 namespace sv {
 cudaError_t launch_sample(const void* zt, const void* zd, const int32_t* xt, int B, int gamma,
@@ -26,7 +27,19 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
                   uint8_t* out_flags, float* debug_logits, void* workspace,
                   size_t workspace_bytes, cudaStream_t stream);
 size_t lmhead_workspace_bytes(int B, int gamma, int64_t V);
-void set_timing_events(void* const* ev, int n);
+}  // namespace sv
+
+namespace sv {
+static cudaEvent_t g_events[kMaxTimingEvents] = {};
+
+void set_timing_events(void* const* ev, int n) {
+  for (int i = 0; i < kMaxTimingEvents; ++i)
+    g_events[i] = (ev && i < n) ? (cudaEvent_t)ev[i] : nullptr;
+}
+
+void mark(int i, cudaStream_t s) {
+  if (i >= 0 && i < kMaxTimingEvents && g_events[i]) cudaEventRecord(g_events[i], s);
+}
 }  // namespace sv
 
 namespace {

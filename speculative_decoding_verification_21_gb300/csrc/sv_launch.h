@@ -1,0 +1,34 @@
+// sv_launch.h -- host-side launch helpers shared by the entry points: optional
+// timing events between kernels and launches with programmatic dependent launch.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace sv {
+
+constexpr int kMaxTimingEvents = 8;
+
+// Record timing event i on the stream if the caller registered one.
+void mark(int i, cudaStream_t s);
+void set_timing_events(void* const* ev, int n);
+
+// Launch with programmatic stream serialisation: the kernel may start while the
+// previous one on the stream drains, and waits for it with griddepcontrol.wait.
+// Without event markers only: an event recorded between the two would order them.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace sv

@@ -1,19 +1,840 @@
-// sv_lmhead.cu -- fused LM head + verify (tcgen05).  Placeholder until the
-// tensor-core kernel lands: reports SV_ERR_UNSUPPORTED.
+// sv_lmhead.cu -- fused LM heads + sampling verify on the 5th-generation tensor
+// cores (tcgen05, tensor memory, 2-D tensor copies) of sm_103a.
+//
+// The logits are the final projections of the two models' passes, z = h W with
+// bf16 operands and fp32 accumulation ("Fast Inference from Transformers via
+// Speculative Decoding", section "The loop: draft, verify in one pass, keep a
+// prefix": one target pass over the gamma+1 positions gives p_1..p_{gamma+1},
+// the draft gives q_i).  They are consumed tile by tile in the epilogue of the
+// GEMM and never written to HBM.  Four kernels per call:
+//
+//   k_lm<1>      persistent, one CTA per SM.  Vocabulary tiles of 128 entries
+//                are dealt round-robin; for each tile the CTA computes the
+//                target block (B(gamma+1) token rows x 128) and then the draft
+//                block (B gamma rows x 128).  Warp 0 streams h and W tiles with
+//                2-D tensor copies into a 4-stage shared-memory ring, warp 1
+//                issues tcgen05.mma into one of two tensor-memory accumulators,
+//                and warps 2-5 drain the other (tcgen05.ld): per-row online
+//                softmax statistics, z at each draft token, and the top-2
+//                Gumbel-max keys of the bonus row p_gamma.
+//   k_lm_finish  one CTA per batch row: row combine and the decision exactly as
+//                for given logits, the bonus draw when all drafts are accepted,
+//                and otherwise a compact copy of the two hidden rows at the
+//                first rejection.
+//   k_lm<2>      the same GEMM for the compact rows only, target and draft
+//                blocks side by side in tensor memory; the epilogue keeps the
+//                top-2 keys of the residual max(0, p_n - q_n) and of p_n.
+//   k_lm_merge   one CTA per compact row: merge, re-decide near ties in double,
+//                fall back to p_n for an empty residual, emit.
+//
+// Keys are log2-domain Gumbel-max keys, y_v - log2(-log2 u_v) with y = z / T *
+// log2 e: the same argmax as log w_v + g_v of the definition, with no underflow
+// of the weights.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <math_constants.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "specverify.h"
+#include "sv_decide.cuh"
+#include "sv_device.cuh"
+#include "sv_launch.h"
+#include "sv_plan.h"
+#include "sv_tma.cuh"
+#include "sv_umma.cuh"
 
 namespace sv {
 
-size_t lmhead_workspace_bytes(int, int, int64_t) { return 0; }
+namespace {
 
-int lmhead_verify(const void*, const void*, int, const void*, const void*, int, const int32_t*,
-                  int, int, int64_t, float, uint64_t, uint64_t, int32_t*, int32_t*, float*,
-                  float*, uint8_t*, float*, void*, size_t, cudaStream_t) {
-  return SV_ERR_UNSUPPORTED;
+constexpr int kTileM = 128;   // token rows per MMA (tensor-memory lanes)
+constexpr int kKBlock = 64;   // hidden entries per stage: one 128-byte swizzle span
+constexpr int kStages = 4;
+constexpr int kABytes = kTileM * kKBlock * 2;      // one A tile (128 rows x 64), 16 KB
+constexpr int kBBytes = kLmTileN * kKBlock * 2;    // one B tile (64 x 128 vocab), 16 KB
+constexpr int kStageBytes = 2 * kABytes + kBBytes; // up to two A tiles + B
+constexpr int kLmThreads = 192;                    // producer, MMA, 4 epilogue warps
+constexpr int kTmemCols = 512;                     // two accumulators of 256 columns
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr size_t kLmSmem = 1024 + (size_t)kStages * kStageBytes + 256;
+
+constexpr uint32_t kIdesc = umma_idesc_bf16(kTileM, kLmTileN, /*a_mn=*/false, /*b_mn=*/true);
+
+struct LmArgs {
+  const int32_t* xt;
+  int B, gamma, V, nvt;
+  int Mt, Md;          // token rows of the target and draft sides
+  int kbt, kbd;        // hidden blocks of 64
+  int Ht, Hd;
+  float temperature;
+  uint64_t seed, round;
+  float2* part;        // [B*R1][nvt] (max, sum) per row and tile
+  float* zat;          // [B*R1] logit at the row's draft token
+  LmCand* bon;         // [B][nvt][2] bonus-row top-2
+  LmCand* res;         // [B][nvt][4] residual top-2, then p_n top-2, per compact row
+  DrawState* state;    // [B]
+  int* slot_b;         // [B] batch row of each compact row
+  uint32_t* ctl;       // count, pass-1 error, pass-2 error
+  const uint16_t* h_t;
+  const uint16_t* h_d;
+  uint16_t* c_t;       // compact hidden rows [B][Ht]
+  uint16_t* c_d;       // [B][Hd]
+  float* dbg;          // [B*R1][V] or null
+  int32_t* out_tokens;
+  int32_t* out_counts;
+  float* out_p;
+  float* out_q;
+  uint8_t* out_flags;
+};
+
+__device__ __forceinline__ bool cand_better(const LmCand& a, const LmCand& b) {
+  if (a.idx < 0) return false;
+  if (b.idx < 0) return true;
+  return a.key > b.key || (a.key == b.key && a.idx < b.idx);
+}
+
+struct Cand2 {
+  LmCand a, b;
+};
+
+__device__ __forceinline__ LmCand cand_empty() { return LmCand{-kInf, -1, 0.0f, 0.0f}; }
+
+__device__ __forceinline__ void cand_insert(Cand2& t, const LmCand& c) {
+  if (cand_better(c, t.a)) {
+    t.b = t.a;
+    t.a = c;
+  } else if (cand_better(c, t.b)) {
+    t.b = c;
+  }
+}
+
+__device__ __forceinline__ LmCand cand_shfl(const LmCand& c, int o) {
+  LmCand r;
+  r.key = __shfl_xor_sync(0xffffffffu, c.key, o);
+  r.idx = __shfl_xor_sync(0xffffffffu, c.idx, o);
+  r.zt = __shfl_xor_sync(0xffffffffu, c.zt, o);
+  r.zd = __shfl_xor_sync(0xffffffffu, c.zd, o);
+  return r;
+}
+
+__device__ __forceinline__ Cand2 warp_cand2(Cand2 t) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const LmCand a = cand_shfl(t.a, o), b = cand_shfl(t.b, o);
+    cand_insert(t, a);
+    cand_insert(t, b);
+  }
+  return t;
+}
+
+// Top-2 over the CTA (valid in thread 0).
+__device__ Cand2 block_cand2(Cand2 t, Cand2* sm /* [32] */) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
+  t = warp_cand2(t);
+  __syncthreads();
+  if (lane == 0) sm[warp] = t;
+  __syncthreads();
+  Cand2 r{cand_empty(), cand_empty()};
+  if (warp == 0) {
+    if (lane < nw) r = sm[lane];
+    r = warp_cand2(r);
+  }
+  return r;
+}
+
+// Bounded wait that also gives up when another role of the CTA has aborted.
+__device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+
+// -log2(-log2 u) noise of entry v at Philox position pos (tag 1), and its double
+// twin -ln(-ln u) for the re-decision.
+__device__ __forceinline__ double gumbel_f64(int64_t v, int pos, int b, uint64_t seed,
+                                             uint64_t round) {
+  const uint4 rnd = philox4x32_10(sv_counter((uint32_t)(v >> 2), 1u, (uint32_t)pos, (uint32_t)b, round),
+                                  (uint32_t)seed, (uint32_t)(seed >> 32));
+  const uint32_t lanes[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+  return -log(sv_neglog_u_f64(lanes[v & 3]));
+}
+
+// The best of a top-2, re-decided in double when the two fp32 keys are within
+// 2^-10 (log2 units).  `key_f64` gives the definition-level key of a candidate.
+template <class F>
+__device__ int redecide(const Cand2& t, F key_f64) {
+  if (t.a.idx < 0) return -1;
+  if (t.b.idx < 0 || !(t.a.key - t.b.key <= 0x1p-10f)) return t.a.idx;
+  const double ka = key_f64(t.a), kb = key_f64(t.b);
+  if (kb > ka || (kb == ka && t.b.idx < t.a.idx)) return t.b.idx;
+  return t.a.idx;
+}
+
+// ---------------------------------------------------------------------------
+// The persistent GEMM + epilogue kernel.  PASS 1: all token rows; PASS 2: the
+// compact rows.  Maps: mA0/mB0 target h and W, mA1/mB1 draft h and W.
+// ---------------------------------------------------------------------------
+struct Seg {
+  const CUtensorMap* amap;
+  const CUtensorMap* bmap;
+  int kblocks, mtiles, col;
+};
+
+template <int PASS>
+struct Jobs;
+
+// Pass 1: per vocabulary tile, job 0 = target block, job 1 = draft block.
+template <>
+struct Jobs<1> {
+  static constexpr int kPerTile = 2;
+  __device__ static int nseg(int) { return 1; }
+  __device__ static Seg seg(int job, int, const CUtensorMap* a0, const CUtensorMap* b0,
+                            const CUtensorMap* a1, const CUtensorMap* b1, const LmArgs& a) {
+    if (job == 0) return Seg{a0, b0, a.kbt, (a.Mt + kTileM - 1) / kTileM, 0};
+    return Seg{a1, b1, a.kbd, (a.Md + kTileM - 1) / kTileM, 0};
+  }
+};
+
+// Pass 2: one job per tile, target block at column 0 and draft block at 128.
+template <>
+struct Jobs<2> {
+  static constexpr int kPerTile = 1;
+  __device__ static int nseg(int) { return 2; }
+  __device__ static Seg seg(int, int s, const CUtensorMap* a0, const CUtensorMap* b0,
+                            const CUtensorMap* a1, const CUtensorMap* b1, const LmArgs& a) {
+    if (s == 0) return Seg{a0, b0, a.kbt, 1, 0};
+    return Seg{a1, b1, a.kbd, 1, kLmTileN};
+  }
+};
+
+// Online (max, sum) update of one row with 32 logits (invalid ones -inf).
+__device__ __forceinline__ void fold32(const float* f, float c, float& mc, float& s) {
+  float cm = f[0];
+#pragma unroll
+  for (int e = 1; e < 32; ++e) cm = fmaxf(cm, f[e]);
+  const float nm = fmaxf(mc, cm * c);
+  if (!(nm > -kInf)) return;
+  float s0 = (mc == -kInf) ? 0.0f : s * ex2(mc - nm), s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    s0 += ex2(fmaf(f[e], c, -nm));
+    s1 += ex2(fmaf(f[e + 1], c, -nm));
+    s2 += ex2(fmaf(f[e + 2], c, -nm));
+    s3 += ex2(fmaf(f[e + 3], c, -nm));
+  }
+  mc = nm;
+  s = (s0 + s1) + (s2 + s3);
+}
+
+// Pass-1 epilogue of one job: side 0 target rows, side 1 draft rows.
+__device__ __forceinline__ void epilogue_pass1(const LmArgs& a, int side, int t, uint32_t tacc,
+                                               int quad, const PhiloxKeys& pk) {
+  const int lane = threadIdx.x & 31;
+  const int gamma = a.gamma, R1 = 2 * gamma + 1, V = a.V;
+  const int M = side ? a.Md : a.Mt;
+  const int mtiles = (M + kTileM - 1) / kTileM;
+  const int v0 = t * kLmTileN;
+  const float c = log2_scale(inv_temperature(a.temperature));
+  for (int m = 0; m < mtiles; ++m) {
+    const int rb = m * kTileM + 32 * quad;
+    if (rb >= M) continue;  // warp-uniform
+    const int r = rb + lane;
+    const bool rv = r < M;
+    int b = 0, k = 0, x = -1;
+    bool bonus = false;
+    if (rv) {
+      if (side == 0) {
+        b = r / (gamma + 1);
+        const int i = r - b * (gamma + 1);
+        k = i;
+        if (i < gamma) x = __ldg(a.xt + (int64_t)b * gamma + i);
+        bonus = (i == gamma);
+      } else {
+        b = r / gamma;
+        const int i = r - b * gamma;
+        k = gamma + 1 + i;
+        x = __ldg(a.xt + r);
+      }
+    }
+    const int64_t grow = (int64_t)b * R1 + k;
+    float mc = -kInf, s = 0.0f;
+    Cand2 top{cand_empty(), cand_empty()};
+    for (int ch = 0; ch < kLmTileN / 32; ++ch) {
+      const int vb = v0 + ch * 32;
+      if (vb >= V) break;  // warp-uniform
+      float f[32];
+      tmem_ld32(tacc + ((uint32_t)(32 * quad) << 16) + (uint32_t)(m * kTileM + ch * 32), f);
+      if (!rv) continue;
+      const int nvalid = min(32, V - vb);
+      if (nvalid < 32) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) f[e] = (e < nvalid) ? f[e] : -kInf;
+      }
+      if (a.dbg) {
+        float4* d = reinterpret_cast<float4*>(a.dbg + grow * V + vb);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (4 * j < nvalid) d[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+      }
+      fold32(f, c, mc, s);
+      if ((unsigned)(x - vb) < 32u) {
+        float g = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) g = (e == x - vb) ? f[e] : g;
+        a.zat[grow] = g;
+      }
+      if (bonus) {
+#pragma unroll
+        for (int g4 = 0; g4 < 8; ++g4) {
+          const int v = vb + 4 * g4;
+          if (v >= V) break;
+          const uint4 rnd = philox_rk(sv_counter((uint32_t)(v >> 2), 1u, (uint32_t)gamma,
+                                                 (uint32_t)b, a.round),
+                                      pk);
+          const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float z = f[4 * g4 + e];
+            const float key = fmaf(z, c, -__log2f(neglog2_u(rr[e])));
+            cand_insert(top, LmCand{key, v + e, z, 0.0f});
+          }
+        }
+      }
+    }
+    if (rv) {
+      a.part[grow * a.nvt + t] = make_float2(mc, s);
+      if (bonus) {
+        LmCand* o = a.bon + ((int64_t)b * a.nvt + t) * 2;
+        o[0] = top.a;
+        o[1] = top.b;
+      }
+    }
+  }
+}
+
+// Pass-2 epilogue of one job (compact rows; target at column 0, draft at 128).
+__device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t tacc, int quad,
+                                               int rows, const PhiloxKeys& pk) {
+  const int lane = threadIdx.x & 31;
+  const int V = a.V;
+  const int rb = 32 * quad;
+  if (rb >= rows) return;  // warp-uniform
+  const int r = rb + lane;
+  const bool rv = r < rows;
+  int b = 0;
+  DrawState st{};
+  if (rv) {
+    b = a.slot_b[r];
+    st = a.state[b];
+  }
+  const bool resid = rv && st.mode == kDrawResidual;
+  const int v0 = t * kLmTileN;
+  Cand2 tr{cand_empty(), cand_empty()}, tp{cand_empty(), cand_empty()};
+  for (int ch = 0; ch < kLmTileN / 32; ++ch) {
+    const int vb = v0 + ch * 32;
+    if (vb >= V) break;
+    float ft[32], fd[32];
+    const uint32_t lanebase = tacc + ((uint32_t)(32 * quad) << 16);
+    tmem_ld32(lanebase + (uint32_t)(ch * 32), ft);
+    tmem_ld32(lanebase + (uint32_t)(kLmTileN + ch * 32), fd);
+    if (!rv) continue;
+#pragma unroll
+    for (int g4 = 0; g4 < 8; ++g4) {
+      const int v = vb + 4 * g4;
+      if (v >= V) break;
+      const uint4 rnd =
+          philox_rk(sv_counter((uint32_t)(v >> 2), 1u, (uint32_t)st.pos, (uint32_t)b, a.round), pk);
+      const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float zt = ft[4 * g4 + e], zd = fd[4 * g4 + e];
+        const float lE = __log2f(neglog2_u(rr[e]));
+        const float kp = fmaf(zt, st.c, -st.mct) - lE;
+        if (zt > -kInf) cand_insert(tp, LmCand{kp, v + e, zt, zd});
+        if (resid) {
+          // x = log2(q/p); p > q iff x < 0; weight p - q = p (1 - 2^x)
+          const float xx = fmaf(zd - zt, st.c, st.K);
+          if (xx < 0.0f) {
+            const float y = xx * kLn2;
+            const float ser = -y * fmaf(y, fmaf(y, fmaf(y, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
+            const float om = (xx > -0.125f) ? ser : 1.0f - ex2(xx);
+            cand_insert(tr, LmCand{kp + __log2f(om), v + e, zt, zd});
+          }
+        }
+      }
+    }
+  }
+  if (rv) {
+    LmCand* o = a.res + ((int64_t)r * a.nvt + t) * 4;
+    o[0] = tr.a;
+    o[1] = tr.b;
+    o[2] = tp.a;
+    o[3] = tp.b;
+  }
+}
+
+template <int PASS>
+__global__ void __launch_bounds__(kLmThreads, 1)
+    k_lm(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mB0,
+         const __grid_constant__ CUtensorMap mA1, const __grid_constant__ CUtensorMap mB1,
+         LmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  int rows2 = 0;
+  if (PASS == 2) {
+    pdl_wait();  // the compact rows and their draw states
+    rows2 = (int)*reinterpret_cast<volatile uint32_t*>(a.ctl);
+    if (rows2 <= 0) return;  // nothing rejected this round (uniform over the grid)
+  }
+  pdl_launch_dependents();
+  const uint32_t base_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* accf = empty + kStages;  // [2]
+  uint64_t* acce = accf + 2;         // [2]
+  uint64_t* fin = acce + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(fin + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(accf + j, 1);
+      mbar_init(acce + j, 4);
+    }
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const int nvt = a.nvt;
+  const int G = (int)gridDim.x;
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < nvt; t += G) {
+        const int v0 = t * kLmTileN;
+        for (int job = 0; ok && job < Jobs<PASS>::kPerTile; ++job) {
+          for (int sg = 0; ok && sg < Jobs<PASS>::nseg(job); ++sg) {
+            const Seg q = Jobs<PASS>::seg(job, sg, &mA0, &mB0, &mA1, &mB1, a);
+            for (int kb = 0; kb < q.kblocks; ++kb, ++it) {
+              const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+              if (!lm_wait(empty + s, ph ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+              }
+              uint8_t* st = smem + s * kStageBytes;
+              mbar_arrive_expect_tx(full + s, (uint32_t)(q.mtiles * kABytes + kBBytes));
+              for (int m = 0; m < q.mtiles; ++m)
+                tma_load_2d(st + m * kABytes, q.amap, kb * kKBlock, m * kTileM, full + s);
+              tma_load_2d(st + 2 * kABytes, q.bmap, v0, kb * kKBlock, full + s);
+              tma_load_2d(st + 2 * kABytes + kBBytes / 2, q.bmap, v0 + kLmTileN / 2, kb * kKBlock,
+                          full + s);
+            }
+          }
+        }
+      }
+      // every issued copy has landed before the CTA may exit
+      for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
+        if (it <= s) continue;
+        const uint32_t last = (it - 1u) - ((it - 1u - s) % kStages);
+        mbar_wait_bounded(full + s, (last / kStages) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      int jobi = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < nvt; t += G) {
+        for (int job = 0; ok && job < Jobs<PASS>::kPerTile; ++job, ++jobi) {
+          const int buf = jobi & 1;
+          const uint32_t ap = (uint32_t)(jobi >> 1) & 1u;
+          if (!lm_wait(acce + buf, ap ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int sg = 0; ok && sg < Jobs<PASS>::nseg(job); ++sg) {
+            const Seg q = Jobs<PASS>::seg(job, sg, &mA0, &mB0, &mA1, &mB1, a);
+            const uint32_t dcol = tbase + (uint32_t)(buf * 256 + q.col);
+            for (int kb = 0; kb < q.kblocks; ++kb, ++it) {
+              const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+              if (!lm_wait(full + s, ph, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t sa = smem_u32(smem + s * kStageBytes);
+              const uint64_t bdesc = umma_smem_desc(sa + 2 * kABytes, kBBytes / 2, 1024);
+              for (int m = 0; m < q.mtiles; ++m) {
+                const uint64_t adesc = umma_smem_desc(sa + m * kABytes, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kKBlock / 16; ++kk)
+                  umma_bf16(dcol + (uint32_t)(m * kTileM), adesc + (uint64_t)(2 * kk),
+                            bdesc + (uint64_t)(128 * kk), kIdesc, (kb | kk) != 0);
+              }
+              umma_commit(empty + s);
+            }
+          }
+          if (ok) umma_commit(accf + buf);
+        }
+      }
+      // all MMAs of this CTA complete before tensor memory is released
+      umma_commit(fin);
+      mbar_wait_bounded(fin, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 2..5, tensor-memory lane quadrant warp%4) ----------------
+    const int quad = warp & 3;
+    const PhiloxKeys pk = philox_keys(a.seed);
+    int jobi = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < nvt; t += G) {
+      for (int job = 0; job < Jobs<PASS>::kPerTile; ++job, ++jobi) {
+        const int buf = jobi & 1;
+        const uint32_t ap = (uint32_t)(jobi >> 1) & 1u;
+        if (!lm_wait(accf + buf, ap, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tacc = tbase + (uint32_t)(buf * 256);
+        if (PASS == 1)
+          epilogue_pass1(a, job, t, tacc, quad, pk);
+        else
+          epilogue_pass2(a, t, tacc, quad, rows2, pk);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce + buf);
+      }
+    }
+  }
+
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(a.ctl + (PASS == 1 ? 1 : 2), 1u);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// k_lm_finish: one CTA per batch row.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
+  const int b = blockIdx.x;
+  const int gamma = a.gamma, R1 = 2 * gamma + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = (int)(blockDim.x >> 5);
+  __shared__ RowStat srs[2 * 32 + 1];
+  __shared__ DraftAt sda[32];
+  __shared__ Cand2 scand[32];
+  __shared__ int s_slot;
+  pdl_wait();  // partials of the GEMM pass
+  pdl_launch_dependents();
+  const bool err = *reinterpret_cast<volatile uint32_t*>(a.ctl + 1) != 0u;
+  if (warp < nw - 1) {
+    for (int k = warp; k < R1; k += nw - 1) {
+      RowStat rs = combine_row(a.part + ((int64_t)b * R1 + k) * a.nvt, a.nvt, nullptr);
+      if (err) {
+        rs.bits |= kRowTimeout | kRowNaN;
+        rs.s = CUDART_NAN;
+      }
+      if (lane == 0) srs[k] = rs;
+    }
+  } else {
+    for (int i = lane; i < gamma; i += 32) {
+      const int32_t x = __ldg(a.xt + (int64_t)b * gamma + i);
+      const bool ok = x >= 0 && x < a.V;
+      const float* za = a.zat + (int64_t)b * R1;
+      sda[i] = DraftAt{x, ok ? __ldcg(za + i) : 0.0f, ok ? __ldcg(za + gamma + 1 + i) : 0.0f};
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    SweepCtx sx{};
+    sx.xt = a.xt;
+    sx.B = a.B;
+    sx.gamma = gamma;
+    sx.V = a.V;
+    sx.temperature = a.temperature;
+    sx.row_T = nullptr;
+    sx.seed = a.seed;
+    sx.round = a.round;
+    sx.state = a.state;
+    sx.out_tokens = a.out_tokens;
+    sx.out_counts = a.out_counts;
+    sx.out_p = a.out_p;
+    sx.out_q = a.out_q;
+    sx.out_flags = a.out_flags;
+    decide_batch_row<SV_F32>(sx, b, srs, sda);
+  }
+  __syncthreads();
+  const DrawState st = a.state[b];
+  if (st.mode == kDrawDone) return;
+  if (st.mode == kDrawSampleRow && st.pos == gamma) {
+    // bonus token: merge the per-tile top-2 of row p_gamma
+    Cand2 t{cand_empty(), cand_empty()};
+    const LmCand* bp = a.bon + (int64_t)b * a.nvt * 2;
+    for (int j = threadIdx.x; j < a.nvt; j += blockDim.x) {
+      cand_insert(t, bp[2 * j]);
+      cand_insert(t, bp[2 * j + 1]);
+    }
+    t = block_cand2(t, scand);
+    if (threadIdx.x == 0) {
+      const double invT = (double)st.invT;
+      int tk = redecide(t, [&](const LmCand& c) {
+        return (double)c.zt * invT + gumbel_f64(c.idx, gamma, b, a.seed, a.round);
+      });
+      int fl = st.flags;
+      if (tk < 0 || tk >= a.V) {
+        tk = 0;
+        fl |= SV_FLAG_ZERO_MASS;
+      }
+      a.out_tokens[(int64_t)b * (gamma + 1) + gamma] = tk;
+      if (a.out_flags) a.out_flags[b] = (uint8_t)fl;
+    }
+    return;
+  }
+  // a draw over a full row at position n: queue the two hidden rows for pass 2
+  if (threadIdx.x == 0) {
+    const int slot = (int)atomicAdd(a.ctl, 1u);
+    a.slot_b[slot] = b;
+    s_slot = slot;
+  }
+  __syncthreads();
+  const int slot = s_slot;
+  const int n = st.pos;
+  const uint4* srct = reinterpret_cast<const uint4*>(a.h_t + ((int64_t)b * (gamma + 1) + n) * a.Ht);
+  const uint4* srcd = reinterpret_cast<const uint4*>(a.h_d + ((int64_t)b * gamma + n) * a.Hd);
+  uint4* dt = reinterpret_cast<uint4*>(a.c_t + (int64_t)slot * a.Ht);
+  uint4* dd = reinterpret_cast<uint4*>(a.c_d + (int64_t)slot * a.Hd);
+  for (int j = threadIdx.x; j < a.Ht / 8; j += blockDim.x) dt[j] = __ldg(srct + j);
+  for (int j = threadIdx.x; j < a.Hd / 8; j += blockDim.x) dd[j] = __ldg(srcd + j);
+}
+
+// ---------------------------------------------------------------------------
+// k_lm_merge: one CTA per compact row.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_lm_merge(LmArgs a) {
+  const int slot = blockIdx.x;
+  __shared__ Cand2 scand[32];
+  pdl_wait();
+  const int rows = (int)*reinterpret_cast<volatile uint32_t*>(a.ctl);
+  if (slot >= rows) return;
+  const bool err = *reinterpret_cast<volatile uint32_t*>(a.ctl + 2) != 0u;
+  const int b = a.slot_b[slot];
+  const DrawState st = a.state[b];
+  const bool resid = st.mode == kDrawResidual;
+  const LmCand* rp = a.res + (int64_t)slot * a.nvt * 4;
+  Cand2 tr{cand_empty(), cand_empty()}, tp{cand_empty(), cand_empty()};
+  for (int j = threadIdx.x; j < a.nvt; j += blockDim.x) {
+    cand_insert(tr, rp[4 * j]);
+    cand_insert(tr, rp[4 * j + 1]);
+    cand_insert(tp, rp[4 * j + 2]);
+    cand_insert(tp, rp[4 * j + 3]);
+  }
+  tr = block_cand2(tr, scand);
+  __syncthreads();
+  tp = block_cand2(tp, scand);
+  if (threadIdx.x != 0) return;
+  int fl = st.flags;
+  int tk = -1;
+  const double invT = (double)st.invT, c = (double)st.c;
+  auto key_p = [&](const LmCand& q) {
+    return (double)q.zt * invT + gumbel_f64(q.idx, st.pos, b, a.seed, a.round);
+  };
+  if (err) {
+    fl |= SV_FLAG_TIMEOUT | SV_FLAG_NONFINITE;
+  } else if (resid && tr.a.idx >= 0) {
+    tk = redecide(tr, [&](const LmCand& q) {
+      const double P = exp2((double)q.zt * c - (double)st.mct) / st.st;
+      const double Q = exp2((double)q.zd * c - (double)st.mcd) / st.sd;
+      const double r = P - Q;
+      return (r > 0.0) ? log(r) + gumbel_f64(q.idx, st.pos, b, a.seed, a.round) : -CUDART_INF;
+    });
+  } else {
+    if (resid) fl |= SV_FLAG_RESIDUAL_FALLBACK;
+    tk = redecide(tp, key_p);
+  }
+  if (tk < 0 || tk >= a.V) {
+    tk = 0;
+    if (!err) fl |= SV_FLAG_ZERO_MASS;
+  }
+  a.out_tokens[(int64_t)b * (a.gamma + 1) + st.pos] = tk;
+  if (a.out_flags) a.out_flags[b] = (uint8_t)fl;
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct LmDevice {
+  int sms = 0;
+  bool ready = false;
+};
+std::mutex g_lm_mu;
+LmDevice g_lm_dev[64];
+EncodeTiled g_encode = nullptr;
+
+cudaError_t lm_device(LmDevice** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_lm_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    g_encode = reinterpret_cast<EncodeTiled>(fn);
+  }
+  LmDevice& d = g_lm_dev[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_lm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLmSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_lm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLmSmem);
+    if (e != cudaSuccess) return e;
+    d.ready = true;
+  }
+  *out = &d;
+  return cudaSuccess;
+}
+
+// Row-major bf16 matrix [rows][cols] as a 2-D tensor map with a box of
+// box_cols x box_rows and 128-byte swizzle (out-of-range elements read as 0).
+bool encode_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_cols, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned_to(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+}  // namespace
+
+size_t lmhead_workspace_bytes(int B, int gamma, int64_t V) {
+  return make_lm_plan(B, gamma, V).total;
+}
+
+int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void* h_draft,
+                  const void* W_draft, int Hd, const int32_t* draft_tokens, int B, int gamma,
+                  int64_t V, float temperature, uint64_t seed, uint64_t round,
+                  int32_t* out_tokens, int32_t* out_counts, float* out_p, float* out_q,
+                  uint8_t* out_flags, float* debug_logits, void* workspace,
+                  size_t workspace_bytes, cudaStream_t stream) {
+  if (!h_target || !W_target || !h_draft || !W_draft || !draft_tokens || !out_tokens ||
+      !out_counts)
+    return SV_ERR_ARG;
+  if (Ht < 64 || Hd < 64 || Ht % 64 || Hd % 64 || Ht > kLmMaxHidden || Hd > kLmMaxHidden ||
+      (int64_t)B * (gamma + 1) > kLmMaxRows || V % 8 != 0 || V > ((int64_t)1 << 31) - 256)
+    return SV_ERR_UNSUPPORTED;
+  if (!aligned_to(h_target, 16) || !aligned_to(W_target, 16) || !aligned_to(h_draft, 16) ||
+      !aligned_to(W_draft, 16) || !aligned_to(draft_tokens, 4) || !aligned_to(out_tokens, 4) ||
+      !aligned_to(out_counts, 4) || (out_p && !aligned_to(out_p, 4)) ||
+      (out_q && !aligned_to(out_q, 4)) || (debug_logits && !aligned_to(debug_logits, 16)))
+    return SV_ERR_ALIGN;
+  const LmPlan pl = make_lm_plan(B, gamma, V);
+  if (!workspace || workspace_bytes < pl.total) return SV_ERR_WORKSPACE;
+  if (!aligned_to(workspace, kAlign)) return SV_ERR_ALIGN;
+  LmDevice* dev = nullptr;
+  if (lm_device(&dev) != cudaSuccess) return SV_ERR_CUDA;
+
+  char* ws = reinterpret_cast<char*>(workspace);
+  LmArgs a{};
+  a.xt = draft_tokens;
+  a.B = B;
+  a.gamma = gamma;
+  a.V = (int)V;
+  a.nvt = pl.nvt;
+  a.Mt = B * (gamma + 1);
+  a.Md = B * gamma;
+  a.kbt = Ht / kKBlock;
+  a.kbd = Hd / kKBlock;
+  a.Ht = Ht;
+  a.Hd = Hd;
+  a.temperature = temperature;
+  a.seed = seed;
+  a.round = round;
+  a.part = reinterpret_cast<float2*>(ws + pl.off_part);
+  a.zat = reinterpret_cast<float*>(ws + pl.off_zat);
+  a.bon = reinterpret_cast<LmCand*>(ws + pl.off_bon);
+  a.res = reinterpret_cast<LmCand*>(ws + pl.off_res);
+  a.state = reinterpret_cast<DrawState*>(ws + pl.off_state);
+  a.slot_b = reinterpret_cast<int*>(ws + pl.off_slot);
+  a.ctl = reinterpret_cast<uint32_t*>(ws + pl.off_ctl);
+  a.h_t = reinterpret_cast<const uint16_t*>(h_target);
+  a.h_d = reinterpret_cast<const uint16_t*>(h_draft);
+  a.c_t = reinterpret_cast<uint16_t*>(ws + pl.off_ct);
+  a.c_d = reinterpret_cast<uint16_t*>(ws + pl.off_cd);
+  a.dbg = debug_logits;
+  a.out_tokens = out_tokens;
+  a.out_counts = out_counts;
+  a.out_p = out_p;
+  a.out_q = out_q;
+  a.out_flags = out_flags;
+
+  CUtensorMap hT, WT, hD, WD, cT, cD;
+  if (!encode_bf16(&hT, h_target, (uint64_t)a.Mt, (uint64_t)Ht, kKBlock, kTileM) ||
+      !encode_bf16(&hD, h_draft, (uint64_t)a.Md, (uint64_t)Hd, kKBlock, kTileM) ||
+      !encode_bf16(&WT, W_target, (uint64_t)Ht, (uint64_t)V, kLmTileN / 2, kKBlock) ||
+      !encode_bf16(&WD, W_draft, (uint64_t)Hd, (uint64_t)V, kLmTileN / 2, kKBlock) ||
+      !encode_bf16(&cT, a.c_t, (uint64_t)B, (uint64_t)Ht, kKBlock, kTileM) ||
+      !encode_bf16(&cD, a.c_d, (uint64_t)B, (uint64_t)Hd, kKBlock, kTileM))
+    return SV_ERR_CUDA;
+
+  cudaError_t e = cudaMemsetAsync(a.ctl, 0, 4 * sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  const unsigned grid = (unsigned)(pl.nvt < dev->sms ? pl.nvt : dev->sms);
+  mark(0, stream);
+  k_lm<1><<<grid, kLmThreads, kLmSmem, stream>>>(hT, WT, hD, WD, a);
+  mark(1, stream);
+  const int fw = ((2 * gamma + 1) < 31 ? (2 * gamma + 1) : 31) + 1;
+  e = launch_pdl(k_lm_finish, dim3((unsigned)B), dim3(32 * fw), 0, stream, a);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  mark(2, stream);
+  e = launch_pdl(k_lm<2>, dim3(grid), dim3(kLmThreads), kLmSmem, stream, cT, WT, cD, WD, a);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  mark(3, stream);
+  e = launch_pdl(k_lm_merge, dim3((unsigned)B), dim3(256), 0, stream, a);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  mark(4, stream);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 }  // namespace sv

@@ -110,4 +110,47 @@ inline GreedyPlan make_greedy_plan(int B, int gamma, int64_t V) {
   return p;
 }
 
+
+// Fused LM head: vocabulary tile width, the largest hidden size whose compact
+// row copies the workspace holds, and the largest token-row count per side.
+constexpr int kLmTileN = 128;
+constexpr int kLmMaxHidden = 16384;
+constexpr int kLmMaxRows = 256;
+
+// One candidate of a Gumbel-max: key (log2 units), vocabulary index, and the
+// target / draft logits there (for the double-precision re-decision).
+struct LmCand {
+  float key;
+  int idx;
+  float zt, zd;
+};
+
+struct LmPlan {
+  int R1 = 0;   // 2*gamma+1 logit rows per batch row
+  int nvt = 0;  // vocabulary tiles
+  // ctl: [0] compact-row count, [1] pass-1 error, [2] pass-2 error (zeroed per call)
+  size_t off_ctl = 0, off_part = 0, off_zat = 0, off_state = 0, off_slot = 0, off_bon = 0,
+         off_res = 0, off_ct = 0, off_cd = 0, total = 0;
+};
+
+inline LmPlan make_lm_plan(int B, int gamma, int64_t V) {
+  LmPlan p;
+  if (B <= 0) return p;
+  p.R1 = 2 * gamma + 1;
+  p.nvt = (int)ceil_div(V, kLmTileN);
+  const size_t rows = (size_t)B * p.R1;
+  size_t o = 0;
+  p.off_ctl = o;    o = align_up(o + 4 * sizeof(uint32_t));
+  p.off_part = o;   o = align_up(o + 8 * rows * p.nvt);
+  p.off_zat = o;    o = align_up(o + sizeof(float) * rows);
+  p.off_state = o;  o = align_up(o + sizeof(DrawState) * (size_t)B);
+  p.off_slot = o;   o = align_up(o + sizeof(int) * (size_t)B);
+  p.off_bon = o;    o = align_up(o + 2 * sizeof(LmCand) * (size_t)B * p.nvt);
+  p.off_res = o;    o = align_up(o + 4 * sizeof(LmCand) * (size_t)B * p.nvt);
+  p.off_ct = o;     o = align_up(o + 2 * (size_t)B * kLmMaxHidden);
+  p.off_cd = o;     o = align_up(o + 2 * (size_t)B * kLmMaxHidden);
+  p.total = o;
+  return p;
+}
+
 }  // namespace sv

@@ -35,6 +35,7 @@
 #include "sv_plan.h"
 #include "sv_tma.cuh"
 #include "sv_decide.cuh"
+#include "sv_launch.h"
 
 namespace sv {
 
@@ -750,16 +751,6 @@ k_alpha(const void* __restrict__ zt, const void* __restrict__ zd, int gamma, int
 // --------------------------------------------------------------------------
 // Host side.
 // --------------------------------------------------------------------------
-static cudaEvent_t g_events[4] = {nullptr, nullptr, nullptr, nullptr};
-
-void set_timing_events(void* const* ev, int n) {
-  for (int i = 0; i < 4; ++i) g_events[i] = (ev && i < n) ? (cudaEvent_t)ev[i] : nullptr;
-}
-
-static inline void mark(int i, cudaStream_t s) {
-  if (g_events[i]) cudaEventRecord(g_events[i], s);
-}
-
 // Per-device launch facts for the persistent sweep, looked up once per device.
 struct DeviceInfo {
   int sms = 0;
@@ -796,25 +787,6 @@ static cudaError_t device_info(DeviceInfo** out) {
   }
   *out = &d;
   return cudaSuccess;
-}
-
-// Launch with programmatic stream serialisation: the kernel may start while the
-// previous one on the stream drains, and waits for it with griddepcontrol.wait.
-// Without event markers only: an event recorded between the two would order them.
-template <class... KArgs, class... Args>
-static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
-                              Args... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <int DT>
@@ -857,12 +829,12 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   }
   mark(1, stream);
   const int fw = (R1 < 31 ? R1 : 31) + 1;  // one warp per row, one prefetching
-  cudaError_t e = launch_pdl(k_finish<DT>, dim3((unsigned)B), dim3(32 * fw), stream, sx, cnt);
+  cudaError_t e = launch_pdl(k_finish<DT>, dim3((unsigned)B), dim3(32 * fw), 0, stream, sx, cnt);
   if (e != cudaSuccess) return e;
   mark(2, stream);
   DrawArgs da{zt, zd, B, gamma, V, seed, round, state, draw_cnt, cnt + 2 * B, part3, pl.nsplit3,
               out_tokens, out_flags};
-  e = launch_pdl(k_draw<DT>, dim3((unsigned)((int64_t)pl.nsplit3 * B)), dim3(kThreads), stream,
+  e = launch_pdl(k_draw<DT>, dim3((unsigned)((int64_t)pl.nsplit3 * B)), dim3(kThreads), 0, stream,
                  da);
   if (e != cudaSuccess) return e;
   mark(3, stream);

@@ -102,3 +102,37 @@ def test_binding_refuses_cpu_tensors():
     xt = torch.zeros(1, 1, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA"):
         sv.spec_verify(zt, zd, xt)
+
+
+def _lm(L, ht=FAKE, Wt=FAKE, Ht=128, hd=FAKE, Wd=FAKE, Hd=128, xt=FAKE, B=2, g=2, V=1024,
+        T=1.0, tok=FAKE, cnt=FAKE, dbg=None, ws=FAKE, wsb=1 << 26):
+    return L.spec_lmhead_verify(ht, Wt, Ht, hd, Wd, Hd, xt, B, g, V, T, 0, 0, tok, cnt, None,
+                                None, None, dbg, ws, wsb, None)
+
+
+def test_lmhead_argument_errors():
+    L = sv.load()
+    assert _lm(L, g=0) == -1
+    assert _lm(L, T=0.0) == -1
+    assert _lm(L, ht=None) == -1
+    assert _lm(L, Wd=None) == -1
+    assert _lm(L, Ht=100) == -6            # hidden sizes must be multiples of 64
+    assert _lm(L, Hd=32) == -6
+    assert _lm(L, Ht=16384 + 64) == -6     # beyond the compact-row copies
+    assert _lm(L, B=52, g=4) == -6         # B*(gamma+1) = 260 > 256 token rows
+    assert _lm(L, V=1001) == -6            # W rows must be 16-byte multiples
+    assert _lm(L, Wt=FAKE_MIS) == -3
+    assert _lm(L, hd=FAKE_MIS) == -3
+    assert _lm(L, dbg=FAKE_MIS) == -3
+    assert _lm(L, wsb=1024) == -4
+    assert _lm(L, ws=None) == -4
+    assert _lm(L, ws=ctypes.c_void_p(0x10010)) == -3
+    assert _lm(L, B=0) == 0
+
+
+def test_lmhead_workspace_size():
+    need = sv.workspace_bytes(32, 4, 128256, 2)
+    # compact copies of up to B hidden rows per side at the largest hidden size
+    assert need >= 2 * 32 * 16384 * 2
+    assert need % 256 == 0
+    assert sv.workspace_bytes(64, 4, 128256, 2) > need
