@@ -51,14 +51,15 @@ namespace {
 
 constexpr int kTileM = 128;   // token rows per MMA (tensor-memory lanes)
 constexpr int kKBlock = 64;   // hidden entries per stage: one 128-byte swizzle span
-constexpr int kStages = 4;
-constexpr int kABytes = kTileM * kKBlock * 2;      // one A tile (128 rows x 64), 16 KB
-constexpr int kBBytes = kLmTileN * kKBlock * 2;    // one B tile (64 x 128 vocab), 16 KB
-constexpr int kStageBytes = 2 * kABytes + kBBytes; // up to two A tiles + B
-constexpr int kLmThreads = 192;                    // producer, MMA, 4 epilogue warps
-constexpr int kTmemCols = 512;                     // two accumulators of 256 columns
+constexpr int kWBytes = kLmTileN * kKBlock * 2;  // one W tile (64 hidden x 128 vocab), 16 KB
+constexpr int kEpiWarps = 8;     // two per tensor-memory lane quadrant, each half the columns
+constexpr int kLmThreads = 32 * (3 + kEpiWarps);  // W producer, MMA issuer, h producer, epilogue
+constexpr int kTmemCols = 512;   // two accumulators of 256 columns
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr size_t kLmSmem = 1024 + (size_t)kStages * kStageBytes + 256;
+constexpr int kMaxWStages = 12;
+constexpr int kMaxAStages = 8;
+constexpr size_t kSmemBudget = 227 * 1024;  // dynamic shared memory of one CTA
+constexpr size_t kSmemFixed = 1024 + 512;   // 1024-byte alignment slack + barriers
 
 constexpr uint32_t kIdesc = umma_idesc_bf16(kTileM, kLmTileN, /*a_mn=*/false, /*b_mn=*/true);
 
@@ -68,12 +69,16 @@ struct LmArgs {
   int Mt, Md;          // token rows of the target and draft sides
   int kbt, kbd;        // hidden blocks of 64
   int Ht, Hd;
+  int box_t, box_d;    // h rows per tensor copy: rows rounded up to 8 (pass 2: compact rows)
+  int perm_t;          // target rows in smem are position-major (row i*B + b), else b*(gamma+1) + i
+  int nws, nas;        // W-ring and h-ring stages
+  int a_bytes;         // bytes of one h stage (box rows x 128)
   float temperature;
   uint64_t seed, round;
-  float2* part;        // [B*R1][nvt] (max, sum) per row and tile
+  float2* part;        // [B*R1][nvt][2] (max, sum) per row, tile and column half
   float* zat;          // [B*R1] logit at the row's draft token
-  LmCand* bon;         // [B][nvt][2] bonus-row top-2
-  LmCand* res;         // [B][nvt][4] residual top-2, then p_n top-2, per compact row
+  LmCand* bon;         // [B][nvt][2][2] bonus-row top-2 per tile and column half
+  LmCand* res;         // [B][nvt][2][4] residual top-2, then p_n top-2, per compact row
   DrawState* state;    // [B]
   int* slot_b;         // [B] batch row of each compact row
   uint32_t* ctl;       // count, pass-1 error, pass-2 error
@@ -154,6 +159,14 @@ __device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity, volatile
   return false;
 }
 
+// The same for a whole warp: lane 0 polls, the others wait at the shuffle.
+__device__ __forceinline__ bool lm_wait_warp(uint64_t* bar, uint32_t parity,
+                                             volatile int* abort_flag) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = lm_wait(bar, parity, abort_flag);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 // -log2(-log2 u) noise of entry v at Philox position pos (tag 1), and its double
 // twin -ln(-ln u) for the re-decision.
 __device__ __forceinline__ double gumbel_f64(int64_t v, int pos, int b, uint64_t seed,
@@ -182,8 +195,24 @@ __device__ int redecide(const Cand2& t, F key_f64) {
 struct Seg {
   const CUtensorMap* amap;
   const CUtensorMap* bmap;
-  int kblocks, mtiles, col;
+  int kblocks;
+  int mtiles;  // 1 or 2 MMA row tiles
+  int start1;  // first h row of the second tile (rows start1 .. start1+127)
+  int col;     // tensor-memory column of the block within the accumulator
+  int box;     // h rows per copy (rounded up to 8)
+  int rows;    // rows a copy delivers (its transaction bytes / 128)
+  bool perm;   // a 3-D copy: position-major target rows
 };
+
+// The second 128-row tile of a side with 128 < M <= 256 rows ends at the last
+// row (rounded up to 8) and overlaps the first; the overlap is computed twice
+// and kept once, so no row of a copy is padding.
+__device__ __forceinline__ Seg side_seg(const CUtensorMap* am, const CUtensorMap* bm, int kb, int M,
+                                        int box, int col, bool perm) {
+  const bool two = M > kTileM;
+  // a 2-D box always delivers `box` rows (zero-filled past M); the 3-D box exactly M
+  return Seg{am, bm, kb, two ? 2 : 1, two ? box - kTileM : 0, col, box, perm ? M : box, perm};
+}
 
 template <int PASS>
 struct Jobs;
@@ -195,8 +224,8 @@ struct Jobs<1> {
   __device__ static int nseg(int) { return 1; }
   __device__ static Seg seg(int job, int, const CUtensorMap* a0, const CUtensorMap* b0,
                             const CUtensorMap* a1, const CUtensorMap* b1, const LmArgs& a) {
-    if (job == 0) return Seg{a0, b0, a.kbt, (a.Mt + kTileM - 1) / kTileM, 0};
-    return Seg{a1, b1, a.kbd, (a.Md + kTileM - 1) / kTileM, 0};
+    if (job == 0) return side_seg(a0, b0, a.kbt, a.Mt, a.box_t, 0, a.perm_t != 0);
+    return side_seg(a1, b1, a.kbd, a.Md, a.box_d, 0, false);
   }
 };
 
@@ -207,74 +236,111 @@ struct Jobs<2> {
   __device__ static int nseg(int) { return 2; }
   __device__ static Seg seg(int, int s, const CUtensorMap* a0, const CUtensorMap* b0,
                             const CUtensorMap* a1, const CUtensorMap* b1, const LmArgs& a) {
-    if (s == 0) return Seg{a0, b0, a.kbt, 1, 0};
-    return Seg{a1, b1, a.kbd, 1, kLmTileN};
+    if (s == 0) return Seg{a0, b0, a.kbt, 1, 0, 0, a.box_t, a.box_t, false};
+    return Seg{a1, b1, a.kbd, 1, 0, kLmTileN, a.box_d, a.box_d, false};
   }
 };
 
-// Online (max, sum) update of one row with 32 logits (invalid ones -inf).
-__device__ __forceinline__ void fold32(const float* f, float c, float& mc, float& s) {
-  float cm = f[0];
-#pragma unroll
-  for (int e = 1; e < 32; ++e) cm = fmaxf(cm, f[e]);
-  const float nm = fmaxf(mc, cm * c);
-  if (!(nm > -kInf)) return;
-  float s0 = (mc == -kInf) ? 0.0f : s * ex2(mc - nm), s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-#pragma unroll
-  for (int e = 0; e < 32; e += 4) {
-    s0 += ex2(fmaf(f[e], c, -nm));
-    s1 += ex2(fmaf(f[e + 1], c, -nm));
-    s2 += ex2(fmaf(f[e + 2], c, -nm));
-    s3 += ex2(fmaf(f[e + 3], c, -nm));
+// Stage index and phase of a ring of n stages.
+struct Ring {
+  uint32_t i = 0, ph = 0;
+  __device__ __forceinline__ void next(uint32_t n) {
+    if (++i == n) {
+      i = 0;
+      ph ^= 1u;
+    }
   }
-  mc = nm;
-  s = (s0 + s1) + (s2 + s3);
+};
+
+// Wait (bounded) until every copy issued into a ring has landed.
+__device__ void drain_ring(uint64_t* full, uint32_t n, uint32_t issued) {
+  for (uint32_t s = 0; s < n; ++s) {
+    if (issued <= s) continue;
+    const uint32_t last = (issued - 1u) - ((issued - 1u - s) % n);
+    mbar_wait_bounded(full + s, (last / n) & 1u);
+  }
 }
 
-// Pass-1 epilogue of one job: side 0 target rows, side 1 draft rows.
+// Online (max, sum) update of one row with 32 logits (invalid ones -inf).
+__device__ __forceinline__ void fold32(const float* f, float c, float& mc, float& s) {
+  float m8[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    m8[j] = fmaxf(fmaxf(f[4 * j], f[4 * j + 1]), fmaxf(f[4 * j + 2], f[4 * j + 3]));
+  const float cm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+  const float nm = fmaxf(mc, cm * c);
+  if (!(nm > -kInf)) return;
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = ex2(fmaf(f[j], c, -nm));
+#pragma unroll
+  for (int e = 8; e < 32; ++e) acc[e & 7] += ex2(fmaf(f[e], c, -nm));
+  const float old = (mc == -kInf) ? 0.0f : s * ex2(mc - nm);
+  mc = nm;
+  s = old + (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])));
+}
+
+__device__ __forceinline__ Cand2 merge2(const Cand2* t) {
+  Cand2 r = t[0];
+  cand_insert(r, t[1].a);
+  cand_insert(r, t[1].b);
+  return r;
+}
+
+// Pass-1 epilogue of one job (side 0 target rows, side 1 draft rows) for this
+// warp's lane quadrant and column half (two 32-column chunks of the tile).
 __device__ __forceinline__ void epilogue_pass1(const LmArgs& a, int side, int t, uint32_t tacc,
-                                               int quad, const PhiloxKeys& pk) {
+                                               int quad, int half, const PhiloxKeys& pk) {
   const int lane = threadIdx.x & 31;
-  const int gamma = a.gamma, R1 = 2 * gamma + 1, V = a.V;
+  const int gamma = a.gamma, R1 = 2 * gamma + 1, V = a.V, B = a.B;
   const int M = side ? a.Md : a.Mt;
-  const int mtiles = (M + kTileM - 1) / kTileM;
+  const int box = side ? a.box_d : a.box_t;
+  const int mtiles = M > kTileM ? 2 : 1;
   const int v0 = t * kLmTileN;
   const float c = log2_scale(inv_temperature(a.temperature));
   for (int m = 0; m < mtiles; ++m) {
-    const int rb = m * kTileM + 32 * quad;
-    if (rb >= M) continue;  // warp-uniform
+    // tile m holds rows start .. start+127; rows below `lo` belong to tile 0
+    const int start = m ? box - kTileM : 0, lo = m ? kTileM : 0;
+    const int rb = start + 32 * quad;
+    if (rb >= M || rb + 31 < lo) continue;  // warp-uniform
+    uint32_t raw[2][32];
+    const uint32_t ta = tacc + ((uint32_t)(32 * quad) << 16) + (uint32_t)(m * kTileM + half * 64);
+    tmem_ld32_async(ta, raw[0]);
+    tmem_ld32_async(ta + 32, raw[1]);
+    tmem_wait_ld();
     const int r = rb + lane;
-    const bool rv = r < M;
-    int b = 0, k = 0, x = -1;
+    if (r >= M || r < lo) continue;
+    int b, k, x = -1;
     bool bonus = false;
-    if (rv) {
-      if (side == 0) {
-        b = r / (gamma + 1);
-        const int i = r - b * (gamma + 1);
-        k = i;
-        if (i < gamma) x = __ldg(a.xt + (int64_t)b * gamma + i);
-        bonus = (i == gamma);
+    if (side == 0) {
+      int i;
+      if (a.perm_t) {
+        i = r / B;
+        b = r - i * B;
       } else {
-        b = r / gamma;
-        const int i = r - b * gamma;
-        k = gamma + 1 + i;
-        x = __ldg(a.xt + r);
+        b = r / (gamma + 1);
+        i = r - b * (gamma + 1);
       }
+      k = i;
+      if (i < gamma) x = __ldg(a.xt + (int64_t)b * gamma + i);
+      bonus = (i == gamma);
+    } else {
+      b = r / gamma;
+      k = gamma + 1 + (r - b * gamma);
+      x = __ldg(a.xt + r);
     }
     const int64_t grow = (int64_t)b * R1 + k;
     float mc = -kInf, s = 0.0f;
-    Cand2 top{cand_empty(), cand_empty()};
-    for (int ch = 0; ch < kLmTileN / 32; ++ch) {
-      const int vb = v0 + ch * 32;
-      if (vb >= V) break;  // warp-uniform
-      float f[32];
-      tmem_ld32(tacc + ((uint32_t)(32 * quad) << 16) + (uint32_t)(m * kTileM + ch * 32), f);
-      if (!rv) continue;
-      const int nvalid = min(32, V - vb);
-      if (nvalid < 32) {
+    Cand2 top[2] = {Cand2{cand_empty(), cand_empty()}, Cand2{cand_empty(), cand_empty()}};
 #pragma unroll
-        for (int e = 0; e < 32; ++e) f[e] = (e < nvalid) ? f[e] : -kInf;
-      }
+    for (int c2 = 0; c2 < 2; ++c2) {
+      const int vb = v0 + half * 64 + c2 * 32;
+      if (vb >= V) break;
+      float f[32];
+      const int nvalid = min(32, V - vb);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) f[e] = (e < nvalid) ? __uint_as_float(raw[c2][e]) : -kInf;
       if (a.dbg) {
         float4* d = reinterpret_cast<float4*>(a.dbg + grow * V + vb);
 #pragma unroll
@@ -301,29 +367,29 @@ __device__ __forceinline__ void epilogue_pass1(const LmArgs& a, int side, int t,
           for (int e = 0; e < 4; ++e) {
             const float z = f[4 * g4 + e];
             const float key = fmaf(z, c, -__log2f(neglog2_u(rr[e])));
-            cand_insert(top, LmCand{key, v + e, z, 0.0f});
+            cand_insert(top[e & 1], LmCand{key, v + e, z, 0.0f});
           }
         }
       }
     }
-    if (rv) {
-      a.part[grow * a.nvt + t] = make_float2(mc, s);
-      if (bonus) {
-        LmCand* o = a.bon + ((int64_t)b * a.nvt + t) * 2;
-        o[0] = top.a;
-        o[1] = top.b;
-      }
+    a.part[(grow * a.nvt + t) * 2 + half] = make_float2(mc, s);
+    if (bonus) {
+      const Cand2 tb = merge2(top);
+      LmCand* o = a.bon + (((int64_t)b * a.nvt + t) * 2 + half) * 2;
+      o[0] = tb.a;
+      o[1] = tb.b;
     }
   }
 }
 
 // Pass-2 epilogue of one job (compact rows; target at column 0, draft at 128).
 __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t tacc, int quad,
-                                               int rows, const PhiloxKeys& pk) {
+                                               int half, int rows, const PhiloxKeys& pk) {
   const int lane = threadIdx.x & 31;
   const int V = a.V;
   const int rb = 32 * quad;
   if (rb >= rows) return;  // warp-uniform
+  const uint32_t ta = tacc + ((uint32_t)(32 * quad) << 16) + (uint32_t)(half * 64);
   const int r = rb + lane;
   const bool rv = r < rows;
   int b = 0;
@@ -332,17 +398,19 @@ __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t 
     b = a.slot_b[r];
     st = a.state[b];
   }
-  const bool resid = rv && st.mode == kDrawResidual;
-  const int v0 = t * kLmTileN;
-  Cand2 tr{cand_empty(), cand_empty()}, tp{cand_empty(), cand_empty()};
-  for (int ch = 0; ch < kLmTileN / 32; ++ch) {
-    const int vb = v0 + ch * 32;
-    if (vb >= V) break;
-    float ft[32], fd[32];
-    const uint32_t lanebase = tacc + ((uint32_t)(32 * quad) << 16);
-    tmem_ld32(lanebase + (uint32_t)(ch * 32), ft);
-    tmem_ld32(lanebase + (uint32_t)(kLmTileN + ch * 32), fd);
-    if (!rv) continue;
+  const bool resid = st.mode == kDrawResidual;
+  const int v0 = t * kLmTileN + half * 64;
+  Cand2 tr[2], tp[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) tr[j] = tp[j] = Cand2{cand_empty(), cand_empty()};
+#pragma unroll 1
+  for (int c2 = 0; c2 < 2; ++c2) {
+    uint32_t rt[32], rd[32];
+    tmem_ld32_async(ta + (uint32_t)(c2 * 32), rt);
+    tmem_ld32_async(ta + (uint32_t)(kLmTileN + c2 * 32), rd);
+    tmem_wait_ld();
+    const int vb = v0 + c2 * 32;
+    if (!rv || vb >= V) continue;
 #pragma unroll
     for (int g4 = 0; g4 < 8; ++g4) {
       const int v = vb + 4 * g4;
@@ -352,10 +420,11 @@ __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t 
       const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float zt = ft[4 * g4 + e], zd = fd[4 * g4 + e];
+        const float zt = __uint_as_float(rt[4 * g4 + e]);
+        const float zd = __uint_as_float(rd[4 * g4 + e]);
         const float lE = __log2f(neglog2_u(rr[e]));
         const float kp = fmaf(zt, st.c, -st.mct) - lE;
-        if (zt > -kInf) cand_insert(tp, LmCand{kp, v + e, zt, zd});
+        if (zt > -kInf) cand_insert(tp[e & 1], LmCand{kp, v + e, zt, zd});
         if (resid) {
           // x = log2(q/p); p > q iff x < 0; weight p - q = p (1 - 2^x)
           const float xx = fmaf(zd - zt, st.c, st.K);
@@ -363,19 +432,19 @@ __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t 
             const float y = xx * kLn2;
             const float ser = -y * fmaf(y, fmaf(y, fmaf(y, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
             const float om = (xx > -0.125f) ? ser : 1.0f - ex2(xx);
-            cand_insert(tr, LmCand{kp + __log2f(om), v + e, zt, zd});
+            cand_insert(tr[e & 1], LmCand{kp + __log2f(om), v + e, zt, zd});
           }
         }
       }
     }
   }
-  if (rv) {
-    LmCand* o = a.res + ((int64_t)r * a.nvt + t) * 4;
-    o[0] = tr.a;
-    o[1] = tr.b;
-    o[2] = tp.a;
-    o[3] = tp.b;
-  }
+  if (!rv) return;
+  const Cand2 r2 = merge2(tr), p2 = merge2(tp);
+  LmCand* o = a.res + (((int64_t)r * a.nvt + t) * 2 + half) * 4;
+  o[0] = r2.a;
+  o[1] = r2.b;
+  o[2] = p2.a;
+  o[3] = p2.b;
 }
 
 template <int PASS>
@@ -391,25 +460,37 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     if (rows2 <= 0) return;  // nothing rejected this round (uniform over the grid)
   }
   pdl_launch_dependents();
+  // Shared memory: h ring, then W ring, then barriers.  An MMA reads a
+  // 128-row window from the start of its h tile; rows past the copied box
+  // (the rest of the stage, the next stages or the W ring) only feed
+  // accumulator rows that are never read.
+  const uint32_t nws = (uint32_t)a.nws, nas = (uint32_t)a.nas;
   const uint32_t base_u32 = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* accf = empty + kStages;  // [2]
-  uint64_t* acce = accf + 2;         // [2]
+  uint8_t* aring = smem_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
+  uint8_t* wring = aring + (size_t)nas * a.a_bytes;
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(wring + (size_t)nws * kWBytes);
+  uint64_t* wempty = wfull + kMaxWStages;
+  uint64_t* afull = wempty + kMaxWStages;
+  uint64_t* aempty = afull + kMaxAStages;
+  uint64_t* accf = aempty + kMaxAStages;  // [2]
+  uint64_t* acce = accf + 2;           // [2]
   uint64_t* fin = acce + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(fin + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full + s, 1);
-      mbar_init(empty + s, 1);
+    for (uint32_t s = 0; s < nws; ++s) {
+      mbar_init(wfull + s, 1);
+      mbar_init(wempty + s, 1);
+    }
+    for (uint32_t s = 0; s < nas; ++s) {
+      mbar_init(afull + s, 1);
+      mbar_init(aempty + s, 1);
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(accf + j, 1);
-      mbar_init(acce + j, 4);
+      mbar_init(acce + j, kEpiWarps);
     }
     mbar_init(fin, 1);
     *abort_flag = 0;
@@ -426,45 +507,54 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   const int nvt = a.nvt;
   const int G = (int)gridDim.x;
 
-  if (warp == 0) {
-    // ---------------- producer ----------------
+  if (warp == 0 || warp == 2) {
+    // ---------------- producers: W tiles (warp 0), h tiles (warp 2) ----------------
     if (lane == 0) {
-      uint32_t it = 0;
+      const bool isw = (warp == 0);
+      const uint64_t pol = isw ? l2_policy_evict_first() : l2_policy_evict_last();
+      uint64_t* full = isw ? wfull : afull;
+      uint64_t* empty = isw ? wempty : aempty;
+      const uint32_t n = isw ? nws : nas;
+      Ring r;
+      uint32_t issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < nvt; t += G) {
         const int v0 = t * kLmTileN;
         for (int job = 0; ok && job < Jobs<PASS>::kPerTile; ++job) {
           for (int sg = 0; ok && sg < Jobs<PASS>::nseg(job); ++sg) {
             const Seg q = Jobs<PASS>::seg(job, sg, &mA0, &mB0, &mA1, &mB1, a);
-            for (int kb = 0; kb < q.kblocks; ++kb, ++it) {
-              const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
-              if (!lm_wait(empty + s, ph ^ 1u, abort_flag)) {
+            for (int kb = 0; kb < q.kblocks; ++kb) {
+              if (!lm_wait(empty + r.i, r.ph ^ 1u, abort_flag)) {
                 ok = false;
                 break;
               }
-              uint8_t* st = smem + s * kStageBytes;
-              mbar_arrive_expect_tx(full + s, (uint32_t)(q.mtiles * kABytes + kBBytes));
-              for (int m = 0; m < q.mtiles; ++m)
-                tma_load_2d(st + m * kABytes, q.amap, kb * kKBlock, m * kTileM, full + s);
-              tma_load_2d(st + 2 * kABytes, q.bmap, v0, kb * kKBlock, full + s);
-              tma_load_2d(st + 2 * kABytes + kBBytes / 2, q.bmap, v0 + kLmTileN / 2, kb * kKBlock,
-                          full + s);
+              if (isw) {
+                uint8_t* st = wring + (size_t)r.i * kWBytes;
+                mbar_arrive_expect_tx(full + r.i, (uint32_t)kWBytes);
+                tma_load_2d_hint(st, q.bmap, v0, kb * kKBlock, full + r.i, pol);
+                tma_load_2d_hint(st + kWBytes / 2, q.bmap, v0 + kLmTileN / 2, kb * kKBlock,
+                                 full + r.i, pol);
+              } else {
+                uint8_t* st = aring + (size_t)r.i * a.a_bytes;
+                mbar_arrive_expect_tx(full + r.i, (uint32_t)(q.rows * kKBlock * 2));
+                if (q.perm)
+                  tma_load_3d_hint(st, q.amap, kb * kKBlock, 0, 0, full + r.i, pol);
+                else
+                  tma_load_2d_hint(st, q.amap, kb * kKBlock, 0, full + r.i, pol);
+              }
+              r.next(n);
+              ++issued;
             }
           }
         }
       }
-      // every issued copy has landed before the CTA may exit
-      for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
-        if (it <= s) continue;
-        const uint32_t last = (it - 1u) - ((it - 1u - s) % kStages);
-        mbar_wait_bounded(full + s, (last / kStages) & 1u);
-      }
+      drain_ring(full, n, issued);  // every issued copy has landed before the CTA may exit
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      uint32_t it = 0;
+      Ring rw, ra;
       int jobi = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < nvt; t += G) {
@@ -479,23 +569,28 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           for (int sg = 0; ok && sg < Jobs<PASS>::nseg(job); ++sg) {
             const Seg q = Jobs<PASS>::seg(job, sg, &mA0, &mB0, &mA1, &mB1, a);
             const uint32_t dcol = tbase + (uint32_t)(buf * 256 + q.col);
-            for (int kb = 0; kb < q.kblocks; ++kb, ++it) {
-              const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
-              if (!lm_wait(full + s, ph, abort_flag)) {
+            for (int kb = 0; kb < q.kblocks; ++kb) {
+              if (!lm_wait(wfull + rw.i, rw.ph, abort_flag) ||
+                  !lm_wait(afull + ra.i, ra.ph, abort_flag)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              const uint32_t sa = smem_u32(smem + s * kStageBytes);
-              const uint64_t bdesc = umma_smem_desc(sa + 2 * kABytes, kBBytes / 2, 1024);
+              const uint32_t wa = smem_u32(wring + (size_t)rw.i * kWBytes);
+              const uint32_t aa = smem_u32(aring + (size_t)ra.i * a.a_bytes);
+              const uint64_t bdesc = umma_smem_desc(wa, kWBytes / 2, 1024);
               for (int m = 0; m < q.mtiles; ++m) {
-                const uint64_t adesc = umma_smem_desc(sa + m * kABytes, 16, 1024);
+                const uint32_t row0 = m ? (uint32_t)q.start1 : 0u;
+                const uint64_t adesc = umma_smem_desc(aa + row0 * (kKBlock * 2), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kKBlock / 16; ++kk)
                   umma_bf16(dcol + (uint32_t)(m * kTileM), adesc + (uint64_t)(2 * kk),
                             bdesc + (uint64_t)(128 * kk), kIdesc, (kb | kk) != 0);
               }
-              umma_commit(empty + s);
+              umma_commit(wempty + rw.i);
+              umma_commit(aempty + ra.i);
+              rw.next(nws);
+              ra.next(nas);
             }
           }
           if (ok) umma_commit(accf + buf);
@@ -507,8 +602,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue (warps 2..5, tensor-memory lane quadrant warp%4) ----------------
-    const int quad = warp & 3;
+    // ---------- epilogue (warps 3..10: lane quadrant warp%4, column half (warp-3)/4) ----------
+    const int quad = warp & 3, half = (warp - 3) >> 2;
     const PhiloxKeys pk = philox_keys(a.seed);
     int jobi = 0;
     bool ok = true;
@@ -516,16 +611,16 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       for (int job = 0; job < Jobs<PASS>::kPerTile; ++job, ++jobi) {
         const int buf = jobi & 1;
         const uint32_t ap = (uint32_t)(jobi >> 1) & 1u;
-        if (!lm_wait(accf + buf, ap, abort_flag)) {
+        if (!lm_wait_warp(accf + buf, ap, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t tacc = tbase + (uint32_t)(buf * 256);
         if (PASS == 1)
-          epilogue_pass1(a, job, t, tacc, quad, pk);
+          epilogue_pass1(a, job, t, tacc, quad, half, pk);
         else
-          epilogue_pass2(a, t, tacc, quad, rows2, pk);
+          epilogue_pass2(a, t, tacc, quad, half, rows2, pk);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce + buf);
@@ -556,7 +651,7 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
   const bool err = *reinterpret_cast<volatile uint32_t*>(a.ctl + 1) != 0u;
   if (warp < nw - 1) {
     for (int k = warp; k < R1; k += nw - 1) {
-      RowStat rs = combine_row(a.part + ((int64_t)b * R1 + k) * a.nvt, a.nvt, nullptr);
+      RowStat rs = combine_row(a.part + ((int64_t)b * R1 + k) * a.nvt * 2, a.nvt * 2, nullptr);
       if (err) {
         rs.bits |= kRowTimeout | kRowNaN;
         rs.s = CUDART_NAN;
@@ -596,8 +691,8 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
   if (st.mode == kDrawSampleRow && st.pos == gamma) {
     // bonus token: merge the per-tile top-2 of row p_gamma
     Cand2 t{cand_empty(), cand_empty()};
-    const LmCand* bp = a.bon + (int64_t)b * a.nvt * 2;
-    for (int j = threadIdx.x; j < a.nvt; j += blockDim.x) {
+    const LmCand* bp = a.bon + (int64_t)b * a.nvt * 4;
+    for (int j = threadIdx.x; j < 2 * a.nvt; j += blockDim.x) {
       cand_insert(t, bp[2 * j]);
       cand_insert(t, bp[2 * j + 1]);
     }
@@ -647,9 +742,9 @@ __global__ void __launch_bounds__(256) k_lm_merge(LmArgs a) {
   const int b = a.slot_b[slot];
   const DrawState st = a.state[b];
   const bool resid = st.mode == kDrawResidual;
-  const LmCand* rp = a.res + (int64_t)slot * a.nvt * 4;
+  const LmCand* rp = a.res + (int64_t)slot * a.nvt * 8;
   Cand2 tr{cand_empty(), cand_empty()}, tp{cand_empty(), cand_empty()};
-  for (int j = threadIdx.x; j < a.nvt; j += blockDim.x) {
+  for (int j = threadIdx.x; j < 2 * a.nvt; j += blockDim.x) {
     cand_insert(tr, rp[4 * j]);
     cand_insert(tr, rp[4 * j + 1]);
     cand_insert(tp, rp[4 * j + 2]);
@@ -720,9 +815,9 @@ cudaError_t lm_device(LmDevice** out) {
   if (!d.ready) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_lm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLmSmem);
+    e = cudaFuncSetAttribute(k_lm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_lm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLmSmem);
+    e = cudaFuncSetAttribute(k_lm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
     if (e != cudaSuccess) return e;
     d.ready = true;
   }
@@ -744,7 +839,38 @@ bool encode_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// h [B][P][H] bf16 read as a 3-D box (64 hidden, B, P) with the position
+// dimension outermost: smem row i*B + b holds h[b][i].
+bool encode_bf16_pos_major(CUtensorMap* map, const void* base, int B, int P, int H) {
+  const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)B, (cuuint64_t)P};
+  const cuuint64_t strides[2] = {(cuuint64_t)P * H * 2, (cuuint64_t)H * 2};
+  const cuuint32_t box[3] = {kKBlock, (cuuint32_t)B, (cuuint32_t)P};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned_to(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+int round8(int x) { return (x + 7) & ~7; }
+
+// Shared-memory rings of one pass: h stages of exactly the copied box (about
+// 80 KB of them, 3..8 stages), the W ring takes the rest of the budget.  The
+// W ring (>= 16 KB) after the h ring keeps every 128-row MMA window inside
+// shared memory.
+void ring_config(LmArgs& a, int box_rows, size_t* smem) {
+  a.a_bytes = box_rows * kKBlock * 2;
+  int nas = (80 * 1024) / a.a_bytes;
+  nas = nas < 3 ? 3 : (nas > kMaxAStages ? kMaxAStages : nas);
+  a.nas = nas;
+  const size_t fixed = kSmemFixed + (size_t)nas * a.a_bytes;
+  int nws = (int)((kSmemBudget - fixed) / kWBytes);
+  nws = nws > kMaxWStages ? kMaxWStages : nws;
+  a.nws = nws;
+  *smem = fixed + (size_t)nws * kWBytes;
+}
 
 }  // namespace
 
@@ -809,26 +935,40 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   a.out_q = out_q;
   a.out_flags = out_flags;
 
+  // pass 1: all token rows; pass 2: the compact rows (at most B per side)
+  LmArgs a2 = a;
+  a.box_t = round8(a.Mt);
+  a.box_d = round8(a.Md);
+  size_t smem1 = 0, smem2 = 0;
+  ring_config(a, a.box_t > a.box_d ? a.box_t : a.box_d, &smem1);
+  a2.box_t = a2.box_d = round8(B);
+  ring_config(a2, a2.box_t, &smem2);
+
   CUtensorMap hT, WT, hD, WD, cT, cD;
-  if (!encode_bf16(&hT, h_target, (uint64_t)a.Mt, (uint64_t)Ht, kKBlock, kTileM) ||
-      !encode_bf16(&hD, h_draft, (uint64_t)a.Md, (uint64_t)Hd, kKBlock, kTileM) ||
+  // target rows position-major (all batch rows of position 0, then 1, ...), so
+  // the bonus rows p_gamma share warps; the plain order if the map is refused
+  a.perm_t = encode_bf16_pos_major(&hT, h_target, B, gamma + 1, Ht) ? 1 : 0;
+  if (!a.perm_t &&
+      !encode_bf16(&hT, h_target, (uint64_t)a.Mt, (uint64_t)Ht, kKBlock, (uint32_t)a.box_t))
+    return SV_ERR_CUDA;
+  if (!encode_bf16(&hD, h_draft, (uint64_t)a.Md, (uint64_t)Hd, kKBlock, (uint32_t)a.box_d) ||
       !encode_bf16(&WT, W_target, (uint64_t)Ht, (uint64_t)V, kLmTileN / 2, kKBlock) ||
       !encode_bf16(&WD, W_draft, (uint64_t)Hd, (uint64_t)V, kLmTileN / 2, kKBlock) ||
-      !encode_bf16(&cT, a.c_t, (uint64_t)B, (uint64_t)Ht, kKBlock, kTileM) ||
-      !encode_bf16(&cD, a.c_d, (uint64_t)B, (uint64_t)Hd, kKBlock, kTileM))
+      !encode_bf16(&cT, a.c_t, (uint64_t)B, (uint64_t)Ht, kKBlock, (uint32_t)a2.box_t) ||
+      !encode_bf16(&cD, a.c_d, (uint64_t)B, (uint64_t)Hd, kKBlock, (uint32_t)a2.box_d))
     return SV_ERR_CUDA;
 
   cudaError_t e = cudaMemsetAsync(a.ctl, 0, 4 * sizeof(uint32_t), stream);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   const unsigned grid = (unsigned)(pl.nvt < dev->sms ? pl.nvt : dev->sms);
   mark(0, stream);
-  k_lm<1><<<grid, kLmThreads, kLmSmem, stream>>>(hT, WT, hD, WD, a);
+  k_lm<1><<<grid, kLmThreads, smem1, stream>>>(hT, WT, hD, WD, a);
   mark(1, stream);
   const int fw = ((2 * gamma + 1) < 31 ? (2 * gamma + 1) : 31) + 1;
   e = launch_pdl(k_lm_finish, dim3((unsigned)B), dim3(32 * fw), 0, stream, a);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   mark(2, stream);
-  e = launch_pdl(k_lm<2>, dim3(grid), dim3(kLmThreads), kLmSmem, stream, cT, WT, cD, WD, a);
+  e = launch_pdl(k_lm<2>, dim3(grid), dim3(kLmThreads), smem2, stream, cT, WT, cD, WD, a2);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   mark(3, stream);
   e = launch_pdl(k_lm_merge, dim3((unsigned)B), dim3(256), 0, stream, a);

@@ -141,12 +141,13 @@ inline LmPlan make_lm_plan(int B, int gamma, int64_t V) {
   const size_t rows = (size_t)B * p.R1;
   size_t o = 0;
   p.off_ctl = o;    o = align_up(o + 4 * sizeof(uint32_t));
-  p.off_part = o;   o = align_up(o + 8 * rows * p.nvt);
+  // two partials per row and tile (the two column halves of the epilogue)
+  p.off_part = o;   o = align_up(o + 8 * rows * p.nvt * 2);
   p.off_zat = o;    o = align_up(o + sizeof(float) * rows);
   p.off_state = o;  o = align_up(o + sizeof(DrawState) * (size_t)B);
   p.off_slot = o;   o = align_up(o + sizeof(int) * (size_t)B);
-  p.off_bon = o;    o = align_up(o + 2 * sizeof(LmCand) * (size_t)B * p.nvt);
-  p.off_res = o;    o = align_up(o + 4 * sizeof(LmCand) * (size_t)B * p.nvt);
+  p.off_bon = o;    o = align_up(o + 2 * sizeof(LmCand) * (size_t)B * p.nvt * 2);
+  p.off_res = o;    o = align_up(o + 4 * sizeof(LmCand) * (size_t)B * p.nvt * 2);
   p.off_ct = o;     o = align_up(o + 2 * (size_t)B * kLmMaxHidden);
   p.off_cd = o;     o = align_up(o + 2 * (size_t)B * kLmMaxHidden);
   p.total = o;
