@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the greedy and fused LM-head measurements")
     return ap.parse_args()
 
 
@@ -60,6 +62,21 @@ def peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def tensor_peaks():
+    """(burst, sustained) dense bf16 TFLOP/s and where they come from."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+# DRAM bytes per launch of the dominant kernel from an ncu capture of the same
+# workload (profiles/ holds the summary); None when the kernel changed since.
+SWEEP_TRAFFIC_BYTES = 151462656  # 147779840 read + 3682816 written, profiles/k_sweep_tma_sample_b64.md
 
 
 class ClockSampler:
@@ -346,6 +363,11 @@ def run_ours(args):
                "sample": f"{rows} batch rows ({rows / B:.2f} rounds) of this workload, "
                          f"single-threaded, {el:.1f} s"}
 
+    extra = {}
+    if not args.no_extra:
+        extra["greedy"] = measure_greedy(L, dev, stream, rank)
+        extra["lmhead"] = measure_lmhead(L, dev, stream, rank)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": rounds_per_s, "unit": UNIT, "n_gpus": world,
@@ -360,14 +382,131 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "kernel": "k_sweep", "achieved": sweep_gbs,
                          "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": sweep_gbs / hbm, "frac_of_8TBs": sweep_gbs / 8000.0,
-                         "traffic": None, "algorithmic_bytes": sweep_bytes},
+                         "traffic": SWEEP_TRAFFIC_BYTES, "algorithmic_bytes": sweep_bytes},
             "kernel_ms": kavg,
             "gpu_launches": 3 * args.steps,  # k_sweep(_tma), k_finish, k_draw
             "clocks": clk.summary(),
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        line.update(extra)
         print(json.dumps(line), flush=True)
+
+
+def _kernel_times(L, stream, call, nkern, reps, warm=3):
+    """Average per-kernel ms of `call(i)` via the library's timing events, and
+    the average ms of a whole call without events."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nkern + 1)]
+    for e in ev:
+        e.record(stream)
+    torch.cuda.synchronize()
+    arr = (ctypes.c_void_p * (nkern + 1))(*[ctypes.c_void_p(e.cuda_event) for e in ev])
+    for i in range(warm):
+        call(i)
+    torch.cuda.synchronize()
+    acc = [0.0] * nkern
+    for i in range(reps):
+        L.sv_set_timing_events(ctypes.cast(arr, ctypes.c_void_p), nkern + 1)
+        call(warm + i)
+        L.sv_set_timing_events(None, 0)
+        torch.cuda.synchronize()
+        for k in range(nkern):
+            acc[k] += ev[k].elapsed_time(ev[k + 1])
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for i in range(reps):
+        call(warm + reps + i)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    return [a / reps for a in acc], s0.elapsed_time(s1) / reps
+
+
+def measure_greedy(L, dev, stream, rank, reps=400):
+    """Greedy verify on greedy_b64 (B=64, gamma=5, V=32000, bf16); inputs rotate
+    over >= 4x L2."""
+    import torch
+    import speculative_decoding_verification_21_gb300 as sv
+    from speculative_decoding_verification_21_gb300 import workloads as wl
+    B, g, V = 64, 5, 32000
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2**20)
+    per = B * (g + 1) * V * 2
+    nsets = max(2, -(-4 * l2 // per))
+    sets = [wl.greedy_b64(seed=2002 + 31 * k + 7 * rank, device=dev) for k in range(nsets)]
+    for s in sets:
+        s.zd = None  # greedy reads target logits only
+    torch.cuda.empty_cache()
+    tok = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = sv.alloc_workspace(B, g, V, 1, device=dev)
+    P = ctypes.c_void_p
+    sh = P(stream.cuda_stream)
+
+    def call(i):
+        s = sets[i % nsets]
+        rc = L.spec_verify_greedy(P(s.zt.data_ptr()), P(s.xt.data_ptr()), B, g, V, 1,
+                                  P(tok.data_ptr()), P(cnt.data_ptr()), P(ws.data_ptr()),
+                                  ctypes.c_size_t(ws.numel()), sh)
+        if rc != 0:
+            raise RuntimeError(sv.status_string(rc))
+
+    kms, ms = _kernel_times(L, stream, call, 1, reps)
+    hbm, kind = peaks()
+    gbs = per / (kms[0] / 1000.0) / 1e9
+    return {"workload": "greedy_b64", "B": B, "gamma": g, "V": V, "dtype": "bf16",
+            "rounds_per_s": 1000.0 / ms, "ms_per_round": ms, "kernel_ms": {"k_greedy": kms[0]},
+            "roofline": {"bound": "hbm", "kernel": "k_greedy", "achieved": gbs, "peak": hbm,
+                         "peak_kind": kind, "unit": "GB/s", "frac": gbs / hbm,
+                         "algorithmic_bytes": per},
+            "l2_policy": f"inputs rotate over {nsets} sets of {per / 1e6:.1f} MB"}
+
+
+def measure_lmhead(L, dev, stream, rank, reps=100):
+    """Fused LM heads + verify on lmhead_b32 (B=32, gamma=4, V=128256, target
+    hidden 4096, draft hidden 2048, bf16): the weights (1.58 GB) exceed L2."""
+    import torch
+    import speculative_decoding_verification_21_gb300 as sv
+    from speculative_decoding_verification_21_gb300 import workloads as wl
+    B, g, V, Ht, Hd = 32, 4, 128256, 4096, 2048
+    w = wl.lmhead_b32(seed=1005 + 7 * rank, device=dev)
+    e = w.extra
+    tok = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B,), dtype=torch.int32, device=dev)
+    flg = torch.empty((B,), dtype=torch.uint8, device=dev)
+    ws = sv.alloc_workspace(B, g, V, 2, device=dev)
+    P = ctypes.c_void_p
+    sh = P(stream.cuda_stream)
+
+    def call(i):
+        rc = L.spec_lmhead_verify(P(e["h_t"].data_ptr()), P(e["W_t"].data_ptr()), Ht,
+                                  P(e["h_d"].data_ptr()), P(e["W_d"].data_ptr()), Hd,
+                                  P(w.xt.data_ptr()), B, g, V, ctypes.c_float(1.0), 0, i,
+                                  P(tok.data_ptr()), P(cnt.data_ptr()), None, None,
+                                  P(flg.data_ptr()), None, P(ws.data_ptr()),
+                                  ctypes.c_size_t(ws.numel()), sh)
+        if rc != 0:
+            raise RuntimeError(sv.status_string(rc))
+
+    kms, ms = _kernel_times(L, stream, call, 4, reps)
+    rejected = float((cnt < g).float().mean().item())
+    hbm, kind = peaks()
+    tb, ts, tkind = tensor_peaks()
+    wbytes = 2 * V * (Ht + Hd)
+    flops1 = 2.0 * V * (B * (g + 1) * Ht + B * g * Hd)
+    gbs1 = wbytes / (kms[0] / 1000.0) / 1e9
+    tf1 = flops1 / (kms[0] / 1000.0) / 1e12
+    return {"workload": "lmhead_b32", "B": B, "gamma": g, "V": V, "Ht": Ht, "Hd": Hd,
+            "dtype": "bf16 operands, fp32 accumulate",
+            "rounds_per_s": 1000.0 / ms, "ms_per_round": ms,
+            "kernel_ms": {"k_lm_pass1": kms[0], "k_lm_finish": kms[1], "k_lm_pass2": kms[2],
+                          "k_lm_merge": kms[3]},
+            "rows_needing_pass2": rejected,
+            "roofline": {"bound": "hbm", "kernel": "k_lm_pass1", "achieved": gbs1, "peak": hbm,
+                         "peak_kind": kind, "unit": "GB/s", "frac": gbs1 / hbm,
+                         "algorithmic_bytes": wbytes},
+            "tensor": {"kernel": "k_lm_pass1", "achieved": tf1, "peak": tb, "peak_kind": tkind,
+                       "unit": "TFLOP/s", "frac": tf1 / tb, "algorithmic_flops": flops1},
+            "gpu_launches_per_round": 4}
 
 
 def main():
