@@ -35,34 +35,11 @@
 #include "sv_plan.h"
 #include "sv_tma.cuh"
 #include "sv_decide.cuh"
+#include "sv_draw.cuh"
+#include "sv_sweep.cuh"
 #include "sv_launch.h"
 
 namespace sv {
-
-// Sum of 2^(y - my) over one lane's vectors, my = max of its raw logits times c.
-template <int DT>
-__device__ __forceinline__ MS ms_of_vectors(const uint4* v, int nv, float c) {
-  float m = -kInf;
-#pragma unroll
-  for (int u = 0; u < 8; ++u)
-    if (u < nv) m = fmaxf(m, vmax<DT>(v[u]));
-  if (!(m > -kInf)) return MS{-kInf, 0.0f};
-  const float mc = m * c;
-  float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    if (u < nv) {
-      float f[VecInfo<DT>::kElems];
-      unpack<DT>(v[u], f);
-#pragma unroll
-      for (int e = 0; e < VecInfo<DT>::kElems; e += 2) {
-        s0 += ex2(fmaf(f[e], c, -mc));
-        s1 += ex2(fmaf(f[e + 1], c, -mc));
-      }
-    }
-  }
-  return MS{mc, s0 + s1};
-}
 
 // One CTA per batch row: row statistics (one warp per row) while one more warp
 // fetches the draft tokens and their target/draft logits, then the decision.
@@ -194,112 +171,11 @@ __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
   }
 }
 
-// Per-lane online (max, sum) update with a chunk maximum m of raw logits.
-__device__ __forceinline__ void lane_raise_max(float m, float c, float& zmax, float& mc,
-                                               float& sacc) {
-  if (m > zmax) {
-    const float mcn = m * c;
-    sacc = (zmax == -kInf) ? 0.0f : sacc * ex2(mc - mcn);
-    mc = mcn;
-    zmax = m;
-  }
-}
-
-// One full 4 KB chunk in shared memory: each lane takes 8 of its 256 vectors.
-// The maximum is a packed tree over the raw words, then one exp2 per logit.
-template <int DT>
-__device__ __forceinline__ void chunk_update_full(const uint4* sv, int lane, float c, float& zmax,
-                                                  float& mc, float& sacc) {
-  uint4 v[8];
-#pragma unroll
-  for (int u = 0; u < 8; ++u) v[u] = sv[lane + 32 * u];
-  float m;
-  if constexpr (DT == SV_BF16) {
-    uint32_t a[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      uint32_t p, q;
-      asm("max.bf16x2 %0, %1, %2;" : "=r"(p) : "r"(v[u].x), "r"(v[u].y));
-      asm("max.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(v[u].z), "r"(v[u].w));
-      asm("max.bf16x2 %0, %1, %2;" : "=r"(a[u]) : "r"(p), "r"(q));
-    }
-#pragma unroll
-    for (int k = 4; k > 0; k >>= 1)
-#pragma unroll
-      for (int u = 0; u < k; ++u) asm("max.bf16x2 %0, %1, %2;" : "=r"(a[u]) : "r"(a[u]), "r"(a[u + k]));
-    m = fmaxf(bf16lo(a[0]), bf16hi(a[0]));
-  } else {
-    float a[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      a[u] = fmaxf(fmaxf(__uint_as_float(v[u].x), __uint_as_float(v[u].y)),
-                   fmaxf(__uint_as_float(v[u].z), __uint_as_float(v[u].w)));
-#pragma unroll
-    for (int k = 4; k > 0; k >>= 1)
-#pragma unroll
-      for (int u = 0; u < k; ++u) a[u] = fmaxf(a[u], a[u + k]);
-    m = a[0];
-  }
-  lane_raise_max(m, c, zmax, mc, sacc);
-  if (!(zmax > -kInf)) return;
-  const float nm = -mc;
-  float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if constexpr (DT == SV_BF16) {
-        s0 += ex2(fmaf(bf16lo(w[q]), c, nm));
-        s1 += ex2(fmaf(bf16hi(w[q]), c, nm));
-      } else {
-        if (q & 1) s1 += ex2(fmaf(__uint_as_float(w[q]), c, nm));
-        else s0 += ex2(fmaf(__uint_as_float(w[q]), c, nm));
-      }
-    }
-    if (u & 1) { s2 += s0; s3 += s1; s0 = 0.0f; s1 = 0.0f; }
-  }
-  sacc += (s0 + s1) + (s2 + s3);
-}
-
 // --------------------------------------------------------------------------
 // TMA sweep (rows a multiple of 16 bytes long): persistent, per-warp pipelines.
 // Chunk c of the [b][row][chunk] order goes to warp c mod W, so the whole GPU
 // walks memory in address order; each chunk leaves one (max, sum) partial.
 // --------------------------------------------------------------------------
-// Position of a chunk: batch row b, row k of it, chunk j of the row, advanced
-// by a fixed stride without divisions.
-struct ChunkPos {
-  int b, k, j;
-};
-struct ChunkStep {
-  int db, dk, dj;  // stride W = ((db * R1) + dk) * nch + dj chunks
-};
-__device__ __forceinline__ void advance(ChunkPos& p, const ChunkStep& d, int R1, int nch) {
-  p.j += d.dj;
-  int carry_k = 0;
-  if (p.j >= nch) {
-    p.j -= nch;
-    carry_k = 1;
-  }
-  p.k += d.dk + carry_k;
-  int carry_b = 0;
-  if (p.k >= R1) {
-    p.k -= R1;
-    carry_b = 1;
-  }
-  p.b += d.db + carry_b;
-}
-
-// Warp max of m, then one rescale per lane and a warp sum.
-__device__ __forceinline__ MS warp_reduce_ms_fast(MS v) {
-  const float M = warp_max(v.m);
-  float s = (v.m > -kInf) ? v.s * ex2(v.m - M) : 0.0f;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  return MS{M, (M > -kInf) ? s : 0.0f};
-}
-
 template <int DT>
 __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
   pdl_launch_dependents();  // the finish kernel may be scheduled now; it waits for us
@@ -438,182 +314,6 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
 // --------------------------------------------------------------------------
 // Draw of the target's own token.
 // --------------------------------------------------------------------------
-struct DrawArgs {
-  const void* zt;
-  const void* zd;
-  int B, gamma;
-  int64_t V;
-  uint64_t seed, round;
-  const DrawState* state;  // [B]
-  uint32_t* counter;       // [B] CTAs done per batch row
-  uint32_t* work;          // unused by the CTA-per-chunk draw
-  Top2* part3;             // [B][nsplit3]
-  int nsplit3;             // CTAs per batch row
-  int32_t* out_tokens;
-  uint8_t* out_flags;
-};
-
-// Keys of one 4-entry Philox group v = v0 .. v0+3 from already loaded logits;
-// the running best is kept as a fraction num/den and compared by cross-products.
-template <bool RESID>
-__device__ __forceinline__ void draw_keys(const float* ztv, const float* zdv, int v0,
-                                          const DrawState& st, uint4 rnd, float& bn, float& bd,
-                                          int& bi) {
-  const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float et = ex2(fmaf(ztv[e], st.c, -st.mct));
-    float wgt;
-    bool cand;
-    if (RESID) {
-      // x = log2(q/p) for this entry; p > q iff x < 0; weight p - q = p (1 - 2^x)
-      const float x = fmaf(zdv[e] - ztv[e], st.c, st.K);
-      cand = x < 0.0f;
-      const float y = x * kLn2;
-      // 1 - 2^x: Taylor series of -expm1(y) near 0, 1 - 2^x directly elsewhere
-      const float ser = -y * fmaf(y, fmaf(y, fmaf(y, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
-      const float om = (x > -0.125f) ? ser : 1.0f - ex2(x);
-      wgt = et * om;
-    } else {
-      cand = ztv[e] > -kInf;
-      wgt = et;
-    }
-    const float E = neglog2_u(rr[e]);
-    if (cand && wgt * bd > bn * E) {
-      bn = wgt;
-      bd = E;
-      bi = v0 + e;
-    }
-  }
-}
-
-// Raw 4-entry group of a row (bf16: 8 bytes, fp32: 16 bytes) and its widening.
-template <int DT>
-struct Group;
-template <>
-struct Group<SV_BF16> {
-  uint2 v;
-};
-template <>
-struct Group<SV_F32> {
-  float4 v;
-};
-
-template <int DT>
-__device__ __forceinline__ Group<DT> load_group(const char* row, int g, int V, bool vec_ok,
-                                                float pad) {
-  Group<DT> out;
-  const int v0 = 4 * g;
-  if (vec_ok && v0 + 3 < V) {
-    if constexpr (DT == SV_F32)
-      out.v = __ldg(reinterpret_cast<const float4*>(row) + g);
-    else
-      out.v = __ldg(reinterpret_cast<const uint2*>(row) + g);
-  } else {
-    float f[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) f[e] = (v0 + e < V) ? load_logit<DT>(row, v0 + e) : pad;
-    if constexpr (DT == SV_F32) {
-      out.v = make_float4(f[0], f[1], f[2], f[3]);
-    } else {
-      // re-pack as bf16 bits (the values are bf16-exact)
-      out.v.x = (__float_as_uint(f[0]) >> 16) | (__float_as_uint(f[1]) & 0xFFFF0000u);
-      out.v.y = (__float_as_uint(f[2]) >> 16) | (__float_as_uint(f[3]) & 0xFFFF0000u);
-    }
-  }
-  return out;
-}
-
-template <int DT>
-__device__ __forceinline__ void widen(const Group<DT>& g, float* f) {
-  if constexpr (DT == SV_F32) {
-    f[0] = g.v.x; f[1] = g.v.y; f[2] = g.v.z; f[3] = g.v.w;
-  } else {
-    f[0] = bf16lo(g.v.x); f[1] = bf16hi(g.v.x); f[2] = bf16lo(g.v.y); f[3] = bf16hi(g.v.y);
-  }
-}
-
-// This thread's best key over groups [g0, g1); all loads of a step in flight together.
-template <int DT, bool RESID>
-__device__ __forceinline__ KI draw_range(const char* rt, const char* rd, int g0, int g1, int V,
-                                         bool vec_ok, const DrawState& st, uint32_t b,
-                                         const PhiloxKeys& pk, uint64_t round) {
-  float bn = -1.0f, bd = 1.0f;
-  int bi = -1;
-  constexpr int U = (DT == SV_F32) ? 4 : 8;
-  const int stride = (int)blockDim.x;
-  for (int g = g0 + (int)threadIdx.x; g < g1; g += U * stride) {
-    Group<DT> gt[U], gd[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int gg = g + u * stride;
-      if (gg < g1) {
-        gt[u] = load_group<DT>(rt, gg, V, vec_ok, -kInf);
-        if (RESID) gd[u] = load_group<DT>(rd, gg, V, vec_ok, 0.0f);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int gg = g + u * stride;
-      if (gg < g1) {
-        float zt4[4], zd4[4];
-        widen<DT>(gt[u], zt4);
-        if (RESID) widen<DT>(gd[u], zd4);
-        const uint4 rnd = philox_rk(sv_counter((uint32_t)gg, 1u, (uint32_t)st.pos, b, round), pk);
-        draw_keys<RESID>(zt4, zd4, 4 * gg, st, rnd, bn, bd, bi);
-      }
-    }
-  }
-  KI r;
-  r.i = bi;
-  r.k = (bi >= 0) ? bn / bd : -kInf;
-  return r;
-}
-
-// Double-precision key with the oracle-level definition, for the refinement.
-template <int DT>
-__device__ double draw_key_f64(const char* rt, const char* rd, int64_t v, const DrawState& st,
-                               bool resid, uint32_t b, uint64_t seed, uint64_t round) {
-  const uint4 rnd = philox4x32_10(sv_counter((uint32_t)(v >> 2), 1u, (uint32_t)st.pos, b, round),
-                                  (uint32_t)seed, (uint32_t)(seed >> 32));
-  const uint32_t lanes[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
-  const double lnE = log(sv_neglog_u_f64(lanes[v & 3]));
-  const double zt = (double)load_logit<DT>(rt, v);
-  if (!resid) return zt * (double)st.invT - lnE;
-  const double zd = (double)load_logit<DT>(rd, v);
-  const double P = exp2(zt * (double)st.c - (double)st.mct) / st.st;
-  const double Q = exp2(zd * (double)st.c - (double)st.mcd) / st.sd;
-  const double r = P - Q;
-  return (r > 0.0) ? log(r) - lnE : -CUDART_INF;
-}
-
-__device__ __forceinline__ Top2 block_top2(KI mine) {
-  __shared__ Top2 sm[kThreads / 32];
-  Top2 t{mine, KI{-kInf, -1}};
-  t = warp_reduce_top2(t);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) sm[warp] = t;
-  __syncthreads();
-  Top2 r{KI{-kInf, -1}, KI{-kInf, -1}};
-  if (warp == 0) {
-    if (lane < (int)(blockDim.x >> 5)) r = sm[lane];
-    r = warp_reduce_top2(r);
-  }
-  return r;  // valid in warp 0
-}
-
-template <int DT>
-__device__ int refine(const Top2& t, const char* rt, const char* rd, const DrawState& st,
-                      bool resid, uint32_t b, uint64_t seed, uint64_t round) {
-  if (t.a.i < 0) return -1;
-  if (t.b.i < 0 || !(t.a.k - t.b.k <= t.a.k * 0x1p-10f)) return t.a.i;
-  const double ka = draw_key_f64<DT>(rt, rd, t.a.i, st, resid, b, seed, round);
-  const double kb = draw_key_f64<DT>(rt, rd, t.b.i, st, resid, b, seed, round);
-  if (kb > ka || (kb == ka && t.b.i < t.a.i)) return t.b.i;
-  return t.a.i;
-}
-
 template <int DT>
 __global__ void __launch_bounds__(kThreads) k_draw(DrawArgs a) {
   const int b = (int)(blockIdx.x / (unsigned)a.nsplit3);

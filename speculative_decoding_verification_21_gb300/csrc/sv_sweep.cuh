@@ -1,0 +1,142 @@
+// sv_sweep.cuh -- per-lane and per-warp pieces of the softmax-statistics sweep:
+// online (max, sum of 2^(y - max)) over a 4 KB chunk in shared memory, chunk
+// positions advanced without divisions, and the warp combine.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "specverify.h"
+#include "sv_device.cuh"
+#include "sv_plan.h"
+
+namespace sv {
+
+// Sum of 2^(y - my) over one lane's vectors, my = max of its raw logits times c.
+template <int DT>
+__device__ __forceinline__ MS ms_of_vectors(const uint4* v, int nv, float c) {
+  float m = -kInf;
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    if (u < nv) m = fmaxf(m, vmax<DT>(v[u]));
+  if (!(m > -kInf)) return MS{-kInf, 0.0f};
+  const float mc = m * c;
+  float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    if (u < nv) {
+      float f[VecInfo<DT>::kElems];
+      unpack<DT>(v[u], f);
+#pragma unroll
+      for (int e = 0; e < VecInfo<DT>::kElems; e += 2) {
+        s0 += ex2(fmaf(f[e], c, -mc));
+        s1 += ex2(fmaf(f[e + 1], c, -mc));
+      }
+    }
+  }
+  return MS{mc, s0 + s1};
+}
+
+// Per-lane online (max, sum) update with a chunk maximum m of raw logits.
+__device__ __forceinline__ void lane_raise_max(float m, float c, float& zmax, float& mc,
+                                               float& sacc) {
+  if (m > zmax) {
+    const float mcn = m * c;
+    sacc = (zmax == -kInf) ? 0.0f : sacc * ex2(mc - mcn);
+    mc = mcn;
+    zmax = m;
+  }
+}
+
+// One full 4 KB chunk in shared memory: each lane takes 8 of its 256 vectors.
+// The maximum is a packed tree over the raw words, then one exp2 per logit.
+template <int DT>
+__device__ __forceinline__ void chunk_update_full(const uint4* sv, int lane, float c, float& zmax,
+                                                  float& mc, float& sacc) {
+  uint4 v[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) v[u] = sv[lane + 32 * u];
+  float m;
+  if constexpr (DT == SV_BF16) {
+    uint32_t a[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      uint32_t p, q;
+      asm("max.bf16x2 %0, %1, %2;" : "=r"(p) : "r"(v[u].x), "r"(v[u].y));
+      asm("max.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(v[u].z), "r"(v[u].w));
+      asm("max.bf16x2 %0, %1, %2;" : "=r"(a[u]) : "r"(p), "r"(q));
+    }
+#pragma unroll
+    for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+      for (int u = 0; u < k; ++u) asm("max.bf16x2 %0, %1, %2;" : "=r"(a[u]) : "r"(a[u]), "r"(a[u + k]));
+    m = fmaxf(bf16lo(a[0]), bf16hi(a[0]));
+  } else {
+    float a[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      a[u] = fmaxf(fmaxf(__uint_as_float(v[u].x), __uint_as_float(v[u].y)),
+                   fmaxf(__uint_as_float(v[u].z), __uint_as_float(v[u].w)));
+#pragma unroll
+    for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+      for (int u = 0; u < k; ++u) a[u] = fmaxf(a[u], a[u + k]);
+    m = a[0];
+  }
+  lane_raise_max(m, c, zmax, mc, sacc);
+  if (!(zmax > -kInf)) return;
+  const float nm = -mc;
+  float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if constexpr (DT == SV_BF16) {
+        s0 += ex2(fmaf(bf16lo(w[q]), c, nm));
+        s1 += ex2(fmaf(bf16hi(w[q]), c, nm));
+      } else {
+        if (q & 1) s1 += ex2(fmaf(__uint_as_float(w[q]), c, nm));
+        else s0 += ex2(fmaf(__uint_as_float(w[q]), c, nm));
+      }
+    }
+    if (u & 1) { s2 += s0; s3 += s1; s0 = 0.0f; s1 = 0.0f; }
+  }
+  sacc += (s0 + s1) + (s2 + s3);
+}
+
+// Position of a chunk: batch row b, row k of it, chunk j of the row, advanced
+// by a fixed stride without divisions.
+struct ChunkPos {
+  int b, k, j;
+};
+struct ChunkStep {
+  int db, dk, dj;  // stride W = ((db * R1) + dk) * nch + dj chunks
+};
+__device__ __forceinline__ void advance(ChunkPos& p, const ChunkStep& d, int R1, int nch) {
+  p.j += d.dj;
+  int carry_k = 0;
+  if (p.j >= nch) {
+    p.j -= nch;
+    carry_k = 1;
+  }
+  p.k += d.dk + carry_k;
+  int carry_b = 0;
+  if (p.k >= R1) {
+    p.k -= R1;
+    carry_b = 1;
+  }
+  p.b += d.db + carry_b;
+}
+
+// Warp max of m, then one rescale per lane and a warp sum.
+__device__ __forceinline__ MS warp_reduce_ms_fast(MS v) {
+  const float M = warp_max(v.m);
+  float s = (v.m > -kInf) ? v.s * ex2(v.m - M) : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return MS{M, (M > -kInf) ? s : 0.0f};
+}
+
+}  // namespace sv

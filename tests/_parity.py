@@ -31,7 +31,9 @@ def compare_sampling(gpu: dict, orc: dict, gamma: int, rows=None, check_pq=True)
             same = True
         if not same:
             ng = int(gpu["counts"][b])
-            if ng != no:
+            if not 0 <= ng <= gamma:
+                bad.append(b)
+            elif ng != no:
                 j = min(ng, no)
                 margin = abs(orc["u"][b, j] - orc["ratio"][b, j])
                 is_near = bool(margin < NEAR_TIE)
