@@ -116,7 +116,7 @@ __device__ __forceinline__ KI draw_range(const char* rt, const char* rd, int g0,
                                          const PhiloxKeys& pk, uint64_t round) {
   float bn = -1.0f, bd = 1.0f;
   int bi = -1;
-  constexpr int U = (DT == SV_F32) ? 4 : 8;
+  constexpr int U = 4;  // 4 groups in flight per row keeps 64 registers: 4 CTAs per SM
   const int stride = (int)blockDim.x;
   for (int g = g0 + (int)threadIdx.x; g < g1; g += U * stride) {
     Group<DT> gt[U], gd[U];

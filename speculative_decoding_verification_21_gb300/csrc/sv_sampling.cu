@@ -3,7 +3,8 @@
 // One round for B independent batch rows, after Algorithm 1 of "Fast Inference
 // from Transformers via Speculative Decoding" (section "The loop: draft, verify
 // in one pass, keep a prefix") and the course notes "Speculative Decoding"
-// ("The algorithm").  Two kernels per call (three with the optional overlap):
+// ("The algorithm").  Four kernels per call (five with the optional overlap),
+// chained by programmatic dependent launch:
 //
 //   sweep     online softmax statistics of every chunk of all 2*gamma+1 logit
 //             rows: max and sum of 2^(y - max), y = z * T^-1 * log2 e.
@@ -11,17 +12,18 @@
 //             persistent kernel; every warp streams 4 KB chunks, interleaved
 //             across warps in batch-row order, through a 3-stage bulk-copy (TMA)
 //             pipeline in shared memory.  k_sweep (any shape): one CTA per
-//             8192-logit chunk with 16-byte vector loads.  In both, the warp
-//             that finishes the last chunk of a row combines the row, and the
-//             one that finishes the last row of a batch row makes the decision:
-//             p(x_i), q(x_i), u_i, accept iff u_i <= p/q, first rejection by a
-//             warp ballot, the accepted prefix, and the set-up of the draw.
+//             8192-logit chunk with 16-byte vector loads.
+//   k_finish  one CTA per batch row: the row statistics from the chunk
+//             partials, then the decision: p(x_i), q(x_i), u_i, accept iff
+//             u_i <= p/q, first rejection by a warp ballot, the accepted prefix,
+//             and the set-up of the draw.
 //   k_draw    the target's own token -- bonus row p_gamma or residual
 //             max(0, p_n - q_n) -- as a Gumbel-max in the exponential-race form
-//             argmax w_v / E_v (E_v = -ln u_v, the same argmax as log w_v + g_v),
-//             split over CTAs; the last CTA of a batch row merges their top-2
-//             keys and, when the best two are within 2^-10, re-decides between
-//             them in double with the oracle-level definition.
+//             argmax w_v / E_v (E_v = -log2 u_v, the same argmax as
+//             log w_v + g_v), one CTA per 8192 entries keeping its top-2 keys;
+//   k_draw_merge  one CTA per batch row merges them and, when the best two are
+//             within 2^-10, re-decides between them in double with the
+//             oracle-level definition.
 //   k_alpha   optional overlap sum_v min(p_i, q_i) ("The acceptance rate is the
 //             overlap of p and q").
 #include <cuda_runtime.h>
@@ -314,17 +316,18 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
 // --------------------------------------------------------------------------
 // Draw of the target's own token.
 // --------------------------------------------------------------------------
+// One CTA per (batch row, kChunkDraw entries): the CTA's top-2 keys of the
+// draw, written to its slot; the merge kernel that follows picks the token.
 template <int DT>
-__global__ void __launch_bounds__(kThreads) k_draw(DrawArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) k_draw(DrawArgs a) {
   const int b = (int)(blockIdx.x / (unsigned)a.nsplit3);
   const int split = (int)(blockIdx.x - (unsigned)b * (unsigned)a.nsplit3);
   const int gamma = a.gamma;
   const int64_t V = a.V;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait();  // the decision's draw states and zeroed counters
+  pdl_wait();  // the decision's draw states
+  pdl_launch_dependents();
   const DrawState st = a.state[b];
   if (st.mode == kDrawDone) return;
-
   const bool resid = (st.mode == kDrawResidual);
   const char* rt = row_ptr<DT>(a.zt, a.zd, b, st.pos, gamma, V);
   const char* rd = resid ? row_ptr<DT>(a.zt, a.zd, b, gamma + 1 + st.pos, gamma, V) : nullptr;
@@ -336,19 +339,24 @@ __global__ void __launch_bounds__(kThreads) k_draw(DrawArgs a) {
   const PhiloxKeys pk = philox_keys(a.seed);
   KI mine = resid ? draw_range<DT, true>(rt, rd, g0, g1, Vi, vec_ok, st, b, pk, a.round)
                   : draw_range<DT, false>(rt, rd, g0, g1, Vi, vec_ok, st, b, pk, a.round);
-  Top2 t = block_top2(mine);
+  const Top2 t = block_top2(mine);
+  if (threadIdx.x == 0) a.part3[(int64_t)b * a.nsplit3 + split] = t;
+}
 
-  __shared__ bool s_last;
-  if (tid == 0) {
-    a.part3[(int64_t)b * a.nsplit3 + split] = t;
-    __threadfence();
-    s_last = is_last(atomicAdd(a.counter + b, 1u), (uint32_t)a.nsplit3);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // last CTA of batch row b: merge the per-CTA top-2 and decide
+// One CTA per batch row: merge the per-CTA top-2 keys, re-decide a near tie in
+// double, and redraw from p_n if the residual had no positive entry.
+template <int DT>
+__global__ void __launch_bounds__(kThreads) k_draw_merge(DrawArgs a) {
+  const int b = blockIdx.x;
+  const int gamma = a.gamma;
+  const int64_t V = a.V;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();  // the draw's partials
+  const DrawState st = a.state[b];
+  if (st.mode == kDrawDone) return;
+  const bool resid = (st.mode == kDrawResidual);
+  const char* rt = row_ptr<DT>(a.zt, a.zd, b, st.pos, gamma, V);
+  const char* rd = resid ? row_ptr<DT>(a.zt, a.zd, b, gamma + 1 + st.pos, gamma, V) : nullptr;
   Top2 m{KI{-kInf, -1}, KI{-kInf, -1}};
   for (int j = tid; j < a.nsplit3; j += blockDim.x) {
     const float4 raw =
@@ -378,7 +386,9 @@ __global__ void __launch_bounds__(kThreads) k_draw(DrawArgs a) {
     // the residual had no positive entry in floating point: draw from p_n itself
     DrawState sp = st;
     sp.mode = kDrawSampleRow;
-    KI f = draw_range<DT, false>(rt, nullptr, 0, ngroups, Vi, vec_ok, sp, b, pk, a.round);
+    const PhiloxKeys pk = philox_keys(a.seed);
+    KI f = draw_range<DT, false>(rt, nullptr, 0, (int)ceil_div(V, 4), (int)V, (V % 4) == 0, sp,
+                                 (uint32_t)b, pk, a.round);
     Top2 tf = block_top2(f);
     if (tid == 0)
       s_tok = refine<DT>(tf, rt, nullptr, sp, false, (uint32_t)b, a.seed, a.round);
@@ -536,6 +546,8 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
               out_tokens, out_flags};
   e = launch_pdl(k_draw<DT>, dim3((unsigned)((int64_t)pl.nsplit3 * B)), dim3(kThreads), 0, stream,
                  da);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(k_draw_merge<DT>, dim3((unsigned)B), dim3(kThreads), 0, stream, da);
   if (e != cudaSuccess) return e;
   mark(3, stream);
   if (out_alpha) {
