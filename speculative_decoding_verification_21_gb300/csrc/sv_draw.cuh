@@ -42,14 +42,14 @@ __device__ __forceinline__ void draw_keys(const float* ztv, const float* zdv, in
     float wgt;
     bool cand;
     if (RESID) {
-      // x = log2(q/p) for this entry; p > q iff x < 0; weight p - q = p (1 - 2^x)
-      const float x = fmaf(zdv[e] - ztv[e], st.c, st.K);
-      cand = x < 0.0f;
-      const float y = x * kLn2;
-      // 1 - 2^x: Taylor series of -expm1(y) near 0, 1 - 2^x directly elsewhere
-      const float ser = -y * fmaf(y, fmaf(y, fmaf(y, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
-      const float om = (x > -0.125f) ? ser : 1.0f - ex2(x);
-      wgt = et * om;
+      // weight p - q up to the common factor 2^-mct / St: 2^(zt c - mct) minus
+      // 2^(zd c + K - mct) (K = log2 of the normaliser ratio); p > q iff the
+      // first is larger.  Where p and q nearly agree the difference loses
+      // relative precision, but only for weights far below the top keys, and any
+      // misordering of the top two is re-decided in double (refine)
+      const float ed = ex2(fmaf(zdv[e], st.c, st.K - st.mct));
+      cand = et > ed;
+      wgt = et - ed;
     } else {
       cand = ztv[e] > -kInf;
       wgt = et;
