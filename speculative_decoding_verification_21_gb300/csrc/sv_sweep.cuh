@@ -87,22 +87,31 @@ __device__ __forceinline__ void chunk_update_full(const uint4* sv, int lane, flo
   lane_raise_max(m, c, zmax, mc, sacc);
   if (!(zmax > -kInf)) return;
   const float nm = -mc;
-  float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+  // pairs (even, odd element) in packed fp32x2: the same sums, in the same
+  // order, as two scalar accumulators s0 (even) and s1 (odd) folded into
+  // s2, s3 every second vector
+  const uint64_t c2 = pack2(c, c), nm2 = pack2(nm, nm), zero2 = pack2(0.0f, 0.0f);
+  uint64_t s01 = zero2, s23 = zero2;
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
     const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if constexpr (DT == SV_BF16) {
-        s0 += ex2(fmaf(bf16lo(w[q]), c, nm));
-        s1 += ex2(fmaf(bf16hi(w[q]), c, nm));
-      } else {
-        if (q & 1) s1 += ex2(fmaf(__uint_as_float(w[q]), c, nm));
-        else s0 += ex2(fmaf(__uint_as_float(w[q]), c, nm));
-      }
+    for (int q = 0; q < 4; q += (DT == SV_BF16) ? 1 : 2) {
+      const uint64_t z2 = (DT == SV_BF16)
+                              ? pack2(bf16lo(w[q]), bf16hi(w[q]))
+                              : pack2(__uint_as_float(w[q]), __uint_as_float(w[q + 1]));
+      float y0, y1;
+      unpack2(ffma2(z2, c2, nm2), y0, y1);
+      s01 = fadd2(s01, pack2(ex2(y0), ex2(y1)));
     }
-    if (u & 1) { s2 += s0; s3 += s1; s0 = 0.0f; s1 = 0.0f; }
+    if (u & 1) {
+      s23 = fadd2(s23, s01);
+      s01 = zero2;
+    }
   }
+  float s0, s1, s2, s3;
+  unpack2(s01, s0, s1);
+  unpack2(s23, s2, s3);
   sacc += (s0 + s1) + (s2 + s3);
 }
 
