@@ -50,14 +50,15 @@ namespace sv {
 namespace {
 
 constexpr int kTileM = 128;   // token rows per MMA (tensor-memory lanes)
-constexpr int kKBlock = 64;   // hidden entries per stage: one 128-byte swizzle span
-constexpr int kWBytes = kLmTileN * kKBlock * 2;  // one W tile (64 hidden x 128 vocab), 16 KB
+constexpr int kKAtom = 64;    // hidden entries of one 128-byte swizzle span
+constexpr int kKBlock = 128;  // hidden entries per stage: two spans
+constexpr int kWHalf = (kLmTileN / 2) * kKBlock * 2;  // W box: 64 vocab x 128 hidden, 16 KB
+constexpr int kWBytes = 2 * kWHalf;                    // one W tile per stage, 32 KB
 constexpr int kEpiWarps = 8;     // two per tensor-memory lane quadrant, each half the columns
 constexpr int kLmThreads = 32 * (3 + kEpiWarps);  // W producer, MMA issuer, h producer, epilogue
 constexpr int kTmemCols = 512;   // two accumulators of 256 columns
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr int kMaxWStages = 12;
-constexpr int kMaxAStages = 8;
+constexpr int kMaxStages = 8;
 constexpr size_t kSmemBudget = 227 * 1024;  // dynamic shared memory of one CTA
 constexpr size_t kSmemFixed = 1024 + 512;   // 1024-byte alignment slack + barriers
 
@@ -71,8 +72,8 @@ struct LmArgs {
   int Ht, Hd;
   int box_t, box_d;    // h rows per tensor copy: rows rounded up to 8 (pass 2: compact rows)
   int perm_t;          // target rows in smem are position-major (row i*B + b), else b*(gamma+1) + i
-  int nws, nas;        // W-ring and h-ring stages
-  int a_bytes;         // bytes of one h stage (box rows x 128)
+  int nstages;         // ring stages (h tiles and W tile per stage)
+  int a_half;          // bytes of the h tile of one 64-wide span (box rows x 128)
   float temperature;
   uint64_t seed, round;
   float2* part;        // [B*R1][nvt][2] (max, sum) per row, tile and column half
@@ -460,33 +461,27 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     if (rows2 <= 0) return;  // nothing rejected this round (uniform over the grid)
   }
   pdl_launch_dependents();
-  // Shared memory: h ring, then W ring, then barriers.  An MMA reads a
-  // 128-row window from the start of its h tile; rows past the copied box
-  // (the rest of the stage, the next stages or the W ring) only feed
-  // accumulator rows that are never read.
-  const uint32_t nws = (uint32_t)a.nws, nas = (uint32_t)a.nas;
+  // Shared memory: a ring of stages [h span 0 | h span 1 | W vocab half 0 |
+  // W vocab half 1], then barriers.  An MMA reads a 128-row window from the
+  // start of its h tile; rows past the copied box (the rest of the stage or the
+  // next stage) only feed accumulator rows that are never read.
+  const uint32_t nst = (uint32_t)a.nstages;
+  const size_t stage_bytes = (size_t)2 * a.a_half + kWBytes;
   const uint32_t base_u32 = smem_u32(smem_raw);
-  uint8_t* aring = smem_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
-  uint8_t* wring = aring + (size_t)nas * a.a_bytes;
-  uint64_t* wfull = reinterpret_cast<uint64_t*>(wring + (size_t)nws * kWBytes);
-  uint64_t* wempty = wfull + kMaxWStages;
-  uint64_t* afull = wempty + kMaxWStages;
-  uint64_t* aempty = afull + kMaxAStages;
-  uint64_t* accf = aempty + kMaxAStages;  // [2]
-  uint64_t* acce = accf + 2;           // [2]
+  uint8_t* ring = smem_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)nst * stage_bytes);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* accf = empty + kMaxStages;  // [2]
+  uint64_t* acce = accf + 2;            // [2]
   uint64_t* fin = acce + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(fin + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (uint32_t s = 0; s < nws; ++s) {
-      mbar_init(wfull + s, 1);
-      mbar_init(wempty + s, 1);
-    }
-    for (uint32_t s = 0; s < nas; ++s) {
-      mbar_init(afull + s, 1);
-      mbar_init(aempty + s, 1);
+    for (uint32_t s = 0; s < nst; ++s) {
+      mbar_init(full + s, 2);  // both producers
+      mbar_init(empty + s, 1);
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(accf + j, 1);
@@ -512,9 +507,6 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     if (lane == 0) {
       const bool isw = (warp == 0);
       const uint64_t pol = isw ? l2_policy_evict_first() : l2_policy_evict_last();
-      uint64_t* full = isw ? wfull : afull;
-      uint64_t* empty = isw ? wempty : aempty;
-      const uint32_t n = isw ? nws : nas;
       Ring r;
       uint32_t issued = 0;
       bool ok = true;
@@ -528,33 +520,37 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                 ok = false;
                 break;
               }
+              uint8_t* st = ring + (size_t)r.i * stage_bytes;
+              const int k0 = kb * kKBlock;  // spans past the hidden size read as zeros
               if (isw) {
-                uint8_t* st = wring + (size_t)r.i * kWBytes;
+                uint8_t* wst = st + 2 * (size_t)a.a_half;
                 mbar_arrive_expect_tx(full + r.i, (uint32_t)kWBytes);
-                tma_load_2d_hint(st, q.bmap, v0, kb * kKBlock, full + r.i, pol);
-                tma_load_2d_hint(st + kWBytes / 2, q.bmap, v0 + kLmTileN / 2, kb * kKBlock,
-                                 full + r.i, pol);
+                tma_load_2d_hint(wst, q.bmap, v0, k0, full + r.i, pol);
+                tma_load_2d_hint(wst + kWHalf, q.bmap, v0 + kLmTileN / 2, k0, full + r.i, pol);
               } else {
-                uint8_t* st = aring + (size_t)r.i * a.a_bytes;
-                mbar_arrive_expect_tx(full + r.i, (uint32_t)(q.rows * kKBlock * 2));
-                if (q.perm)
-                  tma_load_3d_hint(st, q.amap, kb * kKBlock, 0, 0, full + r.i, pol);
-                else
-                  tma_load_2d_hint(st, q.amap, kb * kKBlock, 0, full + r.i, pol);
+                mbar_arrive_expect_tx(full + r.i, (uint32_t)(2 * q.rows * kKAtom * 2));
+                for (int h = 0; h < 2; ++h) {
+                  if (q.perm)
+                    tma_load_3d_hint(st + (size_t)h * a.a_half, q.amap, k0 + h * kKAtom, 0, 0,
+                                     full + r.i, pol);
+                  else
+                    tma_load_2d_hint(st + (size_t)h * a.a_half, q.amap, k0 + h * kKAtom, 0,
+                                     full + r.i, pol);
+                }
               }
-              r.next(n);
+              r.next(nst);
               ++issued;
             }
           }
         }
       }
-      drain_ring(full, n, issued);  // every issued copy has landed before the CTA may exit
+      drain_ring(full, nst, issued);  // every issued copy has landed before the CTA may exit
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      Ring rw, ra;
+      Ring r;
       int jobi = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < nvt; t += G) {
@@ -570,27 +566,28 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const Seg q = Jobs<PASS>::seg(job, sg, &mA0, &mB0, &mA1, &mB1, a);
             const uint32_t dcol = tbase + (uint32_t)(buf * 256 + q.col);
             for (int kb = 0; kb < q.kblocks; ++kb) {
-              if (!lm_wait(wfull + rw.i, rw.ph, abort_flag) ||
-                  !lm_wait(afull + ra.i, ra.ph, abort_flag)) {
+              // one wait per stage: the copies of both producers have landed
+              if (!lm_wait(full + r.i, r.ph, abort_flag)) {
                 ok = false;
                 break;
               }
-              tc_fence_after();
-              const uint32_t wa = smem_u32(wring + (size_t)rw.i * kWBytes);
-              const uint32_t aa = smem_u32(aring + (size_t)ra.i * a.a_bytes);
-              const uint64_t bdesc = umma_smem_desc(wa, kWBytes / 2, 1024);
+              const uint32_t sa = smem_u32(ring + (size_t)r.i * stage_bytes);
+              const uint64_t bdesc = umma_smem_desc(sa + 2 * (uint32_t)a.a_half, kWHalf, 1024);
               for (int m = 0; m < q.mtiles; ++m) {
                 const uint32_t row0 = m ? (uint32_t)q.start1 : 0u;
-                const uint64_t adesc = umma_smem_desc(aa + row0 * (kKBlock * 2), 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < kKBlock / 16; ++kk)
-                  umma_bf16(dcol + (uint32_t)(m * kTileM), adesc + (uint64_t)(2 * kk),
-                            bdesc + (uint64_t)(128 * kk), kIdesc, (kb | kk) != 0);
+                for (int h = 0; h < 2; ++h) {
+                  const uint64_t adesc =
+                      umma_smem_desc(sa + (uint32_t)(h * a.a_half) + row0 * (kKAtom * 2), 16, 1024);
+#pragma unroll
+                  for (int kk = 0; kk < kKAtom / 16; ++kk)
+                    umma_bf16(dcol + (uint32_t)(m * kTileM), adesc + (uint64_t)(2 * kk),
+                              bdesc + (uint64_t)(128 * (h * (kKAtom / 16) + kk)), kIdesc,
+                              (kb | h | kk) != 0);
+                }
               }
-              umma_commit(wempty + rw.i);
-              umma_commit(aempty + ra.i);
-              rw.next(nws);
-              ra.next(nas);
+              umma_commit(empty + r.i);
+              r.next(nst);
             }
           }
           if (ok) umma_commit(accf + buf);
@@ -844,7 +841,7 @@ bool encode_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
 bool encode_bf16_pos_major(CUtensorMap* map, const void* base, int B, int P, int H) {
   const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)B, (cuuint64_t)P};
   const cuuint64_t strides[2] = {(cuuint64_t)P * H * 2, (cuuint64_t)H * 2};
-  const cuuint32_t box[3] = {kKBlock, (cuuint32_t)B, (cuuint32_t)P};
+  const cuuint32_t box[3] = {kKAtom, (cuuint32_t)B, (cuuint32_t)P};
   const cuuint32_t estr[3] = {1, 1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -856,20 +853,17 @@ bool aligned_to(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p
 
 int round8(int x) { return (x + 7) & ~7; }
 
-// Shared-memory rings of one pass: h stages of exactly the copied box (about
-// 80 KB of them, 3..8 stages), the W ring takes the rest of the budget.  The
-// W ring (>= 16 KB) after the h ring keeps every 128-row MMA window inside
-// shared memory.
+// The ring of one pass: as many stages of (two h spans of `box_rows` rows and a
+// 32 KB W tile) as the shared memory holds.  The h spans are at least 1 KB
+// apart-aligned (rows are a multiple of 8); the W tile after them keeps every
+// 128-row MMA window inside the stage.
 void ring_config(LmArgs& a, int box_rows, size_t* smem) {
-  a.a_bytes = box_rows * kKBlock * 2;
-  int nas = (80 * 1024) / a.a_bytes;
-  nas = nas < 3 ? 3 : (nas > kMaxAStages ? kMaxAStages : nas);
-  a.nas = nas;
-  const size_t fixed = kSmemFixed + (size_t)nas * a.a_bytes;
-  int nws = (int)((kSmemBudget - fixed) / kWBytes);
-  nws = nws > kMaxWStages ? kMaxWStages : nws;
-  a.nws = nws;
-  *smem = fixed + (size_t)nws * kWBytes;
+  a.a_half = box_rows * kKAtom * 2;
+  const size_t stage = (size_t)2 * a.a_half + kWBytes;
+  int n = (int)((kSmemBudget - kSmemFixed) / stage);
+  n = n > kMaxStages ? kMaxStages : n;
+  a.nstages = n;
+  *smem = kSmemFixed + (size_t)n * stage;
 }
 
 }  // namespace
@@ -910,8 +904,8 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   a.nvt = pl.nvt;
   a.Mt = B * (gamma + 1);
   a.Md = B * gamma;
-  a.kbt = Ht / kKBlock;
-  a.kbd = Hd / kKBlock;
+  a.kbt = (Ht + kKBlock - 1) / kKBlock;
+  a.kbd = (Hd + kKBlock - 1) / kKBlock;
   a.Ht = Ht;
   a.Hd = Hd;
   a.temperature = temperature;
@@ -949,13 +943,13 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   // the bonus rows p_gamma share warps; the plain order if the map is refused
   a.perm_t = encode_bf16_pos_major(&hT, h_target, B, gamma + 1, Ht) ? 1 : 0;
   if (!a.perm_t &&
-      !encode_bf16(&hT, h_target, (uint64_t)a.Mt, (uint64_t)Ht, kKBlock, (uint32_t)a.box_t))
+      !encode_bf16(&hT, h_target, (uint64_t)a.Mt, (uint64_t)Ht, kKAtom, (uint32_t)a.box_t))
     return SV_ERR_CUDA;
-  if (!encode_bf16(&hD, h_draft, (uint64_t)a.Md, (uint64_t)Hd, kKBlock, (uint32_t)a.box_d) ||
+  if (!encode_bf16(&hD, h_draft, (uint64_t)a.Md, (uint64_t)Hd, kKAtom, (uint32_t)a.box_d) ||
       !encode_bf16(&WT, W_target, (uint64_t)Ht, (uint64_t)V, kLmTileN / 2, kKBlock) ||
       !encode_bf16(&WD, W_draft, (uint64_t)Hd, (uint64_t)V, kLmTileN / 2, kKBlock) ||
-      !encode_bf16(&cT, a.c_t, (uint64_t)B, (uint64_t)Ht, kKBlock, (uint32_t)a2.box_t) ||
-      !encode_bf16(&cD, a.c_d, (uint64_t)B, (uint64_t)Hd, kKBlock, (uint32_t)a2.box_d))
+      !encode_bf16(&cT, a.c_t, (uint64_t)B, (uint64_t)Ht, kKAtom, (uint32_t)a2.box_t) ||
+      !encode_bf16(&cD, a.c_d, (uint64_t)B, (uint64_t)Hd, kKAtom, (uint32_t)a2.box_d))
     return SV_ERR_CUDA;
 
   cudaError_t e = cudaMemsetAsync(a.ctl, 0, 4 * sizeof(uint32_t), stream);
