@@ -11,19 +11,22 @@
 //   k_lm<1>      persistent, one CTA per SM.  Vocabulary tiles of 128 entries
 //                are dealt round-robin; for each tile the CTA computes the
 //                target block (B(gamma+1) token rows x 128) and then the draft
-//                block (B gamma rows x 128).  Warp 0 streams h and W tiles with
-//                2-D tensor copies into a 4-stage shared-memory ring, warp 1
-//                issues tcgen05.mma into one of two tensor-memory accumulators,
-//                and warps 2-5 drain the other (tcgen05.ld): per-row online
-//                softmax statistics, z at each draft token, and the top-2
-//                Gumbel-max keys of the bonus row p_gamma.
+//                block (B gamma rows x 128).  Warps 0 and 2 stream W and h
+//                with tensor copies into one shared-memory ring whose stages
+//                hold a 128-wide hidden block of both, warp 1 issues
+//                tcgen05.mma into one of two tensor-memory accumulators, and
+//                warps 3-10 drain the other (tcgen05.ld): per-row online
+//                softmax statistics carried over the CTA's tiles, z at each
+//                draft token, and the top-2 Gumbel-max keys of the bonus row
+//                p_gamma; one partial per row and CTA.
 //   k_lm_finish  one CTA per batch row: row combine and the decision exactly as
 //                for given logits, the bonus draw when all drafts are accepted,
 //                and otherwise a compact copy of the two hidden rows at the
 //                first rejection.
-//   k_lm<2>      the same GEMM for the compact rows only, target and draft
-//                blocks side by side in tensor memory; the epilogue keeps the
-//                top-2 keys of the residual max(0, p_n - q_n) and of p_n.
+//   k_lm<2>      the same GEMM for the compact rows only (tiles in reverse
+//                order), target and draft blocks side by side in tensor
+//                memory; the epilogue keeps the top-2 keys of the residual
+//                max(0, p_n - q_n) and of p_n over the CTA's tiles.
 //   k_lm_merge   one CTA per compact row: merge, re-decide near ties in double,
 //                fall back to p_n for an empty residual, emit.
 //
@@ -67,6 +70,7 @@ constexpr uint32_t kIdesc = umma_idesc_bf16(kTileM, kLmTileN, /*a_mn=*/false, /*
 struct LmArgs {
   const int32_t* xt;
   int B, gamma, V, nvt;
+  int nslot;           // CTAs of the GEMM passes: partials per row and column half
   int Mt, Md;          // token rows of the target and draft sides
   int kbt, kbd;        // hidden blocks of 64
   int Ht, Hd;
@@ -76,10 +80,10 @@ struct LmArgs {
   int a_half;          // bytes of the h tile of one 64-wide span (box rows x 128)
   float temperature;
   uint64_t seed, round;
-  float2* part;        // [B*R1][nvt][2] (max, sum) per row, tile and column half
+  float2* part;        // [B*R1][nslot][2] (max, sum) per row, CTA and column half
   float* zat;          // [B*R1] logit at the row's draft token
-  LmCand* bon;         // [B][nvt][2][2] bonus-row top-2 per tile and column half
-  LmCand* res;         // [B][nvt][2][4] residual top-2, then p_n top-2, per compact row
+  LmCand* bon;         // [B][nslot][2][2] bonus-row top-2 per CTA and column half
+  LmCand* res;         // [B][nslot][2][4] residual top-2, then p_n top-2, per compact row
   DrawState* state;    // [B]
   int* slot_b;         // [B] batch row of each compact row
   uint32_t* ctl;       // count, pass-1 error, pass-2 error
@@ -242,6 +246,14 @@ struct Jobs<2> {
   }
 };
 
+// Vocabulary tile of the CTA's tile counter t.  The recompute pass walks the
+// tiles in the reverse order, so that its first tiles are the ones the first
+// pass read last (still in L2).
+template <int PASS>
+__device__ __forceinline__ int vocab_tile(int t, int nvt) {
+  return PASS == 2 ? nvt - 1 - t : t;
+}
+
 // Stage index and phase of a ring of n stages.
 struct Ring {
   uint32_t i = 0, ph = 0;
@@ -289,50 +301,87 @@ __device__ __forceinline__ Cand2 merge2(const Cand2* t) {
   return r;
 }
 
-// Pass-1 epilogue of one job (side 0 target rows, side 1 draft rows) for this
-// warp's lane quadrant and column half (two 32-column chunks of the tile).
-__device__ __forceinline__ void epilogue_pass1(const LmArgs& a, int side, int t, uint32_t tacc,
-                                               int quad, int half, const PhiloxKeys& pk) {
-  const int lane = threadIdx.x & 31;
-  const int gamma = a.gamma, R1 = 2 * gamma + 1, V = a.V, B = a.B;
+// Row of a side handled by this thread in row tile m (-1: none).  Tile m holds
+// rows start .. start+127; rows below 128 of the second tile belong to the first.
+__device__ __forceinline__ int side_row(const LmArgs& a, int side, int m, int quad, int lane) {
   const int M = side ? a.Md : a.Mt;
   const int box = side ? a.box_d : a.box_t;
-  const int mtiles = M > kTileM ? 2 : 1;
+  if (m == 1 && M <= kTileM) return -1;
+  const int r = (m ? box - kTileM : 0) + 32 * quad + lane;
+  return (r < M && r >= m * kTileM) ? r : -1;
+}
+
+// Batch row b, logit row k within it (0..gamma target, gamma+1.. draft) and the
+// draft token at the row (-1: none) of token row r of a side.
+struct RowId {
+  int b, k, x;
+};
+__device__ __forceinline__ RowId row_id(const LmArgs& a, int side, int r) {
+  const int gamma = a.gamma;
+  RowId id;
+  if (side == 0) {
+    int i;
+    if (a.perm_t) {
+      i = r / a.B;
+      id.b = r - i * a.B;
+    } else {
+      id.b = r / (gamma + 1);
+      i = r - id.b * (gamma + 1);
+    }
+    id.k = i;
+    id.x = (i < gamma) ? __ldg(a.xt + (int64_t)id.b * gamma + i) : -1;
+  } else {
+    id.b = r / gamma;
+    id.k = gamma + 1 + (r - id.b * gamma);
+    id.x = __ldg(a.xt + r);
+  }
+  return id;
+}
+
+// What a pass-1 epilogue thread carries over the vocabulary tiles of its CTA:
+// the online (max, sum) of each of its rows and the bonus-row top-2.
+struct Pass1Carry {
+  float mc[2][2], s[2][2];  // [side][row tile]
+  Cand2 bon[2];             // [row tile] (target side)
+};
+
+__device__ __forceinline__ void carry_init(Pass1Carry& cy) {
+#pragma unroll
+  for (int sd = 0; sd < 2; ++sd)
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      cy.mc[sd][m] = -kInf;
+      cy.s[sd][m] = 0.0f;
+    }
+  cy.bon[0] = cy.bon[1] = Cand2{cand_empty(), cand_empty()};
+}
+
+// Pass-1 epilogue of one job (SIDE 0 target rows, 1 draft rows) for this warp's
+// lane quadrant and column half (two 32-column chunks of the tile).
+template <int SIDE>
+__device__ __forceinline__ void epilogue_pass1(const LmArgs& a, int t, uint32_t tacc, int quad,
+                                               int half, const PhiloxKeys& pk, Pass1Carry& cy) {
+  const int lane = threadIdx.x & 31;
+  const int gamma = a.gamma, R1 = 2 * gamma + 1, V = a.V;
+  const int M = SIDE ? a.Md : a.Mt;
+  const int box = SIDE ? a.box_d : a.box_t;
   const int v0 = t * kLmTileN;
   const float c = log2_scale(inv_temperature(a.temperature));
-  for (int m = 0; m < mtiles; ++m) {
-    // tile m holds rows start .. start+127; rows below `lo` belong to tile 0
-    const int start = m ? box - kTileM : 0, lo = m ? kTileM : 0;
-    const int rb = start + 32 * quad;
-    if (rb >= M || rb + 31 < lo) continue;  // warp-uniform
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    if (m == 1 && M <= kTileM) break;
+    const int rb = (m ? box - kTileM : 0) + 32 * quad;
+    if (rb >= M || rb + 31 < m * kTileM) continue;  // warp-uniform
     uint32_t raw[2][32];
     const uint32_t ta = tacc + ((uint32_t)(32 * quad) << 16) + (uint32_t)(m * kTileM + half * 64);
     tmem_ld32_async(ta, raw[0]);
     tmem_ld32_async(ta + 32, raw[1]);
     tmem_wait_ld();
-    const int r = rb + lane;
-    if (r >= M || r < lo) continue;
-    int b, k, x = -1;
-    bool bonus = false;
-    if (side == 0) {
-      int i;
-      if (a.perm_t) {
-        i = r / B;
-        b = r - i * B;
-      } else {
-        b = r / (gamma + 1);
-        i = r - b * (gamma + 1);
-      }
-      k = i;
-      if (i < gamma) x = __ldg(a.xt + (int64_t)b * gamma + i);
-      bonus = (i == gamma);
-    } else {
-      b = r / gamma;
-      k = gamma + 1 + (r - b * gamma);
-      x = __ldg(a.xt + r);
-    }
-    const int64_t grow = (int64_t)b * R1 + k;
-    float mc = -kInf, s = 0.0f;
+    const int r = side_row(a, SIDE, m, quad, lane);
+    if (r < 0) continue;
+    const RowId id = row_id(a, SIDE, r);
+    const bool bonus = (SIDE == 0) && id.k == gamma;
+    const int64_t grow = (int64_t)id.b * R1 + id.k;
     Cand2 top[2] = {Cand2{cand_empty(), cand_empty()}, Cand2{cand_empty(), cand_empty()}};
 #pragma unroll
     for (int c2 = 0; c2 < 2; ++c2) {
@@ -348,11 +397,11 @@ __device__ __forceinline__ void epilogue_pass1(const LmArgs& a, int side, int t,
         for (int j = 0; j < 8; ++j)
           if (4 * j < nvalid) d[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
       }
-      fold32(f, c, mc, s);
-      if ((unsigned)(x - vb) < 32u) {
+      fold32(f, c, cy.mc[SIDE][m], cy.s[SIDE][m]);
+      if ((unsigned)(id.x - vb) < 32u) {
         float g = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) g = (e == x - vb) ? f[e] : g;
+        for (int e = 0; e < 32; ++e) g = (e == id.x - vb) ? f[e] : g;
         a.zat[grow] = g;
       }
       if (bonus) {
@@ -361,7 +410,7 @@ __device__ __forceinline__ void epilogue_pass1(const LmArgs& a, int side, int t,
           const int v = vb + 4 * g4;
           if (v >= V) break;
           const uint4 rnd = philox_rk(sv_counter((uint32_t)(v >> 2), 1u, (uint32_t)gamma,
-                                                 (uint32_t)b, a.round),
+                                                 (uint32_t)id.b, a.round),
                                       pk);
           const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
 #pragma unroll
@@ -373,19 +422,45 @@ __device__ __forceinline__ void epilogue_pass1(const LmArgs& a, int side, int t,
         }
       }
     }
-    a.part[(grow * a.nvt + t) * 2 + half] = make_float2(mc, s);
-    if (bonus) {
-      const Cand2 tb = merge2(top);
-      LmCand* o = a.bon + (((int64_t)b * a.nvt + t) * 2 + half) * 2;
-      o[0] = tb.a;
-      o[1] = tb.b;
+    if (SIDE == 0 && bonus) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        cand_insert(cy.bon[m], top[j].a);
+        cand_insert(cy.bon[m], top[j].b);
+      }
     }
   }
 }
 
-// Pass-2 epilogue of one job (compact rows; target at column 0, draft at 128).
+// One partial per row, CTA and column half: slot (row * nslot + cta) * 2 + half.
+__device__ __forceinline__ void pass1_flush(const LmArgs& a, const Pass1Carry& cy, int quad,
+                                            int half) {
+  const int lane = threadIdx.x & 31;
+  const int R1 = 2 * a.gamma + 1;
+#pragma unroll
+  for (int sd = 0; sd < 2; ++sd)
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const int r = side_row(a, sd, m, quad, lane);
+      if (r < 0) continue;
+      const RowId id = row_id(a, sd, r);
+      const int64_t grow = (int64_t)id.b * R1 + id.k;
+      const int64_t slot = (grow * a.nslot + blockIdx.x) * 2 + half;
+      a.part[slot] = make_float2(cy.mc[sd][m], cy.s[sd][m]);
+      if (sd == 0 && id.k == a.gamma) {
+        LmCand* o = a.bon + (((int64_t)id.b * a.nslot + blockIdx.x) * 2 + half) * 2;
+        o[0] = cy.bon[m].a;
+        o[1] = cy.bon[m].b;
+      }
+    }
+}
+
+// Pass-2 epilogue of one job (compact rows; target at column 0, draft at 128):
+// the residual top-2 `tr` and the p_n top-2 `tp` of this thread's row, carried
+// over the CTA's tiles.
 __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t tacc, int quad,
-                                               int half, int rows, const PhiloxKeys& pk) {
+                                               int half, int rows, const PhiloxKeys& pk,
+                                               Cand2* tr, Cand2* tp) {
   const int lane = threadIdx.x & 31;
   const int V = a.V;
   const int rb = 32 * quad;
@@ -401,9 +476,6 @@ __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t 
   }
   const bool resid = st.mode == kDrawResidual;
   const int v0 = t * kLmTileN + half * 64;
-  Cand2 tr[2], tp[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) tr[j] = tp[j] = Cand2{cand_empty(), cand_empty()};
 #pragma unroll 1
   for (int c2 = 0; c2 < 2; ++c2) {
     uint32_t rt[32], rd[32];
@@ -439,9 +511,14 @@ __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t 
       }
     }
   }
-  if (!rv) return;
+}
+
+__device__ __forceinline__ void pass2_flush(const LmArgs& a, int quad, int half, int rows,
+                                            const Cand2* tr, const Cand2* tp) {
+  const int r = 32 * quad + (threadIdx.x & 31);
+  if (r >= rows) return;
   const Cand2 r2 = merge2(tr), p2 = merge2(tp);
-  LmCand* o = a.res + (((int64_t)r * a.nvt + t) * 2 + half) * 4;
+  LmCand* o = a.res + (((int64_t)r * a.nslot + blockIdx.x) * 2 + half) * 4;
   o[0] = r2.a;
   o[1] = r2.b;
   o[2] = p2.a;
@@ -511,7 +588,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       uint32_t issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < nvt; t += G) {
-        const int v0 = t * kLmTileN;
+        const int v0 = vocab_tile<PASS>(t, nvt) * kLmTileN;
         for (int job = 0; ok && job < Jobs<PASS>::kPerTile; ++job) {
           for (int sg = 0; ok && sg < Jobs<PASS>::nseg(job); ++sg) {
             const Seg q = Jobs<PASS>::seg(job, sg, &mA0, &mB0, &mA1, &mB1, a);
@@ -602,27 +679,47 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     // ---------- epilogue (warps 3..10: lane quadrant warp%4, column half (warp-3)/4) ----------
     const int quad = warp & 3, half = (warp - 3) >> 2;
     const PhiloxKeys pk = philox_keys(a.seed);
+    Pass1Carry cy;
+    Cand2 tr[2], tp[2];
+    if (PASS == 1) {
+      carry_init(cy);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) tr[j] = tp[j] = Cand2{cand_empty(), cand_empty()};
+    }
     int jobi = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < nvt; t += G) {
-      for (int job = 0; job < Jobs<PASS>::kPerTile; ++job, ++jobi) {
-        const int buf = jobi & 1;
-        const uint32_t ap = (uint32_t)(jobi >> 1) & 1u;
+#pragma unroll
+      for (int job = 0; job < Jobs<PASS>::kPerTile; ++job) {
+        const int buf = (jobi + job) & 1;
+        const uint32_t ap = (uint32_t)((jobi + job) >> 1) & 1u;
         if (!lm_wait_warp(accf + buf, ap, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t tacc = tbase + (uint32_t)(buf * 256);
-        if (PASS == 1)
-          epilogue_pass1(a, job, t, tacc, quad, half, pk);
-        else
-          epilogue_pass2(a, t, tacc, quad, half, rows2, pk);
+        const int tv = vocab_tile<PASS>(t, nvt);
+        if (PASS == 1) {
+          if (job == 0)
+            epilogue_pass1<0>(a, tv, tacc, quad, half, pk, cy);
+          else
+            epilogue_pass1<1>(a, tv, tacc, quad, half, pk, cy);
+        } else {
+          epilogue_pass2(a, tv, tacc, quad, half, rows2, pk, tr, tp);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce + buf);
       }
+      jobi += Jobs<PASS>::kPerTile;
     }
+    // partials of this CTA (also after an abort: the error flag marks them)
+    if (PASS == 1)
+      pass1_flush(a, cy, quad, half);
+    else
+      pass2_flush(a, quad, half, rows2, tr, tp);
   }
 
   if (threadIdx.x == 0 && *abort_flag) atomicOr(a.ctl + (PASS == 1 ? 1 : 2), 1u);
@@ -648,7 +745,7 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
   const bool err = *reinterpret_cast<volatile uint32_t*>(a.ctl + 1) != 0u;
   if (warp < nw - 1) {
     for (int k = warp; k < R1; k += nw - 1) {
-      RowStat rs = combine_row(a.part + ((int64_t)b * R1 + k) * a.nvt * 2, a.nvt * 2, nullptr);
+      RowStat rs = combine_row(a.part + ((int64_t)b * R1 + k) * a.nslot * 2, a.nslot * 2, nullptr);
       if (err) {
         rs.bits |= kRowTimeout | kRowNaN;
         rs.s = CUDART_NAN;
@@ -688,8 +785,8 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
   if (st.mode == kDrawSampleRow && st.pos == gamma) {
     // bonus token: merge the per-tile top-2 of row p_gamma
     Cand2 t{cand_empty(), cand_empty()};
-    const LmCand* bp = a.bon + (int64_t)b * a.nvt * 4;
-    for (int j = threadIdx.x; j < 2 * a.nvt; j += blockDim.x) {
+    const LmCand* bp = a.bon + (int64_t)b * a.nslot * 4;
+    for (int j = threadIdx.x; j < 2 * a.nslot; j += blockDim.x) {
       cand_insert(t, bp[2 * j]);
       cand_insert(t, bp[2 * j + 1]);
     }
@@ -739,9 +836,9 @@ __global__ void __launch_bounds__(256) k_lm_merge(LmArgs a) {
   const int b = a.slot_b[slot];
   const DrawState st = a.state[b];
   const bool resid = st.mode == kDrawResidual;
-  const LmCand* rp = a.res + (int64_t)slot * a.nvt * 8;
+  const LmCand* rp = a.res + (int64_t)slot * a.nslot * 8;
   Cand2 tr{cand_empty(), cand_empty()}, tp{cand_empty(), cand_empty()};
-  for (int j = threadIdx.x; j < 2 * a.nvt; j += blockDim.x) {
+  for (int j = threadIdx.x; j < 2 * a.nslot; j += blockDim.x) {
     cand_insert(tr, rp[4 * j]);
     cand_insert(tr, rp[4 * j + 1]);
     cand_insert(tp, rp[4 * j + 2]);
@@ -955,6 +1052,7 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   cudaError_t e = cudaMemsetAsync(a.ctl, 0, 4 * sizeof(uint32_t), stream);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   const unsigned grid = (unsigned)(pl.nvt < dev->sms ? pl.nvt : dev->sms);
+  a.nslot = a2.nslot = (int)grid;
   mark(0, stream);
   k_lm<1><<<grid, kLmThreads, smem1, stream>>>(hT, WT, hD, WD, a);
   mark(1, stream);

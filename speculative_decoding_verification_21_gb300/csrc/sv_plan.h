@@ -141,7 +141,8 @@ inline LmPlan make_lm_plan(int B, int gamma, int64_t V) {
   const size_t rows = (size_t)B * p.R1;
   size_t o = 0;
   p.off_ctl = o;    o = align_up(o + 4 * sizeof(uint32_t));
-  // two partials per row and tile (the two column halves of the epilogue)
+  // two partials per row and CTA of the GEMM passes (the two column halves of
+  // the epilogue); there are at most as many CTAs as vocabulary tiles
   p.off_part = o;   o = align_up(o + 8 * rows * p.nvt * 2);
   p.off_zat = o;    o = align_up(o + sizeof(float) * rows);
   p.off_state = o;  o = align_up(o + sizeof(DrawState) * (size_t)B);
