@@ -16,17 +16,17 @@
 //                hold a 128-wide hidden block of both, warp 1 issues
 //                tcgen05.mma into one of two tensor-memory accumulators, and
 //                warps 3-10 drain the other (tcgen05.ld): per-row online
-//                softmax statistics carried over the CTA's tiles, z at each
-//                draft token, and the top-2 Gumbel-max keys of the bonus row
-//                p_gamma; one partial per row and CTA.
+//                softmax statistics carried over the CTA's tiles and z at each
+//                draft token; one partial per row and CTA.
 //   k_lm_finish  one CTA per batch row: row combine and the decision exactly as
-//                for given logits, the bonus draw when all drafts are accepted,
-//                and otherwise a compact copy of the two hidden rows at the
-//                first rejection.
+//                for given logits, then a compact copy of the hidden rows of
+//                the row to draw from: the residual at the first rejection,
+//                or p_gamma after a clean sweep.
 //   k_lm<2>      the same GEMM for the compact rows only (tiles in reverse
 //                order), target and draft blocks side by side in tensor
-//                memory; the epilogue keeps the top-2 keys of the residual
-//                max(0, p_n - q_n) and of p_n over the CTA's tiles.
+//                memory.  The compact rows are copied into the row tile up to
+//                four times so that all eight epilogue warps share the keys:
+//                top-2 of the residual max(0, p_n - q_n) and of p_n.
 //   k_lm_merge   one CTA per compact row: merge, re-decide near ties in double,
 //                fall back to p_n for an empty residual, emit.
 //
@@ -76,14 +76,14 @@ struct LmArgs {
   int Ht, Hd;
   int box_t, box_d;    // h rows per tensor copy: rows rounded up to 8 (pass 2: compact rows)
   int perm_t;          // target rows in smem are position-major (row i*B + b), else b*(gamma+1) + i
+  int rep, rstride;    // pass 2: copies of the compact rows in the row tile, rows apart
   int nstages;         // ring stages (h tiles and W tile per stage)
   int a_half;          // bytes of the h tile of one 64-wide span (box rows x 128)
   float temperature;
   uint64_t seed, round;
   float2* part;        // [B*R1][nslot][2] (max, sum) per row, CTA and column half
   float* zat;          // [B*R1] logit at the row's draft token
-  LmCand* bon;         // [B][nslot][2][2] bonus-row top-2 per CTA and column half
-  LmCand* res;         // [B][nslot][2][4] residual top-2, then p_n top-2, per compact row
+  LmCand* res;         // [B][nslot][4] residual top-2, then p_n top-2, per compact row
   DrawState* state;    // [B]
   int* slot_b;         // [B] batch row of each compact row
   uint32_t* ctl;       // count, pass-1 error, pass-2 error
@@ -339,10 +339,9 @@ __device__ __forceinline__ RowId row_id(const LmArgs& a, int side, int r) {
 }
 
 // What a pass-1 epilogue thread carries over the vocabulary tiles of its CTA:
-// the online (max, sum) of each of its rows and the bonus-row top-2.
+// the online (max, sum) of each of its rows.
 struct Pass1Carry {
   float mc[2][2], s[2][2];  // [side][row tile]
-  Cand2 bon[2];             // [row tile] (target side)
 };
 
 __device__ __forceinline__ void carry_init(Pass1Carry& cy) {
@@ -353,16 +352,15 @@ __device__ __forceinline__ void carry_init(Pass1Carry& cy) {
       cy.mc[sd][m] = -kInf;
       cy.s[sd][m] = 0.0f;
     }
-  cy.bon[0] = cy.bon[1] = Cand2{cand_empty(), cand_empty()};
 }
 
 // Pass-1 epilogue of one job (SIDE 0 target rows, 1 draft rows) for this warp's
 // lane quadrant and column half (two 32-column chunks of the tile).
 template <int SIDE>
 __device__ __forceinline__ void epilogue_pass1(const LmArgs& a, int t, uint32_t tacc, int quad,
-                                               int half, const PhiloxKeys& pk, Pass1Carry& cy) {
+                                               int half, Pass1Carry& cy) {
   const int lane = threadIdx.x & 31;
-  const int gamma = a.gamma, R1 = 2 * gamma + 1, V = a.V;
+  const int R1 = 2 * a.gamma + 1, V = a.V;
   const int M = SIDE ? a.Md : a.Mt;
   const int box = SIDE ? a.box_d : a.box_t;
   const int v0 = t * kLmTileN;
@@ -380,9 +378,7 @@ __device__ __forceinline__ void epilogue_pass1(const LmArgs& a, int t, uint32_t 
     const int r = side_row(a, SIDE, m, quad, lane);
     if (r < 0) continue;
     const RowId id = row_id(a, SIDE, r);
-    const bool bonus = (SIDE == 0) && id.k == gamma;
     const int64_t grow = (int64_t)id.b * R1 + id.k;
-    Cand2 top[2] = {Cand2{cand_empty(), cand_empty()}, Cand2{cand_empty(), cand_empty()}};
 #pragma unroll
     for (int c2 = 0; c2 < 2; ++c2) {
       const int vb = v0 + half * 64 + c2 * 32;
@@ -404,30 +400,6 @@ __device__ __forceinline__ void epilogue_pass1(const LmArgs& a, int t, uint32_t 
         for (int e = 0; e < 32; ++e) g = (e == id.x - vb) ? f[e] : g;
         a.zat[grow] = g;
       }
-      if (bonus) {
-#pragma unroll
-        for (int g4 = 0; g4 < 8; ++g4) {
-          const int v = vb + 4 * g4;
-          if (v >= V) break;
-          const uint4 rnd = philox_rk(sv_counter((uint32_t)(v >> 2), 1u, (uint32_t)gamma,
-                                                 (uint32_t)id.b, a.round),
-                                      pk);
-          const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float z = f[4 * g4 + e];
-            const float key = fmaf(z, c, -__log2f(neglog2_u(rr[e])));
-            cand_insert(top[e & 1], LmCand{key, v + e, z, 0.0f});
-          }
-        }
-      }
-    }
-    if (SIDE == 0 && bonus) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        cand_insert(cy.bon[m], top[j].a);
-        cand_insert(cy.bon[m], top[j].b);
-      }
     }
   }
 }
@@ -445,28 +417,37 @@ __device__ __forceinline__ void pass1_flush(const LmArgs& a, const Pass1Carry& c
       if (r < 0) continue;
       const RowId id = row_id(a, sd, r);
       const int64_t grow = (int64_t)id.b * R1 + id.k;
-      const int64_t slot = (grow * a.nslot + blockIdx.x) * 2 + half;
-      a.part[slot] = make_float2(cy.mc[sd][m], cy.s[sd][m]);
-      if (sd == 0 && id.k == a.gamma) {
-        LmCand* o = a.bon + (((int64_t)id.b * a.nslot + blockIdx.x) * 2 + half) * 2;
-        o[0] = cy.bon[m].a;
-        o[1] = cy.bon[m].b;
-      }
+      a.part[(grow * a.nslot + blockIdx.x) * 2 + half] = make_float2(cy.mc[sd][m], cy.s[sd][m]);
     }
 }
 
+// Where a pass-2 epilogue warp works.  The compact rows sit in the row tile
+// `rep` times (copy c at lanes c*rstride ..), so that every lane quadrant holds
+// rows; copy c covers the tile's columns [c*128/rep, (c+1)*128/rep), split
+// between the quadrant's two warps.
+struct P2Slice {
+  int copy, row0, ncol, col0;
+};
+__device__ __forceinline__ P2Slice pass2_slice(const LmArgs& a, int quad, int half) {
+  P2Slice sl;
+  sl.copy = (32 * quad) / a.rstride;
+  sl.row0 = 32 * quad - sl.copy * a.rstride;
+  sl.ncol = 64 / a.rep;
+  sl.col0 = sl.copy * (kLmTileN / a.rep) + half * sl.ncol;
+  return sl;
+}
+
 // Pass-2 epilogue of one job (compact rows; target at column 0, draft at 128):
-// the residual top-2 `tr` and the p_n top-2 `tp` of this thread's row, carried
-// over the CTA's tiles.
+// the residual top-2 `tr` and the p_n top-2 `tp` of this thread's row over its
+// column slice, carried over the CTA's tiles.
 __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t tacc, int quad,
                                                int half, int rows, const PhiloxKeys& pk,
                                                Cand2* tr, Cand2* tp) {
   const int lane = threadIdx.x & 31;
   const int V = a.V;
-  const int rb = 32 * quad;
-  if (rb >= rows) return;  // warp-uniform
-  const uint32_t ta = tacc + ((uint32_t)(32 * quad) << 16) + (uint32_t)(half * 64);
-  const int r = rb + lane;
+  const P2Slice sl = pass2_slice(a, quad, half);
+  if (sl.row0 >= rows) return;  // warp-uniform
+  const int r = sl.row0 + lane;
   const bool rv = r < rows;
   int b = 0;
   DrawState st{};
@@ -475,37 +456,40 @@ __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t 
     st = a.state[b];
   }
   const bool resid = st.mode == kDrawResidual;
-  const int v0 = t * kLmTileN + half * 64;
+  const uint32_t ta = tacc + ((uint32_t)(32 * quad) << 16) + (uint32_t)sl.col0;
 #pragma unroll 1
-  for (int c2 = 0; c2 < 2; ++c2) {
-    uint32_t rt[32], rd[32];
-    tmem_ld32_async(ta + (uint32_t)(c2 * 32), rt);
-    tmem_ld32_async(ta + (uint32_t)(kLmTileN + c2 * 32), rd);
+  for (int c16 = 0; c16 < sl.ncol; c16 += 16) {
+    uint32_t rt[16], rd[16];
+    __syncwarp();
+    tmem_ld16_async(ta + (uint32_t)c16, rt);
+    tmem_ld16_async(ta + (uint32_t)(kLmTileN + c16), rd);
     tmem_wait_ld();
-    const int vb = v0 + c2 * 32;
-    if (!rv || vb >= V) continue;
+    const int vb = t * kLmTileN + sl.col0 + c16;
+    if (rv && vb < V) {
 #pragma unroll
-    for (int g4 = 0; g4 < 8; ++g4) {
-      const int v = vb + 4 * g4;
-      if (v >= V) break;
-      const uint4 rnd =
-          philox_rk(sv_counter((uint32_t)(v >> 2), 1u, (uint32_t)st.pos, (uint32_t)b, a.round), pk);
-      const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+      for (int g4 = 0; g4 < 4; ++g4) {
+        const int v = vb + 4 * g4;
+        if (v >= V) break;
+        const uint4 rnd = philox_rk(
+            sv_counter((uint32_t)(v >> 2), 1u, (uint32_t)st.pos, (uint32_t)b, a.round), pk);
+        const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float zt = __uint_as_float(rt[4 * g4 + e]);
-        const float zd = __uint_as_float(rd[4 * g4 + e]);
-        const float lE = __log2f(neglog2_u(rr[e]));
-        const float kp = fmaf(zt, st.c, -st.mct) - lE;
-        if (zt > -kInf) cand_insert(tp[e & 1], LmCand{kp, v + e, zt, zd});
-        if (resid) {
-          // x = log2(q/p); p > q iff x < 0; weight p - q = p (1 - 2^x)
-          const float xx = fmaf(zd - zt, st.c, st.K);
-          if (xx < 0.0f) {
-            const float y = xx * kLn2;
-            const float ser = -y * fmaf(y, fmaf(y, fmaf(y, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
-            const float om = (xx > -0.125f) ? ser : 1.0f - ex2(xx);
-            cand_insert(tr[e & 1], LmCand{kp + __log2f(om), v + e, zt, zd});
+        for (int e = 0; e < 4; ++e) {
+          const float zt = __uint_as_float(rt[4 * g4 + e]);
+          const float zd = __uint_as_float(rd[4 * g4 + e]);
+          const float lE = __log2f(neglog2_u(rr[e]));
+          const float kp = fmaf(zt, st.c, -st.mct) - lE;
+          if (zt > -kInf) cand_insert(tp[e & 1], LmCand{kp, v + e, zt, zd});
+          if (resid) {
+            // x = log2(q/p); p > q iff x < 0; weight p - q = p (1 - 2^x)
+            const float xx = fmaf(zd - zt, st.c, st.K);
+            if (xx < 0.0f) {
+              const float y = xx * kLn2;
+              const float ser =
+                  -y * fmaf(y, fmaf(y, fmaf(y, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
+              const float om = (xx > -0.125f) ? ser : 1.0f - ex2(xx);
+              cand_insert(tr[e & 1], LmCand{kp + __log2f(om), v + e, zt, zd});
+            }
           }
         }
       }
@@ -513,16 +497,38 @@ __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t 
   }
 }
 
+// One candidate set per compact row and CTA: the slices of a row are merged
+// through shared memory (the ring, idle once the last job is drained) by the
+// 256 epilogue threads, then written to res[(row * nslot + cta) * 4 ..].
 __device__ __forceinline__ void pass2_flush(const LmArgs& a, int quad, int half, int rows,
-                                            const Cand2* tr, const Cand2* tp) {
-  const int r = 32 * quad + (threadIdx.x & 31);
-  if (r >= rows) return;
-  const Cand2 r2 = merge2(tr), p2 = merge2(tp);
-  LmCand* o = a.res + (((int64_t)r * a.nslot + blockIdx.x) * 2 + half) * 4;
-  o[0] = r2.a;
-  o[1] = r2.b;
-  o[2] = p2.a;
-  o[3] = p2.b;
+                                            const Cand2* tr, const Cand2* tp, LmCand* sc) {
+  const int nsl = 2 * a.rep;
+  const P2Slice sl = pass2_slice(a, quad, half);
+  const int r = sl.row0 + (threadIdx.x & 31);
+  if (r < rows) {
+    const Cand2 r2 = merge2(tr), p2 = merge2(tp);
+    LmCand* o = sc + ((size_t)r * nsl + sl.copy * 2 + half) * 4;
+    o[0] = r2.a;
+    o[1] = r2.b;
+    o[2] = p2.a;
+    o[3] = p2.b;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+  for (int rr = (int)threadIdx.x - 3 * 32; rr < rows; rr += 32 * kEpiWarps) {
+    Cand2 xr{cand_empty(), cand_empty()}, xp{cand_empty(), cand_empty()};
+    for (int j = 0; j < nsl; ++j) {
+      const LmCand* q = sc + ((size_t)rr * nsl + j) * 4;
+      cand_insert(xr, q[0]);
+      cand_insert(xr, q[1]);
+      cand_insert(xp, q[2]);
+      cand_insert(xp, q[3]);
+    }
+    LmCand* o = a.res + ((int64_t)rr * a.nslot + blockIdx.x) * 4;
+    o[0] = xr.a;
+    o[1] = xr.b;
+    o[2] = xp.a;
+    o[3] = xp.b;
+  }
 }
 
 template <int PASS>
@@ -605,14 +611,17 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                 tma_load_2d_hint(wst, q.bmap, v0, k0, full + r.i, pol);
                 tma_load_2d_hint(wst + kWHalf, q.bmap, v0 + kLmTileN / 2, k0, full + r.i, pol);
               } else {
-                mbar_arrive_expect_tx(full + r.i, (uint32_t)(2 * q.rows * kKAtom * 2));
+                // pass 2: `rep` copies of the compact rows, `rstride` rows apart
+                const int rep = (PASS == 2) ? a.rep : 1;
+                mbar_arrive_expect_tx(full + r.i, (uint32_t)(rep * 2 * q.rows * kKAtom * 2));
                 for (int h = 0; h < 2; ++h) {
-                  if (q.perm)
-                    tma_load_3d_hint(st + (size_t)h * a.a_half, q.amap, k0 + h * kKAtom, 0, 0,
-                                     full + r.i, pol);
-                  else
-                    tma_load_2d_hint(st + (size_t)h * a.a_half, q.amap, k0 + h * kKAtom, 0,
-                                     full + r.i, pol);
+                  for (int cp = 0; cp < rep; ++cp) {
+                    uint8_t* dst = st + (size_t)h * a.a_half + (size_t)cp * a.rstride * (kKAtom * 2);
+                    if (q.perm)
+                      tma_load_3d_hint(dst, q.amap, k0 + h * kKAtom, 0, 0, full + r.i, pol);
+                    else
+                      tma_load_2d_hint(dst, q.amap, k0 + h * kKAtom, 0, full + r.i, pol);
+                  }
                 }
               }
               r.next(nst);
@@ -703,9 +712,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         const int tv = vocab_tile<PASS>(t, nvt);
         if (PASS == 1) {
           if (job == 0)
-            epilogue_pass1<0>(a, tv, tacc, quad, half, pk, cy);
+            epilogue_pass1<0>(a, tv, tacc, quad, half, cy);
           else
-            epilogue_pass1<1>(a, tv, tacc, quad, half, pk, cy);
+            epilogue_pass1<1>(a, tv, tacc, quad, half, cy);
         } else {
           epilogue_pass2(a, tv, tacc, quad, half, rows2, pk, tr, tp);
         }
@@ -719,7 +728,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     if (PASS == 1)
       pass1_flush(a, cy, quad, half);
     else
-      pass2_flush(a, quad, half, rows2, tr, tp);
+      pass2_flush(a, quad, half, rows2, tr, tp, reinterpret_cast<LmCand*>(ring));
   }
 
   if (threadIdx.x == 0 && *abort_flag) atomicOr(a.ctl + (PASS == 1 ? 1 : 2), 1u);
@@ -738,7 +747,6 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = (int)(blockDim.x >> 5);
   __shared__ RowStat srs[2 * 32 + 1];
   __shared__ DraftAt sda[32];
-  __shared__ Cand2 scand[32];
   __shared__ int s_slot;
   pdl_wait();  // partials of the GEMM pass
   pdl_launch_dependents();
@@ -782,31 +790,8 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
   __syncthreads();
   const DrawState st = a.state[b];
   if (st.mode == kDrawDone) return;
-  if (st.mode == kDrawSampleRow && st.pos == gamma) {
-    // bonus token: merge the per-tile top-2 of row p_gamma
-    Cand2 t{cand_empty(), cand_empty()};
-    const LmCand* bp = a.bon + (int64_t)b * a.nslot * 4;
-    for (int j = threadIdx.x; j < 2 * a.nslot; j += blockDim.x) {
-      cand_insert(t, bp[2 * j]);
-      cand_insert(t, bp[2 * j + 1]);
-    }
-    t = block_cand2(t, scand);
-    if (threadIdx.x == 0) {
-      const double invT = (double)st.invT;
-      int tk = redecide(t, [&](const LmCand& c) {
-        return (double)c.zt * invT + gumbel_f64(c.idx, gamma, b, a.seed, a.round);
-      });
-      int fl = st.flags;
-      if (tk < 0 || tk >= a.V) {
-        tk = 0;
-        fl |= SV_FLAG_ZERO_MASS;
-      }
-      a.out_tokens[(int64_t)b * (gamma + 1) + gamma] = tk;
-      if (a.out_flags) a.out_flags[b] = (uint8_t)fl;
-    }
-    return;
-  }
-  // a draw over a full row at position n: queue the two hidden rows for pass 2
+  // a draw over a full row at position n (the residual at the first rejection,
+  // or p_gamma after a clean sweep): queue its hidden rows for pass 2
   if (threadIdx.x == 0) {
     const int slot = (int)atomicAdd(a.ctl, 1u);
     a.slot_b[slot] = b;
@@ -816,11 +801,16 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
   const int slot = s_slot;
   const int n = st.pos;
   const uint4* srct = reinterpret_cast<const uint4*>(a.h_t + ((int64_t)b * (gamma + 1) + n) * a.Ht);
-  const uint4* srcd = reinterpret_cast<const uint4*>(a.h_d + ((int64_t)b * gamma + n) * a.Hd);
   uint4* dt = reinterpret_cast<uint4*>(a.c_t + (int64_t)slot * a.Ht);
   uint4* dd = reinterpret_cast<uint4*>(a.c_d + (int64_t)slot * a.Hd);
   for (int j = threadIdx.x; j < a.Ht / 8; j += blockDim.x) dt[j] = __ldg(srct + j);
-  for (int j = threadIdx.x; j < a.Hd / 8; j += blockDim.x) dd[j] = __ldg(srcd + j);
+  if (n < gamma) {
+    const uint4* srcd = reinterpret_cast<const uint4*>(a.h_d + ((int64_t)b * gamma + n) * a.Hd);
+    for (int j = threadIdx.x; j < a.Hd / 8; j += blockDim.x) dd[j] = __ldg(srcd + j);
+  } else {
+    // p_gamma has no draft row: zeros (its draft logits are never read)
+    for (int j = threadIdx.x; j < a.Hd / 8; j += blockDim.x) dd[j] = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -836,9 +826,9 @@ __global__ void __launch_bounds__(256) k_lm_merge(LmArgs a) {
   const int b = a.slot_b[slot];
   const DrawState st = a.state[b];
   const bool resid = st.mode == kDrawResidual;
-  const LmCand* rp = a.res + (int64_t)slot * a.nslot * 8;
+  const LmCand* rp = a.res + (int64_t)slot * a.nslot * 4;
   Cand2 tr{cand_empty(), cand_empty()}, tp{cand_empty(), cand_empty()};
-  for (int j = threadIdx.x; j < 2 * a.nslot; j += blockDim.x) {
+  for (int j = threadIdx.x; j < a.nslot; j += blockDim.x) {
     cand_insert(tr, rp[4 * j]);
     cand_insert(tr, rp[4 * j + 1]);
     cand_insert(tp, rp[4 * j + 2]);
@@ -1010,7 +1000,6 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   a.round = round;
   a.part = reinterpret_cast<float2*>(ws + pl.off_part);
   a.zat = reinterpret_cast<float*>(ws + pl.off_zat);
-  a.bon = reinterpret_cast<LmCand*>(ws + pl.off_bon);
   a.res = reinterpret_cast<LmCand*>(ws + pl.off_res);
   a.state = reinterpret_cast<DrawState*>(ws + pl.off_state);
   a.slot_b = reinterpret_cast<int*>(ws + pl.off_slot);
@@ -1033,11 +1022,13 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   size_t smem1 = 0, smem2 = 0;
   ring_config(a, a.box_t > a.box_d ? a.box_t : a.box_d, &smem1);
   a2.box_t = a2.box_d = round8(B);
-  ring_config(a2, a2.box_t, &smem2);
+  a2.rep = (B <= 32) ? 4 : (B <= 64 ? 2 : 1);
+  a2.rstride = kTileM / a2.rep;
+  ring_config(a2, a2.rep > 1 ? kTileM : a2.box_t, &smem2);
 
   CUtensorMap hT, WT, hD, WD, cT, cD;
-  // target rows position-major (all batch rows of position 0, then 1, ...), so
-  // the bonus rows p_gamma share warps; the plain order if the map is refused
+  // target rows position-major (all batch rows of position 0, then 1, ...);
+  // the plain order if the map is refused
   a.perm_t = encode_bf16_pos_major(&hT, h_target, B, gamma + 1, Ht) ? 1 : 0;
   if (!a.perm_t &&
       !encode_bf16(&hT, h_target, (uint64_t)a.Mt, (uint64_t)Ht, kKAtom, (uint32_t)a.box_t))

@@ -129,7 +129,7 @@ struct LmPlan {
   int R1 = 0;   // 2*gamma+1 logit rows per batch row
   int nvt = 0;  // vocabulary tiles
   // ctl: [0] compact-row count, [1] pass-1 error, [2] pass-2 error (zeroed per call)
-  size_t off_ctl = 0, off_part = 0, off_zat = 0, off_state = 0, off_slot = 0, off_bon = 0,
+  size_t off_ctl = 0, off_part = 0, off_zat = 0, off_state = 0, off_slot = 0,
          off_res = 0, off_ct = 0, off_cd = 0, total = 0;
 };
 
@@ -147,8 +147,7 @@ inline LmPlan make_lm_plan(int B, int gamma, int64_t V) {
   p.off_zat = o;    o = align_up(o + sizeof(float) * rows);
   p.off_state = o;  o = align_up(o + sizeof(DrawState) * (size_t)B);
   p.off_slot = o;   o = align_up(o + sizeof(int) * (size_t)B);
-  p.off_bon = o;    o = align_up(o + 2 * sizeof(LmCand) * (size_t)B * p.nvt * 2);
-  p.off_res = o;    o = align_up(o + 4 * sizeof(LmCand) * (size_t)B * p.nvt * 2);
+  p.off_res = o;    o = align_up(o + 4 * sizeof(LmCand) * (size_t)B * p.nvt);
   p.off_ct = o;     o = align_up(o + 2 * (size_t)B * kLmMaxHidden);
   p.off_cd = o;     o = align_up(o + 2 * (size_t)B * kLmMaxHidden);
   p.total = o;
