@@ -11,9 +11,9 @@
 //   k_lm<1>      persistent, one CTA per SM.  Vocabulary tiles of 128 entries
 //                are dealt round-robin; for each tile the CTA computes the
 //                target block (B(gamma+1) token rows x 128) and then the draft
-//                block (B gamma rows x 128).  Warps 0 and 2 stream W and h
-//                with tensor copies into one shared-memory ring whose stages
-//                hold a 128-wide hidden block of both, warp 1 issues
+//                block (B gamma rows x 128).  Warps 0 and 2 stream W (from
+//                HBM) and h (from L2) with tensor copies into two shared-
+//                memory rings, a 128-wide hidden block per stage, warp 1 issues
 //                tcgen05.mma into one of two tensor-memory accumulators, and
 //                warps 3-10 drain the other (tcgen05.ld): per-row online
 //                softmax statistics carried over the CTA's tiles and z at each
@@ -61,7 +61,9 @@ constexpr int kEpiWarps = 8;     // two per tensor-memory lane quadrant, each ha
 constexpr int kLmThreads = 32 * (3 + kEpiWarps);  // W producer, MMA issuer, h producer, epilogue
 constexpr int kTmemCols = 512;   // two accumulators of 256 columns
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr int kMaxStages = 8;
+constexpr int kMaxWStages = 8;  // W-ring slots
+constexpr int kHStagesPass2 = 3;  // h-ring slots of the recompute pass (small h tiles)
+constexpr int kMaxRep = 2;      // copies of the compact rows in the recompute pass
 constexpr size_t kSmemBudget = 227 * 1024;  // dynamic shared memory of one CTA
 constexpr size_t kSmemFixed = 1024 + 512;   // 1024-byte alignment slack + barriers
 
@@ -77,8 +79,8 @@ struct LmArgs {
   int box_t, box_d;    // h rows per tensor copy: rows rounded up to 8 (pass 2: compact rows)
   int perm_t;          // target rows in smem are position-major (row i*B + b), else b*(gamma+1) + i
   int rep, rstride;    // pass 2: copies of the compact rows in the row tile, rows apart
-  int nstages;         // ring stages (h tiles and W tile per stage)
-  int a_half;          // bytes of the h tile of one 64-wide span (box rows x 128)
+  int nw, nh;          // W-ring and h-ring slots (nw >= nh)
+  int a_half;          // bytes of the h tile of one 64-wide span (rows x 128)
   float temperature;
   uint64_t seed, round;
   float2* part;        // [B*R1][nslot][2] (max, sum) per row, CTA and column half
@@ -254,8 +256,9 @@ __device__ __forceinline__ int vocab_tile(int t, int nvt) {
   return PASS == 2 ? nvt - 1 - t : t;
 }
 
-// Stage index and phase of a ring of n stages.
-struct Ring {
+// Slot index and phase of a ring of n slots, advanced stage by stage (no
+// division in the issue loops).
+struct Slot {
   uint32_t i = 0, ph = 0;
   __device__ __forceinline__ void next(uint32_t n) {
     if (++i == n) {
@@ -422,9 +425,9 @@ __device__ __forceinline__ void pass1_flush(const LmArgs& a, const Pass1Carry& c
 }
 
 // Where a pass-2 epilogue warp works.  The compact rows sit in the row tile
-// `rep` times (copy c at lanes c*rstride ..), so that every lane quadrant holds
-// rows; copy c covers the tile's columns [c*128/rep, (c+1)*128/rep), split
-// between the quadrant's two warps.
+// `rep` times (copy c at lanes c*rstride ..), so that up to four lane quadrants
+// hold rows; copy c covers the tile's columns [c*128/rep, (c+1)*128/rep), split
+// between the quadrant's two warps.  Quadrants past the last copy stay idle.
 struct P2Slice {
   int copy, row0, ncol, col0;
 };
@@ -446,7 +449,7 @@ __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t 
   const int lane = threadIdx.x & 31;
   const int V = a.V;
   const P2Slice sl = pass2_slice(a, quad, half);
-  if (sl.row0 >= rows) return;  // warp-uniform
+  if (sl.copy >= a.rep || sl.row0 >= rows) return;  // warp-uniform
   const int r = sl.row0 + lane;
   const bool rv = r < rows;
   int b = 0;
@@ -505,7 +508,7 @@ __device__ __forceinline__ void pass2_flush(const LmArgs& a, int quad, int half,
   const int nsl = 2 * a.rep;
   const P2Slice sl = pass2_slice(a, quad, half);
   const int r = sl.row0 + (threadIdx.x & 31);
-  if (r < rows) {
+  if (sl.copy < a.rep && r < rows) {
     const Cand2 r2 = merge2(tr), p2 = merge2(tp);
     LmCand* o = sc + ((size_t)r * nsl + sl.copy * 2 + half) * 4;
     o[0] = r2.a;
@@ -544,25 +547,30 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     if (rows2 <= 0) return;  // nothing rejected this round (uniform over the grid)
   }
   pdl_launch_dependents();
-  // Shared memory: a ring of stages [h span 0 | h span 1 | W vocab half 0 |
-  // W vocab half 1], then barriers.  An MMA reads a 128-row window from the
-  // start of its h tile; rows past the copied box (the rest of the stage or the
-  // next stage) only feed accumulator rows that are never read.
-  const uint32_t nst = (uint32_t)a.nstages;
-  const size_t stage_bytes = (size_t)2 * a.a_half + kWBytes;
+  // Shared memory: the h ring (nh slots of [span 0 | span 1]), the W ring (nw
+  // slots of [vocab half 0 | vocab half 1]), then barriers.  Stage k of the
+  // K loop uses h slot k % nh and W slot k % nw, and the W slot's barriers serve
+  // the stage: `full` completes when the copies of both producers have landed,
+  // `empty` when the MMAs that read the stage are done (the h producer reuses
+  // slot k % nh once stage k - nh is empty).  An MMA reads a 128-row window from
+  // the start of its h span; rows past the copied box only feed accumulator rows
+  // that are never read.
+  const uint32_t nw = (uint32_t)a.nw, nh = (uint32_t)a.nh;
+  const size_t hslot = (size_t)2 * a.a_half;
   const uint32_t base_u32 = smem_u32(smem_raw);
-  uint8_t* ring = smem_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)nst * stage_bytes);
-  uint64_t* empty = full + kMaxStages;
-  uint64_t* accf = empty + kMaxStages;  // [2]
-  uint64_t* acce = accf + 2;            // [2]
+  uint8_t* hring = smem_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
+  uint8_t* wring = hring + (size_t)nh * hslot;
+  uint64_t* full = reinterpret_cast<uint64_t*>(wring + (size_t)nw * kWBytes);
+  uint64_t* empty = full + kMaxWStages;
+  uint64_t* accf = empty + kMaxWStages;  // [2]
+  uint64_t* acce = accf + 2;             // [2]
   uint64_t* fin = acce + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(fin + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (uint32_t s = 0; s < nst; ++s) {
+    for (uint32_t s = 0; s < nw; ++s) {
       mbar_init(full + s, 2);  // both producers
       mbar_init(empty + s, 1);
     }
@@ -590,53 +598,62 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     if (lane == 0) {
       const bool isw = (warp == 0);
       const uint64_t pol = isw ? l2_policy_evict_first() : l2_policy_evict_last();
-      Ring r;
-      uint32_t issued = 0;
+      uint32_t k = 0;  // stage counter
+      Slot w, hs, lag;  // W slot of stage k, h slot of stage k, W slot of stage k - nh
       bool ok = true;
       for (int t = blockIdx.x; ok && t < nvt; t += G) {
         const int v0 = vocab_tile<PASS>(t, nvt) * kLmTileN;
         for (int job = 0; ok && job < Jobs<PASS>::kPerTile; ++job) {
           for (int sg = 0; ok && sg < Jobs<PASS>::nseg(job); ++sg) {
             const Seg q = Jobs<PASS>::seg(job, sg, &mA0, &mB0, &mA1, &mB1, a);
-            for (int kb = 0; kb < q.kblocks; ++kb) {
-              if (!lm_wait(empty + r.i, r.ph ^ 1u, abort_flag)) {
-                ok = false;
-                break;
-              }
-              uint8_t* st = ring + (size_t)r.i * stage_bytes;
+            for (int kb = 0; kb < q.kblocks; ++kb, ++k) {
+              const uint32_t ws = w.i;
               const int k0 = kb * kKBlock;  // spans past the hidden size read as zeros
               if (isw) {
-                uint8_t* wst = st + 2 * (size_t)a.a_half;
-                mbar_arrive_expect_tx(full + r.i, (uint32_t)kWBytes);
-                tma_load_2d_hint(wst, q.bmap, v0, k0, full + r.i, pol);
-                tma_load_2d_hint(wst + kWHalf, q.bmap, v0 + kLmTileN / 2, k0, full + r.i, pol);
+                if (!lm_wait(empty + ws, w.ph ^ 1u, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                uint8_t* wst = wring + (size_t)ws * kWBytes;
+                mbar_arrive_expect_tx(full + ws, (uint32_t)kWBytes);
+                tma_load_2d_hint(wst, q.bmap, v0, k0, full + ws, pol);
+                tma_load_2d_hint(wst + kWHalf, q.bmap, v0 + kLmTileN / 2, k0, full + ws, pol);
               } else {
+                if (k >= nh) {
+                  // stage k - nh, the last to use this h slot, is done
+                  if (!lm_wait(empty + lag.i, lag.ph, abort_flag)) {
+                    ok = false;
+                    break;
+                  }
+                  lag.next(nw);
+                }
+                uint8_t* hst = hring + (size_t)hs.i * hslot;
                 // pass 2: `rep` copies of the compact rows, `rstride` rows apart
                 const int rep = (PASS == 2) ? a.rep : 1;
-                mbar_arrive_expect_tx(full + r.i, (uint32_t)(rep * 2 * q.rows * kKAtom * 2));
+                mbar_arrive_expect_tx(full + ws, (uint32_t)(rep * 2 * q.rows * kKAtom * 2));
                 for (int h = 0; h < 2; ++h) {
                   for (int cp = 0; cp < rep; ++cp) {
-                    uint8_t* dst = st + (size_t)h * a.a_half + (size_t)cp * a.rstride * (kKAtom * 2);
+                    uint8_t* dst = hst + (size_t)h * a.a_half + (size_t)cp * a.rstride * (kKAtom * 2);
                     if (q.perm)
-                      tma_load_3d_hint(dst, q.amap, k0 + h * kKAtom, 0, 0, full + r.i, pol);
+                      tma_load_3d_hint(dst, q.amap, k0 + h * kKAtom, 0, 0, full + ws, pol);
                     else
-                      tma_load_2d_hint(dst, q.amap, k0 + h * kKAtom, 0, full + r.i, pol);
+                      tma_load_2d_hint(dst, q.amap, k0 + h * kKAtom, 0, full + ws, pol);
                   }
                 }
               }
-              r.next(nst);
-              ++issued;
+              w.next(nw);
+              hs.next(nh);
             }
           }
         }
       }
-      drain_ring(full, nst, issued);  // every issued copy has landed before the CTA may exit
+      drain_ring(full, nw, k);  // every issued copy has landed before the CTA may exit
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      Ring r;
+      Slot w, hs;
       int jobi = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < nvt; t += G) {
@@ -652,13 +669,15 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const Seg q = Jobs<PASS>::seg(job, sg, &mA0, &mB0, &mA1, &mB1, a);
             const uint32_t dcol = tbase + (uint32_t)(buf * 256 + q.col);
             for (int kb = 0; kb < q.kblocks; ++kb) {
+              const uint32_t ws = w.i;
               // one wait per stage: the copies of both producers have landed
-              if (!lm_wait(full + r.i, r.ph, abort_flag)) {
+              if (!lm_wait(full + ws, w.ph, abort_flag)) {
                 ok = false;
                 break;
               }
-              const uint32_t sa = smem_u32(ring + (size_t)r.i * stage_bytes);
-              const uint64_t bdesc = umma_smem_desc(sa + 2 * (uint32_t)a.a_half, kWHalf, 1024);
+              const uint32_t sa = smem_u32(hring + (size_t)hs.i * hslot);
+              const uint64_t bdesc =
+                  umma_smem_desc(smem_u32(wring + (size_t)ws * kWBytes), kWHalf, 1024);
               for (int m = 0; m < q.mtiles; ++m) {
                 const uint32_t row0 = m ? (uint32_t)q.start1 : 0u;
 #pragma unroll
@@ -672,8 +691,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                               (kb | h | kk) != 0);
                 }
               }
-              umma_commit(empty + r.i);
-              r.next(nst);
+              umma_commit(empty + ws);
+              w.next(nw);
+              hs.next(nh);
             }
           }
           if (ok) umma_commit(accf + buf);
@@ -728,7 +748,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     if (PASS == 1)
       pass1_flush(a, cy, quad, half);
     else
-      pass2_flush(a, quad, half, rows2, tr, tp, reinterpret_cast<LmCand*>(ring));
+      pass2_flush(a, quad, half, rows2, tr, tp, reinterpret_cast<LmCand*>(hring));
   }
 
   if (threadIdx.x == 0 && *abort_flag) atomicOr(a.ctl + (PASS == 1 ? 1 : 2), 1u);
@@ -940,17 +960,30 @@ bool aligned_to(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p
 
 int round8(int x) { return (x + 7) & ~7; }
 
-// The ring of one pass: as many stages of (two h spans of `box_rows` rows and a
-// 32 KB W tile) as the shared memory holds.  The h spans are at least 1 KB
-// apart-aligned (rows are a multiple of 8); the W tile after them keeps every
-// 128-row MMA window inside the stage.
-void ring_config(LmArgs& a, int box_rows, size_t* smem) {
-  a.a_half = box_rows * kKAtom * 2;
-  const size_t stage = (size_t)2 * a.a_half + kWBytes;
-  int n = (int)((kSmemBudget - kSmemFixed) / stage);
-  n = n > kMaxStages ? kMaxStages : n;
-  a.nstages = n;
-  *smem = kSmemFixed + (size_t)n * stage;
+// The rings of one pass: h slots of two spans of `span_rows` rows, and 32 KB W
+// slots.  nh = 0 gives both rings the same depth (as many stages as fit: the
+// h tiles of the first pass are as large as the W tiles and come from L2 at
+// about the same latency); otherwise nh h slots and as many W slots as the
+// rest of the shared memory holds.  Spans are whole 1 KB swizzle atoms (rows
+// are a multiple of 8).
+bool ring_config(LmArgs& a, int span_rows, int nh, size_t* smem) {
+  a.a_half = span_rows * kKAtom * 2;
+  const size_t hslot = (size_t)2 * a.a_half;
+  const size_t room = kSmemBudget - kSmemFixed;
+  int nw;
+  if (nh == 0) {
+    nh = nw = (int)(room / (hslot + kWBytes));
+  } else {
+    if ((size_t)nh * hslot > room) return false;
+    nw = (int)((room - (size_t)nh * hslot) / kWBytes);
+  }
+  nw = nw > kMaxWStages ? kMaxWStages : nw;
+  nh = nh > nw ? nw : nh;
+  if (nh < 2) return false;
+  a.nh = nh;
+  a.nw = nw;
+  *smem = kSmemFixed + (size_t)nh * hslot + (size_t)nw * kWBytes;
+  return true;
 }
 
 }  // namespace
@@ -1020,11 +1053,14 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   a.box_t = round8(a.Mt);
   a.box_d = round8(a.Md);
   size_t smem1 = 0, smem2 = 0;
-  ring_config(a, a.box_t > a.box_d ? a.box_t : a.box_d, &smem1);
   a2.box_t = a2.box_d = round8(B);
-  a2.rep = (B <= 32) ? 4 : (B <= 64 ? 2 : 1);
-  a2.rstride = kTileM / a2.rep;
-  ring_config(a2, a2.rep > 1 ? kTileM : a2.box_t, &smem2);
+  // copies of the compact rows: one per 32-row-aligned block that fits in 128 lanes
+  a2.rstride = (B + 31) & ~31;
+  a2.rep = kTileM / a2.rstride;
+  a2.rep = a2.rep > kMaxRep ? kMaxRep : a2.rep;
+  if (!ring_config(a, a.box_t > a.box_d ? a.box_t : a.box_d, 0, &smem1) ||
+      !ring_config(a2, a2.rep > 1 ? a2.rep * a2.rstride : a2.box_t, kHStagesPass2, &smem2))
+    return SV_ERR_UNSUPPORTED;
 
   CUtensorMap hT, WT, hD, WD, cT, cD;
   // target rows position-major (all batch rows of position 0, then 1, ...);
