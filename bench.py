@@ -76,7 +76,8 @@ def tensor_peaks():
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture of the same
 # workload (profiles/ holds the summary); None when the kernel changed since.
-SWEEP_TRAFFIC_BYTES = 151462656  # 147779840 read + 3682816 written, profiles/k_sweep_tma_sample_b64.md
+SWEEP_TRAFFIC_BYTES = 151237376  # 147789568 read + 3447808 written, profiles/k_sweep_tma_sample_b64.md
+LMHEAD_PASS1_TRAFFIC_BYTES = 1580866592  # 1577.972 MB read + 2.895 MB written, profiles/k_lm_lmhead.md
 
 
 class ClockSampler:
@@ -488,7 +489,7 @@ def measure_lmhead(L, dev, stream, rank, reps=100):
             raise RuntimeError(sv.status_string(rc))
 
     kms, ms = _kernel_times(L, stream, call, 4, reps)
-    rejected = float((cnt < g).float().mean().item())
+    rejected = float((cnt < g).float().mean().item())  # the rest draw the bonus token
     hbm, kind = peaks()
     tb, ts, tkind = tensor_peaks()
     wbytes = 2 * V * (Ht + Hd)
@@ -500,10 +501,10 @@ def measure_lmhead(L, dev, stream, rank, reps=100):
             "rounds_per_s": 1000.0 / ms, "ms_per_round": ms,
             "kernel_ms": {"k_lm_pass1": kms[0], "k_lm_finish": kms[1], "k_lm_pass2": kms[2],
                           "k_lm_merge": kms[3]},
-            "rows_needing_pass2": rejected,
+            "rows_rejected": rejected,
             "roofline": {"bound": "hbm", "kernel": "k_lm_pass1", "achieved": gbs1, "peak": hbm,
                          "peak_kind": kind, "unit": "GB/s", "frac": gbs1 / hbm,
-                         "algorithmic_bytes": wbytes},
+                         "traffic": LMHEAD_PASS1_TRAFFIC_BYTES, "algorithmic_bytes": wbytes},
             "tensor": {"kernel": "k_lm_pass1", "achieved": tf1, "peak": tb, "peak_kind": tkind,
                        "unit": "TFLOP/s", "frac": tf1 / tb, "algorithmic_flops": flops1},
             "gpu_launches_per_round": 4}
