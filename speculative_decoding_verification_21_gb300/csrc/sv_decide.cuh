@@ -29,7 +29,7 @@ __device__ __forceinline__ const char* row_ptr(const void* zt, const void* zd, i
 }
 
 // --------------------------------------------------------------------------
-// Row combine and decision (k_finish).
+// Row combine and decision (the start of k_draw; k_lm_finish on the fused path).
 // --------------------------------------------------------------------------
 struct SweepCtx {
   const void* zt;
@@ -103,7 +103,9 @@ __device__ __forceinline__ float prob_from(float z, const Exp2& e, const RowStat
 }
 
 // The decision for batch row b (one warp): accept test, prefix, draw set-up.
-// srs[k] holds the statistics of row k of the batch row.
+// srs[k] holds the statistics of row k of the batch row.  With `emit` the
+// warp writes the outputs (prefix, counts, p, q, the draw state, the flags of a
+// finished row); the draw state also goes to *st_out (shared memory) if given.
 // Draft token i of a batch row and the two logits at it.
 struct DraftAt {
   int32_t x;
@@ -112,7 +114,8 @@ struct DraftAt {
 
 template <int DT>
 __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
-                                 const DraftAt* sda) {
+                                 const DraftAt* sda, bool emit = true,
+                                 DrawState* st_out = nullptr) {
   const int lane = threadIdx.x & 31;
   const int gamma = x.gamma;
   const int64_t V = x.V;
@@ -161,8 +164,8 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
     const uint4 rnd = philox4x32_10(sv_counter(0u, 0u, (uint32_t)lane, (uint32_t)b, x.round),
                                     (uint32_t)x.seed, (uint32_t)(x.seed >> 32));
     accept = (sv_u01(rnd.x) <= ratio);
-    if (x.out_p) x.out_p[(int64_t)b * gamma + lane] = (float)P;
-    if (x.out_q) x.out_q[(int64_t)b * gamma + lane] = (float)Q;
+    if (emit && x.out_p) x.out_p[(int64_t)b * gamma + lane] = (float)P;
+    if (emit && x.out_q) x.out_q[(int64_t)b * gamma + lane] = (float)Q;
   }
   const unsigned rej = ~__ballot_sync(0xffffffffu, accept);
   const int n = (rej == 0u) ? 32 : min(__ffs((int)rej) - 1, gamma);
@@ -171,9 +174,11 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
   if (__ballot_sync(0xffffffffu, lane < gamma && lane <= n && qzero)) fl |= SV_FLAG_NONFINITE;
   fl = __reduce_or_sync(0xffffffffu, fl);
   int32_t* tok = x.out_tokens + (int64_t)b * (gamma + 1);
-  if (lane < n) tok[lane] = xi;  // n <= gamma <= 32
-  for (int i = lane; i <= gamma; i += 32)
-    if (i > n) tok[i] = -1;
+  if (emit) {
+    if (lane < n) tok[lane] = xi;  // n <= gamma <= 32
+    for (int i = lane; i <= gamma; i += 32)
+      if (i > n) tok[i] = -1;
+  }
   if (lane == 0) {
     // set up the draw of the target's own token
     const float mct = srs[n].mc;
@@ -214,11 +219,14 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
       }
     }
     st.flags = fl;
-    x.state[b] = st;
-    x.out_counts[b] = n;
-    if (st.mode == kDrawDone) {
-      tok[n] = 0;
-      if (x.out_flags) x.out_flags[b] = (uint8_t)fl;
+    if (st_out) *st_out = st;
+    if (emit) {
+      x.state[b] = st;
+      x.out_counts[b] = n;
+      if (st.mode == kDrawDone) {
+        tok[n] = 0;
+        if (x.out_flags) x.out_flags[b] = (uint8_t)fl;
+      }
     }
   }
 }

@@ -20,11 +20,11 @@ struct DrawArgs {
   int B, gamma;
   int64_t V;
   uint64_t seed, round;
-  const DrawState* state;  // [B]
-  uint32_t* counter;       // [B] CTAs done per batch row
-  uint32_t* work;          // unused by the CTA-per-chunk draw
+  DrawState* state;        // [B] (written by the first draw CTA of each batch row)
+  uint32_t* alpha_cnt;     // [B] counters of the optional overlap kernel, zeroed here
   Top2* part3;             // [B][nsplit3]
   int nsplit3;             // CTAs per batch row
+  int gpc;                 // 4-entry groups per CTA
   int32_t* out_tokens;
   uint8_t* out_flags;
 };

@@ -14,7 +14,8 @@ namespace sv {
 
 constexpr int kThreads = 256;          // threads per CTA for the streaming kernels
 constexpr int64_t kChunkSweep = 8192;  // logits per CTA in the softmax/argmax sweeps
-constexpr int64_t kChunkDraw = 8192;   // vocabulary entries per CTA in the draw pass
+constexpr int64_t kChunkDraw = 8192;   // least vocabulary entries per CTA in the draw pass
+constexpr int kDrawCtasPerSm = 4;      // resident draw CTAs per SM (its launch bounds)
 constexpr size_t kAlign = 256;
 
 // Persistent bulk-copy sweep: warps per CTA, pipeline stages per warp, bytes per chunk.
@@ -68,8 +69,8 @@ struct DrawState {
 struct SamplePlan {
   int R1 = 0;          // logit rows per batch row, 2*gamma+1
   int nsplit1 = 0;     // 8192-logit chunks per row (generic sweep, overlap pass)
-  int nsplit3 = 0;     // CTAs per batch row in the draw pass
-  // counters: [B] draw CTAs, [B] overlap CTAs (zeroed by the finish kernel)
+  int nsplit3 = 0;     // most CTAs per batch row in the draw pass
+  // counters: [B] overlap CTAs (zeroed by the first draw CTA of each batch row)
   size_t off_cnt = 0, cnt_bytes = 0, off_part1 = 0, off_rowstat = 0, off_state = 0,
          off_part3 = 0, off_alpha = 0, total = 0;
 };
@@ -83,7 +84,7 @@ inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
   // per-(row, chunk) partials: enough for the smaller bulk-copy chunks of fp32
   const int64_t nch_max = ceil_div(V, tma_chunk_elems(0));
   size_t o = 0;
-  p.cnt_bytes = sizeof(uint32_t) * (2 * (size_t)B + 1);  // draw, overlap, draw work
+  p.cnt_bytes = sizeof(uint32_t) * (size_t)B;
   p.off_cnt = o;      o = align_up(o + p.cnt_bytes);
   p.off_rowstat = o;  o = align_up(o + sizeof(RowStat) * (size_t)B * p.R1);
   p.off_part1 = o;    o = align_up(o + 8 * (size_t)B * p.R1 * (size_t)nch_max);

@@ -3,7 +3,7 @@
 // One round for B independent batch rows, after Algorithm 1 of "Fast Inference
 // from Transformers via Speculative Decoding" (section "The loop: draft, verify
 // in one pass, keep a prefix") and the course notes "Speculative Decoding"
-// ("The algorithm").  Four kernels per call (five with the optional overlap),
+// ("The algorithm").  Three kernels per call (four with the optional overlap),
 // chained by programmatic dependent launch:
 //
 //   sweep     online softmax statistics of every chunk of all 2*gamma+1 logit
@@ -13,14 +13,14 @@
 //             across warps in batch-row order, through a 3-stage bulk-copy (TMA)
 //             pipeline in shared memory.  k_sweep (any shape): one CTA per
 //             8192-logit chunk with 16-byte vector loads.
-//   k_finish  one CTA per batch row: the row statistics from the chunk
-//             partials, then the decision: p(x_i), q(x_i), u_i, accept iff
-//             u_i <= p/q, first rejection by a warp ballot, the accepted prefix,
-//             and the set-up of the draw.
-//   k_draw    the target's own token -- bonus row p_gamma or residual
-//             max(0, p_n - q_n) -- as a Gumbel-max in the exponential-race form
-//             argmax w_v / E_v (E_v = -log2 u_v, the same argmax as
-//             log w_v + g_v), one CTA per 8192 entries keeping its top-2 keys;
+//   k_draw    one CTA per (batch row, 8192 entries).  Each CTA first takes
+//             its batch row's decision from the chunk partials: the row
+//             statistics, p(x_i), q(x_i), u_i, accept iff u_i <= p/q, first
+//             rejection by a warp ballot (the first CTA of the batch row writes
+//             the prefix and the draw set-up).  Then the target's own token --
+//             bonus row p_gamma or residual max(0, p_n - q_n) -- as a Gumbel-max
+//             in the exponential-race form argmax w_v / E_v (E_v = -log2 u_v,
+//             the same argmax as log w_v + g_v), keeping the CTA's top-2 keys;
 //   k_draw_merge  one CTA per batch row merges them and, when the best two are
 //             within 2^-10, re-decides between them in double with the
 //             oracle-level definition.
@@ -42,48 +42,6 @@
 #include "sv_launch.h"
 
 namespace sv {
-
-// One CTA per batch row: row statistics (one warp per row) while one more warp
-// fetches the draft tokens and their target/draft logits, then the decision.
-template <int DT>
-__global__ void __launch_bounds__(1024) k_finish(SweepCtx x, uint32_t* __restrict__ counters) {
-  const int b = blockIdx.x;
-  const int gamma = x.gamma;
-  const int R1 = 2 * gamma + 1;
-  const int nrw = (int)(blockDim.x >> 5) - 1;  // row warps; the last warp prefetches
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ RowStat srs[65];
-  __shared__ DraftAt sda[32];
-  pdl_launch_dependents();
-  if (warp == nrw) {
-    // independent of the sweep: read before waiting for it
-    if (lane < gamma) {
-      DraftAt d;
-      d.x = __ldg(x.xt + (int64_t)b * gamma + lane);
-      d.zt = d.zd = 0.0f;
-      if (d.x >= 0 && (int64_t)d.x < x.V) {
-        d.zt = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, lane, gamma, x.V), d.x);
-        d.zd = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + lane, gamma, x.V), d.x);
-      }
-      sda[lane] = d;
-    }
-  }
-  pdl_wait();  // the sweep's partials
-  if (threadIdx.x == 0) {  // counters of the draw and overlap kernels that follow
-    counters[b] = 0u;
-    counters[x.B + b] = 0u;
-    if (b == 0) counters[2 * x.B] = 0u;  // the draw's work counter
-  }
-  if (warp < nrw) {
-    for (int k = warp; k < R1; k += nrw) {
-      const RowStat rs = combine_row(x.part + ((int64_t)b * R1 + k) * x.nch, x.nch,
-                                     x.rowstat + (int64_t)b * R1 + k);
-      if (lane == 0) srs[k] = rs;
-    }
-  }
-  __syncthreads();
-  if (warp == 0) decide_batch_row<DT>(x, b, srs, sda);
-}
 
 // --------------------------------------------------------------------------
 // Generic sweep (any V): one CTA per (row, 8192-logit chunk).
@@ -180,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
 // --------------------------------------------------------------------------
 template <int DT>
 __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
-  pdl_launch_dependents();  // the finish kernel may be scheduled now; it waits for us
+  pdl_launch_dependents();  // the draw kernel may be scheduled now; it waits for us
   constexpr int kBytes = (DT == SV_F32) ? 4 : 2;
   constexpr int CH = kSweepChunkBytes / kBytes;  // logits per chunk
   extern __shared__ __align__(128) unsigned char smem[];
@@ -316,17 +274,49 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
 // --------------------------------------------------------------------------
 // Draw of the target's own token.
 // --------------------------------------------------------------------------
-// One CTA per (batch row, kChunkDraw entries): the CTA's top-2 keys of the
-// draw, written to its slot; the merge kernel that follows picks the token.
+// One CTA per (batch row, gpc 4-entry groups).  Every CTA of a batch row first
+// takes the batch row's decision itself from the sweep's partials: one warp
+// per logit row combines its partials, then one warp runs the accept test
+// (the same arithmetic on the same numbers in every CTA, so all agree).  The
+// first CTA of the batch row also writes the row statistics, the accepted
+// prefix, p, q, the count and the draw state.  Then the CTA's top-2 keys of the
+// draw go to its slot; the merge kernel that follows picks the token.
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 4) k_draw(DrawArgs a) {
+__global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, DrawArgs a) {
   const int b = (int)(blockIdx.x / (unsigned)a.nsplit3);
   const int split = (int)(blockIdx.x - (unsigned)b * (unsigned)a.nsplit3);
   const int gamma = a.gamma;
+  const int R1 = 2 * gamma + 1;
   const int64_t V = a.V;
-  pdl_wait();  // the decision's draw states
+  const bool lead = (split == 0);
+  constexpr int kWarps = kThreads / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ RowStat srs[65];
+  __shared__ DraftAt sda[32];
+  __shared__ DrawState s_st;
+  if (warp == kWarps - 1 && lane < gamma) {
+    // independent of the sweep: read before waiting for it
+    DraftAt d;
+    d.x = __ldg(x.xt + (int64_t)b * gamma + lane);
+    d.zt = d.zd = 0.0f;
+    if (d.x >= 0 && (int64_t)d.x < V) {
+      d.zt = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, lane, gamma, V), d.x);
+      d.zd = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + lane, gamma, V), d.x);
+    }
+    sda[lane] = d;
+  }
+  pdl_wait();  // the sweep's partials
   pdl_launch_dependents();
-  const DrawState st = a.state[b];
+  if (lead && threadIdx.x == 0) a.alpha_cnt[b] = 0u;
+  for (int k = warp; k < R1; k += kWarps) {
+    const RowStat rs = combine_row(x.part + ((int64_t)b * R1 + k) * x.nch, x.nch,
+                                   lead ? x.rowstat + (int64_t)b * R1 + k : nullptr);
+    if (lane == 0) srs[k] = rs;
+  }
+  __syncthreads();
+  if (warp == 0) decide_batch_row<DT>(x, b, srs, sda, lead, &s_st);
+  __syncthreads();
+  const DrawState st = s_st;
   if (st.mode == kDrawDone) return;
   const bool resid = (st.mode == kDrawResidual);
   const char* rt = row_ptr<DT>(a.zt, a.zd, b, st.pos, gamma, V);
@@ -334,8 +324,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_draw(DrawArgs a) {
   const bool vec_ok = (V % 4) == 0;  // 4-entry groups start 4-entry aligned in every row
   const int Vi = (int)V;             // V < 2^31
   const int ngroups = (int)ceil_div(V, 4);
-  const int gpc = (int)(kChunkDraw / 4);
-  const int g0 = split * gpc, g1 = min(ngroups, g0 + gpc);
+  const int g0 = split * a.gpc, g1 = min(ngroups, g0 + a.gpc);
   const PhiloxKeys pk = philox_keys(a.seed);
   KI mine = resid ? draw_range<DT, true>(rt, rd, g0, g1, Vi, vec_ok, st, b, pk, a.round)
                   : draw_range<DT, false>(rt, rd, g0, g1, Vi, vec_ok, st, b, pk, a.round);
@@ -513,15 +502,13 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   DrawState* state = reinterpret_cast<DrawState*>(ws + pl.off_state);
   Top2* part3 = reinterpret_cast<Top2*>(ws + pl.off_part3);
   float* apart = reinterpret_cast<float*>(ws + pl.off_alpha);
-  uint32_t* draw_cnt = cnt;
-  uint32_t* alpha_cnt = cnt + B;
-  bool tma = use_tma_sweep(DT, V);
+  uint32_t* alpha_cnt = cnt;
   DeviceInfo* di = nullptr;
-  if (tma) {
+  {
     const cudaError_t e = device_info(&di);
     if (e != cudaSuccess) return e;
-    tma = di->sweep_ctas_per_sm[DT] > 0;
   }
+  const bool tma = use_tma_sweep(DT, V) && di->sweep_ctas_per_sm[DT] > 0;
   const int nch = (int)(tma ? ceil_div(V, tma_chunk_elems(DT)) : ceil_div(V, kChunkSweep));
   SweepCtx sx{zt, zd, xt, B, gamma, V, temperature, row_T, seed, round, nch, part1, rowstat,
               state, out_tokens, out_counts, out_p, out_q, out_flags};
@@ -538,15 +525,21 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
     k_sweep<DT><<<(unsigned)((int64_t)nch * B * R1), kThreads, 0, stream>>>(sx);
   }
   mark(1, stream);
-  const int fw = (R1 < 31 ? R1 : 31) + 1;  // one warp per row, one prefetching
-  cudaError_t e = launch_pdl(k_finish<DT>, dim3((unsigned)B), dim3(32 * fw), 0, stream, sx, cnt);
+  // One resident wave of draw CTAs when the batch allows: every CTA takes its
+  // batch row's decision before drawing, so a second wave would pay that
+  // latency again.  At least kChunkDraw entries per CTA.
+  const int64_t ngroups = ceil_div(V, 4);
+  int64_t nsplit = pl.nsplit3;
+  const int64_t slots = (int64_t)di->sms * kDrawCtasPerSm;
+  if ((int64_t)B * nsplit > slots) nsplit = (slots / B > 1) ? slots / B : 1;
+  const int64_t gpc = ceil_div(ngroups, nsplit);
+  nsplit = ceil_div(ngroups, gpc);  // no CTA without groups
+  DrawArgs da{zt, zd, B, gamma, V, seed, round, state, alpha_cnt, part3, (int)nsplit, (int)gpc,
+              out_tokens, out_flags};
+  cudaError_t e = launch_pdl(k_draw<DT>, dim3((unsigned)(nsplit * B)), dim3(kThreads), 0, stream,
+                             sx, da);
   if (e != cudaSuccess) return e;
   mark(2, stream);
-  DrawArgs da{zt, zd, B, gamma, V, seed, round, state, draw_cnt, cnt + 2 * B, part3, pl.nsplit3,
-              out_tokens, out_flags};
-  e = launch_pdl(k_draw<DT>, dim3((unsigned)((int64_t)pl.nsplit3 * B)), dim3(kThreads), 0, stream,
-                 da);
-  if (e != cudaSuccess) return e;
   e = launch_pdl(k_draw_merge<DT>, dim3((unsigned)B), dim3(kThreads), 0, stream, da);
   if (e != cudaSuccess) return e;
   mark(3, stream);
