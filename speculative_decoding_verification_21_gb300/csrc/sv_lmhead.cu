@@ -24,8 +24,8 @@
 //                or p_gamma after a clean sweep.
 //   k_lm<2>      the same GEMM for the compact rows only (tiles in reverse
 //                order), target and draft blocks side by side in tensor
-//                memory.  The compact rows are copied into the row tile up to
-//                four times so that all eight epilogue warps share the keys:
+//                memory.  The compact rows are copied into the row tile twice
+//                (B <= 64) so that two lane quadrants share the key work:
 //                top-2 of the residual max(0, p_n - q_n) and of p_n.
 //   k_lm_merge   one CTA per compact row: merge, re-decide near ties in double,
 //                fall back to p_n for an empty residual, emit.

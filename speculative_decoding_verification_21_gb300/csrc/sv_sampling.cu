@@ -216,14 +216,25 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
       }
       const uint4* sv = reinterpret_cast<const uint4*>(stage0 + (size_t)s * kSweepChunkBytes);
       float zmax = -kInf, mc = -kInf, sacc = 0.0f;
-      if (pc.j != nch - 1) {
-        chunk_update_full<DT>(sv, lane, c, zmax, mc, sacc);
-      } else {
-        const int nvec = (int)(tail_bytes / 16);
-        uint4 v[8];
+      const bool full = (pc.j != nch - 1);
+      const int nvec = full ? 8 * 32 : (int)(tail_bytes / 16);
+      uint4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (lane + 32 * u < nvec) v[u] = sv[lane + 32 * u];
+      for (int u = 0; u < 8; ++u)
+        if (full || lane + 32 * u < nvec) v[u] = sv[lane + 32 * u];
+      // every lane holds its words: refill the stage before computing on them
+      __syncwarp();
+      if (t + kSweepStages < count) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          issue(s, pi);
+        }
+        advance(pi, step, R1, nch);
+        issued = t + kSweepStages + 1;
+      }
+      if (full) {
+        chunk_update_full<DT>(v, c, zmax, mc, sacc);
+      } else {
         const int nv = (nvec - lane + 31) >> 5;
         float m = -kInf;
 #pragma unroll
@@ -246,15 +257,6 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
           }
           sacc += s0 + s1;
         }
-      }
-      __syncwarp();
-      if (t + kSweepStages < count) {
-        if (lane == 0) {
-          fence_proxy_async_smem();
-          issue(s, pi);
-        }
-        advance(pi, step, R1, nch);
-        issued = t + kSweepStages + 1;
       }
       const MS ms = warp_reduce_ms_fast(MS{mc, sacc});
       res = make_float2(ms.m, ms.s);

@@ -49,14 +49,12 @@ __device__ __forceinline__ void lane_raise_max(float m, float c, float& zmax, fl
   }
 }
 
-// One full 4 KB chunk in shared memory: each lane takes 8 of its 256 vectors.
+// One full 4 KB chunk, each lane holding 8 of its 256 vectors (read from the
+// shared-memory stage beforehand, so that the stage can be refilled first).
 // The maximum is a packed tree over the raw words, then one exp2 per logit.
 template <int DT>
-__device__ __forceinline__ void chunk_update_full(const uint4* sv, int lane, float c, float& zmax,
+__device__ __forceinline__ void chunk_update_full(const uint4 (&v)[8], float c, float& zmax,
                                                   float& mc, float& sacc) {
-  uint4 v[8];
-#pragma unroll
-  for (int u = 0; u < 8; ++u) v[u] = sv[lane + 32 * u];
   float m;
   if constexpr (DT == SV_BF16) {
     uint32_t a[8];
