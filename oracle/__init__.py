@@ -78,6 +78,8 @@ def lib():
             L.svo_spec_verify_rows.argtypes = L.svo_spec_verify.argtypes + [ctypes.c_int,
                                                                             ctypes.c_int]
             L.svo_spec_verify_rows.restype = ctypes.c_int
+            L.svo_spec_verify_ex.argtypes = L.svo_spec_verify_rows.argtypes + [P]
+            L.svo_spec_verify_ex.restype = ctypes.c_int
             L.svo_spec_verify_greedy.argtypes = [P, P, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_int64, ctypes.c_int, P, P]
             L.svo_spec_verify_greedy.restype = ctypes.c_int
@@ -140,10 +142,18 @@ def _dtype_code(a: np.ndarray) -> int:
     raise TypeError(f"logits must be float32 or uint16 (bf16 bits), got {a.dtype}")
 
 
+class _Options(ctypes.Structure):
+    """svo_options (sv_oracle.h)."""
+    _fields_ = [("lenience", ctypes.c_double), ("top_k", ctypes.c_int),
+                ("top_p", ctypes.c_double)]
+
+
 def spec_verify(zt, zd, xt, temperature=1.0, row_temperature=None, seed=0, rnd=0,
-                want_beta=False, rows=None, threads=1):
+                want_beta=False, rows=None, threads=1, lenience=1.0):
     """Sampling verify.  zt [B,g+1,V], zd [B,g,V] (float32 or bf16 bits as uint16),
     xt [B,g] int32.  Returns a dict of numpy arrays.
+
+    lenience: l in (0, 1]; a draft is accepted iff u <= p / (l q) (1: exact).
 
     rows: optional list of batch-row indices to compute (others left zero);
     threads: run disjoint row ranges in that many Python threads (each a plain
@@ -162,13 +172,15 @@ def spec_verify(zt, zd, xt, temperature=1.0, row_temperature=None, seed=0, rnd=0
         flags=np.zeros(B, np.uint8))
     L = lib()
 
+    opt = _Options(float(lenience), 0, 1.0)
+
     def run(b0, b1):
-        rc = L.svo_spec_verify_rows(
+        rc = L.svo_spec_verify_ex(
             _ptr(zt), _ptr(zd), _ptr(xt), B, g, V, _dtype_code(zt), float(temperature),
             _ptr(rowT), int(seed) & (2**64 - 1), int(rnd) & (2**64 - 1), _ptr(out["tokens"]),
             _ptr(out["counts"]), _ptr(out["p"]), _ptr(out["q"]), _ptr(out["ratio"]),
             _ptr(out["u"]), _ptr(out["beta"]), _ptr(out["gap"]), _ptr(out["resid_mass"]),
-            _ptr(out["flags"]), int(b0), int(b1))
+            _ptr(out["flags"]), int(b0), int(b1), ctypes.byref(opt))
         if rc != 0:
             raise ValueError(f"oracle spec_verify rejected its arguments (rc={rc})")
 

@@ -36,8 +36,13 @@ def residual(p: Dist, q: Dist):
 
 def enumerate_round(p_of: Callable[[Tuple[int, ...]], Dist],
                     q_of: Callable[[Tuple[int, ...]], Dist],
-                    V: int, gamma: int) -> Dict[Tuple[int, ...], Fraction]:
-    """Exact distribution of the emitted token tuple of one round."""
+                    V: int, gamma: int, lenience: Fraction = Fraction(1)
+                    ) -> Dict[Tuple[int, ...], Fraction]:
+    """Exact distribution of the emitted token tuple of one round.
+
+    lenience l: the comparison uses l q(x), i.e. accept w.p. min(1, p/(l q))
+    (same page, the paragraph on sharper distributions: Appendix A.5); the
+    correction after a rejection is the residual above, unchanged."""
     out: Dict[Tuple[int, ...], Fraction] = {}
 
     def add(seq, w):
@@ -56,7 +61,7 @@ def enumerate_round(p_of: Callable[[Tuple[int, ...]], Dist],
         for x in range(V):
             if q[x] == 0:
                 continue
-            a = min(Fraction(1), p[x] / q[x])
+            a = min(Fraction(1), p[x] / (lenience * q[x]))
             if a:
                 walk(prefix + (x,), w * q[x] * a)
             rej = w * q[x] * (1 - a)

@@ -239,6 +239,23 @@ int svo_spec_verify_rows(const void* zt, const void* zd, const int32_t* xt,
                          double* p_at, double* q_at, double* ratio_out, double* u_out,
                          double* beta_out, double* gumbel_gap, double* resid_mass,
                          uint8_t* flags, int b_begin, int b_end) {
+  return svo_spec_verify_ex(zt, zd, xt, B, gamma, V, dtype, temperature, row_temperature, seed,
+                            round, tokens, counts, p_at, q_at, ratio_out, u_out, beta_out,
+                            gumbel_gap, resid_mass, flags, b_begin, b_end, NULL);
+}
+
+int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
+                       int B, int gamma, int64_t V, int dtype,
+                       float temperature, const float* row_temperature,
+                       uint64_t seed, uint64_t round,
+                       int32_t* tokens, int32_t* counts,
+                       double* p_at, double* q_at, double* ratio_out, double* u_out,
+                       double* beta_out, double* gumbel_gap, double* resid_mass,
+                       uint8_t* flags, int b_begin, int b_end, const svo_options* opt) {
+  /* Lenience l (Appendix A.5 as the page summarises it): the comparison uses l q(x). */
+  const double l = opt ? opt->lenience : 1.0;
+  if (!(l > 0.0 && l <= 1.0)) return -1;
+  if (opt && (opt->top_k != 0 || opt->top_p != 1.0)) return -1;
   if (B < 0 || gamma < 1 || gamma > 64 || V < 1 || (dtype != SVO_F32 && dtype != SVO_BF16))
     return -1;
   if (b_begin < 0 || b_end > B || b_begin > b_end) return -1;
@@ -287,7 +304,7 @@ int svo_spec_verify_rows(const void* zt, const void* zd, const int32_t* xt,
         P[i] = prob(rt, x);
         Q[i] = prob(rd, x);
       }
-      RATIO[i] = P[i] / Q[i]; /* IEEE: p/0 = inf, 0/0 = NaN (rejects) */
+      RATIO[i] = P[i] / (l * Q[i]); /* IEEE: p/0 = inf, 0/0 = NaN (rejects) */
       U[i] = svo_uniform(seed, 0u, (uint32_t)i, (uint32_t)b, round, 0u, 0);
       if (p_at) p_at[(int64_t)b * gamma + i] = P[i];
       if (q_at) q_at[(int64_t)b * gamma + i] = Q[i];

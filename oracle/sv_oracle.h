@@ -82,6 +82,29 @@ int svo_spec_verify_rows(const void* zt, const void* zd, const int32_t* xt,
                          double* beta, double* gumbel_gap, double* resid_mass,
                          uint8_t* flags, int b_begin, int b_end);
 
+/* Variants of the round.  lenience l ("Fast Inference from Transformers via
+ * Speculative Decoding", the paragraph on sharper distributions, Appendix A.5
+ * as summarised there): q(x) is multiplied by l before the comparison, so a
+ * draft is accepted iff u <= p/(l q); l = 1 is the exact round.  The
+ * correction after a rejection is the residual of Algorithm 1, unchanged (the
+ * page changes only the comparison).  top_k and top_p are reserved (0 and 1:
+ * off) and must keep those values. */
+typedef struct {
+  double lenience; /* in (0, 1] */
+  int top_k;       /* 0 */
+  double top_p;    /* 1 */
+} svo_options;
+
+/* svo_spec_verify_rows with options (NULL: the exact round). */
+int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
+                       int B, int gamma, int64_t V, int dtype,
+                       float temperature, const float* row_temperature,
+                       uint64_t seed, uint64_t round,
+                       int32_t* tokens, int32_t* counts,
+                       double* p_at, double* q_at, double* ratio, double* u_acc,
+                       double* beta, double* gumbel_gap, double* resid_mass,
+                       uint8_t* flags, int b_begin, int b_end, const svo_options* opt);
+
 /* Greedy verify on raw target logits. */
 int svo_spec_verify_greedy(const void* zt, const int32_t* xt, int B, int gamma,
                            int64_t V, int dtype, int32_t* tokens, int32_t* counts);
