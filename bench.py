@@ -369,6 +369,7 @@ def run_ours(args):
     if not args.no_extra:
         extra["greedy"] = measure_greedy(L, dev, stream, rank)
         extra["lmhead"] = measure_lmhead(L, dev, stream, rank)
+        extra["lenience"] = measure_lenience(L, stream, sets, tokens, counts, flags, ws)
 
     if rank == 0:
         line = {
@@ -393,6 +394,48 @@ def run_ours(args):
         }
         line.update(extra)
         print(json.dumps(line), flush=True)
+
+
+def measure_lenience(L, stream, sets, tokens, counts, flags, ws, lenience=0.5, reps=400):
+    """spec_verify_opts with lenience l on the same rotating sample_b64 sets: the
+    lenient comparison u <= p/(l q) costs the same kernels and accepts more."""
+    import torch
+    from speculative_decoding_verification_21_gb300 import _lib
+    P = ctypes.c_void_p
+    sh = P(stream.cuda_stream)
+    B, gamma, V = 64, 4, 128256
+
+    def call(i, l):
+        s = sets[i % len(sets)]
+        opts = _lib.Options(l, 0, 1.0)
+        rc = L.spec_verify_opts(P(s.zt.data_ptr()), P(s.zd.data_ptr()), P(s.xt.data_ptr()), B,
+                                gamma, V, 1, ctypes.c_float(s.temperature), None, 0, i,
+                                P(tokens.data_ptr()), P(counts.data_ptr()), None, None, None,
+                                P(flags.data_ptr()), ctypes.addressof(opts), P(ws.data_ptr()),
+                                ctypes.c_size_t(ws.numel()), sh)
+        if rc != 0:
+            raise RuntimeError(f"spec_verify_opts failed ({rc})")
+
+    acc = {}
+    for l in (1.0, lenience):
+        tot = 0
+        for i in range(len(sets)):
+            call(i, l)
+            tot += int(counts.sum().item())
+        acc[l] = tot / (len(sets) * B)
+    for i in range(3):
+        call(i, lenience)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(reps):
+        call(i, lenience)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    return {"workload": "sample_b64", "lenience": lenience, "rounds_per_s": 1000.0 / ms,
+            "ms_per_round": ms, "mean_accepted": acc[lenience], "mean_accepted_exact": acc[1.0],
+            "gpu_launches_per_round": 3}
 
 
 def _kernel_times(L, stream, call, nkern, reps, warm=3):

@@ -115,6 +115,38 @@ int spec_verify(const void* target_logits, const void* draft_logits,
                 void* cuda_stream);
 
 /*
+ * Variants of the round for spec_verify_opts.
+ *   lenience  l in (0, 1]; 1 is the exact round.  q(x) is multiplied by l before
+ *             the comparison, so draft i is accepted iff u_i <= p_i(x_i) /
+ *             (l q_i(x_i)).  This accepts more and gives up exactness: no token
+ *             is then emitted more than 1/l times as often as the target would
+ *             emit it ("Fast Inference from Transformers via Speculative
+ *             Decoding", the paragraph on sharper distributions, Appendix A.5 as
+ *             summarised there).  The page changes only the comparison, so the
+ *             token drawn after a rejection still comes from max(0, p_n - q_n).
+ *   top_k     reserved: must be 0 (off);  top_p  reserved: must be 1 (off).
+ */
+typedef struct {
+  float lenience;
+  int32_t top_k;
+  float top_p;
+} sv_options;
+
+/*
+ * spec_verify_opts -- spec_verify with sv_options (NULL: the exact round, the
+ * same results as spec_verify).  A lenience outside (0, 1] (or NaN) returns
+ * SV_ERR_ARG; top_k != 0 or top_p != 1 return SV_ERR_UNSUPPORTED.  The other
+ * arguments, outputs and errors are those of spec_verify.
+ */
+int spec_verify_opts(const void* target_logits, const void* draft_logits,
+                     const int32_t* draft_tokens, int B, int gamma, int64_t V, int dtype,
+                     float temperature, const float* row_temperature, uint64_t seed,
+                     uint64_t round, int32_t* out_tokens, int32_t* out_counts,
+                     float* out_p_at_draft, float* out_q_at_draft, float* out_alpha,
+                     uint8_t* out_flags, const sv_options* options, void* workspace,
+                     size_t workspace_bytes, void* cuda_stream);
+
+/*
  * spec_verify_noalloc -- spec_verify for callers that cannot allocate device memory.
  * The pages have no counterpart to this entry point; it exists for the deployment.
  * Some callers are handed only their input and output buffers (a plugin inside
@@ -179,9 +211,11 @@ int spec_lmhead_verify(const void* h_target, const void* W_target, int Ht,
                        void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /* Profiling aid (not thread-safe): when `events` is non-NULL, following calls
- * of spec_verify record events[0] on their stream before the first kernel and
- * events[k] after the k-th of their kernels (the softmax sweep, the decision,
- * the draw; n >= 4).  NULL switches recording off.  The events are cudaEvent_t
+ * record events[0] on their stream before the first kernel and events[k] after
+ * the k-th of their kernels: for spec_verify the softmax sweep, the draw (with
+ * the decision at its start) and the draw merge (n >= 4); for
+ * spec_lmhead_verify the first GEMM pass, the decision, the recompute pass and
+ * the merge (n >= 5).  NULL switches recording off.  The events are cudaEvent_t
  * created by the caller; they change no result. */
 int sv_set_timing_events(void* const* events, int n);
 

@@ -18,8 +18,15 @@ SV_F32, SV_BF16 = 0, 1
 SV_MODE_SAMPLE, SV_MODE_GREEDY, SV_MODE_LMHEAD = 0, 1, 2
 FLAG_ZERO_MASS, FLAG_NONFINITE, FLAG_RESIDUAL_FALLBACK, FLAG_TIMEOUT, FLAG_BAD_TOKEN = 1, 2, 4, 8, 16
 
-EXPORTS = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verify_greedy",
-           "spec_lmhead_verify", "sv_set_timing_events", "sv_status_string", "sv_version")
+EXPORTS = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verify_opts",
+           "spec_verify_greedy", "spec_lmhead_verify", "sv_set_timing_events",
+           "sv_status_string", "sv_version")
+
+
+class Options(ctypes.Structure):
+    """sv_options of include/specverify.h."""
+    _fields_ = [("lenience", ctypes.c_float), ("top_k", ctypes.c_int32),
+                ("top_p", ctypes.c_float)]
 
 
 class SpecVerifyError(RuntimeError):
@@ -56,6 +63,9 @@ def load(build_if_missing: bool = True):
         L.sv_workspace_init.restype = I
         L.spec_verify.argtypes = [P, P, P, I, I, I64, I, F, P, U64, U64, P, P, P, P, P, P, P, SZ, P]
         L.spec_verify.restype = I
+        L.spec_verify_opts.argtypes = [P, P, P, I, I, I64, I, F, P, U64, U64, P, P, P, P, P, P,
+                                       P, P, SZ, P]
+        L.spec_verify_opts.restype = I
         L.spec_verify_greedy.argtypes = [P, P, I, I, I64, I, P, P, P, SZ, P]
         L.spec_verify_greedy.restype = I
         L.spec_lmhead_verify.argtypes = [P, P, I, P, P, I, P, I, I, I64, F, U64, U64, P, P, P, P,
@@ -141,10 +151,11 @@ def alloc_workspace(B: int, gamma: int, V: int, mode: int, device="cuda"):
 def spec_verify(target_logits, draft_logits, draft_tokens, *, temperature: float = 1.0,
                 row_temperature=None, seed: int = 0, round: int = 0, want_pq: bool = True,
                 want_alpha: bool = False, want_flags: bool = True, out=None, workspace=None,
-                stream=None):
+                stream=None, lenience: float = 1.0):
     """Sampling verify through the C ABI.  Returns a dict of device tensors:
     tokens [B, g+1] int32, counts [B] int32, p/q [B, g] float32 (if want_pq),
-    alpha [B] float32 (if want_alpha), flags [B] uint8 (if want_flags)."""
+    alpha [B] float32 (if want_alpha), flags [B] uint8 (if want_flags).
+    lenience: l in (0, 1] (spec_verify_opts; 1 = the exact round)."""
     torch = _torch()
     L = load()
     B, g1, V = target_logits.shape
@@ -170,11 +181,14 @@ def spec_verify(target_logits, draft_logits, draft_tokens, *, temperature: float
     sh = _stream_handle(stream)
     need = workspace_bytes(B, g, V, SV_MODE_SAMPLE)
     ws = workspace if workspace is not None else _ws_cache.get(need, dev, sh.value)
-    rc = L.spec_verify(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g, V,
-                       _dtype_code(target_logits), float(temperature), _ptr(row_temperature),
-                       int(seed) & (2**64 - 1), int(round) & (2**64 - 1), _ptr(o["tokens"]),
-                       _ptr(o["counts"]), _ptr(o.get("p")), _ptr(o.get("q")),
-                       _ptr(o.get("alpha")), _ptr(o.get("flags")), _ptr(ws), ws.numel(), sh)
+    opts = Options(float(lenience), 0, 1.0)
+    rc = L.spec_verify_opts(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g,
+                            V, _dtype_code(target_logits), float(temperature),
+                            _ptr(row_temperature), int(seed) & (2**64 - 1),
+                            int(round) & (2**64 - 1), _ptr(o["tokens"]), _ptr(o["counts"]),
+                            _ptr(o.get("p")), _ptr(o.get("q")), _ptr(o.get("alpha")),
+                            _ptr(o.get("flags")), ctypes.addressof(opts), _ptr(ws), ws.numel(),
+                            sh)
     if rc != SV_OK:
         raise SpecVerifyError(rc, "spec_verify")
     return o

@@ -49,6 +49,7 @@ struct SweepCtx {
   float* out_p;
   float* out_q;
   uint8_t* out_flags;
+  float inv_lenience;    // 1/l of the lenient comparison u <= p/(l q); 1: the exact round
 };
 
 // Row statistics of row r from its chunk partials (one warp, all loads of a
@@ -155,7 +156,7 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
         ratio = p0 ? (q0 ? CUDART_NAN_F : 0.0f) : kInf;
       } else {
         const float d = (ep.hi - eq.hi) + (ep.lo - eq.lo);
-        ratio = exp2f(d) * (float)(rd.s / rt.s);
+        ratio = exp2f(d) * (float)(rd.s / rt.s) * x.inv_lenience;
       }
       qzero = q0 || !(rd.s == rd.s);
     } else {

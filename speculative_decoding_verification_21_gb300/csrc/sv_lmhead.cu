@@ -805,6 +805,7 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
     sx.out_p = a.out_p;
     sx.out_q = a.out_q;
     sx.out_flags = a.out_flags;
+    sx.inv_lenience = 1.0f;
     decide_batch_row<SV_F32>(sx, b, srs, sda);
   }
   __syncthreads();

@@ -36,7 +36,8 @@ cudaError_t launch_sample(const void* zt, const void* zd, const int32_t* xt, int
                           int64_t V, int dtype, float temperature, const float* row_T,
                           uint64_t seed, uint64_t round, int32_t* out_tokens, int32_t* out_counts,
                           float* out_p, float* out_q, float* out_alpha, uint8_t* out_flags,
-                          void* ws, const SamplePlan& pl, cudaStream_t stream);
+                          void* ws, const SamplePlan& pl, cudaStream_t stream,
+                          float lenience);
 }  // namespace sv
 
 namespace {
@@ -99,6 +100,6 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
   const cudaError_t e = sv::launch_sample(
       target_logits, draft_logits, draft_tokens, B, gamma, V, dtype, temperature, row_temperature,
       seed, round, out_tokens, out_counts, out_p_at_draft, out_q_at_draft, out_alpha, out_flags,
-      scratch, pl, (cudaStream_t)cuda_stream);
+      scratch, pl, (cudaStream_t)cuda_stream, 1.0f);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -496,7 +496,7 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
                                    uint64_t seed, uint64_t round, int32_t* out_tokens,
                                    int32_t* out_counts, float* out_p, float* out_q,
                                    float* out_alpha, uint8_t* out_flags, char* ws,
-                                   const SamplePlan& pl, cudaStream_t stream) {
+                                   const SamplePlan& pl, cudaStream_t stream, float lenience) {
   const int R1 = pl.R1;
   uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + pl.off_cnt);
   float2* part1 = reinterpret_cast<float2*>(ws + pl.off_part1);
@@ -513,7 +513,7 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   const bool tma = use_tma_sweep(DT, V) && di->sweep_ctas_per_sm[DT] > 0;
   const int nch = (int)(tma ? ceil_div(V, tma_chunk_elems(DT)) : ceil_div(V, kChunkSweep));
   SweepCtx sx{zt, zd, xt, B, gamma, V, temperature, row_T, seed, round, nch, part1, rowstat,
-              state, out_tokens, out_counts, out_p, out_q, out_flags};
+              state, out_tokens, out_counts, out_p, out_q, out_flags, 1.0f / lenience};
   mark(0, stream);
   if (tma) {
     // one resident wave of warps, chunks dealt round-robin
@@ -557,15 +557,15 @@ cudaError_t launch_sample(const void* zt, const void* zd, const int32_t* xt, int
                           int64_t V, int dtype, float temperature, const float* row_T,
                           uint64_t seed, uint64_t round, int32_t* out_tokens, int32_t* out_counts,
                           float* out_p, float* out_q, float* out_alpha, uint8_t* out_flags,
-                          void* ws, const SamplePlan& pl, cudaStream_t stream) {
+                          void* ws, const SamplePlan& pl, cudaStream_t stream, float lenience) {
   char* w = reinterpret_cast<char*>(ws);
   if (dtype == SV_F32)
     return launch_sample_t<SV_F32>(zt, zd, xt, B, gamma, V, temperature, row_T, seed, round,
                                    out_tokens, out_counts, out_p, out_q, out_alpha, out_flags, w,
-                                   pl, stream);
+                                   pl, stream, lenience);
   return launch_sample_t<SV_BF16>(zt, zd, xt, B, gamma, V, temperature, row_T, seed, round,
                                   out_tokens, out_counts, out_p, out_q, out_alpha, out_flags, w,
-                                  pl, stream);
+                                  pl, stream, lenience);
 }
 
 }  // namespace sv

@@ -63,6 +63,31 @@ def _sv(L, zt=FAKE, zd=FAKE, xt=FAKE, B=2, g=2, V=64, dt=0, T=1.0, rowT=None, to
                          None, ws, wsb, None)
 
 
+def _svo(L, lenience=1.0, top_k=0, top_p=1.0, opts=True, **kw):
+    o = _lib.Options(lenience, top_k, top_p)
+    a = dict(zt=FAKE, zd=FAKE, xt=FAKE, B=2, g=2, V=64, dt=0, T=1.0, tok=FAKE, cnt=FAKE, ws=FAKE,
+             wsb=1 << 20)
+    a.update(kw)
+    return L.spec_verify_opts(a["zt"], a["zd"], a["xt"], a["B"], a["g"], a["V"], a["dt"], a["T"],
+                              None, 0, 0, a["tok"], a["cnt"], None, None, None, None,
+                              ctypes.addressof(o) if opts else None, a["ws"], a["wsb"], None)
+
+
+def test_spec_verify_opts_argument_errors():
+    L = sv.load()
+    for bad in (0.0, -0.25, 1.0000001, 2.0, float("nan"), float("inf")):
+        assert _svo(L, lenience=bad) == -1, bad
+    assert _svo(L, top_k=5) == -6
+    assert _svo(L, top_p=0.9) == -6
+    # the remaining arguments are checked as by spec_verify
+    assert _svo(L, lenience=0.5, g=0) == -1
+    assert _svo(L, lenience=0.5, dt=7) == -2
+    assert _svo(L, lenience=0.5, zt=FAKE_MIS) == -3
+    assert _svo(L, lenience=0.5, ws=None) == -4
+    assert _svo(L, opts=False, ws=None) == -4
+    assert _svo(L, lenience=0.5, B=0) == 0  # nothing to do
+
+
 def test_spec_verify_argument_errors():
     L = sv.load()
     assert _sv(L, g=0) == -1

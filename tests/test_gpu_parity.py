@@ -28,16 +28,17 @@ def _cuda():
     sv.load()
 
 
-def run_both(w, seed=0, rnd=0, rows=None, want_alpha=False):
+def run_both(w, seed=0, rnd=0, rows=None, want_alpha=False, lenience=1.0):
     g = sv.spec_verify(w.zt, w.zd, w.xt, temperature=w.temperature,
                        row_temperature=w.row_temperature, seed=seed, round=rnd,
-                       want_alpha=want_alpha)
+                       want_alpha=want_alpha, lenience=lenience)
     torch.cuda.synchronize()
     gpu = to_np(g)
     rowT = None if w.row_temperature is None else w.row_temperature.cpu().numpy()
     orc = oracle.spec_verify(wl.to_oracle(w.zt), wl.to_oracle(w.zd), w.xt.cpu().numpy(),
                              temperature=w.temperature, row_temperature=rowT, seed=seed, rnd=rnd,
-                             rows=rows, threads=THREADS, want_beta=want_alpha)
+                             rows=rows, threads=THREADS, want_beta=want_alpha,
+                             lenience=lenience)
     return gpu, orc
 
 
@@ -74,6 +75,22 @@ def test_sample_b64_full(sigma):
         near, dec = near + n, dec + d
         if r == 0:
             np.testing.assert_allclose(gpu["alpha"], orc["alpha"], rtol=1e-5)
+    assert near <= 1e-4 * max(dec, 1e4)
+
+
+@pytest.mark.parametrize("lenience", [0.5, 0.1])
+def test_sample_b64_lenience(lenience):
+    """Lenient comparison u <= p/(l q) against the oracle's, and more acceptances
+    than the exact round on the same inputs and uniforms."""
+    w = wl.sample_b64(sigma=1.0)
+    near = dec = 0
+    for r in range(2):
+        gpu, orc = run_both(w, seed=0, rnd=r, lenience=lenience)
+        n, d = assert_parity(gpu, orc, w.gamma, what=f"sample_b64 lenience={lenience} round {r}")
+        near, dec = near + n, dec + d
+        exact, _ = run_both(w, seed=0, rnd=r, rows=[0])
+        assert np.all(gpu["counts"] >= exact["counts"])
+        assert gpu["counts"].sum() > exact["counts"].sum()
     assert near <= 1e-4 * max(dec, 1e4)
 
 
