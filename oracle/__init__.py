@@ -149,11 +149,12 @@ class _Options(ctypes.Structure):
 
 
 def spec_verify(zt, zd, xt, temperature=1.0, row_temperature=None, seed=0, rnd=0,
-                want_beta=False, rows=None, threads=1, lenience=1.0):
+                want_beta=False, rows=None, threads=1, lenience=1.0, top_k=0):
     """Sampling verify.  zt [B,g+1,V], zd [B,g,V] (float32 or bf16 bits as uint16),
     xt [B,g] int32.  Returns a dict of numpy arrays.
 
     lenience: l in (0, 1]; a draft is accepted iff u <= p / (l q) (1: exact).
+    top_k: keep the entries of every row at or above its k-th largest logit (0: off).
 
     rows: optional list of batch-row indices to compute (others left zero);
     threads: run disjoint row ranges in that many Python threads (each a plain
@@ -172,7 +173,7 @@ def spec_verify(zt, zd, xt, temperature=1.0, row_temperature=None, seed=0, rnd=0
         flags=np.zeros(B, np.uint8))
     L = lib()
 
-    opt = _Options(float(lenience), 0, 1.0)
+    opt = _Options(float(lenience), int(top_k), 1.0)
 
     def run(b0, b1):
         rc = L.svo_spec_verify_ex(

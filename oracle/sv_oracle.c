@@ -156,9 +156,36 @@ typedef struct {
   double S;   /* sum_v exp(s_v - m), 0 if no finite entry */
 } row_t;
 
-/* Temperature then softmax statistics of one row ([A3]). */
-static void load_row(row_t* r, const void* base, int dtype, int64_t off, int64_t V, double invT) {
+/* Descending order for qsort. */
+static int cmp_desc(const void* a, const void* b) {
+  const double x = *(const double*)a, y = *(const double*)b;
+  return (x < y) - (x > y);
+}
+
+/* The k-th largest of the row's values that are not NaN (counting repeats);
+ * -inf when the row has fewer than k of them.  `buf` holds V doubles. */
+static double kth_largest(const double* s, int64_t V, int k, double* buf) {
+  int64_t n = 0;
+  for (int64_t v = 0; v < V; ++v)
+    if (!isnan(s[v])) buf[n++] = s[v];
+  if (k > n) return -INFINITY;
+  qsort(buf, (size_t)n, sizeof(double), cmp_desc);
+  return buf[k - 1];
+}
+
+/* Temperature, the top-k adjustment, then softmax statistics of one row ([A3]).
+ * Top-k ([A3]: top-k zeroes the tail and renormalises): with top_k > 0 every
+ * entry below the k-th largest scaled logit gets weight 0 (-inf); entries equal
+ * to it are kept, and NaN entries are left as they are (they mark the row
+ * non-finite).  `buf` holds V doubles. */
+static void load_row(row_t* r, const void* base, int dtype, int64_t off, int64_t V, double invT,
+                     int top_k, double* buf) {
   for (int64_t v = 0; v < V; ++v) r->s[v] = logit_at(base, dtype, off + v) * invT;
+  if (top_k > 0) {
+    const double tau = kth_largest(r->s, V, top_k, buf);
+    for (int64_t v = 0; v < V; ++v)
+      if (r->s[v] < tau) r->s[v] = -INFINITY;
+  }
   double m = -INFINITY;
   for (int64_t v = 0; v < V; ++v)
     if (r->s[v] > m) m = r->s[v];
@@ -254,8 +281,9 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
                        uint8_t* flags, int b_begin, int b_end, const svo_options* opt) {
   /* Lenience l (Appendix A.5 as the page summarises it): the comparison uses l q(x). */
   const double l = opt ? opt->lenience : 1.0;
+  const int top_k = opt ? opt->top_k : 0;
   if (!(l > 0.0 && l <= 1.0)) return -1;
-  if (opt && (opt->top_k != 0 || opt->top_p != 1.0)) return -1;
+  if (top_k < 0 || (opt && opt->top_p != 1.0)) return -1;
   if (B < 0 || gamma < 1 || gamma > 64 || V < 1 || (dtype != SVO_F32 && dtype != SVO_BF16))
     return -1;
   if (b_begin < 0 || b_end > B || b_begin > b_end) return -1;
@@ -273,6 +301,15 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
       return -1;
     }
   }
+  double* kbuf = NULL; /* scratch of the top-k selection */
+  if (top_k > 0) {
+    kbuf = (double*)malloc((size_t)V * sizeof(double));
+    if (!kbuf) {
+      for (int r = 0; r < R; ++r) free(rows[r].s);
+      free(rows);
+      return -1;
+    }
+  }
 
   for (int b = b_begin; b < b_end; ++b) {
     float T = row_temperature ? row_temperature[b] : temperature;
@@ -282,9 +319,10 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
     uint8_t flag = 0;
 
     for (int i = 0; i <= gamma; ++i)
-      load_row(&rows[i], zt, dtype, ((int64_t)b * (gamma + 1) + i) * V, V, invT);
+      load_row(&rows[i], zt, dtype, ((int64_t)b * (gamma + 1) + i) * V, V, invT, top_k, kbuf);
     for (int i = 0; i < gamma; ++i)
-      load_row(&rows[gamma + 1 + i], zd, dtype, ((int64_t)b * gamma + i) * V, V, invT);
+      load_row(&rows[gamma + 1 + i], zd, dtype, ((int64_t)b * gamma + i) * V, V, invT, top_k,
+               kbuf);
     for (int r = 0; r < R; ++r) {
       if (rows[r].m == -INFINITY) flag |= SVO_FLAG_ZERO_MASS;
       if (row_nonfinite(&rows[r])) flag |= SVO_FLAG_NONFINITE;
@@ -371,6 +409,7 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
 
   for (int r = 0; r < R; ++r) free(rows[r].s);
   free(rows);
+  free(kbuf);
   return 0;
 }
 

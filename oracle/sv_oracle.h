@@ -87,11 +87,15 @@ int svo_spec_verify_rows(const void* zt, const void* zd, const int32_t* xt,
  * as summarised there): q(x) is multiplied by l before the comparison, so a
  * draft is accepted iff u <= p/(l q); l = 1 is the exact round.  The
  * correction after a rejection is the residual of Algorithm 1, unchanged (the
- * page changes only the comparison).  top_k and top_p are reserved (0 and 1:
- * off) and must keep those values. */
+ * page changes only the comparison).
+ * top_k (same page, "already adjusted" distributions: top-k zeroes the tail and
+ * renormalises): with top_k > 0 every target and draft row keeps the entries
+ * whose scaled logit is at least its k-th largest (ties at the boundary kept,
+ * NaN left in place), the rest get probability 0; 0 is off.  top_p is reserved
+ * (1: off) and must keep that value. */
 typedef struct {
   double lenience; /* in (0, 1] */
-  int top_k;       /* 0 */
+  int top_k;       /* >= 0 */
   double top_p;    /* 1 */
 } svo_options;
 
