@@ -124,7 +124,14 @@ int spec_verify(const void* target_logits, const void* draft_logits,
  *             Decoding", the paragraph on sharper distributions, Appendix A.5 as
  *             summarised there).  The page changes only the comparison, so the
  *             token drawn after a rejection still comes from max(0, p_n - q_n).
- *   top_k     reserved: must be 0 (off);  top_p  reserved: must be 1 (off).
+ *   top_k     0: off.  k > 0: every target and draft row is adjusted before the
+ *             round: entries whose logit is below the row's k-th largest
+ *             (repeats counted, NaN not ranked) get probability 0 and the rest
+ *             are renormalised; ties at the boundary are all kept (same page,
+ *             section "The loop": top-k zeroes the tail and renormalises, and
+ *             the round runs on the adjusted p and q).  k >= V changes nothing.
+ *             Costs one radix-select pass over every row before the sweep.
+ *   top_p     reserved: must be 1 (off).
  */
 typedef struct {
   float lenience;
@@ -134,9 +141,10 @@ typedef struct {
 
 /*
  * spec_verify_opts -- spec_verify with sv_options (NULL: the exact round, the
- * same results as spec_verify).  A lenience outside (0, 1] (or NaN) returns
- * SV_ERR_ARG; top_k != 0 or top_p != 1 return SV_ERR_UNSUPPORTED.  The other
- * arguments, outputs and errors are those of spec_verify.
+ * same results as spec_verify).  A lenience outside (0, 1] (or NaN) or a
+ * negative top_k returns SV_ERR_ARG; top_p != 1 returns SV_ERR_UNSUPPORTED.
+ * The other arguments, outputs and errors are those of spec_verify.  With
+ * top_k, p_at_draft / q_at_draft and alpha are those of the adjusted rows.
  */
 int spec_verify_opts(const void* target_logits, const void* draft_logits,
                      const int32_t* draft_tokens, int B, int gamma, int64_t V, int dtype,

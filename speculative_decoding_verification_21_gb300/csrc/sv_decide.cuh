@@ -50,6 +50,7 @@ struct SweepCtx {
   float* out_q;
   uint8_t* out_flags;
   float inv_lenience;    // 1/l of the lenient comparison u <= p/(l q); 1: the exact round
+  const float* thr;      // [B][R1] top-k thresholds (logits below have weight 0) or null
 };
 
 // Row statistics of row r from its chunk partials (one warp, all loads of a
@@ -188,6 +189,8 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
     st.pos = n;
     st.c = c;
     st.invT = invT;
+    st.tt = x.thr ? x.thr[(int64_t)b * R1 + n] : -kInf;
+    st.td = (x.thr && n < gamma) ? x.thr[(int64_t)b * R1 + gamma + 1 + n] : -kInf;
     const bool t_ok = (St > 0.0) && (St < 1e308) && (mct < kInf);
     if (n == gamma) {
       if (t_ok) {

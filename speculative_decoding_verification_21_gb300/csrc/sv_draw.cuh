@@ -31,14 +31,16 @@ struct DrawArgs {
 
 // Keys of one 4-entry Philox group v = v0 .. v0+3 from already loaded logits;
 // the running best is kept as a fraction num/den and compared by cross-products.
-template <bool RESID>
+// With TOPK, logits below the rows' top-k thresholds (st.tt, st.td) have weight 0.
+template <bool RESID, bool TOPK>
 __device__ __forceinline__ void draw_keys(const float* ztv, const float* zdv, int v0,
                                           const DrawState& st, uint4 rnd, float& bn, float& bd,
                                           int& bi) {
   const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float et = ex2(fmaf(ztv[e], st.c, -st.mct));
+    const float zt = (TOPK && ztv[e] < st.tt) ? -kInf : ztv[e];
+    const float et = ex2(fmaf(zt, st.c, -st.mct));
     float wgt;
     bool cand;
     if (RESID) {
@@ -47,11 +49,12 @@ __device__ __forceinline__ void draw_keys(const float* ztv, const float* zdv, in
       // first is larger.  Where p and q nearly agree the difference loses
       // relative precision, but only for weights far below the top keys, and any
       // misordering of the top two is re-decided in double (refine)
-      const float ed = ex2(fmaf(zdv[e], st.c, st.K - st.mct));
+      const float zd = (TOPK && zdv[e] < st.td) ? -kInf : zdv[e];
+      const float ed = ex2(fmaf(zd, st.c, st.K - st.mct));
       cand = et > ed;
       wgt = et - ed;
     } else {
-      cand = ztv[e] > -kInf;
+      cand = zt > -kInf;
       wgt = et;
     }
     const float E = neglog2_u(rr[e]);
@@ -110,7 +113,7 @@ __device__ __forceinline__ void widen(const Group<DT>& g, float* f) {
 }
 
 // This thread's best key over groups [g0, g1); all loads of a step in flight together.
-template <int DT, bool RESID>
+template <int DT, bool RESID, bool TOPK>
 __device__ __forceinline__ KI draw_range(const char* rt, const char* rd, int g0, int g1, int V,
                                          bool vec_ok, const DrawState& st, uint32_t b,
                                          const PhiloxKeys& pk, uint64_t round) {
@@ -136,7 +139,7 @@ __device__ __forceinline__ KI draw_range(const char* rt, const char* rd, int g0,
         widen<DT>(gt[u], zt4);
         if (RESID) widen<DT>(gd[u], zd4);
         const uint4 rnd = philox_rk(sv_counter((uint32_t)gg, 1u, (uint32_t)st.pos, b, round), pk);
-        draw_keys<RESID>(zt4, zd4, 4 * gg, st, rnd, bn, bd, bi);
+        draw_keys<RESID, TOPK>(zt4, zd4, 4 * gg, st, rnd, bn, bd, bi);
       }
     }
   }
@@ -154,9 +157,11 @@ __device__ double draw_key_f64(const char* rt, const char* rd, int64_t v, const 
                                   (uint32_t)seed, (uint32_t)(seed >> 32));
   const uint32_t lanes[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
   const double lnE = log(sv_neglog_u_f64(lanes[v & 3]));
-  const double zt = (double)load_logit<DT>(rt, v);
+  const float zt32 = load_logit<DT>(rt, v);
+  const double zt = (zt32 < st.tt) ? -CUDART_INF : (double)zt32;  // top-k: below the threshold
   if (!resid) return zt * (double)st.invT - lnE;
-  const double zd = (double)load_logit<DT>(rd, v);
+  const float zd32 = load_logit<DT>(rd, v);
+  const double zd = (zd32 < st.td) ? -CUDART_INF : (double)zd32;
   const double P = exp2(zt * (double)st.c - (double)st.mct) / st.st;
   const double Q = exp2(zd * (double)st.c - (double)st.mcd) / st.sd;
   const double r = P - Q;

@@ -806,6 +806,7 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
     sx.out_q = a.out_q;
     sx.out_flags = a.out_flags;
     sx.inv_lenience = 1.0f;
+    sx.thr = nullptr;
     decide_batch_row<SV_F32>(sx, b, srs, sda);
   }
   __syncthreads();

@@ -62,6 +62,8 @@ struct DrawState {
   float mcd;     // draft row n: scaled max (residual only)
   float K;       // (mct + log2 St) - (mcd + log2 Sd), log2 of q/p offset
   int flags;     // SV_FLAG_* gathered by the decision
+  float tt;      // top-k threshold of target row n: logits below it have weight 0 (-inf: off)
+  float td;      // top-k threshold of draft row n (residual only)
   double st;     // target row n: sum
   double sd;     // draft row n: sum (residual only)
 };
@@ -72,7 +74,7 @@ struct SamplePlan {
   int nsplit3 = 0;     // most CTAs per batch row in the draw pass
   // counters: [B] overlap CTAs (zeroed by the first draw CTA of each batch row)
   size_t off_cnt = 0, cnt_bytes = 0, off_part1 = 0, off_rowstat = 0, off_state = 0,
-         off_part3 = 0, off_alpha = 0, total = 0;
+         off_part3 = 0, off_alpha = 0, off_thr = 0, total = 0;
 };
 
 inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
@@ -91,6 +93,7 @@ inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
   p.off_state = o;    o = align_up(o + sizeof(DrawState) * (size_t)B);
   p.off_part3 = o;    o = align_up(o + 16 * (size_t)B * p.nsplit3);
   p.off_alpha = o;    o = align_up(o + sizeof(float) * (size_t)B * gamma * p.nsplit1);
+  p.off_thr = o;      o = align_up(o + sizeof(float) * (size_t)B * p.R1);  // top-k thresholds
   p.total = o;
   return p;
 }

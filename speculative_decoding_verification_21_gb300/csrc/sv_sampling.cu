@@ -78,7 +78,7 @@ __device__ __forceinline__ void for_each_in_chunk(const char* row, int64_t lo, i
   for (int64_t v = a1 + tid; v < hi; v += blockDim.x) f_one(v, load_logit<DT>(row, v));
 }
 
-template <int DT>
+template <int DT, bool TOPK>
 __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
   pdl_launch_dependents();
   const int R1 = 2 * x.gamma + 1;
@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
   const char* row = row_ptr<DT>(x.zt, x.zd, b, k, x.gamma, x.V);
   const int64_t lo = (int64_t)split * kChunkSweep;
   const int64_t hi = min(x.V, lo + kChunkSweep);
+  const float tau = TOPK ? x.thr[r] : -kInf;  // logits below the top-k threshold add nothing
 
   float zmax = -kInf, mc = -kInf, s = 0.0f;
   auto raise_max = [&](float m) {
@@ -110,13 +111,14 @@ __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
           unpack<DT>(vec, f);
           float acc = 0.0f;
 #pragma unroll
-          for (int e = 0; e < VecInfo<DT>::kElems; ++e) acc += ex2(fmaf(f[e], c, -mc));
+          for (int e = 0; e < VecInfo<DT>::kElems; ++e)
+            acc += (TOPK && f[e] < tau) ? 0.0f : ex2(fmaf(f[e], c, -mc));
           s += acc;
         }
       },
       [&](int64_t, float z) {
         raise_max(z);
-        if (zmax > -kInf) s += ex2(fmaf(z, c, -mc));
+        if (zmax > -kInf && !(TOPK && z < tau)) s += ex2(fmaf(z, c, -mc));
       });
 
   MS v = warp_reduce_ms(MS{mc, s});
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
 // Chunk c of the [b][row][chunk] order goes to warp c mod W, so the whole GPU
 // walks memory in address order; each chunk leaves one (max, sum) partial.
 // --------------------------------------------------------------------------
-template <int DT>
+template <int DT, bool TOPK>
 __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
   pdl_launch_dependents();  // the draw kernel may be scheduled now; it waits for us
   constexpr int kBytes = (DT == SV_F32) ? 4 : 2;
@@ -214,6 +216,8 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
         const float T = x.row_T ? __ldg(x.row_T + cur_b) : x.temperature;
         c = log2_scale(inv_temperature(T));
       }
+      // logits below the row's top-k threshold add nothing to the sum
+      const float tau = TOPK ? __ldg(x.thr + (int64_t)pc.b * R1 + pc.k) : -kInf;
       const uint4* sv = reinterpret_cast<const uint4*>(stage0 + (size_t)s * kSweepChunkBytes);
       float zmax = -kInf, mc = -kInf, sacc = 0.0f;
       const bool full = (pc.j != nch - 1);
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
         issued = t + kSweepStages + 1;
       }
       if (full) {
-        chunk_update_full<DT>(v, c, zmax, mc, sacc);
+        chunk_update_full<DT, TOPK>(v, c, tau, zmax, mc, sacc);
       } else {
         const int nv = (nvec - lane + 31) >> 5;
         float m = -kInf;
@@ -250,8 +254,8 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
               unpack<DT>(v[u], f);
 #pragma unroll
               for (int e = 0; e < VecInfo<DT>::kElems; e += 2) {
-                s0 += ex2(fmaf(f[e], c, -mc));
-                s1 += ex2(fmaf(f[e + 1], c, -mc));
+                s0 += (TOPK && f[e] < tau) ? 0.0f : ex2(fmaf(f[e], c, -mc));
+                s1 += (TOPK && f[e + 1] < tau) ? 0.0f : ex2(fmaf(f[e + 1], c, -mc));
               }
             }
           }
@@ -274,6 +278,131 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
 }
 
 // --------------------------------------------------------------------------
+// Top-k thresholds ("Fast Inference from Transformers via Speculative
+// Decoding", section "The loop": top-k zeroes the tail of p and q and
+// renormalises; every entry at or above the k-th largest logit is kept).
+// --------------------------------------------------------------------------
+// Order-preserving key of a float: a larger float has a larger key (-0 sorts
+// just below +0; the two compare equal as floats, so either gives the same cut).
+__device__ __forceinline__ uint32_t fkey(float z) {
+  const uint32_t u = __float_as_uint(z);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_inv(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Histogram of one radix pass: the digit (bits [shift, shift+width) of the key)
+// of every ranked entry whose higher bits equal `prefix` under `mask`, counted
+// into this warp's own copy of the histogram (fewer lanes collide on one
+// shared-memory counter).
+template <int DT>
+__device__ __forceinline__ void topk_pass(const char* base, int64_t V, uint32_t prefix,
+                                          uint32_t mask, int shift, uint32_t dmask,
+                                          uint32_t* hist) {
+  auto count = [&](float z) {
+    if (z != z) return;  // NaN is not ranked
+    const uint32_t key = fkey(z);
+    if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
+  };
+  for_each_in_chunk<DT, 4>(
+      base, 0, V,
+      [&](int64_t, const uint4& vec) {
+        float f[VecInfo<DT>::kElems];
+        unpack<DT>(vec, f);
+#pragma unroll
+        for (int e = 0; e < VecInfo<DT>::kElems; ++e) count(f[e]);
+      },
+      [&](int64_t, float z) { count(z); });
+}
+
+// One CTA per logit row: thr[row] = the k-th largest of the row's non-NaN
+// values (repeats counted), -inf when it has fewer than k of them.  A
+// most-significant-digit radix select over fkey with per-warp histograms: bf16
+// values fill only the top 16 bits of the key (digits of 10 and 6 bits; the
+// wide first digit spreads logits, which crowd into a few exponents), fp32
+// values all 32 (four 8-bit digits).
+template <int DT>
+__global__ void __launch_bounds__(kThreads) k_topk(const void* zt, const void* zd, int gamma,
+                                                  int64_t V, int k, float* __restrict__ thr) {
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kPasses = (DT == SV_BF16) ? 2 : 4;
+  constexpr int kMaxBins = (DT == SV_BF16) ? 1024 : 256;
+  __shared__ uint32_t hist[kWarps][kMaxBins];
+  __shared__ uint32_t s_sel[3];  // prefix, rank still to find within it, fewer-than-k flag
+  const int R1 = 2 * gamma + 1;
+  const int row = blockIdx.x;
+  const int b = row / R1, kk = row - b * R1;
+  const char* base = row_ptr<DT>(zt, zd, b, kk, gamma, V);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t prefix = 0, mask = 0, remaining = (uint32_t)k;
+  int shift = 32;
+  bool few = false;
+  for (int pass = 0; pass < kPasses && !few; ++pass) {
+    const int width = (DT == SV_BF16) ? (pass == 0 ? 10 : 6) : 8;
+    shift -= width;
+    const uint32_t dmask = (1u << width) - 1u;
+    const int nbins = 1 << width;
+    for (int i = threadIdx.x; i < kWarps * kMaxBins; i += blockDim.x) (&hist[0][0])[i] = 0u;
+    __syncthreads();
+    topk_pass<DT>(base, V, prefix, mask, shift, dmask, hist[warp]);
+    __syncthreads();
+    for (int d = threadIdx.x; d < nbins; d += blockDim.x) {  // sum the warps' copies
+      uint32_t n = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) n += hist[w][d];
+      hist[0][d] = n;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds `per` digits from top - l*per down; counts accumulate from the top
+      const int per = nbins / 32;
+      const int top = nbins - 1 - per * lane;
+      uint32_t cl = 0;
+      for (int j = 0; j < per; ++j) cl += hist[0][top - j];
+      uint32_t incl = cl;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const uint32_t excl = incl - cl;
+      const bool mine = excl < remaining && remaining <= incl;
+      if (__ballot_sync(0xffffffffu, mine) == 0u) {
+        if (lane == 0) s_sel[2] = 1u;  // fewer than k ranked values: nothing is cut
+      } else if (mine) {
+        uint32_t above = excl;
+        int d = top;
+        for (int j = 0; j < per; ++j, --d) {
+          const uint32_t n = hist[0][d];
+          if (above + n >= remaining) break;
+          above += n;
+        }
+        s_sel[0] = prefix | ((uint32_t)d << shift);
+        s_sel[1] = remaining - above;
+        s_sel[2] = 0u;
+      }
+    }
+    __syncthreads();
+    few = s_sel[2] != 0u;
+    prefix = s_sel[0];
+    remaining = s_sel[1];
+    mask |= dmask << shift;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    float tau = -kInf;
+    if (!few) {
+      // bf16 keys leave the low 16 bits to the sign: 0 for a positive value, 1s otherwise
+      const uint32_t key =
+          (DT == SV_BF16) ? (prefix | ((prefix & 0x80000000u) ? 0u : 0xFFFFu)) : prefix;
+      tau = fkey_inv(key);
+    }
+    thr[row] = tau;
+  }
+}
+
+// --------------------------------------------------------------------------
 // Draw of the target's own token.
 // --------------------------------------------------------------------------
 // One CTA per (batch row, gpc 4-entry groups).  Every CTA of a batch row first
@@ -283,7 +412,7 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
 // first CTA of the batch row also writes the row statistics, the accepted
 // prefix, p, q, the count and the draw state.  Then the CTA's top-2 keys of the
 // draw go to its slot; the merge kernel that follows picks the token.
-template <int DT>
+template <int DT, bool TOPK>
 __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, DrawArgs a) {
   const int b = (int)(blockIdx.x / (unsigned)a.nsplit3);
   const int split = (int)(blockIdx.x - (unsigned)b * (unsigned)a.nsplit3);
@@ -304,6 +433,10 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
     if (d.x >= 0 && (int64_t)d.x < V) {
       d.zt = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, lane, gamma, V), d.x);
       d.zd = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + lane, gamma, V), d.x);
+      if (TOPK) {  // a draft token outside a row's top-k has probability 0 there
+        if (d.zt < __ldg(x.thr + (int64_t)b * R1 + lane)) d.zt = -kInf;
+        if (d.zd < __ldg(x.thr + (int64_t)b * R1 + gamma + 1 + lane)) d.zd = -kInf;
+      }
     }
     sda[lane] = d;
   }
@@ -328,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
   const int ngroups = (int)ceil_div(V, 4);
   const int g0 = split * a.gpc, g1 = min(ngroups, g0 + a.gpc);
   const PhiloxKeys pk = philox_keys(a.seed);
-  KI mine = resid ? draw_range<DT, true>(rt, rd, g0, g1, Vi, vec_ok, st, b, pk, a.round)
-                  : draw_range<DT, false>(rt, rd, g0, g1, Vi, vec_ok, st, b, pk, a.round);
+  KI mine = resid ? draw_range<DT, true, TOPK>(rt, rd, g0, g1, Vi, vec_ok, st, b, pk, a.round)
+                  : draw_range<DT, false, TOPK>(rt, rd, g0, g1, Vi, vec_ok, st, b, pk, a.round);
   const Top2 t = block_top2(mine);
   if (threadIdx.x == 0) a.part3[(int64_t)b * a.nsplit3 + split] = t;
 }
@@ -378,7 +511,7 @@ __global__ void __launch_bounds__(kThreads) k_draw_merge(DrawArgs a) {
     DrawState sp = st;
     sp.mode = kDrawSampleRow;
     const PhiloxKeys pk = philox_keys(a.seed);
-    KI f = draw_range<DT, false>(rt, nullptr, 0, (int)ceil_div(V, 4), (int)V, (V % 4) == 0, sp,
+    KI f = draw_range<DT, false, true>(rt, nullptr, 0, (int)ceil_div(V, 4), (int)V, (V % 4) == 0, sp,
                                  (uint32_t)b, pk, a.round);
     Top2 tf = block_top2(f);
     if (tid == 0)
@@ -405,8 +538,9 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads)
 k_alpha(const void* __restrict__ zt, const void* __restrict__ zd, int gamma, int64_t V,
         float temperature, const float* __restrict__ row_T, int nsplit,
-        const RowStat* __restrict__ rowstat, float* __restrict__ part,
-        uint32_t* __restrict__ counter, float* __restrict__ out_alpha) {
+        const RowStat* __restrict__ rowstat, const float* __restrict__ thr,
+        float* __restrict__ part, uint32_t* __restrict__ counter,
+        float* __restrict__ out_alpha) {
   const int64_t per_b = (int64_t)gamma * nsplit;
   const int b = (int)(blockIdx.x / per_b);
   const int rem = (int)(blockIdx.x - b * per_b);
@@ -421,10 +555,14 @@ k_alpha(const void* __restrict__ zt, const void* __restrict__ zd, int gamma, int
   const char* rt = row_ptr<DT>(zt, zd, b, i, gamma, V);
   const char* rd = row_ptr<DT>(zt, zd, b, gamma + 1 + i, gamma, V);
   const int64_t lo = (int64_t)split * kChunkSweep, hi = min(V, lo + kChunkSweep);
+  // top-k thresholds of the two rows (-inf: no adjustment)
+  const float tt = thr ? thr[(int64_t)b * R1 + i] : -kInf;
+  const float td = thr ? thr[(int64_t)b * R1 + gamma + 1 + i] : -kInf;
   float acc = 0.0f;
   for (int64_t v = lo + threadIdx.x; v < hi; v += blockDim.x) {
-    const float pt = (it > 0.0f) ? ex2(fmaf(load_logit<DT>(rt, v), c, -rs_t.mc)) * it : 0.0f;
-    const float pd = (id > 0.0f) ? ex2(fmaf(load_logit<DT>(rd, v), c, -rs_d.mc)) * id : 0.0f;
+    const float zt = load_logit<DT>(rt, v), zd = load_logit<DT>(rd, v);
+    const float pt = (it > 0.0f && !(zt < tt)) ? ex2(fmaf(zt, c, -rs_t.mc)) * it : 0.0f;
+    const float pd = (id > 0.0f && !(zd < td)) ? ex2(fmaf(zd, c, -rs_d.mc)) * id : 0.0f;
     acc += fminf(pt, pd);
   }
 #pragma unroll
@@ -455,9 +593,20 @@ k_alpha(const void* __restrict__ zt, const void* __restrict__ zd, int gamma, int
 // Per-device launch facts for the persistent sweep, looked up once per device.
 struct DeviceInfo {
   int sms = 0;
-  int sweep_ctas_per_sm[2] = {0, 0};  // by dtype
+  int sweep_ctas_per_sm[2][2] = {{0, 0}, {0, 0}};  // by dtype, then top-k variant
   bool ready = false;
 };
+
+template <int DT, bool TOPK>
+static cudaError_t sweep_setup(DeviceInfo& d) {
+  const int smem = (int)sweep_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(k_sweep_tma<DT, TOPK>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sweep_ctas_per_sm[DT][TOPK ? 1 : 0],
+                                                       k_sweep_tma<DT, TOPK>, kSweepWarps * 32,
+                                                       smem);
+}
 static std::mutex g_dev_mu;
 static DeviceInfo g_dev[64];
 
@@ -471,18 +620,10 @@ static cudaError_t device_info(DeviceInfo** out) {
   if (!d.ready) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int smem = (int)sweep_smem_bytes();
-    e = cudaFuncSetAttribute(k_sweep_tma<SV_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_sweep_tma<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sweep_ctas_per_sm[SV_F32],
-                                                      k_sweep_tma<SV_F32>, kSweepWarps * 32, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sweep_ctas_per_sm[SV_BF16],
-                                                      k_sweep_tma<SV_BF16>, kSweepWarps * 32, smem);
-    if (e != cudaSuccess) return e;
+    if ((e = sweep_setup<SV_F32, false>(d)) != cudaSuccess) return e;
+    if ((e = sweep_setup<SV_BF16, false>(d)) != cudaSuccess) return e;
+    if ((e = sweep_setup<SV_F32, true>(d)) != cudaSuccess) return e;
+    if ((e = sweep_setup<SV_BF16, true>(d)) != cudaSuccess) return e;
 
     d.ready = true;
   }
@@ -496,7 +637,8 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
                                    uint64_t seed, uint64_t round, int32_t* out_tokens,
                                    int32_t* out_counts, float* out_p, float* out_q,
                                    float* out_alpha, uint8_t* out_flags, char* ws,
-                                   const SamplePlan& pl, cudaStream_t stream, float lenience) {
+                                   const SamplePlan& pl, cudaStream_t stream, float lenience,
+                                   int top_k) {
   const int R1 = pl.R1;
   uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + pl.off_cnt);
   float2* part1 = reinterpret_cast<float2*>(ws + pl.off_part1);
@@ -504,27 +646,42 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   DrawState* state = reinterpret_cast<DrawState*>(ws + pl.off_state);
   Top2* part3 = reinterpret_cast<Top2*>(ws + pl.off_part3);
   float* apart = reinterpret_cast<float*>(ws + pl.off_alpha);
+  float* thr = reinterpret_cast<float*>(ws + pl.off_thr);
   uint32_t* alpha_cnt = cnt;
   DeviceInfo* di = nullptr;
   {
     const cudaError_t e = device_info(&di);
     if (e != cudaSuccess) return e;
   }
-  const bool tma = use_tma_sweep(DT, V) && di->sweep_ctas_per_sm[DT] > 0;
+  // top-k adjusts the rows only when it cuts something: k < V
+  const bool topk = top_k > 0 && (int64_t)top_k < V;
+  const int tk = topk ? 1 : 0;
+  const bool tma = use_tma_sweep(DT, V) && di->sweep_ctas_per_sm[DT][tk] > 0;
   const int nch = (int)(tma ? ceil_div(V, tma_chunk_elems(DT)) : ceil_div(V, kChunkSweep));
   SweepCtx sx{zt, zd, xt, B, gamma, V, temperature, row_T, seed, round, nch, part1, rowstat,
-              state, out_tokens, out_counts, out_p, out_q, out_flags, 1.0f / lenience};
+              state, out_tokens, out_counts, out_p, out_q, out_flags, 1.0f / lenience,
+              topk ? thr : nullptr};
   mark(0, stream);
+  if (topk)
+    k_topk<DT><<<(unsigned)((int64_t)B * R1), kThreads, 0, stream>>>(zt, zd, gamma, V, top_k,
+                                                                        thr);
   if (tma) {
     // one resident wave of warps, chunks dealt round-robin
     const int64_t nc = (int64_t)B * R1 * nch;
-    const int64_t full = (int64_t)di->sms * di->sweep_ctas_per_sm[DT];
+    const int64_t full = (int64_t)di->sms * di->sweep_ctas_per_sm[DT][tk];
     const int64_t need = ceil_div(nc, kSweepWarps);
     const int64_t g = full < need ? full : need;
-    k_sweep_tma<DT><<<(unsigned)(g < 1 ? 1 : g), kSweepWarps * 32, sweep_smem_bytes(), stream>>>(
-        sx);
+    const dim3 grid((unsigned)(g < 1 ? 1 : g));
+    if (topk)
+      k_sweep_tma<DT, true><<<grid, kSweepWarps * 32, sweep_smem_bytes(), stream>>>(sx);
+    else
+      k_sweep_tma<DT, false><<<grid, kSweepWarps * 32, sweep_smem_bytes(), stream>>>(sx);
   } else {
-    k_sweep<DT><<<(unsigned)((int64_t)nch * B * R1), kThreads, 0, stream>>>(sx);
+    const dim3 grid((unsigned)((int64_t)nch * B * R1));
+    if (topk)
+      k_sweep<DT, true><<<grid, kThreads, 0, stream>>>(sx);
+    else
+      k_sweep<DT, false><<<grid, kThreads, 0, stream>>>(sx);
   }
   mark(1, stream);
   // One resident wave of draw CTAs when the batch allows: every CTA takes its
@@ -538,8 +695,10 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   nsplit = ceil_div(ngroups, gpc);  // no CTA without groups
   DrawArgs da{zt, zd, B, gamma, V, seed, round, state, alpha_cnt, part3, (int)nsplit, (int)gpc,
               out_tokens, out_flags};
-  cudaError_t e = launch_pdl(k_draw<DT>, dim3((unsigned)(nsplit * B)), dim3(kThreads), 0, stream,
-                             sx, da);
+  cudaError_t e = topk ? launch_pdl(k_draw<DT, true>, dim3((unsigned)(nsplit * B)),
+                                    dim3(kThreads), 0, stream, sx, da)
+                       : launch_pdl(k_draw<DT, false>, dim3((unsigned)(nsplit * B)),
+                                    dim3(kThreads), 0, stream, sx, da);
   if (e != cudaSuccess) return e;
   mark(2, stream);
   e = launch_pdl(k_draw_merge<DT>, dim3((unsigned)B), dim3(kThreads), 0, stream, da);
@@ -548,7 +707,7 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   if (out_alpha) {
     const int ns = (int)ceil_div(V, kChunkSweep);
     k_alpha<DT><<<(unsigned)((int64_t)ns * gamma * B), kThreads, 0, stream>>>(
-        zt, zd, gamma, V, temperature, row_T, ns, rowstat, apart, alpha_cnt, out_alpha);
+        zt, zd, gamma, V, temperature, row_T, ns, rowstat, sx.thr, apart, alpha_cnt, out_alpha);
   }
   return cudaGetLastError();
 }
@@ -557,15 +716,16 @@ cudaError_t launch_sample(const void* zt, const void* zd, const int32_t* xt, int
                           int64_t V, int dtype, float temperature, const float* row_T,
                           uint64_t seed, uint64_t round, int32_t* out_tokens, int32_t* out_counts,
                           float* out_p, float* out_q, float* out_alpha, uint8_t* out_flags,
-                          void* ws, const SamplePlan& pl, cudaStream_t stream, float lenience) {
+                          void* ws, const SamplePlan& pl, cudaStream_t stream, float lenience,
+                          int top_k) {
   char* w = reinterpret_cast<char*>(ws);
   if (dtype == SV_F32)
     return launch_sample_t<SV_F32>(zt, zd, xt, B, gamma, V, temperature, row_T, seed, round,
                                    out_tokens, out_counts, out_p, out_q, out_alpha, out_flags, w,
-                                   pl, stream, lenience);
+                                   pl, stream, lenience, top_k);
   return launch_sample_t<SV_BF16>(zt, zd, xt, B, gamma, V, temperature, row_T, seed, round,
                                   out_tokens, out_counts, out_p, out_q, out_alpha, out_flags, w,
-                                  pl, stream, lenience);
+                                  pl, stream, lenience, top_k);
 }
 
 }  // namespace sv

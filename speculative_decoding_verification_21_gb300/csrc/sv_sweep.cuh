@@ -52,9 +52,10 @@ __device__ __forceinline__ void lane_raise_max(float m, float c, float& zmax, fl
 // One full 4 KB chunk, each lane holding 8 of its 256 vectors (read from the
 // shared-memory stage beforehand, so that the stage can be refilled first).
 // The maximum is a packed tree over the raw words, then one exp2 per logit.
-template <int DT>
-__device__ __forceinline__ void chunk_update_full(const uint4 (&v)[8], float c, float& zmax,
-                                                  float& mc, float& sacc) {
+// With TOPK, logits below tau (the row's top-k threshold) add nothing to the sum.
+template <int DT, bool TOPK = false>
+__device__ __forceinline__ void chunk_update_full(const uint4 (&v)[8], float c, float tau,
+                                                  float& zmax, float& mc, float& sacc) {
   float m;
   if constexpr (DT == SV_BF16) {
     uint32_t a[8];
@@ -95,11 +96,15 @@ __device__ __forceinline__ void chunk_update_full(const uint4 (&v)[8], float c, 
     const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
     for (int q = 0; q < 4; q += (DT == SV_BF16) ? 1 : 2) {
-      const uint64_t z2 = (DT == SV_BF16)
-                              ? pack2(bf16lo(w[q]), bf16hi(w[q]))
-                              : pack2(__uint_as_float(w[q]), __uint_as_float(w[q + 1]));
+      const float za = (DT == SV_BF16) ? bf16lo(w[q]) : __uint_as_float(w[q]);
+      const float zb = (DT == SV_BF16) ? bf16hi(w[q]) : __uint_as_float(w[q + 1]);
+      const uint64_t z2 = pack2(za, zb);
       float y0, y1;
       unpack2(ffma2(z2, c2, nm2), y0, y1);
+      if (TOPK) {
+        y0 = (za < tau) ? -kInf : y0;
+        y1 = (zb < tau) ? -kInf : y1;
+      }
       s01 = fadd2(s01, pack2(ex2(y0), ex2(y1)));
     }
     if (u & 1) {

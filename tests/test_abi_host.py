@@ -77,7 +77,7 @@ def test_spec_verify_opts_argument_errors():
     L = sv.load()
     for bad in (0.0, -0.25, 1.0000001, 2.0, float("nan"), float("inf")):
         assert _svo(L, lenience=bad) == -1, bad
-    assert _svo(L, top_k=5) == -6
+    assert _svo(L, top_k=-1) == -1
     assert _svo(L, top_p=0.9) == -6
     # the remaining arguments are checked as by spec_verify
     assert _svo(L, lenience=0.5, g=0) == -1
