@@ -145,16 +145,19 @@ def _dtype_code(a: np.ndarray) -> int:
 class _Options(ctypes.Structure):
     """svo_options (sv_oracle.h)."""
     _fields_ = [("lenience", ctypes.c_double), ("top_k", ctypes.c_int),
-                ("top_p", ctypes.c_double)]
+                ("top_p", ctypes.c_double), ("nucleus_gap", ctypes.c_void_p)]
 
 
 def spec_verify(zt, zd, xt, temperature=1.0, row_temperature=None, seed=0, rnd=0,
-                want_beta=False, rows=None, threads=1, lenience=1.0, top_k=0):
+                want_beta=False, rows=None, threads=1, lenience=1.0, top_k=0, top_p=1.0):
     """Sampling verify.  zt [B,g+1,V], zd [B,g,V] (float32 or bf16 bits as uint16),
     xt [B,g] int32.  Returns a dict of numpy arrays.
 
     lenience: l in (0, 1]; a draft is accepted iff u <= p / (l q) (1: exact).
     top_k: keep the entries of every row at or above its k-th largest logit (0: off).
+    top_p: then keep each row's nucleus of probability top_p (1: off); the output
+    "nucleus_gap" [B] is the smallest distance of top_p from a cut's cumulative
+    probabilities in the batch row.
 
     rows: optional list of batch-row indices to compute (others left zero);
     threads: run disjoint row ranges in that many Python threads (each a plain
@@ -173,7 +176,8 @@ def spec_verify(zt, zd, xt, temperature=1.0, row_temperature=None, seed=0, rnd=0
         flags=np.zeros(B, np.uint8))
     L = lib()
 
-    opt = _Options(float(lenience), int(top_k), 1.0)
+    out["nucleus_gap"] = np.full(B, np.inf)
+    opt = _Options(float(lenience), int(top_k), float(top_p), _ptr(out["nucleus_gap"]))
 
     def run(b0, b1):
         rc = L.svo_spec_verify_ex(

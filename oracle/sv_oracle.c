@@ -151,9 +151,10 @@ static double logit_at(const void* base, int dtype, int64_t idx) {
 }
 
 typedef struct {
-  double* s;  /* scaled logits s_v = z_v * invT          */
-  double m;   /* max_v s_v                                */
-  double S;   /* sum_v exp(s_v - m), 0 if no finite entry */
+  double* s;   /* scaled logits s_v = z_v * invT          */
+  double m;    /* max_v s_v                                */
+  double S;    /* sum_v exp(s_v - m), 0 if no finite entry */
+  double gap;  /* top-p: distance of top_p from the cumulative masses around the cut */
 } row_t;
 
 /* Descending order for qsort. */
@@ -178,14 +179,7 @@ static double kth_largest(const double* s, int64_t V, int k, double* buf) {
  * entry below the k-th largest scaled logit gets weight 0 (-inf); entries equal
  * to it are kept, and NaN entries are left as they are (they mark the row
  * non-finite).  `buf` holds V doubles. */
-static void load_row(row_t* r, const void* base, int dtype, int64_t off, int64_t V, double invT,
-                     int top_k, double* buf) {
-  for (int64_t v = 0; v < V; ++v) r->s[v] = logit_at(base, dtype, off + v) * invT;
-  if (top_k > 0) {
-    const double tau = kth_largest(r->s, V, top_k, buf);
-    for (int64_t v = 0; v < V; ++v)
-      if (r->s[v] < tau) r->s[v] = -INFINITY;
-  }
+static void row_stats(row_t* r, int64_t V) {
   double m = -INFINITY;
   for (int64_t v = 0; v < V; ++v)
     if (r->s[v] > m) m = r->s[v];
@@ -194,6 +188,51 @@ static void load_row(row_t* r, const void* base, int dtype, int64_t off, int64_t
     for (int64_t v = 0; v < V; ++v) S += exp(r->s[v] - m);
   r->m = m;
   r->S = S;
+}
+
+/* Top-p (nucleus; [A3]: nucleus zeroes the tail and renormalises): the
+ * smallest set of largest-logit entries whose probability reaches top_p,
+ * with every entry equal to the last one kept.  Groups of equal scaled logits
+ * are added largest first; the cut is the first group at which the cumulative
+ * probability reaches top_p.  r->gap is the distance of top_p from the
+ * cumulative probabilities just before and at the cut.  Rows that are empty
+ * or not finite are left as they are. */
+static void nucleus(row_t* r, int64_t V, double top_p, double* buf) {
+  r->gap = INFINITY;
+  if (!(top_p < 1.0) || !(r->S > 0.0) || !isfinite(r->S) || !isfinite(r->m)) return;
+  int64_t n = 0;
+  for (int64_t v = 0; v < V; ++v)
+    if (r->s[v] > -INFINITY) buf[n++] = r->s[v];
+  qsort(buf, (size_t)n, sizeof(double), cmp_desc);
+  double C = 0.0, prev = 0.0, tau = -INFINITY;
+  for (int64_t i = 0; i < n;) {
+    int64_t j = i;
+    while (j < n && buf[j] == buf[i]) ++j;
+    C += (double)(j - i) * exp(buf[i] - r->m) / r->S;
+    if (C >= top_p) {
+      tau = buf[i];
+      r->gap = fmin(C - top_p, top_p - prev);
+      break;
+    }
+    prev = C;
+    i = j;
+  }
+  if (tau == -INFINITY) return; /* rounding left the total below top_p: keep all */
+  for (int64_t v = 0; v < V; ++v)
+    if (r->s[v] < tau) r->s[v] = -INFINITY;
+  row_stats(r, V);
+}
+
+static void load_row(row_t* r, const void* base, int dtype, int64_t off, int64_t V, double invT,
+                     int top_k, double top_p, double* buf) {
+  for (int64_t v = 0; v < V; ++v) r->s[v] = logit_at(base, dtype, off + v) * invT;
+  if (top_k > 0) {
+    const double tau = kth_largest(r->s, V, top_k, buf);
+    for (int64_t v = 0; v < V; ++v)
+      if (r->s[v] < tau) r->s[v] = -INFINITY;
+  }
+  row_stats(r, V);
+  nucleus(r, V, top_p, buf);
 }
 
 static double prob(const row_t* r, int64_t v) {
@@ -282,8 +321,9 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
   /* Lenience l (Appendix A.5 as the page summarises it): the comparison uses l q(x). */
   const double l = opt ? opt->lenience : 1.0;
   const int top_k = opt ? opt->top_k : 0;
+  const double top_p = opt ? opt->top_p : 1.0;
   if (!(l > 0.0 && l <= 1.0)) return -1;
-  if (top_k < 0 || (opt && opt->top_p != 1.0)) return -1;
+  if (top_k < 0 || !(top_p > 0.0 && top_p <= 1.0)) return -1;
   if (B < 0 || gamma < 1 || gamma > 64 || V < 1 || (dtype != SVO_F32 && dtype != SVO_BF16))
     return -1;
   if (b_begin < 0 || b_end > B || b_begin > b_end) return -1;
@@ -301,8 +341,8 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
       return -1;
     }
   }
-  double* kbuf = NULL; /* scratch of the top-k selection */
-  if (top_k > 0) {
+  double* kbuf = NULL; /* scratch of the top-k and top-p selections */
+  if (top_k > 0 || top_p < 1.0) {
     kbuf = (double*)malloc((size_t)V * sizeof(double));
     if (!kbuf) {
       for (int r = 0; r < R; ++r) free(rows[r].s);
@@ -319,14 +359,18 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
     uint8_t flag = 0;
 
     for (int i = 0; i <= gamma; ++i)
-      load_row(&rows[i], zt, dtype, ((int64_t)b * (gamma + 1) + i) * V, V, invT, top_k, kbuf);
+      load_row(&rows[i], zt, dtype, ((int64_t)b * (gamma + 1) + i) * V, V, invT, top_k, top_p,
+               kbuf);
     for (int i = 0; i < gamma; ++i)
       load_row(&rows[gamma + 1 + i], zd, dtype, ((int64_t)b * gamma + i) * V, V, invT, top_k,
-               kbuf);
+               top_p, kbuf);
+    double ngap = INFINITY;
     for (int r = 0; r < R; ++r) {
       if (rows[r].m == -INFINITY) flag |= SVO_FLAG_ZERO_MASS;
       if (row_nonfinite(&rows[r])) flag |= SVO_FLAG_NONFINITE;
+      ngap = fmin(ngap, rows[r].gap);
     }
+    if (opt && opt->nucleus_gap) opt->nucleus_gap[b] = ngap;
 
     /* p(x~_i), q(x~_i) and the ratio for every draft position. */
     double P[64], Q[64], RATIO[64], U[64];

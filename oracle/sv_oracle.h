@@ -91,12 +91,17 @@ int svo_spec_verify_rows(const void* zt, const void* zd, const int32_t* xt,
  * top_k (same page, "already adjusted" distributions: top-k zeroes the tail and
  * renormalises): with top_k > 0 every target and draft row keeps the entries
  * whose scaled logit is at least its k-th largest (ties at the boundary kept,
- * NaN left in place), the rest get probability 0; 0 is off.  top_p is reserved
- * (1: off) and must keep that value. */
+ * NaN left in place), the rest get probability 0; 0 is off.
+ * top_p (nucleus, same passage), after top-k: every row keeps the smallest set
+ * of largest-logit entries whose probability reaches top_p (entries equal to
+ * the last one kept too); 1 is off.  nucleus_gap (optional output, [B]): per
+ * batch row the smallest distance of top_p from the cumulative probabilities
+ * just before and at a row's cut (inf without a cut). */
 typedef struct {
-  double lenience; /* in (0, 1] */
-  int top_k;       /* >= 0 */
-  double top_p;    /* 1 */
+  double lenience;     /* in (0, 1] */
+  int top_k;           /* >= 0 */
+  double top_p;        /* in (0, 1] */
+  double* nucleus_gap; /* [B] or NULL */
 } svo_options;
 
 /* svo_spec_verify_rows with options (NULL: the exact round). */
