@@ -372,6 +372,7 @@ def run_ours(args):
         extra["lenience"] = measure_options(L, stream, sets, tokens, counts, flags, ws,
                                             lenience=0.5)
         extra["top_k"] = measure_options(L, stream, sets, tokens, counts, flags, ws, top_k=50)
+        extra["top_p"] = measure_options(L, stream, sets, tokens, counts, flags, ws, top_p=0.9)
 
     if rank == 0:
         line = {
@@ -399,20 +400,21 @@ def run_ours(args):
 
 
 def measure_options(L, stream, sets, tokens, counts, flags, ws, lenience=1.0, top_k=0,
-                    reps=400):
+                    top_p=1.0, reps=400):
     """spec_verify_opts on the same rotating sample_b64 sets.  Lenience l: the
     comparison u <= p/(l q) costs the same kernels and accepts more.  top_k:
     one radix-select pass over every row before the sweep, and the round on the
-    adjusted rows."""
+    adjusted rows.  top_p: a sweep for the row maxima, the nucleus cut, then the
+    round on the adjusted rows."""
     import torch
     from speculative_decoding_verification_21_gb300 import _lib
     P = ctypes.c_void_p
     sh = P(stream.cuda_stream)
     B, gamma, V = 64, 4, 128256
 
-    def call(i, l, k):
+    def call(i, l, k, p):
         s = sets[i % len(sets)]
-        opts = _lib.Options(l, k, 1.0)
+        opts = _lib.Options(l, k, p)
         rc = L.spec_verify_opts(P(s.zt.data_ptr()), P(s.zd.data_ptr()), P(s.xt.data_ptr()), B,
                                 gamma, V, 1, ctypes.c_float(s.temperature), None, 0, i,
                                 P(tokens.data_ptr()), P(counts.data_ptr()), None, None, None,
@@ -422,27 +424,29 @@ def measure_options(L, stream, sets, tokens, counts, flags, ws, lenience=1.0, to
             raise RuntimeError(f"spec_verify_opts failed ({rc})")
 
     acc = {}
-    for key, (l, k) in (("plain", (1.0, 0)), ("variant", (lenience, top_k))):
+    for key, (l, k, p) in (("plain", (1.0, 0, 1.0)), ("variant", (lenience, top_k, top_p))):
         tot = 0
         for i in range(len(sets)):
-            call(i, l, k)
+            call(i, l, k, p)
             tot += int(counts.sum().item())
         acc[key] = tot / (len(sets) * B)
     for i in range(3):
-        call(i, lenience, top_k)
+        call(i, lenience, top_k, top_p)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for i in range(reps):
-        call(i, lenience, top_k)
+        call(i, lenience, top_k, top_p)
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / reps
     out = {"workload": "sample_b64", "rounds_per_s": 1000.0 / ms, "ms_per_round": ms,
            "mean_accepted": acc["variant"], "mean_accepted_plain": acc["plain"],
-           "gpu_launches_per_round": 4 if top_k else 3}
+           "gpu_launches_per_round": 3 + (1 if top_k else 0) + (2 if top_p < 1.0 else 0)}
     if lenience != 1.0:
         out["lenience"] = lenience
+    if top_p < 1.0:
+        out["top_p"] = top_p
     if top_k:
         out["top_k"] = top_k
         out["note"] = ("drafts are the workload's (drawn from the unadjusted q); tokens outside "

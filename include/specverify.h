@@ -131,7 +131,15 @@ int spec_verify(const void* target_logits, const void* draft_logits,
  *             section "The loop": top-k zeroes the tail and renormalises, and
  *             the round runs on the adjusted p and q).  k >= V changes nothing.
  *             Costs one radix-select pass over every row before the sweep.
- *   top_p     reserved: must be 1 (off).
+ *   top_p     in (0, 1]; 1: off.  After top-k, every row keeps the smallest set
+ *             of its largest-logit entries whose probability reaches top_p,
+ *             every entry equal to the last one kept as well (same passage:
+ *             nucleus zeroes the tail and renormalises).  The cut depends on the
+ *             temperature.  Costs a sweep for the row maxima and a radix-select
+ *             pass with exact fixed-point mass sums before the round's sweep;
+ *             where top_p lies within about 1e-6 of a cumulative probability at
+ *             the cut, the cut may differ from one taken in exact arithmetic by
+ *             that boundary group.
  */
 typedef struct {
   float lenience;
@@ -141,10 +149,10 @@ typedef struct {
 
 /*
  * spec_verify_opts -- spec_verify with sv_options (NULL: the exact round, the
- * same results as spec_verify).  A lenience outside (0, 1] (or NaN) or a
- * negative top_k returns SV_ERR_ARG; top_p != 1 returns SV_ERR_UNSUPPORTED.
- * The other arguments, outputs and errors are those of spec_verify.  With
- * top_k, p_at_draft / q_at_draft and alpha are those of the adjusted rows.
+ * same results as spec_verify).  A lenience or top_p outside (0, 1] (or NaN)
+ * or a negative top_k returns SV_ERR_ARG.  The other arguments, outputs and
+ * errors are those of spec_verify.  With top_k or top_p, p_at_draft /
+ * q_at_draft and alpha are those of the adjusted rows.
  */
 int spec_verify_opts(const void* target_logits, const void* draft_logits,
                      const int32_t* draft_tokens, int B, int gamma, int64_t V, int dtype,

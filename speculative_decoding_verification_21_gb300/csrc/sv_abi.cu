@@ -17,7 +17,7 @@ cudaError_t launch_sample(const void* zt, const void* zd, const int32_t* xt, int
                           uint64_t seed, uint64_t round, int32_t* out_tokens, int32_t* out_counts,
                           float* out_p, float* out_q, float* out_alpha, uint8_t* out_flags,
                           void* ws, const SamplePlan& pl, cudaStream_t stream,
-                          float lenience, int top_k);
+                          float lenience, int top_k, float top_p);
 cudaError_t launch_greedy(const void* zt, const int32_t* xt, int B, int gamma, int64_t V,
                           int dtype, int32_t* out_tokens, int32_t* out_counts, void* ws,
                           const GreedyPlan& pl, cudaStream_t stream);
@@ -104,13 +104,14 @@ int spec_verify_opts(const void* target_logits, const void* draft_logits,
                      float* out_p_at_draft, float* out_q_at_draft, float* out_alpha,
                      uint8_t* out_flags, const sv_options* options, void* workspace,
                      size_t workspace_bytes, void* cuda_stream) {
-  float lenience = 1.0f;
+  float lenience = 1.0f, top_p = 1.0f;
   int top_k = 0;
   if (options) {
     lenience = options->lenience;
     top_k = options->top_k;
-    if (!(lenience > 0.0f && lenience <= 1.0f) || top_k < 0) return SV_ERR_ARG;
-    if (options->top_p != 1.0f) return SV_ERR_UNSUPPORTED;
+    top_p = options->top_p;
+    if (!(lenience > 0.0f && lenience <= 1.0f) || top_k < 0 || !(top_p > 0.0f && top_p <= 1.0f))
+      return SV_ERR_ARG;
   }
   int st = check_shape(B, gamma, V);
   if (st != SV_OK) return st;
@@ -131,7 +132,7 @@ int spec_verify_opts(const void* target_logits, const void* draft_logits,
   const cudaError_t e = sv::launch_sample(
       target_logits, draft_logits, draft_tokens, B, gamma, V, dtype, temperature, row_temperature,
       seed, round, out_tokens, out_counts, out_p_at_draft, out_q_at_draft, out_alpha, out_flags,
-      workspace, pl, (cudaStream_t)cuda_stream, lenience, top_k);
+      workspace, pl, (cudaStream_t)cuda_stream, lenience, top_k, top_p);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

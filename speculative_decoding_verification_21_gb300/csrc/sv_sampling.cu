@@ -402,6 +402,132 @@ __global__ void __launch_bounds__(kThreads) k_topk(const void* zt, const void* z
   }
 }
 
+// Nucleus (top-p) threshold of one logit row (same passage: nucleus zeroes the
+// tail and renormalises).  The row keeps the smallest set of largest-logit
+// entries whose probability reaches top_p, entries equal to the last one kept
+// as well: thr = the largest logit t such that the mass of {z >= t} reaches
+// top_p of the row's mass.  One CTA per row, after a sweep that gave the row's
+// max; entries below the row's top-k threshold (thr on entry, when has_k) do
+// not count.  Masses 2^(z c - max) are summed as 40-bit fixed point in 64-bit
+// integer histograms, so the sums are exact and independent of order, by
+// most-significant-digit passes over order-preserving keys (bf16: digits of 10
+// and 6 bits; fp32: four of 8).  Empty or non-finite rows keep thr as it was.
+template <int DT>
+__global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int has_k,
+                                                  float* __restrict__ thr) {
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kPasses = (DT == SV_BF16) ? 2 : 4;
+  constexpr int kMaxBins = (DT == SV_BF16) ? 1024 : 256;
+  constexpr double kFix = 1099511627776.0;  // 2^40
+  extern __shared__ unsigned long long hist64[];  // [kWarps][kMaxBins]
+  __shared__ RowStat s_rs;
+  __shared__ uint32_t s_sel[2];       // prefix, no-cut flag
+  __shared__ double s_target;
+  const int R1 = 2 * x.gamma + 1;
+  const int row = blockIdx.x;
+  const int b = row / R1, kk = row - b * R1;
+  const int64_t V = x.V;
+  const char* base = row_ptr<DT>(x.zt, x.zd, b, kk, x.gamma, V);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float T = x.row_T ? __ldg(x.row_T + b) : x.temperature;
+  const float c = log2_scale(inv_temperature(T));
+  const float tk = has_k ? thr[row] : -kInf;
+  if (!has_k && threadIdx.x == 0) thr[row] = -kInf;  // no cut unless one is found below
+  if (warp == 0) {
+    const RowStat rs = combine_row(x.part + (int64_t)row * x.nch, x.nch, nullptr);
+    if (lane == 0) s_rs = rs;
+  }
+  __syncthreads();
+  const RowStat rs = s_rs;
+  if ((rs.bits & (kRowNaN | kRowTimeout)) || !(rs.s > 0.0) || !(rs.s < 1e300) ||
+      !(fabsf(rs.mc) < kInf))
+    return;  // empty or not finite: no cut (uniform over the CTA)
+  const float mc = rs.mc;
+  uint32_t prefix = 0, mask = 0;
+  int shift = 32;
+  double target = 0.0;  // fixed-point mass still to reach inside the current prefix
+  for (int pass = 0; pass < kPasses; ++pass) {
+    const int width = (DT == SV_BF16) ? (pass == 0 ? 10 : 6) : 8;
+    shift -= width;
+    const uint32_t dmask = (1u << width) - 1u;
+    const int nbins = 1 << width;
+    for (int i = threadIdx.x; i < kWarps * kMaxBins; i += blockDim.x) hist64[i] = 0ull;
+    __syncthreads();
+    unsigned long long* h = hist64 + warp * kMaxBins;
+    auto add = [&](float z) {
+      if (!(z >= tk)) return;  // NaN, or below the top-k threshold
+      const uint32_t key = fkey(z);
+      if ((key & mask) != prefix) return;
+      const float m = ex2(fmaf(z, c, -mc));  // <= 1
+      atomicAdd(&h[(key >> shift) & dmask], (unsigned long long)__float2ull_rn(m * (float)kFix));
+    };
+    for_each_in_chunk<DT, 4>(
+        base, 0, V,
+        [&](int64_t, const uint4& vec) {
+          float f[VecInfo<DT>::kElems];
+          unpack<DT>(vec, f);
+#pragma unroll
+          for (int e = 0; e < VecInfo<DT>::kElems; ++e) add(f[e]);
+        },
+        [&](int64_t, float z) { add(z); });
+    __syncthreads();
+    for (int d = threadIdx.x; d < nbins; d += blockDim.x) {  // sum the warps' copies
+      unsigned long long n = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) n += hist64[w * kMaxBins + d];
+      hist64[d] = n;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int per = nbins / 32;
+      const int top = nbins - 1 - per * lane;
+      unsigned long long cl = 0;
+      for (int j = 0; j < per; ++j) cl += hist64[top - j];
+      unsigned long long incl = cl;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (pass == 0) {
+        // the whole kept mass is the last lane's total
+        const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
+        target = (double)top_p * (double)total;
+      } else {
+        target = s_target;
+      }
+      const unsigned long long excl = incl - cl;
+      const bool mine = (double)excl < target && target <= (double)incl;
+      if (__ballot_sync(0xffffffffu, mine) == 0u) {
+        if (lane == 0) s_sel[1] = 1u;  // nothing to cut (no mass, or rounding at the end)
+      } else if (mine) {
+        unsigned long long above = excl;
+        int d = top;
+        for (int j = 0; j < per; ++j, --d) {
+          const unsigned long long n = hist64[d];
+          if ((double)(above + n) >= target) break;
+          above += n;
+        }
+        s_sel[0] = prefix | ((uint32_t)d << shift);
+        s_sel[1] = 0u;
+        s_target = target - (double)above;
+      }
+    }
+    __syncthreads();
+    if (s_sel[1]) return;  // keep thr as it was
+    prefix = s_sel[0];
+    target = s_target;
+    mask |= dmask << shift;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    // bf16 keys leave the low 16 bits to the sign: 0 for a positive value, 1s otherwise
+    const uint32_t key =
+        (DT == SV_BF16) ? (prefix | ((prefix & 0x80000000u) ? 0u : 0xFFFFu)) : prefix;
+    thr[row] = fkey_inv(key);
+  }
+}
+
 // --------------------------------------------------------------------------
 // Draw of the target's own token.
 // --------------------------------------------------------------------------
@@ -597,6 +723,11 @@ struct DeviceInfo {
   bool ready = false;
 };
 
+// Dynamic shared memory of k_topp: per-warp 64-bit mass histograms.
+static size_t topp_smem_bytes(int dtype) {
+  return (size_t)(kThreads / 32) * (dtype == SV_BF16 ? 1024 : 256) * sizeof(unsigned long long);
+}
+
 template <int DT, bool TOPK>
 static cudaError_t sweep_setup(DeviceInfo& d) {
   const int smem = (int)sweep_smem_bytes();
@@ -620,6 +751,9 @@ static cudaError_t device_info(DeviceInfo** out) {
   if (!d.ready) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_topp<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)topp_smem_bytes(SV_BF16));
+    if (e != cudaSuccess) return e;
     if ((e = sweep_setup<SV_F32, false>(d)) != cudaSuccess) return e;
     if ((e = sweep_setup<SV_BF16, false>(d)) != cudaSuccess) return e;
     if ((e = sweep_setup<SV_F32, true>(d)) != cudaSuccess) return e;
@@ -638,7 +772,7 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
                                    int32_t* out_counts, float* out_p, float* out_q,
                                    float* out_alpha, uint8_t* out_flags, char* ws,
                                    const SamplePlan& pl, cudaStream_t stream, float lenience,
-                                   int top_k) {
+                                   int top_k, float top_p) {
   const int R1 = pl.R1;
   uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + pl.off_cnt);
   float2* part1 = reinterpret_cast<float2*>(ws + pl.off_part1);
@@ -653,36 +787,49 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
     const cudaError_t e = device_info(&di);
     if (e != cudaSuccess) return e;
   }
-  // top-k adjusts the rows only when it cuts something: k < V
+  // top-k adjusts the rows only when it cuts something: k < V; top-p when p < 1
   const bool topk = top_k > 0 && (int64_t)top_k < V;
-  const int tk = topk ? 1 : 0;
+  const bool topp = top_p < 1.0f;
+  const bool masked = topk || topp;  // the round runs on thresholded rows
+  const int tk = masked ? 1 : 0;
   const bool tma = use_tma_sweep(DT, V) && di->sweep_ctas_per_sm[DT][tk] > 0;
   const int nch = (int)(tma ? ceil_div(V, tma_chunk_elems(DT)) : ceil_div(V, kChunkSweep));
   SweepCtx sx{zt, zd, xt, B, gamma, V, temperature, row_T, seed, round, nch, part1, rowstat,
               state, out_tokens, out_counts, out_p, out_q, out_flags, 1.0f / lenience,
-              topk ? thr : nullptr};
+              masked ? thr : nullptr};
+  auto sweep = [&](bool with_thr, const SweepCtx& ctx) {
+    if (tma) {
+      // one resident wave of warps, chunks dealt round-robin
+      const int64_t nc = (int64_t)B * R1 * nch;
+      const int64_t full = (int64_t)di->sms * di->sweep_ctas_per_sm[DT][with_thr ? 1 : 0];
+      const int64_t need = ceil_div(nc, kSweepWarps);
+      const int64_t g = full < need ? full : need;
+      const dim3 grid((unsigned)(g < 1 ? 1 : g));
+      if (with_thr)
+        k_sweep_tma<DT, true><<<grid, kSweepWarps * 32, sweep_smem_bytes(), stream>>>(ctx);
+      else
+        k_sweep_tma<DT, false><<<grid, kSweepWarps * 32, sweep_smem_bytes(), stream>>>(ctx);
+    } else {
+      const dim3 grid((unsigned)((int64_t)nch * B * R1));
+      if (with_thr)
+        k_sweep<DT, true><<<grid, kThreads, 0, stream>>>(ctx);
+      else
+        k_sweep<DT, false><<<grid, kThreads, 0, stream>>>(ctx);
+    }
+  };
   mark(0, stream);
   if (topk)
     k_topk<DT><<<(unsigned)((int64_t)B * R1), kThreads, 0, stream>>>(zt, zd, gamma, V, top_k,
                                                                         thr);
-  if (tma) {
-    // one resident wave of warps, chunks dealt round-robin
-    const int64_t nc = (int64_t)B * R1 * nch;
-    const int64_t full = (int64_t)di->sms * di->sweep_ctas_per_sm[DT][tk];
-    const int64_t need = ceil_div(nc, kSweepWarps);
-    const int64_t g = full < need ? full : need;
-    const dim3 grid((unsigned)(g < 1 ? 1 : g));
-    if (topk)
-      k_sweep_tma<DT, true><<<grid, kSweepWarps * 32, sweep_smem_bytes(), stream>>>(sx);
-    else
-      k_sweep_tma<DT, false><<<grid, kSweepWarps * 32, sweep_smem_bytes(), stream>>>(sx);
-  } else {
-    const dim3 grid((unsigned)((int64_t)nch * B * R1));
-    if (topk)
-      k_sweep<DT, true><<<grid, kThreads, 0, stream>>>(sx);
-    else
-      k_sweep<DT, false><<<grid, kThreads, 0, stream>>>(sx);
+  if (topp) {
+    // the row maxima (after top-k) for the nucleus masses, then the nucleus cut
+    SweepCtx s0 = sx;
+    s0.thr = topk ? thr : nullptr;
+    sweep(topk, s0);
+    k_topp<DT><<<(unsigned)((int64_t)B * R1), kThreads, topp_smem_bytes(DT), stream>>>(
+        sx, top_p, topk ? 1 : 0, thr);
   }
+  sweep(masked, sx);
   mark(1, stream);
   // One resident wave of draw CTAs when the batch allows: every CTA takes its
   // batch row's decision before drawing, so a second wave would pay that
@@ -695,8 +842,8 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   nsplit = ceil_div(ngroups, gpc);  // no CTA without groups
   DrawArgs da{zt, zd, B, gamma, V, seed, round, state, alpha_cnt, part3, (int)nsplit, (int)gpc,
               out_tokens, out_flags};
-  cudaError_t e = topk ? launch_pdl(k_draw<DT, true>, dim3((unsigned)(nsplit * B)),
-                                    dim3(kThreads), 0, stream, sx, da)
+  cudaError_t e = masked ? launch_pdl(k_draw<DT, true>, dim3((unsigned)(nsplit * B)),
+                                      dim3(kThreads), 0, stream, sx, da)
                        : launch_pdl(k_draw<DT, false>, dim3((unsigned)(nsplit * B)),
                                     dim3(kThreads), 0, stream, sx, da);
   if (e != cudaSuccess) return e;
@@ -717,15 +864,15 @@ cudaError_t launch_sample(const void* zt, const void* zd, const int32_t* xt, int
                           uint64_t seed, uint64_t round, int32_t* out_tokens, int32_t* out_counts,
                           float* out_p, float* out_q, float* out_alpha, uint8_t* out_flags,
                           void* ws, const SamplePlan& pl, cudaStream_t stream, float lenience,
-                          int top_k) {
+                          int top_k, float top_p) {
   char* w = reinterpret_cast<char*>(ws);
   if (dtype == SV_F32)
     return launch_sample_t<SV_F32>(zt, zd, xt, B, gamma, V, temperature, row_T, seed, round,
                                    out_tokens, out_counts, out_p, out_q, out_alpha, out_flags, w,
-                                   pl, stream, lenience, top_k);
+                                   pl, stream, lenience, top_k, top_p);
   return launch_sample_t<SV_BF16>(zt, zd, xt, B, gamma, V, temperature, row_T, seed, round,
                                   out_tokens, out_counts, out_p, out_q, out_alpha, out_flags, w,
-                                  pl, stream, lenience, top_k);
+                                  pl, stream, lenience, top_k, top_p);
 }
 
 }  // namespace sv

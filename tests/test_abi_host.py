@@ -78,7 +78,8 @@ def test_spec_verify_opts_argument_errors():
     for bad in (0.0, -0.25, 1.0000001, 2.0, float("nan"), float("inf")):
         assert _svo(L, lenience=bad) == -1, bad
     assert _svo(L, top_k=-1) == -1
-    assert _svo(L, top_p=0.9) == -6
+    for bad in (0.0, -0.5, 1.5, float("nan")):
+        assert _svo(L, top_p=bad) == -1, bad
     # the remaining arguments are checked as by spec_verify
     assert _svo(L, lenience=0.5, g=0) == -1
     assert _svo(L, lenience=0.5, dt=7) == -2
