@@ -139,7 +139,8 @@ int spec_verify(const void* target_logits, const void* draft_logits,
  *             pass with exact fixed-point mass sums before the round's sweep;
  *             where top_p lies within about 1e-6 of a cumulative probability at
  *             the cut, the cut may differ from one taken in exact arithmetic by
- *             that boundary group.
+ *             that boundary group.  top_p < 1 needs V <= 2^21
+ *             (SV_ERR_UNSUPPORTED otherwise).
  */
 typedef struct {
   float lenience;

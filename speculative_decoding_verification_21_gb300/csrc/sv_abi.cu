@@ -112,6 +112,7 @@ int spec_verify_opts(const void* target_logits, const void* draft_logits,
     top_p = options->top_p;
     if (!(lenience > 0.0f && lenience <= 1.0f) || top_k < 0 || !(top_p > 0.0f && top_p <= 1.0f))
       return SV_ERR_ARG;
+    if (top_p < 1.0f && V > (int64_t(1) << 21)) return SV_ERR_UNSUPPORTED;  // nucleus sums
   }
   int st = check_shape(B, gamma, V);
   if (st != SV_OK) return st;

@@ -408,10 +408,13 @@ __global__ void __launch_bounds__(kThreads) k_topk(const void* zt, const void* z
 // as well: thr = the largest logit t such that the mass of {z >= t} reaches
 // top_p of the row's mass.  One CTA per row, after a sweep that gave the row's
 // max; entries below the row's top-k threshold (thr on entry, when has_k) do
-// not count.  Masses 2^(z c - max) are summed as 40-bit fixed point in 64-bit
-// integer histograms, so the sums are exact and independent of order, by
-// most-significant-digit passes over order-preserving keys (bf16: digits of 10
-// and 6 bits; fp32: four of 8).  Empty or non-finite rows keep thr as it was.
+// not count.  Masses 2^(z c - max) are summed as 40-bit fixed point, so the
+// sums are exact and independent of order, by most-significant-digit passes
+// over order-preserving keys (bf16: digits of 10 and 6 bits; fp32: four of 8).
+// Each mass goes in three 14-bit parts to three 32-bit per-warp histograms
+// (native shared-memory atomics; a warp adds at most 2^18 entries, so no part
+// overflows for V <= 2^21), combined in 64 bits per digit afterwards.  Empty or
+// non-finite rows keep thr as it was.
 template <int DT>
 __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int has_k,
                                                   float* __restrict__ thr) {
@@ -419,7 +422,7 @@ __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int 
   constexpr int kPasses = (DT == SV_BF16) ? 2 : 4;
   constexpr int kMaxBins = (DT == SV_BF16) ? 1024 : 256;
   constexpr double kFix = 1099511627776.0;  // 2^40
-  extern __shared__ unsigned long long hist64[];  // [kWarps][kMaxBins]
+  extern __shared__ unsigned long long hist64[];  // [kMaxBins] combined, then parts
   __shared__ RowStat s_rs;
   __shared__ uint32_t s_sel[2];       // prefix, no-cut flag
   __shared__ double s_target;
@@ -451,15 +454,22 @@ __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int 
     shift -= width;
     const uint32_t dmask = (1u << width) - 1u;
     const int nbins = 1 << width;
-    for (int i = threadIdx.x; i < kWarps * kMaxBins; i += blockDim.x) hist64[i] = 0ull;
+    uint32_t* parts = reinterpret_cast<uint32_t*>(hist64 + kMaxBins);  // [3][kWarps][kMaxBins]
+    for (int i = threadIdx.x; i < 3 * kWarps * kMaxBins; i += blockDim.x) parts[i] = 0u;
     __syncthreads();
-    unsigned long long* h = hist64 + warp * kMaxBins;
+    uint32_t* h0 = parts + warp * kMaxBins;
+    uint32_t* h1 = h0 + kWarps * kMaxBins;
+    uint32_t* h2 = h1 + kWarps * kMaxBins;
     auto add = [&](float z) {
       if (!(z >= tk)) return;  // NaN, or below the top-k threshold
       const uint32_t key = fkey(z);
       if ((key & mask) != prefix) return;
       const float m = ex2(fmaf(z, c, -mc));  // <= 1
-      atomicAdd(&h[(key >> shift) & dmask], (unsigned long long)__float2ull_rn(m * (float)kFix));
+      const unsigned long long f = __float2ull_rn(m * (float)kFix);
+      const uint32_t d = (key >> shift) & dmask;
+      atomicAdd(&h0[d], (uint32_t)(f & 0x3FFFu));
+      atomicAdd(&h1[d], (uint32_t)((f >> 14) & 0x3FFFu));
+      atomicAdd(&h2[d], (uint32_t)(f >> 28));
     };
     for_each_in_chunk<DT, 4>(
         base, 0, V,
@@ -474,7 +484,12 @@ __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int 
     for (int d = threadIdx.x; d < nbins; d += blockDim.x) {  // sum the warps' copies
       unsigned long long n = 0;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) n += hist64[w * kMaxBins + d];
+      for (int w = 0; w < kWarps; ++w) {
+        const int i = w * kMaxBins + d;
+        n += (unsigned long long)parts[i] +
+             ((unsigned long long)parts[kWarps * kMaxBins + i] << 14) +
+             ((unsigned long long)parts[2 * kWarps * kMaxBins + i] << 28);
+      }
       hist64[d] = n;
     }
     __syncthreads();
@@ -723,9 +738,11 @@ struct DeviceInfo {
   bool ready = false;
 };
 
-// Dynamic shared memory of k_topp: per-warp 64-bit mass histograms.
+// Dynamic shared memory of k_topp: the combined 64-bit histogram, then three
+// 32-bit per-warp histograms of the mass parts.
 static size_t topp_smem_bytes(int dtype) {
-  return (size_t)(kThreads / 32) * (dtype == SV_BF16 ? 1024 : 256) * sizeof(unsigned long long);
+  const size_t bins = dtype == SV_BF16 ? 1024 : 256;
+  return bins * sizeof(unsigned long long) + 3 * (size_t)(kThreads / 32) * bins * sizeof(uint32_t);
 }
 
 template <int DT, bool TOPK>
