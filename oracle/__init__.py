@@ -83,6 +83,10 @@ def lib():
             L.svo_spec_verify_greedy.argtypes = [P, P, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_int64, ctypes.c_int, P, P]
             L.svo_spec_verify_greedy.restype = ctypes.c_int
+            L.svo_draft_sample.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                           ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int, P, P,
+                                           P, P]
+            L.svo_draft_sample.restype = ctypes.c_int
             L.svo_lmhead_logits.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                             P, ctypes.c_int64, P]
             _lib = L
@@ -218,6 +222,20 @@ def spec_verify_greedy(zt, xt):
     if rc != 0:
         raise ValueError(f"oracle spec_verify_greedy rejected its arguments (rc={rc})")
     return dict(tokens=tokens, counts=counts)
+
+
+def draft_sample(logits, temperature=1.0, seed=0, rnd=0, pos=0):
+    """Draft sampling of one position from logits [B, V] (float32): Gumbel-max with
+    Philox tag 2.  Returns tokens [B], q [B] = q(x), lse [B], gap [B]."""
+    z = np.ascontiguousarray(logits, dtype=np.float32)
+    B, V = z.shape
+    out = dict(tokens=np.zeros(B, np.int32), q=np.zeros(B), lse=np.zeros(B), gap=np.zeros(B))
+    rc = lib().svo_draft_sample(_ptr(z), B, V, float(temperature), int(seed) & (2**64 - 1),
+                                int(rnd) & (2**64 - 1), int(pos), _ptr(out["tokens"]),
+                                _ptr(out["q"]), _ptr(out["lse"]), _ptr(out["gap"]))
+    if rc != 0:
+        raise ValueError(f"oracle draft_sample rejected its arguments (rc={rc})")
+    return out
 
 
 def lmhead_logits(h_bits, W_bits, cols=None):

@@ -89,9 +89,14 @@ void svo_uniform_row(uint64_t seed, uint32_t tag, uint32_t pos, uint32_t b, uint
 }
 
 /* Gumbel noise for vocabulary entry v at a draw position (tag 1). */
-static double gumbel(uint64_t seed, uint32_t pos, uint32_t b, uint64_t round, int64_t v) {
-  double u = svo_uniform(seed, 1u, pos, b, round, (uint32_t)(v >> 2), (int)(v & 3));
+static double gumbel_tag(uint64_t seed, uint32_t tag, uint32_t pos, uint32_t b, uint64_t round,
+                         int64_t v) {
+  double u = svo_uniform(seed, tag, pos, b, round, (uint32_t)(v >> 2), (int)(v & 3));
   return -log(-log(u));
+}
+
+static double gumbel(uint64_t seed, uint32_t pos, uint32_t b, uint64_t round, int64_t v) {
+  return gumbel_tag(seed, 1u, pos, b, round, v);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -521,4 +526,48 @@ void svo_lmhead_logits(const uint16_t* h, const uint16_t* W, int M, int H, int64
       out[(int64_t)m * nc + j] = (float)acc;
     }
   }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Draft sampling ([A1] step 1: x_i ~ q_i, drawn autoregressively by the     */
+/* draft model; [B1] "The algorithm": x~_{t+i} ~ q(. | ...)).                */
+/* ------------------------------------------------------------------------ */
+int svo_draft_sample(const float* logits, int B, int64_t V, float temperature, uint64_t seed,
+                     uint64_t round, int pos, int32_t* tokens, double* q_at, double* lse,
+                     double* gumbel_gap) {
+  if (B < 0 || V < 1 || pos < 0 || !(temperature > 0.0f) || !isfinite(temperature)) return -1;
+  if (B == 0) return 0;
+  if (!logits || !tokens) return -1;
+  /* the single-precision reciprocal of T, as for the verify step ([A3]) */
+  const float invT_f = 1.0f / temperature;
+  const double invT = (double)invT_f;
+  for (int b = 0; b < B; ++b) {
+    const float* z = logits + (int64_t)b * V;
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v)
+      if ((double)z[v] * invT > m) m = (double)z[v] * invT;
+    double S = 0.0;
+    if (m != -INFINITY)
+      for (int64_t v = 0; v < V; ++v) S += exp((double)z[v] * invT - m);
+    /* Gumbel-max: argmax_v s_v + g_v over the finite s_v, ties to the lowest v */
+    int64_t best = -1;
+    double k1 = -INFINITY, k2 = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+      const double sv = (double)z[v] * invT;
+      if (!(sv > -INFINITY) || sv == INFINITY) continue;
+      const double key = sv + gumbel_tag(seed, 2u, (uint32_t)pos, (uint32_t)b, round, v);
+      if (best < 0 || key > k1) {
+        k2 = k1;
+        k1 = key;
+        best = v;
+      } else if (key > k2) {
+        k2 = key;
+      }
+    }
+    tokens[b] = best < 0 ? 0 : (int32_t)best;
+    if (q_at) q_at[b] = (best < 0 || !(S > 0.0)) ? 0.0 : exp((double)z[best] * invT - m) / S;
+    if (lse) lse[b] = m + log(S);
+    if (gumbel_gap) gumbel_gap[b] = (best < 0) ? INFINITY : k1 - k2;
+  }
+  return 0;
 }

@@ -118,6 +118,16 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
 int svo_spec_verify_greedy(const void* zt, const int32_t* xt, int B, int gamma,
                            int64_t V, int dtype, int32_t* tokens, int32_t* counts);
 
+/* Draft sampling of one position from given logits [B][V] (float): with
+ * s = z * fl32(1/T), x = argmax_v s_v + g_v over finite s_v (ties to the lowest
+ * v), g_v Gumbel from Philox with tag 2 at position pos (counter (v>>2,
+ * (2<<24)|pos, b, round), lane v&3).  Outputs tokens [B] (0 for an empty row),
+ * q_at [B] = q(x), lse [B] = log sum_v exp(s_v), gumbel_gap [B] = top-1 minus
+ * top-2 key; the last three may be NULL.  Returns 0, or -1 on bad arguments. */
+int svo_draft_sample(const float* logits, int B, int64_t V, float temperature, uint64_t seed,
+                     uint64_t round, int pos, int32_t* tokens, double* q_at, double* lse,
+                     double* gumbel_gap);
+
 /* Plain matmul reference for the fused LM head: logits[M][V] = h[M][H] * W[H][V]
  * with bf16 inputs, accumulated in double, written as float. */
 void svo_lmhead_logits(const uint16_t* h, const uint16_t* W, int M, int H, int64_t V,
