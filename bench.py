@@ -369,6 +369,7 @@ def run_ours(args):
     if not args.no_extra:
         extra["greedy"] = measure_greedy(L, dev, stream, rank)
         extra["lmhead"] = measure_lmhead(L, dev, stream, rank)
+        extra["lmhead_draft"] = measure_draft(L, dev, stream, rank)
         extra["lenience"] = measure_options(L, stream, sets, tokens, counts, flags, ws,
                                             lenience=0.5)
         extra["top_k"] = measure_options(L, stream, sets, tokens, counts, flags, ws, top_k=50)
@@ -458,17 +459,18 @@ def _kernel_times(L, stream, call, nkern, reps, warm=3):
     """Average per-kernel ms of `call(i)` via the library's timing events, and
     the average ms of a whole call without events."""
     import torch
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nkern + 1)]
+    nev = max(4, nkern + 1)  # the library takes at least 4 events; a call marks nkern + 1
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
     for e in ev:
         e.record(stream)
     torch.cuda.synchronize()
-    arr = (ctypes.c_void_p * (nkern + 1))(*[ctypes.c_void_p(e.cuda_event) for e in ev])
+    arr = (ctypes.c_void_p * nev)(*[ctypes.c_void_p(e.cuda_event) for e in ev])
     for i in range(warm):
         call(i)
     torch.cuda.synchronize()
     acc = [0.0] * nkern
     for i in range(reps):
-        L.sv_set_timing_events(ctypes.cast(arr, ctypes.c_void_p), nkern + 1)
+        L.sv_set_timing_events(ctypes.cast(arr, ctypes.c_void_p), nev)
         call(warm + i)
         L.sv_set_timing_events(None, 0)
         torch.cuda.synchronize()
@@ -520,6 +522,44 @@ def measure_greedy(L, dev, stream, rank, reps=400):
                          "peak_kind": kind, "unit": "GB/s", "frac": gbs / hbm,
                          "algorithmic_bytes": per},
             "l2_policy": f"inputs rotate over {nsets} sets of {per / 1e6:.1f} MB"}
+
+
+def measure_draft(L, dev, stream, rank, reps=200):
+    """Draft LM head + draw of one draft position (spec_lmhead_draft) on the draft
+    side of lmhead_b32: B=32, draft hidden 2048, V=128256, bf16; W_draft (525 MB)
+    exceeds L2."""
+    import torch
+    import speculative_decoding_verification_21_gb300 as sv
+    from speculative_decoding_verification_21_gb300 import workloads as wl
+    B, g, V, Hd = 32, 4, 128256, 2048
+    w = wl.lmhead_b32(seed=1005 + 7 * rank, device=dev)
+    e = w.extra
+    h = e["h_d"].reshape(B, g, Hd)[:, 0].contiguous()
+    tok = torch.empty((B,), dtype=torch.int32, device=dev)
+    q = torch.empty((B,), dtype=torch.float32, device=dev)
+    ws = sv.alloc_workspace(B, 1, V, 3, device=dev)
+    P = ctypes.c_void_p
+    sh = P(stream.cuda_stream)
+
+    def call(i):
+        rc = L.spec_lmhead_draft(P(h.data_ptr()), P(e["W_d"].data_ptr()), Hd, B, V,
+                                 ctypes.c_float(1.0), 0, i, i % g, P(tok.data_ptr()),
+                                 P(q.data_ptr()), None, None, P(ws.data_ptr()),
+                                 ctypes.c_size_t(ws.numel()), sh)
+        if rc != 0:
+            raise RuntimeError(sv.status_string(rc))
+
+    kms, ms = _kernel_times(L, stream, call, 2, reps)
+    hbm, kind = peaks()
+    wbytes = 2 * V * Hd
+    gbs = wbytes / (kms[0] / 1000.0) / 1e9
+    return {"workload": "lmhead_b32 draft side", "B": B, "V": V, "Hd": Hd,
+            "dtype": "bf16 operands, fp32 accumulate", "draws_per_s": 1000.0 / ms,
+            "ms_per_draw": ms, "kernel_ms": {"k_lm_draft": kms[0], "k_lm_draft_merge": kms[1]},
+            "roofline": {"bound": "hbm", "kernel": "k_lm_draft", "achieved": gbs, "peak": hbm,
+                         "peak_kind": kind, "unit": "GB/s", "frac": gbs / hbm,
+                         "algorithmic_bytes": wbytes},
+            "gpu_launches_per_draw": 2}
 
 
 def measure_lmhead(L, dev, stream, rank, reps=100):

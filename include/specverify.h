@@ -76,7 +76,7 @@ enum {
   SV_FLAG_BAD_TOKEN = 16         /* a draft token outside [0, V): treated as p = q = 0    */
 };
 
-enum { SV_MODE_SAMPLE = 0, SV_MODE_GREEDY = 1, SV_MODE_LMHEAD = 2 };
+enum { SV_MODE_SAMPLE = 0, SV_MODE_GREEDY = 1, SV_MODE_LMHEAD = 2, SV_MODE_DRAFT = 3 };
 
 /* Bytes of workspace a call with these sizes needs (0 for B == 0).  `mode` is one
  * of SV_MODE_*.  For SV_MODE_LMHEAD, V and the hidden sizes of spec_lmhead_verify
@@ -226,6 +226,34 @@ int spec_lmhead_verify(const void* h_target, const void* W_target, int Ht,
                        int32_t* out_tokens, int32_t* out_counts, float* out_p_at_draft,
                        float* out_q_at_draft, uint8_t* out_flags, float* debug_logits,
                        void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * spec_lmhead_draft -- the draft side of a round for one position: the draft
+ * model's LM head and the draw of its token ("Fast Inference ...", section "The
+ * loop", step 1: run M_q gamma times, drawing x_i ~ q_i; the course notes' "The
+ * algorithm": x_{t+i} ~ q(. | prefix)).  The draft model's forward pass that
+ * gives h_draft is the caller's.
+ *   h_draft  [B][Hd] bf16: the draft's last hidden state of each batch row
+ *   W_draft  [Hd][V] bf16
+ *   pos      the position i of the tokens drawn (0..gamma-1), part of the RNG counter
+ * q = softmax(z / T) with z = h_draft W_draft (bf16 operands, fp32 accumulation
+ * on the tensor cores) and the scale fl32(1/T) as for the verify step; the token
+ * is argmax_v z_v/T + g_v, ties to the lowest v, with g_v Gumbel noise from
+ * Philox tag 2 at position pos (counter (v>>2, (2<<24)|pos, b, lo32(round)),
+ * lane v&3).  The logits are not written to HBM.
+ * Outputs (device):
+ *   out_tokens   [B] int32, the drafted tokens x_i (0 for an empty row)
+ *   out_q        [B] float or NULL: q_i(x_i)
+ *   out_lse      [B] float or NULL: log sum_v exp(z_v / T)
+ *   debug_logits NULL in production; else [B][V] float receives the logits used
+ *   workspace    >= sv_workspace_bytes(B, 1, V, SV_MODE_DRAFT)
+ * Returns SV_ERR_UNSUPPORTED for Hd not a multiple of 64 (or above 16384),
+ * B > 128 or V not a multiple of 8; SV_ERR_ARG for pos outside [0, 2^24).
+ */
+int spec_lmhead_draft(const void* h_draft, const void* W_draft, int Hd, int B, int64_t V,
+                      float temperature, uint64_t seed, uint64_t round, int pos,
+                      int32_t* out_tokens, float* out_q, float* out_lse, float* debug_logits,
+                      void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /* Profiling aid (not thread-safe): when `events` is non-NULL, following calls
  * record events[0] on their stream before the first kernel and events[k] after

@@ -15,12 +15,12 @@ from . import build as _build
 
 SV_OK = 0
 SV_F32, SV_BF16 = 0, 1
-SV_MODE_SAMPLE, SV_MODE_GREEDY, SV_MODE_LMHEAD = 0, 1, 2
+SV_MODE_SAMPLE, SV_MODE_GREEDY, SV_MODE_LMHEAD, SV_MODE_DRAFT = 0, 1, 2, 3
 FLAG_ZERO_MASS, FLAG_NONFINITE, FLAG_RESIDUAL_FALLBACK, FLAG_TIMEOUT, FLAG_BAD_TOKEN = 1, 2, 4, 8, 16
 
 EXPORTS = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verify_opts",
-           "spec_verify_greedy", "spec_lmhead_verify", "sv_set_timing_events",
-           "sv_status_string", "sv_version")
+           "spec_verify_greedy", "spec_lmhead_verify", "spec_lmhead_draft",
+           "sv_set_timing_events", "sv_status_string", "sv_version")
 
 
 class Options(ctypes.Structure):
@@ -71,6 +71,8 @@ def load(build_if_missing: bool = True):
         L.spec_lmhead_verify.argtypes = [P, P, I, P, P, I, P, I, I, I64, F, U64, U64, P, P, P, P,
                                          P, P, P, SZ, P]
         L.spec_lmhead_verify.restype = I
+        L.spec_lmhead_draft.argtypes = [P, P, I, I, I64, F, U64, U64, I, P, P, P, P, P, SZ, P]
+        L.spec_lmhead_draft.restype = I
         L.sv_set_timing_events.argtypes = [P, I]
         L.sv_set_timing_events.restype = I
         L.sv_status_string.argtypes = [I]
@@ -254,4 +256,33 @@ def spec_lmhead_verify(h_target, W_target, h_draft, W_draft, draft_tokens, *, B:
                               _ptr(ws), ws.numel(), sh)
     if rc != SV_OK:
         raise SpecVerifyError(rc, "spec_lmhead_verify")
+    return o
+
+
+def spec_lmhead_draft(h_draft, W_draft, *, pos: int, temperature: float = 1.0, seed: int = 0,
+                      round: int = 0, debug_logits=None, out=None, workspace=None,
+                      stream=None):
+    """Draft LM head + draw of one draft position through the C ABI (bf16 inputs).
+    Returns tokens [B] int32, q [B] float32 (q(x)), lse [B] float32."""
+    torch = _torch()
+    L = load()
+    B, Hd = h_draft.shape
+    V = W_draft.shape[1]
+    if tuple(W_draft.shape) != (Hd, V):
+        raise ValueError("shape mismatch in spec_lmhead_draft")
+    _check_cuda(h_draft, W_draft, debug_logits)
+    dev = h_draft.device
+    o = dict(out or {})
+    o.setdefault("tokens", torch.empty((B,), dtype=torch.int32, device=dev))
+    o.setdefault("q", torch.empty((B,), dtype=torch.float32, device=dev))
+    o.setdefault("lse", torch.empty((B,), dtype=torch.float32, device=dev))
+    sh = _stream_handle(stream)
+    need = workspace_bytes(B, 1, V, SV_MODE_DRAFT)
+    ws = workspace if workspace is not None else _ws_cache.get(need, dev, sh.value)
+    rc = L.spec_lmhead_draft(_ptr(h_draft), _ptr(W_draft), Hd, B, V, float(temperature),
+                             int(seed) & (2**64 - 1), int(round) & (2**64 - 1), int(pos),
+                             _ptr(o["tokens"]), _ptr(o["q"]), _ptr(o["lse"]),
+                             _ptr(debug_logits), _ptr(ws), ws.numel(), sh)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_lmhead_draft")
     return o

@@ -28,6 +28,11 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
                   uint8_t* out_flags, float* debug_logits, void* workspace,
                   size_t workspace_bytes, cudaStream_t stream);
 size_t lmhead_workspace_bytes(int B, int gamma, int64_t V);
+int lmhead_draft(const void* h_draft, const void* W_draft, int Hd, int B, int64_t V,
+                 float temperature, uint64_t seed, uint64_t round, int pos, int32_t* out_tokens,
+                 float* out_q, float* out_lse, float* debug_logits, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream);
+size_t lmhead_draft_workspace_bytes(int B, int64_t V);
 }  // namespace sv
 
 namespace sv {
@@ -72,6 +77,7 @@ size_t sv_workspace_bytes(int B, int gamma, int64_t V, int mode) {
     case SV_MODE_SAMPLE: return sv::make_sample_plan(B, gamma, V).total;
     case SV_MODE_GREEDY: return sv::make_greedy_plan(B, gamma, V).total;
     case SV_MODE_LMHEAD: return sv::lmhead_workspace_bytes(B, gamma, V);
+    case SV_MODE_DRAFT: return sv::lmhead_draft_workspace_bytes(B, V);
     default: return 0;
   }
 }
@@ -172,6 +178,18 @@ int spec_lmhead_verify(const void* h_target, const void* W_target, int Ht, const
                            V, temperature, seed, round, out_tokens, out_counts, out_p_at_draft,
                            out_q_at_draft, out_flags, debug_logits, workspace, workspace_bytes,
                            (cudaStream_t)cuda_stream);
+}
+
+int spec_lmhead_draft(const void* h_draft, const void* W_draft, int Hd, int B, int64_t V,
+                      float temperature, uint64_t seed, uint64_t round, int pos,
+                      int32_t* out_tokens, float* out_q, float* out_lse, float* debug_logits,
+                      void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (B < 0 || V < 1 || V >= ((int64_t)1 << 31)) return SV_ERR_ARG;
+  if (!(temperature > 0.0f && std::isfinite(temperature))) return SV_ERR_ARG;
+  if (B == 0) return SV_OK;
+  return sv::lmhead_draft(h_draft, W_draft, Hd, B, V, temperature, seed, round, pos, out_tokens,
+                          out_q, out_lse, debug_logits, workspace, workspace_bytes,
+                          (cudaStream_t)cuda_stream);
 }
 
 int sv_set_timing_events(void* const* events, int n) {

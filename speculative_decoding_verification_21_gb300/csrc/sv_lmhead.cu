@@ -78,7 +78,8 @@ struct LmArgs {
   int Ht, Hd;
   int box_t, box_d;    // h rows per tensor copy: rows rounded up to 8 (pass 2: compact rows)
   int perm_t;          // target rows in smem are position-major (row i*B + b), else b*(gamma+1) + i
-  int rep, rstride;    // pass 2: copies of the compact rows in the row tile, rows apart
+  int rep, rstride;    // passes 2, 3: copies of the rows in the row tile, rows apart
+  int draft_pos;       // pass 3: position of the draft tokens being sampled
   int nw, nh;          // W-ring and h-ring slots (nw >= nh)
   int a_half;          // bytes of the h tile of one 64-wide span (rows x 128)
   float temperature;
@@ -174,11 +175,12 @@ __device__ __forceinline__ bool lm_wait_warp(uint64_t* bar, uint32_t parity,
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// -log2(-log2 u) noise of entry v at Philox position pos (tag 1), and its double
-// twin -ln(-ln u) for the re-decision.
+// -log2(-log2 u) noise of entry v at Philox position pos (tag 1 for the
+// verify's draws, tag 2 for draft sampling), and its double twin -ln(-ln u)
+// for the re-decision.
 __device__ __forceinline__ double gumbel_f64(int64_t v, int pos, int b, uint64_t seed,
-                                             uint64_t round) {
-  const uint4 rnd = philox4x32_10(sv_counter((uint32_t)(v >> 2), 1u, (uint32_t)pos, (uint32_t)b, round),
+                                             uint64_t round, uint32_t tag = 1u) {
+  const uint4 rnd = philox4x32_10(sv_counter((uint32_t)(v >> 2), tag, (uint32_t)pos, (uint32_t)b, round),
                                   (uint32_t)seed, (uint32_t)(seed >> 32));
   const uint32_t lanes[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
   return -log(sv_neglog_u_f64(lanes[v & 3]));
@@ -245,6 +247,17 @@ struct Jobs<2> {
                             const CUtensorMap* a1, const CUtensorMap* b1, const LmArgs& a) {
     if (s == 0) return Seg{a0, b0, a.kbt, 1, 0, 0, a.box_t, a.box_t, false};
     return Seg{a1, b1, a.kbd, 1, 0, kLmTileN, a.box_d, a.box_d, false};
+  }
+};
+
+// Pass 3 (draft sampling): one job per tile, the draft rows' block at column 0.
+template <>
+struct Jobs<3> {
+  static constexpr int kPerTile = 1;
+  __device__ static int nseg(int) { return 1; }
+  __device__ static Seg seg(int, int, const CUtensorMap* a0, const CUtensorMap* b0,
+                            const CUtensorMap*, const CUtensorMap*, const LmArgs& a) {
+    return Seg{a0, b0, a.kbd, 1, 0, 0, a.box_d, a.box_d, false};
   }
 };
 
@@ -534,6 +547,114 @@ __device__ __forceinline__ void pass2_flush(const LmArgs& a, int quad, int half,
   }
 }
 
+// What a pass-3 (draft sampling) epilogue thread carries over the CTA's tiles:
+// its row's online (max, sum) over its column slice and the top-2 Gumbel-max
+// keys z c - log2(-log2 u) (Philox tag 2 at the draft position).
+struct Pass3Carry {
+  float mc, s;
+  Cand2 t[2];
+};
+
+// Pass-3 epilogue of one tile: rows are batch rows (copied into the row tile
+// as in pass 2); the draft logits of the tile's columns in this warp's slice.
+__device__ __forceinline__ void epilogue_pass3(const LmArgs& a, int t, uint32_t tacc, int quad,
+                                               int half, const PhiloxKeys& pk, Pass3Carry& cy) {
+  const int lane = threadIdx.x & 31;
+  const int V = a.V, B = a.B;
+  const P2Slice sl = pass2_slice(a, quad, half);
+  if (sl.copy >= a.rep || sl.row0 >= B) return;  // warp-uniform
+  const int r = sl.row0 + lane;  // batch row
+  const bool rv = r < B;
+  const float c = log2_scale(inv_temperature(a.temperature));
+  const uint32_t ta = tacc + ((uint32_t)(32 * quad) << 16) + (uint32_t)sl.col0;
+#pragma unroll 1
+  for (int c16 = 0; c16 < sl.ncol; c16 += 16) {
+    uint32_t raw[16];
+    __syncwarp();
+    tmem_ld16_async(ta + (uint32_t)c16, raw);
+    tmem_wait_ld();
+    const int vb = t * kLmTileN + sl.col0 + c16;
+    if (rv && vb < V) {
+      const int nvalid = min(16, V - vb);
+      float f[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) f[e] = (e < nvalid) ? __uint_as_float(raw[e]) : -kInf;
+      if (a.dbg) {
+        float4* d = reinterpret_cast<float4*>(a.dbg + (int64_t)r * V + vb);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (4 * j < nvalid) d[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+      }
+      // online (max, sum of 2^(z c - max))
+      float m4[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        m4[j] = fmaxf(fmaxf(f[4 * j], f[4 * j + 1]), fmaxf(f[4 * j + 2], f[4 * j + 3]));
+      const float nm = fmaxf(cy.mc, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c);
+      if (nm > -kInf) {
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e & 3] += ex2(fmaf(f[e], c, -nm));
+        const float old = (cy.mc == -kInf) ? 0.0f : cy.s * ex2(cy.mc - nm);
+        cy.mc = nm;
+        cy.s = old + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+      }
+      // Gumbel-max keys
+#pragma unroll
+      for (int g4 = 0; g4 < 4; ++g4) {
+        const int v = vb + 4 * g4;
+        if (v >= V) break;
+        const uint4 rnd =
+            philox_rk(sv_counter((uint32_t)(v >> 2), 2u, (uint32_t)a.draft_pos, (uint32_t)r,
+                                 a.round),
+                      pk);
+        const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float z = f[4 * g4 + e];
+          if (z > -kInf)
+            cand_insert(cy.t[e & 1], LmCand{fmaf(z, c, -__log2f(neglog2_u(rr[e]))), v + e, z, 0.0f});
+        }
+      }
+    }
+  }
+}
+
+// One (max, sum) partial and one top-2 per batch row and CTA: the slices of a
+// row are merged through shared memory (the ring, idle after the last job).
+__device__ __forceinline__ void pass3_flush(const LmArgs& a, int quad, int half,
+                                            const Pass3Carry& cy, unsigned char* smem) {
+  const int B = a.B;
+  const int nsl = 2 * a.rep;
+  const P2Slice sl = pass2_slice(a, quad, half);
+  const int r = sl.row0 + (threadIdx.x & 31);
+  LmCand* sc = reinterpret_cast<LmCand*>(smem);                         // [B][nsl][2]
+  float2* sm = reinterpret_cast<float2*>(sc + (size_t)B * nsl * 2);     // [B][nsl]
+  if (sl.copy < a.rep && r < B) {
+    const Cand2 t2 = merge2(cy.t);
+    LmCand* o = sc + ((size_t)r * nsl + sl.copy * 2 + half) * 2;
+    o[0] = t2.a;
+    o[1] = t2.b;
+    sm[(size_t)r * nsl + sl.copy * 2 + half] = make_float2(cy.mc, cy.s);
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+  for (int rr = (int)threadIdx.x - 3 * 32; rr < B; rr += 32 * kEpiWarps) {
+    Cand2 x{cand_empty(), cand_empty()};
+    MS ms{-kInf, 0.0f};
+    for (int j = 0; j < nsl; ++j) {
+      const LmCand* q = sc + ((size_t)rr * nsl + j) * 2;
+      cand_insert(x, q[0]);
+      cand_insert(x, q[1]);
+      const float2 p = sm[(size_t)rr * nsl + j];
+      ms = ms_combine(ms, MS{p.x, p.y});
+    }
+    a.part[(int64_t)rr * a.nslot + blockIdx.x] = make_float2(ms.m, ms.s);
+    LmCand* o = a.res + ((int64_t)rr * a.nslot + blockIdx.x) * 2;
+    o[0] = x.a;
+    o[1] = x.b;
+  }
+}
+
 template <int PASS>
 __global__ void __launch_bounds__(kLmThreads, 1)
     k_lm(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mB0,
@@ -629,7 +750,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                 }
                 uint8_t* hst = hring + (size_t)hs.i * hslot;
                 // pass 2: `rep` copies of the compact rows, `rstride` rows apart
-                const int rep = (PASS == 2) ? a.rep : 1;
+                const int rep = (PASS >= 2) ? a.rep : 1;
                 mbar_arrive_expect_tx(full + ws, (uint32_t)(rep * 2 * q.rows * kKAtom * 2));
                 for (int h = 0; h < 2; ++h) {
                   for (int cp = 0; cp < rep; ++cp) {
@@ -709,12 +830,17 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const int quad = warp & 3, half = (warp - 3) >> 2;
     const PhiloxKeys pk = philox_keys(a.seed);
     Pass1Carry cy;
+    Pass3Carry cy3;
     Cand2 tr[2], tp[2];
     if (PASS == 1) {
       carry_init(cy);
-    } else {
+    } else if (PASS == 2) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) tr[j] = tp[j] = Cand2{cand_empty(), cand_empty()};
+    } else {
+      cy3.mc = -kInf;
+      cy3.s = 0.0f;
+      cy3.t[0] = cy3.t[1] = Cand2{cand_empty(), cand_empty()};
     }
     int jobi = 0;
     bool ok = true;
@@ -735,8 +861,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             epilogue_pass1<0>(a, tv, tacc, quad, half, cy);
           else
             epilogue_pass1<1>(a, tv, tacc, quad, half, cy);
-        } else {
+        } else if (PASS == 2) {
           epilogue_pass2(a, tv, tacc, quad, half, rows2, pk, tr, tp);
+        } else {
+          epilogue_pass3(a, tv, tacc, quad, half, pk, cy3);
         }
         tc_fence_before();
         __syncwarp();
@@ -747,8 +875,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     // partials of this CTA (also after an abort: the error flag marks them)
     if (PASS == 1)
       pass1_flush(a, cy, quad, half);
-    else
+    else if (PASS == 2)
       pass2_flush(a, quad, half, rows2, tr, tp, reinterpret_cast<LmCand*>(hring));
+    else
+      pass3_flush(a, quad, half, cy3, hring);
   }
 
   if (threadIdx.x == 0 && *abort_flag) atomicOr(a.ctl + (PASS == 1 ? 1 : 2), 1u);
@@ -888,6 +1018,55 @@ __global__ void __launch_bounds__(256) k_lm_merge(LmArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// k_lm_draft_merge: one CTA per batch row of a draft-sampling call: the row's
+// (max, sum) from the per-CTA partials, the token from the per-CTA top-2 keys
+// (re-decided in double near a tie), q(x) and the log-normaliser.
+// ---------------------------------------------------------------------------
+struct DraftOut {
+  int32_t* tokens;
+  float* q;
+  float* lse;
+};
+
+__global__ void __launch_bounds__(256) k_lm_draft_merge(LmArgs a, DraftOut out) {
+  const int b = blockIdx.x;
+  __shared__ Cand2 scand[32];
+  __shared__ RowStat s_rs;
+  pdl_wait();
+  const bool err = *reinterpret_cast<volatile uint32_t*>(a.ctl + 2) != 0u;
+  if (threadIdx.x < 32) {
+    const RowStat rs = combine_row(a.part + (int64_t)b * a.nslot, a.nslot, nullptr);
+    if (threadIdx.x == 0) s_rs = rs;
+  }
+  Cand2 t{cand_empty(), cand_empty()};
+  const LmCand* rp = a.res + (int64_t)b * a.nslot * 2;
+  for (int j = threadIdx.x; j < a.nslot; j += blockDim.x) {
+    cand_insert(t, rp[2 * j]);
+    cand_insert(t, rp[2 * j + 1]);
+  }
+  t = block_cand2(t, scand);
+  if (threadIdx.x != 0) return;
+  const RowStat rs = s_rs;
+  const float invT_f = inv_temperature(a.temperature);
+  const double invT = (double)invT_f;
+  int tk = redecide(t, [&](const LmCand& q) {
+    return (double)q.zt * invT + gumbel_f64(q.idx, a.draft_pos, b, a.seed, a.round, 2u);
+  });
+  float zt = 0.0f;
+  if (tk >= 0) {
+    zt = (tk == t.a.idx) ? t.a.zt : t.b.zt;
+  }
+  const bool ok = !err && tk >= 0 && rs.s > 0.0 && !(rs.bits & kRowNaN);
+  if (tk < 0 || err) tk = 0;
+  out.tokens[b] = tk;
+  const double c = (double)log2_scale(invT_f);
+  if (out.q) out.q[b] = ok ? (float)(exp2((double)zt * c - (double)rs.mc) / rs.s) : 0.0f;
+  if (out.lse)
+    out.lse[b] = (rs.s > 0.0) ? (float)(((double)rs.mc + log2(rs.s)) * 0.6931471805599453)
+                              : -CUDART_INF_F;
+}
+
+// ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -924,6 +1103,8 @@ cudaError_t lm_device(LmDevice** out) {
     e = cudaFuncSetAttribute(k_lm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_lm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_lm<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
     if (e != cudaSuccess) return e;
     d.ready = true;
   }
@@ -1095,6 +1276,71 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   e = launch_pdl(k_lm_merge, dim3((unsigned)B), dim3(256), 0, stream, a);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   mark(4, stream);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+size_t lmhead_draft_workspace_bytes(int B, int64_t V) { return make_draft_plan(B, V).total; }
+
+// Draft sampling of one position: z = h_draft W_draft (tensor cores), x ~
+// softmax(z / T) by Gumbel-max on Philox tag 2, q(x) and the log-normaliser.
+int lmhead_draft(const void* h_draft, const void* W_draft, int Hd, int B, int64_t V,
+                 float temperature, uint64_t seed, uint64_t round, int pos, int32_t* out_tokens,
+                 float* out_q, float* out_lse, float* debug_logits, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream) {
+  if (!h_draft || !W_draft || !out_tokens || pos < 0 || pos > 0xFFFFFF) return SV_ERR_ARG;
+  if (Hd < 64 || Hd % 64 || Hd > kLmMaxHidden || B > kTileM || V % 8 != 0 ||
+      V > ((int64_t)1 << 31) - 256)
+    return SV_ERR_UNSUPPORTED;
+  if (!aligned_to(h_draft, 16) || !aligned_to(W_draft, 16) || !aligned_to(out_tokens, 4) ||
+      (out_q && !aligned_to(out_q, 4)) || (out_lse && !aligned_to(out_lse, 4)) ||
+      (debug_logits && !aligned_to(debug_logits, 16)))
+    return SV_ERR_ALIGN;
+  const DraftPlan pl = make_draft_plan(B, V);
+  if (!workspace || workspace_bytes < pl.total) return SV_ERR_WORKSPACE;
+  if (!aligned_to(workspace, kAlign)) return SV_ERR_ALIGN;
+  LmDevice* dev = nullptr;
+  if (lm_device(&dev) != cudaSuccess) return SV_ERR_CUDA;
+
+  char* ws = reinterpret_cast<char*>(workspace);
+  LmArgs a{};
+  a.B = B;
+  a.gamma = 1;
+  a.V = (int)V;
+  a.nvt = pl.nvt;
+  a.Md = B;
+  a.kbd = (Hd + kKBlock - 1) / kKBlock;
+  a.Hd = Hd;
+  a.temperature = temperature;
+  a.seed = seed;
+  a.round = round;
+  a.draft_pos = pos;
+  a.ctl = reinterpret_cast<uint32_t*>(ws + pl.off_ctl);
+  a.part = reinterpret_cast<float2*>(ws + pl.off_part);
+  a.res = reinterpret_cast<LmCand*>(ws + pl.off_cand);
+  a.dbg = debug_logits;
+  a.box_d = round8(B);
+  // copies of the rows: one per 32-row-aligned block that fits in 128 lanes
+  a.rstride = (B + 31) & ~31;
+  a.rep = kTileM / a.rstride;
+  a.rep = a.rep > kMaxRep ? kMaxRep : a.rep;
+  size_t smem = 0;
+  if (!ring_config(a, a.rep > 1 ? a.rep * a.rstride : a.box_d, kHStagesPass2, &smem))
+    return SV_ERR_UNSUPPORTED;
+  CUtensorMap hD, WD;
+  if (!encode_bf16(&hD, h_draft, (uint64_t)B, (uint64_t)Hd, kKAtom, (uint32_t)a.box_d) ||
+      !encode_bf16(&WD, W_draft, (uint64_t)Hd, (uint64_t)V, kLmTileN / 2, kKBlock))
+    return SV_ERR_CUDA;
+  cudaError_t e = cudaMemsetAsync(a.ctl, 0, 4 * sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  const unsigned grid = (unsigned)(pl.nvt < dev->sms ? pl.nvt : dev->sms);
+  a.nslot = (int)grid;
+  mark(0, stream);
+  k_lm<3><<<grid, kLmThreads, smem, stream>>>(hD, WD, hD, WD, a);
+  mark(1, stream);
+  e = launch_pdl(k_lm_draft_merge, dim3((unsigned)B), dim3(256), 0, stream, a,
+                 DraftOut{out_tokens, out_q, out_lse});
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  mark(2, stream);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

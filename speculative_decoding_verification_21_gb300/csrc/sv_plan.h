@@ -158,4 +158,23 @@ inline LmPlan make_lm_plan(int B, int gamma, int64_t V) {
   return p;
 }
 
+// Workspace of a draft-sampling call (spec_lmhead_draft): per (batch row, CTA)
+// one (max, sum) partial and a top-2 of keys; control words.
+struct DraftPlan {
+  int nvt = 0;
+  size_t off_ctl = 0, off_part = 0, off_cand = 0, total = 0;
+};
+
+inline DraftPlan make_draft_plan(int B, int64_t V) {
+  DraftPlan p;
+  if (B <= 0) return p;
+  p.nvt = (int)ceil_div(V, kLmTileN);
+  size_t o = 0;
+  p.off_ctl = o;   o = align_up(o + 4 * sizeof(uint32_t));
+  p.off_part = o;  o = align_up(o + 8 * (size_t)B * p.nvt);
+  p.off_cand = o;  o = align_up(o + 2 * sizeof(LmCand) * (size_t)B * p.nvt);
+  p.total = o;
+  return p;
+}
+
 }  // namespace sv

@@ -162,3 +162,32 @@ def test_lmhead_workspace_size():
     assert need >= 2 * 32 * 16384 * 2
     assert need % 256 == 0
     assert sv.workspace_bytes(64, 4, 128256, 2) > need
+
+
+def test_lmhead_draft_argument_errors():
+    L = sv.load()
+
+    def call(h=FAKE, W=FAKE, Hd=128, B=4, V=1024, T=1.0, pos=0, tok=FAKE, ws=FAKE, wsb=1 << 22):
+        return L.spec_lmhead_draft(h, W, Hd, B, V, T, 0, 0, pos, tok, None, None, None, ws, wsb,
+                                   None)
+    assert call(B=0) == 0
+    assert call(T=0.0) == -1
+    assert call(T=float("nan")) == -1
+    assert call(V=0) == -1
+    assert call(h=None) == -1
+    assert call(tok=None) == -1
+    assert call(pos=-1) == -1
+    assert call(pos=1 << 24) == -1
+    assert call(Hd=100) == -6
+    assert call(Hd=16384 + 64) == -6
+    assert call(B=129) == -6
+    assert call(V=1001) == -6
+    assert call(h=FAKE_MIS) == -3
+    assert call(ws=None) == -4
+    assert call(wsb=16) == -4
+
+
+def test_draft_workspace_size():
+    a = sv.workspace_bytes(32, 1, 128256, 3)
+    assert a > 0 and a % 256 == 0
+    assert sv.workspace_bytes(64, 1, 128256, 3) > a
