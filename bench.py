@@ -544,7 +544,7 @@ def measure_draft(L, dev, stream, rank, reps=200):
     def call(i):
         rc = L.spec_lmhead_draft(P(h.data_ptr()), P(e["W_d"].data_ptr()), Hd, B, V,
                                  ctypes.c_float(1.0), 0, i, i % g, P(tok.data_ptr()),
-                                 P(q.data_ptr()), None, None, P(ws.data_ptr()),
+                                 P(q.data_ptr()), None, None, None, P(ws.data_ptr()),
                                  ctypes.c_size_t(ws.numel()), sh)
         if rc != 0:
             raise RuntimeError(sv.status_string(rc))
@@ -590,6 +590,30 @@ def measure_lmhead(L, dev, stream, rank, reps=100):
 
     kms, ms = _kernel_times(L, stream, call, 4, reps)
     rejected = float((cnt < g).float().mean().item())  # the rest draw the bonus token
+
+    # the same round with the draft rows' statistics from the draft step
+    # (spec_lmhead_draft at each position, outside the timed region): the first
+    # GEMM pass streams W_target only
+    hd3 = e["h_d"].reshape(B, g, Hd)
+    xt_d = torch.empty((B, g), dtype=torch.int32, device=dev)
+    lse = torch.empty((B, g), dtype=torch.float32, device=dev)
+    logit = torch.empty((B, g), dtype=torch.float32, device=dev)
+    for i in range(g):
+        o = sv.spec_lmhead_draft(hd3[:, i].contiguous(), e["W_d"], pos=i, temperature=1.0,
+                                 seed=0, round=0)
+        xt_d[:, i], lse[:, i], logit[:, i] = o["tokens"], o["lse"], o["logit"]
+
+    def call_drafted(i):
+        rc = L.spec_lmhead_verify_drafted(
+            P(e["h_t"].data_ptr()), P(e["W_t"].data_ptr()), Ht, P(e["h_d"].data_ptr()),
+            P(e["W_d"].data_ptr()), Hd, P(xt_d.data_ptr()), P(lse.data_ptr()),
+            P(logit.data_ptr()), B, g, V, ctypes.c_float(1.0), 0, i, P(tok.data_ptr()),
+            P(cnt.data_ptr()), None, None, P(flg.data_ptr()), None, P(ws.data_ptr()),
+            ctypes.c_size_t(ws.numel()), sh)
+        if rc != 0:
+            raise RuntimeError(sv.status_string(rc))
+
+    dkms, dms = _kernel_times(L, stream, call_drafted, 4, reps)
     hbm, kind = peaks()
     tb, ts, tkind = tensor_peaks()
     wbytes = 2 * V * (Ht + Hd)
@@ -607,7 +631,12 @@ def measure_lmhead(L, dev, stream, rank, reps=100):
                          "traffic": LMHEAD_PASS1_TRAFFIC_BYTES, "algorithmic_bytes": wbytes},
             "tensor": {"kernel": "k_lm_pass1", "achieved": tf1, "peak": tb, "peak_kind": tkind,
                        "unit": "TFLOP/s", "frac": tf1 / tb, "algorithmic_flops": flops1},
-            "gpu_launches_per_round": 4}
+            "gpu_launches_per_round": 4,
+            "drafted": {"api": "spec_lmhead_verify_drafted", "rounds_per_s": 1000.0 / dms,
+                        "ms_per_round": dms,
+                        "kernel_ms": {"k_lm_pass1_target": dkms[0], "k_lm_finish": dkms[1],
+                                      "k_lm_pass2": dkms[2], "k_lm_merge": dkms[3]},
+                        "note": "drafts, lse and logits from spec_lmhead_draft (not timed)"}}
 
 
 def main():

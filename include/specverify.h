@@ -245,6 +245,7 @@ int spec_lmhead_verify(const void* h_target, const void* W_target, int Ht,
  *   out_tokens   [B] int32, the drafted tokens x_i (0 for an empty row)
  *   out_q        [B] float or NULL: q_i(x_i)
  *   out_lse      [B] float or NULL: log sum_v exp(z_v / T)
+ *   out_logit    [B] float or NULL: z at the drafted token (-inf for an empty row)
  *   debug_logits NULL in production; else [B][V] float receives the logits used
  *   workspace    >= sv_workspace_bytes(B, 1, V, SV_MODE_DRAFT)
  * Returns SV_ERR_UNSUPPORTED for Hd not a multiple of 64 (or above 16384),
@@ -252,8 +253,31 @@ int spec_lmhead_verify(const void* h_target, const void* W_target, int Ht,
  */
 int spec_lmhead_draft(const void* h_draft, const void* W_draft, int Hd, int B, int64_t V,
                       float temperature, uint64_t seed, uint64_t round, int pos,
-                      int32_t* out_tokens, float* out_q, float* out_lse, float* debug_logits,
-                      void* workspace, size_t workspace_bytes, void* cuda_stream);
+                      int32_t* out_tokens, float* out_q, float* out_lse, float* out_logit,
+                      float* debug_logits, void* workspace, size_t workspace_bytes,
+                      void* cuda_stream);
+
+/*
+ * spec_lmhead_verify_drafted -- spec_lmhead_verify for a round whose drafts came
+ * from spec_lmhead_draft: the draft step already knows each draft row's
+ * log-normaliser and the logit at its token, so the first GEMM pass computes
+ * the target rows only (W_target alone streams once; W_draft is read only by
+ * the pass that redraws a rejected row).
+ *   draft_lse    [B][gamma] float: out_lse of the draft step at each position
+ *   draft_logit  [B][gamma] float: out_logit of the draft step at each position
+ *   other arguments as spec_lmhead_verify (the same temperature as the draft
+ *   step); debug_logits receives the target rows only.
+ * q_i(x_i) is exp(draft_logit / T - draft_lse); the draft rows' flags follow
+ * from draft_lse (-inf: no mass; NaN or +inf: not finite).
+ */
+int spec_lmhead_verify_drafted(const void* h_target, const void* W_target, int Ht,
+                               const void* h_draft, const void* W_draft, int Hd,
+                               const int32_t* draft_tokens, const float* draft_lse,
+                               const float* draft_logit, int B, int gamma, int64_t V,
+                               float temperature, uint64_t seed, uint64_t round,
+                               int32_t* out_tokens, int32_t* out_counts, float* out_p_at_draft,
+                               float* out_q_at_draft, uint8_t* out_flags, float* debug_logits,
+                               void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /* Profiling aid (not thread-safe): when `events` is non-NULL, following calls
  * record events[0] on their stream before the first kernel and events[k] after

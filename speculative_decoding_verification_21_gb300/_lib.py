@@ -20,6 +20,7 @@ FLAG_ZERO_MASS, FLAG_NONFINITE, FLAG_RESIDUAL_FALLBACK, FLAG_TIMEOUT, FLAG_BAD_T
 
 EXPORTS = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verify_opts",
            "spec_verify_greedy", "spec_lmhead_verify", "spec_lmhead_draft",
+           "spec_lmhead_verify_drafted",
            "sv_set_timing_events", "sv_status_string", "sv_version")
 
 
@@ -71,7 +72,10 @@ def load(build_if_missing: bool = True):
         L.spec_lmhead_verify.argtypes = [P, P, I, P, P, I, P, I, I, I64, F, U64, U64, P, P, P, P,
                                          P, P, P, SZ, P]
         L.spec_lmhead_verify.restype = I
-        L.spec_lmhead_draft.argtypes = [P, P, I, I, I64, F, U64, U64, I, P, P, P, P, P, SZ, P]
+        L.spec_lmhead_draft.argtypes = [P, P, I, I, I64, F, U64, U64, I, P, P, P, P, P, P, SZ, P]
+        L.spec_lmhead_verify_drafted.argtypes = [P, P, I, P, P, I, P, P, P, I, I, I64, F, U64,
+                                                 U64, P, P, P, P, P, P, P, SZ, P]
+        L.spec_lmhead_verify_drafted.restype = I
         L.spec_lmhead_draft.restype = I
         L.sv_set_timing_events.argtypes = [P, I]
         L.sv_set_timing_events.restype = I
@@ -259,11 +263,52 @@ def spec_lmhead_verify(h_target, W_target, h_draft, W_draft, draft_tokens, *, B:
     return o
 
 
+def spec_lmhead_verify_drafted(h_target, W_target, h_draft, W_draft, draft_tokens, draft_lse,
+                               draft_logit, *, B: int, gamma: int, temperature: float = 1.0,
+                               seed: int = 0, round: int = 0, want_pq: bool = True,
+                               want_flags: bool = True, debug_logits=None, out=None,
+                               workspace=None, stream=None):
+    """spec_lmhead_verify with the draft rows' statistics from the draft step
+    (draft_lse, draft_logit [B, gamma] float32, spec_lmhead_draft's lse and logit)."""
+    torch = _torch()
+    L = load()
+    Mt, Ht = h_target.shape
+    Md, Hd = h_draft.shape
+    V = W_target.shape[1]
+    if Mt != B * (gamma + 1) or Md != B * gamma or tuple(W_target.shape) != (Ht, V) or \
+            tuple(W_draft.shape) != (Hd, V) or tuple(draft_tokens.shape) != (B, gamma) or \
+            tuple(draft_lse.shape) != (B, gamma) or tuple(draft_logit.shape) != (B, gamma):
+        raise ValueError("shape mismatch in spec_lmhead_verify_drafted")
+    _check_cuda(h_target, W_target, h_draft, W_draft, draft_tokens, draft_lse, draft_logit,
+                debug_logits)
+    dev = h_target.device
+    o = dict(out or {})
+    o.setdefault("tokens", torch.empty((B, gamma + 1), dtype=torch.int32, device=dev))
+    o.setdefault("counts", torch.empty((B,), dtype=torch.int32, device=dev))
+    if want_pq:
+        o.setdefault("p", torch.empty((B, gamma), dtype=torch.float32, device=dev))
+        o.setdefault("q", torch.empty((B, gamma), dtype=torch.float32, device=dev))
+    if want_flags:
+        o.setdefault("flags", torch.empty((B,), dtype=torch.uint8, device=dev))
+    sh = _stream_handle(stream)
+    need = workspace_bytes(B, gamma, V, SV_MODE_LMHEAD)
+    ws = workspace if workspace is not None else _ws_cache.get(need, dev, sh.value)
+    rc = L.spec_lmhead_verify_drafted(
+        _ptr(h_target), _ptr(W_target), Ht, _ptr(h_draft), _ptr(W_draft), Hd,
+        _ptr(draft_tokens), _ptr(draft_lse), _ptr(draft_logit), B, gamma, V,
+        float(temperature), int(seed) & (2**64 - 1), int(round) & (2**64 - 1),
+        _ptr(o["tokens"]), _ptr(o["counts"]), _ptr(o.get("p")), _ptr(o.get("q")),
+        _ptr(o.get("flags")), _ptr(debug_logits), _ptr(ws), ws.numel(), sh)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_lmhead_verify_drafted")
+    return o
+
+
 def spec_lmhead_draft(h_draft, W_draft, *, pos: int, temperature: float = 1.0, seed: int = 0,
                       round: int = 0, debug_logits=None, out=None, workspace=None,
                       stream=None):
     """Draft LM head + draw of one draft position through the C ABI (bf16 inputs).
-    Returns tokens [B] int32, q [B] float32 (q(x)), lse [B] float32."""
+    Returns tokens [B] int32, q [B] float32 (q(x)), lse [B] float32, logit [B] float32."""
     torch = _torch()
     L = load()
     B, Hd = h_draft.shape
@@ -276,12 +321,13 @@ def spec_lmhead_draft(h_draft, W_draft, *, pos: int, temperature: float = 1.0, s
     o.setdefault("tokens", torch.empty((B,), dtype=torch.int32, device=dev))
     o.setdefault("q", torch.empty((B,), dtype=torch.float32, device=dev))
     o.setdefault("lse", torch.empty((B,), dtype=torch.float32, device=dev))
+    o.setdefault("logit", torch.empty((B,), dtype=torch.float32, device=dev))
     sh = _stream_handle(stream)
     need = workspace_bytes(B, 1, V, SV_MODE_DRAFT)
     ws = workspace if workspace is not None else _ws_cache.get(need, dev, sh.value)
     rc = L.spec_lmhead_draft(_ptr(h_draft), _ptr(W_draft), Hd, B, V, float(temperature),
                              int(seed) & (2**64 - 1), int(round) & (2**64 - 1), int(pos),
-                             _ptr(o["tokens"]), _ptr(o["q"]), _ptr(o["lse"]),
+                             _ptr(o["tokens"]), _ptr(o["q"]), _ptr(o["lse"]), _ptr(o["logit"]),
                              _ptr(debug_logits), _ptr(ws), ws.numel(), sh)
     if rc != SV_OK:
         raise SpecVerifyError(rc, "spec_lmhead_draft")

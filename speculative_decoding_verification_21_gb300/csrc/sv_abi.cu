@@ -26,12 +26,13 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
                   int64_t V, float temperature, uint64_t seed, uint64_t round,
                   int32_t* out_tokens, int32_t* out_counts, float* out_p, float* out_q,
                   uint8_t* out_flags, float* debug_logits, void* workspace,
-                  size_t workspace_bytes, cudaStream_t stream);
+                  size_t workspace_bytes, cudaStream_t stream, const float* draft_lse,
+                  const float* draft_logit);
 size_t lmhead_workspace_bytes(int B, int gamma, int64_t V);
 int lmhead_draft(const void* h_draft, const void* W_draft, int Hd, int B, int64_t V,
                  float temperature, uint64_t seed, uint64_t round, int pos, int32_t* out_tokens,
-                 float* out_q, float* out_lse, float* debug_logits, void* workspace,
-                 size_t workspace_bytes, cudaStream_t stream);
+                 float* out_q, float* out_lse, float* out_logit, float* debug_logits,
+                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 size_t lmhead_draft_workspace_bytes(int B, int64_t V);
 }  // namespace sv
 
@@ -177,18 +178,38 @@ int spec_lmhead_verify(const void* h_target, const void* W_target, int Ht, const
   return sv::lmhead_verify(h_target, W_target, Ht, h_draft, W_draft, Hd, draft_tokens, B, gamma,
                            V, temperature, seed, round, out_tokens, out_counts, out_p_at_draft,
                            out_q_at_draft, out_flags, debug_logits, workspace, workspace_bytes,
-                           (cudaStream_t)cuda_stream);
+                           (cudaStream_t)cuda_stream, nullptr, nullptr);
+}
+
+int spec_lmhead_verify_drafted(const void* h_target, const void* W_target, int Ht,
+                               const void* h_draft, const void* W_draft, int Hd,
+                               const int32_t* draft_tokens, const float* draft_lse,
+                               const float* draft_logit, int B, int gamma, int64_t V,
+                               float temperature, uint64_t seed, uint64_t round,
+                               int32_t* out_tokens, int32_t* out_counts, float* out_p_at_draft,
+                               float* out_q_at_draft, uint8_t* out_flags, float* debug_logits,
+                               void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  int st = check_shape(B, gamma, V);
+  if (st != SV_OK) return st;
+  if (!(temperature > 0.0f && std::isfinite(temperature))) return SV_ERR_ARG;
+  if (B == 0) return SV_OK;
+  if (!draft_lse || !draft_logit) return SV_ERR_ARG;
+  return sv::lmhead_verify(h_target, W_target, Ht, h_draft, W_draft, Hd, draft_tokens, B, gamma,
+                           V, temperature, seed, round, out_tokens, out_counts, out_p_at_draft,
+                           out_q_at_draft, out_flags, debug_logits, workspace, workspace_bytes,
+                           (cudaStream_t)cuda_stream, draft_lse, draft_logit);
 }
 
 int spec_lmhead_draft(const void* h_draft, const void* W_draft, int Hd, int B, int64_t V,
                       float temperature, uint64_t seed, uint64_t round, int pos,
-                      int32_t* out_tokens, float* out_q, float* out_lse, float* debug_logits,
-                      void* workspace, size_t workspace_bytes, void* cuda_stream) {
+                      int32_t* out_tokens, float* out_q, float* out_lse, float* out_logit,
+                      float* debug_logits, void* workspace, size_t workspace_bytes,
+                      void* cuda_stream) {
   if (B < 0 || V < 1 || V >= ((int64_t)1 << 31)) return SV_ERR_ARG;
   if (!(temperature > 0.0f && std::isfinite(temperature))) return SV_ERR_ARG;
   if (B == 0) return SV_OK;
   return sv::lmhead_draft(h_draft, W_draft, Hd, B, V, temperature, seed, round, pos, out_tokens,
-                          out_q, out_lse, debug_logits, workspace, workspace_bytes,
+                          out_q, out_lse, out_logit, debug_logits, workspace, workspace_bytes,
                           (cudaStream_t)cuda_stream);
 }
 

@@ -80,6 +80,8 @@ struct LmArgs {
   int perm_t;          // target rows in smem are position-major (row i*B + b), else b*(gamma+1) + i
   int rep, rstride;    // passes 2, 3: copies of the rows in the row tile, rows apart
   int draft_pos;       // pass 3: position of the draft tokens being sampled
+  const float* dlse;   // [B][gamma] draft rows' log-normalisers from the draft step, or null
+  const float* dlogit; // [B][gamma] draft logits at the drafted tokens (with dlse)
   int nw, nh;          // W-ring and h-ring slots (nw >= nh)
   int a_half;          // bytes of the h tile of one 64-wide span (rows x 128)
   float temperature;
@@ -247,6 +249,17 @@ struct Jobs<2> {
                             const CUtensorMap* a1, const CUtensorMap* b1, const LmArgs& a) {
     if (s == 0) return Seg{a0, b0, a.kbt, 1, 0, 0, a.box_t, a.box_t, false};
     return Seg{a1, b1, a.kbd, 1, 0, kLmTileN, a.box_d, a.box_d, false};
+  }
+};
+
+// Pass 4 (the first pass of a drafted round): the target block only.
+template <>
+struct Jobs<4> {
+  static constexpr int kPerTile = 1;
+  __device__ static int nseg(int) { return 1; }
+  __device__ static Seg seg(int, int, const CUtensorMap* a0, const CUtensorMap* b0,
+                            const CUtensorMap*, const CUtensorMap*, const LmArgs& a) {
+    return side_seg(a0, b0, a.kbt, a.Mt, a.box_t, 0, a.perm_t != 0);
   }
 };
 
@@ -421,12 +434,15 @@ __device__ __forceinline__ void epilogue_pass1(const LmArgs& a, int t, uint32_t 
 }
 
 // One partial per row, CTA and column half: slot (row * nslot + cta) * 2 + half.
+// NSIDES 1: the target rows only (the draft rows' statistics come from the
+// draft step).
+template <int NSIDES>
 __device__ __forceinline__ void pass1_flush(const LmArgs& a, const Pass1Carry& cy, int quad,
                                             int half) {
   const int lane = threadIdx.x & 31;
   const int R1 = 2 * a.gamma + 1;
 #pragma unroll
-  for (int sd = 0; sd < 2; ++sd)
+  for (int sd = 0; sd < NSIDES; ++sd)
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
       const int r = side_row(a, sd, m, quad, lane);
@@ -749,8 +765,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                   lag.next(nw);
                 }
                 uint8_t* hst = hring + (size_t)hs.i * hslot;
-                // pass 2: `rep` copies of the compact rows, `rstride` rows apart
-                const int rep = (PASS >= 2) ? a.rep : 1;
+                // passes 2 and 3: `rep` copies of the rows, `rstride` rows apart
+                const int rep = (PASS == 2 || PASS == 3) ? a.rep : 1;
                 mbar_arrive_expect_tx(full + ws, (uint32_t)(rep * 2 * q.rows * kKAtom * 2));
                 for (int h = 0; h < 2; ++h) {
                   for (int cp = 0; cp < rep; ++cp) {
@@ -832,7 +848,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     Pass1Carry cy;
     Pass3Carry cy3;
     Cand2 tr[2], tp[2];
-    if (PASS == 1) {
+    if (PASS == 1 || PASS == 4) {
       carry_init(cy);
     } else if (PASS == 2) {
 #pragma unroll
@@ -856,7 +872,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         tc_fence_after();
         const uint32_t tacc = tbase + (uint32_t)(buf * 256);
         const int tv = vocab_tile<PASS>(t, nvt);
-        if (PASS == 1) {
+        if (PASS == 1 || PASS == 4) {
           if (job == 0)
             epilogue_pass1<0>(a, tv, tacc, quad, half, cy);
           else
@@ -874,14 +890,16 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     }
     // partials of this CTA (also after an abort: the error flag marks them)
     if (PASS == 1)
-      pass1_flush(a, cy, quad, half);
+      pass1_flush<2>(a, cy, quad, half);
+    else if (PASS == 4)
+      pass1_flush<1>(a, cy, quad, half);
     else if (PASS == 2)
       pass2_flush(a, quad, half, rows2, tr, tp, reinterpret_cast<LmCand*>(hring));
     else
       pass3_flush(a, quad, half, cy3, hring);
   }
 
-  if (threadIdx.x == 0 && *abort_flag) atomicOr(a.ctl + (PASS == 1 ? 1 : 2), 1u);
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(a.ctl + ((PASS == 1 || PASS == 4) ? 1 : 2), 1u);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -903,7 +921,17 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
   const bool err = *reinterpret_cast<volatile uint32_t*>(a.ctl + 1) != 0u;
   if (warp < nw - 1) {
     for (int k = warp; k < R1; k += nw - 1) {
-      RowStat rs = combine_row(a.part + ((int64_t)b * R1 + k) * a.nslot * 2, a.nslot * 2, nullptr);
+      RowStat rs;
+      if (a.dlse && k > gamma) {
+        // a drafted round: the draft row's statistics are its log-normaliser,
+        // as max = lse log2 e with sum 1
+        const float lse = __ldg(a.dlse + (int64_t)b * gamma + (k - gamma - 1));
+        rs.mc = lse * kLog2e;
+        rs.bits = (lse != lse) ? kRowNaN : 0;
+        rs.s = (lse != lse) ? CUDART_NAN : ((lse == -kInf) ? 0.0 : 1.0);
+      } else {
+        rs = combine_row(a.part + ((int64_t)b * R1 + k) * a.nslot * 2, a.nslot * 2, nullptr);
+      }
       if (err) {
         rs.bits |= kRowTimeout | kRowNaN;
         rs.s = CUDART_NAN;
@@ -915,7 +943,8 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
       const int32_t x = __ldg(a.xt + (int64_t)b * gamma + i);
       const bool ok = x >= 0 && x < a.V;
       const float* za = a.zat + (int64_t)b * R1;
-      sda[i] = DraftAt{x, ok ? __ldcg(za + i) : 0.0f, ok ? __ldcg(za + gamma + 1 + i) : 0.0f};
+      const float zd = a.dlogit ? __ldg(a.dlogit + (int64_t)b * gamma + i) : __ldcg(za + gamma + 1 + i);
+      sda[i] = DraftAt{x, ok ? __ldcg(za + i) : 0.0f, ok ? zd : 0.0f};
     }
   }
   __syncthreads();
@@ -1026,6 +1055,7 @@ struct DraftOut {
   int32_t* tokens;
   float* q;
   float* lse;
+  float* logit;
 };
 
 __global__ void __launch_bounds__(256) k_lm_draft_merge(LmArgs a, DraftOut out) {
@@ -1064,6 +1094,7 @@ __global__ void __launch_bounds__(256) k_lm_draft_merge(LmArgs a, DraftOut out) 
   if (out.lse)
     out.lse[b] = (rs.s > 0.0) ? (float)(((double)rs.mc + log2(rs.s)) * 0.6931471805599453)
                               : -CUDART_INF_F;
+  if (out.logit) out.logit[b] = ok ? zt : -CUDART_INF_F;
 }
 
 // ---------------------------------------------------------------------------
@@ -1105,6 +1136,8 @@ cudaError_t lm_device(LmDevice** out) {
     e = cudaFuncSetAttribute(k_lm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_lm<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_lm<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
     if (e != cudaSuccess) return e;
     d.ready = true;
   }
@@ -1180,7 +1213,11 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
                   int64_t V, float temperature, uint64_t seed, uint64_t round,
                   int32_t* out_tokens, int32_t* out_counts, float* out_p, float* out_q,
                   uint8_t* out_flags, float* debug_logits, void* workspace,
-                  size_t workspace_bytes, cudaStream_t stream) {
+                  size_t workspace_bytes, cudaStream_t stream, const float* draft_lse,
+                  const float* draft_logit) {
+  const bool drafted = draft_lse != nullptr;  // the draft rows' statistics are given
+  if (drafted && (!draft_logit || !aligned_to(draft_lse, 4) || !aligned_to(draft_logit, 4)))
+    return draft_logit ? SV_ERR_ALIGN : SV_ERR_ARG;
   if (!h_target || !W_target || !h_draft || !W_draft || !draft_tokens || !out_tokens ||
       !out_counts)
     return SV_ERR_ARG;
@@ -1230,8 +1267,11 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   a.out_p = out_p;
   a.out_q = out_q;
   a.out_flags = out_flags;
+  a.dlse = draft_lse;
+  a.dlogit = draft_logit;
 
-  // pass 1: all token rows; pass 2: the compact rows (at most B per side)
+  // pass 1: all token rows (a drafted round: the target rows only); pass 2: the
+  // compact rows (at most B per side)
   LmArgs a2 = a;
   a.box_t = round8(a.Mt);
   a.box_d = round8(a.Md);
@@ -1241,7 +1281,7 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   a2.rstride = (B + 31) & ~31;
   a2.rep = kTileM / a2.rstride;
   a2.rep = a2.rep > kMaxRep ? kMaxRep : a2.rep;
-  if (!ring_config(a, a.box_t > a.box_d ? a.box_t : a.box_d, 0, &smem1) ||
+  if (!ring_config(a, (drafted || a.box_t > a.box_d) ? a.box_t : a.box_d, 0, &smem1) ||
       !ring_config(a2, a2.rep > 1 ? a2.rep * a2.rstride : a2.box_t, kHStagesPass2, &smem2))
     return SV_ERR_UNSUPPORTED;
 
@@ -1264,7 +1304,10 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   const unsigned grid = (unsigned)(pl.nvt < dev->sms ? pl.nvt : dev->sms);
   a.nslot = a2.nslot = (int)grid;
   mark(0, stream);
-  k_lm<1><<<grid, kLmThreads, smem1, stream>>>(hT, WT, hD, WD, a);
+  if (drafted)
+    k_lm<4><<<grid, kLmThreads, smem1, stream>>>(hT, WT, hT, WT, a);
+  else
+    k_lm<1><<<grid, kLmThreads, smem1, stream>>>(hT, WT, hD, WD, a);
   mark(1, stream);
   const int fw = ((2 * gamma + 1) < 31 ? (2 * gamma + 1) : 31) + 1;
   e = launch_pdl(k_lm_finish, dim3((unsigned)B), dim3(32 * fw), 0, stream, a);
@@ -1285,15 +1328,15 @@ size_t lmhead_draft_workspace_bytes(int B, int64_t V) { return make_draft_plan(B
 // softmax(z / T) by Gumbel-max on Philox tag 2, q(x) and the log-normaliser.
 int lmhead_draft(const void* h_draft, const void* W_draft, int Hd, int B, int64_t V,
                  float temperature, uint64_t seed, uint64_t round, int pos, int32_t* out_tokens,
-                 float* out_q, float* out_lse, float* debug_logits, void* workspace,
-                 size_t workspace_bytes, cudaStream_t stream) {
+                 float* out_q, float* out_lse, float* out_logit, float* debug_logits,
+                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!h_draft || !W_draft || !out_tokens || pos < 0 || pos > 0xFFFFFF) return SV_ERR_ARG;
   if (Hd < 64 || Hd % 64 || Hd > kLmMaxHidden || B > kTileM || V % 8 != 0 ||
       V > ((int64_t)1 << 31) - 256)
     return SV_ERR_UNSUPPORTED;
   if (!aligned_to(h_draft, 16) || !aligned_to(W_draft, 16) || !aligned_to(out_tokens, 4) ||
       (out_q && !aligned_to(out_q, 4)) || (out_lse && !aligned_to(out_lse, 4)) ||
-      (debug_logits && !aligned_to(debug_logits, 16)))
+      (out_logit && !aligned_to(out_logit, 4)) || (debug_logits && !aligned_to(debug_logits, 16)))
     return SV_ERR_ALIGN;
   const DraftPlan pl = make_draft_plan(B, V);
   if (!workspace || workspace_bytes < pl.total) return SV_ERR_WORKSPACE;
@@ -1338,7 +1381,7 @@ int lmhead_draft(const void* h_draft, const void* W_draft, int Hd, int B, int64_
   k_lm<3><<<grid, kLmThreads, smem, stream>>>(hD, WD, hD, WD, a);
   mark(1, stream);
   e = launch_pdl(k_lm_draft_merge, dim3((unsigned)B), dim3(256), 0, stream, a,
-                 DraftOut{out_tokens, out_q, out_lse});
+                 DraftOut{out_tokens, out_q, out_lse, out_logit});
   if (e != cudaSuccess) return SV_ERR_CUDA;
   mark(2, stream);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;

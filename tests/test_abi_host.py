@@ -168,8 +168,8 @@ def test_lmhead_draft_argument_errors():
     L = sv.load()
 
     def call(h=FAKE, W=FAKE, Hd=128, B=4, V=1024, T=1.0, pos=0, tok=FAKE, ws=FAKE, wsb=1 << 22):
-        return L.spec_lmhead_draft(h, W, Hd, B, V, T, 0, 0, pos, tok, None, None, None, ws, wsb,
-                                   None)
+        return L.spec_lmhead_draft(h, W, Hd, B, V, T, 0, 0, pos, tok, None, None, None, None, ws,
+                                   wsb, None)
     assert call(B=0) == 0
     assert call(T=0.0) == -1
     assert call(T=float("nan")) == -1
@@ -191,3 +191,20 @@ def test_draft_workspace_size():
     a = sv.workspace_bytes(32, 1, 128256, 3)
     assert a > 0 and a % 256 == 0
     assert sv.workspace_bytes(64, 1, 128256, 3) > a
+
+
+def test_lmhead_verify_drafted_argument_errors():
+    L = sv.load()
+
+    def call(lse=FAKE, logit=FAKE, B=4, g=2, V=1024, T=1.0, Ht=128, ws=FAKE, wsb=1 << 26):
+        return L.spec_lmhead_verify_drafted(FAKE, FAKE, Ht, FAKE, FAKE, 128, FAKE, lse, logit, B,
+                                            g, V, T, 0, 0, FAKE, FAKE, None, None, None, None,
+                                            ws, wsb, None)
+    assert call(B=0) == 0
+    assert call(lse=None) == -1
+    assert call(logit=None) == -1
+    assert call(T=0.0) == -1
+    assert call(g=0) == -1
+    assert call(lse=ctypes.c_void_p(0x10002)) == -3
+    assert call(Ht=100) == -6
+    assert call(ws=None) == -4

@@ -114,3 +114,54 @@ def test_draft_then_verify_chain():
                               seed=4, round=9)
     torch.cuda.synchronize()
     np.testing.assert_allclose(v["q"].cpu().numpy(), qd.cpu().numpy(), rtol=1e-4)
+
+
+def _drafted_round(B, gamma, V, Ht, Hd, seed, T=1.0, rnd=0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    h_t = torch.randn((B * (gamma + 1), Ht), generator=g, device="cuda").to(torch.bfloat16)
+    W_t = (torch.randn((Ht, V), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    # a draft close to the target, so that rounds accept some drafts
+    h_d = (h_t.reshape(B, gamma + 1, Ht)[:, :gamma].float() +
+           0.05 * torch.randn((B, gamma, Hd), generator=g, device="cuda")).to(torch.bfloat16)
+    W_d = (W_t.float() + 0.002 * torch.randn((Hd, V), generator=g, device="cuda")).to(
+        torch.bfloat16)
+    xt = torch.empty((B, gamma), dtype=torch.int32, device="cuda")
+    lse = torch.empty((B, gamma), device="cuda")
+    logit = torch.empty((B, gamma), device="cuda")
+    zd = torch.empty((B, gamma, V), device="cuda")
+    for i in range(gamma):
+        dbg = torch.empty((B, V), device="cuda")
+        o = sv.spec_lmhead_draft(h_d[:, i].contiguous(), W_d, pos=i, temperature=T, seed=seed,
+                                 round=rnd, debug_logits=dbg)
+        xt[:, i], lse[:, i], logit[:, i] = o["tokens"], o["lse"], o["logit"]
+        zd[:, i] = dbg
+    h_d = h_d.reshape(B * gamma, Hd).contiguous()
+    return h_t, W_t, h_d, W_d, xt, lse, logit, zd
+
+
+@pytest.mark.parametrize("B,gamma,V,Ht,Hd", [(8, 3, 4096, 128, 128), (32, 4, 16384, 256, 256)])
+def test_drafted_verify_parity(B, gamma, V, Ht, Hd):
+    """spec_lmhead_verify_drafted against the oracle on the logits both steps used:
+    the target rows from the verify's debug output, the draft rows from the draft
+    step's."""
+    from tests._parity import assert_parity, to_np
+    T = 0.9
+    for rnd in range(2):
+        h_t, W_t, h_d, W_d, xt, lse, logit, zd = _drafted_round(B, gamma, V, Ht, Hd, seed=41 + rnd,
+                                                                 T=T, rnd=rnd)
+        dbg = torch.full((B * (2 * gamma + 1), V), float("nan"), device="cuda")
+        v = sv.spec_lmhead_verify_drafted(h_t, W_t, h_d, W_d, xt, lse, logit, B=B, gamma=gamma,
+                                          temperature=T, seed=7, round=rnd, debug_logits=dbg)
+        torch.cuda.synchronize()
+        zt = dbg.reshape(B, 2 * gamma + 1, V)[:, :gamma + 1]
+        assert torch.isfinite(zt).all()
+        orc = oracle.spec_verify(zt.cpu().numpy(), zd.cpu().numpy(), xt.cpu().numpy(),
+                                 temperature=T, seed=7, rnd=rnd, threads=8)
+        assert_parity(to_np(v), orc, gamma, what=f"drafted verify B={B} round {rnd}")
+        assert int(orc["counts"].max()) > 0  # some drafts accepted
+        # the plain fused verify on the same inputs agrees
+        w = sv.spec_lmhead_verify(h_t, W_t, h_d, W_d, xt, B=B, gamma=gamma, temperature=T, seed=7,
+                                  round=rnd)
+        torch.cuda.synchronize()
+        assert torch.equal(w["counts"], v["counts"])
+        assert torch.equal(w["tokens"], v["tokens"])
