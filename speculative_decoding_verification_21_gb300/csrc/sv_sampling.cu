@@ -292,66 +292,48 @@ __device__ __forceinline__ float fkey_inv(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Histogram of one radix pass: the digit (bits [shift, shift+width) of the key)
-// of every ranked entry whose higher bits equal `prefix` under `mask`, counted
-// into this warp's own copy of the histogram (fewer lanes collide on one
-// shared-memory counter).
+// Histogram digits of the top-k radix select: bf16 values fill only the top 16
+// bits of the key (digits of 10 and 6 bits; the wide first digit spreads
+// logits, which crowd into a few exponents), fp32 values all 32 (four of 8).
 template <int DT>
-__device__ __forceinline__ void topk_pass(const char* base, int64_t V, uint32_t prefix,
-                                          uint32_t mask, int shift, uint32_t dmask,
-                                          uint32_t* hist) {
-  auto count = [&](float z) {
-    if (z != z) return;  // NaN is not ranked
-    const uint32_t key = fkey(z);
-    if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
-  };
-  for_each_in_chunk<DT, 4>(
-      base, 0, V,
-      [&](int64_t, const uint4& vec) {
-        float f[VecInfo<DT>::kElems];
-        unpack<DT>(vec, f);
-#pragma unroll
-        for (int e = 0; e < VecInfo<DT>::kElems; ++e) count(f[e]);
-      },
-      [&](int64_t, float z) { count(z); });
-}
+struct RadixDigits {
+  static constexpr int kPasses = (DT == SV_BF16) ? 2 : 4;
+  static constexpr int kMaxBins = (DT == SV_BF16) ? 1024 : 256;
+  __device__ static int width(int pass) { return (DT == SV_BF16) ? (pass == 0 ? 10 : 6) : 8; }
+};
 
-// One CTA per logit row: thr[row] = the k-th largest of the row's non-NaN
-// values (repeats counted), -inf when it has fewer than k of them.  A
-// most-significant-digit radix select over fkey with per-warp histograms: bf16
-// values fill only the top 16 bits of the key (digits of 10 and 6 bits; the
-// wide first digit spreads logits, which crowd into a few exponents), fp32
-// values all 32 (four 8-bit digits).
-template <int DT>
-__global__ void __launch_bounds__(kThreads) k_topk(const void* zt, const void* zd, int gamma,
-                                                  int64_t V, int k, float* __restrict__ thr) {
+// The k-th largest of the values that `visit` hands this CTA (each thread calls
+// its argument for each of its values; NaN is not ranked), repeats counted;
+// -inf when there are fewer than k.  A most-significant-digit radix select over
+// fkey with per-warp shared-memory histograms hist[kWarps][kMaxBins] (fewer
+// lanes collide on one counter).  Called by all threads; returns in all.
+template <int DT, class Visit>
+__device__ float radix_kth(Visit&& visit, int k, uint32_t* hist, uint32_t* s_sel) {
   constexpr int kWarps = kThreads / 32;
-  constexpr int kPasses = (DT == SV_BF16) ? 2 : 4;
-  constexpr int kMaxBins = (DT == SV_BF16) ? 1024 : 256;
-  __shared__ uint32_t hist[kWarps][kMaxBins];
-  __shared__ uint32_t s_sel[3];  // prefix, rank still to find within it, fewer-than-k flag
-  const int R1 = 2 * gamma + 1;
-  const int row = blockIdx.x;
-  const int b = row / R1, kk = row - b * R1;
-  const char* base = row_ptr<DT>(zt, zd, b, kk, gamma, V);
+  using Dg = RadixDigits<DT>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t prefix = 0, mask = 0, remaining = (uint32_t)k;
   int shift = 32;
   bool few = false;
-  for (int pass = 0; pass < kPasses && !few; ++pass) {
-    const int width = (DT == SV_BF16) ? (pass == 0 ? 10 : 6) : 8;
+  for (int pass = 0; pass < Dg::kPasses && !few; ++pass) {
+    const int width = Dg::width(pass);
     shift -= width;
     const uint32_t dmask = (1u << width) - 1u;
     const int nbins = 1 << width;
-    for (int i = threadIdx.x; i < kWarps * kMaxBins; i += blockDim.x) (&hist[0][0])[i] = 0u;
+    for (int i = threadIdx.x; i < kWarps * Dg::kMaxBins; i += blockDim.x) hist[i] = 0u;
     __syncthreads();
-    topk_pass<DT>(base, V, prefix, mask, shift, dmask, hist[warp]);
+    uint32_t* h = hist + warp * Dg::kMaxBins;
+    visit([&](float z) {
+      if (z != z) return;  // NaN is not ranked
+      const uint32_t key = fkey(z);
+      if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & dmask], 1u);
+    });
     __syncthreads();
     for (int d = threadIdx.x; d < nbins; d += blockDim.x) {  // sum the warps' copies
       uint32_t n = 0;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) n += hist[w][d];
-      hist[0][d] = n;
+      for (int w = 0; w < kWarps; ++w) n += hist[w * Dg::kMaxBins + d];
+      hist[d] = n;
     }
     __syncthreads();
     if (warp == 0) {
@@ -359,7 +341,7 @@ __global__ void __launch_bounds__(kThreads) k_topk(const void* zt, const void* z
       const int per = nbins / 32;
       const int top = nbins - 1 - per * lane;
       uint32_t cl = 0;
-      for (int j = 0; j < per; ++j) cl += hist[0][top - j];
+      for (int j = 0; j < per; ++j) cl += hist[top - j];
       uint32_t incl = cl;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -369,12 +351,12 @@ __global__ void __launch_bounds__(kThreads) k_topk(const void* zt, const void* z
       const uint32_t excl = incl - cl;
       const bool mine = excl < remaining && remaining <= incl;
       if (__ballot_sync(0xffffffffu, mine) == 0u) {
-        if (lane == 0) s_sel[2] = 1u;  // fewer than k ranked values: nothing is cut
+        if (lane == 0) s_sel[2] = 1u;  // fewer than k ranked values
       } else if (mine) {
         uint32_t above = excl;
         int d = top;
         for (int j = 0; j < per; ++j, --d) {
-          const uint32_t n = hist[0][d];
+          const uint32_t n = hist[d];
           if (above + n >= remaining) break;
           above += n;
         }
@@ -390,16 +372,170 @@ __global__ void __launch_bounds__(kThreads) k_topk(const void* zt, const void* z
     mask |= dmask << shift;
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    float tau = -kInf;
-    if (!few) {
-      // bf16 keys leave the low 16 bits to the sign: 0 for a positive value, 1s otherwise
-      const uint32_t key =
-          (DT == SV_BF16) ? (prefix | ((prefix & 0x80000000u) ? 0u : 0xFFFFu)) : prefix;
-      tau = fkey_inv(key);
-    }
-    thr[row] = tau;
+  if (few) return -kInf;
+  // bf16 keys leave the low 16 bits to the sign: 0 for a positive value, 1s otherwise
+  const uint32_t key =
+      (DT == SV_BF16) ? (prefix | ((prefix & 0x80000000u) ? 0u : 0xFFFFu)) : prefix;
+  return fkey_inv(key);
+}
+
+// Every value of one logit row, for radix_kth (16-byte vectors where aligned).
+template <int DT>
+struct RowVisit {
+  const char* base;
+  int64_t V;
+  template <class F>
+  __device__ void operator()(F&& f) const {
+    for_each_in_chunk<DT, 4>(
+        base, 0, V,
+        [&](int64_t, const uint4& vec) {
+          float v[VecInfo<DT>::kElems];
+          unpack<DT>(vec, v);
+#pragma unroll
+          for (int e = 0; e < VecInfo<DT>::kElems; ++e) f(v[e]);
+        },
+        [&](int64_t, float z) { f(z); });
   }
+};
+
+// One CTA per logit row: thr[row] = the k-th largest of the row's non-NaN
+// values (repeats counted), -inf when it has fewer than k of them.
+template <int DT>
+__global__ void __launch_bounds__(kThreads) k_topk(const void* zt, const void* zd, int gamma,
+                                                  int64_t V, int k, float* __restrict__ thr) {
+  __shared__ uint32_t hist[(kThreads / 32) * RadixDigits<DT>::kMaxBins];
+  __shared__ uint32_t s_sel[3];
+  const int R1 = 2 * gamma + 1;
+  const int row = blockIdx.x;
+  const int b = row / R1, kk = row - b * R1;
+  const float tau = radix_kth<DT>(RowVisit<DT>{row_ptr<DT>(zt, zd, b, kk, gamma, V), V}, k,
+                                  hist, s_sel);
+  if (threadIdx.x == 0) thr[row] = tau;
+}
+
+// Shared-memory candidates of the top-k select that follows a plain sweep.
+constexpr int kTopkCandCap = 4096;
+
+// Dynamic shared memory of k_topk_cand: per-warp histograms, then candidates.
+static size_t topk_cand_smem_bytes(int dtype) {
+  return (size_t)(kThreads / 32) * (dtype == SV_BF16 ? 1024 : 256) * sizeof(uint32_t) +
+         (size_t)kTopkCandCap * sizeof(float);
+}
+
+// Top-k after a plain sweep, from candidates (one CTA per logit row).  The k-th
+// largest logit is at least the k-th largest of the row's chunk maxima (k
+// chunks each hold a value at or above that), so only entries whose scaled
+// value reaches that bound can be kept: they are gathered into shared memory,
+// the threshold is their k-th largest, and the kept mass is summed over them.
+// The row's chunk partials are then replaced by one partial of the kept
+// entries, so the round needs no second sweep.  With more than kTopkCandCap
+// candidates, or k above the number of chunks, the threshold comes from radix
+// passes over the whole row and the kept mass from one more pass.  A row with a
+// NaN or timed-out partial is left as it is (no cut).
+template <int DT>
+__global__ void __launch_bounds__(kThreads) k_topk_cand(SweepCtx x, int k,
+                                                       float* __restrict__ thr) {
+  constexpr int kWarps = kThreads / 32;
+  extern __shared__ uint32_t dsm[];
+  uint32_t* hist = dsm;  // [kWarps][RadixDigits<DT>::kMaxBins]
+  float* cand = reinterpret_cast<float*>(dsm + kWarps * RadixDigits<DT>::kMaxBins);
+  __shared__ uint32_t s_sel[3];
+  __shared__ uint32_t s_n;
+  __shared__ int s_bad;
+  __shared__ float s_max;
+  __shared__ float s_red[kWarps];
+  const int R1 = 2 * x.gamma + 1;
+  const int row = blockIdx.x;
+  const int b = row / R1, kk = row - b * R1;
+  const int64_t V = x.V;
+  const int nch = x.nch;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float2* pr = x.part + (int64_t)row * nch;
+  const RowVisit<DT> rowv{row_ptr<DT>(x.zt, x.zd, b, kk, x.gamma, V), V};
+  const float T = x.row_T ? __ldg(x.row_T + b) : x.temperature;
+  const float c = log2_scale(inv_temperature(T));
+  if (threadIdx.x == 0) {
+    s_n = 0u;
+    s_bad = 0;
+  }
+  __syncthreads();
+  // the row's max and whether it is usable
+  float m = -kInf;
+  int bad = 0;
+  for (int j = threadIdx.x; j < nch; j += blockDim.x) {
+    const float2 p = __ldcg(pr + j);
+    if (p.x != p.x || p.y < 0.0f) bad = 1;
+    m = fmaxf(m, p.x);
+  }
+  m = warp_max(m);
+  const bool any_bad = __any_sync(0xffffffffu, bad) != 0;
+  if (lane == 0) {
+    s_red[warp] = m;
+    if (any_bad) atomicOr(&s_bad, 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mm = -kInf;
+    for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, s_red[w]);
+    s_max = mm;
+  }
+  __syncthreads();
+  if (s_bad || !(s_max > -kInf)) {  // not finite, timed out or empty: no cut
+    if (threadIdx.x == 0) thr[row] = -kInf;
+    return;
+  }
+  const float M = s_max;
+  // lower bound of the threshold: the k-th largest scaled chunk max
+  const float bound = (k <= nch) ? radix_kth<SV_F32>(
+                                       [&](auto&& f) {
+                                         for (int j = threadIdx.x; j < nch; j += blockDim.x)
+                                           f(__ldcg(pr + j).x);
+                                       },
+                                       k, hist, s_sel)
+                                 : -kInf;
+  if (bound > -kInf) {
+    rowv([&](float z) {
+      if (z == z && z * c >= bound) {
+        const uint32_t i = atomicAdd(&s_n, 1u);
+        if (i < (uint32_t)kTopkCandCap) cand[i] = z;
+      }
+    });
+  }
+  __syncthreads();
+  const uint32_t n = s_n;
+  const bool from_cand = bound > -kInf && n <= (uint32_t)kTopkCandCap;
+  float tau;
+  if (from_cand) {
+    tau = radix_kth<DT>(
+        [&](auto&& f) {
+          for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) f(cand[i]);
+        },
+        k, hist, s_sel);
+  } else {
+    tau = radix_kth<DT>(rowv, k, hist, s_sel);
+  }
+  // the kept mass, relative to the row's max
+  float sum = 0.0f;
+  auto add = [&](float z) {
+    if (z >= tau) sum += ex2(fmaf(z, c, -M));
+  };
+  if (from_cand) {
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) add(cand[i]);
+  } else {
+    rowv(add);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  __syncthreads();
+  if (lane == 0) s_red[warp] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float S = 0.0f;
+    for (int w = 0; w < kWarps; ++w) S += s_red[w];
+    thr[row] = tau;
+    pr[0] = make_float2(M, S);
+  }
+  for (int j = 1 + (int)threadIdx.x; j < nch; j += blockDim.x) pr[j] = make_float2(-kInf, 0.0f);
 }
 
 // Nucleus (top-p) threshold of one logit row (same passage: nucleus zeroes the
@@ -771,6 +907,12 @@ static cudaError_t device_info(DeviceInfo** out) {
     e = cudaFuncSetAttribute(k_topp<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)topp_smem_bytes(SV_BF16));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_topk_cand<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)topk_cand_smem_bytes(SV_BF16));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_topk_cand<SV_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)topk_cand_smem_bytes(SV_F32));
+    if (e != cudaSuccess) return e;
     if ((e = sweep_setup<SV_F32, false>(d)) != cudaSuccess) return e;
     if ((e = sweep_setup<SV_BF16, false>(d)) != cudaSuccess) return e;
     if ((e = sweep_setup<SV_F32, true>(d)) != cudaSuccess) return e;
@@ -835,7 +977,15 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
     }
   };
   mark(0, stream);
-  if (topk)
+  if (topk && !topp) {
+    // top-k alone: a plain sweep, then the threshold and the kept mass from the
+    // entries at or above the k-th largest chunk max (no second sweep)
+    sweep(false, sx);
+    k_topk_cand<DT><<<(unsigned)((int64_t)B * R1), kThreads, topk_cand_smem_bytes(DT), stream>>>(
+        sx, top_k, thr);
+    mark(1, stream);
+  }
+  if (topk && topp)
     k_topk<DT><<<(unsigned)((int64_t)B * R1), kThreads, 0, stream>>>(zt, zd, gamma, V, top_k,
                                                                         thr);
   if (topp) {
@@ -846,8 +996,10 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
     k_topp<DT><<<(unsigned)((int64_t)B * R1), kThreads, topp_smem_bytes(DT), stream>>>(
         sx, top_p, topk ? 1 : 0, thr);
   }
-  sweep(masked, sx);
-  mark(1, stream);
+  if (!(topk && !topp)) {
+    sweep(masked, sx);
+    mark(1, stream);
+  }
   // One resident wave of draw CTAs when the batch allows: every CTA takes its
   // batch row's decision before drawing, so a second wave would pay that
   // latency again.  At least kChunkDraw entries per CTA.

@@ -1,7 +1,9 @@
 """Top-k adjusted verify (spec_verify_opts, top_k) on the GPU against the oracle.
 
-The GPU finds each row's threshold with a radix select and masks the tail in
-the sweep, the decision, the draw and the overlap; the oracle sorts each row.
+The GPU finds each row's threshold from candidates at or above the k-th largest
+chunk max (or, for large k, many candidates or ties, by radix passes over the
+row) and masks the tail in the decision, the draw and the overlap; the oracle
+sorts each row.
 Rules are those of tests/_parity.py.  Also: k >= V is the plain round bit for
 bit, and k = 1 with drafts at the draft argmax equals greedy verify.
 """
@@ -74,7 +76,10 @@ def test_sample_b64_topk(k):
                                             (torch.bfloat16, 4099, 33, False),
                                             (torch.bfloat16, 2048, 10, True),
                                             (torch.float32, 3000, 100, True),
-                                            (torch.float32, 64, 63, False)])
+                                            (torch.float32, 64, 63, False),
+                                            (torch.bfloat16, 40000, 10, False),
+                                            (torch.bfloat16, 40000, 10, True),
+                                            (torch.float32, 30000, 5, False)])
 def test_topk_shapes_and_ties(dtype, V, k, ties):
     B, g = 24, 3
     zt, zd, gen = case(V, B, g, dtype, seed=V + k, ties=ties)
