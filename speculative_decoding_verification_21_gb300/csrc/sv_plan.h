@@ -20,7 +20,7 @@ constexpr size_t kAlign = 256;
 
 // Persistent bulk-copy sweep: warps per CTA, pipeline stages per warp, bytes per chunk.
 constexpr int kSweepWarps = 8;
-constexpr int kSweepStages = 3;
+constexpr int kSweepStages = 2;
 constexpr int kSweepChunkBytes = 4096;
 
 SV_HD inline size_t sweep_smem_bytes() {

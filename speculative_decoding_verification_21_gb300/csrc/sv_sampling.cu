@@ -10,7 +10,7 @@
 //             rows: max and sum of 2^(y - max), y = z * T^-1 * log2 e.
 //             k_sweep_tma (rows whose byte length is a multiple of 16): a
 //             persistent kernel; every warp streams 4 KB chunks, interleaved
-//             across warps in batch-row order, through a 3-stage bulk-copy (TMA)
+//             across warps in batch-row order, through a 2-stage bulk-copy (TMA)
 //             pipeline in shared memory.  k_sweep (any shape): one CTA per
 //             8192-logit chunk with 16-byte vector loads.
 //   k_draw    one CTA per (batch row, 8192 entries).  Each CTA first takes
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
 // walks memory in address order; each chunk leaves one (max, sum) partial.
 // --------------------------------------------------------------------------
 template <int DT, bool TOPK>
-__global__ void __launch_bounds__(kSweepWarps * 32, 2) k_sweep_tma(SweepCtx x) {
+__global__ void __launch_bounds__(kSweepWarps * 32, 3) k_sweep_tma(SweepCtx x) {
   pdl_launch_dependents();  // the draw kernel may be scheduled now; it waits for us
   constexpr int kBytes = (DT == SV_F32) ? 4 : 2;
   constexpr int CH = kSweepChunkBytes / kBytes;  // logits per chunk
