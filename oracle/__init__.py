@@ -66,6 +66,9 @@ def lib():
             L.svo_uniform_row.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
                                           ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int64,
                                           ctypes.c_int64, P]
+            L.svo_draw_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
+                                           ctypes.c_uint64]
+            L.svo_draw_uniform.restype = ctypes.c_double
             for name in ("svo_accept_mass", "svo_residual"):
                 getattr(L, name).argtypes = [P, P, ctypes.c_int64, P]
                 getattr(L, name).restype = ctypes.c_double
@@ -107,6 +110,11 @@ def philox4x32_10(ctr, key) -> np.ndarray:
 
 def uniform(seed, tag, pos, b, rnd, c0, lane) -> float:
     return lib().svo_uniform(seed, tag, pos, b, rnd, c0, lane)
+
+
+def draw_uniform(seed, pos, b, rnd) -> float:
+    """The uniform U in [0, 1) (53 bits) of the target's own draw at position pos."""
+    return lib().svo_draw_uniform(int(seed) & (2**64 - 1), pos, b, int(rnd) & (2**64 - 1))
 
 
 def uniform_row(seed, tag, pos, b, rnd, v0, n) -> np.ndarray:
@@ -162,6 +170,10 @@ def spec_verify(zt, zd, xt, temperature=1.0, row_temperature=None, seed=0, rnd=0
     top_p: then keep each row's nucleus of probability top_p (1: off); the output
     "nucleus_gap" [B] is the smallest distance of top_p from a cut's cumulative
     probabilities in the batch row.
+
+    The target's own token is drawn by the inverse transform; "gap" [B] is the
+    distance of U W from the nearer end of the drawn token's cumulative interval
+    (probability units; NaN for an empty row).
 
     rows: optional list of batch-row indices to compute (others left zero);
     threads: run disjoint row ranges in that many Python threads (each a plain

@@ -26,8 +26,12 @@
  * Readings where the pages are silent (each also listed in the design notes):
  *  - temperature: s = z * fl32(1/T) for target and draft rows alike;
  *  - the accept comparison is "<=", with IEEE p/q (p/0 = inf accepts, 0/0 rejects);
- *  - "sample" = Gumbel-max argmax(log w_v + g_v), g = -log(-log u), ties to the
- *    lowest index, u from Philox4x32-10 with the documented counter layout;
+ *  - "sample" the target's own token = inverse transform: one uniform U in [0, 1)
+ *    with 53 random bits (Philox4x32-10, tag 1, at the draw position), and the
+ *    smallest v, in vocabulary order, whose cumulative weight exceeds U times the
+ *    total weight;
+ *  - "sample" a draft token (the draft side) = Gumbel-max argmax(log w_v + g_v),
+ *    g = -log(-log u), ties to the lowest index, u from Philox tag 2;
  *  - an all-zero residual (possible only by rounding) falls back to p_n;
  *  - an empty row (no finite logit) emits token 0 and sets ZERO_MASS.
  */
@@ -88,15 +92,23 @@ void svo_uniform_row(uint64_t seed, uint32_t tag, uint32_t pos, uint32_t b, uint
   }
 }
 
-/* Gumbel noise for vocabulary entry v at a draw position (tag 1). */
+/* Gumbel noise for vocabulary entry v at a draft position (tag 2). */
 static double gumbel_tag(uint64_t seed, uint32_t tag, uint32_t pos, uint32_t b, uint64_t round,
                          int64_t v) {
   double u = svo_uniform(seed, tag, pos, b, round, (uint32_t)(v >> 2), (int)(v & 3));
   return -log(-log(u));
 }
 
-static double gumbel(uint64_t seed, uint32_t pos, uint32_t b, uint64_t round, int64_t v) {
-  return gumbel_tag(seed, 1u, pos, b, round, v);
+/* The uniform of the target's own draw at position pos: counter (0, 1<<24 | pos,
+ * b, round); the top 21 bits of word 0 and all 32 bits of word 1 form a 53-bit
+ * integer k, and U = k 2^-53 lies in [0, 1). */
+double svo_draw_uniform(uint64_t seed, uint32_t pos, uint32_t b, uint64_t round) {
+  uint32_t ctr[4] = {0u, (1u << 24) | (pos & 0xFFFFFFu), b, (uint32_t)round};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  svo_philox4x32_10(ctr, key, out);
+  uint64_t k = ((uint64_t)(out[0] >> 11) << 32) | (uint64_t)out[1];
+  return (double)k * 0x1p-53;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -247,43 +259,55 @@ static double prob(const row_t* r, int64_t v) {
 
 static int row_nonfinite(const row_t* r) { return !isfinite(r->S) || isnan(r->m) || r->m == INFINITY; }
 
-/* Gumbel-max over the entries whose log-weight lw(v) is finite:
- * argmax_v lw(v) + g_v, ties to the lowest v.  Returns -1 if there is no
- * candidate; *gap = top1 - top2 key (inf with a single candidate). */
-typedef double (*logw_fn)(const void* ctx, int64_t v);
+/* Inverse-transform draw: with W the sum of the weights w(v) >= 0 and
+ * C_v = w(0) + ... + w(v), the smallest v with C_v > U W.  Returns -1 when no
+ * weight is positive.  *gap is the distance of U W from the nearer end of the
+ * chosen entry's interval [C_{v-1}, C_v) (in the weights' units).  When the
+ * rounded sums leave U W at or above C_{V-1}, the last positive entry is taken
+ * with gap 0. */
+typedef double (*weight_fn)(const void* ctx, int64_t v);
 
-static int64_t gumbel_argmax(logw_fn lw, const void* ctx, int64_t V, uint64_t seed, uint32_t pos,
-                             uint32_t b, uint64_t round, double* gap) {
-  int64_t best = -1;
-  double k1 = -INFINITY, k2 = -INFINITY;
+static int64_t inverse_cdf_draw(weight_fn w, const void* ctx, int64_t V, double U, double* gap) {
+  double W = 0.0;
+  int64_t last = -1;
   for (int64_t v = 0; v < V; ++v) {
-    double w = lw(ctx, v);
-    if (!(w > -INFINITY) || w == INFINITY) continue; /* excludes -inf, NaN, +inf */
-    double key = w + gumbel(seed, pos, b, round, v);
-    if (best < 0 || key > k1) {
-      k2 = k1;
-      k1 = key;
-      best = v;
-    } else if (key > k2) {
-      k2 = key;
+    double x = w(ctx, v);
+    if (x > 0.0) {
+      W += x;
+      last = v;
     }
   }
-  if (gap) *gap = best < 0 ? NAN : k1 - k2;
-  return best;
+  if (gap) *gap = NAN;
+  if (last < 0) return -1;
+  const double t = U * W;
+  double C = 0.0;
+  for (int64_t v = 0; v <= last; ++v) {
+    double x = w(ctx, v);
+    if (!(x > 0.0)) continue;
+    double Cn = C + x;
+    if (Cn > t) {
+      if (gap) *gap = fmin(t - C, Cn - t);
+      return v;
+    }
+    C = Cn;
+  }
+  if (gap) *gap = 0.0;
+  return last;
 }
 
-static double logw_scaled_logit(const void* ctx, int64_t v) { return ((const row_t*)ctx)->s[v]; }
+/* p(v) of a loaded row. */
+static double weight_prob(const void* ctx, int64_t v) { return prob((const row_t*)ctx, v); }
 
 typedef struct {
   const row_t* t;
   const row_t* d;
 } pair_t;
 
-/* log max(0, p - q) with p, q the normalised target/draft probabilities. */
-static double logw_residual(const void* ctx, int64_t v) {
+/* max(0, p(v) - q(v)) with p, q the normalised target/draft probabilities ([A2]). */
+static double weight_residual(const void* ctx, int64_t v) {
   const pair_t* pr = (const pair_t*)ctx;
   double r = prob(pr->t, v) - prob(pr->d, v);
-  return r > 0.0 ? log(r) : -INFINITY;
+  return r > 0.0 ? r : 0.0;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -295,11 +319,11 @@ int svo_spec_verify(const void* zt, const void* zd, const int32_t* xt,
                     uint64_t seed, uint64_t round,
                     int32_t* tokens, int32_t* counts,
                     double* p_at, double* q_at, double* ratio_out, double* u_out,
-                    double* beta_out, double* gumbel_gap, double* resid_mass,
+                    double* beta_out, double* draw_gap, double* resid_mass,
                     uint8_t* flags) {
   return svo_spec_verify_rows(zt, zd, xt, B, gamma, V, dtype, temperature, row_temperature, seed,
                               round, tokens, counts, p_at, q_at, ratio_out, u_out, beta_out,
-                              gumbel_gap, resid_mass, flags, 0, B);
+                              draw_gap, resid_mass, flags, 0, B);
 }
 
 int svo_spec_verify_rows(const void* zt, const void* zd, const int32_t* xt,
@@ -308,11 +332,11 @@ int svo_spec_verify_rows(const void* zt, const void* zd, const int32_t* xt,
                          uint64_t seed, uint64_t round,
                          int32_t* tokens, int32_t* counts,
                          double* p_at, double* q_at, double* ratio_out, double* u_out,
-                         double* beta_out, double* gumbel_gap, double* resid_mass,
+                         double* beta_out, double* draw_gap, double* resid_mass,
                          uint8_t* flags, int b_begin, int b_end) {
   return svo_spec_verify_ex(zt, zd, xt, B, gamma, V, dtype, temperature, row_temperature, seed,
                             round, tokens, counts, p_at, q_at, ratio_out, u_out, beta_out,
-                            gumbel_gap, resid_mass, flags, b_begin, b_end, NULL);
+                            draw_gap, resid_mass, flags, b_begin, b_end, NULL);
 }
 
 int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
@@ -321,7 +345,7 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
                        uint64_t seed, uint64_t round,
                        int32_t* tokens, int32_t* counts,
                        double* p_at, double* q_at, double* ratio_out, double* u_out,
-                       double* beta_out, double* gumbel_gap, double* resid_mass,
+                       double* beta_out, double* draw_gap, double* resid_mass,
                        uint8_t* flags, int b_begin, int b_end, const svo_options* opt) {
   /* Lenience l (Appendix A.5 as the page summarises it): the comparison uses l q(x). */
   const double l = opt ? opt->lenience : 1.0;
@@ -408,28 +432,24 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
       break;
     }
 
-    /* The target's own token. */
+    /* The target's own token, by the inverse transform with the uniform of position n. */
     int64_t t;
     double gap = NAN, rmass = NAN;
+    const double Ud = svo_draw_uniform(seed, (uint32_t)n, (uint32_t)b, round);
     if (n == gamma) {
       /* Clean sweep: bonus token from p_gamma. */
-      t = gumbel_argmax(logw_scaled_logit, &rows[gamma], V, seed, (uint32_t)gamma, (uint32_t)b,
-                        round, &gap);
+      t = inverse_cdf_draw(weight_prob, &rows[gamma], V, Ud, &gap);
       if (t < 0) { t = 0; flag |= SVO_FLAG_ZERO_MASS; }
     } else {
       /* Rejection at n: residual max(0, p_n - q_n). */
       pair_t pr = {&rows[n], &rows[gamma + 1 + n]};
       rmass = 0.0;
-      for (int64_t v = 0; v < V; ++v) {
-        double r = prob(pr.t, v) - prob(pr.d, v);
-        if (r > 0.0) rmass += r;
-      }
-      t = gumbel_argmax(logw_residual, &pr, V, seed, (uint32_t)n, (uint32_t)b, round, &gap);
+      for (int64_t v = 0; v < V; ++v) rmass += weight_residual(&pr, v);
+      t = inverse_cdf_draw(weight_residual, &pr, V, Ud, &gap);
       if (t < 0) {
         /* Residual empty in floating point: sample p_n itself. */
         flag |= SVO_FLAG_RESIDUAL_FALLBACK;
-        t = gumbel_argmax(logw_scaled_logit, &rows[n], V, seed, (uint32_t)n, (uint32_t)b, round,
-                          &gap);
+        t = inverse_cdf_draw(weight_prob, &rows[n], V, Ud, &gap);
         if (t < 0) { t = 0; flag |= SVO_FLAG_ZERO_MASS; }
       }
     }
@@ -451,7 +471,7 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
         beta_out[(int64_t)b * gamma + i] = beta;
       }
     }
-    if (gumbel_gap) gumbel_gap[b] = gap;
+    if (draw_gap) draw_gap[b] = gap;
     if (resid_mass) resid_mass[b] = rmass;
     if (flags) flags[b] = flag;
   }

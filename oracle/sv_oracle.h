@@ -49,6 +49,11 @@ double svo_uniform(uint64_t seed, uint32_t tag, uint32_t pos, uint32_t b,
 void svo_uniform_row(uint64_t seed, uint32_t tag, uint32_t pos, uint32_t b, uint64_t round,
                      int64_t v0, int64_t n, double* out);
 
+/* Uniform in [0,1) of the target's own draw at position pos: counter
+ * (0, (1<<24)|pos, b, lo32(round)); U = k 2^-53 with
+ * k = (out[0] >> 11) * 2^32 + out[1]. */
+double svo_draw_uniform(uint64_t seed, uint32_t pos, uint32_t b, uint64_t round);
+
 /* Probability-level pieces of the accept/reject rule (double in, double out). */
 double svo_accept_mass(const double* p, const double* q, int64_t V, double* out_min);
 double svo_residual(const double* p, const double* q, int64_t V, double* out_resid);
@@ -59,7 +64,10 @@ double svo_softmax(const double* s, int64_t V, double* p);
 /* Full sampling verify.  Optional outputs may be NULL.
  *   p_at, q_at, ratio, u_acc : [B][gamma]  p(x~), q(x~), p/q, acceptance uniform
  *   beta                     : [B][gamma]  sum_v min(p_i, q_i)   (diagnostic)
- *   gumbel_gap               : [B]         top1 - top2 Gumbel key of the emitted draw
+ *   draw_gap                 : [B]         distance of U W from the nearer end of the
+ *                                          drawn token's cumulative interval, in
+ *                                          probability units (the inverse transform:
+ *                                          W the total weight, U the draw uniform)
  *   resid_mass               : [B]         sum_v max(0, p_n - q_n) (NaN if n == gamma)
  * Returns 0, or -1 on bad arguments. */
 int svo_spec_verify(const void* zt, const void* zd, const int32_t* xt,
@@ -68,7 +76,7 @@ int svo_spec_verify(const void* zt, const void* zd, const int32_t* xt,
                     uint64_t seed, uint64_t round,
                     int32_t* tokens, int32_t* counts,
                     double* p_at, double* q_at, double* ratio, double* u_acc,
-                    double* beta, double* gumbel_gap, double* resid_mass,
+                    double* beta, double* draw_gap, double* resid_mass,
                     uint8_t* flags);
 
 /* Same, for batch rows [b_begin, b_end) only (rows keep their global index b in
@@ -79,7 +87,7 @@ int svo_spec_verify_rows(const void* zt, const void* zd, const int32_t* xt,
                          uint64_t seed, uint64_t round,
                          int32_t* tokens, int32_t* counts,
                          double* p_at, double* q_at, double* ratio, double* u_acc,
-                         double* beta, double* gumbel_gap, double* resid_mass,
+                         double* beta, double* draw_gap, double* resid_mass,
                          uint8_t* flags, int b_begin, int b_end);
 
 /* Variants of the round.  lenience l ("Fast Inference from Transformers via
@@ -111,7 +119,7 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
                        uint64_t seed, uint64_t round,
                        int32_t* tokens, int32_t* counts,
                        double* p_at, double* q_at, double* ratio, double* u_acc,
-                       double* beta, double* gumbel_gap, double* resid_mass,
+                       double* beta, double* draw_gap, double* resid_mass,
                        uint8_t* flags, int b_begin, int b_end, const svo_options* opt);
 
 /* Greedy verify on raw target logits. */

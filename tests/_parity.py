@@ -4,9 +4,13 @@ Rules (the verify step's stated tolerances):
   * greedy outputs are compared bit for bit;
   * sampled tokens and counts are compared bit for bit, except at a near-tie of
     the decision where the two first differ: an acceptance test with
-    |u - p/q| < 1e-6, or a Gumbel draw whose top-2 keys are within 1e-6, both
-    measured on the oracle's double-precision values; near-ties are counted and
-    must stay under 1e-4 of all decisions;
+    |u - p/q| < 1e-6, or a draw whose U W lies within 4e-6 (probability units)
+    of an end of the drawn token's cumulative interval, both measured on the
+    oracle's double-precision values; near-ties are counted and must stay under
+    1e-4 of all decisions.  The draw bound: the GPU sums fp32 weights (about
+    3e-7 relative error each from exp2 and the scaled logit, 1e-7 from each
+    fp32 partial sum of at most 16 terms in order) into its cumulative sums, so
+    its interval ends move by at most about 1e-6 of the total;
   * p(x), q(x) and alpha agree within 1e-5 relative;
   * flags agree exactly;
   * with a nucleus (top-p) cut, a batch row whose oracle-reported nucleus gap is
@@ -15,6 +19,7 @@ Rules (the verify step's stated tolerances):
 import numpy as np
 
 NEAR_TIE = 1e-6
+NEAR_DRAW = 4e-6
 NEAR_TIE_RATE = 1e-4
 REL_TOL = 1e-5
 # a nucleus (top-p) cut whose top_p lies this close to a cumulative probability
@@ -48,7 +53,7 @@ def compare_sampling(gpu: dict, orc: dict, gamma: int, rows=None, check_pq=True)
                 margin = abs(orc["u"][b, j] - orc["ratio"][b, j])
                 is_near = bool(margin < NEAR_TIE)
             else:
-                is_near = bool(orc["gap"][b] < NEAR_TIE)
+                is_near = bool(orc["gap"][b] < NEAR_DRAW)
             if is_near:
                 near += 1
             else:
