@@ -271,12 +271,12 @@ def run_ours(args):
     # per-kernel events on a subset of the timed steps
     EVERY = 16
     n_ev = args.steps // EVERY + 1
-    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ev)]
     for es in evsets:  # materialise the underlying cudaEvent_t before taking handles
         for e in es:
             e.record(stream)
     torch.cuda.synchronize(dev)
-    evptrs = [(ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in es])
+    evptrs = [(ctypes.c_void_p * 3)(*[ctypes.c_void_p(e.cuda_event) for e in es])
               for es in evsets]
     assert all(e.cuda_event for es in evsets for e in es)
 
@@ -292,7 +292,7 @@ def run_ours(args):
         k = 0
         for i in range(args.steps):
             if i % EVERY == 0:
-                L.sv_set_timing_events(ctypes.cast(evptrs[k], ctypes.c_void_p), 4)
+                L.sv_set_timing_events(ctypes.cast(evptrs[k], ctypes.c_void_p), 3)
                 step(args.warmup + i)
                 L.sv_set_timing_events(None, 0)
                 k += 1
@@ -303,11 +303,10 @@ def run_ours(args):
     barrier(world)
     ms = start.elapsed_time(stop)
     ms = max_over_ranks(ms, world)
-    kern = {"k_sweep": [], "k_draw": [], "k_draw_merge": []}
+    kern = {"k_sweep": [], "k_draw": []}
     for es in evsets[:k]:
         kern["k_sweep"].append(es[0].elapsed_time(es[1]))
-        kern["k_draw"].append(es[1].elapsed_time(es[2]))  # includes the decision
-        kern["k_draw_merge"].append(es[2].elapsed_time(es[3]))
+        kern["k_draw"].append(es[1].elapsed_time(es[2]))  # the decision, the draw, the select
     kavg = {n: (sum(v) / len(v) if v else None) for n, v in kern.items()}
 
     rounds_per_s = world * args.steps / (ms / 1000.0)
@@ -391,7 +390,7 @@ def run_ours(args):
                          "frac": sweep_gbs / hbm, "frac_of_8TBs": sweep_gbs / 8000.0,
                          "traffic": SWEEP_TRAFFIC_BYTES, "algorithmic_bytes": sweep_bytes},
             "kernel_ms": kavg,
-            "gpu_launches": 3 * args.steps,  # k_sweep(_tma), k_draw, k_draw_merge
+            "gpu_launches": 2 * args.steps,  # k_sweep(_tma), k_draw
             "clocks": clk.summary(),
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -443,7 +442,7 @@ def measure_options(L, stream, sets, tokens, counts, flags, ws, lenience=1.0, to
     ms = a.elapsed_time(b) / reps
     out = {"workload": "sample_b64", "rounds_per_s": 1000.0 / ms, "ms_per_round": ms,
            "mean_accepted": acc["variant"], "mean_accepted_plain": acc["plain"],
-           "gpu_launches_per_round": 3 + (1 if top_k else 0) + (2 if top_p < 1.0 else 0)}
+           "gpu_launches_per_round": 2 + (1 if top_k else 0) + (2 if top_p < 1.0 else 0)}
     if lenience != 1.0:
         out["lenience"] = lenience
     if top_p < 1.0:
@@ -459,7 +458,7 @@ def _kernel_times(L, stream, call, nkern, reps, warm=3):
     """Average per-kernel ms of `call(i)` via the library's timing events, and
     the average ms of a whole call without events."""
     import torch
-    nev = max(4, nkern + 1)  # the library takes at least 4 events; a call marks nkern + 1
+    nev = max(3, nkern + 1)  # a call marks nkern + 1 events
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
     for e in ev:
         e.record(stream)

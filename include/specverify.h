@@ -19,11 +19,15 @@
  *   target argmax at the stop position.
  *
  * Randomness (no state): Philox4x32-10 (Salmon et al., SC'11), key = (lo32(seed),
- * hi32(seed)), counter = (c0, (tag<<24)|position, b, lo32(round)); tag 0 is the
- * acceptance uniform (c0 = 0, lane 0), tag 1 the Gumbel noise of vocabulary entry
- * v (c0 = v>>2, lane v&3); u = (2*(x>>9)+1)*2^-24 in (0,1).  Sampling is Gumbel-max
- * argmax_v(log w_v - log(-log u_v)) with ties to the lowest index.  Same inputs and
- * (seed, round) give the same outputs on any stream, launch shape or GPU.
+ * hi32(seed)), counter = (c0, (tag<<24)|position, b, lo32(round)).  Tag 0 is the
+ * acceptance uniform (c0 = 0, lane 0; u = (2*(x>>9)+1)*2^-24 in (0,1)).  Tag 1 at
+ * the draw position n (c0 = 0) gives the uniform of the target's own token,
+ * U = k 2^-53 in [0,1) with k = (x0>>11)*2^32 + x1, and the token is drawn by the
+ * inverse transform: the smallest v, in vocabulary order, whose cumulative weight
+ * exceeds U times the total weight (weights max(0, p_n - q_n), or p_n, formed
+ * and summed in fp32 and fp64 on the GPU: the interval ends are exact up to
+ * about 1e-6 of the total).  Same inputs and (seed, round) give the same outputs
+ * on any stream, launch shape or GPU.
  *
  * Conventions for every entry point:
  *   - All array arguments are DEVICE pointers, row-major and contiguous; the caller
@@ -281,11 +285,12 @@ int spec_lmhead_verify_drafted(const void* h_target, const void* W_target, int H
 
 /* Profiling aid (not thread-safe): when `events` is non-NULL, following calls
  * record events[0] on their stream before the first kernel and events[k] after
- * the k-th of their kernels: for spec_verify the softmax sweep, the draw (with
- * the decision at its start) and the draw merge (n >= 4); for
+ * the k-th of their kernels: for spec_verify the softmax sweep and the draw
+ * (with the decision at its start and the select at its end; n >= 3); for
  * spec_lmhead_verify the first GEMM pass, the decision, the recompute pass and
- * the merge (n >= 5).  NULL switches recording off.  The events are cudaEvent_t
- * created by the caller; they change no result. */
+ * the merge (n >= 5).  Only events[0..n-1] are recorded (n >= 1; at most 8).
+ * NULL switches recording off.  The events are cudaEvent_t created by the
+ * caller; they change no result. */
 int sv_set_timing_events(void* const* events, int n);
 
 /* Human-readable name of a status code. */

@@ -214,7 +214,7 @@ int spec_lmhead_draft(const void* h_draft, const void* W_draft, int Hd, int B, i
 }
 
 int sv_set_timing_events(void* const* events, int n) {
-  if (events && n < 4) return SV_ERR_ARG;
+  if (events && n < 1) return SV_ERR_ARG;
   sv::set_timing_events(events, n);
   return SV_OK;
 }

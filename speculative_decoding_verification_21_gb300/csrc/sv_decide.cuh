@@ -51,36 +51,65 @@ struct SweepCtx {
   uint8_t* out_flags;
   float inv_lenience;    // 1/l of the lenient comparison u <= p/(l q); 1: the exact round
   const float* thr;      // [B][R1] top-k thresholds (logits below have weight 0) or null
+  uint32_t* done;        // [B] arrival counters of the draw, zeroed by every sweep
 };
 
-// Row statistics of row r from its chunk partials (one warp, all loads of a
-// lane in flight together), kept by lane 0 and written to rowstat[r].
-__device__ __forceinline__ RowStat combine_row(const float2* pr, int nch, RowStat* out) {
-  const int lane = threadIdx.x & 31;
-  float m = -kInf, s = 0.0f;
-  int bits = 0;
-#pragma unroll 4
-  for (int j = lane; j < nch; j += 32) {
-    const float2 p = __ldcg(pr + j);
-    if (p.x != p.x) bits |= kRowNaN;
-    if (p.y < 0.0f) bits |= kRowTimeout;
-    if (p.x > m) {
-      s = (m == -kInf) ? 0.0f : s * exp2f(m - p.x);
-      m = p.x;
-    }
-    if (p.x > -kInf) s += p.y * exp2f(p.x - m);
+// Online (max, sum) of a lane's share of one row's chunk partials.
+struct RowAcc {
+  float m, s;
+  int bits;
+};
+__device__ __forceinline__ void row_acc_add(RowAcc& a, float2 p) {
+  if (p.x != p.x) a.bits |= kRowNaN;
+  if (p.y < 0.0f) a.bits |= kRowTimeout;
+  if (p.x > a.m) {
+    a.s = (a.m == -kInf) ? 0.0f : a.s * exp2f(a.m - p.x);
+    a.m = p.x;
   }
-  const float M = warp_max(m);
-  float sl = (m > -kInf) ? s * exp2f(m - M) : 0.0f;
+  if (p.x > -kInf) a.s += p.y * exp2f(p.x - a.m);
+}
+// The warp's combined statistics, kept by lane 0 and written to *out.
+__device__ __forceinline__ RowStat row_acc_finish(const RowAcc& a, RowStat* out) {
+  const int lane = threadIdx.x & 31;
+  const float M = warp_max(a.m);
+  float sl = (a.m > -kInf) ? a.s * exp2f(a.m - M) : 0.0f;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, o);
-  bits = __reduce_or_sync(0xffffffffu, bits);
+  const int bits = __reduce_or_sync(0xffffffffu, a.bits);
   RowStat rs;
   rs.mc = M;
   rs.bits = bits;
   rs.s = (bits & kRowNaN) ? CUDART_NAN : (double)sl;
   if (lane == 0 && out) *out = rs;
   return rs;
+}
+
+// Row statistics of row r from its chunk partials (one warp, all loads of a
+// lane in flight together), kept by lane 0 and written to rowstat[r].
+__device__ __forceinline__ RowStat combine_row(const float2* pr, int nch, RowStat* out) {
+  const int lane = threadIdx.x & 31;
+  RowAcc a{-kInf, 0.0f, 0};
+#pragma unroll 4
+  for (int j = lane; j < nch; j += 32) row_acc_add(a, __ldcg(pr + j));
+  return row_acc_finish(a, out);
+}
+
+// Two rows by one warp with the loads of both in flight together (p1 may be
+// null); each row's arithmetic is that of combine_row.
+__device__ __forceinline__ void combine_row2(const float2* p0, const float2* p1, int nch,
+                                             RowStat* out0, RowStat* out1, RowStat& r0,
+                                             RowStat& r1) {
+  const int lane = threadIdx.x & 31;
+  RowAcc a0{-kInf, 0.0f, 0}, a1{-kInf, 0.0f, 0};
+#pragma unroll 4
+  for (int j = lane; j < nch; j += 32) {
+    const float2 x0 = __ldcg(p0 + j);
+    const float2 x1 = p1 ? __ldcg(p1 + j) : make_float2(-kInf, 0.0f);
+    row_acc_add(a0, x0);
+    row_acc_add(a1, x1);
+  }
+  r0 = row_acc_finish(a0, out0);
+  r1 = row_acc_finish(a1, p1 ? out1 : nullptr);
 }
 
 // log2 of the unnormalised probability, e = z c - mc, carried in two floats:
@@ -98,10 +127,10 @@ __device__ __forceinline__ Exp2 exponent_at(float z, float c, float mc) {
   return Exp2{a, err + pl};
 }
 // p(x) from its exponent and the row sum (0 for a -inf logit or an empty row).
-__device__ __forceinline__ float prob_from(float z, const Exp2& e, const RowStat& r) {
-  if (!(r.s > 0.0)) return (r.s == 0.0) ? 0.0f : (float)r.s;  // NaN stays NaN
+__device__ __forceinline__ float prob_from(float z, const Exp2& e, float s) {
+  if (!(s > 0.0f)) return (s == 0.0f) ? 0.0f : s;  // NaN stays NaN
   if (z == -kInf) return 0.0f;
-  return exp2f(e.hi) * fmaf(e.lo, kLn2, 1.0f) / (float)r.s;
+  return exp2f(e.hi) * fmaf(e.lo, kLn2, 1.0f) / s;
 }
 
 // The decision for batch row b (one warp): accept test, prefix, draw set-up.
@@ -130,11 +159,11 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
   for (int k = lane; k < R1; k += 32) {
     const RowStat v = srs[k];
     if (v.mc == -kInf) fl |= SV_FLAG_ZERO_MASS;
-    if (!(v.s < CUDART_INF) || v.mc == kInf || !temperature_ok(T)) fl |= SV_FLAG_NONFINITE;
+    if (!((float)v.s < kInf) || v.mc == kInf || !temperature_ok(T)) fl |= SV_FLAG_NONFINITE;
     if (v.bits & kRowTimeout) fl |= SV_FLAG_TIMEOUT | SV_FLAG_NONFINITE;
   }
   bool accept = false, bad = false, qzero = false;
-  double P = 0.0, Q = 0.0;
+  float P = 0.0f, Q = 0.0f;
   int32_t xi = 0;
   if (lane < gamma) {
     const DraftAt da = sda[lane];
@@ -145,29 +174,31 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
       const float zx = da.zt;
       const float zy = da.zd;
       const RowStat rt = srs[lane], rd = srs[gamma + 1 + lane];
+      // the row sums are fp32 values (kept in double fields): compare and divide in fp32
+      const float st_ = (float)rt.s, sd_ = (float)rd.s;
       const Exp2 ep = exponent_at(zx, c, rt.mc), eq = exponent_at(zy, c, rd.mc);
-      P = prob_from(zx, ep, rt);
-      Q = prob_from(zy, eq, rd);
+      P = prob_from(zx, ep, st_);
+      Q = prob_from(zy, eq, sd_);
       // p/q from the exponent difference (no underflow of p and q themselves);
       // q = 0 with p > 0 gives inf (accept), p = q = 0 gives NaN (reject)
-      const bool p0 = !(rt.s > 0.0) || zx == -kInf, q0 = !(rd.s > 0.0) || zy == -kInf;
-      if (rt.s != rt.s || rd.s != rd.s) {
+      const bool p0 = !(st_ > 0.0f) || zx == -kInf, q0 = !(sd_ > 0.0f) || zy == -kInf;
+      if (st_ != st_ || sd_ != sd_) {
         ratio = CUDART_NAN_F;
       } else if (p0 || q0) {
         ratio = p0 ? (q0 ? CUDART_NAN_F : 0.0f) : kInf;
       } else {
         const float d = (ep.hi - eq.hi) + (ep.lo - eq.lo);
-        ratio = exp2f(d) * (float)(rd.s / rt.s) * x.inv_lenience;
+        ratio = exp2f(d) * __fdiv_rn(sd_, st_) * x.inv_lenience;
       }
-      qzero = q0 || !(rd.s == rd.s);
+      qzero = q0 || !(sd_ == sd_);
     } else {
       qzero = true;
     }
     const uint4 rnd = philox4x32_10(sv_counter(0u, 0u, (uint32_t)lane, (uint32_t)b, x.round),
                                     (uint32_t)x.seed, (uint32_t)(x.seed >> 32));
     accept = (sv_u01(rnd.x) <= ratio);
-    if (emit && x.out_p) x.out_p[(int64_t)b * gamma + lane] = (float)P;
-    if (emit && x.out_q) x.out_q[(int64_t)b * gamma + lane] = (float)Q;
+    if (emit && x.out_p) x.out_p[(int64_t)b * gamma + lane] = P;
+    if (emit && x.out_q) x.out_q[(int64_t)b * gamma + lane] = Q;
   }
   const unsigned rej = ~__ballot_sync(0xffffffffu, accept);
   const int n = (rej == 0u) ? 32 : min(__ffs((int)rej) - 1, gamma);

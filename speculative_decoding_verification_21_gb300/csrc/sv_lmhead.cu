@@ -25,14 +25,15 @@
 //   k_lm<2>      the same GEMM for the compact rows only (tiles in reverse
 //                order), target and draft blocks side by side in tensor
 //                memory.  The compact rows are copied into the row tile twice
-//                (B <= 64) so that two lane quadrants share the key work:
-//                top-2 of the residual max(0, p_n - q_n) and of p_n.
-//   k_lm_merge   one CTA per compact row: merge, re-decide near ties in double,
-//                fall back to p_n for an empty residual, emit.
+//                (B <= 64) so that two lane quadrants share the epilogue: per
+//                16-entry chunk the fp32 sums of the draw weights (residual
+//                max(0, p_n - q_n) and p_n), and the chunk's logits.
+//   k_lm_merge   one CTA per compact row: the token by the inverse transform
+//                (sv_draw.cuh) from the chunk sums and the stored logits of
+//                the one chunk it lands in; p_n for an empty residual; emit.
 //
-// Keys are log2-domain Gumbel-max keys, y_v - log2(-log2 u_v) with y = z / T *
-// log2 e: the same argmax as log w_v + g_v of the definition, with no underflow
-// of the weights.
+// Draft sampling (spec_lmhead_draft) is a third use of the GEMM (k_lm<3>) with
+// Gumbel-max keys y_v - log2(-log2 u_v), y = z / T * log2 e, on Philox tag 2.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -43,6 +44,7 @@
 #include "specverify.h"
 #include "sv_decide.cuh"
 #include "sv_device.cuh"
+#include "sv_draw.cuh"
 #include "sv_launch.h"
 #include "sv_plan.h"
 #include "sv_tma.cuh"
@@ -88,7 +90,18 @@ struct LmArgs {
   uint64_t seed, round;
   float2* part;        // [B*R1][nslot][2] (max, sum) per row, CTA and column half
   float* zat;          // [B*R1] logit at the row's draft token
-  LmCand* res;         // [B][nslot][4] residual top-2, then p_n top-2, per compact row
+  LmCand* res;         // pass 3: [B][nslot][2] top-2 Gumbel keys per batch row and CTA
+  int nchunk;          // pass 2: 16-entry chunks per row, ceil(V / 16)
+  float* csum_r;       // pass 2: [B][nchunk] residual weight sums per compact row
+  float* csum_p;       // pass 2: [B][nchunk] p_n weight sums per compact row
+  float* lz_t;         // pass 2: [B][V] target logits of the compact rows
+  float* lz_d;         // pass 2: [B][V] draft logits of the compact rows (residual rows)
+  uint64_t* tsum_r;    // pass 2: [B][nvt] residual weight per vocabulary tile (fixed point)
+  uint64_t* tsum_p;    // pass 2: [B][nvt] p_n weight per vocabulary tile (zeroed by finish)
+  uint64_t* gsum_r;    // pass 2: [B][ngrp] the same per group of 32 tiles
+  uint64_t* gsum_p;
+  int ngrp;            // ceil(nvt / 32)
+  int fsh;             // fixed-point scale of the draw sums
   DrawState* state;    // [B]
   int* slot_b;         // [B] batch row of each compact row
   uint32_t* ctl;       // count, pass-1 error, pass-2 error
@@ -177,11 +190,10 @@ __device__ __forceinline__ bool lm_wait_warp(uint64_t* bar, uint32_t parity,
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// -log2(-log2 u) noise of entry v at Philox position pos (tag 1 for the
-// verify's draws, tag 2 for draft sampling), and its double twin -ln(-ln u)
-// for the re-decision.
+// The double-precision Gumbel noise -ln(-ln u) of entry v at Philox position
+// pos (tag 2: draft sampling), for the re-decision of a near tie.
 __device__ __forceinline__ double gumbel_f64(int64_t v, int pos, int b, uint64_t seed,
-                                             uint64_t round, uint32_t tag = 1u) {
+                                             uint64_t round, uint32_t tag) {
   const uint4 rnd = philox4x32_10(sv_counter((uint32_t)(v >> 2), tag, (uint32_t)pos, (uint32_t)b, round),
                                   (uint32_t)seed, (uint32_t)(seed >> 32));
   const uint32_t lanes[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
@@ -470,24 +482,24 @@ __device__ __forceinline__ P2Slice pass2_slice(const LmArgs& a, int quad, int ha
 }
 
 // Pass-2 epilogue of one job (compact rows; target at column 0, draft at 128):
-// the residual top-2 `tr` and the p_n top-2 `tp` of this thread's row over its
-// column slice, carried over the CTA's tiles.
+// for every 16-column chunk of this thread's row and column slice, the fp32
+// sums (added in order) of the draw weights -- p_n, and for a residual row
+// max(0, p_n - q_n) -- and the logits themselves, from which the merge
+// recomputes the weights of the one chunk it walks (the same bits).  Each
+// chunk sum is also added, in fixed point, to its vocabulary tile's total and
+// to its group's (32 tiles) total (integer atomics: exact in any order).
 __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t tacc, int quad,
-                                               int half, int rows, const PhiloxKeys& pk,
-                                               Cand2* tr, Cand2* tp) {
+                                               int half, int rows) {
   const int lane = threadIdx.x & 31;
   const int V = a.V;
   const P2Slice sl = pass2_slice(a, quad, half);
   if (sl.copy >= a.rep || sl.row0 >= rows) return;  // warp-uniform
   const int r = sl.row0 + lane;
   const bool rv = r < rows;
-  int b = 0;
   DrawState st{};
-  if (rv) {
-    b = a.slot_b[r];
-    st = a.state[b];
-  }
+  if (rv) st = a.state[a.slot_b[r]];
   const bool resid = st.mode == kDrawResidual;
+  const float kd = __fsub_rn(st.K, st.mct);
   const uint32_t ta = tacc + ((uint32_t)(32 * quad) << 16) + (uint32_t)sl.col0;
 #pragma unroll 1
   for (int c16 = 0; c16 < sl.ncol; c16 += 16) {
@@ -496,70 +508,40 @@ __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t 
     tmem_ld16_async(ta + (uint32_t)c16, rt);
     tmem_ld16_async(ta + (uint32_t)(kLmTileN + c16), rd);
     tmem_wait_ld();
-    const int vb = t * kLmTileN + sl.col0 + c16;
+    const int vb = t * kLmTileN + sl.col0 + c16;  // a multiple of 16
     if (rv && vb < V) {
+      float zt[16], zd[16];
+      float sp = 0.0f, sr = 0.0f;
 #pragma unroll
-      for (int g4 = 0; g4 < 4; ++g4) {
-        const int v = vb + 4 * g4;
-        if (v >= V) break;
-        const uint4 rnd = philox_rk(
-            sv_counter((uint32_t)(v >> 2), 1u, (uint32_t)st.pos, (uint32_t)b, a.round), pk);
-        const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+      for (int e = 0; e < 16; ++e) {
+        const bool in = vb + e < V;  // columns past V hold no logit
+        zt[e] = in ? __uint_as_float(rt[e]) : -kInf;
+        zd[e] = in ? __uint_as_float(rd[e]) : -kInf;
+        sp = __fadd_rn(sp, draw_weight<false, false>(zt[e], 0.0f, st, kd));
+        if (resid) sr = __fadd_rn(sr, draw_weight<true, false>(zt[e], zd[e], st, kd));
+      }
+      const int64_t ci = (int64_t)r * a.nchunk + (vb >> 4);
+      const int64_t ti = (int64_t)r * a.nvt + t, gi = (int64_t)r * a.ngrp + (t >> 5);
+      a.csum_p[ci] = sp;
+      const uint64_t fp = to_fix(sp, a.fsh);
+      atomicAdd(reinterpret_cast<unsigned long long*>(a.tsum_p + ti), fp);
+      atomicAdd(reinterpret_cast<unsigned long long*>(a.gsum_p + gi), fp);
+      if (resid) {
+        a.csum_r[ci] = sr;
+        const uint64_t fr = to_fix(sr, a.fsh);
+        atomicAdd(reinterpret_cast<unsigned long long*>(a.tsum_r + ti), fr);
+        atomicAdd(reinterpret_cast<unsigned long long*>(a.gsum_r + gi), fr);
+      }
+      float4* pt = reinterpret_cast<float4*>(a.lz_t + (int64_t)r * V + vb);  // V % 8 == 0
+      float4* pd = reinterpret_cast<float4*>(a.lz_d + (int64_t)r * V + vb);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float zt = __uint_as_float(rt[4 * g4 + e]);
-          const float zd = __uint_as_float(rd[4 * g4 + e]);
-          const float lE = __log2f(neglog2_u(rr[e]));
-          const float kp = fmaf(zt, st.c, -st.mct) - lE;
-          if (zt > -kInf) cand_insert(tp[e & 1], LmCand{kp, v + e, zt, zd});
-          if (resid) {
-            // x = log2(q/p); p > q iff x < 0; weight p - q = p (1 - 2^x)
-            const float xx = fmaf(zd - zt, st.c, st.K);
-            if (xx < 0.0f) {
-              const float y = xx * kLn2;
-              const float ser =
-                  -y * fmaf(y, fmaf(y, fmaf(y, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
-              const float om = (xx > -0.125f) ? ser : 1.0f - ex2(xx);
-              cand_insert(tr[e & 1], LmCand{kp + __log2f(om), v + e, zt, zd});
-            }
-          }
+      for (int q = 0; q < 4; ++q) {
+        if (vb + 4 * q < V) {
+          pt[q] = make_float4(zt[4 * q], zt[4 * q + 1], zt[4 * q + 2], zt[4 * q + 3]);
+          if (resid) pd[q] = make_float4(zd[4 * q], zd[4 * q + 1], zd[4 * q + 2], zd[4 * q + 3]);
         }
       }
     }
-  }
-}
-
-// One candidate set per compact row and CTA: the slices of a row are merged
-// through shared memory (the ring, idle once the last job is drained) by the
-// 256 epilogue threads, then written to res[(row * nslot + cta) * 4 ..].
-__device__ __forceinline__ void pass2_flush(const LmArgs& a, int quad, int half, int rows,
-                                            const Cand2* tr, const Cand2* tp, LmCand* sc) {
-  const int nsl = 2 * a.rep;
-  const P2Slice sl = pass2_slice(a, quad, half);
-  const int r = sl.row0 + (threadIdx.x & 31);
-  if (sl.copy < a.rep && r < rows) {
-    const Cand2 r2 = merge2(tr), p2 = merge2(tp);
-    LmCand* o = sc + ((size_t)r * nsl + sl.copy * 2 + half) * 4;
-    o[0] = r2.a;
-    o[1] = r2.b;
-    o[2] = p2.a;
-    o[3] = p2.b;
-  }
-  asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-  for (int rr = (int)threadIdx.x - 3 * 32; rr < rows; rr += 32 * kEpiWarps) {
-    Cand2 xr{cand_empty(), cand_empty()}, xp{cand_empty(), cand_empty()};
-    for (int j = 0; j < nsl; ++j) {
-      const LmCand* q = sc + ((size_t)rr * nsl + j) * 4;
-      cand_insert(xr, q[0]);
-      cand_insert(xr, q[1]);
-      cand_insert(xp, q[2]);
-      cand_insert(xp, q[3]);
-    }
-    LmCand* o = a.res + ((int64_t)rr * a.nslot + blockIdx.x) * 4;
-    o[0] = xr.a;
-    o[1] = xr.b;
-    o[2] = xp.a;
-    o[3] = xp.b;
   }
 }
 
@@ -847,13 +829,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const PhiloxKeys pk = philox_keys(a.seed);
     Pass1Carry cy;
     Pass3Carry cy3;
-    Cand2 tr[2], tp[2];
     if (PASS == 1 || PASS == 4) {
       carry_init(cy);
-    } else if (PASS == 2) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) tr[j] = tp[j] = Cand2{cand_empty(), cand_empty()};
-    } else {
+    } else if (PASS == 3) {
       cy3.mc = -kInf;
       cy3.s = 0.0f;
       cy3.t[0] = cy3.t[1] = Cand2{cand_empty(), cand_empty()};
@@ -878,7 +856,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           else
             epilogue_pass1<1>(a, tv, tacc, quad, half, cy);
         } else if (PASS == 2) {
-          epilogue_pass2(a, tv, tacc, quad, half, rows2, pk, tr, tp);
+          epilogue_pass2(a, tv, tacc, quad, half, rows2);
         } else {
           epilogue_pass3(a, tv, tacc, quad, half, pk, cy3);
         }
@@ -893,9 +871,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       pass1_flush<2>(a, cy, quad, half);
     else if (PASS == 4)
       pass1_flush<1>(a, cy, quad, half);
-    else if (PASS == 2)
-      pass2_flush(a, quad, half, rows2, tr, tp, reinterpret_cast<LmCand*>(hring));
-    else
+    else if (PASS == 3)
       pass3_flush(a, quad, half, cy3, hring);
   }
 
@@ -981,6 +957,14 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
   __syncthreads();
   const int slot = s_slot;
   const int n = st.pos;
+  for (int j = threadIdx.x; j < a.nvt; j += blockDim.x) {
+    a.tsum_r[(int64_t)slot * a.nvt + j] = 0ull;
+    a.tsum_p[(int64_t)slot * a.nvt + j] = 0ull;
+  }
+  for (int j = threadIdx.x; j < a.ngrp; j += blockDim.x) {
+    a.gsum_r[(int64_t)slot * a.ngrp + j] = 0ull;
+    a.gsum_p[(int64_t)slot * a.ngrp + j] = 0ull;
+  }
   const uint4* srct = reinterpret_cast<const uint4*>(a.h_t + ((int64_t)b * (gamma + 1) + n) * a.Ht);
   uint4* dt = reinterpret_cast<uint4*>(a.c_t + (int64_t)slot * a.Ht);
   uint4* dd = reinterpret_cast<uint4*>(a.c_d + (int64_t)slot * a.Hd);
@@ -995,50 +979,76 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// k_lm_merge: one CTA per compact row.
+// k_lm_merge: one warp per compact row.  The token by the inverse transform
+// from the pass-2 sums: the group of 32 vocabulary tiles holding t = floor(U W)
+// (fixed point), the tile, the 16-entry chunk, then the entry from the stored
+// logits; the residual's fallback to p_n when it has no positive weight.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_lm_merge(LmArgs a) {
+__global__ void __launch_bounds__(32) k_lm_merge(LmArgs a) {
   const int slot = blockIdx.x;
-  __shared__ Cand2 scand[32];
+  const int lane = threadIdx.x & 31;
   pdl_wait();
   const int rows = (int)*reinterpret_cast<volatile uint32_t*>(a.ctl);
   if (slot >= rows) return;
   const bool err = *reinterpret_cast<volatile uint32_t*>(a.ctl + 2) != 0u;
   const int b = a.slot_b[slot];
   const DrawState st = a.state[b];
-  const bool resid = st.mode == kDrawResidual;
-  const LmCand* rp = a.res + (int64_t)slot * a.nslot * 4;
-  Cand2 tr{cand_empty(), cand_empty()}, tp{cand_empty(), cand_empty()};
-  for (int j = threadIdx.x; j < a.nslot; j += blockDim.x) {
-    cand_insert(tr, rp[4 * j]);
-    cand_insert(tr, rp[4 * j + 1]);
-    cand_insert(tp, rp[4 * j + 2]);
-    cand_insert(tp, rp[4 * j + 3]);
-  }
-  tr = block_cand2(tr, scand);
-  __syncthreads();
-  tp = block_cand2(tp, scand);
-  if (threadIdx.x != 0) return;
+  const int V = a.V;
   int fl = st.flags;
   int tk = -1;
-  const double invT = (double)st.invT, c = (double)st.c;
-  auto key_p = [&](const LmCand& q) {
-    return (double)q.zt * invT + gumbel_f64(q.idx, st.pos, b, a.seed, a.round);
-  };
   if (err) {
     fl |= SV_FLAG_TIMEOUT | SV_FLAG_NONFINITE;
-  } else if (resid && tr.a.idx >= 0) {
-    tk = redecide(tr, [&](const LmCand& q) {
-      const double P = exp2((double)q.zt * c - (double)st.mct) / st.st;
-      const double Q = exp2((double)q.zd * c - (double)st.mcd) / st.sd;
-      const double r = P - Q;
-      return (r > 0.0) ? log(r) + gumbel_f64(q.idx, st.pos, b, a.seed, a.round) : -CUDART_INF;
-    });
   } else {
-    if (resid) fl |= SV_FLAG_RESIDUAL_FALLBACK;
-    tk = redecide(tp, key_p);
+    const uint64_t k53 = draw_uniform53(a.seed, (uint32_t)st.pos, (uint32_t)b, a.round);
+    bool resid = st.mode == kDrawResidual;
+    const int64_t go = (int64_t)slot * a.ngrp;
+    uint64_t W = warp_total((resid ? a.gsum_r : a.gsum_p) + go, a.ngrp);
+    if (resid && W == 0) {
+      // the residual had no positive entry in floating point: draw from p_n itself
+      fl |= SV_FLAG_RESIDUAL_FALLBACK;
+      resid = false;
+      W = warp_total(a.gsum_p + go, a.ngrp);
+    }
+    if (W > 0) {
+      const uint64_t t = scale_fix(k53, W);  // < W
+      uint64_t base = 0;
+      const int g = warp_find<2>((resid ? a.gsum_r : a.gsum_p) + go, a.ngrp, t, 0ull, &base);
+      const int t0 = 32 * g;
+      const int tl = t0 + warp_find<1>((resid ? a.tsum_r : a.tsum_p) + (int64_t)slot * a.nvt + t0,
+                                       min(32, a.nvt - t0), t, base, &base);
+      // the chunk of the tile: its fixed-point sums add up to the tile's
+      const float* cs = (resid ? a.csum_r : a.csum_p) + (int64_t)slot * a.nchunk;
+      const int c0 = tl * (kLmTileN / 16), nc = min(a.nchunk - c0, kLmTileN / 16);
+      const uint64_t x = (lane < nc) ? to_fix(__ldcg(cs + c0 + lane), a.fsh) : 0ull;
+      uint64_t P = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, P, o);
+        if (lane >= o) P += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, base + P > t);
+      const int c = __ffs((int)hit) - 1;
+      if (lane == c) {
+        const int vb = (c0 + c) * 16;
+        const float* zt = a.lz_t + (int64_t)slot * V + vb;
+        const float* zd = a.lz_d + (int64_t)slot * V + vb;
+        const float kd = __fsub_rn(st.K, st.mct);
+        float w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const bool in = vb + e < V;
+          const float zv = in ? __ldcg(zt + e) : -kInf;
+          w[e] = resid ? draw_weight<true, false>(zv, in ? __ldcg(zd + e) : -kInf, st, kd)
+                       : draw_weight<false, false>(zv, 0.0f, st, kd);
+        }
+        const int e = pick_in_run<16>(w, 0ull, t - (base + P - x), a.fsh);
+        tk = e >= 0 ? vb + e : -1;
+      }
+      tk = __shfl_sync(0xffffffffu, tk, c < 0 ? 0 : c);
+    }
   }
-  if (tk < 0 || tk >= a.V) {
+  if (lane != 0) return;
+  if (tk < 0 || tk >= V) {
     tk = 0;
     if (!err) fl |= SV_FLAG_ZERO_MASS;
   }
@@ -1253,7 +1263,17 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   a.round = round;
   a.part = reinterpret_cast<float2*>(ws + pl.off_part);
   a.zat = reinterpret_cast<float*>(ws + pl.off_zat);
-  a.res = reinterpret_cast<LmCand*>(ws + pl.off_res);
+  a.nchunk = (int)ceil_div(V, 16);
+  a.csum_r = reinterpret_cast<float*>(ws + pl.off_csr);
+  a.csum_p = reinterpret_cast<float*>(ws + pl.off_csp);
+  a.lz_t = reinterpret_cast<float*>(ws + pl.off_lzt);
+  a.lz_d = reinterpret_cast<float*>(ws + pl.off_lzd);
+  a.tsum_r = reinterpret_cast<uint64_t*>(ws + pl.off_tsr);
+  a.tsum_p = reinterpret_cast<uint64_t*>(ws + pl.off_tsp);
+  a.ngrp = (pl.nvt + 31) / 32;
+  a.gsum_r = reinterpret_cast<uint64_t*>(ws + pl.off_gsr);
+  a.gsum_p = reinterpret_cast<uint64_t*>(ws + pl.off_gsp);
+  a.fsh = fix_shift(V);
   a.state = reinterpret_cast<DrawState*>(ws + pl.off_state);
   a.slot_b = reinterpret_cast<int*>(ws + pl.off_slot);
   a.ctl = reinterpret_cast<uint32_t*>(ws + pl.off_ctl);
@@ -1316,7 +1336,7 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   e = launch_pdl(k_lm<2>, dim3(grid), dim3(kLmThreads), smem2, stream, cT, WT, cD, WD, a2);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   mark(3, stream);
-  e = launch_pdl(k_lm_merge, dim3((unsigned)B), dim3(256), 0, stream, a);
+  e = launch_pdl(k_lm_merge, dim3((unsigned)B), dim3(32), 0, stream, a);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   mark(4, stream);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;

@@ -72,9 +72,10 @@ struct SamplePlan {
   int R1 = 0;          // logit rows per batch row, 2*gamma+1
   int nsplit1 = 0;     // 8192-logit chunks per row (generic sweep, overlap pass)
   int nsplit3 = 0;     // most CTAs per batch row in the draw pass
-  // counters: [B] overlap CTAs (zeroed by the first draw CTA of each batch row)
+  // counters: [B] overlap CTAs (zeroed by the first draw CTA of each batch row),
+  // then [B] draw CTAs that finished their segment sums (zeroed by the sweep)
   size_t off_cnt = 0, cnt_bytes = 0, off_part1 = 0, off_rowstat = 0, off_state = 0,
-         off_part3 = 0, off_alpha = 0, off_thr = 0, total = 0;
+         off_segsum = 0, off_ctot = 0, off_alpha = 0, off_thr = 0, total = 0;
 };
 
 inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
@@ -86,12 +87,14 @@ inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
   // per-(row, chunk) partials: enough for the smaller bulk-copy chunks of fp32
   const int64_t nch_max = ceil_div(V, tma_chunk_elems(0));
   size_t o = 0;
-  p.cnt_bytes = sizeof(uint32_t) * (size_t)B;
+  p.cnt_bytes = 2 * sizeof(uint32_t) * (size_t)B;
   p.off_cnt = o;      o = align_up(o + p.cnt_bytes);
   p.off_rowstat = o;  o = align_up(o + sizeof(RowStat) * (size_t)B * p.R1);
   p.off_part1 = o;    o = align_up(o + 8 * (size_t)B * p.R1 * (size_t)nch_max);
   p.off_state = o;    o = align_up(o + sizeof(DrawState) * (size_t)B);
-  p.off_part3 = o;    o = align_up(o + 16 * (size_t)B * p.nsplit3);
+  // draw: one fixed-point weight sum per 256-entry segment of the row drawn from
+  p.off_segsum = o;   o = align_up(o + sizeof(uint64_t) * (size_t)B * (size_t)ceil_div(V, 256));
+  p.off_ctot = o;     o = align_up(o + sizeof(uint64_t) * (size_t)B * p.nsplit3);  // per draw CTA
   p.off_alpha = o;    o = align_up(o + sizeof(float) * (size_t)B * gamma * p.nsplit1);
   p.off_thr = o;      o = align_up(o + sizeof(float) * (size_t)B * p.R1);  // top-k thresholds
   p.total = o;
@@ -134,7 +137,8 @@ struct LmPlan {
   int nvt = 0;  // vocabulary tiles
   // ctl: [0] compact-row count, [1] pass-1 error, [2] pass-2 error (zeroed per call)
   size_t off_ctl = 0, off_part = 0, off_zat = 0, off_state = 0, off_slot = 0,
-         off_res = 0, off_ct = 0, off_cd = 0, total = 0;
+         off_csr = 0, off_csp = 0, off_lzt = 0, off_lzd = 0, off_tsr = 0, off_tsp = 0,
+         off_gsr = 0, off_gsp = 0, off_ct = 0, off_cd = 0, total = 0;
 };
 
 inline LmPlan make_lm_plan(int B, int gamma, int64_t V) {
@@ -151,7 +155,16 @@ inline LmPlan make_lm_plan(int B, int gamma, int64_t V) {
   p.off_zat = o;    o = align_up(o + sizeof(float) * rows);
   p.off_state = o;  o = align_up(o + sizeof(DrawState) * (size_t)B);
   p.off_slot = o;   o = align_up(o + sizeof(int) * (size_t)B);
-  p.off_res = o;    o = align_up(o + 4 * sizeof(LmCand) * (size_t)B * p.nvt);
+  // the draw: weight sums per 16-entry chunk and the logits of each compact row
+  const size_t nchunk = (size_t)ceil_div(V, 16);
+  p.off_csr = o;    o = align_up(o + sizeof(float) * (size_t)B * nchunk);
+  p.off_csp = o;    o = align_up(o + sizeof(float) * (size_t)B * nchunk);
+  p.off_lzt = o;    o = align_up(o + sizeof(float) * (size_t)B * (size_t)V);
+  p.off_lzd = o;    o = align_up(o + sizeof(float) * (size_t)B * (size_t)V);
+  p.off_tsr = o;    o = align_up(o + sizeof(uint64_t) * (size_t)B * p.nvt);
+  p.off_tsp = o;    o = align_up(o + sizeof(uint64_t) * (size_t)B * p.nvt);
+  p.off_gsr = o;    o = align_up(o + sizeof(uint64_t) * (size_t)B * ((p.nvt + 31) / 32));
+  p.off_gsp = o;    o = align_up(o + sizeof(uint64_t) * (size_t)B * ((p.nvt + 31) / 32));
   p.off_ct = o;     o = align_up(o + 2 * (size_t)B * kLmMaxHidden);
   p.off_cd = o;     o = align_up(o + 2 * (size_t)B * kLmMaxHidden);
   p.total = o;

@@ -3,7 +3,7 @@
 // One round for B independent batch rows, after Algorithm 1 of "Fast Inference
 // from Transformers via Speculative Decoding" (section "The loop: draft, verify
 // in one pass, keep a prefix") and the course notes "Speculative Decoding"
-// ("The algorithm").  Three kernels per call (four with the optional overlap),
+// ("The algorithm").  Two kernels per call (three with the optional overlap),
 // chained by programmatic dependent launch:
 //
 //   sweep     online softmax statistics of every chunk of all 2*gamma+1 logit
@@ -13,17 +13,15 @@
 //             across warps in batch-row order, through a 2-stage bulk-copy (TMA)
 //             pipeline in shared memory.  k_sweep (any shape): one CTA per
 //             8192-logit chunk with 16-byte vector loads.
-//   k_draw    one CTA per (batch row, 8192 entries).  Each CTA first takes
-//             its batch row's decision from the chunk partials: the row
-//             statistics, p(x_i), q(x_i), u_i, accept iff u_i <= p/q, first
-//             rejection by a warp ballot (the first CTA of the batch row writes
-//             the prefix and the draw set-up).  Then the target's own token --
-//             bonus row p_gamma or residual max(0, p_n - q_n) -- as a Gumbel-max
-//             in the exponential-race form argmax w_v / E_v (E_v = -log2 u_v,
-//             the same argmax as log w_v + g_v), keeping the CTA's top-2 keys;
-//   k_draw_merge  one CTA per batch row merges them and, when the best two are
-//             within 2^-10, re-decides between them in double with the
-//             oracle-level definition.
+//   k_draw    one CTA per (batch row, slice of at least 8192 entries).  Each
+//             CTA first takes its batch row's decision from the chunk partials:
+//             the row statistics, p(x_i), q(x_i), u_i, accept iff u_i <= p/q,
+//             first rejection by a warp ballot (the first CTA of the batch row
+//             writes the prefix and the draw set-up).  Then the target's own
+//             token -- bonus row p_gamma or residual max(0, p_n - q_n) -- by the
+//             inverse transform: each CTA sums the weights of its 256-entry
+//             segments, and the CTA of the batch row that finishes last finds
+//             the entry whose cumulative interval holds U W (sv_draw.cuh).
 //   k_alpha   optional overlap sum_v min(p_i, q_i) ("The acceptance rate is the
 //             overlap of p and q").
 #include <cuda_runtime.h>
@@ -78,9 +76,17 @@ __device__ __forceinline__ void for_each_in_chunk(const char* row, int64_t lo, i
   for (int64_t v = a1 + tid; v < hi; v += blockDim.x) f_one(v, load_logit<DT>(row, v));
 }
 
+// The draw's per-batch-row arrival counters start at 0 in every call; the draw
+// touches them only after this grid has completed.
+__device__ __forceinline__ void zero_draw_counters(const SweepCtx& x) {
+  if (blockIdx.x == 0 && x.done)
+    for (int i = threadIdx.x; i < x.B; i += blockDim.x) x.done[i] = 0u;
+}
+
 template <int DT, bool TOPK>
 __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
   pdl_launch_dependents();
+  zero_draw_counters(x);
   const int R1 = 2 * x.gamma + 1;
   const int64_t item = blockIdx.x;  // (row, chunk) flattened, rows in batch-row order
   const int64_t r = item / x.nch;
@@ -141,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
 template <int DT, bool TOPK>
 __global__ void __launch_bounds__(kSweepWarps * 32, 3) k_sweep_tma(SweepCtx x) {
   pdl_launch_dependents();  // the draw kernel may be scheduled now; it waits for us
+  zero_draw_counters(x);
   constexpr int kBytes = (DT == SV_F32) ? 4 : 2;
   constexpr int CH = kSweepChunkBytes / kBytes;  // logits per chunk
   extern __shared__ __align__(128) unsigned char smem[];
@@ -682,17 +689,19 @@ __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int 
 // --------------------------------------------------------------------------
 // Draw of the target's own token.
 // --------------------------------------------------------------------------
-// One CTA per (batch row, gpc 4-entry groups).  Every CTA of a batch row first
-// takes the batch row's decision itself from the sweep's partials: one warp
-// per logit row combines its partials, then one warp runs the accept test
-// (the same arithmetic on the same numbers in every CTA, so all agree).  The
-// first CTA of the batch row also writes the row statistics, the accepted
-// prefix, p, q, the count and the draw state.  Then the CTA's top-2 keys of the
-// draw go to its slot; the merge kernel that follows picks the token.
+// One CTA per (batch row, spc segments of 256 entries).  Every CTA of a batch
+// row first takes the batch row's decision itself from the sweep's partials:
+// one warp per logit row combines its partials, then one warp runs the accept
+// test (the same arithmetic on the same numbers in every CTA, so all agree).
+// The first CTA of the batch row also writes the row statistics, the accepted
+// prefix, p, q, the count and the draw state.  Then the CTA writes the weight
+// sums of its segments; the CTA that finishes last (a counter per batch row)
+// draws the token from all of them by the inverse transform, falls back to p_n
+// when the residual has no positive weight, and emits.
 template <int DT, bool TOPK>
 __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, DrawArgs a) {
-  const int b = (int)(blockIdx.x / (unsigned)a.nsplit3);
-  const int split = (int)(blockIdx.x - (unsigned)b * (unsigned)a.nsplit3);
+  const int b = (int)(blockIdx.x / (unsigned)a.nsplit);
+  const int split = (int)(blockIdx.x - (unsigned)b * (unsigned)a.nsplit);
   const int gamma = a.gamma;
   const int R1 = 2 * gamma + 1;
   const int64_t V = a.V;
@@ -702,6 +711,7 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
   __shared__ RowStat srs[65];
   __shared__ DraftAt sda[32];
   __shared__ DrawState s_st;
+  __shared__ int s_last;
   if (warp == kWarps - 1 && lane < gamma) {
     // independent of the sweep: read before waiting for it
     DraftAt d;
@@ -720,90 +730,82 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
   pdl_wait();  // the sweep's partials
   pdl_launch_dependents();
   if (lead && threadIdx.x == 0) a.alpha_cnt[b] = 0u;
-  for (int k = warp; k < R1; k += kWarps) {
-    const RowStat rs = combine_row(x.part + ((int64_t)b * R1 + k) * x.nch, x.nch,
-                                   lead ? x.rowstat + (int64_t)b * R1 + k : nullptr);
-    if (lane == 0) srs[k] = rs;
+  for (int k = warp; k < R1; k += 2 * kWarps) {
+    // rows k and k + kWarps together: one round of partial loads for R1 <= 16
+    const int k2 = k + kWarps;
+    const int64_t r0 = (int64_t)b * R1 + k, r2 = (int64_t)b * R1 + k2;
+    RowStat rs0, rs2;
+    combine_row2(x.part + r0 * x.nch, k2 < R1 ? x.part + r2 * x.nch : nullptr, x.nch,
+                 lead ? x.rowstat + r0 : nullptr, lead ? x.rowstat + r2 : nullptr, rs0, rs2);
+    if (lane == 0) {
+      srs[k] = rs0;
+      if (k2 < R1) srs[k2] = rs2;
+    }
   }
   __syncthreads();
   if (warp == 0) decide_batch_row<DT>(x, b, srs, sda, lead, &s_st);
   __syncthreads();
   const DrawState st = s_st;
-  if (st.mode == kDrawDone) return;
+  if (st.mode == kDrawDone) return;  // the same in every CTA of the batch row
   const bool resid = (st.mode == kDrawResidual);
   const char* rt = row_ptr<DT>(a.zt, a.zd, b, st.pos, gamma, V);
   const char* rd = resid ? row_ptr<DT>(a.zt, a.zd, b, gamma + 1 + st.pos, gamma, V) : nullptr;
-  const bool vec_ok = (V % 4) == 0;  // 4-entry groups start 4-entry aligned in every row
-  const int Vi = (int)V;             // V < 2^31
-  const int ngroups = (int)ceil_div(V, 4);
-  const int g0 = split * a.gpc, g1 = min(ngroups, g0 + a.gpc);
-  const PhiloxKeys pk = philox_keys(a.seed);
-  KI mine = resid ? draw_range<DT, true, TOPK>(rt, rd, g0, g1, Vi, vec_ok, st, b, pk, a.round)
-                  : draw_range<DT, false, TOPK>(rt, rd, g0, g1, Vi, vec_ok, st, b, pk, a.round);
-  const Top2 t = block_top2(mine);
-  if (threadIdx.x == 0) a.part3[(int64_t)b * a.nsplit3 + split] = t;
-}
-
-// One CTA per batch row: merge the per-CTA top-2 keys, re-decide a near tie in
-// double, and redraw from p_n if the residual had no positive entry.
-template <int DT>
-__global__ void __launch_bounds__(kThreads) k_draw_merge(DrawArgs a) {
-  const int b = blockIdx.x;
-  const int gamma = a.gamma;
-  const int64_t V = a.V;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait();  // the draw's partials
-  const DrawState st = a.state[b];
-  if (st.mode == kDrawDone) return;
-  const bool resid = (st.mode == kDrawResidual);
-  const char* rt = row_ptr<DT>(a.zt, a.zd, b, st.pos, gamma, V);
-  const char* rd = resid ? row_ptr<DT>(a.zt, a.zd, b, gamma + 1 + st.pos, gamma, V) : nullptr;
-  Top2 m{KI{-kInf, -1}, KI{-kInf, -1}};
-  for (int j = tid; j < a.nsplit3; j += blockDim.x) {
-    const float4 raw =
-        __ldcg(reinterpret_cast<const float4*>(a.part3 + (int64_t)b * a.nsplit3 + j));
-    Top2 p;
-    p.a.k = raw.x;
-    p.a.i = __float_as_int(raw.y);
-    p.b.k = raw.z;
-    p.b.i = __float_as_int(raw.w);
-    m = top2_merge(m, p);
-  }
-  __shared__ Top2 sm2[kThreads / 32];
-  m = warp_reduce_top2(m);
-  if (lane == 0) sm2[warp] = m;
-  __syncthreads();
+  uint64_t* seg = a.segsum + (int64_t)b * a.nseg;
+  const int s0 = split * a.spc, s1 = min(a.nseg, s0 + a.spc);
+  __shared__ uint64_t s_wtot[kWarps];
   __shared__ int s_tok;
-  __shared__ int s_fallback;
-  if (tid == 0) {
-    Top2 r{KI{-kInf, -1}, KI{-kInf, -1}};
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r = top2_merge(r, sm2[w]);
-    const int tk = refine<DT>(r, rt, rd, st, resid, (uint32_t)b, a.seed, a.round);
-    s_tok = tk;
-    s_fallback = (tk < 0 && resid) ? 1 : 0;
+  const uint64_t wt =
+      resid ? segment_sums<DT, true, TOPK>(rt, rd, V, a.vec, st, s0, s1, warp, kWarps, a.fsh, seg)
+            : segment_sums<DT, false, TOPK>(rt, nullptr, V, a.vec, st, s0, s1, warp, kWarps,
+                                            a.fsh, seg);
+  if (lane == 0) s_wtot[warp] = wt;
+  __threadfence();  // this CTA's segment sums before its arrival
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint64_t ct = 0;
+    for (int w = 0; w < kWarps; ++w) ct += s_wtot[w];
+    a.ctot[(int64_t)b * a.nsplit + split] = ct;
+    __threadfence();
+    s_last = (atomicAdd(a.done + b, 1u) == (unsigned)(a.nsplit - 1)) ? 1 : 0;
   }
   __syncthreads();
-  if (s_fallback) {
+  if (!s_last) return;
+  __threadfence();  // every other CTA's sums are visible from here
+  const uint64_t k53 = draw_uniform53(a.seed, (uint32_t)st.pos, (uint32_t)b, a.round);
+  const uint64_t* ctot = a.ctot + (int64_t)b * a.nsplit;
+  int fl = st.flags;
+  if (warp == 0) {
+    const int t = resid ? draw_select_warp<DT, true, TOPK>(rt, rd, V, a.vec, st, seg, a.nseg,
+                                                           ctot, a.nsplit, a.spc, a.fsh, k53)
+                        : draw_select_warp<DT, false, TOPK>(rt, nullptr, V, a.vec, st, seg,
+                                                            a.nseg, ctot, a.nsplit, a.spc,
+                                                            a.fsh, k53);
+    if (lane == 0) s_tok = t;
+  }
+  __syncthreads();
+  int tok = s_tok;
+  if (resid && tok < 0) {
     // the residual had no positive entry in floating point: draw from p_n itself
+    fl |= SV_FLAG_RESIDUAL_FALLBACK;
     DrawState sp = st;
     sp.mode = kDrawSampleRow;
-    const PhiloxKeys pk = philox_keys(a.seed);
-    KI f = draw_range<DT, false, true>(rt, nullptr, 0, (int)ceil_div(V, 4), (int)V, (V % 4) == 0, sp,
-                                 (uint32_t)b, pk, a.round);
-    Top2 tf = block_top2(f);
-    if (tid == 0)
-      s_tok = refine<DT>(tf, rt, nullptr, sp, false, (uint32_t)b, a.seed, a.round);
+    segment_sums<DT, false, TOPK>(rt, nullptr, V, a.vec, sp, 0, a.nseg, warp, kWarps, a.fsh,
+                                  seg);
     __syncthreads();
+    if (warp == 0) {
+      const int t = draw_select_warp<DT, false, TOPK>(rt, nullptr, V, a.vec, sp, seg, a.nseg,
+                                                      nullptr, 0, 0, a.fsh, k53);
+      if (lane == 0) s_tok = t;
+    }
+    __syncthreads();
+    tok = s_tok;
   }
-  if (tid == 0) {
-    int tk = s_tok;
-    int fl = st.flags;
-    if (s_fallback) fl |= SV_FLAG_RESIDUAL_FALLBACK;
-    if (tk < 0) {
-      tk = 0;
+  if (threadIdx.x == 0) {
+    if (tok < 0) {
+      tok = 0;
       fl |= SV_FLAG_ZERO_MASS;
     }
-    a.out_tokens[(int64_t)b * (gamma + 1) + st.pos] = tk;
+    a.out_tokens[(int64_t)b * (gamma + 1) + st.pos] = tok;
     if (a.out_flags) a.out_flags[b] = (uint8_t)fl;
   }
 }
@@ -937,10 +939,12 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   float2* part1 = reinterpret_cast<float2*>(ws + pl.off_part1);
   RowStat* rowstat = reinterpret_cast<RowStat*>(ws + pl.off_rowstat);
   DrawState* state = reinterpret_cast<DrawState*>(ws + pl.off_state);
-  Top2* part3 = reinterpret_cast<Top2*>(ws + pl.off_part3);
+  uint64_t* segsum = reinterpret_cast<uint64_t*>(ws + pl.off_segsum);
+  uint64_t* ctot = reinterpret_cast<uint64_t*>(ws + pl.off_ctot);
   float* apart = reinterpret_cast<float*>(ws + pl.off_alpha);
   float* thr = reinterpret_cast<float*>(ws + pl.off_thr);
   uint32_t* alpha_cnt = cnt;
+  uint32_t* done = cnt + B;
   DeviceInfo* di = nullptr;
   {
     const cudaError_t e = device_info(&di);
@@ -955,7 +959,7 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   const int nch = (int)(tma ? ceil_div(V, tma_chunk_elems(DT)) : ceil_div(V, kChunkSweep));
   SweepCtx sx{zt, zd, xt, B, gamma, V, temperature, row_T, seed, round, nch, part1, rowstat,
               state, out_tokens, out_counts, out_p, out_q, out_flags, 1.0f / lenience,
-              masked ? thr : nullptr};
+              masked ? thr : nullptr, done};
   auto sweep = [&](bool with_thr, const SweepCtx& ctx) {
     if (tma) {
       // one resident wave of warps, chunks dealt round-robin
@@ -1003,23 +1007,23 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   // One resident wave of draw CTAs when the batch allows: every CTA takes its
   // batch row's decision before drawing, so a second wave would pay that
   // latency again.  At least kChunkDraw entries per CTA.
-  const int64_t ngroups = ceil_div(V, 4);
+  const int64_t nseg = ceil_div(V, kDrawSegEntries);
   int64_t nsplit = pl.nsplit3;
   const int64_t slots = (int64_t)di->sms * kDrawCtasPerSm;
   if ((int64_t)B * nsplit > slots) nsplit = (slots / B > 1) ? slots / B : 1;
-  const int64_t gpc = ceil_div(ngroups, nsplit);
-  nsplit = ceil_div(ngroups, gpc);  // no CTA without groups
-  DrawArgs da{zt, zd, B, gamma, V, seed, round, state, alpha_cnt, part3, (int)nsplit, (int)gpc,
-              out_tokens, out_flags};
+  const int64_t spc = ceil_div(nseg, nsplit);
+  nsplit = ceil_div(nseg, spc);  // no CTA without segments
+  const int64_t vec_elems = (DT == SV_F32) ? 4 : 8;
+  const bool vec = (V % vec_elems) == 0 && (reinterpret_cast<uintptr_t>(zt) % 16) == 0 &&
+                   (reinterpret_cast<uintptr_t>(zd) % 16) == 0;
+  DrawArgs da{zt, zd, B, gamma, V, seed, round, alpha_cnt, done, segsum, ctot, fix_shift(V),
+              (int)nseg, (int)nsplit, (int)spc, vec, out_tokens, out_flags};
   cudaError_t e = masked ? launch_pdl(k_draw<DT, true>, dim3((unsigned)(nsplit * B)),
                                       dim3(kThreads), 0, stream, sx, da)
                        : launch_pdl(k_draw<DT, false>, dim3((unsigned)(nsplit * B)),
                                     dim3(kThreads), 0, stream, sx, da);
   if (e != cudaSuccess) return e;
   mark(2, stream);
-  e = launch_pdl(k_draw_merge<DT>, dim3((unsigned)B), dim3(kThreads), 0, stream, da);
-  if (e != cudaSuccess) return e;
-  mark(3, stream);
   if (out_alpha) {
     const int ns = (int)ceil_div(V, kChunkSweep);
     k_alpha<DT><<<(unsigned)((int64_t)ns * gamma * B), kThreads, 0, stream>>>(

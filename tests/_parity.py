@@ -7,10 +7,11 @@ Rules (the verify step's stated tolerances):
     |u - p/q| < 1e-6, or a draw whose U W lies within 4e-6 (probability units)
     of an end of the drawn token's cumulative interval, both measured on the
     oracle's double-precision values; near-ties are counted and must stay under
-    1e-4 of all decisions.  The draw bound: the GPU sums fp32 weights (about
-    3e-7 relative error each from exp2 and the scaled logit, 1e-7 from each
-    fp32 partial sum of at most 16 terms in order) into its cumulative sums, so
-    its interval ends move by at most about 1e-6 of the total;
+    1e-4 of all decisions.  The draw bound: the GPU forms fp32 weights (about
+    3e-7 relative error each from exp2 and the scaled logit), adds runs of at
+    most 16 of them in fp32 (at most 15 roundings of 2^-24 relative) and the
+    runs exactly in 2^-32 fixed point, so its interval ends move by at most
+    about 1e-6 of the total;
   * p(x), q(x) and alpha agree within 1e-5 relative;
   * flags agree exactly;
   * with a nucleus (top-p) cut, a batch row whose oracle-reported nucleus gap is

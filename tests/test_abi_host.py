@@ -208,3 +208,12 @@ def test_lmhead_verify_drafted_argument_errors():
     assert call(lse=ctypes.c_void_p(0x10002)) == -3
     assert call(Ht=100) == -6
     assert call(ws=None) == -4
+
+
+def test_timing_events_argument_check():
+    """A non-NULL event array needs n >= 1; NULL switches recording off.  No event
+    is recorded here (no call follows while they are set)."""
+    L = sv.load()
+    arr = (ctypes.c_void_p * 1)(ctypes.c_void_p(0x10000))
+    assert L.sv_set_timing_events(ctypes.cast(arr, ctypes.c_void_p), 0) == -1
+    assert L.sv_set_timing_events(None, 0) == 0
