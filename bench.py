@@ -76,7 +76,7 @@ def tensor_peaks():
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture of the same
 # workload (profiles/ holds the summary); None when the kernel changed since.
-SWEEP_TRAFFIC_BYTES = 150907392  # 147779072 read + 3128320 written, profiles/k_sweep_tma_sample_b64.md
+SWEEP_TRAFFIC_BYTES = 151403776  # 148485120 read + 2918656 written, profiles/k_sweep_vec_sample_b64.md
 LMHEAD_PASS1_TRAFFIC_BYTES = 1580866592  # 1577.972 MB read + 2.895 MB written, profiles/k_lm_lmhead.md
 
 

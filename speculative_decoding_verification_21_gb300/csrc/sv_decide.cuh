@@ -52,7 +52,55 @@ struct SweepCtx {
   float inv_lenience;    // 1/l of the lenient comparison u <= p/(l q); 1: the exact round
   const float* thr;      // [B][R1] top-k thresholds (logits below have weight 0) or null
   uint32_t* done;        // [B] arrival counters of the draw, zeroed by every sweep
+  float2* epart;         // vector sweep: [B*R1][2] head and tail pieces, `part` holds one
+                         // partial per 4 KB block of the two arrays; null: [B*R1][nch]
 };
+
+// The chunk partials of one logit row, in row order.  Generic sweep: nch
+// consecutive partials.  Vector sweep: the head piece, the partials of the row's
+// inner 4 KB blocks (consecutive in the per-block array), the tail piece.
+struct RowParts {
+  float2* head;
+  float2* inner;
+  float2* tail;
+  int n;       // partials in all
+  int ninner;  // vector sweep: inner blocks (-1: generic layout)
+  __device__ __forceinline__ float2* at(int j) const {
+    if (ninner < 0) return head + j;
+    return (j == 0) ? head : ((j <= ninner) ? inner + (j - 1) : tail);
+  }
+};
+
+// Row rid = b*R1 + k of batch row b.  The vector sweep cuts each of the two
+// arrays (target rows, draft rows) into 4 KB blocks aligned in memory; block
+// indices count the target array's blocks first.
+template <int DT>
+__device__ __forceinline__ RowParts row_parts(const SweepCtx& x, int64_t rid) {
+  RowParts p;
+  if (!x.epart) {
+    p.head = x.part + rid * x.nch;
+    p.inner = p.tail = nullptr;
+    p.n = x.nch;
+    p.ninner = -1;
+    return p;
+  }
+  const int gamma = x.gamma, R1 = 2 * gamma + 1;
+  const int b = (int)(rid / R1), k = (int)(rid - (int64_t)b * R1);
+  const int64_t RB = x.V * ((DT == SV_F32) ? 4 : 2);
+  const uintptr_t zt = reinterpret_cast<uintptr_t>(x.zt), zd = reinterpret_cast<uintptr_t>(x.zd);
+  const int64_t hd0 = (int64_t)(zt & 4095u), hd1 = (int64_t)(zd & 4095u);
+  const int64_t NC0 = ((int64_t)x.B * (gamma + 1) * RB + hd0 + 4095) >> 12;
+  const bool arr = k > gamma;
+  const int64_t ra = arr ? (int64_t)b * gamma + (k - gamma - 1) : (int64_t)b * (gamma + 1) + k;
+  const int64_t a0 = ra * RB + (arr ? hd1 : hd0);
+  const int64_t in0 = (a0 + 4095) >> 12, in1 = (a0 + RB) >> 12;  // inner blocks [in0, in1)
+  p.head = x.epart + 2 * rid;
+  p.tail = p.head + 1;
+  p.ninner = (int)(in1 - in0);
+  p.inner = x.part + (arr ? NC0 : 0) + in0;
+  p.n = p.ninner + 2;
+  return p;
+}
 
 // Online (max, sum) of a lane's share of one row's chunk partials.
 struct RowAcc {
@@ -79,7 +127,7 @@ __device__ __forceinline__ RowStat row_acc_finish(const RowAcc& a, RowStat* out)
   RowStat rs;
   rs.mc = M;
   rs.bits = bits;
-  rs.s = (bits & kRowNaN) ? CUDART_NAN : (double)sl;
+  rs.s = (bits & kRowNaN) ? CUDART_NAN_F : sl;
   if (lane == 0 && out) *out = rs;
   return rs;
 }
@@ -94,22 +142,32 @@ __device__ __forceinline__ RowStat combine_row(const float2* pr, int nch, RowSta
   return row_acc_finish(a, out);
 }
 
-// Two rows by one warp with the loads of both in flight together (p1 may be
-// null); each row's arithmetic is that of combine_row.
-__device__ __forceinline__ void combine_row2(const float2* p0, const float2* p1, int nch,
-                                             RowStat* out0, RowStat* out1, RowStat& r0,
-                                             RowStat& r1) {
+// The same over a row's partials in any layout.
+__device__ __forceinline__ RowStat combine_parts(const RowParts& p, RowStat* out) {
+  const int lane = threadIdx.x & 31;
+  RowAcc a{-kInf, 0.0f, 0};
+#pragma unroll 4
+  for (int j = lane; j < p.n; j += 32) row_acc_add(a, __ldcg(p.at(j)));
+  return row_acc_finish(a, out);
+}
+
+// Two rows by one warp with the loads of both in flight together (p1.n may be
+// 0: no second row); each row's arithmetic is that of combine_row.
+__device__ __forceinline__ void combine_parts2(const RowParts& p0, const RowParts& p1,
+                                               RowStat* out0, RowStat* out1, RowStat& r0,
+                                               RowStat& r1) {
   const int lane = threadIdx.x & 31;
   RowAcc a0{-kInf, 0.0f, 0}, a1{-kInf, 0.0f, 0};
+  const int n = max(p0.n, p1.n);
 #pragma unroll 4
-  for (int j = lane; j < nch; j += 32) {
-    const float2 x0 = __ldcg(p0 + j);
-    const float2 x1 = p1 ? __ldcg(p1 + j) : make_float2(-kInf, 0.0f);
+  for (int j = lane; j < n; j += 32) {
+    const float2 x0 = (j < p0.n) ? __ldcg(p0.at(j)) : make_float2(-kInf, 0.0f);
+    const float2 x1 = (j < p1.n) ? __ldcg(p1.at(j)) : make_float2(-kInf, 0.0f);
     row_acc_add(a0, x0);
     row_acc_add(a1, x1);
   }
   r0 = row_acc_finish(a0, out0);
-  r1 = row_acc_finish(a1, p1 ? out1 : nullptr);
+  r1 = row_acc_finish(a1, p1.n ? out1 : nullptr);
 }
 
 // log2 of the unnormalised probability, e = z c - mc, carried in two floats:
@@ -159,7 +217,7 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
   for (int k = lane; k < R1; k += 32) {
     const RowStat v = srs[k];
     if (v.mc == -kInf) fl |= SV_FLAG_ZERO_MASS;
-    if (!((float)v.s < kInf) || v.mc == kInf || !temperature_ok(T)) fl |= SV_FLAG_NONFINITE;
+    if (!(v.s < kInf) || v.mc == kInf || !temperature_ok(T)) fl |= SV_FLAG_NONFINITE;
     if (v.bits & kRowTimeout) fl |= SV_FLAG_TIMEOUT | SV_FLAG_NONFINITE;
   }
   bool accept = false, bad = false, qzero = false;
@@ -174,8 +232,7 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
       const float zx = da.zt;
       const float zy = da.zd;
       const RowStat rt = srs[lane], rd = srs[gamma + 1 + lane];
-      // the row sums are fp32 values (kept in double fields): compare and divide in fp32
-      const float st_ = (float)rt.s, sd_ = (float)rd.s;
+      const float st_ = rt.s, sd_ = rd.s;
       const Exp2 ep = exponent_at(zx, c, rt.mc), eq = exponent_at(zy, c, rd.mc);
       P = prob_from(zx, ep, st_);
       Q = prob_from(zy, eq, sd_);
@@ -215,14 +272,14 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
   if (lane == 0) {
     // set up the draw of the target's own token
     const float mct = srs[n].mc;
-    const double St = srs[n].s;
+    const float St = srs[n].s;
     DrawState st{};
     st.pos = n;
     st.c = c;
     st.invT = invT;
     st.tt = x.thr ? x.thr[(int64_t)b * R1 + n] : -kInf;
     st.td = (x.thr && n < gamma) ? x.thr[(int64_t)b * R1 + gamma + 1 + n] : -kInf;
-    const bool t_ok = (St > 0.0) && (St < 1e308) && (mct < kInf);
+    const bool t_ok = (St > 0.0f) && (St < kInf) && (mct < kInf);
     if (n == gamma) {
       if (t_ok) {
         st.mode = kDrawSampleRow;
@@ -233,14 +290,14 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
       }
     } else {
       const float mcd = srs[gamma + 1 + n].mc;
-      const double Sd = srs[gamma + 1 + n].s;
-      const bool d_nonfinite = !(Sd < 1e308) || mcd == kInf;
+      const float Sd = srs[gamma + 1 + n].s;
+      const bool d_nonfinite = !(Sd < kInf) || mcd == kInf;
       if (!t_ok || d_nonfinite) {
         // p_n has no mass (or a row is not finite): the residual and its fallback
         // are empty; token 0
         st.mode = kDrawDone;
-        if (St == 0.0) fl |= SV_FLAG_RESIDUAL_FALLBACK;
-      } else if (Sd == 0.0) {
+        if (St == 0.0f) fl |= SV_FLAG_RESIDUAL_FALLBACK;
+      } else if (Sd == 0.0f) {
         st.mode = kDrawSampleRow;  // q_n has no mass: max(0, p_n - q_n) = p_n
         st.mct = mct;
         st.st = St;
@@ -250,7 +307,7 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
         st.st = St;
         st.mcd = mcd;
         st.sd = Sd;
-        st.K = (mct - mcd) + (log2f((float)St) - log2f((float)Sd));
+        st.K = (mct - mcd) + (log2f(St) - log2f(Sd));
       }
     }
     st.flags = fl;

@@ -264,6 +264,47 @@ __device__ __forceinline__ int warp_find(const uint64_t* v, int n, uint64_t t, u
   return -1;
 }
 
+// warp_find over all n <= 32 kPickAll words in one round of loads, with W (the
+// total) and t = floor(U W) taken from the same registers.  -1 when W = 0.
+constexpr int kPickAll = 16;
+__device__ __forceinline__ int warp_pick_all(const uint64_t* v, int n, uint64_t k53,
+                                             uint64_t* W, uint64_t* t, uint64_t* before) {
+  const int lane = threadIdx.x & 31;
+  uint64_t x[kPickAll], ls = 0;
+#pragma unroll
+  for (int r = 0; r < kPickAll; ++r) {
+    const int j = lane * kPickAll + r;
+    x[r] = (j < n) ? __ldcg(v + j) : 0ull;
+    ls += x[r];
+  }
+  uint64_t P = ls;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t y = __shfl_up_sync(0xffffffffu, P, o);
+    if (lane >= o) P += y;
+  }
+  *W = __shfl_sync(0xffffffffu, P, 31);
+  *t = scale_fix(k53, *W);
+  *before = 0;
+  if (*W == 0) return -1;
+  const unsigned hit = __ballot_sync(0xffffffffu, P > *t);
+  const int l = __ffs((int)hit) - 1;
+  int idx = 0;
+  uint64_t acc = P - ls;
+  if (lane == l) {
+#pragma unroll
+    for (int r = 0; r < kPickAll; ++r) {
+      if (acc + x[r] > *t) {
+        idx = lane * kPickAll + r;
+        break;
+      }
+      acc += x[r];
+    }
+  }
+  *before = __shfl_sync(0xffffffffu, acc, l);
+  return __shfl_sync(0xffffffffu, idx, l);
+}
+
 // The entry of a run of weights w[0..M) holding trel (fixed point, measured
 // from `lo`, the run's start): the first e whose fp32 prefix, added in order,
 // ends past it.  The run's own sum is the prefix at M - 1, so an entry is
@@ -292,17 +333,24 @@ __device__ int draw_select_warp(const char* rt, const char* rd, int64_t V, bool 
                                 const DrawState& st, const uint64_t* seg, int nseg,
                                 const uint64_t* ctot, int ngrp, int spc, int fsh, uint64_t k53) {
   const int lane = threadIdx.x & 31;
-  const uint64_t W = ctot ? warp_total(ctot, ngrp) : warp_total(seg, nseg);
-  if (W == 0) return -1;
-  const uint64_t t = scale_fix(k53, W);  // < W
-  uint64_t base = 0;
-  int s0 = 0, cnt = nseg;
-  if (ctot) {
-    const int c = warp_find<2>(ctot, ngrp, t, 0ull, &base);
-    s0 = c * spc;
-    cnt = min(nseg - s0, spc);
+  uint64_t W, t, base = 0;
+  int s = 0;
+  if (nseg <= 32 * kPickAll) {
+    // one round of loads: all segment sums at once give W, t and the segment
+    s = warp_pick_all(seg, nseg, k53, &W, &t, &base);
+    if (W == 0) return -1;
+  } else {
+    W = ctot ? warp_total(ctot, ngrp) : warp_total(seg, nseg);
+    if (W == 0) return -1;
+    t = scale_fix(k53, W);  // < W
+    int s0 = 0, cnt = nseg;
+    if (ctot) {
+      const int c = warp_find<2>(ctot, ngrp, t, 0ull, &base);
+      s0 = c * spc;
+      cnt = min(nseg - s0, spc);
+    }
+    s = s0 + warp_find<4>(seg + s0, cnt, t, base, &base);
   }
-  const int s = s0 + warp_find<2>(seg + s0, cnt, t, base, &base);
   const float kd = RESID ? __fsub_rn(st.K, st.mct) : 0.0f;
   const int64_t v0 = (int64_t)s * kDrawSegEntries + lane * kDrawLaneEntries;
   const Raw8<DT> xt = load_raw8<DT>(rt, v0, V, vec, -kInf);

@@ -904,13 +904,13 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
         const float lse = __ldg(a.dlse + (int64_t)b * gamma + (k - gamma - 1));
         rs.mc = lse * kLog2e;
         rs.bits = (lse != lse) ? kRowNaN : 0;
-        rs.s = (lse != lse) ? CUDART_NAN : ((lse == -kInf) ? 0.0 : 1.0);
+        rs.s = (lse != lse) ? CUDART_NAN_F : ((lse == -kInf) ? 0.0f : 1.0f);
       } else {
         rs = combine_row(a.part + ((int64_t)b * R1 + k) * a.nslot * 2, a.nslot * 2, nullptr);
       }
       if (err) {
         rs.bits |= kRowTimeout | kRowNaN;
-        rs.s = CUDART_NAN;
+        rs.s = CUDART_NAN_F;
       }
       if (lane == 0) srs[k] = rs;
     }

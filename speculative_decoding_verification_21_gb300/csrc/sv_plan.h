@@ -18,31 +18,42 @@ constexpr int64_t kChunkDraw = 8192;   // least vocabulary entries per CTA in th
 constexpr int kDrawCtasPerSm = 4;      // resident draw CTAs per SM (its launch bounds)
 constexpr size_t kAlign = 256;
 
-// Persistent bulk-copy sweep: warps per CTA, pipeline stages per warp, bytes per chunk.
+// Persistent vector sweep: warps per CTA, resident CTAs per SM (its launch bounds),
+// bytes per chunk.
 constexpr int kSweepWarps = 8;
-constexpr int kSweepStages = 2;
+constexpr int kSweepCtasPerSm = 2;
 constexpr int kSweepChunkBytes = 4096;
 
-SV_HD inline size_t sweep_smem_bytes() {
-  return (size_t)kSweepWarps * kSweepStages * kSweepChunkBytes +
-         (size_t)kSweepWarps * kSweepStages * sizeof(uint64_t);
-}
-// Logits per bulk-copy chunk for a dtype (0 = fp32, 1 = bf16).
-SV_HD inline int64_t tma_chunk_elems(int dtype) { return kSweepChunkBytes / (dtype == 0 ? 4 : 2); }
-// The bulk-copy sweep needs every row to start on a 16-byte boundary.
-SV_HD inline bool use_tma_sweep(int dtype, int64_t V) {
-  return (V * (dtype == 0 ? 4 : 2)) % 16 == 0;
+// The vector sweep needs every row to start on a 16-byte boundary (the bases are)
+// and rows of at least one chunk, so that a chunk touches at most two rows.
+SV_HD inline bool use_vec_sweep(int dtype, int64_t V) {
+  const int64_t rb = V * (dtype == 0 ? 4 : 2);
+  return rb % 16 == 0 && rb >= kSweepChunkBytes;
 }
 
 SV_HD inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 SV_HD inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Partials of a sweep, at most: one per 4 KB block of the target and draft arrays of
+// fp32 rows (either base may sit anywhere in its first block: one more block each),
+// the two edge pieces of every row, or one per kChunkSweep-logit split of every row.
+SV_HD inline int64_t vec_sweep_blocks(int B, int gamma, int64_t V) {
+  const int64_t rb = V * 4;
+  return ceil_div((int64_t)B * (gamma + 1) * rb, 4096) + 1 + ceil_div((int64_t)B * gamma * rb, 4096) + 1;
+}
+SV_HD inline int64_t vec_sweep_partials(int B, int gamma, int64_t V) {
+  const int64_t rows = (int64_t)B * (2 * gamma + 1);
+  const int64_t vec = vec_sweep_blocks(B, gamma, V) + 2 * rows;
+  const int64_t gen = rows * ceil_div(V, kChunkSweep);
+  return vec > gen ? vec : gen;
+}
 
 // Per-row softmax statistics after the chunk combine: max (scaled, log2 units),
 // row condition bits, and the sum of 2^(y - max) in double.
 struct RowStat {
   float mc;
   int bits;  // kRowNaN | kRowTimeout
-  double s;
+  float s;   // sum of 2^(y - mc) over the row (fp32 throughout: GB300 runs fp64 slowly)
 };
 constexpr int kRowNaN = 1, kRowTimeout = 2;
 
@@ -64,8 +75,8 @@ struct DrawState {
   int flags;     // SV_FLAG_* gathered by the decision
   float tt;      // top-k threshold of target row n: logits below it have weight 0 (-inf: off)
   float td;      // top-k threshold of draft row n (residual only)
-  double st;     // target row n: sum
-  double sd;     // draft row n: sum (residual only)
+  float st;      // target row n: sum
+  float sd;      // draft row n: sum (residual only)
 };
 
 struct SamplePlan {
@@ -84,8 +95,10 @@ inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
   p.R1 = 2 * gamma + 1;
   p.nsplit1 = (int)ceil_div(V, kChunkSweep);
   p.nsplit3 = (int)ceil_div(V, kChunkDraw);
-  // per-(row, chunk) partials: enough for the smaller bulk-copy chunks of fp32
-  const int64_t nch_max = ceil_div(V, tma_chunk_elems(0));
+  // chunk partials: [row][8192-logit split] (generic sweep), or one per 4 KB block of
+  // the two logit arrays plus [row][2] edge pieces (vector sweep; fp32 has the most)
+  const int64_t nparts = vec_sweep_partials(B, gamma, V);
+  const int64_t nch_max = ceil_div(nparts, (int64_t)B * p.R1);
   size_t o = 0;
   p.cnt_bytes = 2 * sizeof(uint32_t) * (size_t)B;
   p.off_cnt = o;      o = align_up(o + p.cnt_bytes);

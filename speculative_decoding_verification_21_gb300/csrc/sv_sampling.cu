@@ -8,11 +8,11 @@
 //
 //   sweep     online softmax statistics of every chunk of all 2*gamma+1 logit
 //             rows: max and sum of 2^(y - max), y = z * T^-1 * log2 e.
-//             k_sweep_tma (rows whose byte length is a multiple of 16): a
+//             k_sweep_vec (rows whose byte length is a multiple of 16): a
 //             persistent kernel; every warp streams 4 KB chunks, interleaved
-//             across warps in batch-row order, through a 2-stage bulk-copy (TMA)
-//             pipeline in shared memory.  k_sweep (any shape): one CTA per
-//             8192-logit chunk with 16-byte vector loads.
+//             across warps in batch-row order, two chunks in registers (one
+//             reduced while the next loads).  k_sweep (any shape): one CTA
+//             per 8192-logit chunk with 16-byte vector loads.
 //   k_draw    one CTA per (batch row, slice of at least 8192 entries).  Each
 //             CTA first takes its batch row's decision from the chunk partials:
 //             the row statistics, p(x_i), q(x_i), u_i, accept iff u_i <= p/q,
@@ -140,147 +140,160 @@ __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
 }
 
 // --------------------------------------------------------------------------
-// TMA sweep (rows a multiple of 16 bytes long): persistent, per-warp pipelines.
-// Chunk c of the [b][row][chunk] order goes to warp c mod W, so the whole GPU
-// walks memory in address order; each chunk leaves one (max, sum) partial.
+// Vector sweep (rows a multiple of 16 bytes and at least 4 KB long): persistent,
+// one resident wave.  The target rows and the draft rows are two arrays, each
+// cut into 4 KB blocks aligned to 4 KB in memory (no load straddles two of the
+// DRAM's 4 KB blocks: 13% faster than blocks aligned to the rows).  Block g of
+// the two arrays in turn (the target array's first) goes to warp g mod W, so the
+// whole GPU walks memory in address order, and leaves one (max, sum) partial in
+// part[g]; the loop does nothing else (per-block row bookkeeping cost 13%).  A
+// block that holds the end of one row and the start of the next, or an array's
+// edge, is reduced all the same and its partial is never read: each row's two
+// edge pieces (from its start to the first block boundary, from the last one to
+// its end) are reduced first, one row per warp, into epart[row][0..1].  A warp
+// holds two blocks in registers: it reduces one while the 16-byte loads of the
+// next are in flight (non-allocating in L1: every byte is read once).
 // --------------------------------------------------------------------------
 template <int DT, bool TOPK>
-__global__ void __launch_bounds__(kSweepWarps * 32, 3) k_sweep_tma(SweepCtx x) {
+__global__ void __launch_bounds__(kSweepWarps * 32, kSweepCtasPerSm) k_sweep_vec(SweepCtx x) {
   pdl_launch_dependents();  // the draw kernel may be scheduled now; it waits for us
   zero_draw_counters(x);
-  constexpr int kBytes = (DT == SV_F32) ? 4 : 2;
-  constexpr int CH = kSweepChunkBytes / kBytes;  // logits per chunk
-  extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  unsigned char* stage0 = smem + (size_t)warp * kSweepStages * kSweepChunkBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kSweepWarps * kSweepStages *
-                                                          kSweepChunkBytes) +
-                   warp * kSweepStages;
   const int gamma = x.gamma;
-  const int64_t V = x.V;
-  const int nch = x.nch;
   const int R1 = 2 * gamma + 1;
-  const int64_t NC = (int64_t)x.B * R1 * nch;
+  const int64_t RB = x.V * ((DT == SV_F32) ? 4 : 2);  // row bytes, a multiple of 16, >= 4 KB
+  const char* const base0 = reinterpret_cast<const char*>(x.zt);
+  const char* const base1 = reinterpret_cast<const char*>(x.zd);
+  const int64_t AB0 = (int64_t)x.B * (gamma + 1) * RB, AB1 = (int64_t)x.B * gamma * RB;
+  const int64_t hd0 = (int64_t)(reinterpret_cast<uintptr_t>(base0) & 4095u);
+  const int64_t hd1 = (int64_t)(reinterpret_cast<uintptr_t>(base1) & 4095u);
+  const int64_t NC0 = (AB0 + hd0 + 4095) >> 12, NC1 = (AB1 + hd1 + 4095) >> 12;
   const int64_t W = (int64_t)gridDim.x * kSweepWarps;
   const int64_t w = (int64_t)blockIdx.x * kSweepWarps + warp;
-  const int count = (w < NC) ? (int)((NC - w + W - 1) / W) : 0;  // chunks w, w+W, ...
-  const uint32_t tail_bytes = (uint32_t)((V - (int64_t)(nch - 1) * CH) * kBytes);
-  const size_t row_bytes = (size_t)V * kBytes;
-
-  if (lane == 0) {
-    for (int s = 0; s < kSweepStages; ++s) mbar_init(bars + s, 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-
-  auto pos_of = [&](int64_t cidx) {
-    ChunkPos p;
-    const int64_t r = cidx / nch;
-    p.j = (int)(cidx - r * nch);
-    p.b = (int)(r / R1);
-    p.k = (int)(r - (int64_t)p.b * R1);
-    return p;
+  const bool uniform_T = (x.row_T == nullptr);
+  const float c_all = log2_scale(inv_temperature(x.temperature));
+  auto scale_of = [&](int b) {
+    return uniform_T ? c_all : log2_scale(inv_temperature(__ldg(x.row_T + b)));
   };
-  ChunkStep step;
-  {
-    const int64_t r = W / nch;
-    step.dj = (int)(W - r * nch);
-    step.db = (int)(r / R1);
-    step.dk = (int)(r - (int64_t)step.db * R1);
-  }
-  auto src_of = [&](const ChunkPos& p) -> const char* {
-    const char* row = (p.k <= gamma)
-        ? reinterpret_cast<const char*>(x.zt) + ((size_t)p.b * (gamma + 1) + p.k) * row_bytes
-        : reinterpret_cast<const char*>(x.zd) + ((size_t)p.b * gamma + (p.k - gamma - 1)) * row_bytes;
-    return row + (size_t)p.j * kSweepChunkBytes;
+  // n <= 256 consecutive 16-byte vectors of one row, and their (max, sum)
+  auto load_piece = [&](uint4 (&v)[8], const uint4* src, int nv) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v[u] = (lane + 32 * u < nv) ? ld_stream16(src + lane + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
   };
-  auto issue = [&](int s, const ChunkPos& p) {  // lane 0 only
-    const uint32_t bytes = (p.j == nch - 1) ? tail_bytes : (uint32_t)kSweepChunkBytes;
-    mbar_arrive_expect_tx(bars + s, bytes);
-    bulk_g2s(stage0 + (size_t)s * kSweepChunkBytes, src_of(p), bytes, bars + s);
-  };
-
-  ChunkPos pi = pos_of(w);  // next chunk to issue
-  for (int s = 0; s < kSweepStages && s < count; ++s) {
-    if (lane == 0) issue(s, pi);
-    advance(pi, step, R1, nch);
-  }
-
-  bool dead = false;  // a bounded wait ran out: stop loading, mark what is left
-  int issued = count < kSweepStages ? count : kSweepStages;  // chunks issued so far
-  ChunkPos pc = pos_of(w);  // chunk being computed
-  int64_t cidx = w;
-  int cur_b = -1;
-  float c = 0.0f;
-  for (int t = 0; t < count; ++t, cidx += W, advance(pc, step, R1, nch)) {
-    const int s = t % kSweepStages;
-    const uint32_t parity = (uint32_t)((t / kSweepStages) & 1);
-    float2 res;
-    if (!dead) dead = __any_sync(0xffffffffu, !mbar_wait_bounded(bars + s, parity));
-    if (!dead) {
-      if (pc.b != cur_b) {
-        cur_b = pc.b;
-        const float T = x.row_T ? __ldg(x.row_T + cur_b) : x.temperature;
-        c = log2_scale(inv_temperature(T));
-      }
-      // logits below the row's top-k threshold add nothing to the sum
-      const float tau = TOPK ? __ldg(x.thr + (int64_t)pc.b * R1 + pc.k) : -kInf;
-      const uint4* sv = reinterpret_cast<const uint4*>(stage0 + (size_t)s * kSweepChunkBytes);
-      float zmax = -kInf, mc = -kInf, sacc = 0.0f;
-      const bool full = (pc.j != nch - 1);
-      const int nvec = full ? 8 * 32 : (int)(tail_bytes / 16);
-      uint4 v[8];
+  auto reduce_piece = [&](const uint4 (&v)[8], int nv, float c, float tau) {
+    if (nv <= 0) return make_float2(-kInf, 0.0f);
+    float zmax = -kInf, mc = -kInf, sacc = 0.0f, m = -kInf;
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (full || lane + 32 * u < nvec) v[u] = sv[lane + 32 * u];
-      // every lane holds its words: refill the stage before computing on them
-      __syncwarp();
-      if (t + kSweepStages < count) {
-        if (lane == 0) {
-          fence_proxy_async_smem();
-          issue(s, pi);
-        }
-        advance(pi, step, R1, nch);
-        issued = t + kSweepStages + 1;
-      }
-      if (full) {
-        chunk_update_full<DT, TOPK>(v, c, tau, zmax, mc, sacc);
-      } else {
-        const int nv = (nvec - lane + 31) >> 5;
-        float m = -kInf;
+    for (int u = 0; u < 8; ++u)
+      if (lane + 32 * u < nv) m = fmaxf(m, vmax<DT>(v[u]));
+    lane_raise_max(m, c, zmax, mc, sacc);
+    if (zmax > -kInf) {
+      float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (u < nv) m = fmaxf(m, vmax<DT>(v[u]));
-        lane_raise_max(m, c, zmax, mc, sacc);
-        if (zmax > -kInf) {
-          float s0 = 0.0f, s1 = 0.0f;
+      for (int u = 0; u < 8; ++u) {
+        if (lane + 32 * u < nv) {
+          float f[VecInfo<DT>::kElems];
+          unpack<DT>(v[u], f);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            if (u < nv) {
-              float f[VecInfo<DT>::kElems];
-              unpack<DT>(v[u], f);
-#pragma unroll
-              for (int e = 0; e < VecInfo<DT>::kElems; e += 2) {
-                s0 += (TOPK && f[e] < tau) ? 0.0f : ex2(fmaf(f[e], c, -mc));
-                s1 += (TOPK && f[e + 1] < tau) ? 0.0f : ex2(fmaf(f[e + 1], c, -mc));
-              }
-            }
+          for (int e = 0; e < VecInfo<DT>::kElems; e += 2) {
+            s0 += (TOPK && f[e] < tau) ? 0.0f : ex2(fmaf(f[e], c, -mc));
+            s1 += (TOPK && f[e + 1] < tau) ? 0.0f : ex2(fmaf(f[e + 1], c, -mc));
           }
-          sacc += s0 + s1;
         }
       }
-      const MS ms = warp_reduce_ms_fast(MS{mc, sacc});
-      res = make_float2(ms.m, ms.s);
-    } else {
-      res = make_float2(CUDART_NAN_F, -1.0f);  // timed-out chunk: flagged downstream
+      sacc += s0 + s1;
     }
-    if (lane == 0) x.part[cidx] = res;  // chunk order = [b][row][chunk]
+    const MS ms = warp_reduce_ms_fast(MS{mc, sacc});
+    return make_float2(ms.m, ms.s);
+  };
+
+  // ---- edge pieces: row q of the two arrays' rows goes to warp q mod W ----
+  const int64_t nrows = (int64_t)x.B * R1;
+  for (int64_t q = w; q < nrows; q += W) {
+    const bool arr = q >= (int64_t)x.B * (gamma + 1);
+    const int64_t ra = arr ? q - (int64_t)x.B * (gamma + 1) : q;
+    const int per = arr ? gamma : gamma + 1;
+    const int b = (int)ra / per, kk = (int)ra - b * per;
+    const int64_t rid = (int64_t)b * R1 + (arr ? gamma + 1 : 0) + kk;
+    const char* const rowp = (arr ? base1 : base0) + ra * RB;
+    const int64_t a0 = ra * RB + (arr ? hd1 : hd0), a1 = a0 + RB;  // 4 KB-block coordinates
+    const int64_t in0 = (a0 + 4095) & ~(int64_t)4095, in1 = a1 & ~(int64_t)4095;
+    const float c = scale_of(b);
+    const float tau = TOPK ? __ldg(x.thr + rid) : -kInf;
+    const uint4* rv = reinterpret_cast<const uint4*>(rowp);
+    // head [a0, in0) and tail [in1, a1), each shorter than 4 KB (in1 >= in0: a row is
+    // at least one block long); the loads of both in flight together
+    const int nh = (int)((in0 - a0) >> 4), nt = (int)((a1 - in1) >> 4);
+    uint4 vh[8], vt[8];
+    load_piece(vh, rv, nh);
+    load_piece(vt, rv + ((in1 - a0) >> 4), nt);
+    const float2 h = reduce_piece(vh, nh, c, tau);
+    const float2 t = reduce_piece(vt, nt, c, tau);
+    if (lane == 0) {
+      x.epart[2 * rid] = h;
+      x.epart[2 * rid + 1] = t;
+    }
   }
-  if (dead && lane == 0) {
-    // let copies still in flight land before the CTA's shared memory is released:
-    // the last chunk issued into each stage, at its phase
-    for (int t = (issued > kSweepStages ? issued - kSweepStages : 0); t < issued; ++t)
-      mbar_wait_bounded(bars + (t % kSweepStages), (uint32_t)((t / kSweepStages) & 1), 1u << 16);
+
+  // ---- every 4 KB block ----
+  const int64_t NC = NC0 + NC1;
+  if (w >= NC) return;
+  // the block's start, moved inside its array where the block crosses the array's edge
+  // (such a block's partial is never read)
+  auto src_of = [&](int64_t g) {
+    const bool arr = g >= NC0;
+    const int64_t AB = arr ? AB1 : AB0;
+    int64_t s = (arr ? g - NC0 : g) * 4096 - (arr ? hd1 : hd0);
+    s = s < 0 ? 0 : (s + 4096 > AB ? AB - 4096 : s);
+    return reinterpret_cast<const uint4*>((arr ? base1 : base0) + s);
+  };
+  auto load = [&](uint4 (&v)[8], int64_t g) {
+    const uint4* src = src_of(g);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = ld_stream16(src + lane + 32 * u);
+  };
+  // the batch row of block g's first vector, for a per-row temperature (a block that
+  // crosses into the next batch row is an edge block: its partial is not read)
+  auto batch_of = [&](int64_t g) {
+    if (uniform_T) return 0;
+    const bool arr = g >= NC0;
+    int64_t s = (arr ? g - NC0 : g) * 4096 - (arr ? hd1 : hd0);
+    s = s < 0 ? 0 : s;
+    return (int)((s / RB) / (arr ? gamma : gamma + 1));
+  };
+  auto fin = [&](const uint4 (&v)[8], int64_t g) {
+    float zmax = -kInf, mc = -kInf, sacc = 0.0f;
+    // top-k: the block's own row threshold is applied to its inner blocks by the
+    // row's own value (an edge block's partial is not read)
+    float tau = -kInf;
+    if (TOPK) {
+      const bool arr = g >= NC0;
+      int64_t s = (arr ? g - NC0 : g) * 4096 - (arr ? hd1 : hd0);
+      s = s < 0 ? 0 : s;
+      const int64_t ra = s / RB;
+      const int per = arr ? gamma : gamma + 1;
+      const int b = (int)ra / per;
+      tau = __ldg(x.thr + (int64_t)b * R1 + (arr ? gamma + 1 : 0) + ((int)ra - b * per));
+    }
+    chunk_update_full<DT, TOPK>(v, scale_of(batch_of(g)), tau, zmax, mc, sacc);
+    const MS ms = warp_reduce_ms_fast(MS{mc, sacc});
+    if (lane == 0) x.part[g] = make_float2(ms.m, ms.s);
+  };
+  uint4 va[8], vb[8];
+  int64_t ch = w;
+  load(va, ch);
+  for (;;) {
+    // a holds block ch; b gets ch + W while a is reduced, then the roles swap
+    const int64_t n1 = ch + W;
+    if (n1 < NC) load(vb, n1);
+    fin(va, ch);
+    if (n1 >= NC) break;
+    const int64_t n2 = n1 + W;
+    if (n2 < NC) load(va, n2);
+    fin(vb, n1);
+    if (n2 >= NC) break;
+    ch = n2;
   }
 }
 
@@ -455,9 +468,9 @@ __global__ void __launch_bounds__(kThreads) k_topk_cand(SweepCtx x, int k,
   const int row = blockIdx.x;
   const int b = row / R1, kk = row - b * R1;
   const int64_t V = x.V;
-  const int nch = x.nch;
+  const RowParts rp = row_parts<DT>(x, row);
+  const int nch = rp.n;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float2* pr = x.part + (int64_t)row * nch;
   const RowVisit<DT> rowv{row_ptr<DT>(x.zt, x.zd, b, kk, x.gamma, V), V};
   const float T = x.row_T ? __ldg(x.row_T + b) : x.temperature;
   const float c = log2_scale(inv_temperature(T));
@@ -470,7 +483,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_cand(SweepCtx x, int k,
   float m = -kInf;
   int bad = 0;
   for (int j = threadIdx.x; j < nch; j += blockDim.x) {
-    const float2 p = __ldcg(pr + j);
+    const float2 p = __ldcg(rp.at(j));
     if (p.x != p.x || p.y < 0.0f) bad = 1;
     m = fmaxf(m, p.x);
   }
@@ -496,7 +509,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_cand(SweepCtx x, int k,
   const float bound = (k <= nch) ? radix_kth<SV_F32>(
                                        [&](auto&& f) {
                                          for (int j = threadIdx.x; j < nch; j += blockDim.x)
-                                           f(__ldcg(pr + j).x);
+                                           f(__ldcg(rp.at(j)).x);
                                        },
                                        k, hist, s_sel)
                                  : -kInf;
@@ -540,9 +553,9 @@ __global__ void __launch_bounds__(kThreads) k_topk_cand(SweepCtx x, int k,
     float S = 0.0f;
     for (int w = 0; w < kWarps; ++w) S += s_red[w];
     thr[row] = tau;
-    pr[0] = make_float2(M, S);
+    *rp.at(0) = make_float2(M, S);
   }
-  for (int j = 1 + (int)threadIdx.x; j < nch; j += blockDim.x) pr[j] = make_float2(-kInf, 0.0f);
+  for (int j = 1 + (int)threadIdx.x; j < nch; j += blockDim.x) *rp.at(j) = make_float2(-kInf, 0.0f);
 }
 
 // Nucleus (top-p) threshold of one logit row (same passage: nucleus zeroes the
@@ -580,12 +593,12 @@ __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int 
   const float tk = has_k ? thr[row] : -kInf;
   if (!has_k && threadIdx.x == 0) thr[row] = -kInf;  // no cut unless one is found below
   if (warp == 0) {
-    const RowStat rs = combine_row(x.part + (int64_t)row * x.nch, x.nch, nullptr);
+    const RowStat rs = combine_parts(row_parts<DT>(x, row), nullptr);
     if (lane == 0) s_rs = rs;
   }
   __syncthreads();
   const RowStat rs = s_rs;
-  if ((rs.bits & (kRowNaN | kRowTimeout)) || !(rs.s > 0.0) || !(rs.s < 1e300) ||
+  if ((rs.bits & (kRowNaN | kRowTimeout)) || !(rs.s > 0.0f) || !(rs.s < kInf) ||
       !(fabsf(rs.mc) < kInf))
     return;  // empty or not finite: no cut (uniform over the CTA)
   const float mc = rs.mc;
@@ -735,8 +748,10 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
     const int k2 = k + kWarps;
     const int64_t r0 = (int64_t)b * R1 + k, r2 = (int64_t)b * R1 + k2;
     RowStat rs0, rs2;
-    combine_row2(x.part + r0 * x.nch, k2 < R1 ? x.part + r2 * x.nch : nullptr, x.nch,
-                 lead ? x.rowstat + r0 : nullptr, lead ? x.rowstat + r2 : nullptr, rs0, rs2);
+    RowParts p2 = row_parts<DT>(x, k2 < R1 ? r2 : r0);
+    if (k2 >= R1) p2.n = 0;
+    combine_parts2(row_parts<DT>(x, r0), p2, lead ? x.rowstat + r0 : nullptr,
+                   lead ? x.rowstat + r2 : nullptr, rs0, rs2);
     if (lane == 0) {
       srs[k] = rs0;
       if (k2 < R1) srs[k2] = rs2;
@@ -752,6 +767,15 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
   const char* rd = resid ? row_ptr<DT>(a.zt, a.zd, b, gamma + 1 + st.pos, gamma, V) : nullptr;
   uint64_t* seg = a.segsum + (int64_t)b * a.nseg;
   const int s0 = split * a.spc, s1 = min(a.nseg, s0 + a.spc);
+  if (a.vec && threadIdx.x < 2 && (threadIdx.x == 0 || resid)) {
+    // the slice's bytes of each row it reads, requested from HBM at once so that the
+    // warps' later segments find them in L2
+    constexpr int64_t kEl = (DT == SV_F32) ? 4 : 2;
+    const int64_t e0 = (int64_t)s0 * kDrawSegEntries;
+    const int64_t e1 = min(V, (int64_t)s1 * kDrawSegEntries);
+    if (e1 > e0)
+      bulk_prefetch_l2((threadIdx.x ? rd : rt) + e0 * kEl, (uint32_t)((e1 - e0) * kEl));
+  }
   __shared__ uint64_t s_wtot[kWarps];
   __shared__ int s_tok;
   const uint64_t wt =
@@ -829,8 +853,8 @@ k_alpha(const void* __restrict__ zt, const void* __restrict__ zd, int gamma, int
   const float c = log2_scale(inv_temperature(T));
   const RowStat rs_t = rowstat[(int64_t)b * R1 + i];
   const RowStat rs_d = rowstat[(int64_t)b * R1 + gamma + 1 + i];
-  const float it = (rs_t.s > 0.0) ? (float)(1.0 / rs_t.s) : 0.0f;
-  const float id = (rs_d.s > 0.0) ? (float)(1.0 / rs_d.s) : 0.0f;
+  const float it = (rs_t.s > 0.0f) ? 1.0f / rs_t.s : 0.0f;
+  const float id = (rs_d.s > 0.0f) ? 1.0f / rs_d.s : 0.0f;
   const char* rt = row_ptr<DT>(zt, zd, b, i, gamma, V);
   const char* rd = row_ptr<DT>(zt, zd, b, gamma + 1 + i, gamma, V);
   const int64_t lo = (int64_t)split * kChunkSweep, hi = min(V, lo + kChunkSweep);
@@ -885,13 +909,9 @@ static size_t topp_smem_bytes(int dtype) {
 
 template <int DT, bool TOPK>
 static cudaError_t sweep_setup(DeviceInfo& d) {
-  const int smem = (int)sweep_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(k_sweep_tma<DT, TOPK>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sweep_ctas_per_sm[DT][TOPK ? 1 : 0],
-                                                       k_sweep_tma<DT, TOPK>, kSweepWarps * 32,
-                                                       smem);
+                                                       k_sweep_vec<DT, TOPK>, kSweepWarps * 32,
+                                                       0);
 }
 static std::mutex g_dev_mu;
 static DeviceInfo g_dev[64];
@@ -955,23 +975,26 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   const bool topp = top_p < 1.0f;
   const bool masked = topk || topp;  // the round runs on thresholded rows
   const int tk = masked ? 1 : 0;
-  const bool tma = use_tma_sweep(DT, V) && di->sweep_ctas_per_sm[DT][tk] > 0;
-  const int nch = (int)(tma ? ceil_div(V, tma_chunk_elems(DT)) : ceil_div(V, kChunkSweep));
+  const bool vec_sweep = use_vec_sweep(DT, V) && di->sweep_ctas_per_sm[DT][tk] > 0;
+  // generic sweep: [row][8192-logit split]; vector sweep: one partial per 4 KB block of
+  // the two arrays, then [row][2] edge pieces
+  const int nch = (int)ceil_div(V, kChunkSweep);
   SweepCtx sx{zt, zd, xt, B, gamma, V, temperature, row_T, seed, round, nch, part1, rowstat,
               state, out_tokens, out_counts, out_p, out_q, out_flags, 1.0f / lenience,
-              masked ? thr : nullptr, done};
+              masked ? thr : nullptr, done,
+              vec_sweep ? part1 + vec_sweep_blocks(B, gamma, V) : nullptr};
   auto sweep = [&](bool with_thr, const SweepCtx& ctx) {
-    if (tma) {
+    if (vec_sweep) {
       // one resident wave of warps, chunks dealt round-robin
-      const int64_t nc = (int64_t)B * R1 * nch;
+      const int64_t nc = vec_sweep_blocks(B, gamma, V);
       const int64_t full = (int64_t)di->sms * di->sweep_ctas_per_sm[DT][with_thr ? 1 : 0];
       const int64_t need = ceil_div(nc, kSweepWarps);
       const int64_t g = full < need ? full : need;
       const dim3 grid((unsigned)(g < 1 ? 1 : g));
       if (with_thr)
-        k_sweep_tma<DT, true><<<grid, kSweepWarps * 32, sweep_smem_bytes(), stream>>>(ctx);
+        k_sweep_vec<DT, true><<<grid, kSweepWarps * 32, 0, stream>>>(ctx);
       else
-        k_sweep_tma<DT, false><<<grid, kSweepWarps * 32, sweep_smem_bytes(), stream>>>(ctx);
+        k_sweep_vec<DT, false><<<grid, kSweepWarps * 32, 0, stream>>>(ctx);
     } else {
       const dim3 grid((unsigned)((int64_t)nch * B * R1));
       if (with_thr)

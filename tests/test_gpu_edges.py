@@ -154,3 +154,29 @@ def test_misaligned_pointer_rejected():
     with pytest.raises(sv.SpecVerifyError) as e:
         sv.spec_verify(zt_mis, zd, xt)
     assert e.value.status == -3
+
+
+@pytest.mark.parametrize("V,dtype", [(131072, torch.bfloat16), (131080, torch.bfloat16),
+                                     (262147, torch.float32)])
+def test_large_vocab_search_levels(V, dtype):
+    """Rows of at most 512 draw segments are searched in one round; longer rows go
+    through the per-CTA totals first (and a ragged tail)."""
+    zt, zd, xt = rand_case(V, B=8, g=2, dtype=dtype, seed=V % 1000)
+    for r in range(3):
+        g, o = both(zt, zd, xt, seed=5, rnd=r)
+        assert_parity(g, o, 2, what=f"V={V} {dtype} round {r}")
+
+
+def test_forced_empty_residual_long_row():
+    """The empty-residual fallback on a row longer than one search round."""
+    V, B = 140000, 4
+    gen = torch.Generator(device="cuda").manual_seed(3)
+    row = torch.randn(V, generator=gen, device="cuda")
+    row[11] = float("-inf")
+    zt = row.expand(B, 2, V).contiguous()
+    zd = row.expand(B, 1, V).contiguous()
+    xt = torch.full((B, 1), 11, dtype=torch.int32, device="cuda")
+    for r in range(2):
+        g, o = both(zt, zd, xt, seed=8, rnd=r)
+        assert_parity(g, o, 1, what=f"forced empty residual, V={V}")
+        assert np.all(g["flags"] & sv.FLAG_RESIDUAL_FALLBACK)
