@@ -26,8 +26,10 @@
  * inverse transform: the smallest v, in vocabulary order, whose cumulative weight
  * exceeds U times the total weight (weights max(0, p_n - q_n), or p_n, formed
  * and summed in fp32 and fp64 on the GPU: the interval ends are exact up to
- * about 1e-6 of the total).  Same inputs and (seed, round) give the same outputs
- * on any stream, launch shape or GPU.
+ * about 1e-6 of the total).  Same inputs at the same addresses and (seed, round)
+ * give the same outputs on any stream, launch shape or GPU (the row sums are
+ * split along 4 KB blocks of memory, so a copy at another address may round
+ * their last bits differently).
  *
  * Conventions for every entry point:
  *   - All array arguments are DEVICE pointers, row-major and contiguous; the caller

@@ -180,3 +180,23 @@ def test_forced_empty_residual_long_row():
         g, o = both(zt, zd, xt, seed=8, rnd=r)
         assert_parity(g, o, 1, what=f"forced empty residual, V={V}")
         assert np.all(g["flags"] & sv.FLAG_RESIDUAL_FALLBACK)
+
+
+@pytest.mark.parametrize("dtype,off_t,off_d", [(torch.bfloat16, 8, 24), (torch.bfloat16, 2040, 8),
+                                               (torch.float32, 4, 1020)])
+def test_logits_not_block_aligned(dtype, off_t, off_d):
+    """Logit arrays that start inside a 4 KB block of memory (16-byte aligned views):
+    the sweep's blocks are aligned to memory, so every row's head and tail pieces
+    fall elsewhere in its blocks."""
+    B, g, V = 8, 3, 6000
+    zt0, zd0, xt = rand_case(V, B=B, g=g, dtype=dtype, seed=off_t + off_d)
+    bt = torch.empty(zt0.numel() + off_t, dtype=dtype, device="cuda")
+    bd = torch.empty(zd0.numel() + off_d, dtype=dtype, device="cuda")
+    zt = bt[off_t:].view(zt0.shape)
+    zd = bd[off_d:].view(zd0.shape)
+    zt.copy_(zt0)
+    zd.copy_(zd0)
+    assert zt.data_ptr() % 4096 != 0 and zt.data_ptr() % 16 == 0
+    for r in range(3):
+        gg, o = both(zt, zd, xt, seed=3, rnd=r, want_alpha=(r == 0))
+        assert_parity(gg, o, g, what=f"offsets {off_t}/{off_d} {dtype} round {r}")
