@@ -577,7 +577,6 @@ __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int 
   constexpr int kWarps = kThreads / 32;
   constexpr int kPasses = (DT == SV_BF16) ? 2 : 4;
   constexpr int kMaxBins = (DT == SV_BF16) ? 1024 : 256;
-  constexpr double kFix = 1099511627776.0;  // 2^40
   extern __shared__ unsigned long long hist64[];  // [kMaxBins] combined, then parts
   __shared__ RowStat s_rs;
   __shared__ uint32_t s_sel[2];       // prefix, no-cut flag
@@ -621,7 +620,9 @@ __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int 
       const uint32_t key = fkey(z);
       if ((key & mask) != prefix) return;
       const float m = ex2(fmaf(z, c, -mc));  // <= 1
-      const unsigned long long f = __float2ull_rn(m * (float)kFix);
+      // m 2^40 rounded to the nearest integer (ties to even), from the float's bits: the
+      // conversion instruction to a 64-bit integer runs on the slow fp64 pipe
+      const unsigned long long f = to_fix(m, 40);
       const uint32_t d = (key >> shift) & dmask;
       atomicAdd(&h0[d], (uint32_t)(f & 0x3FFFu));
       atomicAdd(&h1[d], (uint32_t)((f >> 14) & 0x3FFFu));
