@@ -768,15 +768,6 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
   const char* rd = resid ? row_ptr<DT>(a.zt, a.zd, b, gamma + 1 + st.pos, gamma, V) : nullptr;
   uint64_t* seg = a.segsum + (int64_t)b * a.nseg;
   const int s0 = split * a.spc, s1 = min(a.nseg, s0 + a.spc);
-  if (a.vec && threadIdx.x < 2 && (threadIdx.x == 0 || resid)) {
-    // the slice's bytes of each row it reads, requested from HBM at once so that the
-    // warps' later segments find them in L2
-    constexpr int64_t kEl = (DT == SV_F32) ? 4 : 2;
-    const int64_t e0 = (int64_t)s0 * kDrawSegEntries;
-    const int64_t e1 = min(V, (int64_t)s1 * kDrawSegEntries);
-    if (e1 > e0)
-      bulk_prefetch_l2((threadIdx.x ? rd : rt) + e0 * kEl, (uint32_t)((e1 - e0) * kEl));
-  }
   __shared__ uint64_t s_wtot[kWarps];
   __shared__ int s_tok;
   const uint64_t wt =

@@ -1,5 +1,6 @@
-// sv_tma.cuh -- bulk asynchronous copies (TMA, non-tensor) and mbarriers, as
-// inline PTX for sm_103a.
+// sv_tma.cuh -- mbarriers, async-proxy fences, an ordered atomic and the
+// programmatic-dependent-launch controls, as inline PTX for sm_103a (the tensor
+// copies that use the mbarriers are in sv_umma.cuh).
 #pragma once
 
 #include <cstdint>
@@ -52,24 +53,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
-// Global -> shared bulk copy of `bytes` (multiple of 16, both addresses 16-byte
-// aligned), completing `bytes` of transaction count on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                        uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 
 // Release/acquire atomic add at GPU scope: orders this thread's earlier writes
 // before the add and later reads after it, without a full fence.
-// Ask for `bytes` (a multiple of 16, 16-byte aligned source) to be brought into L2,
-// without waiting for them.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 __device__ __forceinline__ uint32_t atom_add_acqrel_gpu(uint32_t* p, uint32_t v) {
   uint32_t old;
