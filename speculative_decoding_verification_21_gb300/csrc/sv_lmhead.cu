@@ -27,10 +27,11 @@
 //                memory.  The compact rows are copied into the row tile twice
 //                (B <= 64) so that two lane quadrants share the epilogue: per
 //                16-entry chunk the fp32 sums of the draw weights (residual
-//                max(0, p_n - q_n) and p_n), and the chunk's logits.
+//                max(0, p_n - q_n) and p_n).
 //   k_lm_merge   one CTA per compact row: the token by the inverse transform
-//                (sv_draw.cuh) from the chunk sums and the stored logits of
-//                the one chunk it lands in; p_n for an empty residual; emit.
+//                (sv_draw.cuh) from the chunk sums, and the 16 logits of the
+//                one chunk it lands in recomputed from h and W; p_n for an
+//                empty residual; emit.
 //
 // Draft sampling (spec_lmhead_draft) is a third use of the GEMM (k_lm<3>) with
 // Gumbel-max keys y_v - log2(-log2 u_v), y = z / T * log2 e, on Philox tag 2.
@@ -94,8 +95,8 @@ struct LmArgs {
   int nchunk;          // pass 2: 16-entry chunks per row, ceil(V / 16)
   float* csum_r;       // pass 2: [B][nchunk] residual weight sums per compact row
   float* csum_p;       // pass 2: [B][nchunk] p_n weight sums per compact row
-  float* lz_t;         // pass 2: [B][V] target logits of the compact rows
-  float* lz_d;         // pass 2: [B][V] draft logits of the compact rows (residual rows)
+  const uint16_t* W_t;  // merge: the weights, for the 16 logits of one chunk
+  const uint16_t* W_d;
   uint64_t* tsum_r;    // pass 2: [B][nvt] residual weight per vocabulary tile (fixed point)
   uint64_t* tsum_p;    // pass 2: [B][nvt] p_n weight per vocabulary tile (zeroed by finish)
   uint64_t* gsum_r;    // pass 2: [B][ngrp] the same per group of 32 tiles
@@ -484,10 +485,9 @@ __device__ __forceinline__ P2Slice pass2_slice(const LmArgs& a, int quad, int ha
 // Pass-2 epilogue of one job (compact rows; target at column 0, draft at 128):
 // for every 16-column chunk of this thread's row and column slice, the fp32
 // sums (added in order) of the draw weights -- p_n, and for a residual row
-// max(0, p_n - q_n) -- and the logits themselves, from which the merge
-// recomputes the weights of the one chunk it walks (the same bits).  Each
-// chunk sum is also added, in fixed point, to its vocabulary tile's total and
-// to its group's (32 tiles) total (integer atomics: exact in any order).
+// max(0, p_n - q_n).  Each chunk sum is also added, in fixed point, to its
+// vocabulary tile's total and to its group's (32 tiles) total (integer atomics:
+// exact in any order).  No logit leaves the tensor memory.
 __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t tacc, int quad,
                                                int half, int rows) {
   const int lane = threadIdx.x & 31;
@@ -531,15 +531,6 @@ __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t 
         const uint64_t fr = to_fix(sr, a.fsh);
         atomicAdd(reinterpret_cast<unsigned long long*>(a.tsum_r + ti), fr);
         atomicAdd(reinterpret_cast<unsigned long long*>(a.gsum_r + gi), fr);
-      }
-      float4* pt = reinterpret_cast<float4*>(a.lz_t + (int64_t)r * V + vb);  // V % 8 == 0
-      float4* pd = reinterpret_cast<float4*>(a.lz_d + (int64_t)r * V + vb);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (vb + 4 * q < V) {
-          pt[q] = make_float4(zt[4 * q], zt[4 * q + 1], zt[4 * q + 2], zt[4 * q + 3]);
-          if (resid) pd[q] = make_float4(zd[4 * q], zd[4 * q + 1], zd[4 * q + 2], zd[4 * q + 3]);
-        }
       }
     }
   }
@@ -979,14 +970,21 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// k_lm_merge: one warp per compact row.  The token by the inverse transform
-// from the pass-2 sums: the group of 32 vocabulary tiles holding t = floor(U W)
-// (fixed point), the tile, the 16-entry chunk, then the entry from the stored
-// logits; the residual's fallback to p_n when it has no positive weight.
+// k_lm_merge: one CTA per compact row.  The token by the inverse transform
+// from the pass-2 sums: warp 0 finds the group of 32 vocabulary tiles holding
+// t = floor(U W) (fixed point), the tile and the 16-entry chunk; the CTA then
+// recomputes that chunk's 16 logits from the compact hidden rows and the
+// weights (fp32 sums over the hidden dimension on the CUDA cores, so their last
+// bits may differ from the tensor cores': where U W falls within that rounding
+// of an entry's edge the last positive entry of the chunk is taken), and the
+// entry follows.  The residual's fallback to p_n when it has no positive weight.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(32) k_lm_merge(LmArgs a) {
+__global__ void __launch_bounds__(1024) k_lm_merge(LmArgs a) {
   const int slot = blockIdx.x;
-  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ int s_c, s_fl, s_resid;
+  __shared__ uint64_t s_trel;
+  __shared__ float s_z[2][32][16];
   pdl_wait();
   const int rows = (int)*reinterpret_cast<volatile uint32_t*>(a.ctl);
   if (slot >= rows) return;
@@ -994,60 +992,137 @@ __global__ void __launch_bounds__(32) k_lm_merge(LmArgs a) {
   const int b = a.slot_b[slot];
   const DrawState st = a.state[b];
   const int V = a.V;
-  int fl = st.flags;
-  int tk = -1;
-  if (err) {
-    fl |= SV_FLAG_TIMEOUT | SV_FLAG_NONFINITE;
-  } else {
-    const uint64_t k53 = draw_uniform53(a.seed, (uint32_t)st.pos, (uint32_t)b, a.round);
+  if (warp == 0) {
+    int fl = st.flags;
+    int c = -1;
+    uint64_t trel = 0;
     bool resid = st.mode == kDrawResidual;
-    const int64_t go = (int64_t)slot * a.ngrp;
-    uint64_t W = warp_total((resid ? a.gsum_r : a.gsum_p) + go, a.ngrp);
-    if (resid && W == 0) {
-      // the residual had no positive entry in floating point: draw from p_n itself
-      fl |= SV_FLAG_RESIDUAL_FALLBACK;
-      resid = false;
-      W = warp_total(a.gsum_p + go, a.ngrp);
-    }
-    if (W > 0) {
-      const uint64_t t = scale_fix(k53, W);  // < W
-      uint64_t base = 0;
-      const int g = warp_find<2>((resid ? a.gsum_r : a.gsum_p) + go, a.ngrp, t, 0ull, &base);
-      const int t0 = 32 * g;
-      const int tl = t0 + warp_find<1>((resid ? a.tsum_r : a.tsum_p) + (int64_t)slot * a.nvt + t0,
-                                       min(32, a.nvt - t0), t, base, &base);
-      // the chunk of the tile: its fixed-point sums add up to the tile's
-      const float* cs = (resid ? a.csum_r : a.csum_p) + (int64_t)slot * a.nchunk;
-      const int c0 = tl * (kLmTileN / 16), nc = min(a.nchunk - c0, kLmTileN / 16);
-      const uint64_t x = (lane < nc) ? to_fix(__ldcg(cs + c0 + lane), a.fsh) : 0ull;
-      uint64_t P = x;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint64_t y = __shfl_up_sync(0xffffffffu, P, o);
-        if (lane >= o) P += y;
+    if (err) {
+      fl |= SV_FLAG_TIMEOUT | SV_FLAG_NONFINITE;
+    } else {
+      const uint64_t k53 = draw_uniform53(a.seed, (uint32_t)st.pos, (uint32_t)b, a.round);
+      const int64_t go = (int64_t)slot * a.ngrp;
+      uint64_t W = warp_total((resid ? a.gsum_r : a.gsum_p) + go, a.ngrp);
+      if (resid && W == 0) {
+        // the residual had no positive entry in floating point: draw from p_n itself
+        fl |= SV_FLAG_RESIDUAL_FALLBACK;
+        resid = false;
+        W = warp_total(a.gsum_p + go, a.ngrp);
       }
-      const unsigned hit = __ballot_sync(0xffffffffu, base + P > t);
-      const int c = __ffs((int)hit) - 1;
-      if (lane == c) {
-        const int vb = (c0 + c) * 16;
-        const float* zt = a.lz_t + (int64_t)slot * V + vb;
-        const float* zd = a.lz_d + (int64_t)slot * V + vb;
-        const float kd = __fsub_rn(st.K, st.mct);
-        float w[16];
+      if (W > 0) {
+        const uint64_t t = scale_fix(k53, W);  // < W
+        uint64_t base = 0;
+        const int g = warp_find<2>((resid ? a.gsum_r : a.gsum_p) + go, a.ngrp, t, 0ull, &base);
+        const int t0 = 32 * g;
+        const int tl = t0 + warp_find<1>((resid ? a.tsum_r : a.tsum_p) + (int64_t)slot * a.nvt + t0,
+                                         min(32, a.nvt - t0), t, base, &base);
+        // the chunk of the tile: its fixed-point sums add up to the tile's
+        const float* cs = (resid ? a.csum_r : a.csum_p) + (int64_t)slot * a.nchunk;
+        const int c0 = tl * (kLmTileN / 16), nc = min(a.nchunk - c0, kLmTileN / 16);
+        const uint64_t x = (lane < nc) ? to_fix(__ldcg(cs + c0 + lane), a.fsh) : 0ull;
+        uint64_t P = x;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const bool in = vb + e < V;
-          const float zv = in ? __ldcg(zt + e) : -kInf;
-          w[e] = resid ? draw_weight<true, false>(zv, in ? __ldcg(zd + e) : -kInf, st, kd)
-                       : draw_weight<false, false>(zv, 0.0f, st, kd);
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint64_t y = __shfl_up_sync(0xffffffffu, P, o);
+          if (lane >= o) P += y;
         }
-        const int e = pick_in_run<16>(w, 0ull, t - (base + P - x), a.fsh);
-        tk = e >= 0 ? vb + e : -1;
+        const unsigned hit = __ballot_sync(0xffffffffu, base + P > t);
+        const int l = __ffs((int)hit) - 1;
+        if (l >= 0) {
+          c = c0 + l;
+          trel = t - (base + __shfl_sync(0xffffffffu, P - x, l));
+        }
       }
-      tk = __shfl_sync(0xffffffffu, tk, c < 0 ? 0 : c);
+    }
+    if (lane == 0) {
+      s_c = c;
+      s_trel = trel;
+      s_fl = fl;
+      s_resid = resid ? 1 : 0;
     }
   }
-  if (lane != 0) return;
+  __syncthreads();
+  const int c = s_c;
+  int tk = -1;
+  if (c >= 0) {
+    // the chunk's logits: thread t sums hidden entries t, t + 1024, ... for the 16
+    // columns (the target row, and for a residual the draft row)
+    const int vb = c * 16;
+    const bool resid = s_resid != 0;
+    for (int side = 0; side < (resid ? 2 : 1); ++side) {
+      const uint16_t* h = side ? a.c_d + (int64_t)slot * a.Hd : a.c_t + (int64_t)slot * a.Ht;
+      const uint16_t* Wm = side ? a.W_d : a.W_t;
+      const int H = side ? a.Hd : a.Ht;
+      float acc[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
+      constexpr int kU = 4;  // hidden entries per thread and round: their loads in flight together
+      for (int k0 = tid; k0 < H; k0 += kU * (int)blockDim.x) {
+        uint4 w0[kU], w1[kU];
+        float hk[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int k = k0 + u * (int)blockDim.x;
+          hk[u] = 0.0f;
+          w0[u] = w1[u] = make_uint4(0u, 0u, 0u, 0u);
+          if (k < H) {
+            hk[u] = __uint_as_float((uint32_t)__ldcg(h + k) << 16);
+            const uint4* wr = reinterpret_cast<const uint4*>(Wm + (int64_t)k * V + vb);  // V % 8 == 0
+            // a last chunk may hold 8 entries (V % 16 == 8): nothing past the row is read
+            w0[u] = __ldg(wr);
+            if (vb + 8 < V) w1[u] = __ldg(wr + 1);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const uint32_t ww[8] = {w0[u].x, w0[u].y, w0[u].z, w0[u].w,
+                                  w1[u].x, w1[u].y, w1[u].z, w1[u].w};
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            acc[2 * q] = fmaf(hk[u], bf16lo(ww[q]), acc[2 * q]);
+            acc[2 * q + 1] = fmaf(hk[u], bf16hi(ww[q]), acc[2 * q + 1]);
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) s_z[side][warp][e] = acc[e];
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const float kd = __fsub_rn(st.K, st.mct);
+      float w[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float zt = 0.0f, zd = 0.0f;
+        for (int q = 0; q < (int)(blockDim.x >> 5); ++q) {
+          zt += s_z[0][q][e];
+          if (resid) zd += s_z[1][q][e];
+        }
+        const bool in = vb + e < V;
+        w[e] = !in ? 0.0f
+                   : (resid ? draw_weight<true, false>(zt, zd, st, kd)
+                            : draw_weight<false, false>(zt, 0.0f, st, kd));
+      }
+      int e = pick_in_run<16>(w, 0ull, s_trel, a.fsh);
+      if (e < 0) {  // rounding put U W past the recomputed chunk: its last positive entry
+        for (int q = 15; q >= 0; --q)
+          if (w[q] > 0.0f) {
+            e = q;
+            break;
+          }
+      }
+      tk = e >= 0 ? vb + e : -1;
+    }
+  }
+  if (tid != 0) return;
+  int fl = s_fl;
   if (tk < 0 || tk >= V) {
     tk = 0;
     if (!err) fl |= SV_FLAG_ZERO_MASS;
@@ -1266,8 +1341,8 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   a.nchunk = (int)ceil_div(V, 16);
   a.csum_r = reinterpret_cast<float*>(ws + pl.off_csr);
   a.csum_p = reinterpret_cast<float*>(ws + pl.off_csp);
-  a.lz_t = reinterpret_cast<float*>(ws + pl.off_lzt);
-  a.lz_d = reinterpret_cast<float*>(ws + pl.off_lzd);
+  a.W_t = reinterpret_cast<const uint16_t*>(W_target);
+  a.W_d = reinterpret_cast<const uint16_t*>(W_draft);
   a.tsum_r = reinterpret_cast<uint64_t*>(ws + pl.off_tsr);
   a.tsum_p = reinterpret_cast<uint64_t*>(ws + pl.off_tsp);
   a.ngrp = (pl.nvt + 31) / 32;
@@ -1336,7 +1411,7 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   e = launch_pdl(k_lm<2>, dim3(grid), dim3(kLmThreads), smem2, stream, cT, WT, cD, WD, a2);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   mark(3, stream);
-  e = launch_pdl(k_lm_merge, dim3((unsigned)B), dim3(32), 0, stream, a);
+  e = launch_pdl(k_lm_merge, dim3((unsigned)B), dim3(1024), 0, stream, a);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   mark(4, stream);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;

@@ -150,7 +150,7 @@ struct LmPlan {
   int nvt = 0;  // vocabulary tiles
   // ctl: [0] compact-row count, [1] pass-1 error, [2] pass-2 error (zeroed per call)
   size_t off_ctl = 0, off_part = 0, off_zat = 0, off_state = 0, off_slot = 0,
-         off_csr = 0, off_csp = 0, off_lzt = 0, off_lzd = 0, off_tsr = 0, off_tsp = 0,
+         off_csr = 0, off_csp = 0, off_tsr = 0, off_tsp = 0,
          off_gsr = 0, off_gsp = 0, off_ct = 0, off_cd = 0, total = 0;
 };
 
@@ -168,12 +168,10 @@ inline LmPlan make_lm_plan(int B, int gamma, int64_t V) {
   p.off_zat = o;    o = align_up(o + sizeof(float) * rows);
   p.off_state = o;  o = align_up(o + sizeof(DrawState) * (size_t)B);
   p.off_slot = o;   o = align_up(o + sizeof(int) * (size_t)B);
-  // the draw: weight sums per 16-entry chunk and the logits of each compact row
+  // the draw: weight sums per 16-entry chunk, per tile and per group of 32 tiles
   const size_t nchunk = (size_t)ceil_div(V, 16);
   p.off_csr = o;    o = align_up(o + sizeof(float) * (size_t)B * nchunk);
   p.off_csp = o;    o = align_up(o + sizeof(float) * (size_t)B * nchunk);
-  p.off_lzt = o;    o = align_up(o + sizeof(float) * (size_t)B * (size_t)V);
-  p.off_lzd = o;    o = align_up(o + sizeof(float) * (size_t)B * (size_t)V);
   p.off_tsr = o;    o = align_up(o + sizeof(uint64_t) * (size_t)B * p.nvt);
   p.off_tsp = o;    o = align_up(o + sizeof(uint64_t) * (size_t)B * p.nvt);
   p.off_gsr = o;    o = align_up(o + sizeof(uint64_t) * (size_t)B * ((p.nvt + 31) / 32));
