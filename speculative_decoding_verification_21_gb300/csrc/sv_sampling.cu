@@ -565,18 +565,25 @@ __global__ void __launch_bounds__(kThreads) k_topk_cand(SweepCtx x, int k,
 // top_p of the row's mass.  One CTA per row, after a sweep that gave the row's
 // max; entries below the row's top-k threshold (thr on entry, when has_k) do
 // not count.  Masses 2^(z c - max) are summed as 40-bit fixed point, so the
-// sums are exact and independent of order, by most-significant-digit passes
-// over order-preserving keys (bf16: digits of 10 and 6 bits; fp32: four of 8).
-// Each mass goes in three 14-bit parts to three 32-bit per-warp histograms
-// (native shared-memory atomics; a warp adds at most 2^18 entries, so no part
-// overflows for V <= 2^21), combined in 64 bits per digit afterwards.  Empty or
-// non-finite rows keep thr as it was.
+// sums are exact and independent of order.  The first pass bins every entry
+// by its log2 mass, z c - max, in steps of 1/32 (1024 bins; masses below 2^-32
+// share the lowest), a digit that never decreases as z grows and that spreads
+// the logits over hundreds of bins (bins over the float's leading bits would
+// crowd them into a few exponents, and lanes adding to one counter serialise).
+// Most-significant-digit passes over order-preserving keys (bf16: digits of 10
+// and 6 bits; fp32: four of 8) then refine among the entries of the chosen
+// mass bin only: every entry of a higher bin has a larger logit than all of
+// them, every entry of a lower bin a smaller one, so the cut is the same as a
+// select over the keys of the whole row.  Each mass goes in three 14-bit parts
+// to three 32-bit per-warp histograms (native shared-memory atomics; a warp
+// adds at most 2^18 entries, so no part overflows for V <= 2^21), combined in
+// 64 bits per digit afterwards.  Empty or non-finite rows keep thr as it was.  Empty or non-finite rows keep thr as it was.
 template <int DT>
 __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int has_k,
                                                   float* __restrict__ thr) {
   constexpr int kWarps = kThreads / 32;
-  constexpr int kPasses = (DT == SV_BF16) ? 2 : 4;
-  constexpr int kMaxBins = (DT == SV_BF16) ? 1024 : 256;
+  constexpr int kPasses = 1 + ((DT == SV_BF16) ? 2 : 4);
+  constexpr int kMaxBins = 1024;
   extern __shared__ unsigned long long hist64[];  // [kMaxBins] combined, then parts
   __shared__ RowStat s_rs;
   __shared__ uint32_t s_sel[2];       // prefix, no-cut flag
@@ -601,12 +608,16 @@ __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int 
       !(fabsf(rs.mc) < kInf))
     return;  // empty or not finite: no cut (uniform over the CTA)
   const float mc = rs.mc;
-  uint32_t prefix = 0, mask = 0;
+  // mass bin of an entry from its scaled logit u = z c - max (<= 0 up to rounding)
+  auto mass_bin = [](float u) -> uint32_t {
+    return 1023u - (uint32_t)fminf(fmaxf(-32.0f * u, 0.0f), 1023.0f);
+  };
+  uint32_t bin0 = 0, prefix = 0, mask = 0;
   int shift = 32;
   double target = 0.0;  // fixed-point mass still to reach inside the current prefix
   for (int pass = 0; pass < kPasses; ++pass) {
-    const int width = (DT == SV_BF16) ? (pass == 0 ? 10 : 6) : 8;
-    shift -= width;
+    const int width = pass == 0 ? 10 : (DT == SV_BF16) ? (pass == 1 ? 10 : 6) : 8;
+    if (pass > 0) shift -= width;
     const uint32_t dmask = (1u << width) - 1u;
     const int nbins = 1 << width;
     uint32_t* parts = reinterpret_cast<uint32_t*>(hist64 + kMaxBins);  // [3][kWarps][kMaxBins]
@@ -617,13 +628,18 @@ __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int 
     uint32_t* h2 = h1 + kWarps * kMaxBins;
     auto add = [&](float z) {
       if (!(z >= tk)) return;  // NaN, or below the top-k threshold
-      const uint32_t key = fkey(z);
-      if ((key & mask) != prefix) return;
-      const float m = ex2(fmaf(z, c, -mc));  // <= 1
+      const float u = fmaf(z, c, -mc);
+      const uint32_t mb = mass_bin(u);
+      uint32_t d = mb;
+      if (pass > 0) {
+        const uint32_t key = fkey(z);
+        if (mb != bin0 || (key & mask) != prefix) return;
+        d = (key >> shift) & dmask;
+      }
+      const float m = ex2(u);  // <= 1
       // m 2^40 rounded to the nearest integer (ties to even), from the float's bits: the
       // conversion instruction to a 64-bit integer runs on the slow fp64 pipe
       const unsigned long long f = to_fix(m, 40);
-      const uint32_t d = (key >> shift) & dmask;
       atomicAdd(&h0[d], (uint32_t)(f & 0x3FFFu));
       atomicAdd(&h1[d], (uint32_t)((f >> 14) & 0x3FFFu));
       atomicAdd(&h2[d], (uint32_t)(f >> 28));
@@ -680,16 +696,20 @@ __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int 
           if ((double)(above + n) >= target) break;
           above += n;
         }
-        s_sel[0] = prefix | ((uint32_t)d << shift);
+        s_sel[0] = (uint32_t)d;
         s_sel[1] = 0u;
         s_target = target - (double)above;
       }
     }
     __syncthreads();
     if (s_sel[1]) return;  // keep thr as it was
-    prefix = s_sel[0];
+    if (pass == 0) {
+      bin0 = s_sel[0];
+    } else {
+      prefix |= s_sel[0] << shift;
+      mask |= dmask << shift;
+    }
     target = s_target;
-    mask |= dmask << shift;
     __syncthreads();
   }
   if (threadIdx.x == 0) {
@@ -893,9 +913,9 @@ struct DeviceInfo {
 };
 
 // Dynamic shared memory of k_topp: the combined 64-bit histogram, then three
-// 32-bit per-warp histograms of the mass parts.
-static size_t topp_smem_bytes(int dtype) {
-  const size_t bins = dtype == SV_BF16 ? 1024 : 256;
+// 32-bit per-warp histograms of the mass parts (1024 bins: the widest digit).
+static size_t topp_smem_bytes() {
+  const size_t bins = 1024;
   return bins * sizeof(unsigned long long) + 3 * (size_t)(kThreads / 32) * bins * sizeof(uint32_t);
 }
 
@@ -919,7 +939,10 @@ static cudaError_t device_info(DeviceInfo** out) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_topp<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)topp_smem_bytes(SV_BF16));
+                             (int)topp_smem_bytes());
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_topp<SV_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)topp_smem_bytes());
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_topk_cand<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)topk_cand_smem_bytes(SV_BF16));
@@ -1012,7 +1035,7 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
     SweepCtx s0 = sx;
     s0.thr = topk ? thr : nullptr;
     sweep(topk, s0);
-    k_topp<DT><<<(unsigned)((int64_t)B * R1), kThreads, topp_smem_bytes(DT), stream>>>(
+    k_topp<DT><<<(unsigned)((int64_t)B * R1), kThreads, topp_smem_bytes(), stream>>>(
         sx, top_p, topk ? 1 : 0, thr);
   }
   if (!(topk && !topp)) {
