@@ -1095,21 +1095,23 @@ __global__ void __launch_bounds__(1024) k_lm_merge(LmArgs a) {
       }
     }
     __syncthreads();
-    if (tid == 0) {
+    if (warp == 0) {
+      // lane e sums entry e of the target row over the warps in order, lane 16 + e that of
+      // the draft row; lane e then forms weight e, and lane 0 picks from all 16
+      const int e16 = lane & 15, side = lane >> 4;
+      float z = 0.0f;
+      if (side == 0 || resid)
+        for (int q = 0; q < (int)(blockDim.x >> 5); ++q) z += s_z[side][q][e16];
+      const float zd = __shfl_sync(0xffffffffu, z, 16 + e16);
       const float kd = __fsub_rn(st.K, st.mct);
+      const bool in = side == 0 && vb + e16 < V;
+      const float wl = !in ? 0.0f
+                           : (resid ? draw_weight<true, false>(z, zd, st, kd)
+                                    : draw_weight<false, false>(z, 0.0f, st, kd));
       float w[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        float zt = 0.0f, zd = 0.0f;
-        for (int q = 0; q < (int)(blockDim.x >> 5); ++q) {
-          zt += s_z[0][q][e];
-          if (resid) zd += s_z[1][q][e];
-        }
-        const bool in = vb + e < V;
-        w[e] = !in ? 0.0f
-                   : (resid ? draw_weight<true, false>(zt, zd, st, kd)
-                            : draw_weight<false, false>(zt, 0.0f, st, kd));
-      }
+      for (int q = 0; q < 16; ++q) w[q] = __shfl_sync(0xffffffffu, wl, q);
+      if (lane != 0) return;
       int e = pick_in_run<16>(w, 0ull, s_trel, a.fsh);
       if (e < 0) {  // rounding put U W past the recomputed chunk: its last positive entry
         for (int q = 15; q >= 0; --q)
