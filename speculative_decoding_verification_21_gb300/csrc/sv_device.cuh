@@ -47,20 +47,7 @@ __device__ __forceinline__ float sv_u01(uint32_t x) {
   return __uint2float_rn(2u * (x >> 9) + 1u) * 0x1p-24f;
 }
 
-// E = -ln(u) for u = sv_u01(x), to ~1e-5 relative at worst.  u is built from
-// the bits directly: 1 + m 2^-23 is exact in fp32 and subtracting 1 - 2^-24 is
-// exact, giving (2m+1) 2^-24.  Near u = 1 the logarithm is taken from
-// w = 1 - u (exact) with the series -ln(1-w) = w + w^2/2 + w^3/3 + ...;
-// elsewhere from the hardware log2.
-__device__ __forceinline__ float sv_neglog_u(uint32_t x) {
-  const float u = __uint_as_float(0x3f800000u | (x >> 9)) - 0x1.fffffep-1f;
-  const float w = 1.0f - u;
-  const float series = w * fmaf(w, fmaf(w, 1.0f / 3.0f, 0.5f), 1.0f);
-  const float viaLog = -__log2f(u) * kLn2;
-  return (w < 0x1p-8f) ? series : viaLog;
-}
-
-// Exact-ish double version used where a decision is refined (same definition).
+// E = -ln(u) for u = sv_u01(x) in double, where a decision is refined.
 __device__ __forceinline__ double sv_neglog_u_f64(uint32_t x) {
   const double u = (2.0 * (double)(x >> 9) + 1.0) * 0x1p-24;
   return -log(u);
@@ -204,12 +191,6 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-__device__ __forceinline__ double warp_sum_f64(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 // (key, index) with "larger key wins, lower index wins ties".
 struct KI {
   float k;
@@ -218,39 +199,6 @@ struct KI {
 
 __device__ __forceinline__ bool ki_better(KI a, KI b) {
   return (a.k > b.k) || (a.k == b.k && (unsigned)a.i < (unsigned)b.i);
-}
-
-// Top-2 of (key, index) pairs.
-struct Top2 {
-  KI a, b;
-};
-
-__device__ __forceinline__ Top2 top2_insert(Top2 t, KI x) {
-  if (ki_better(x, t.a)) {
-    t.b = t.a;
-    t.a = x;
-  } else if (ki_better(x, t.b)) {
-    t.b = x;
-  }
-  return t;
-}
-
-__device__ __forceinline__ Top2 top2_merge(Top2 t, Top2 o) {
-  t = top2_insert(t, o.a);
-  return top2_insert(t, o.b);
-}
-
-__device__ __forceinline__ Top2 warp_reduce_top2(Top2 t) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    Top2 w;
-    w.a.k = __shfl_xor_sync(0xffffffffu, t.a.k, o);
-    w.a.i = __shfl_xor_sync(0xffffffffu, t.a.i, o);
-    w.b.k = __shfl_xor_sync(0xffffffffu, t.b.k, o);
-    w.b.i = __shfl_xor_sync(0xffffffffu, t.b.i, o);
-    t = top2_merge(t, w);
-  }
-  return t;
 }
 
 __device__ __forceinline__ KI warp_reduce_ki(KI t) {

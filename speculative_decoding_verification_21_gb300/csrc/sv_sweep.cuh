@@ -1,6 +1,6 @@
 // sv_sweep.cuh -- per-lane and per-warp pieces of the softmax-statistics sweep:
-// online (max, sum of 2^(y - max)) over a 4 KB chunk in shared memory, chunk
-// positions advanced without divisions, and the warp combine.
+// online (max, sum of 2^(y - max)) over a 4 KB block held in registers, and the
+// warp combine.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -13,31 +13,6 @@
 
 namespace sv {
 
-// Sum of 2^(y - my) over one lane's vectors, my = max of its raw logits times c.
-template <int DT>
-__device__ __forceinline__ MS ms_of_vectors(const uint4* v, int nv, float c) {
-  float m = -kInf;
-#pragma unroll
-  for (int u = 0; u < 8; ++u)
-    if (u < nv) m = fmaxf(m, vmax<DT>(v[u]));
-  if (!(m > -kInf)) return MS{-kInf, 0.0f};
-  const float mc = m * c;
-  float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    if (u < nv) {
-      float f[VecInfo<DT>::kElems];
-      unpack<DT>(v[u], f);
-#pragma unroll
-      for (int e = 0; e < VecInfo<DT>::kElems; e += 2) {
-        s0 += ex2(fmaf(f[e], c, -mc));
-        s1 += ex2(fmaf(f[e + 1], c, -mc));
-      }
-    }
-  }
-  return MS{mc, s0 + s1};
-}
-
 // Per-lane online (max, sum) update with a chunk maximum m of raw logits.
 __device__ __forceinline__ void lane_raise_max(float m, float c, float& zmax, float& mc,
                                                float& sacc) {
@@ -49,8 +24,7 @@ __device__ __forceinline__ void lane_raise_max(float m, float c, float& zmax, fl
   }
 }
 
-// One full 4 KB chunk, each lane holding 8 of its 256 vectors (read from the
-// shared-memory stage beforehand, so that the stage can be refilled first).
+// One full 4 KB block, each lane holding 8 of its 256 vectors in registers.
 // The maximum is a packed tree over the raw words, then one exp2 per logit.
 // With TOPK, logits below tau (the row's top-k threshold) add nothing to the sum.
 template <int DT, bool TOPK = false>
@@ -116,30 +90,6 @@ __device__ __forceinline__ void chunk_update_full(const uint4 (&v)[8], float c, 
   unpack2(s01, s0, s1);
   unpack2(s23, s2, s3);
   sacc += (s0 + s1) + (s2 + s3);
-}
-
-// Position of a chunk: batch row b, row k of it, chunk j of the row, advanced
-// by a fixed stride without divisions.
-struct ChunkPos {
-  int b, k, j;
-};
-struct ChunkStep {
-  int db, dk, dj;  // stride W = ((db * R1) + dk) * nch + dj chunks
-};
-__device__ __forceinline__ void advance(ChunkPos& p, const ChunkStep& d, int R1, int nch) {
-  p.j += d.dj;
-  int carry_k = 0;
-  if (p.j >= nch) {
-    p.j -= nch;
-    carry_k = 1;
-  }
-  p.k += d.dk + carry_k;
-  int carry_b = 0;
-  if (p.k >= R1) {
-    p.k -= R1;
-    carry_b = 1;
-  }
-  p.b += d.db + carry_b;
 }
 
 // Warp max of m, then one rescale per lane and a warp sum.

@@ -1,6 +1,6 @@
-// sv_tma.cuh -- mbarriers, async-proxy fences, an ordered atomic and the
-// programmatic-dependent-launch controls, as inline PTX for sm_103a (the tensor
-// copies that use the mbarriers are in sv_umma.cuh).
+// sv_tma.cuh -- mbarriers and the programmatic-dependent-launch controls, as
+// inline PTX for sm_103a (the tensor copies that use the mbarriers are in
+// sv_umma.cuh).
 #pragma once
 
 #include <cstdint>
@@ -19,12 +19,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 // Make mbarrier initialisation visible to the async proxy (the bulk-copy unit).
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-// Order this thread's generic-proxy shared-memory accesses before later
-// async-proxy (bulk copy) accesses of the same memory.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -53,16 +47,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
-
-// Release/acquire atomic add at GPU scope: orders this thread's earlier writes
-// before the add and later reads after it, without a full fence.
-
-__device__ __forceinline__ uint32_t atom_add_acqrel_gpu(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
-               : "memory");
-  return old;
-}
 
 // Programmatic dependent launch: let the next kernel on the stream launch
 // early / wait here until the previous kernel has completed and its writes are

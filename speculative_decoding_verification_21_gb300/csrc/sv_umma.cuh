@@ -114,18 +114,9 @@ __device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t* r) {
       : "r"(taddr));
 }
 
-// 2-D tiled bulk tensor copy global -> shared, completing on an mbarrier.
-// Coordinates are in elements: c0 along the innermost dimension.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// The same copy with an L2 cache policy (see l2_policy_*).
+// 2-D tiled bulk tensor copy global -> shared, completing on an mbarrier, with
+// an L2 cache policy (see l2_policy_*).  Coordinates are in elements: c0 along
+// the innermost dimension.
 __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int c0, int c1,
                                                  uint64_t* bar, uint64_t policy) {
   asm volatile(
