@@ -87,6 +87,12 @@ def test_spec_verify_opts_argument_errors():
     assert _svo(L, lenience=0.5, ws=None) == -4
     assert _svo(L, opts=False, ws=None) == -4
     assert _svo(L, lenience=0.5, B=0) == 0  # nothing to do
+    # nucleus sums are exact for V <= 2^21 only; no workspace, so nothing can launch
+    big = (1 << 21) + 8
+    assert _svo(L, top_p=0.9, V=big, ws=None) == -6
+    assert _svo(L, top_p=0.9, V=1 << 21, ws=None) == -4
+    assert _svo(L, top_p=1.0, V=big, ws=None) == -4
+    assert _svo(L, top_k=50, V=big, ws=None) == -4
 
 
 def test_spec_verify_argument_errors():
