@@ -113,7 +113,7 @@ def uniform(seed, tag, pos, b, rnd, c0, lane) -> float:
 
 
 def draw_uniform(seed, pos, b, rnd) -> float:
-    """The uniform U in [0, 1) (53 bits) of the target's own draw at position pos."""
+    """The uniform U in [0, 1) (53 bits) of the inverse-transform draw at position pos."""
     return lib().svo_draw_uniform(int(seed) & (2**64 - 1), pos, b, int(rnd) & (2**64 - 1))
 
 
@@ -157,11 +157,16 @@ def _dtype_code(a: np.ndarray) -> int:
 class _Options(ctypes.Structure):
     """svo_options (sv_oracle.h)."""
     _fields_ = [("lenience", ctypes.c_double), ("top_k", ctypes.c_int),
-                ("top_p", ctypes.c_double), ("nucleus_gap", ctypes.c_void_p)]
+                ("top_p", ctypes.c_double), ("nucleus_gap", ctypes.c_void_p),
+                ("sampler", ctypes.c_int)]
+
+
+SAMPLERS = {"gumbel": 0, "inverse": 1}
 
 
 def spec_verify(zt, zd, xt, temperature=1.0, row_temperature=None, seed=0, rnd=0,
-                want_beta=False, rows=None, threads=1, lenience=1.0, top_k=0, top_p=1.0):
+                want_beta=False, rows=None, threads=1, lenience=1.0, top_k=0, top_p=1.0,
+                sampler="gumbel"):
     """Sampling verify.  zt [B,g+1,V], zd [B,g,V] (float32 or bf16 bits as uint16),
     xt [B,g] int32.  Returns a dict of numpy arrays.
 
@@ -171,9 +176,13 @@ def spec_verify(zt, zd, xt, temperature=1.0, row_temperature=None, seed=0, rnd=0
     "nucleus_gap" [B] is the smallest distance of top_p from a cut's cumulative
     probabilities in the batch row.
 
-    The target's own token is drawn by the inverse transform; "gap" [B] is the
+    sampler: how the target's own token (residual or bonus) is drawn.  "gumbel"
+    (default): argmax of log w_v + g_v with Gumbel noise from Philox tag 1 at the
+    draw position, ties to the lowest index; "gap" [B] is the top-1 minus top-2
+    key (natural-log units; inf with one candidate, NaN for an empty row).
+    "inverse": the inverse transform with one 53-bit uniform U; "gap" [B] is the
     distance of U W from the nearer end of the drawn token's cumulative interval
-    (probability units; NaN for an empty row).
+    (probability units).
 
     rows: optional list of batch-row indices to compute (others left zero);
     threads: run disjoint row ranges in that many Python threads (each a plain
@@ -193,7 +202,8 @@ def spec_verify(zt, zd, xt, temperature=1.0, row_temperature=None, seed=0, rnd=0
     L = lib()
 
     out["nucleus_gap"] = np.full(B, np.inf)
-    opt = _Options(float(lenience), int(top_k), float(top_p), _ptr(out["nucleus_gap"]))
+    opt = _Options(float(lenience), int(top_k), float(top_p), _ptr(out["nucleus_gap"]),
+                   SAMPLERS[sampler])
 
     def run(b0, b1):
         rc = L.svo_spec_verify_ex(

@@ -26,10 +26,13 @@
  * Readings where the pages are silent (each also listed in the design notes):
  *  - temperature: s = z * fl32(1/T) for target and draft rows alike;
  *  - the accept comparison is "<=", with IEEE p/q (p/0 = inf accepts, 0/0 rejects);
- *  - "sample" the target's own token = inverse transform: one uniform U in [0, 1)
- *    with 53 random bits (Philox4x32-10, tag 1, at the draw position), and the
- *    smallest v, in vocabulary order, whose cumulative weight exceeds U times the
- *    total weight;
+ *  - "sample" the target's own token = Gumbel-max (the default): the argmax over
+ *    the entries of positive weight of log w_v + g_v, g_v = -log(-log u_v), ties
+ *    to the lowest index, with u_v from Philox4x32-10 tag 1 at the draw position
+ *    (counter word 0 = v>>2, output lane v&3).  Opt-in alternative: the inverse
+ *    transform, one uniform U in [0, 1) with 53 random bits (tag 1 at the draw
+ *    position, counter word 0 = 0) and the smallest v, in vocabulary order, whose
+ *    cumulative weight exceeds U times the total weight;
  *  - "sample" a draft token (the draft side) = Gumbel-max argmax(log w_v + g_v),
  *    g = -log(-log u), ties to the lowest index, u from Philox tag 2;
  *  - an all-zero residual (possible only by rounding) falls back to p_n;
@@ -92,7 +95,8 @@ void svo_uniform_row(uint64_t seed, uint32_t tag, uint32_t pos, uint32_t b, uint
   }
 }
 
-/* Gumbel noise for vocabulary entry v at a draft position (tag 2). */
+/* Gumbel noise for vocabulary entry v: tag 1 at the target's draw position, tag 2
+ * at a draft position. */
 static double gumbel_tag(uint64_t seed, uint32_t tag, uint32_t pos, uint32_t b, uint64_t round,
                          int64_t v) {
   double u = svo_uniform(seed, tag, pos, b, round, (uint32_t)(v >> 2), (int)(v & 3));
@@ -259,14 +263,39 @@ static double prob(const row_t* r, int64_t v) {
 
 static int row_nonfinite(const row_t* r) { return !isfinite(r->S) || isnan(r->m) || r->m == INFINITY; }
 
+/* Gumbel-max draw (the default sampler of the target's own token): the argmax
+ * over the entries with w(v) > 0 of log w(v) + g_v, g_v the Gumbel noise of entry
+ * v (tag 1 at position pos), ties to the lowest v.  Returns -1 when no weight is
+ * positive.  *gap is the top-1 key minus the top-2 key (inf with one candidate),
+ * the margin by which the draw was decided. */
+typedef double (*weight_fn)(const void* ctx, int64_t v);
+
+static int64_t gumbel_draw(weight_fn w, const void* ctx, int64_t V, uint64_t seed, uint32_t pos,
+                           uint32_t b, uint64_t round, double* gap) {
+  int64_t best = -1;
+  double k1 = -INFINITY, k2 = -INFINITY;
+  for (int64_t v = 0; v < V; ++v) {
+    double x = w(ctx, v);
+    if (!(x > 0.0) || x == INFINITY) continue;
+    double key = log(x) + gumbel_tag(seed, 1u, pos, b, round, v);
+    if (best < 0 || key > k1) {
+      k2 = k1;
+      k1 = key;
+      best = v;
+    } else if (key > k2) {
+      k2 = key;
+    }
+  }
+  if (gap) *gap = best < 0 ? NAN : k1 - k2;
+  return best;
+}
+
 /* Inverse-transform draw: with W the sum of the weights w(v) >= 0 and
  * C_v = w(0) + ... + w(v), the smallest v with C_v > U W.  Returns -1 when no
  * weight is positive.  *gap is the distance of U W from the nearer end of the
  * chosen entry's interval [C_{v-1}, C_v) (in the weights' units).  When the
  * rounded sums leave U W at or above C_{V-1}, the last positive entry is taken
  * with gap 0. */
-typedef double (*weight_fn)(const void* ctx, int64_t v);
-
 static int64_t inverse_cdf_draw(weight_fn w, const void* ctx, int64_t V, double U, double* gap) {
   double W = 0.0;
   int64_t last = -1;
@@ -351,7 +380,9 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
   const double l = opt ? opt->lenience : 1.0;
   const int top_k = opt ? opt->top_k : 0;
   const double top_p = opt ? opt->top_p : 1.0;
+  const int sampler = opt ? opt->sampler : SVO_SAMPLER_GUMBEL;
   if (!(l > 0.0 && l <= 1.0)) return -1;
+  if (sampler != SVO_SAMPLER_GUMBEL && sampler != SVO_SAMPLER_INVERSE) return -1;
   if (top_k < 0 || !(top_p > 0.0 && top_p <= 1.0)) return -1;
   if (B < 0 || gamma < 1 || gamma > 64 || V < 1 || (dtype != SVO_F32 && dtype != SVO_BF16))
     return -1;
@@ -432,27 +463,33 @@ int svo_spec_verify_ex(const void* zt, const void* zd, const int32_t* xt,
       break;
     }
 
-    /* The target's own token, by the inverse transform with the uniform of position n. */
+    /* The target's own token at position n: Gumbel-max (default) or the inverse
+     * transform with the uniform of position n (opt-in). */
     int64_t t;
     double gap = NAN, rmass = NAN;
     const double Ud = svo_draw_uniform(seed, (uint32_t)n, (uint32_t)b, round);
+#define SVO_DRAW(wfn, ctx)                                                        \
+  (sampler == SVO_SAMPLER_INVERSE ? inverse_cdf_draw((wfn), (ctx), V, Ud, &gap)   \
+                                  : gumbel_draw((wfn), (ctx), V, seed, (uint32_t)n, \
+                                                (uint32_t)b, round, &gap))
     if (n == gamma) {
       /* Clean sweep: bonus token from p_gamma. */
-      t = inverse_cdf_draw(weight_prob, &rows[gamma], V, Ud, &gap);
+      t = SVO_DRAW(weight_prob, &rows[gamma]);
       if (t < 0) { t = 0; flag |= SVO_FLAG_ZERO_MASS; }
     } else {
       /* Rejection at n: residual max(0, p_n - q_n). */
       pair_t pr = {&rows[n], &rows[gamma + 1 + n]};
       rmass = 0.0;
       for (int64_t v = 0; v < V; ++v) rmass += weight_residual(&pr, v);
-      t = inverse_cdf_draw(weight_residual, &pr, V, Ud, &gap);
+      t = SVO_DRAW(weight_residual, &pr);
       if (t < 0) {
-        /* Residual empty in floating point: sample p_n itself. */
+        /* Residual empty in floating point: sample p_n itself (same noise). */
         flag |= SVO_FLAG_RESIDUAL_FALLBACK;
-        t = inverse_cdf_draw(weight_prob, &rows[n], V, Ud, &gap);
+        t = SVO_DRAW(weight_prob, &rows[n]);
         if (t < 0) { t = 0; flag |= SVO_FLAG_ZERO_MASS; }
       }
     }
+#undef SVO_DRAW
 
     /* Emit x~_0..x~_{n-1}, t, then -1 padding. */
     int32_t* out = tokens + (int64_t)b * (gamma + 1);

@@ -49,7 +49,12 @@ double svo_uniform(uint64_t seed, uint32_t tag, uint32_t pos, uint32_t b,
 void svo_uniform_row(uint64_t seed, uint32_t tag, uint32_t pos, uint32_t b, uint64_t round,
                      int64_t v0, int64_t n, double* out);
 
-/* Uniform in [0,1) of the target's own draw at position pos: counter
+/* Samplers of the target's own token (the residual after a rejection, or the
+ * bonus token): Gumbel-max over per-entry noise of Philox tag 1 at the draw
+ * position (default), or the inverse transform with one 53-bit uniform. */
+enum { SVO_SAMPLER_GUMBEL = 0, SVO_SAMPLER_INVERSE = 1 };
+
+/* Uniform in [0,1) of the inverse-transform draw at position pos: counter
  * (0, (1<<24)|pos, b, lo32(round)); U = k 2^-53 with
  * k = (out[0] >> 11) * 2^32 + out[1]. */
 double svo_draw_uniform(uint64_t seed, uint32_t pos, uint32_t b, uint64_t round);
@@ -64,10 +69,12 @@ double svo_softmax(const double* s, int64_t V, double* p);
 /* Full sampling verify.  Optional outputs may be NULL.
  *   p_at, q_at, ratio, u_acc : [B][gamma]  p(x~), q(x~), p/q, acceptance uniform
  *   beta                     : [B][gamma]  sum_v min(p_i, q_i)   (diagnostic)
- *   draw_gap                 : [B]         distance of U W from the nearer end of the
- *                                          drawn token's cumulative interval, in
- *                                          probability units (the inverse transform:
- *                                          W the total weight, U the draw uniform)
+ *   draw_gap                 : [B]         the margin of the target's own draw:
+ *                                          Gumbel-max (default): top-1 minus top-2
+ *                                          key, log w + g in natural-log units;
+ *                                          inverse transform: distance of U W from
+ *                                          the nearer end of the drawn token's
+ *                                          cumulative interval (probability units)
  *   resid_mass               : [B]         sum_v max(0, p_n - q_n) (NaN if n == gamma)
  * Returns 0, or -1 on bad arguments. */
 int svo_spec_verify(const void* zt, const void* zd, const int32_t* xt,
@@ -104,12 +111,14 @@ int svo_spec_verify_rows(const void* zt, const void* zd, const int32_t* xt,
  * of largest-logit entries whose probability reaches top_p (entries equal to
  * the last one kept too); 1 is off.  nucleus_gap (optional output, [B]): per
  * batch row the smallest distance of top_p from the cumulative probabilities
- * just before and at a row's cut (inf without a cut). */
+ * just before and at a row's cut (inf without a cut).  sampler: SVO_SAMPLER_*
+ * for the target's own token. */
 typedef struct {
   double lenience;     /* in (0, 1] */
   int top_k;           /* >= 0 */
   double top_p;        /* in (0, 1] */
   double* nucleus_gap; /* [B] or NULL */
+  int sampler;         /* SVO_SAMPLER_GUMBEL (default) or SVO_SAMPLER_INVERSE */
 } svo_options;
 
 /* svo_spec_verify_rows with options (NULL: the exact round). */

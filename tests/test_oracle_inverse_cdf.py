@@ -27,7 +27,7 @@ import oracle
 
 def _round(zt, zd, xt, seed, rnd, T=1.0):
     return oracle.spec_verify(zt.astype(np.float32), zd.astype(np.float32), xt.astype(np.int32),
-                              temperature=T, seed=seed, rnd=rnd)
+                              temperature=T, seed=seed, rnd=rnd, sampler="inverse")
 
 
 def _searchsorted_draw(w, U):
