@@ -120,6 +120,11 @@ int spec_verify(const void* target_logits, const void* draft_logits,
                 uint8_t* out_flags, void* workspace, size_t workspace_bytes,
                 void* cuda_stream);
 
+/* How the target's own token (the residual after a rejection, or the bonus
+ * token) is drawn; see the header comment.  SV_SAMPLER_GUMBEL is the round's
+ * contract; SV_SAMPLER_INVERSE is an opt-in alternative with its own stream. */
+enum { SV_SAMPLER_GUMBEL = 0, SV_SAMPLER_INVERSE = 1 };
+
 /*
  * Variants of the round for spec_verify_opts.
  *   lenience  l in (0, 1]; 1 is the exact round.  q(x) is multiplied by l before
@@ -147,11 +152,19 @@ int spec_verify(const void* target_logits, const void* draft_logits,
  *             the cut, the cut may differ from one taken in exact arithmetic by
  *             that boundary group.  top_p < 1 needs V <= 2^21
  *             (SV_ERR_UNSUPPORTED otherwise).
+ *   sampler   SV_SAMPLER_GUMBEL (default) or SV_SAMPLER_INVERSE: the inverse
+ *             transform with one 53-bit uniform per draw (tag 1 at the draw
+ *             position, counter word 0 = 0; U = k 2^-53, k = (x0>>11) 2^32 +
+ *             x1): the smallest v, in vocabulary order, whose cumulative weight
+ *             exceeds U times the total weight, the weights summed in fp32 runs
+ *             of 8 and exactly above them, so an interval end is exact up to
+ *             about 1e-6 of the total.
  */
 typedef struct {
   float lenience;
   int32_t top_k;
   float top_p;
+  int32_t sampler;  /* SV_SAMPLER_GUMBEL (0, the default) or SV_SAMPLER_INVERSE */
 } sv_options;
 
 /*

@@ -27,7 +27,11 @@ EXPORTS = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verif
 class Options(ctypes.Structure):
     """sv_options of include/specverify.h."""
     _fields_ = [("lenience", ctypes.c_float), ("top_k", ctypes.c_int32),
-                ("top_p", ctypes.c_float)]
+                ("top_p", ctypes.c_float), ("sampler", ctypes.c_int32)]
+
+
+SV_SAMPLER_GUMBEL, SV_SAMPLER_INVERSE = 0, 1
+SAMPLERS = {"gumbel": SV_SAMPLER_GUMBEL, "inverse": SV_SAMPLER_INVERSE}
 
 
 class SpecVerifyError(RuntimeError):
@@ -157,13 +161,16 @@ def alloc_workspace(B: int, gamma: int, V: int, mode: int, device="cuda"):
 def spec_verify(target_logits, draft_logits, draft_tokens, *, temperature: float = 1.0,
                 row_temperature=None, seed: int = 0, round: int = 0, want_pq: bool = True,
                 want_alpha: bool = False, want_flags: bool = True, out=None, workspace=None,
-                stream=None, lenience: float = 1.0, top_k: int = 0, top_p: float = 1.0):
+                stream=None, lenience: float = 1.0, top_k: int = 0, top_p: float = 1.0,
+                sampler: str = "gumbel"):
     """Sampling verify through the C ABI.  Returns a dict of device tensors:
     tokens [B, g+1] int32, counts [B] int32, p/q [B, g] float32 (if want_pq),
     alpha [B] float32 (if want_alpha), flags [B] uint8 (if want_flags).
     lenience: l in (0, 1] (spec_verify_opts; 1 = the exact round).
     top_k: adjust every row to its k largest logits, ties kept (0 = off).
-    top_p: then to its nucleus of probability top_p (1 = off)."""
+    top_p: then to its nucleus of probability top_p (1 = off).
+    sampler: "gumbel" (the round's contract) or "inverse" (the opt-in inverse
+    transform) for the target's own token."""
     torch = _torch()
     L = load()
     B, g1, V = target_logits.shape
@@ -189,7 +196,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, *, temperature: float
     sh = _stream_handle(stream)
     need = workspace_bytes(B, g, V, SV_MODE_SAMPLE)
     ws = workspace if workspace is not None else _ws_cache.get(need, dev, sh.value)
-    opts = Options(float(lenience), int(top_k), float(top_p))
+    opts = Options(float(lenience), int(top_k), float(top_p), SAMPLERS[sampler])
     rc = L.spec_verify_opts(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, g,
                             V, _dtype_code(target_logits), float(temperature),
                             _ptr(row_temperature), int(seed) & (2**64 - 1),

@@ -17,7 +17,7 @@ cudaError_t launch_sample(const void* zt, const void* zd, const int32_t* xt, int
                           uint64_t seed, uint64_t round, int32_t* out_tokens, int32_t* out_counts,
                           float* out_p, float* out_q, float* out_alpha, uint8_t* out_flags,
                           void* ws, const SamplePlan& pl, cudaStream_t stream,
-                          float lenience, int top_k, float top_p);
+                          float lenience, int top_k, float top_p, int sampler);
 cudaError_t launch_greedy(const void* zt, const int32_t* xt, int B, int gamma, int64_t V,
                           int dtype, int32_t* out_tokens, int32_t* out_counts, void* ws,
                           const GreedyPlan& pl, cudaStream_t stream);
@@ -112,12 +112,14 @@ int spec_verify_opts(const void* target_logits, const void* draft_logits,
                      uint8_t* out_flags, const sv_options* options, void* workspace,
                      size_t workspace_bytes, void* cuda_stream) {
   float lenience = 1.0f, top_p = 1.0f;
-  int top_k = 0;
+  int top_k = 0, sampler = SV_SAMPLER_GUMBEL;
   if (options) {
     lenience = options->lenience;
     top_k = options->top_k;
     top_p = options->top_p;
-    if (!(lenience > 0.0f && lenience <= 1.0f) || top_k < 0 || !(top_p > 0.0f && top_p <= 1.0f))
+    sampler = options->sampler;
+    if (!(lenience > 0.0f && lenience <= 1.0f) || top_k < 0 || !(top_p > 0.0f && top_p <= 1.0f) ||
+        (sampler != SV_SAMPLER_GUMBEL && sampler != SV_SAMPLER_INVERSE))
       return SV_ERR_ARG;
     if (top_p < 1.0f && V > (int64_t(1) << 21)) return SV_ERR_UNSUPPORTED;  // nucleus sums
   }
@@ -140,7 +142,7 @@ int spec_verify_opts(const void* target_logits, const void* draft_logits,
   const cudaError_t e = sv::launch_sample(
       target_logits, draft_logits, draft_tokens, B, gamma, V, dtype, temperature, row_temperature,
       seed, round, out_tokens, out_counts, out_p_at_draft, out_q_at_draft, out_alpha, out_flags,
-      workspace, pl, (cudaStream_t)cuda_stream, lenience, top_k, top_p);
+      workspace, pl, (cudaStream_t)cuda_stream, lenience, top_k, top_p, sampler);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

@@ -40,8 +40,8 @@ struct SweepCtx {
   float temperature;
   const float* row_T;
   uint64_t seed, round;
-  int nch;               // chunk partials per logit row
-  float2* part;          // [B][R1][nch]
+  int np;                // partials per logit row: 4 KB chunks (vector sweep) or splits
+  float2* part;          // [B][R1][np] (largest logit as given, sum of 2^(y - max y))
   RowStat* rowstat;      // [B][R1]
   DrawState* state;      // [B]
   int32_t* out_tokens;
@@ -52,69 +52,41 @@ struct SweepCtx {
   float inv_lenience;    // 1/l of the lenient comparison u <= p/(l q); 1: the exact round
   const float* thr;      // [B][R1] top-k thresholds (logits below have weight 0) or null
   uint32_t* done;        // [B] arrival counters of the draw, zeroed by every sweep
-  float2* epart;         // vector sweep: [B*R1][2] head and tail pieces, `part` holds one
-                         // partial per 4 KB block of the two arrays; null: [B*R1][nch]
 };
 
-// The chunk partials of one logit row, in row order.  Generic sweep: nch
-// consecutive partials.  Vector sweep: the head piece, the partials of the row's
-// inner 4 KB blocks (consecutive in the per-block array), the tail piece.
+// The partials of one logit row, in row order: [np] consecutive entries.  Each
+// covers a piece of the row counted from the row's start (a 4 KB chunk, or a
+// kChunkSweep-logit split), so they do not depend on where the row sits in
+// memory.
 struct RowParts {
-  float2* head;
-  float2* inner;
-  float2* tail;
-  int n;       // partials in all
-  int ninner;  // vector sweep: inner blocks (-1: generic layout)
-  __device__ __forceinline__ float2* at(int j) const {
-    if (ninner < 0) return head + j;
-    return (j == 0) ? head : ((j <= ninner) ? inner + (j - 1) : tail);
-  }
+  float2* p;
+  int n;
+  __device__ __forceinline__ float2* at(int j) const { return p + j; }
 };
-
-// Row rid = b*R1 + k of batch row b.  The vector sweep cuts each of the two
-// arrays (target rows, draft rows) into 4 KB blocks aligned in memory; block
-// indices count the target array's blocks first.
 template <int DT>
 __device__ __forceinline__ RowParts row_parts(const SweepCtx& x, int64_t rid) {
-  RowParts p;
-  if (!x.epart) {
-    p.head = x.part + rid * x.nch;
-    p.inner = p.tail = nullptr;
-    p.n = x.nch;
-    p.ninner = -1;
-    return p;
-  }
-  const int gamma = x.gamma, R1 = 2 * gamma + 1;
-  const int b = (int)(rid / R1), k = (int)(rid - (int64_t)b * R1);
-  const int64_t RB = x.V * ((DT == SV_F32) ? 4 : 2);
-  const uintptr_t zt = reinterpret_cast<uintptr_t>(x.zt), zd = reinterpret_cast<uintptr_t>(x.zd);
-  const int64_t hd0 = (int64_t)(zt & 4095u), hd1 = (int64_t)(zd & 4095u);
-  const int64_t NC0 = ((int64_t)x.B * (gamma + 1) * RB + hd0 + 4095) >> 12;
-  const bool arr = k > gamma;
-  const int64_t ra = arr ? (int64_t)b * gamma + (k - gamma - 1) : (int64_t)b * (gamma + 1) + k;
-  const int64_t a0 = ra * RB + (arr ? hd1 : hd0);
-  const int64_t in0 = (a0 + 4095) >> 12, in1 = (a0 + RB) >> 12;  // inner blocks [in0, in1)
-  p.head = x.epart + 2 * rid;
-  p.tail = p.head + 1;
-  p.ninner = (int)(in1 - in0);
-  p.inner = x.part + (arr ? NC0 : 0) + in0;
-  p.n = p.ninner + 2;
-  return p;
+  return RowParts{x.part + rid * x.np, x.np};
 }
 
 // Online (max, sum) of a lane's share of one row's chunk partials.
+// A partial is (largest logit z, sum of 2^(y - z c)) with c the row's scale; the
+// fused LM head's partials carry the scaled max itself (c = 1).
 struct RowAcc {
   float m, s;
   int bits;
+  float z;
 };
-__device__ __forceinline__ void row_acc_add(RowAcc& a, float2 p) {
+__device__ __forceinline__ RowAcc row_acc_init() { return RowAcc{-kInf, 0.0f, 0, -kInf}; }
+__device__ __forceinline__ void row_acc_add(RowAcc& a, float2 p, float c) {
   if (p.x != p.x) a.bits |= kRowNaN;
   if (p.y < 0.0f) a.bits |= kRowTimeout;
-  if (p.x > a.m) {
-    a.s = (a.m == -kInf) ? 0.0f : a.s * exp2f(a.m - p.x);
-    a.m = p.x;
+  a.z = fmaxf(a.z, p.x);
+  const float m = p.x * c;  // the partial's own scaled max, bit for bit
+  if (m > a.m) {
+    a.s = (a.m == -kInf) ? 0.0f : a.s * exp2f(a.m - m);
+    a.m = m;
   }
-  if (p.x > -kInf) a.s += p.y * exp2f(p.x - a.m);
+  if (m > -kInf) a.s += p.y * exp2f(m - a.m);
 }
 // The warp's combined statistics, kept by lane 0 and written to *out.
 __device__ __forceinline__ RowStat row_acc_finish(const RowAcc& a, RowStat* out) {
@@ -128,26 +100,28 @@ __device__ __forceinline__ RowStat row_acc_finish(const RowAcc& a, RowStat* out)
   rs.mc = M;
   rs.bits = bits;
   rs.s = (bits & kRowNaN) ? CUDART_NAN_F : sl;
+  rs.z = warp_max(a.z);
   if (lane == 0 && out) *out = rs;
   return rs;
 }
 
 // Row statistics of row r from its chunk partials (one warp, all loads of a
 // lane in flight together), kept by lane 0 and written to rowstat[r].
-__device__ __forceinline__ RowStat combine_row(const float2* pr, int nch, RowStat* out) {
+__device__ __forceinline__ RowStat combine_row(const float2* pr, int nch, RowStat* out,
+                                               float c) {
   const int lane = threadIdx.x & 31;
-  RowAcc a{-kInf, 0.0f, 0};
+  RowAcc a = row_acc_init();
 #pragma unroll 4
-  for (int j = lane; j < nch; j += 32) row_acc_add(a, __ldcg(pr + j));
+  for (int j = lane; j < nch; j += 32) row_acc_add(a, __ldcg(pr + j), c);
   return row_acc_finish(a, out);
 }
 
 // The same over a row's partials in any layout.
-__device__ __forceinline__ RowStat combine_parts(const RowParts& p, RowStat* out) {
+__device__ __forceinline__ RowStat combine_parts(const RowParts& p, RowStat* out, float c) {
   const int lane = threadIdx.x & 31;
-  RowAcc a{-kInf, 0.0f, 0};
+  RowAcc a = row_acc_init();
 #pragma unroll 4
-  for (int j = lane; j < p.n; j += 32) row_acc_add(a, __ldcg(p.at(j)));
+  for (int j = lane; j < p.n; j += 32) row_acc_add(a, __ldcg(p.at(j)), c);
   return row_acc_finish(a, out);
 }
 
@@ -155,16 +129,16 @@ __device__ __forceinline__ RowStat combine_parts(const RowParts& p, RowStat* out
 // 0: no second row); each row's arithmetic is that of combine_row.
 __device__ __forceinline__ void combine_parts2(const RowParts& p0, const RowParts& p1,
                                                RowStat* out0, RowStat* out1, RowStat& r0,
-                                               RowStat& r1) {
+                                               RowStat& r1, float c) {
   const int lane = threadIdx.x & 31;
-  RowAcc a0{-kInf, 0.0f, 0}, a1{-kInf, 0.0f, 0};
+  RowAcc a0 = row_acc_init(), a1 = row_acc_init();
   const int n = max(p0.n, p1.n);
 #pragma unroll 4
   for (int j = lane; j < n; j += 32) {
     const float2 x0 = (j < p0.n) ? __ldcg(p0.at(j)) : make_float2(-kInf, 0.0f);
     const float2 x1 = (j < p1.n) ? __ldcg(p1.at(j)) : make_float2(-kInf, 0.0f);
-    row_acc_add(a0, x0);
-    row_acc_add(a1, x1);
+    row_acc_add(a0, x0, c);
+    row_acc_add(a1, x1, c);
   }
   r0 = row_acc_finish(a0, out0);
   r1 = row_acc_finish(a1, p1.n ? out1 : nullptr);
@@ -275,6 +249,8 @@ __device__ void decide_batch_row(const SweepCtx& x, int b, const RowStat* srs,
     const float St = srs[n].s;
     DrawState st{};
     st.pos = n;
+    st.zmt = srs[n].z;
+    st.zmd = (n < gamma) ? srs[gamma + 1 + n].z : -kInf;
     st.c = c;
     st.invT = invT;
     st.tt = x.thr ? x.thr[(int64_t)b * R1 + n] : -kInf;

@@ -25,13 +25,13 @@
 //   k_lm<2>      the same GEMM for the compact rows only (tiles in reverse
 //                order), target and draft blocks side by side in tensor
 //                memory.  The compact rows are copied into the row tile twice
-//                (B <= 64) so that two lane quadrants share the epilogue: per
-//                16-entry chunk the fp32 sums of the draw weights (residual
-//                max(0, p_n - q_n) and p_n).
-//   k_lm_merge   one CTA per compact row: the token by the inverse transform
-//                (sv_draw.cuh) from the chunk sums, and the 16 logits of the
-//                one chunk it lands in recomputed from h and W; p_n for an
-//                empty residual; emit.
+//                (B <= 64) so that two lane quadrants share the epilogue: the
+//                Gumbel-max race of the draw (Philox tag 1 at the draw
+//                position), the best two keys of the residual max(0, p_n - q_n)
+//                and of p_n per row and CTA, with the logits at them.
+//   k_lm_merge   one warp per compact row: the best two over the CTAs,
+//                re-decided in double near a tie from the logits the keys came
+//                from; p_n for an empty residual; emit.
 //
 // Draft sampling (spec_lmhead_draft) is a third use of the GEMM (k_lm<3>) with
 // Gumbel-max keys y_v - log2(-log2 u_v), y = z / T * log2 e, on Philox tag 2.
@@ -92,17 +92,8 @@ struct LmArgs {
   float2* part;        // [B*R1][nslot][2] (max, sum) per row, CTA and column half
   float* zat;          // [B*R1] logit at the row's draft token
   LmCand* res;         // pass 3: [B][nslot][2] top-2 Gumbel keys per batch row and CTA
-  int nchunk;          // pass 2: 16-entry chunks per row, ceil(V / 16)
-  float* csum_r;       // pass 2: [B][nchunk] residual weight sums per compact row
-  float* csum_p;       // pass 2: [B][nchunk] p_n weight sums per compact row
-  const uint16_t* W_t;  // merge: the weights, for the 16 logits of one chunk
-  const uint16_t* W_d;
-  uint64_t* tsum_r;    // pass 2: [B][nvt] residual weight per vocabulary tile (fixed point)
-  uint64_t* tsum_p;    // pass 2: [B][nvt] p_n weight per vocabulary tile (zeroed by finish)
-  uint64_t* gsum_r;    // pass 2: [B][ngrp] the same per group of 32 tiles
-  uint64_t* gsum_p;
-  int ngrp;            // ceil(nvt / 32)
-  int fsh;             // fixed-point scale of the draw sums
+  LmCand* res2;        // pass 2: [B][nslot][4] per compact row and CTA: the best two keys
+                       // of the residual race, then of p_n
   DrawState* state;    // [B]
   int* slot_b;         // [B] batch row of each compact row
   uint32_t* ctl;       // count, pass-1 error, pass-2 error
@@ -482,14 +473,22 @@ __device__ __forceinline__ P2Slice pass2_slice(const LmArgs& a, int quad, int ha
   return sl;
 }
 
+// What a pass-2 epilogue thread carries over the CTA's tiles: the best two keys
+// of its compact row's residual race and of p_n over its column slice (two
+// interleaved top-2s each, merged at the end).
+struct Pass2Carry {
+  Cand2 r[2], p[2];
+};
+
 // Pass-2 epilogue of one job (compact rows; target at column 0, draft at 128):
-// for every 16-column chunk of this thread's row and column slice, the fp32
-// sums (added in order) of the draw weights -- p_n, and for a residual row
-// max(0, p_n - q_n).  Each chunk sum is also added, in fixed point, to its
-// vocabulary tile's total and to its group's (32 tiles) total (integer atomics:
-// exact in any order).  No logit leaves the tensor memory.
+// the Gumbel-max race of this thread's row over its column slice, keys
+// log2 w_v - log2 E_v with E_v = -log2 u_v (u_v from Philox tag 1 at the draw
+// position of the row's batch row), w = p_n for every entry and w = max(0, p_n -
+// q_n) for a residual row, both up to the row's factor 2^-mct / St.  No logit
+// leaves the tensor memory: the candidates carry their two logits.
 __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t tacc, int quad,
-                                               int half, int rows) {
+                                               int half, int rows, const PhiloxKeys& pk,
+                                               Pass2Carry& cy) {
   const int lane = threadIdx.x & 31;
   const int V = a.V;
   const P2Slice sl = pass2_slice(a, quad, half);
@@ -497,7 +496,11 @@ __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t 
   const int r = sl.row0 + lane;
   const bool rv = r < rows;
   DrawState st{};
-  if (rv) st = a.state[a.slot_b[r]];
+  int b = 0;
+  if (rv) {
+    b = a.slot_b[r];
+    st = a.state[b];
+  }
   const bool resid = st.mode == kDrawResidual;
   const float kd = __fsub_rn(st.K, st.mct);
   const uint32_t ta = tacc + ((uint32_t)(32 * quad) << 16) + (uint32_t)sl.col0;
@@ -510,27 +513,26 @@ __device__ __forceinline__ void epilogue_pass2(const LmArgs& a, int t, uint32_t 
     tmem_wait_ld();
     const int vb = t * kLmTileN + sl.col0 + c16;  // a multiple of 16
     if (rv && vb < V) {
-      float zt[16], zd[16];
-      float sp = 0.0f, sr = 0.0f;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const bool in = vb + e < V;  // columns past V hold no logit
-        zt[e] = in ? __uint_as_float(rt[e]) : -kInf;
-        zd[e] = in ? __uint_as_float(rd[e]) : -kInf;
-        sp = __fadd_rn(sp, draw_weight<false, false>(zt[e], 0.0f, st, kd));
-        if (resid) sr = __fadd_rn(sr, draw_weight<true, false>(zt[e], zd[e], st, kd));
-      }
-      const int64_t ci = (int64_t)r * a.nchunk + (vb >> 4);
-      const int64_t ti = (int64_t)r * a.nvt + t, gi = (int64_t)r * a.ngrp + (t >> 5);
-      a.csum_p[ci] = sp;
-      const uint64_t fp = to_fix(sp, a.fsh);
-      atomicAdd(reinterpret_cast<unsigned long long*>(a.tsum_p + ti), fp);
-      atomicAdd(reinterpret_cast<unsigned long long*>(a.gsum_p + gi), fp);
-      if (resid) {
-        a.csum_r[ci] = sr;
-        const uint64_t fr = to_fix(sr, a.fsh);
-        atomicAdd(reinterpret_cast<unsigned long long*>(a.tsum_r + ti), fr);
-        atomicAdd(reinterpret_cast<unsigned long long*>(a.gsum_r + gi), fr);
+      for (int g4 = 0; g4 < 4; ++g4) {
+        const int v = vb + 4 * g4;
+        if (v >= V) break;  // columns past V hold no logit
+        const uint4 rnd =
+            philox_rk(sv_counter((uint32_t)(v >> 2), 1u, (uint32_t)st.pos, (uint32_t)b, a.round), pk);
+        const uint32_t rr[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float zt = __uint_as_float(rt[4 * g4 + e]);
+          const float zd = __uint_as_float(rd[4 * g4 + e]);
+          if (!(zt > -kInf)) continue;  // weight 0 (or not a number)
+          const float lE = __log2f(neglog2_u(rr[e]));
+          const float yt = __fmaf_rn(zt, st.c, -st.mct);
+          cand_insert(cy.p[e & 1], LmCand{yt - lE, v + e, zt, zd});
+          if (resid) {
+            const float et = ex2(yt), ed = ex2(__fmaf_rn(zd, st.c, kd));
+            if (et > ed) cand_insert(cy.r[e & 1], LmCand{__log2f(__fsub_rn(et, ed)) - lE, v + e, zt, zd});
+          }
+        }
       }
     }
   }
@@ -641,6 +643,41 @@ __device__ __forceinline__ void pass3_flush(const LmArgs& a, int quad, int half,
     LmCand* o = a.res + ((int64_t)rr * a.nslot + blockIdx.x) * 2;
     o[0] = x.a;
     o[1] = x.b;
+  }
+}
+
+// One set of candidates per compact row and CTA (the residual's best two, then
+// p_n's): the row's column slices are merged through shared memory (the ring,
+// idle after the last job).
+__device__ __forceinline__ void pass2_flush(const LmArgs& a, int quad, int half, int rows,
+                                            const Pass2Carry& cy, unsigned char* smem) {
+  const int nsl = 2 * a.rep;
+  const P2Slice sl = pass2_slice(a, quad, half);
+  const int r = sl.row0 + (threadIdx.x & 31);
+  LmCand* sc = reinterpret_cast<LmCand*>(smem);  // [rows][nsl][4]
+  if (sl.copy < a.rep && r < rows) {
+    const Cand2 tr = merge2(cy.r), tp = merge2(cy.p);
+    LmCand* o = sc + ((size_t)r * nsl + sl.copy * 2 + half) * 4;
+    o[0] = tr.a;
+    o[1] = tr.b;
+    o[2] = tp.a;
+    o[3] = tp.b;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+  for (int rr = (int)threadIdx.x - 3 * 32; rr < rows; rr += 32 * kEpiWarps) {
+    Cand2 xr{cand_empty(), cand_empty()}, xp = xr;
+    for (int j = 0; j < nsl; ++j) {
+      const LmCand* q = sc + ((size_t)rr * nsl + j) * 4;
+      cand_insert(xr, q[0]);
+      cand_insert(xr, q[1]);
+      cand_insert(xp, q[2]);
+      cand_insert(xp, q[3]);
+    }
+    LmCand* o = a.res2 + ((int64_t)rr * a.nslot + blockIdx.x) * 4;
+    o[0] = xr.a;
+    o[1] = xr.b;
+    o[2] = xp.a;
+    o[3] = xp.b;
   }
 }
 
@@ -819,9 +856,12 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const int quad = warp & 3, half = (warp - 3) >> 2;
     const PhiloxKeys pk = philox_keys(a.seed);
     Pass1Carry cy;
+    Pass2Carry cy2;
     Pass3Carry cy3;
     if (PASS == 1 || PASS == 4) {
       carry_init(cy);
+    } else if (PASS == 2) {
+      cy2.r[0] = cy2.r[1] = cy2.p[0] = cy2.p[1] = Cand2{cand_empty(), cand_empty()};
     } else if (PASS == 3) {
       cy3.mc = -kInf;
       cy3.s = 0.0f;
@@ -847,7 +887,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           else
             epilogue_pass1<1>(a, tv, tacc, quad, half, cy);
         } else if (PASS == 2) {
-          epilogue_pass2(a, tv, tacc, quad, half, rows2);
+          epilogue_pass2(a, tv, tacc, quad, half, rows2, pk, cy2);
         } else {
           epilogue_pass3(a, tv, tacc, quad, half, pk, cy3);
         }
@@ -862,6 +902,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       pass1_flush<2>(a, cy, quad, half);
     else if (PASS == 4)
       pass1_flush<1>(a, cy, quad, half);
+    else if (PASS == 2)
+      pass2_flush(a, quad, half, rows2, cy2, hring);
     else if (PASS == 3)
       pass3_flush(a, quad, half, cy3, hring);
   }
@@ -897,7 +939,7 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
         rs.bits = (lse != lse) ? kRowNaN : 0;
         rs.s = (lse != lse) ? CUDART_NAN_F : ((lse == -kInf) ? 0.0f : 1.0f);
       } else {
-        rs = combine_row(a.part + ((int64_t)b * R1 + k) * a.nslot * 2, a.nslot * 2, nullptr);
+        rs = combine_row(a.part + ((int64_t)b * R1 + k) * a.nslot * 2, a.nslot * 2, nullptr, 1.0f);
       }
       if (err) {
         rs.bits |= kRowTimeout | kRowNaN;
@@ -948,14 +990,6 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
   __syncthreads();
   const int slot = s_slot;
   const int n = st.pos;
-  for (int j = threadIdx.x; j < a.nvt; j += blockDim.x) {
-    a.tsum_r[(int64_t)slot * a.nvt + j] = 0ull;
-    a.tsum_p[(int64_t)slot * a.nvt + j] = 0ull;
-  }
-  for (int j = threadIdx.x; j < a.ngrp; j += blockDim.x) {
-    a.gsum_r[(int64_t)slot * a.ngrp + j] = 0ull;
-    a.gsum_p[(int64_t)slot * a.ngrp + j] = 0ull;
-  }
   const uint4* srct = reinterpret_cast<const uint4*>(a.h_t + ((int64_t)b * (gamma + 1) + n) * a.Ht);
   uint4* dt = reinterpret_cast<uint4*>(a.c_t + (int64_t)slot * a.Ht);
   uint4* dd = reinterpret_cast<uint4*>(a.c_d + (int64_t)slot * a.Hd);
@@ -970,162 +1004,54 @@ __global__ void __launch_bounds__(1024) k_lm_finish(LmArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// k_lm_merge: one CTA per compact row.  The token by the inverse transform
-// from the pass-2 sums: warp 0 finds the group of 32 vocabulary tiles holding
-// t = floor(U W) (fixed point), the tile and the 16-entry chunk; the CTA then
-// recomputes that chunk's 16 logits from the compact hidden rows and the
-// weights (fp32 sums over the hidden dimension on the CUDA cores, so their last
-// bits may differ from the tensor cores': where U W falls within that rounding
-// of an entry's edge the last positive entry of the chunk is taken), and the
-// entry follows.  The residual's fallback to p_n when it has no positive weight.
+// k_lm_merge: one warp per compact row.  The best two keys of the residual
+// race over the recompute pass's CTAs (p_n's when the residual had no positive
+// entry: the fallback), re-decided in double when within 2^-10 (log2 units):
+// log(p_n - q_n) + g with p_n = 2^(z c - mct) / St, q_n likewise, or z / T + g
+// for a draw from p_n, on the logits the candidates carry.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) k_lm_merge(LmArgs a) {
+__global__ void __launch_bounds__(32) k_lm_merge(LmArgs a) {
   const int slot = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ int s_c, s_fl, s_resid;
-  __shared__ uint64_t s_trel;
-  __shared__ float s_z[2][32][16];
+  const int lane = threadIdx.x & 31;
   pdl_wait();
   const int rows = (int)*reinterpret_cast<volatile uint32_t*>(a.ctl);
   if (slot >= rows) return;
   const bool err = *reinterpret_cast<volatile uint32_t*>(a.ctl + 2) != 0u;
   const int b = a.slot_b[slot];
   const DrawState st = a.state[b];
-  const int V = a.V;
-  if (warp == 0) {
-    int fl = st.flags;
-    int c = -1;
-    uint64_t trel = 0;
-    bool resid = st.mode == kDrawResidual;
-    if (err) {
-      fl |= SV_FLAG_TIMEOUT | SV_FLAG_NONFINITE;
+  Cand2 R{cand_empty(), cand_empty()}, P = R;
+  for (int j = lane; j < a.nslot; j += 32) {
+    const LmCand* q = a.res2 + ((int64_t)slot * a.nslot + j) * 4;
+    cand_insert(R, q[0]);
+    cand_insert(R, q[1]);
+    cand_insert(P, q[2]);
+    cand_insert(P, q[3]);
+  }
+  R = warp_cand2(R);
+  P = warp_cand2(P);
+  int fl = st.flags;
+  bool use_r = false;
+  Cand2 T = P;
+  if (st.mode == kDrawResidual) {
+    if (R.a.idx >= 0) {
+      T = R;
+      use_r = true;
     } else {
-      const uint64_t k53 = draw_uniform53(a.seed, (uint32_t)st.pos, (uint32_t)b, a.round);
-      const int64_t go = (int64_t)slot * a.ngrp;
-      uint64_t W = warp_total((resid ? a.gsum_r : a.gsum_p) + go, a.ngrp);
-      if (resid && W == 0) {
-        // the residual had no positive entry in floating point: draw from p_n itself
-        fl |= SV_FLAG_RESIDUAL_FALLBACK;
-        resid = false;
-        W = warp_total(a.gsum_p + go, a.ngrp);
-      }
-      if (W > 0) {
-        const uint64_t t = scale_fix(k53, W);  // < W
-        uint64_t base = 0;
-        const int g = warp_find<2>((resid ? a.gsum_r : a.gsum_p) + go, a.ngrp, t, 0ull, &base);
-        const int t0 = 32 * g;
-        const int tl = t0 + warp_find<1>((resid ? a.tsum_r : a.tsum_p) + (int64_t)slot * a.nvt + t0,
-                                         min(32, a.nvt - t0), t, base, &base);
-        // the chunk of the tile: its fixed-point sums add up to the tile's
-        const float* cs = (resid ? a.csum_r : a.csum_p) + (int64_t)slot * a.nchunk;
-        const int c0 = tl * (kLmTileN / 16), nc = min(a.nchunk - c0, kLmTileN / 16);
-        const uint64_t x = (lane < nc) ? to_fix(__ldcg(cs + c0 + lane), a.fsh) : 0ull;
-        uint64_t P = x;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint64_t y = __shfl_up_sync(0xffffffffu, P, o);
-          if (lane >= o) P += y;
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, base + P > t);
-        const int l = __ffs((int)hit) - 1;
-        if (l >= 0) {
-          c = c0 + l;
-          trel = t - (base + __shfl_sync(0xffffffffu, P - x, l));
-        }
-      }
-    }
-    if (lane == 0) {
-      s_c = c;
-      s_trel = trel;
-      s_fl = fl;
-      s_resid = resid ? 1 : 0;
+      fl |= SV_FLAG_RESIDUAL_FALLBACK;  // no positive residual entry: p_n, the same noise
     }
   }
-  __syncthreads();
-  const int c = s_c;
-  int tk = -1;
-  if (c >= 0) {
-    // the chunk's logits: thread t sums hidden entries t, t + 1024, ... for the 16
-    // columns (the target row, and for a residual the draft row)
-    const int vb = c * 16;
-    const bool resid = s_resid != 0;
-    for (int side = 0; side < (resid ? 2 : 1); ++side) {
-      const uint16_t* h = side ? a.c_d + (int64_t)slot * a.Hd : a.c_t + (int64_t)slot * a.Ht;
-      const uint16_t* Wm = side ? a.W_d : a.W_t;
-      const int H = side ? a.Hd : a.Ht;
-      float acc[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
-      constexpr int kU = 4;  // hidden entries per thread and round: their loads in flight together
-      for (int k0 = tid; k0 < H; k0 += kU * (int)blockDim.x) {
-        uint4 w0[kU], w1[kU];
-        float hk[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int k = k0 + u * (int)blockDim.x;
-          hk[u] = 0.0f;
-          w0[u] = w1[u] = make_uint4(0u, 0u, 0u, 0u);
-          if (k < H) {
-            hk[u] = __uint_as_float((uint32_t)__ldcg(h + k) << 16);
-            const uint4* wr = reinterpret_cast<const uint4*>(Wm + (int64_t)k * V + vb);  // V % 8 == 0
-            // a last chunk may hold 8 entries (V % 16 == 8): nothing past the row is read
-            w0[u] = __ldg(wr);
-            if (vb + 8 < V) w1[u] = __ldg(wr + 1);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const uint32_t ww[8] = {w0[u].x, w0[u].y, w0[u].z, w0[u].w,
-                                  w1[u].x, w1[u].y, w1[u].z, w1[u].w};
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            acc[2 * q] = fmaf(hk[u], bf16lo(ww[q]), acc[2 * q]);
-            acc[2 * q + 1] = fmaf(hk[u], bf16hi(ww[q]), acc[2 * q + 1]);
-          }
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
-      }
-      if (lane == 0) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) s_z[side][warp][e] = acc[e];
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane e sums entry e of the target row over the warps in order, lane 16 + e that of
-      // the draft row; lane e then forms weight e, and lane 0 picks from all 16
-      const int e16 = lane & 15, side = lane >> 4;
-      float z = 0.0f;
-      if (side == 0 || resid)
-        for (int q = 0; q < (int)(blockDim.x >> 5); ++q) z += s_z[side][q][e16];
-      const float zd = __shfl_sync(0xffffffffu, z, 16 + e16);
-      const float kd = __fsub_rn(st.K, st.mct);
-      const bool in = side == 0 && vb + e16 < V;
-      const float wl = !in ? 0.0f
-                           : (resid ? draw_weight<true, false>(z, zd, st, kd)
-                                    : draw_weight<false, false>(z, 0.0f, st, kd));
-      float w[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) w[q] = __shfl_sync(0xffffffffu, wl, q);
-      if (lane != 0) return;
-      int e = pick_in_run<16>(w, 0ull, s_trel, a.fsh);
-      if (e < 0) {  // rounding put U W past the recomputed chunk: its last positive entry
-        for (int q = 15; q >= 0; --q)
-          if (w[q] > 0.0f) {
-            e = q;
-            break;
-          }
-      }
-      tk = e >= 0 ? vb + e : -1;
-    }
-  }
-  if (tid != 0) return;
-  int fl = s_fl;
-  if (tk < 0 || tk >= V) {
+  const double c = (double)st.c, invT = (double)st.invT;
+  int tk = redecide(T, [&](const LmCand& q) -> double {
+    const double g = gumbel_f64(q.idx, st.pos, b, a.seed, a.round, 1u);
+    if (!use_r) return (double)q.zt * invT + g;
+    const double p = exp2((double)q.zt * c - (double)st.mct) / (double)st.st;
+    const double pq = (q.zd > -kInf) ? exp2((double)q.zd * c - (double)st.mcd) / (double)st.sd : 0.0;
+    const double w = p - pq;
+    return (w > 0.0) ? log(w) + g : -HUGE_VAL;
+  });
+  if (lane != 0) return;
+  if (err) fl |= SV_FLAG_TIMEOUT | SV_FLAG_NONFINITE;
+  if (tk < 0 || tk >= a.V) {
     tk = 0;
     if (!err) fl |= SV_FLAG_ZERO_MASS;
   }
@@ -1152,7 +1078,7 @@ __global__ void __launch_bounds__(256) k_lm_draft_merge(LmArgs a, DraftOut out) 
   pdl_wait();
   const bool err = *reinterpret_cast<volatile uint32_t*>(a.ctl + 2) != 0u;
   if (threadIdx.x < 32) {
-    const RowStat rs = combine_row(a.part + (int64_t)b * a.nslot, a.nslot, nullptr);
+    const RowStat rs = combine_row(a.part + (int64_t)b * a.nslot, a.nslot, nullptr, 1.0f);
     if (threadIdx.x == 0) s_rs = rs;
   }
   Cand2 t{cand_empty(), cand_empty()};
@@ -1340,17 +1266,7 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   a.round = round;
   a.part = reinterpret_cast<float2*>(ws + pl.off_part);
   a.zat = reinterpret_cast<float*>(ws + pl.off_zat);
-  a.nchunk = (int)ceil_div(V, 16);
-  a.csum_r = reinterpret_cast<float*>(ws + pl.off_csr);
-  a.csum_p = reinterpret_cast<float*>(ws + pl.off_csp);
-  a.W_t = reinterpret_cast<const uint16_t*>(W_target);
-  a.W_d = reinterpret_cast<const uint16_t*>(W_draft);
-  a.tsum_r = reinterpret_cast<uint64_t*>(ws + pl.off_tsr);
-  a.tsum_p = reinterpret_cast<uint64_t*>(ws + pl.off_tsp);
-  a.ngrp = (pl.nvt + 31) / 32;
-  a.gsum_r = reinterpret_cast<uint64_t*>(ws + pl.off_gsr);
-  a.gsum_p = reinterpret_cast<uint64_t*>(ws + pl.off_gsp);
-  a.fsh = fix_shift(V);
+  a.res2 = reinterpret_cast<LmCand*>(ws + pl.off_res2);
   a.state = reinterpret_cast<DrawState*>(ws + pl.off_state);
   a.slot_b = reinterpret_cast<int*>(ws + pl.off_slot);
   a.ctl = reinterpret_cast<uint32_t*>(ws + pl.off_ctl);
@@ -1413,7 +1329,7 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
   e = launch_pdl(k_lm<2>, dim3(grid), dim3(kLmThreads), smem2, stream, cT, WT, cD, WD, a2);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   mark(3, stream);
-  e = launch_pdl(k_lm_merge, dim3((unsigned)B), dim3(1024), 0, stream, a);
+  e = launch_pdl(k_lm_merge, dim3((unsigned)B), dim3(32), 0, stream, a);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   mark(4, stream);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;

@@ -37,7 +37,7 @@ cudaError_t launch_sample(const void* zt, const void* zd, const int32_t* xt, int
                           uint64_t seed, uint64_t round, int32_t* out_tokens, int32_t* out_counts,
                           float* out_p, float* out_q, float* out_alpha, uint8_t* out_flags,
                           void* ws, const SamplePlan& pl, cudaStream_t stream,
-                          float lenience, int top_k, float top_p);
+                          float lenience, int top_k, float top_p, int sampler);
 }  // namespace sv
 
 namespace {
@@ -100,6 +100,6 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
   const cudaError_t e = sv::launch_sample(
       target_logits, draft_logits, draft_tokens, B, gamma, V, dtype, temperature, row_temperature,
       seed, round, out_tokens, out_counts, out_p_at_draft, out_q_at_draft, out_alpha, out_flags,
-      scratch, pl, (cudaStream_t)cuda_stream, 1.0f, 0, 1.0f);
+      scratch, pl, (cudaStream_t)cuda_stream, 1.0f, 0, 1.0f, SV_SAMPLER_GUMBEL);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -24,29 +24,31 @@ constexpr int kSweepWarps = 8;
 constexpr int kSweepCtasPerSm = 2;
 constexpr int kSweepChunkBytes = 4096;
 
-// The vector sweep needs every row to start on a 16-byte boundary (the bases are)
-// and rows of at least one chunk, so that a chunk touches at most two rows.
+// The vector sweep cuts every row into chunks of 4 KB counted from the row's
+// start (the last one may be shorter) and loads 16-byte vectors, so every row
+// must start on a 16-byte boundary: rows whose byte length is a multiple of 16
+// (the bases are 16-byte aligned).  Results do not depend on where the arrays
+// sit in memory, only on the values and the shapes.
 SV_HD inline bool use_vec_sweep(int dtype, int64_t V) {
   const int64_t rb = V * (dtype == 0 ? 4 : 2);
-  return rb % 16 == 0 && rb >= kSweepChunkBytes;
+  return rb % 16 == 0;
 }
 
 SV_HD inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 SV_HD inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Partials of a sweep, at most: one per 4 KB block of the target and draft arrays of
-// fp32 rows (either base may sit anywhere in its first block: one more block each),
-// the two edge pieces of every row, or one per kChunkSweep-logit split of every row.
-SV_HD inline int64_t vec_sweep_blocks(int B, int gamma, int64_t V) {
-  const int64_t rb = V * 4;
-  return ceil_div((int64_t)B * (gamma + 1) * rb, 4096) + 1 + ceil_div((int64_t)B * gamma * rb, 4096) + 1;
+// Partials per logit row: one per 4 KB chunk of the row (vector sweep) or per
+// kChunkSweep-logit split (generic sweep).  A workspace is sized for the most
+// of either over both element types: one per 1024 logits.
+SV_HD inline int64_t vec_sweep_chunks(int dtype, int64_t V) {
+  return ceil_div(V * (dtype == 0 ? 4 : 2), (int64_t)kSweepChunkBytes);
 }
-SV_HD inline int64_t vec_sweep_partials(int B, int gamma, int64_t V) {
-  const int64_t rows = (int64_t)B * (2 * gamma + 1);
-  const int64_t vec = vec_sweep_blocks(B, gamma, V) + 2 * rows;
-  const int64_t gen = rows * ceil_div(V, kChunkSweep);
-  return vec > gen ? vec : gen;
-}
+SV_HD inline int64_t max_row_partials(int64_t V) { return ceil_div(V, (int64_t)1024); }
+
+// The fused round's draw: each batch row's token is raced in slices of
+// kRaceSlice vocabulary entries, one warp per slice.
+constexpr int kRaceSlice = 1024;
+SV_HD inline int64_t race_slices(int64_t V) { return ceil_div(V, (int64_t)kRaceSlice); }
 
 // Per-row softmax statistics after the chunk combine: max (scaled, log2 units),
 // row condition bits, and the sum of 2^(y - max) in double.
@@ -54,6 +56,7 @@ struct RowStat {
   float mc;
   int bits;  // kRowNaN | kRowTimeout
   float s;   // sum of 2^(y - mc) over the row (fp32 throughout: GB300 runs fp64 slowly)
+  float z;   // the row's largest logit as given (mc = z * scale), where the partials carry it
 };
 constexpr int kRowNaN = 1, kRowTimeout = 2;
 
@@ -77,38 +80,50 @@ struct DrawState {
   float td;      // top-k threshold of draft row n (residual only)
   float st;      // target row n: sum
   float sd;      // draft row n: sum (residual only)
+  float zmt;     // target row n: largest logit as given (mct = zmt * c)
+  float zmd;     // draft row n: largest logit as given (residual only)
 };
 
 struct SamplePlan {
   int R1 = 0;          // logit rows per batch row, 2*gamma+1
-  int nsplit1 = 0;     // 8192-logit chunks per row (generic sweep, overlap pass)
-  int nsplit3 = 0;     // most CTAs per batch row in the draw pass
+  int npmax = 0;       // partials per row the workspace holds (one per 1024 logits)
+  int nsplit3 = 0;     // most CTAs per batch row in the inverse-transform draw
+  int nrace = 0;       // race slices per batch row (fused round)
+  // The fused round's words, zeroed before every call and laid out together:
+  // an abort word, the decision of each batch row [B][3], the race candidates
+  // [B][nrace][4], then the sweep's partials (one 8-byte word per chunk,
+  // [B][R1][chunks]).  The other paths use the partials as float2 pairs.
+  size_t off_abort = 0, off_dword = 0, off_cword = 0, off_part1 = 0;
   // counters: [B] overlap CTAs (zeroed by the first draw CTA of each batch row),
-  // then [B] draw CTAs that finished their segment sums (zeroed by the sweep)
-  size_t off_cnt = 0, cnt_bytes = 0, off_part1 = 0, off_rowstat = 0, off_state = 0,
-         off_segsum = 0, off_ctot = 0, off_alpha = 0, off_thr = 0, total = 0;
+  // then [B] draw CTAs that finished (zeroed by the sweep)
+  size_t off_cnt = 0, cnt_bytes = 0, off_rowstat = 0, off_state = 0, off_segsum = 0,
+         off_ctot = 0, off_alpha = 0, off_thr = 0, total = 0;
+  // bytes to zero before a fused round with `np` partials per row
+  size_t fused_zero_bytes(int B, int np) const {
+    return (off_part1 - off_abort) + (size_t)8 * B * R1 * np;
+  }
 };
 
 inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
   SamplePlan p;
   if (B <= 0) return p;
   p.R1 = 2 * gamma + 1;
-  p.nsplit1 = (int)ceil_div(V, kChunkSweep);
+  p.npmax = (int)max_row_partials(V);
   p.nsplit3 = (int)ceil_div(V, kChunkDraw);
-  // chunk partials: [row][8192-logit split] (generic sweep), or one per 4 KB block of
-  // the two logit arrays plus [row][2] edge pieces (vector sweep; fp32 has the most)
-  const int64_t nparts = vec_sweep_partials(B, gamma, V);
-  const int64_t nch_max = ceil_div(nparts, (int64_t)B * p.R1);
+  p.nrace = (int)race_slices(V);
   size_t o = 0;
+  p.off_abort = o;    o += sizeof(uint64_t);
+  p.off_dword = o;    o += sizeof(uint64_t) * 3 * (size_t)B;
+  p.off_cword = o;    o += sizeof(uint64_t) * 4 * (size_t)B * p.nrace;
+  p.off_part1 = o;    o = align_up(o + 8 * (size_t)B * p.R1 * (size_t)p.npmax);
   p.cnt_bytes = 2 * sizeof(uint32_t) * (size_t)B;
   p.off_cnt = o;      o = align_up(o + p.cnt_bytes);
   p.off_rowstat = o;  o = align_up(o + sizeof(RowStat) * (size_t)B * p.R1);
-  p.off_part1 = o;    o = align_up(o + 8 * (size_t)B * p.R1 * (size_t)nch_max);
   p.off_state = o;    o = align_up(o + sizeof(DrawState) * (size_t)B);
-  // draw: one fixed-point weight sum per 256-entry segment of the row drawn from
+  // inverse-transform draw: one fixed-point weight sum per 256-entry segment
   p.off_segsum = o;   o = align_up(o + sizeof(uint64_t) * (size_t)B * (size_t)ceil_div(V, 256));
   p.off_ctot = o;     o = align_up(o + sizeof(uint64_t) * (size_t)B * p.nsplit3);  // per draw CTA
-  p.off_alpha = o;    o = align_up(o + sizeof(float) * (size_t)B * gamma * p.nsplit1);
+  p.off_alpha = o;    o = align_up(o + sizeof(float) * (size_t)B * gamma * ceil_div(V, kChunkSweep));
   p.off_thr = o;      o = align_up(o + sizeof(float) * (size_t)B * p.R1);  // top-k thresholds
   p.total = o;
   return p;
@@ -149,9 +164,8 @@ struct LmPlan {
   int R1 = 0;   // 2*gamma+1 logit rows per batch row
   int nvt = 0;  // vocabulary tiles
   // ctl: [0] compact-row count, [1] pass-1 error, [2] pass-2 error (zeroed per call)
-  size_t off_ctl = 0, off_part = 0, off_zat = 0, off_state = 0, off_slot = 0,
-         off_csr = 0, off_csp = 0, off_tsr = 0, off_tsp = 0,
-         off_gsr = 0, off_gsp = 0, off_ct = 0, off_cd = 0, total = 0;
+  size_t off_ctl = 0, off_part = 0, off_zat = 0, off_state = 0, off_slot = 0, off_res2 = 0,
+         off_ct = 0, off_cd = 0, total = 0;
 };
 
 inline LmPlan make_lm_plan(int B, int gamma, int64_t V) {
@@ -168,14 +182,9 @@ inline LmPlan make_lm_plan(int B, int gamma, int64_t V) {
   p.off_zat = o;    o = align_up(o + sizeof(float) * rows);
   p.off_state = o;  o = align_up(o + sizeof(DrawState) * (size_t)B);
   p.off_slot = o;   o = align_up(o + sizeof(int) * (size_t)B);
-  // the draw: weight sums per 16-entry chunk, per tile and per group of 32 tiles
-  const size_t nchunk = (size_t)ceil_div(V, 16);
-  p.off_csr = o;    o = align_up(o + sizeof(float) * (size_t)B * nchunk);
-  p.off_csp = o;    o = align_up(o + sizeof(float) * (size_t)B * nchunk);
-  p.off_tsr = o;    o = align_up(o + sizeof(uint64_t) * (size_t)B * p.nvt);
-  p.off_tsp = o;    o = align_up(o + sizeof(uint64_t) * (size_t)B * p.nvt);
-  p.off_gsr = o;    o = align_up(o + sizeof(uint64_t) * (size_t)B * ((p.nvt + 31) / 32));
-  p.off_gsp = o;    o = align_up(o + sizeof(uint64_t) * (size_t)B * ((p.nvt + 31) / 32));
+  // the draw: per compact row and GEMM CTA (at most one per vocabulary tile) the
+  // best two race candidates of the residual and of p_n
+  p.off_res2 = o;   o = align_up(o + 4 * sizeof(LmCand) * (size_t)B * p.nvt);
   p.off_ct = o;     o = align_up(o + 2 * (size_t)B * kLmMaxHidden);
   p.off_cd = o;     o = align_up(o + 2 * (size_t)B * kLmMaxHidden);
   p.total = o;

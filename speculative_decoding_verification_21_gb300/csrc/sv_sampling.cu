@@ -1,27 +1,27 @@
-// sv_sampling.cu -- sampling verify on sm_103a.
+// sv_sampling.cu -- the sampling verify's separate kernels on sm_103a.
 //
 // One round for B independent batch rows, after Algorithm 1 of "Fast Inference
 // from Transformers via Speculative Decoding" (section "The loop: draft, verify
 // in one pass, keep a prefix") and the course notes "Speculative Decoding"
-// ("The algorithm").  Two kernels per call (three with the optional overlap),
-// chained by programmatic dependent launch:
+// ("The algorithm").  The plain round (and the lenient one) on rows that are a
+// multiple of 16 bytes long runs as one fused kernel (sv_round.cu).  The other
+// rounds -- top-k or top-p adjusted rows, rows of any length, the opt-in
+// inverse-transform sampler -- run as separate kernels chained by programmatic
+// dependent launch:
 //
 //   sweep     online softmax statistics of every chunk of all 2*gamma+1 logit
-//             rows: max and sum of 2^(y - max), y = z * T^-1 * log2 e.
-//             k_sweep_vec (rows whose byte length is a multiple of 16): a
-//             persistent kernel; every warp streams 4 KB chunks, interleaved
-//             across warps in batch-row order, two chunks in registers (one
-//             reduced while the next loads).  k_sweep (any shape): one CTA
-//             per 8192-logit chunk with 16-byte vector loads.
-//   k_draw    one CTA per (batch row, slice of at least 8192 entries).  Each
-//             CTA first takes its batch row's decision from the chunk partials:
-//             the row statistics, p(x_i), q(x_i), u_i, accept iff u_i <= p/q,
-//             first rejection by a warp ballot (the first CTA of the batch row
-//             writes the prefix and the draw set-up).  Then the target's own
-//             token -- bonus row p_gamma or residual max(0, p_n - q_n) -- by the
-//             inverse transform: each CTA sums the weights of its 256-entry
-//             segments, and the CTA of the batch row that finishes last finds
-//             the entry whose cumulative interval holds U W (sv_draw.cuh).
+//             rows, counted from each row's start: the largest logit and the
+//             sum of 2^(y - max y), y = z * T^-1 * log2 e.  k_sweep_vec (rows a
+//             multiple of 16 bytes): the persistent loop over 4 KB chunks of
+//             sv_units.cuh.  k_sweep (any shape): one CTA per 8192-logit split.
+//   top-k / top-p thresholds (k_topk_cand, k_topk, k_topp), then a thresholded
+//             sweep where needed.
+//   k_race    the default draw: one CTA per (batch row, slice); every CTA takes
+//             its batch row's decision from the partials (accept test, first
+//             rejection by a warp ballot), races its slice by Gumbel-max
+//             (sv_gumbel.cuh), and the CTA of the batch row that finishes last
+//             merges the slices' best two and emits.
+//   k_draw    the opt-in inverse-transform draw (sv_draw.cuh), same structure.
 //   k_alpha   optional overlap sum_v min(p_i, q_i) ("The acceptance rate is the
 //             overlap of p and q").
 #include <cuda_runtime.h>
@@ -36,7 +36,9 @@
 #include "sv_tma.cuh"
 #include "sv_decide.cuh"
 #include "sv_draw.cuh"
+#include "sv_gumbel.cuh"
 #include "sv_sweep.cuh"
+#include "sv_units.cuh"
 #include "sv_launch.h"
 
 namespace sv {
@@ -89,8 +91,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
   zero_draw_counters(x);
   const int R1 = 2 * x.gamma + 1;
   const int64_t item = blockIdx.x;  // (row, chunk) flattened, rows in batch-row order
-  const int64_t r = item / x.nch;
-  const int split = (int)(item - r * x.nch);
+  const int64_t r = item / x.np;
+  const int split = (int)(item - r * x.np);
   const int b = (int)(r / R1), k = (int)(r - (int64_t)b * R1);
   const float T = x.row_T ? __ldg(x.row_T + b) : x.temperature;
   const float c = log2_scale(inv_temperature(T));
@@ -128,173 +130,41 @@ __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
       });
 
   MS v = warp_reduce_ms(MS{mc, s});
+  const float zw = warp_max(zmax);
   __shared__ MS sm[kThreads / 32];
+  __shared__ float sz[kThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) sm[warp] = v;
+  if (lane == 0) {
+    sm[warp] = v;
+    sz[warp] = zw;
+  }
   __syncthreads();
   if (warp == 0) {
     v = (lane < (int)(blockDim.x >> 5)) ? sm[lane] : MS{-kInf, 0.0f};
     v = warp_reduce_ms(v);
-    if (lane == 0) x.part[item] = make_float2(v.m, v.s);
+    // the split's largest logit as given (its scaled max is v.m, bit for bit)
+    const float Z = warp_max((lane < (int)(blockDim.x >> 5)) ? sz[lane] : -kInf);
+    if (lane == 0) x.part[item] = make_float2(Z, v.s);
   }
 }
 
 // --------------------------------------------------------------------------
-// Vector sweep (rows a multiple of 16 bytes and at least 4 KB long): persistent,
-// one resident wave.  The target rows and the draft rows are two arrays, each
-// cut into 4 KB blocks aligned to 4 KB in memory (no load straddles two of the
-// DRAM's 4 KB blocks: 13% faster than blocks aligned to the rows).  Block g of
-// the two arrays in turn (the target array's first) goes to warp g mod W, so the
-// whole GPU walks memory in address order, and leaves one (max, sum) partial in
-// part[g]; the loop does nothing else (per-block row bookkeeping cost 13%).  A
-// block that holds the end of one row and the start of the next, or an array's
-// edge, is reduced all the same and its partial is never read: each row's two
-// edge pieces (from its start to the first block boundary, from the last one to
-// its end) are reduced first, one row per warp, into epart[row][0..1].  A warp
-// holds two blocks in registers: it reduces one while the 16-byte loads of the
-// next are in flight (non-allocating in L1: every byte is read once).
+// Vector sweep (rows a multiple of 16 bytes): persistent, one resident wave, the
+// 4 KB chunks of every row counted from the row's start (sv_units.cuh); one
+// partial per chunk, part[(b R1 + k) nck + j].
 // --------------------------------------------------------------------------
 template <int DT, bool TOPK>
 __global__ void __launch_bounds__(kSweepWarps * 32, kSweepCtasPerSm) k_sweep_vec(SweepCtx x) {
-  pdl_launch_dependents();  // the draw kernel may be scheduled now; it waits for us
+  pdl_launch_dependents();  // the next kernel may be scheduled now; it waits for us
   zero_draw_counters(x);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gamma = x.gamma;
-  const int R1 = 2 * gamma + 1;
-  const int64_t RB = x.V * ((DT == SV_F32) ? 4 : 2);  // row bytes, a multiple of 16, >= 4 KB
-  const char* const base0 = reinterpret_cast<const char*>(x.zt);
-  const char* const base1 = reinterpret_cast<const char*>(x.zd);
-  const int64_t AB0 = (int64_t)x.B * (gamma + 1) * RB, AB1 = (int64_t)x.B * gamma * RB;
-  const int64_t hd0 = (int64_t)(reinterpret_cast<uintptr_t>(base0) & 4095u);
-  const int64_t hd1 = (int64_t)(reinterpret_cast<uintptr_t>(base1) & 4095u);
-  const int64_t NC0 = (AB0 + hd0 + 4095) >> 12, NC1 = (AB1 + hd1 + 4095) >> 12;
+  const int64_t NU = (int64_t)x.B * (2 * x.gamma + 1) * x.np;
   const int64_t W = (int64_t)gridDim.x * kSweepWarps;
-  const int64_t w = (int64_t)blockIdx.x * kSweepWarps + warp;
-  const bool uniform_T = (x.row_T == nullptr);
-  const float c_all = log2_scale(inv_temperature(x.temperature));
-  auto scale_of = [&](int b) {
-    return uniform_T ? c_all : log2_scale(inv_temperature(__ldg(x.row_T + b)));
-  };
-  // n <= 256 consecutive 16-byte vectors of one row, and their (max, sum)
-  auto load_piece = [&](uint4 (&v)[8], const uint4* src, int nv) {
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      v[u] = (lane + 32 * u < nv) ? ld_stream16(src + lane + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
-  };
-  auto reduce_piece = [&](const uint4 (&v)[8], int nv, float c, float tau) {
-    if (nv <= 0) return make_float2(-kInf, 0.0f);
-    float zmax = -kInf, mc = -kInf, sacc = 0.0f, m = -kInf;
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (lane + 32 * u < nv) m = fmaxf(m, vmax<DT>(v[u]));
-    lane_raise_max(m, c, zmax, mc, sacc);
-    if (zmax > -kInf) {
-      float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (lane + 32 * u < nv) {
-          float f[VecInfo<DT>::kElems];
-          unpack<DT>(v[u], f);
-#pragma unroll
-          for (int e = 0; e < VecInfo<DT>::kElems; e += 2) {
-            s0 += (TOPK && f[e] < tau) ? 0.0f : ex2(fmaf(f[e], c, -mc));
-            s1 += (TOPK && f[e + 1] < tau) ? 0.0f : ex2(fmaf(f[e + 1], c, -mc));
-          }
-        }
-      }
-      sacc += s0 + s1;
-    }
-    const MS ms = warp_reduce_ms_fast(MS{mc, sacc});
-    return make_float2(ms.m, ms.s);
-  };
-
-  // ---- edge pieces: row q of the two arrays' rows goes to warp q mod W ----
-  const int64_t nrows = (int64_t)x.B * R1;
-  for (int64_t q = w; q < nrows; q += W) {
-    const bool arr = q >= (int64_t)x.B * (gamma + 1);
-    const int64_t ra = arr ? q - (int64_t)x.B * (gamma + 1) : q;
-    const int per = arr ? gamma : gamma + 1;
-    const int b = (int)ra / per, kk = (int)ra - b * per;
-    const int64_t rid = (int64_t)b * R1 + (arr ? gamma + 1 : 0) + kk;
-    const char* const rowp = (arr ? base1 : base0) + ra * RB;
-    const int64_t a0 = ra * RB + (arr ? hd1 : hd0), a1 = a0 + RB;  // 4 KB-block coordinates
-    const int64_t in0 = (a0 + 4095) & ~(int64_t)4095, in1 = a1 & ~(int64_t)4095;
-    const float c = scale_of(b);
-    const float tau = TOPK ? __ldg(x.thr + rid) : -kInf;
-    const uint4* rv = reinterpret_cast<const uint4*>(rowp);
-    // head [a0, in0) and tail [in1, a1), each shorter than 4 KB (in1 >= in0: a row is
-    // at least one block long); the loads of both in flight together
-    const int nh = (int)((in0 - a0) >> 4), nt = (int)((a1 - in1) >> 4);
-    uint4 vh[8], vt[8];
-    load_piece(vh, rv, nh);
-    load_piece(vt, rv + ((in1 - a0) >> 4), nt);
-    const float2 h = reduce_piece(vh, nh, c, tau);
-    const float2 t = reduce_piece(vt, nt, c, tau);
-    if (lane == 0) {
-      x.epart[2 * rid] = h;
-      x.epart[2 * rid + 1] = t;
-    }
-  }
-
-  // ---- every 4 KB block ----
-  const int64_t NC = NC0 + NC1;
-  if (w >= NC) return;
-  // the block's start, moved inside its array where the block crosses the array's edge
-  // (such a block's partial is never read)
-  auto src_of = [&](int64_t g) {
-    const bool arr = g >= NC0;
-    const int64_t AB = arr ? AB1 : AB0;
-    int64_t s = (arr ? g - NC0 : g) * 4096 - (arr ? hd1 : hd0);
-    s = s < 0 ? 0 : (s + 4096 > AB ? AB - 4096 : s);
-    return reinterpret_cast<const uint4*>((arr ? base1 : base0) + s);
-  };
-  auto load = [&](uint4 (&v)[8], int64_t g) {
-    const uint4* src = src_of(g);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = ld_stream16(src + lane + 32 * u);
-  };
-  // the batch row of block g's first vector, for a per-row temperature (a block that
-  // crosses into the next batch row is an edge block: its partial is not read)
-  auto batch_of = [&](int64_t g) {
-    if (uniform_T) return 0;
-    const bool arr = g >= NC0;
-    int64_t s = (arr ? g - NC0 : g) * 4096 - (arr ? hd1 : hd0);
-    s = s < 0 ? 0 : s;
-    return (int)((s / RB) / (arr ? gamma : gamma + 1));
-  };
-  auto fin = [&](const uint4 (&v)[8], int64_t g) {
-    float zmax = -kInf, mc = -kInf, sacc = 0.0f;
-    // top-k: the block's own row threshold is applied to its inner blocks by the
-    // row's own value (an edge block's partial is not read)
-    float tau = -kInf;
-    if (TOPK) {
-      const bool arr = g >= NC0;
-      int64_t s = (arr ? g - NC0 : g) * 4096 - (arr ? hd1 : hd0);
-      s = s < 0 ? 0 : s;
-      const int64_t ra = s / RB;
-      const int per = arr ? gamma : gamma + 1;
-      const int b = (int)ra / per;
-      tau = __ldg(x.thr + (int64_t)b * R1 + (arr ? gamma + 1 : 0) + ((int)ra - b * per));
-    }
-    chunk_update_full<DT, TOPK>(v, scale_of(batch_of(g)), tau, zmax, mc, sacc);
-    const MS ms = warp_reduce_ms_fast(MS{mc, sacc});
-    if (lane == 0) x.part[g] = make_float2(ms.m, ms.s);
-  };
-  uint4 va[8], vb[8];
-  int64_t ch = w;
-  load(va, ch);
-  for (;;) {
-    // a holds block ch; b gets ch + W while a is reduced, then the roles swap
-    const int64_t n1 = ch + W;
-    if (n1 < NC) load(vb, n1);
-    fin(va, ch);
-    if (n1 >= NC) break;
-    const int64_t n2 = n1 + W;
-    if (n2 < NC) load(va, n2);
-    fin(vb, n1);
-    if (n2 >= NC) break;
-    ch = n2;
-  }
+  unit_loop<DT, TOPK>(
+      x, x.np, (NU - 1) / W,
+      [&](int64_t g, float2 p) {
+        if ((threadIdx.x & 31) == 0) x.part[g] = p;
+      },
+      [](int64_t) {});
 }
 
 // --------------------------------------------------------------------------
@@ -479,7 +349,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_cand(SweepCtx x, int k,
     s_bad = 0;
   }
   __syncthreads();
-  // the row's max and whether it is usable
+  // the row's largest logit and whether it is usable
   float m = -kInf;
   int bad = 0;
   for (int j = threadIdx.x; j < nch; j += blockDim.x) {
@@ -504,8 +374,9 @@ __global__ void __launch_bounds__(kThreads) k_topk_cand(SweepCtx x, int k,
     if (threadIdx.x == 0) thr[row] = -kInf;
     return;
   }
-  const float M = s_max;
-  // lower bound of the threshold: the k-th largest scaled chunk max
+  const float Mz = s_max;     // the row's largest logit
+  const float M = Mz * c;     // its scaled max, bit for bit the sweep's
+  // lower bound of the threshold: the k-th largest chunk max
   const float bound = (k <= nch) ? radix_kth<SV_F32>(
                                        [&](auto&& f) {
                                          for (int j = threadIdx.x; j < nch; j += blockDim.x)
@@ -515,7 +386,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_cand(SweepCtx x, int k,
                                  : -kInf;
   if (bound > -kInf) {
     rowv([&](float z) {
-      if (z == z && z * c >= bound) {
+      if (z == z && z >= bound) {
         const uint32_t i = atomicAdd(&s_n, 1u);
         if (i < (uint32_t)kTopkCandCap) cand[i] = z;
       }
@@ -553,7 +424,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_cand(SweepCtx x, int k,
     float S = 0.0f;
     for (int w = 0; w < kWarps; ++w) S += s_red[w];
     thr[row] = tau;
-    *rp.at(0) = make_float2(M, S);
+    *rp.at(0) = make_float2(Mz, S);
   }
   for (int j = 1 + (int)threadIdx.x; j < nch; j += blockDim.x) *rp.at(j) = make_float2(-kInf, 0.0f);
 }
@@ -599,7 +470,7 @@ __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int 
   const float tk = has_k ? thr[row] : -kInf;
   if (!has_k && threadIdx.x == 0) thr[row] = -kInf;  // no cut unless one is found below
   if (warp == 0) {
-    const RowStat rs = combine_parts(row_parts<DT>(x, row), nullptr);
+    const RowStat rs = combine_parts(row_parts<DT>(x, row), nullptr, c);
     if (lane == 0) s_rs = rs;
   }
   __syncthreads();
@@ -732,20 +603,20 @@ __global__ void __launch_bounds__(kThreads) k_topp(SweepCtx x, float top_p, int 
 // sums of its segments; the CTA that finishes last (a counter per batch row)
 // draws the token from all of them by the inverse transform, falls back to p_n
 // when the residual has no positive weight, and emits.
+// The decision of batch row b taken by one CTA of the draw: the draft tokens and
+// the logits at them (read before waiting for the previous kernel), the row
+// statistics (one warp per logit row), then the accept test by warp 0.  Every
+// CTA of the batch row computes the same numbers; the lead CTA writes the
+// outputs of the decision.  The draw set-up lands in *s_st.
 template <int DT, bool TOPK>
-__global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, DrawArgs a) {
-  const int b = (int)(blockIdx.x / (unsigned)a.nsplit);
-  const int split = (int)(blockIdx.x - (unsigned)b * (unsigned)a.nsplit);
-  const int gamma = a.gamma;
+__device__ __forceinline__ void decide_in_cta(const SweepCtx& x, int b, bool lead,
+                                              uint32_t* alpha_cnt, RowStat* srs, DraftAt* sda,
+                                              DrawState* s_st) {
+  const int gamma = x.gamma;
   const int R1 = 2 * gamma + 1;
-  const int64_t V = a.V;
-  const bool lead = (split == 0);
+  const int64_t V = x.V;
   constexpr int kWarps = kThreads / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ RowStat srs[65];
-  __shared__ DraftAt sda[32];
-  __shared__ DrawState s_st;
-  __shared__ int s_last;
   if (warp == kWarps - 1 && lane < gamma) {
     // independent of the sweep: read before waiting for it
     DraftAt d;
@@ -754,16 +625,22 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
     if (d.x >= 0 && (int64_t)d.x < V) {
       d.zt = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, lane, gamma, V), d.x);
       d.zd = load_logit<DT>(row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + lane, gamma, V), d.x);
-      if (TOPK) {  // a draft token outside a row's top-k has probability 0 there
-        if (d.zt < __ldg(x.thr + (int64_t)b * R1 + lane)) d.zt = -kInf;
-        if (d.zd < __ldg(x.thr + (int64_t)b * R1 + gamma + 1 + lane)) d.zd = -kInf;
-      }
     }
     sda[lane] = d;
   }
-  pdl_wait();  // the sweep's partials
+  pdl_wait();  // the sweep's partials (and the top-k thresholds)
   pdl_launch_dependents();
-  if (lead && threadIdx.x == 0) a.alpha_cnt[b] = 0u;
+  if (TOPK && warp == kWarps - 1 && lane < gamma) {
+    // a draft token outside a row's top-k has probability 0 there
+    DraftAt d = sda[lane];
+    if (d.x >= 0 && (int64_t)d.x < V) {
+      if (d.zt < __ldcg(x.thr + (int64_t)b * R1 + lane)) d.zt = -kInf;
+      if (d.zd < __ldcg(x.thr + (int64_t)b * R1 + gamma + 1 + lane)) d.zd = -kInf;
+    }
+    sda[lane] = d;
+  }
+  if (lead && threadIdx.x == 0) alpha_cnt[b] = 0u;
+  const float c_b = log2_scale(inv_temperature(x.row_T ? __ldg(x.row_T + b) : x.temperature));
   for (int k = warp; k < R1; k += 2 * kWarps) {
     // rows k and k + kWarps together: one round of partial loads for R1 <= 16
     const int k2 = k + kWarps;
@@ -772,15 +649,31 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
     RowParts p2 = row_parts<DT>(x, k2 < R1 ? r2 : r0);
     if (k2 >= R1) p2.n = 0;
     combine_parts2(row_parts<DT>(x, r0), p2, lead ? x.rowstat + r0 : nullptr,
-                   lead ? x.rowstat + r2 : nullptr, rs0, rs2);
+                   lead ? x.rowstat + r2 : nullptr, rs0, rs2, c_b);
     if (lane == 0) {
       srs[k] = rs0;
       if (k2 < R1) srs[k2] = rs2;
     }
   }
   __syncthreads();
-  if (warp == 0) decide_batch_row<DT>(x, b, srs, sda, lead, &s_st);
+  if (warp == 0) decide_batch_row<DT>(x, b, srs, sda, lead, s_st);
   __syncthreads();
+}
+
+template <int DT, bool TOPK>
+__global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, DrawArgs a) {
+  const int b = (int)(blockIdx.x / (unsigned)a.nsplit);
+  const int split = (int)(blockIdx.x - (unsigned)b * (unsigned)a.nsplit);
+  const int gamma = a.gamma;
+  const int64_t V = a.V;
+  const bool lead = (split == 0);
+  constexpr int kWarps = kThreads / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ RowStat srs[65];
+  __shared__ DraftAt sda[32];
+  __shared__ DrawState s_st;
+  __shared__ int s_last;
+  decide_in_cta<DT, TOPK>(x, b, lead, a.alpha_cnt, srs, sda, &s_st);
   const DrawState st = s_st;
   if (st.mode == kDrawDone) return;  // the same in every CTA of the batch row
   const bool resid = (st.mode == kDrawResidual);
@@ -844,6 +737,92 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
     a.out_tokens[(int64_t)b * (gamma + 1) + st.pos] = tok;
     if (a.out_flags) a.out_flags[b] = (uint8_t)fl;
   }
+}
+
+// --------------------------------------------------------------------------
+// The target's own token by Gumbel-max after a separate sweep (the default
+// sampler on the rounds that do not run fused): one CTA per (batch row, spc race
+// slices of kRaceSlice entries).  Every CTA takes its batch row's decision,
+// each warp races slices w, w + 8, ... of the CTA's, the CTA keeps the best two
+// of the residual race and of p_n, and the CTA of the batch row that finishes
+// last (a per-batch-row counter the sweep zeroes) merges them and emits.
+// --------------------------------------------------------------------------
+struct RaceArgs {
+  uint64_t* cword;      // [B][nsplit][4] best two of the residual race and of p_n per CTA
+  uint32_t* alpha_cnt;  // [B] counters of the optional overlap kernel, zeroed here
+  uint32_t* done;       // [B] CTAs of the batch row that finished (zeroed by the sweep)
+  int nsplit;           // CTAs per batch row
+  int spc;              // race slices per CTA
+  bool vec;             // 16-byte loads of 8 entries are aligned in every row
+};
+
+template <int DT, bool TOPK>
+__global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_race(SweepCtx x, RaceArgs a) {
+  const int b = (int)(blockIdx.x / (unsigned)a.nsplit);
+  const int split = (int)(blockIdx.x - (unsigned)b * (unsigned)a.nsplit);
+  const int gamma = x.gamma;
+  const int64_t V = x.V;
+  constexpr int kWarps = kThreads / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ RowStat srs[65];
+  __shared__ DraftAt sda[32];
+  __shared__ DrawState s_st;
+  __shared__ RaceTop2 s_r[kWarps], s_p[kWarps];
+  __shared__ int s_last;
+  decide_in_cta<DT, TOPK>(x, b, split == 0, a.alpha_cnt, srs, sda, &s_st);
+  const DrawState st = s_st;
+  if (st.mode == kDrawDone) return;  // the same in every CTA of the batch row
+  const bool resid = st.mode == kDrawResidual;
+  const char* rt = row_ptr<DT>(x.zt, x.zd, b, st.pos, gamma, V);
+  const char* rd = resid ? row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + st.pos, gamma, V) : rt;
+  const float kd = resid ? __fsub_rn(st.K, st.mct) : 0.0f;
+  const int S = (int)race_slices(V);
+  const int s1 = min(S, (split + 1) * a.spc);
+  RaceTop2 tr = race_top2_empty(), tp = race_top2_empty();
+  for (int sl = split * a.spc + warp; sl < s1; sl += kWarps) {
+    const int64_t lo = (int64_t)sl * kRaceSlice;
+    const int64_t hi = (lo + kRaceSlice < V) ? lo + kRaceSlice : V;
+    if (resid)
+      race_range<DT, true, TOPK>(rt, rd, lo, hi, V, a.vec, st, kd, x.seed, x.round, b, tr, tp);
+    else
+      race_range<DT, false, TOPK>(rt, rd, lo, hi, V, a.vec, st, kd, x.seed, x.round, b, tr, tp);
+  }
+  tr = race_warp(tr);
+  tp = race_warp(tp);
+  if (lane == 0) {
+    s_r[warp] = tr;
+    s_p[warp] = tp;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    RaceTop2 r = (lane < kWarps) ? s_r[lane] : race_top2_empty();
+    RaceTop2 p = (lane < kWarps) ? s_p[lane] : race_top2_empty();
+    r = race_warp(r);
+    p = race_warp(p);
+    if (lane == 0) {
+      uint64_t* o = a.cword + ((int64_t)b * a.nsplit + split) * 4;
+      o[0] = key_word(race_key(r.a));
+      o[1] = key_word(race_key(r.b));
+      o[2] = key_word(race_key(p.a));
+      o[3] = key_word(race_key(p.b));
+      __threadfence();  // this CTA's candidates before its arrival
+      s_last = (atomicAdd(a.done + b, 1u) == (unsigned)(a.nsplit - 1)) ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  if (!s_last || warp != 0) return;
+  __threadfence();  // every other CTA's candidates are visible from here
+  KeyTop2 R{KeyIdx{-1.0f, -1}, KeyIdx{-1.0f, -1}}, P = R;
+  const uint64_t* cw = a.cword + (int64_t)b * a.nsplit * 4;
+  for (int j = lane; j < a.nsplit; j += 32) {
+    key_insert(R, key_unword(__ldcg(reinterpret_cast<const unsigned long long*>(cw) + 4 * j + 0)));
+    key_insert(R, key_unword(__ldcg(reinterpret_cast<const unsigned long long*>(cw) + 4 * j + 1)));
+    key_insert(P, key_unword(__ldcg(reinterpret_cast<const unsigned long long*>(cw) + 4 * j + 2)));
+    key_insert(P, key_unword(__ldcg(reinterpret_cast<const unsigned long long*>(cw) + 4 * j + 3)));
+  }
+  R = key_warp(R);
+  P = key_warp(P);
+  race_emit<DT>(x, b, st, R, P, false);
 }
 
 // --------------------------------------------------------------------------
@@ -961,6 +940,9 @@ static cudaError_t device_info(DeviceInfo** out) {
   return cudaSuccess;
 }
 
+cudaError_t launch_round(const SweepCtx& x, int dtype, char* ws, const SamplePlan& pl,
+                         cudaStream_t stream);
+
 template <int DT>
 static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t* xt, int B,
                                    int gamma, int64_t V, float temperature, const float* row_T,
@@ -968,7 +950,7 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
                                    int32_t* out_counts, float* out_p, float* out_q,
                                    float* out_alpha, uint8_t* out_flags, char* ws,
                                    const SamplePlan& pl, cudaStream_t stream, float lenience,
-                                   int top_k, float top_p) {
+                                   int top_k, float top_p, int sampler) {
   const int R1 = pl.R1;
   uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + pl.off_cnt);
   float2* part1 = reinterpret_cast<float2*>(ws + pl.off_part1);
@@ -991,17 +973,53 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   const bool masked = topk || topp;  // the round runs on thresholded rows
   const int tk = masked ? 1 : 0;
   const bool vec_sweep = use_vec_sweep(DT, V) && di->sweep_ctas_per_sm[DT][tk] > 0;
-  // generic sweep: [row][8192-logit split]; vector sweep: one partial per 4 KB block of
-  // the two arrays, then [row][2] edge pieces
+  // partials per row: 4 KB chunks (vector sweep) or kChunkSweep-logit splits
   const int nch = (int)ceil_div(V, kChunkSweep);
-  SweepCtx sx{zt, zd, xt, B, gamma, V, temperature, row_T, seed, round, nch, part1, rowstat,
-              state, out_tokens, out_counts, out_p, out_q, out_flags, 1.0f / lenience,
-              masked ? thr : nullptr, done,
-              vec_sweep ? part1 + vec_sweep_blocks(B, gamma, V) : nullptr};
+  SweepCtx sx{};
+  sx.zt = zt;
+  sx.zd = zd;
+  sx.xt = xt;
+  sx.B = B;
+  sx.gamma = gamma;
+  sx.V = V;
+  sx.temperature = temperature;
+  sx.row_T = row_T;
+  sx.seed = seed;
+  sx.round = round;
+  sx.np = vec_sweep ? (int)vec_sweep_chunks(DT, V) : nch;
+  sx.part = part1;
+  sx.rowstat = rowstat;
+  sx.state = state;
+  sx.out_tokens = out_tokens;
+  sx.out_counts = out_counts;
+  sx.out_p = out_p;
+  sx.out_q = out_q;
+  sx.out_flags = out_flags;
+  sx.inv_lenience = 1.0f / lenience;
+  sx.thr = masked ? thr : nullptr;
+  sx.done = done;
+  const auto alpha = [&]() -> cudaError_t {
+    if (!out_alpha) return cudaSuccess;
+    const int ns = (int)ceil_div(V, kChunkSweep);
+    k_alpha<DT><<<(unsigned)((int64_t)ns * gamma * B), kThreads, 0, stream>>>(
+        zt, zd, gamma, V, temperature, row_T, ns, rowstat, sx.thr, apart, alpha_cnt, out_alpha);
+    return cudaGetLastError();
+  };
+  if (!masked && vec_sweep && sampler == SV_SAMPLER_GUMBEL) {
+    // the plain (or lenient) round: one fused kernel
+    cudaError_t e = launch_round(sx, DT, ws, pl, stream);
+    if (e != cudaSuccess) return e;
+    if (out_alpha) {
+      // the overlap's counters start at zero (the fused round does not touch them)
+      e = cudaMemsetAsync(alpha_cnt, 0, sizeof(uint32_t) * (size_t)B, stream);
+      if (e != cudaSuccess) return e;
+    }
+    return alpha();
+  }
   auto sweep = [&](bool with_thr, const SweepCtx& ctx) {
     if (vec_sweep) {
       // one resident wave of warps, chunks dealt round-robin
-      const int64_t nc = vec_sweep_blocks(B, gamma, V);
+      const int64_t nc = (int64_t)B * R1 * ctx.np;
       const int64_t full = (int64_t)di->sms * di->sweep_ctas_per_sm[DT][with_thr ? 1 : 0];
       const int64_t need = ceil_div(nc, kSweepWarps);
       const int64_t g = full < need ? full : need;
@@ -1042,32 +1060,44 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
     sweep(masked, sx);
     mark(1, stream);
   }
-  // One resident wave of draw CTAs when the batch allows: every CTA takes its
-  // batch row's decision before drawing, so a second wave would pay that
-  // latency again.  At least kChunkDraw entries per CTA.
-  const int64_t nseg = ceil_div(V, kDrawSegEntries);
-  int64_t nsplit = pl.nsplit3;
-  const int64_t slots = (int64_t)di->sms * kDrawCtasPerSm;
-  if ((int64_t)B * nsplit > slots) nsplit = (slots / B > 1) ? slots / B : 1;
-  const int64_t spc = ceil_div(nseg, nsplit);
-  nsplit = ceil_div(nseg, spc);  // no CTA without segments
   const int64_t vec_elems = (DT == SV_F32) ? 4 : 8;
   const bool vec = (V % vec_elems) == 0 && (reinterpret_cast<uintptr_t>(zt) % 16) == 0 &&
                    (reinterpret_cast<uintptr_t>(zd) % 16) == 0;
-  DrawArgs da{zt, zd, B, gamma, V, seed, round, alpha_cnt, done, segsum, ctot, fix_shift(V),
-              (int)nseg, (int)nsplit, (int)spc, vec, out_tokens, out_flags};
-  cudaError_t e = masked ? launch_pdl(k_draw<DT, true>, dim3((unsigned)(nsplit * B)),
-                                      dim3(kThreads), 0, stream, sx, da)
-                       : launch_pdl(k_draw<DT, false>, dim3((unsigned)(nsplit * B)),
-                                    dim3(kThreads), 0, stream, sx, da);
+  const int64_t slots = (int64_t)di->sms * kDrawCtasPerSm;
+  cudaError_t e = cudaSuccess;
+  if (sampler == SV_SAMPLER_INVERSE) {
+    // One resident wave of draw CTAs when the batch allows: every CTA takes its
+    // batch row's decision before drawing, so a second wave would pay that
+    // latency again.  At least kChunkDraw entries per CTA.
+    const int64_t nseg = ceil_div(V, kDrawSegEntries);
+    int64_t nsplit = pl.nsplit3;
+    if ((int64_t)B * nsplit > slots) nsplit = (slots / B > 1) ? slots / B : 1;
+    const int64_t spc = ceil_div(nseg, nsplit);
+    nsplit = ceil_div(nseg, spc);  // no CTA without segments
+    DrawArgs da{zt, zd, B, gamma, V, seed, round, alpha_cnt, done, segsum, ctot, fix_shift(V),
+                (int)nseg, (int)nsplit, (int)spc, vec, out_tokens, out_flags};
+    e = masked ? launch_pdl(k_draw<DT, true>, dim3((unsigned)(nsplit * B)), dim3(kThreads), 0,
+                            stream, sx, da)
+               : launch_pdl(k_draw<DT, false>, dim3((unsigned)(nsplit * B)), dim3(kThreads), 0,
+                            stream, sx, da);
+  } else {
+    // Gumbel-max: one resident wave of race CTAs when the batch allows, at least
+    // two slices per CTA
+    const int64_t S = race_slices(V);
+    int64_t nsplit = (S + 1) / 2;
+    if ((int64_t)B * nsplit > slots) nsplit = (slots / B > 1) ? slots / B : 1;
+    const int64_t spc = ceil_div(S, nsplit);
+    nsplit = ceil_div(S, spc);  // no CTA without slices
+    RaceArgs ra{reinterpret_cast<uint64_t*>(ws + pl.off_cword), alpha_cnt, done, (int)nsplit,
+                (int)spc, vec};
+    e = masked ? launch_pdl(k_race<DT, true>, dim3((unsigned)(nsplit * B)), dim3(kThreads), 0,
+                            stream, sx, ra)
+               : launch_pdl(k_race<DT, false>, dim3((unsigned)(nsplit * B)), dim3(kThreads), 0,
+                            stream, sx, ra);
+  }
   if (e != cudaSuccess) return e;
   mark(2, stream);
-  if (out_alpha) {
-    const int ns = (int)ceil_div(V, kChunkSweep);
-    k_alpha<DT><<<(unsigned)((int64_t)ns * gamma * B), kThreads, 0, stream>>>(
-        zt, zd, gamma, V, temperature, row_T, ns, rowstat, sx.thr, apart, alpha_cnt, out_alpha);
-  }
-  return cudaGetLastError();
+  return alpha();
 }
 
 cudaError_t launch_sample(const void* zt, const void* zd, const int32_t* xt, int B, int gamma,
@@ -1075,15 +1105,15 @@ cudaError_t launch_sample(const void* zt, const void* zd, const int32_t* xt, int
                           uint64_t seed, uint64_t round, int32_t* out_tokens, int32_t* out_counts,
                           float* out_p, float* out_q, float* out_alpha, uint8_t* out_flags,
                           void* ws, const SamplePlan& pl, cudaStream_t stream, float lenience,
-                          int top_k, float top_p) {
+                          int top_k, float top_p, int sampler) {
   char* w = reinterpret_cast<char*>(ws);
   if (dtype == SV_F32)
     return launch_sample_t<SV_F32>(zt, zd, xt, B, gamma, V, temperature, row_T, seed, round,
                                    out_tokens, out_counts, out_p, out_q, out_alpha, out_flags, w,
-                                   pl, stream, lenience, top_k, top_p);
+                                   pl, stream, lenience, top_k, top_p, sampler);
   return launch_sample_t<SV_BF16>(zt, zd, xt, B, gamma, V, temperature, row_T, seed, round,
                                   out_tokens, out_counts, out_p, out_q, out_alpha, out_flags, w,
-                                  pl, stream, lenience, top_k, top_p);
+                                  pl, stream, lenience, top_k, top_p, sampler);
 }
 
 }  // namespace sv

@@ -92,6 +92,83 @@ __device__ __forceinline__ void chunk_update_full(const uint4 (&v)[8], float c, 
   sacc += (s0 + s1) + (s2 + s3);
 }
 
+// A chunk shorter than 4 KB (the end of a row): lanes hold vectors lane + 32u
+// for lane + 32u < nv; the same arithmetic as a full chunk otherwise.
+template <int DT, bool TOPK = false>
+__device__ __forceinline__ void chunk_update_part(const uint4 (&v)[8], int nv, float c, float tau,
+                                                  float& zmax, float& mc, float& sacc) {
+  const int lane = threadIdx.x & 31;
+  float m = -kInf;
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    if (lane + 32 * u < nv) m = fmaxf(m, vmax<DT>(v[u]));
+  lane_raise_max(m, c, zmax, mc, sacc);
+  if (!(zmax > -kInf)) return;
+  float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    if (lane + 32 * u < nv) {
+      float f[VecInfo<DT>::kElems];
+      unpack<DT>(v[u], f);
+#pragma unroll
+      for (int e = 0; e < VecInfo<DT>::kElems; e += 2) {
+        s0 += (TOPK && f[e] < tau) ? 0.0f : ex2(fmaf(f[e], c, -mc));
+        s1 += (TOPK && f[e + 1] < tau) ? 0.0f : ex2(fmaf(f[e + 1], c, -mc));
+      }
+    }
+  }
+  sacc += s0 + s1;
+}
+
+// The chunk's partial from the lanes' (largest logit, scaled max, sum): the
+// largest logit z of the chunk as given, and the sum of 2^(y - z c) (z c is the
+// largest of the lanes' scaled maxima, bit for bit: scaling is monotone).
+__device__ __forceinline__ float2 warp_chunk_partial(float zmax, float mc, float sacc, float c) {
+  const float Z = warp_max(zmax);
+  const float M = Z * c;
+  float s = (mc > -kInf) ? sacc * ex2(mc - M) : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return make_float2(Z, (M > -kInf) ? s : 0.0f);
+}
+
+// Chunks of the vector sweep: row k of batch row b is cut into nck chunks of
+// 4 KB from its start, unit g = (b R1 + k) nck + j.  A warp walks g, g + W,
+// g + 2W, ...; the cursor (b, k, j) advances by fixed increments (no division
+// in the loop: the next chunk's address is ready before its loads are due).
+struct UnitCursor {
+  int b, k, j;
+};
+struct UnitWalk {
+  int R1, nck, dj, dk, db;
+  __device__ __forceinline__ void init(int R1_, int nck_, int W) {
+    R1 = R1_;
+    nck = nck_;
+    dj = W % nck;
+    const int dr = W / nck;
+    dk = dr % R1;
+    db = dr / R1;
+  }
+  __device__ __forceinline__ UnitCursor at(int64_t g) const {
+    const int64_t r = g / nck;
+    return UnitCursor{(int)(r / R1), (int)(r % R1), (int)(g - r * nck)};
+  }
+  __device__ __forceinline__ void step(UnitCursor& c) const {
+    c.j += dj;
+    int k = c.k + dk;
+    if (c.j >= nck) {
+      c.j -= nck;
+      ++k;
+    }
+    c.b += db;
+    if (k >= R1) {
+      k -= R1;
+      ++c.b;
+    }
+    c.k = k;
+  }
+};
+
 // Warp max of m, then one rescale per lane and a warp sum.
 __device__ __forceinline__ MS warp_reduce_ms_fast(MS v) {
   const float M = warp_max(v.m);

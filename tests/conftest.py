@@ -24,3 +24,15 @@ def golden():
             return json.load(f)
 
     return load
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Decision and near-tie counts of the GPU parity tests, printed under -q too."""
+    from tests._parity import RECORD
+    if not RECORD:
+        return
+    terminalreporter.write_sep("-", "parity: decisions and near-ties (|u - p/q| < 1e-6 or "
+                                    "Gumbel top-2 gap < 1e-6, on the oracle's values)")
+    for what, dec, near, near_o in RECORD:
+        terminalreporter.write_line(f"{what}: {dec} decisions, {near} differing at a near-tie, "
+                                    f"{near_o} near-ties in the oracle's round")

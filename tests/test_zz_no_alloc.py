@@ -63,12 +63,18 @@ def test_noalloc_matches_spec_verify_on_two_calls_in_a_row():
     stream = torch.cuda.current_stream()
     # two calls in a row with different sizes, so the second starts from the
     # first call's leftovers in the shared scratch array
+    # a third case in fp32 logits with a per-row temperature
+    w3 = wl.sample_b64(sigma=1.0, B=16, gamma=2, V=4000, seed=79)
+    w3.zt, w3.zd = w3.zt.float().contiguous(), w3.zd.float().contiguous()
+    w3.row_temperature = torch.linspace(0.5, 1.5, w3.B, device=w3.zt.device)
     cases = [(wl.sample_b64(sigma=1.0, B=32, gamma=4, V=50000, seed=77), 5, 0),
-             (wl.sample_b64(sigma=0.5, B=48, gamma=3, V=32771, seed=78), 5, 1)]
+             (wl.sample_b64(sigma=0.5, B=48, gamma=3, V=32771, seed=78), 5, 1),
+             (w3, 6, 2)]
     for w, seed, rnd in cases:
         assert sv.workspace_bytes(w.B, w.gamma, w.V, 0) <= LIMIT
         got = _call_noalloc(w, seed, rnd, stream)
-        ref = sv.spec_verify(w.zt, w.zd, w.xt, temperature=w.temperature, seed=seed, round=rnd,
+        ref = sv.spec_verify(w.zt, w.zd, w.xt, temperature=w.temperature,
+                             row_temperature=w.row_temperature, seed=seed, round=rnd,
                              want_alpha=True)
         torch.cuda.synchronize()
         assert torch.equal(got["tokens"], ref["tokens"])
