@@ -1,16 +1,21 @@
 #!/usr/bin/env python3
 """Benchmark of the verify-and-sample step on GB300.
 
-One step = one call of spec_verify (softmax sweep over all 2*gamma+1 logit rows,
-accept test, residual/bonus draw) on one round of the sample_b64 workload:
+One step = one call of spec_verify on one round of the sample_b64 workload:
 B=64, gamma=4, V=128256, bf16 logits, T=0.8, draft noise sigma=1 (Zipf(1.1)
-target bias).  Metric: verify rounds per second (whole job, all GPUs); the
-line also carries verified positions/s (B*gamma per round).
+target bias).  The call is one fused kernel (softmax sweep over all 2*gamma+1
+logit rows, accept test, Gumbel-max residual/bonus draw) after a small memset of
+its hand-over words.  Metric: verify rounds per second (whole job, all GPUs);
+the line also carries verified positions/s (B*gamma per round).
 
 Timing: W untimed warm-up steps, then K steps between a barrier +
 cuda.synchronize() on both sides, CUDA events on the launching stream, max over
 ranks.  Inputs rotate through enough sets to exceed 4x the L2 size, so no step
-reads logits the previous step left in L2.
+reads logits the previous step left in L2.  Per-kernel times come from a
+separate loop of at least 200 calls with the library's timing events, with the
+SM clocks sampled during it.  The other workloads (B=1 fp32, B=256 gamma=8,
+the draft-noise sweep, greedy, the fused LM heads, the round's variants) are
+reported in the same line.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
@@ -36,7 +41,8 @@ if ROOT not in sys.path:
 METRIC = "spec_verify rounds/s & positions/s at B=64,γ=4,V=128256; HBM GB/s % of peak"
 UNIT = "rounds/s"
 WORKLOAD = dict(workload="sample_b64", B=64, gamma=4, V=128256, dtype="bf16", temperature=0.8,
-                sigma=1.0, target="N(0,2^2)+Zipf(1.1) bias", draft="target+N(0,sigma^2)")
+                sigma=1.0, seed=1003, target="N(0,2^2)+Zipf(1.1) bias",
+                draft="target+N(0,sigma^2)")
 
 
 def parse():
@@ -44,6 +50,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--kernel-reps", type=int, default=400,
+                    help="calls of the per-kernel timing loop (at least 200)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sigma", type=float, default=1.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -76,8 +84,27 @@ def tensor_peaks():
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture of the same
 # workload (profiles/ holds the summary); None when the kernel changed since.
-SWEEP_TRAFFIC_BYTES = 151403776  # 148485120 read + 2918656 written, profiles/k_sweep_vec_sample_b64.md
+ROUND_TRAFFIC_BYTES = None
 LMHEAD_PASS1_TRAFFIC_BYTES = 1580866592  # 1577.972 MB read + 2.895 MB written, profiles/k_lm_lmhead.md
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
 
 
 class ClockSampler:
@@ -217,7 +244,7 @@ def run_reference(args):
             "config": dict(WORKLOAD, sigma=args.sigma),
             "positions_per_s": val * 64 * 4,
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -227,102 +254,135 @@ def run_reference(args):
 # ----------------------------------------------------------------------------
 # Our arm.
 # ----------------------------------------------------------------------------
+def _verify_call(L, stream, sets, tokens, counts, flags, ws, B, gamma, V, dt):
+    """A spec_verify call on input set i % len(sets), round i (seed 0)."""
+    import speculative_decoding_verification_21_gb300 as sv
+    P = ctypes.c_void_p
+    sh = P(stream.cuda_stream)
+    argsets = [(P(s.zt.data_ptr()), P(s.zd.data_ptr()), P(s.xt.data_ptr()), B, gamma, V, dt,
+                ctypes.c_float(s.temperature),
+                None if s.row_temperature is None else P(s.row_temperature.data_ptr()))
+               for s in sets]
+    tail = (P(tokens.data_ptr()), P(counts.data_ptr()), None, None, None, P(flags.data_ptr()),
+            P(ws.data_ptr()), ctypes.c_size_t(ws.numel()), sh)
+    fn = L.spec_verify
+
+    def call(i):
+        rc = fn(*argsets[i % len(argsets)], 0, i, *tail)
+        if rc != 0:
+            raise RuntimeError(f"spec_verify failed: {sv.status_string(rc)}")
+    return call
+
+
+def _rotation(make, per_bytes, dev):
+    """Input sets of one workload whose logits add up to at least 4x the L2."""
+    import torch
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2**20)
+    n = max(2, -(-4 * l2 // per_bytes))
+    return [make(k) for k in range(n)], l2
+
+
+def measure_sampling(L, dev, stream, name, sets, B, gamma, V, dt, reps, extra_keys=None):
+    """Back-to-back rounds/s of spec_verify on rotating input sets, the per-kernel
+    times from the library's events (the fused round: its memset and k_round),
+    and the HBM roofline of the round's kernel on the logit bytes."""
+    import torch
+    import speculative_decoding_verification_21_gb300 as sv
+    tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    counts = torch.empty((B,), dtype=torch.int32, device=dev)
+    flags = torch.empty((B,), dtype=torch.uint8, device=dev)
+    ws = sv.alloc_workspace(B, gamma, V, 0, device=dev)
+    call = _verify_call(L, stream, sets, tokens, counts, flags, ws, B, gamma, V, dt)
+    kms, ms = _kernel_times(L, stream, call, 2, reps)
+    hbm, kind = peaks()
+    esz = 4 if dt == 0 else 2
+    nbytes = B * (2 * gamma + 1) * V * esz
+    gbs = nbytes / (kms[1] / 1000.0) / 1e9
+    acc = 0
+    for i in range(len(sets)):
+        call(i)
+        acc += int(counts.sum().item())
+    out = {"workload": name, "B": B, "gamma": gamma, "V": V,
+           "dtype": "f32" if dt == 0 else "bf16",
+           "rounds_per_s": 1000.0 / ms, "positions_per_s": 1000.0 / ms * B * gamma,
+           "ms_per_round": ms, "kernel_ms": {"memset": kms[0], "k_round": kms[1]},
+           "mean_accepted": acc / (len(sets) * B),
+           "roofline": {"bound": "hbm", "kernel": "k_round", "achieved": gbs, "peak": hbm,
+                        "peak_kind": kind, "unit": "GB/s", "frac": gbs / hbm,
+                        "frac_of_8TBs": gbs / 8000.0, "algorithmic_bytes": nbytes,
+                        "step_frac": nbytes / (ms / 1000.0) / 1e9 / hbm},
+           "l2_policy": f"inputs rotate over {len(sets)} sets",
+           "gpu_launches_per_round": 1}
+    if extra_keys:
+        out.update(extra_keys)
+    return out
+
+
 def run_ours(args):
     import torch
 
     import speculative_decoding_verification_21_gb300 as sv
-    from speculative_decoding_verification_21_gb300 import _lib
     from speculative_decoding_verification_21_gb300 import workloads as wl
 
     world, rank, local = dist_setup(args)
     L = sv.load(build_if_missing=False)
     dev = torch.device("cuda", local)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", 126 * 2**20)
     B, gamma, V = 64, 4, 128256
+    seed0 = WORKLOAD["seed"]
 
-    # input sets: rotate through >= 4x L2 of logits
-    base = wl.sample_b64(sigma=args.sigma, seed=1003 + 17 * rank, device=dev)
+    # input sets: rotate through >= 4x L2 of logits; each rank its own replica
+    base = wl.sample_b64(sigma=args.sigma, seed=seed0 + 17 * rank, device=dev)
     set_bytes = base.logit_bytes
-    nsets = max(2, -(-4 * l2 // set_bytes))
-    sets = [base] + [wl.sample_b64(sigma=args.sigma, seed=1003 + 17 * rank + 1000 * k, device=dev)
-                     for k in range(1, nsets)]
+    sets, l2 = _rotation(lambda k: base if k == 0 else wl.sample_b64(
+        sigma=args.sigma, seed=seed0 + 17 * rank + 1000 * k, device=dev), set_bytes, dev)
+    nsets = len(sets)
     stream = torch.cuda.current_stream(dev)
-    sh = ctypes.c_void_p(stream.cuda_stream)
     tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
     counts = torch.empty((B,), dtype=torch.int32, device=dev)
     flags = torch.empty((B,), dtype=torch.uint8, device=dev)
     ws = sv.alloc_workspace(B, gamma, V, 0, device=dev)
-    P = ctypes.c_void_p
-    argsets = []
-    for s in sets:
-        argsets.append((P(s.zt.data_ptr()), P(s.zd.data_ptr()), P(s.xt.data_ptr()), B, gamma, V,
-                        1, ctypes.c_float(s.temperature), None))
-    tail = (P(tokens.data_ptr()), P(counts.data_ptr()), None, None, None, P(flags.data_ptr()),
-            P(ws.data_ptr()), ctypes.c_size_t(ws.numel()), sh)
-    fn = L.spec_verify
-
-    def step(i):
-        a = argsets[i % nsets]
-        rc = fn(*a, 0, i, *tail)
-        if rc != 0:
-            raise RuntimeError(f"spec_verify failed: {sv.status_string(rc)}")
-
-    # per-kernel events on a subset of the timed steps
-    EVERY = 16
-    n_ev = args.steps // EVERY + 1
-    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ev)]
-    for es in evsets:  # materialise the underlying cudaEvent_t before taking handles
-        for e in es:
-            e.record(stream)
-    torch.cuda.synchronize(dev)
-    evptrs = [(ctypes.c_void_p * 3)(*[ctypes.c_void_p(e.cuda_event) for e in es])
-              for es in evsets]
-    assert all(e.cuda_event for es in evsets for e in es)
+    step = _verify_call(L, stream, sets, tokens, counts, flags, ws, B, gamma, V, 1)
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
     barrier(world)
     torch.cuda.synchronize(dev)
-
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         start.record(stream)
-        k = 0
         for i in range(args.steps):
-            if i % EVERY == 0:
-                L.sv_set_timing_events(ctypes.cast(evptrs[k], ctypes.c_void_p), 3)
-                step(args.warmup + i)
-                L.sv_set_timing_events(None, 0)
-                k += 1
-            else:
-                step(args.warmup + i)
+            step(args.warmup + i)
         stop.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
     ms = start.elapsed_time(stop)
     ms = max_over_ranks(ms, world)
-    kern = {"k_sweep": [], "k_draw": []}
-    for es in evsets[:k]:
-        kern["k_sweep"].append(es[0].elapsed_time(es[1]))
-        kern["k_draw"].append(es[1].elapsed_time(es[2]))  # the decision, the draw, the select
-    kavg = {n: (sum(v) / len(v) if v else None) for n, v in kern.items()}
-
     rounds_per_s = world * args.steps / (ms / 1000.0)
+
+    # per-kernel times: a separate loop of >= 200 calls with the library's events
+    reps = max(200, args.kernel_reps)
+    with ClockSampler(local) as kclk:
+        kms, call_ms = _kernel_times(L, stream, step, 2, reps)
+    kavg = {"memset": kms[0], "k_round": kms[1], "call": call_ms}
     hbm, peak_kind = peaks()
     sweep_bytes = B * (2 * gamma + 1) * V * 2
-    sweep_gbs = sweep_bytes / (kavg["k_sweep"] / 1000.0) / 1e9
+    round_gbs = sweep_bytes / (kms[1] / 1000.0) / 1e9
 
     # end-to-end through the C ABI with host buffers (pinned), copies inside the timed region
     e2e = None
     if not args.no_e2e:
+        fn = L.spec_verify
+        P = ctypes.c_void_p
+        sh = P(stream.cuda_stream)
         hz = [(s.zt.cpu().pin_memory(), s.zd.cpu().pin_memory(), s.xt.cpu().pin_memory())
               for s in sets[:2]]
         dzt, dzd, dxt = torch.empty_like(base.zt), torch.empty_like(base.zd), torch.empty_like(
             base.xt)
         htok = torch.empty((B, gamma + 1), dtype=torch.int32).pin_memory()
         hcnt = torch.empty((B,), dtype=torch.int32).pin_memory()
+        tail = (P(tokens.data_ptr()), P(counts.data_ptr()), None, None, None,
+                P(flags.data_ptr()), P(ws.data_ptr()), ctypes.c_size_t(ws.numel()), sh)
         e2e_steps = max(20, min(400, args.steps // 50))
 
         def e2e_step(i):
@@ -360,19 +420,24 @@ def run_ours(args):
         w_np = (wl.to_oracle(base.zt), wl.to_oracle(base.zd), base.xt.cpu().numpy(),
                 base.temperature, B)
         val, rows, steps_done, el = oracle_rounds_per_s(w_np, args.cpu_seconds)
-        cpu = {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
+        cpu = {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "cpu_model": cpu_model(),
                "sample": f"{rows} batch rows ({rows / B:.2f} rounds) of this workload, "
                          f"single-threaded, {el:.1f} s"}
 
     extra = {}
     if not args.no_extra:
+        del sets
+        torch.cuda.empty_cache()
+        extra["configs"] = measure_configs(L, dev, stream, rank, reps)
         extra["greedy"] = measure_greedy(L, dev, stream, rank)
         extra["lmhead"] = measure_lmhead(L, dev, stream, rank)
         extra["lmhead_draft"] = measure_draft(L, dev, stream, rank)
-        extra["lenience"] = measure_options(L, stream, sets, tokens, counts, flags, ws,
+        osets = [wl.sample_b64(sigma=args.sigma, seed=seed0 + 17 * rank + 1000 * k, device=dev)
+                 for k in range(nsets)]
+        extra["lenience"] = measure_options(L, stream, osets, tokens, counts, flags, ws,
                                             lenience=0.5)
-        extra["top_k"] = measure_options(L, stream, sets, tokens, counts, flags, ws, top_k=50)
-        extra["top_p"] = measure_options(L, stream, sets, tokens, counts, flags, ws, top_p=0.9)
+        extra["top_k"] = measure_options(L, stream, osets, tokens, counts, flags, ws, top_k=50)
+        extra["top_p"] = measure_options(L, stream, osets, tokens, counts, flags, ws, top_p=0.9)
 
     if rank == 0:
         line = {
@@ -380,18 +445,21 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": dict(WORKLOAD, sigma=args.sigma, l2_policy=(
-                f"inputs rotate over {nsets} sets of {set_bytes / 1e6:.1f} MB "
-                f"(>= 4x L2 {l2 / 2**20:.0f} MiB)"), parallelism=f"replicas x{world}"),
+            "config": dict(WORKLOAD, sigma=args.sigma),
+            "l2_policy": (f"inputs rotate over {nsets} sets of {set_bytes / 1e6:.1f} MB "
+                          f"(>= 4x L2 {l2 / 2**20:.0f} MiB)"),
+            "parallelism": f"replicas x{world}",
             "positions_per_s": rounds_per_s * B * gamma,
-            "step_effective_gbs": world * sweep_bytes * args.steps / (ms / 1000.0) / 1e9 / world,
-            "roofline": {"bound": "hbm", "kernel": "k_sweep", "achieved": sweep_gbs,
+            "step_effective_gbs": sweep_bytes * args.steps / (ms / world / 1000.0) / 1e9 / world,
+            "roofline": {"bound": "hbm", "kernel": "k_round", "achieved": round_gbs,
                          "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": sweep_gbs / hbm, "frac_of_8TBs": sweep_gbs / 8000.0,
-                         "traffic": SWEEP_TRAFFIC_BYTES, "algorithmic_bytes": sweep_bytes},
+                         "frac": round_gbs / hbm, "frac_of_8TBs": round_gbs / 8000.0,
+                         "traffic": ROUND_TRAFFIC_BYTES, "algorithmic_bytes": sweep_bytes,
+                         "timing": f"CUDA events around k_round, {reps} calls"},
             "kernel_ms": kavg,
-            "gpu_launches": 2 * args.steps,  # k_sweep(_tma), k_draw
+            "gpu_launches": args.steps,  # k_round (plus a memset of its hand-over words)
             "clocks": clk.summary(),
+            "clocks_kernel_loop": kclk.summary(),
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
@@ -399,13 +467,47 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
+def measure_configs(L, dev, stream, rank, reps):
+    """The other sampling workloads: B=1 fp32 (launch-bound), the draft-noise
+    sweep of sample_b64, and B=256 gamma=8 with per-row temperatures."""
+    import torch
+    from speculative_decoding_verification_21_gb300 import workloads as wl
+    out = {}
+    # sample_b1: B=1, gamma=4, V=32000 fp32 -- one generation of many rows, one row per set
+    per = 9 * 32000 * 4
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2**20)
+    nrow = -(-4 * l2 // per)
+    big = wl.sample_b1(seed=1001 + 7 * rank, device=dev, B=nrow)
+    sets = [wl.Workload("sample_b1", 1, 4, 32000, torch.float32, big.temperature,
+                        big.zt[b:b + 1], big.zd[b:b + 1], big.xt[b:b + 1]) for b in range(nrow)]
+    out["sample_b1"] = measure_sampling(L, dev, stream, "sample_b1", sets, 1, 4, 32000, 0, reps)
+    del sets, big
+    for sig in (0.25, 4.0):
+        sets, _ = _rotation(lambda k: wl.sample_b64(sigma=sig, seed=1003 + 17 * rank + 1000 * k,
+                                                    device=dev), 64 * 9 * 128256 * 2, dev)
+        out[f"sample_b64_sigma{sig:g}"] = measure_sampling(
+            L, dev, stream, f"sample_b64 sigma={sig:g}", sets, 64, 4, 128256, 1, reps,
+            {"sigma": sig})
+        del sets
+        torch.cuda.empty_cache()
+    sets, _ = _rotation(lambda k: wl.sample_b256(seed=1004 + 17 * rank + 1000 * k, device=dev),
+                        256 * 17 * 152064 * 2, dev)
+    out["sample_b256"] = measure_sampling(L, dev, stream, "sample_b256", sets, 256, 8, 152064, 1,
+                                          max(200, reps // 2),
+                                          {"note": "per-row T ~ U[0.5,1.5], sigma ~ U[0.1,3], "
+                                                   "-inf on 1% of tokens in 10% of draft rows"})
+    del sets
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_options(L, stream, sets, tokens, counts, flags, ws, lenience=1.0, top_k=0,
                     top_p=1.0, reps=400):
     """spec_verify_opts on the same rotating sample_b64 sets.  Lenience l: the
-    comparison u <= p/(l q) costs the same kernels and accepts more.  top_k:
-    one radix-select pass over every row before the sweep, and the round on the
-    adjusted rows.  top_p: a sweep for the row maxima, the nucleus cut, then the
-    round on the adjusted rows."""
+    comparison u <= p/(l q) runs in the same fused round and accepts more.
+    top_k: a sweep, the threshold from the candidates at or above the k-th
+    largest chunk maximum, and the race on the adjusted rows.  top_p: a sweep for
+    the row maxima, the nucleus cut, the thresholded sweep and the race."""
     import torch
     from speculative_decoding_verification_21_gb300 import _lib
     P = ctypes.c_void_p
@@ -442,7 +544,8 @@ def measure_options(L, stream, sets, tokens, counts, flags, ws, lenience=1.0, to
     ms = a.elapsed_time(b) / reps
     out = {"workload": "sample_b64", "rounds_per_s": 1000.0 / ms, "ms_per_round": ms,
            "mean_accepted": acc["variant"], "mean_accepted_plain": acc["plain"],
-           "gpu_launches_per_round": 2 + (1 if top_k else 0) + (2 if top_p < 1.0 else 0)}
+           "gpu_launches_per_round": (1 if not (top_k or top_p < 1.0) else
+                                      2 + (1 if top_k else 0) + (2 if top_p < 1.0 else 0))}
     if lenience != 1.0:
         out["lenience"] = lenience
     if top_p < 1.0:

@@ -349,6 +349,7 @@ cudaError_t launch_round(const SweepCtx& x, int dtype, char* ws, const SamplePla
   mark(0, stream);
   e = cudaMemsetAsync(ws + pl.off_abort, 0, pl.fused_zero_bytes(B, nck), stream);
   if (e != cudaSuccess) return e;
+  mark(1, stream);
   RoundArgs a;
   a.x = x;
   a.abort = reinterpret_cast<uint32_t*>(ws + pl.off_abort);
@@ -376,7 +377,7 @@ cudaError_t launch_round(const SweepCtx& x, int dtype, char* ws, const SamplePla
   e = (dtype == SV_F32) ? cudaLaunchKernelEx(&cfg, k_round<SV_F32>, a)
                         : cudaLaunchKernelEx(&cfg, k_round<SV_BF16>, a);
   if (e != cudaSuccess) return e;
-  mark(1, stream);
+  mark(2, stream);
   return cudaSuccess;
 }
 
