@@ -9,13 +9,15 @@
 //
 // On the GPU the race is run in ratio form: with E_v = -log2 u_v (an
 // exponential variate in log2 units), argmax log w_v + g_v = argmax w_v / E_v,
-// and the weights need only be known up to a factor common to the row.  Lanes
-// keep their two best entries, compared by cross products (no division); the
-// warp, then the merge, keep the best two of those.  When the two best keys lie
-// within 2^-10 of each other, they are re-decided in double precision from the
-// logits (the key's definition, log w + g), so that the winner differs from an
-// exact evaluation only where the exact keys themselves are within the
-// rounding of the row sums.
+// and the weights need only be known up to a factor common to the row.  Each
+// lane keeps its two largest keys w_v / E_v (a reciprocal and a product per
+// entry, the update by selects); the warp, then the merge, keep the best two of
+// those.  Most entries never reach the key: once a warp holds two candidates,
+// an entry whose Philox word shows an E_v too large for any weight of its run
+// to beat the second-best key is dropped by one integer compare.  When the two best keys lie within 2^-10 of each other,
+// they are re-decided in double precision from the logits (the key's
+// definition, log w + g), so that the winner differs from an exact evaluation
+// only where the exact keys themselves are within the rounding of the row sums.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -30,64 +32,11 @@
 
 namespace sv {
 
-// One entry of the race: weight w (>= 0), exponential variate E (> 0), index.
-struct RaceCand {
-  float w, E;
-  int idx;
-};
-struct RaceTop2 {
-  RaceCand a, b;  // best, second best
-};
-
-__device__ __forceinline__ RaceCand race_empty() { return RaceCand{0.0f, 1.0f, -1}; }
-__device__ __forceinline__ RaceTop2 race_top2_empty() { return RaceTop2{race_empty(), race_empty()}; }
-
-// w/E beats c (w_c/E_c): larger ratio, ties to the lower index (-1 loses).
-__device__ __forceinline__ bool race_beats(float w, float E, int i, const RaceCand& c) {
-  const float l = w * c.E, r = c.w * E;
-  return l > r || (l == r && (unsigned)i < (unsigned)c.idx);
-}
-
-__device__ __forceinline__ void race_insert(RaceTop2& t, float w, float E, int i) {
-  if (!(w > 0.0f)) return;
-  if (race_beats(w, E, i, t.b)) {
-    if (race_beats(w, E, i, t.a)) {
-      t.b = t.a;
-      t.a = RaceCand{w, E, i};
-    } else {
-      t.b = RaceCand{w, E, i};
-    }
-  }
-}
-
-__device__ __forceinline__ void race_insert(RaceTop2& t, const RaceCand& c) {
-  if (c.idx >= 0) race_insert(t, c.w, c.E, c.idx);
-}
-
-__device__ __forceinline__ RaceCand race_shfl(const RaceCand& c, int o) {
-  return RaceCand{__shfl_xor_sync(0xffffffffu, c.w, o), __shfl_xor_sync(0xffffffffu, c.E, o),
-                  __shfl_xor_sync(0xffffffffu, c.idx, o)};
-}
-
-// The best two of the warp's lanes (the same in every lane).
-__device__ __forceinline__ RaceTop2 race_warp(RaceTop2 t) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const RaceCand a = race_shfl(t.a, o), b = race_shfl(t.b, o);
-    race_insert(t, a);
-    race_insert(t, b);
-  }
-  return t;
-}
-
-// A finished candidate: its key w/E as a float and its index (-1: none).
+// A candidate: its key w/E as a float and its index (-1: none, key -inf).
 struct KeyIdx {
   float k;
   int i;
 };
-__device__ __forceinline__ KeyIdx race_key(const RaceCand& c) {
-  return (c.idx < 0) ? KeyIdx{-1.0f, -1} : KeyIdx{__fdiv_rn(c.w, c.E), c.idx};
-}
 __device__ __forceinline__ bool key_beats(const KeyIdx& a, const KeyIdx& b) {
   if (a.i < 0) return false;
   if (b.i < 0) return true;
@@ -96,6 +45,18 @@ __device__ __forceinline__ bool key_beats(const KeyIdx& a, const KeyIdx& b) {
 struct KeyTop2 {
   KeyIdx a, b;
 };
+__device__ __forceinline__ KeyTop2 key_top2_empty() {
+  return KeyTop2{KeyIdx{-kInf, -1}, KeyIdx{-kInf, -1}};
+}
+// An entry in its lane's increasing index order (strictly larger keys win, so
+// an equal key keeps the earlier, lower index): selects only.
+__device__ __forceinline__ void top2_push(KeyTop2& t, float k, int i) {
+  const bool g1 = k > t.a.k, g2 = k > t.b.k;
+  t.b.k = g1 ? t.a.k : (g2 ? k : t.b.k);
+  t.b.i = g1 ? t.a.i : (g2 ? i : t.b.i);
+  t.a.k = g1 ? k : t.a.k;
+  t.a.i = g1 ? i : t.a.i;
+}
 __device__ __forceinline__ void key_insert(KeyTop2& t, const KeyIdx& c) {
   if (key_beats(c, t.a)) {
     t.b = t.a;
@@ -122,7 +83,8 @@ __device__ __forceinline__ uint64_t key_word(const KeyIdx& c) {
   return ((uint64_t)(uint32_t)(c.i + 1) << 32) | (uint64_t)__float_as_uint(c.i < 0 ? -1.0f : c.k);
 }
 __device__ __forceinline__ KeyIdx key_unword(uint64_t w) {
-  return KeyIdx{__uint_as_float((uint32_t)w), (int)(uint32_t)(w >> 32) - 1};
+  const int i = (int)(uint32_t)(w >> 32) - 1;
+  return KeyIdx{i < 0 ? -kInf : __uint_as_float((uint32_t)w), i};
 }
 
 // The Gumbel noise -ln(-ln u) of entry v in double (the re-decision of a near tie).
@@ -163,104 +125,318 @@ __device__ __forceinline__ int race_pick(const KeyTop2& t, F key_f64) {
   return t.a.i;
 }
 
-// One run of eight consecutive entries v0..v0+7 of the race: weights of the
-// residual max(0, p_n - q_n) (RESID) and of p_n, up to the common factor
-// 2^-mct / St, and their exponential variates from the Philox blocks of the
-// run.  Entries past V carry -inf logits (weight 0); below a row's top-k
-// threshold the weight is 0 (TOPK).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The weight of one entry of the race up to the common factor 2^-mct / St:
+// p_n's, or the residual max(0, p_n - q_n) (RESID); 0 below a row's top-k
+// threshold (TOPK).
 template <bool RESID, bool TOPK>
-__device__ __forceinline__ void race_run8(const float (&zt)[8], const float (&zd)[8], int64_t v0,
-                                          const DrawState& st, float kd, uint32_t k0, uint32_t k1,
-                                          uint32_t c1, uint32_t c2, uint32_t c3, RaceTop2& tr,
-                                          RaceTop2& tp) {
-  uint32_t r[8];
+__device__ __forceinline__ float race_weight(float a, float d, const DrawState& st, float kd) {
+  if (TOPK && a < st.tt) a = -kInf;
+  float w = ex2(__fmaf_rn(a, st.c, -st.mct));
+  if (RESID) {
+    if (TOPK && d < st.td) d = -kInf;
+    const float ed = ex2(__fmaf_rn(d, st.c, kd));
+    w = (w > ed) ? __fsub_rn(w, ed) : 0.0f;
+  }
+  return w;
+}
+// Its key w / E from its Philox word; -inf for a weight of 0 (no candidate).
+__device__ __forceinline__ float race_key(float w, uint32_t r) {
+  return (w > 0.0f) ? w * rcp_approx(neglog2_u(r)) : -kInf;
+}
+
+// The largest logit of a run of eight (NaN ignored).
+template <int DT>
+__device__ __forceinline__ float run_max(const Raw8<DT>& x) {
+  if constexpr (DT == SV_F32)
+    return fmaxf(vmax<SV_F32>(x.v[0]), vmax<SV_F32>(x.v[1]));
+  else
+    return vmax<SV_BF16>(x.v[0]);
+}
+
+// Entry e (0..7, not known at compile time) of a run, by selects (no local
+// array).
+template <int DT>
+__device__ __forceinline__ float run_at(const Raw8<DT>& x, int e) {
+  if constexpr (DT == SV_F32) {
+    const uint4 q = (e & 4) ? x.v[1] : x.v[0];
+    const uint32_t lo = (e & 1) ? q.y : q.x, hi = (e & 1) ? q.w : q.z;
+    return __uint_as_float((e & 2) ? hi : lo);
+  } else {
+    const uint4 q = x.v[0];
+    const uint32_t lo = (e & 2) ? q.y : q.x, hi = (e & 2) ? q.w : q.z;
+    const uint32_t w = (e & 4) ? hi : lo;
+    return (e & 1) ? bf16hi(w) : bf16lo(w);
+  }
+}
+__device__ __forceinline__ uint32_t word_at(const uint32_t (&r)[8], int e) {
+  const uint32_t m0 = (e & 1) ? r[1] : r[0], m1 = (e & 1) ? r[3] : r[2];
+  const uint32_t m2 = (e & 1) ? r[5] : r[4], m3 = (e & 1) ? r[7] : r[6];
+  const uint32_t n0 = (e & 2) ? m1 : m0, n1 = (e & 2) ? m3 : m2;
+  return (e & 4) ? n1 : n0;
+}
+
+// The two Philox blocks of the run at v0 (a multiple of 8): word e is entry v0 + e's.
+__device__ __forceinline__ void run_words(int64_t v0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                          const PhiloxKeys& pk, uint32_t (&r)[8]) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const uint4 x = philox4x32_10(make_uint4((uint32_t)(v0 >> 2) + (uint32_t)h, c1, c2, c3), k0, k1);
+    const uint4 x = philox_rk(make_uint4((uint32_t)(v0 >> 2) + (uint32_t)h, c1, c2, c3), pk);
     r[4 * h] = x.x;
     r[4 * h + 1] = x.y;
     r[4 * h + 2] = x.z;
     r[4 * h + 3] = x.w;
   }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    float a = zt[e];
-    if (TOPK && a < st.tt) a = -kInf;
-    const float et = ex2(__fmaf_rn(a, st.c, -st.mct));
-    const float E = neglog2_u(r[e]);
-    const int v = (int)(v0 + e);
-    if (RESID) {
-      float d = zd[e];
-      if (TOPK && d < st.td) d = -kInf;
-      const float ed = ex2(__fmaf_rn(d, st.c, kd));
-      race_insert(tr, (et > ed) ? __fsub_rn(et, ed) : 0.0f, E, v);
-    }
-    race_insert(tp, et, E, v);
+}
+
+// The key of a run's largest-logit entry (the first of equal ones): a seed for
+// the pruning bound.  -inf when that entry has no weight.
+template <int DT, bool RESID, bool TOPK>
+__device__ __forceinline__ float run_seed_key(const Raw8<DT>& xt, const Raw8<DT>& xd, float zmax,
+                                              int64_t v0, const DrawState& st, float kd,
+                                              const PhiloxKeys& pk, uint32_t c1, uint32_t c2,
+                                              uint32_t c3) {
+  int es = 0;
+  for (int e = 7; e >= 0; --e)
+    if (run_at<DT>(xt, e) == zmax) es = e;
+  const int64_t v = v0 + es;
+  const uint4 x = philox_rk(make_uint4((uint32_t)(v >> 2), c1, c2, c3), pk);
+  const int l = (int)(v & 3);
+  const uint32_t r = (l == 0) ? x.x : (l == 1) ? x.y : (l == 2) ? x.z : x.w;
+  return race_key(race_weight<RESID, TOPK>(run_at<DT>(xt, es), RESID ? run_at<DT>(xd, es) : 0.0f,
+                                           st, kd),
+                  r);
+}
+
+// Pruning of a block of four entries (one Philox block): their weights are at
+// most Wb = 2^(max z c - mct) (the residual's lie below p_n's), so an entry's
+// key w_v / E_v stays below th whenever E_v > Wb / th; with u_v = (m_v + 1/2)
+// 2^-23 that holds when m_v < 2^(23 - Wb / th) (1 - 2^-10).  The slack of
+// 2^-10 covers the approximate ex2 / lg2 / reciprocal many times over, so a
+// pruned entry's computed key is below th as well.  tau = (1 + 2^-10) / th, or
+// 0 when th is no positive key.  Returns R: an entry whose Philox word is below
+// R is pruned (0: none).
+__device__ __forceinline__ float prune_tau(float th) {
+  return (th > 0.0f) ? (1.0f + 0x1p-10f) * rcp_approx(th) : 0.0f;
+}
+__device__ __forceinline__ uint32_t prune_word(float zmax, const DrawState& st, float tau) {
+  const float Wb = ex2(__fmaf_rn(zmax, st.c, -st.mct));
+  const float y = ex2(23.0f - Wb * tau) * (1.0f - 0x1p-10f);
+  if (!(tau > 0.0f) || !(y >= 1.0f)) return 0u;  // no bound yet; also NaN
+  return __float2uint_rz(fminf(y, 8388607.0f)) << 9;
+}
+
+// The largest logit of entries 4h..4h+3 of a run (NaN ignored).
+template <int DT>
+__device__ __forceinline__ float half_max(const Raw8<DT>& x, int h) {
+  if constexpr (DT == SV_F32) {
+    return vmax<SV_F32>(x.v[h]);
+  } else {
+    const uint32_t a = h ? x.v[0].z : x.v[0].x, b = h ? x.v[0].w : x.v[0].y;
+    uint32_t m;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+    return fmaxf(bf16lo(m), bf16hi(m));
   }
 }
 
+// A lower bound of the second-best key over a warp's candidates: the larger
+// of every lane's second key and the second largest first key.  At least two
+// distinct entries hold keys >= the bound, so an entry whose key lies below it
+// is in no final best two.  The same value in every lane; -inf while there is
+// no such pair.
+__device__ __forceinline__ float warp_second_bound(const KeyTop2& t) {
+  const float m1 = warp_max(t.a.k);
+  return warp_max(t.a.k == m1 ? t.b.k : t.a.k);
+}
+
+// Runs of eight per lane and round of loads (the same bytes for both types),
+// 16-byte vectors per run and row, and the shared memory a racing warp stages
+// its rounds in: two rounds of both rows.
+template <int DT>
+struct RaceStage {
+  static constexpr int kRuns = (DT == SV_F32) ? 2 : 4;
+  static constexpr int kVecs = (DT == SV_F32) ? 2 : 1;
+  static constexpr int kRound = kRuns * 2 * kVecs * 32;  // uint4 per round, both rows
+};
+constexpr size_t kRaceWarpSmem = 2 * 4 * 2 * 32 * sizeof(uint4);  // 8 KB, both types
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(smem)),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_group() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // The race over entries [lo, hi) of row n (and of draft row n for a residual):
-// lane l takes the runs of eight at lo + 8 (l + 32 i), kRunsInFlight of them
-// with their loads in flight together.  lo is a multiple of 8; `vec`: rows start
-// on 16-byte boundaries (16-byte loads).
-constexpr int kRaceRunsInFlight = 2;
+// lane l takes the runs of eight at lo + 8 (l + 32 i), kRuns of them per
+// round of loads.  Whole 16-byte runs go through the warp's shared memory `sb`
+// (kRaceWarpSmem bytes) by cp.async, the next round's copies in flight while
+// this round is raced; a run cut by the row's end (or any run of rows that do
+// not start on 16-byte boundaries, !vec) is loaded directly.  Each lane reads
+// back only its own copies.  lo is a multiple of 8.  `th` (the same in every
+// lane) is the warp's bound on the second-best key, carried from one range to
+// the next; while it is unset, the largest-logit entry of each lane's first
+// run is keyed first to set it.  `thw` (or null) is a bound shared by every
+// warp racing the same draw: each round reads it and raises it to th
+// afterwards (any warp's bound holds for the union of their candidates).
 template <int DT, bool RESID, bool TOPK>
 __device__ __forceinline__ void race_range(const char* rt, const char* rd, int64_t lo, int64_t hi,
                                            int64_t V, bool vec, const DrawState& st, float kd,
-                                           uint64_t seed, uint64_t round, int b, RaceTop2& tr,
-                                           RaceTop2& tp) {
+                                           uint64_t seed, uint64_t round, int b, KeyTop2& t,
+                                           float& th, uint32_t* thw, uint4* sb) {
+  using RS = RaceStage<DT>;
+  constexpr int kRuns = RS::kRuns, kVecs = RS::kVecs;
+  constexpr int kElem = (DT == SV_F32) ? 4 : 2;
   const int lane = threadIdx.x & 31;
-  const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  const PhiloxKeys pk = philox_keys(seed);
+  // th into the shared bound (no reply waited for; keys are positive, so their
+  // bits order as integers)
+  auto share = [&]() {
+    if (thw != nullptr && lane == 0 && th > 0.0f)
+      asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(thw), "r"(__float_as_uint(th))
+                   : "memory");
+  };
   const uint32_t c1 = (1u << 24) | (uint32_t)st.pos, c2 = (uint32_t)b, c3 = (uint32_t)round;
   const int nrun = (int)((hi - lo + 7) >> 3);
-  for (int r0 = 0; r0 < nrun; r0 += 32 * kRaceRunsInFlight) {
-    Raw8<DT> xt[kRaceRunsInFlight], xd[kRaceRunsInFlight];
+  // slot of (round buffer s, run u, row w, vector q) for this lane
+  auto slot = [&](int s, int u, int w, int q) {
+    return sb + s * RS::kRound + ((u * 2 + w) * kVecs + q) * 32 + lane;
+  };
+  auto whole = [&](int64_t v0) { return vec && v0 + 8 <= V; };
+  auto issue = [&](int r0, int s) {
 #pragma unroll
-    for (int u = 0; u < kRaceRunsInFlight; ++u) {
+    for (int u = 0; u < kRuns; ++u) {
       const int r = r0 + lane + 32 * u;
-      if (r < nrun) {
-        const int64_t v0 = lo + 8 * (int64_t)r;
+      const int64_t v0 = lo + 8 * (int64_t)r;
+      if (r < nrun && whole(v0)) {
+#pragma unroll
+        for (int q = 0; q < kVecs; ++q) {
+          cp_async16(slot(s, u, 0, q), rt + v0 * kElem + 16 * q);
+          if (RESID) cp_async16(slot(s, u, 1, q), rd + v0 * kElem + 16 * q);
+        }
+      }
+    }
+    cp_async_commit_group();
+  };
+  issue(0, 0);
+  for (int r0 = 0, s = 0; r0 < nrun; r0 += 32 * kRuns, s ^= 1) {
+    uint32_t g = 0u;
+    if (thw != nullptr && lane == 0)
+      asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(g) : "l"(thw) : "memory");
+    if (r0 + 32 * kRuns < nrun)
+      issue(r0 + 32 * kRuns, s ^ 1);  // the next round, into the other buffer
+    else
+      cp_async_commit_group();        // (an empty group: the count stays the same)
+    cp_async_wait_group<1>();         // this round's copies have landed
+    Raw8<DT> xt[kRuns], xd[kRuns];
+#pragma unroll
+    for (int u = 0; u < kRuns; ++u) {
+      const int r = r0 + lane + 32 * u;
+      const int64_t v0 = lo + 8 * (int64_t)r;
+      if (r >= nrun) continue;
+      if (whole(v0)) {
+#pragma unroll
+        for (int q = 0; q < kVecs; ++q) {
+          xt[u].v[q] = *slot(s, u, 0, q);
+          if (RESID) xd[u].v[q] = *slot(s, u, 1, q);
+        }
+      } else {
         xt[u] = load_raw8<DT>(rt, v0, V, vec, -kInf);
         if (RESID) xd[u] = load_raw8<DT>(rd, v0, V, vec, -kInf);
       }
     }
+    g = __shfl_sync(0xffffffffu, g, 0);
+    if (g != 0u) th = fmaxf(th, __uint_as_float(g));
+    if (!(th > 0.0f)) {  // the same in every lane: seeds from each lane's first run
+      const int r = r0 + lane;
+      float k = -kInf;
+      if (r < nrun)
+        k = run_seed_key<DT, RESID, TOPK>(xt[0], xd[0], run_max<DT>(xt[0]), lo + 8 * (int64_t)r, st,
+                                          kd, pk, c1, c2, c3);
+      // the second largest seed over the lanes (distinct entries)
+      const float m1 = warp_max(k);
+      const unsigned top = __ballot_sync(0xffffffffu, k == m1);
+      th = fmaxf(th, (__popc(top) > 1) ? m1 : warp_max(k == m1 ? -kInf : k));
+      share();
+    }
+    // the Philox words of all runs first (independent chains, interleaved),
+    // then the pruning of each block of four against one bound, then the rare
+    // entries left, in increasing order
+    uint32_t rw[kRuns][8];
 #pragma unroll
-    for (int u = 0; u < kRaceRunsInFlight; ++u) {
+    for (int u = 0; u < kRuns; ++u) run_words(lo + 8 * (int64_t)(r0 + lane + 32 * u), c1, c2, c3, pk, rw[u]);
+    const float tau = prune_tau(fmaxf(th, t.b.k));
+#pragma unroll
+    for (int u = 0; u < kRuns; ++u) {
       const int r = r0 + lane + 32 * u;
-      if (r < nrun) {
-        float zt[8], zd[8];
-        unpack8<DT>(xt[u], zt);
-        if (RESID) unpack8<DT>(xd[u], zd);
-        race_run8<RESID, TOPK>(zt, zd, lo + 8 * (int64_t)r, st, kd, k0, k1, c1, c2, c3, tr, tp);
+      uint32_t live = 0u;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t R = prune_word(half_max<DT>(xt[u], h), st, tau);
+#pragma unroll
+        for (int e = 4 * h; e < 4 * h + 4; ++e) live |= (rw[u][e] >= R ? 1u : 0u) << e;
+      }
+      if (r >= nrun) live = 0u;
+      const int64_t v0 = lo + 8 * (int64_t)r;
+      while (live != 0u) {
+        const int e = __ffs((int)live) - 1;
+        live &= live - 1u;
+        const float w = race_weight<RESID, TOPK>(run_at<DT>(xt[u], e),
+                                                 RESID ? run_at<DT>(xd[u], e) : 0.0f, st, kd);
+        top2_push(t, race_key(w, word_at(rw[u], e)), (int)(v0 + e));
       }
     }
+    th = fmaxf(th, warp_second_bound(t));
+    share();
+  }
+  cp_async_wait_group<0>();  // nothing of this range left in flight
+}
+
+// The race of a draw over [lo, hi) of its row in the mode the decision set
+// (residual, or p_n), into t.
+// thw: the bound shared by the warps racing this draw, or null; sb: the warp's
+// kRaceWarpSmem bytes of shared memory.
+template <int DT, bool TOPK>
+__device__ __forceinline__ void race_draw(const SweepCtx& x, int b, const DrawState& st, bool resid,
+                                          int64_t lo, int64_t hi, bool vec, KeyTop2& t,
+                                          float& th, uint32_t* thw, uint4* sb) {
+  const int gamma = x.gamma;
+  const int64_t V = x.V;
+  const char* rt = row_ptr<DT>(x.zt, x.zd, b, st.pos, gamma, V);
+  if (resid) {
+    const char* rd = row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + st.pos, gamma, V);
+    race_range<DT, true, TOPK>(rt, rd, lo, hi, V, vec, st, __fsub_rn(st.K, st.mct), x.seed,
+                               x.round, b, t, th, thw, sb);
+  } else {
+    race_range<DT, false, TOPK>(rt, rt, lo, hi, V, vec, st, 0.0f, x.seed, x.round, b, t, th, thw,
+                                sb);
   }
 }
 
-// The token from the best two of the residual race (R) and of p_n (P) over the
-// whole row: the residual's when it has a positive entry, else p_n's with the
-// fallback flag; re-decided in double near a tie; token 0 and ZERO_MASS when
-// there is none.  One warp; lane 0 writes the token and the flags.
+// The token from the best two keys T over the whole row of the race that drew
+// it (the residual's when use_resid, else p_n's), re-decided in double near a
+// tie; token 0 and ZERO_MASS when there is none.  fl: the flags so far.  One
+// warp; lane 0 writes the token and the flags.
 template <int DT>
-__device__ void race_emit(const SweepCtx& x, int b, const DrawState& st, const KeyTop2& R,
-                          const KeyTop2& P, bool lost) {
+__device__ __noinline__ void race_emit(const SweepCtx& x, int b, const DrawState& st,
+                                       const KeyTop2& T, bool use_resid, int fl) {
   const int lane = threadIdx.x & 31;
   const int gamma = x.gamma;
   const int64_t V = x.V;
-  const bool resid = st.mode == kDrawResidual;
-  int fl = st.flags;
-  bool use_resid = false;
-  KeyTop2 T = P;
-  if (resid) {
-    if (R.a.i >= 0) {
-      T = R;
-      use_resid = true;
-    } else {
-      fl |= SV_FLAG_RESIDUAL_FALLBACK;  // no positive residual entry: p_n, the same noise
-    }
-  }
   const char* rt = row_ptr<DT>(x.zt, x.zd, b, st.pos, gamma, V);
-  const char* rd = resid ? row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + st.pos, gamma, V) : rt;
+  const char* rd = use_resid ? row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + st.pos, gamma, V) : rt;
   DrawRowsF64 rr;
   rr.invT = (double)st.invT;
   rr.mt = (double)st.zmt * rr.invT;
@@ -276,7 +452,6 @@ __device__ void race_emit(const SweepCtx& x, int b, const DrawState& st, const K
     return draw_key_f64(rr, zt, zd, gumbel_f64(v, st.pos, b, x.seed, x.round, 1u));
   });
   if (lane == 0) {
-    if (lost) fl |= SV_FLAG_TIMEOUT | SV_FLAG_NONFINITE;
     if (tok < 0 || (int64_t)tok >= V) {
       tok = 0;
       fl |= SV_FLAG_ZERO_MASS;
@@ -284,6 +459,19 @@ __device__ void race_emit(const SweepCtx& x, int b, const DrawState& st, const K
     x.out_tokens[(int64_t)b * (gamma + 1) + st.pos] = tok;
     if (x.out_flags) x.out_flags[b] = (uint8_t)fl;
   }
+}
+
+// The empty-residual fallback: p_n raced over the whole row by one warp (rare:
+// max(0, p_n - q_n) has no positive entry in floating point), then emitted;
+// sb: the warp's kRaceWarpSmem bytes of shared memory.
+template <int DT, bool TOPK>
+__device__ __noinline__ void race_fallback_emit(const SweepCtx& x, int b, const DrawState& st,
+                                                bool vec, int fl, uint4* sb) {
+  KeyTop2 t = key_top2_empty();
+  float th = -kInf;
+  race_draw<DT, TOPK>(x, b, st, false, 0, x.V, vec, t, th, nullptr, sb);  // p_n: keys of its own
+  t = key_warp(t);
+  race_emit<DT>(x, b, st, t, false, fl | SV_FLAG_RESIDUAL_FALLBACK);
 }
 
 }  // namespace sv

@@ -16,13 +16,16 @@ constexpr int kThreads = 256;          // threads per CTA for the streaming kern
 constexpr int64_t kChunkSweep = 8192;  // logits per CTA in the softmax/argmax sweeps
 constexpr int64_t kChunkDraw = 8192;   // least vocabulary entries per CTA in the draw pass
 constexpr int kDrawCtasPerSm = 4;      // resident draw CTAs per SM (its launch bounds)
+constexpr int kRaceCtasPerSm = 2;      // resident race CTAs per SM (its launch bounds)
 constexpr size_t kAlign = 256;
 
 // Persistent vector sweep: warps per CTA, resident CTAs per SM (its launch bounds),
-// bytes per chunk.
+// bytes per chunk, chunks in flight per warp (each in a 4 KB shared-memory buffer).
 constexpr int kSweepWarps = 8;
 constexpr int kSweepCtasPerSm = 2;
 constexpr int kSweepChunkBytes = 4096;
+constexpr int kSweepBufs = 2;
+constexpr size_t kSweepSmemBytes = (size_t)kSweepWarps * kSweepBufs * kSweepChunkBytes;
 
 // The vector sweep cuts every row into chunks of 4 KB counted from the row's
 // start (the last one may be shorter) and loads 16-byte vectors, so every row
@@ -45,13 +48,13 @@ SV_HD inline int64_t vec_sweep_chunks(int dtype, int64_t V) {
 }
 SV_HD inline int64_t max_row_partials(int64_t V) { return ceil_div(V, (int64_t)1024); }
 
-// The fused round's draw: each batch row's token is raced in slices of
-// kRaceSlice vocabulary entries, one warp per slice.
+// The race's slices: kRaceSlice vocabulary entries.
 constexpr int kRaceSlice = 1024;
 SV_HD inline int64_t race_slices(int64_t V) { return ceil_div(V, (int64_t)kRaceSlice); }
 
+
 // Per-row softmax statistics after the chunk combine: max (scaled, log2 units),
-// row condition bits, and the sum of 2^(y - max) in double.
+// row condition bits, the sum of 2^(y - max) and the largest logit as given.
 struct RowStat {
   float mc;
   int bits;  // kRowNaN | kRowTimeout
@@ -88,20 +91,15 @@ struct SamplePlan {
   int R1 = 0;          // logit rows per batch row, 2*gamma+1
   int npmax = 0;       // partials per row the workspace holds (one per 1024 logits)
   int nsplit3 = 0;     // most CTAs per batch row in the inverse-transform draw
-  int nrace = 0;       // race slices per batch row (fused round)
-  // The fused round's words, zeroed before every call and laid out together:
-  // an abort word, the decision of each batch row [B][3], the race candidates
-  // [B][nrace][4], then the sweep's partials (one 8-byte word per chunk,
-  // [B][R1][chunks]).  The other paths use the partials as float2 pairs.
-  size_t off_abort = 0, off_dword = 0, off_cword = 0, off_part1 = 0;
+  int nrace = 0;       // race slices per batch row (the most race CTAs per batch row)
+  // the race's shared bound per batch row [B] (zeroed by the sweep), the race
+  // candidates [B][nrace][2] (two per race CTA), then the sweep's partials
+  // [B][R1][partials per row] as float2 pairs
+  size_t off_thw = 0, off_cword = 0, off_part1 = 0;
   // counters: [B] overlap CTAs (zeroed by the first draw CTA of each batch row),
   // then [B] draw CTAs that finished (zeroed by the sweep)
   size_t off_cnt = 0, cnt_bytes = 0, off_rowstat = 0, off_state = 0, off_segsum = 0,
          off_ctot = 0, off_alpha = 0, off_thr = 0, total = 0;
-  // bytes to zero before a fused round with `np` partials per row
-  size_t fused_zero_bytes(int B, int np) const {
-    return (off_part1 - off_abort) + (size_t)8 * B * R1 * np;
-  }
 };
 
 inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
@@ -112,9 +110,9 @@ inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
   p.nsplit3 = (int)ceil_div(V, kChunkDraw);
   p.nrace = (int)race_slices(V);
   size_t o = 0;
-  p.off_abort = o;    o += sizeof(uint64_t);
-  p.off_dword = o;    o += sizeof(uint64_t) * 3 * (size_t)B;
-  p.off_cword = o;    o += sizeof(uint64_t) * 4 * (size_t)B * p.nrace;
+  p.off_thw = o;      o += sizeof(uint32_t) * (size_t)B;
+  o = (o + 7) & ~(size_t)7;
+  p.off_cword = o;    o += sizeof(uint64_t) * 2 * (size_t)B * p.nrace;
   p.off_part1 = o;    o = align_up(o + 8 * (size_t)B * p.R1 * (size_t)p.npmax);
   p.cnt_bytes = 2 * sizeof(uint32_t) * (size_t)B;
   p.off_cnt = o;      o = align_up(o + p.cnt_bytes);

@@ -3,11 +3,7 @@
 // One round for B independent batch rows, after Algorithm 1 of "Fast Inference
 // from Transformers via Speculative Decoding" (section "The loop: draft, verify
 // in one pass, keep a prefix") and the course notes "Speculative Decoding"
-// ("The algorithm").  The plain round (and the lenient one) on rows that are a
-// multiple of 16 bytes long runs as one fused kernel (sv_round.cu).  The other
-// rounds -- top-k or top-p adjusted rows, rows of any length, the opt-in
-// inverse-transform sampler -- run as separate kernels chained by programmatic
-// dependent launch:
+// ("The algorithm"), as kernels chained by programmatic dependent launch:
 //
 //   sweep     online softmax statistics of every chunk of all 2*gamma+1 logit
 //             rows, counted from each row's start: the largest logit and the
@@ -16,11 +12,11 @@
 //             sv_units.cuh.  k_sweep (any shape): one CTA per 8192-logit split.
 //   top-k / top-p thresholds (k_topk_cand, k_topk, k_topp), then a thresholded
 //             sweep where needed.
-//   k_race    the default draw: one CTA per (batch row, slice); every CTA takes
+//   k_race    the default draw: one CTA per (batch row, slices); every CTA takes
 //             its batch row's decision from the partials (accept test, first
-//             rejection by a warp ballot), races its slice by Gumbel-max
+//             rejection by a warp ballot), races its slices by Gumbel-max
 //             (sv_gumbel.cuh), and the CTA of the batch row that finishes last
-//             merges the slices' best two and emits.
+//             merges the CTAs' best two and emits.
 //   k_draw    the opt-in inverse-transform draw (sv_draw.cuh), same structure.
 //   k_alpha   optional overlap sum_v min(p_i, q_i) ("The acceptance rate is the
 //             overlap of p and q").
@@ -83,6 +79,8 @@ __device__ __forceinline__ void for_each_in_chunk(const char* row, int64_t lo, i
 __device__ __forceinline__ void zero_draw_counters(const SweepCtx& x) {
   if (blockIdx.x == 0 && x.done)
     for (int i = threadIdx.x; i < x.B; i += blockDim.x) x.done[i] = 0u;
+  if (blockIdx.x == 0 && x.thw)
+    for (int i = threadIdx.x; i < x.B; i += blockDim.x) x.thw[i] = 0u;
 }
 
 template <int DT, bool TOPK>
@@ -155,16 +153,18 @@ __global__ void __launch_bounds__(kThreads, 4) k_sweep(SweepCtx x) {
 // --------------------------------------------------------------------------
 template <int DT, bool TOPK>
 __global__ void __launch_bounds__(kSweepWarps * 32, kSweepCtasPerSm) k_sweep_vec(SweepCtx x) {
+  extern __shared__ uint4 sweep_buf[];  // [kSweepWarps][kSweepBufs][256]
   pdl_launch_dependents();  // the next kernel may be scheduled now; it waits for us
   zero_draw_counters(x);
   const int64_t NU = (int64_t)x.B * (2 * x.gamma + 1) * x.np;
   const int64_t W = (int64_t)gridDim.x * kSweepWarps;
-  unit_loop<DT, TOPK>(
-      x, x.np, (NU - 1) / W,
-      [&](int64_t g, float2 p) {
+  unit_loop<DT, TOPK, kSweepBufs>(
+      x, x.np, (NU - 1) / W, sweep_buf + (threadIdx.x >> 5) * kSweepBufs * 256,
+      (int)(blockIdx.x * kSweepWarps + (threadIdx.x >> 5)), (int)W,
+      [&](int64_t g, float2 p, int) {
         if ((threadIdx.x & 31) == 0) x.part[g] = p;
       },
-      [](int64_t) {});
+      [](int64_t, int64_t) {});
 }
 
 // --------------------------------------------------------------------------
@@ -740,71 +740,64 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
 }
 
 // --------------------------------------------------------------------------
-// The target's own token by Gumbel-max after a separate sweep (the default
-// sampler on the rounds that do not run fused): one CTA per (batch row, spc race
-// slices of kRaceSlice entries).  Every CTA takes its batch row's decision,
-// each warp races slices w, w + 8, ... of the CTA's, the CTA keeps the best two
-// of the residual race and of p_n, and the CTA of the batch row that finishes
-// last (a per-batch-row counter the sweep zeroes) merges them and emits.
+// k_race: the target's own token by Gumbel-max (the default sampler) after a
+// separate sweep.  One CTA per (batch row, spc race slices of kRaceSlice
+// entries), one resident wave.  Every CTA takes its batch row's decision
+// (decide_in_cta); each warp races one eighth of the CTA's slices in one piece
+// (its rounds of loads staged in shared memory, the next round in flight while
+// one is raced), the CTA keeps the best two, and the CTA of the batch row that
+// finishes last (a per-batch-row counter the sweep zeroes) merges them and
+// emits.  The warps racing one draw share their bound on the second-best key
+// through a word per batch row (zeroed by the sweep).
 // --------------------------------------------------------------------------
 struct RaceArgs {
-  uint64_t* cword;      // [B][nsplit][4] best two of the residual race and of p_n per CTA
-  uint32_t* alpha_cnt;  // [B] counters of the optional overlap kernel, zeroed here
-  uint32_t* done;       // [B] CTAs of the batch row that finished (zeroed by the sweep)
-  int nsplit;           // CTAs per batch row
-  int spc;              // race slices per CTA
-  bool vec;             // 16-byte loads of 8 entries are aligned in every row
+  uint64_t* cword;        // [B][nsplit][2] the race's best two per CTA
+  uint32_t* alpha_cnt;    // [B] counters of the optional overlap kernel, zeroed here
+  uint32_t* done;         // [B] CTAs of the batch row that finished (zeroed by the sweep)
+  int nsplit;             // CTAs per batch row
+  int spc;                // race slices per CTA
+  bool vec;               // 16-byte loads of 8 entries are aligned in every row
 };
+constexpr size_t kRaceSmemBytes = (kThreads / 32) * kRaceWarpSmem;
 
 template <int DT, bool TOPK>
-__global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_race(SweepCtx x, RaceArgs a) {
+__global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) k_race(SweepCtx x, RaceArgs a) {
   const int b = (int)(blockIdx.x / (unsigned)a.nsplit);
   const int split = (int)(blockIdx.x - (unsigned)b * (unsigned)a.nsplit);
-  const int gamma = x.gamma;
   const int64_t V = x.V;
   constexpr int kWarps = kThreads / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  extern __shared__ uint4 race_smem[];  // [kWarps][kRaceWarpSmem / 16]
+  uint4* sb = race_smem + warp * (kRaceWarpSmem / sizeof(uint4));
   __shared__ RowStat srs[65];
   __shared__ DraftAt sda[32];
   __shared__ DrawState s_st;
-  __shared__ RaceTop2 s_r[kWarps], s_p[kWarps];
+  __shared__ KeyTop2 s_t[kWarps];
   __shared__ int s_last;
   decide_in_cta<DT, TOPK>(x, b, split == 0, a.alpha_cnt, srs, sda, &s_st);
   const DrawState st = s_st;
   if (st.mode == kDrawDone) return;  // the same in every CTA of the batch row
   const bool resid = st.mode == kDrawResidual;
-  const char* rt = row_ptr<DT>(x.zt, x.zd, b, st.pos, gamma, V);
-  const char* rd = resid ? row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + st.pos, gamma, V) : rt;
-  const float kd = resid ? __fsub_rn(st.K, st.mct) : 0.0f;
-  const int S = (int)race_slices(V);
-  const int s1 = min(S, (split + 1) * a.spc);
-  RaceTop2 tr = race_top2_empty(), tp = race_top2_empty();
-  for (int sl = split * a.spc + warp; sl < s1; sl += kWarps) {
-    const int64_t lo = (int64_t)sl * kRaceSlice;
-    const int64_t hi = (lo + kRaceSlice < V) ? lo + kRaceSlice : V;
-    if (resid)
-      race_range<DT, true, TOPK>(rt, rd, lo, hi, V, a.vec, st, kd, x.seed, x.round, b, tr, tp);
-    else
-      race_range<DT, false, TOPK>(rt, rd, lo, hi, V, a.vec, st, kd, x.seed, x.round, b, tr, tp);
-  }
-  tr = race_warp(tr);
-  tp = race_warp(tp);
-  if (lane == 0) {
-    s_r[warp] = tr;
-    s_p[warp] = tp;
-  }
+  // the CTA's slices [clo, chi) in one piece per warp (a multiple of 8 entries
+  // each), so that a warp's rounds of loads follow one another
+  const int64_t clo = (int64_t)split * a.spc * kRaceSlice;
+  const int64_t chi = min(V, clo + (int64_t)a.spc * kRaceSlice);
+  const int64_t wlen = ceil_div(ceil_div(chi - clo, (int64_t)kWarps), (int64_t)8) * 8;
+  const int64_t wlo = clo + warp * wlen;
+  const int64_t whi = min(chi, wlo + wlen);
+  KeyTop2 t = key_top2_empty();
+  float th = -kInf;
+  if (wlo < whi) race_draw<DT, TOPK>(x, b, st, resid, wlo, whi, a.vec, t, th, x.thw + b, sb);
+  t = key_warp(t);
+  if (lane == 0) s_t[warp] = t;
   __syncthreads();
   if (warp == 0) {
-    RaceTop2 r = (lane < kWarps) ? s_r[lane] : race_top2_empty();
-    RaceTop2 p = (lane < kWarps) ? s_p[lane] : race_top2_empty();
-    r = race_warp(r);
-    p = race_warp(p);
+    KeyTop2 r = (lane < kWarps) ? s_t[lane] : key_top2_empty();
+    r = key_warp(r);
     if (lane == 0) {
-      uint64_t* o = a.cword + ((int64_t)b * a.nsplit + split) * 4;
-      o[0] = key_word(race_key(r.a));
-      o[1] = key_word(race_key(r.b));
-      o[2] = key_word(race_key(p.a));
-      o[3] = key_word(race_key(p.b));
+      uint64_t* o = a.cword + ((int64_t)b * a.nsplit + split) * 2;
+      o[0] = key_word(r.a);
+      o[1] = key_word(r.b);
       __threadfence();  // this CTA's candidates before its arrival
       s_last = (atomicAdd(a.done + b, 1u) == (unsigned)(a.nsplit - 1)) ? 1 : 0;
     }
@@ -812,17 +805,15 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_race(SweepCtx x, R
   __syncthreads();
   if (!s_last || warp != 0) return;
   __threadfence();  // every other CTA's candidates are visible from here
-  KeyTop2 R{KeyIdx{-1.0f, -1}, KeyIdx{-1.0f, -1}}, P = R;
-  const uint64_t* cw = a.cword + (int64_t)b * a.nsplit * 4;
-  for (int j = lane; j < a.nsplit; j += 32) {
-    key_insert(R, key_unword(__ldcg(reinterpret_cast<const unsigned long long*>(cw) + 4 * j + 0)));
-    key_insert(R, key_unword(__ldcg(reinterpret_cast<const unsigned long long*>(cw) + 4 * j + 1)));
-    key_insert(P, key_unword(__ldcg(reinterpret_cast<const unsigned long long*>(cw) + 4 * j + 2)));
-    key_insert(P, key_unword(__ldcg(reinterpret_cast<const unsigned long long*>(cw) + 4 * j + 3)));
-  }
-  R = key_warp(R);
-  P = key_warp(P);
-  race_emit<DT>(x, b, st, R, P, false);
+  KeyTop2 T = key_top2_empty();
+  const unsigned long long* cw =
+      reinterpret_cast<const unsigned long long*>(a.cword) + (int64_t)b * a.nsplit * 2;
+  for (int j = lane; j < 2 * a.nsplit; j += 32) key_insert(T, key_unword(__ldcg(cw + j)));
+  T = key_warp(T);
+  if (resid && T.a.i < 0)
+    race_fallback_emit<DT, TOPK>(x, b, st, a.vec, st.flags, sb);
+  else
+    race_emit<DT>(x, b, st, T, resid, st.flags);
 }
 
 // --------------------------------------------------------------------------
@@ -888,6 +879,7 @@ k_alpha(const void* __restrict__ zt, const void* __restrict__ zd, int gamma, int
 struct DeviceInfo {
   int sms = 0;
   int sweep_ctas_per_sm[2][2] = {{0, 0}, {0, 0}};  // by dtype, then top-k variant
+  int race_ctas_per_sm[2][2] = {{0, 0}, {0, 0}};   // the same for k_race
   bool ready = false;
 };
 
@@ -900,9 +892,19 @@ static size_t topp_smem_bytes() {
 
 template <int DT, bool TOPK>
 static cudaError_t sweep_setup(DeviceInfo& d) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sweep_ctas_per_sm[DT][TOPK ? 1 : 0],
-                                                       k_sweep_vec<DT, TOPK>, kSweepWarps * 32,
-                                                       0);
+  cudaError_t e = cudaFuncSetAttribute(k_sweep_vec<DT, TOPK>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSweepSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sweep_ctas_per_sm[DT][TOPK ? 1 : 0],
+                                                    k_sweep_vec<DT, TOPK>, kSweepWarps * 32,
+                                                    kSweepSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_race<DT, TOPK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kRaceSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.race_ctas_per_sm[DT][TOPK ? 1 : 0],
+                                                       k_race<DT, TOPK>, kThreads, kRaceSmemBytes);
 }
 static std::mutex g_dev_mu;
 static DeviceInfo g_dev[64];
@@ -939,9 +941,6 @@ static cudaError_t device_info(DeviceInfo** out) {
   *out = &d;
   return cudaSuccess;
 }
-
-cudaError_t launch_round(const SweepCtx& x, int dtype, char* ws, const SamplePlan& pl,
-                         cudaStream_t stream);
 
 template <int DT>
 static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t* xt, int B,
@@ -998,6 +997,7 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
   sx.inv_lenience = 1.0f / lenience;
   sx.thr = masked ? thr : nullptr;
   sx.done = done;
+  sx.thw = reinterpret_cast<uint32_t*>(ws + pl.off_thw);
   const auto alpha = [&]() -> cudaError_t {
     if (!out_alpha) return cudaSuccess;
     const int ns = (int)ceil_div(V, kChunkSweep);
@@ -1005,17 +1005,6 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
         zt, zd, gamma, V, temperature, row_T, ns, rowstat, sx.thr, apart, alpha_cnt, out_alpha);
     return cudaGetLastError();
   };
-  if (!masked && vec_sweep && sampler == SV_SAMPLER_GUMBEL) {
-    // the plain (or lenient) round: one fused kernel
-    cudaError_t e = launch_round(sx, DT, ws, pl, stream);
-    if (e != cudaSuccess) return e;
-    if (out_alpha) {
-      // the overlap's counters start at zero (the fused round does not touch them)
-      e = cudaMemsetAsync(alpha_cnt, 0, sizeof(uint32_t) * (size_t)B, stream);
-      if (e != cudaSuccess) return e;
-    }
-    return alpha();
-  }
   auto sweep = [&](bool with_thr, const SweepCtx& ctx) {
     if (vec_sweep) {
       // one resident wave of warps, chunks dealt round-robin
@@ -1025,9 +1014,9 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
       const int64_t g = full < need ? full : need;
       const dim3 grid((unsigned)(g < 1 ? 1 : g));
       if (with_thr)
-        k_sweep_vec<DT, true><<<grid, kSweepWarps * 32, 0, stream>>>(ctx);
+        k_sweep_vec<DT, true><<<grid, kSweepWarps * 32, kSweepSmemBytes, stream>>>(ctx);
       else
-        k_sweep_vec<DT, false><<<grid, kSweepWarps * 32, 0, stream>>>(ctx);
+        k_sweep_vec<DT, false><<<grid, kSweepWarps * 32, kSweepSmemBytes, stream>>>(ctx);
     } else {
       const dim3 grid((unsigned)((int64_t)nch * B * R1));
       if (with_thr)
@@ -1081,19 +1070,21 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
                : launch_pdl(k_draw<DT, false>, dim3((unsigned)(nsplit * B)), dim3(kThreads), 0,
                             stream, sx, da);
   } else {
-    // Gumbel-max: one resident wave of race CTAs when the batch allows, at least
-    // two slices per CTA
+    // Gumbel-max: one resident wave of race CTAs (every CTA takes its batch
+    // row's decision, so a second wave would pay that latency again), at least
+    // two slices per warp of a CTA
     const int64_t S = race_slices(V);
-    int64_t nsplit = (S + 1) / 2;
-    if ((int64_t)B * nsplit > slots) nsplit = (slots / B > 1) ? slots / B : 1;
+    const int64_t rslots = (int64_t)di->sms * max(1, di->race_ctas_per_sm[DT][masked ? 1 : 0]);
+    int64_t nsplit = ceil_div(S, (int64_t)(2 * kThreads / 32));
+    if ((int64_t)B * nsplit > rslots) nsplit = (rslots / B > 1) ? rslots / B : 1;
     const int64_t spc = ceil_div(S, nsplit);
     nsplit = ceil_div(S, spc);  // no CTA without slices
     RaceArgs ra{reinterpret_cast<uint64_t*>(ws + pl.off_cword), alpha_cnt, done, (int)nsplit,
                 (int)spc, vec};
-    e = masked ? launch_pdl(k_race<DT, true>, dim3((unsigned)(nsplit * B)), dim3(kThreads), 0,
-                            stream, sx, ra)
-               : launch_pdl(k_race<DT, false>, dim3((unsigned)(nsplit * B)), dim3(kThreads), 0,
-                            stream, sx, ra);
+    e = masked ? launch_pdl(k_race<DT, true>, dim3((unsigned)(nsplit * B)), dim3(kThreads),
+                            kRaceSmemBytes, stream, sx, ra)
+               : launch_pdl(k_race<DT, false>, dim3((unsigned)(nsplit * B)), dim3(kThreads),
+                            kRaceSmemBytes, stream, sx, ra);
   }
   if (e != cudaSuccess) return e;
   mark(2, stream);

@@ -4,13 +4,15 @@
 // into nck chunks of 4 KB counted from the row's start; the last chunk of a
 // row may be shorter.  Chunks are numbered in batch-row order, g = (b R1 + k)
 // nck + j, and warp w of W takes g = w, w + W, w + 2W, ...: the whole GPU walks
-// the batch rows in order, so each batch row's chunks are complete at a known
-// point of the loop.  A warp holds two chunks in registers, reducing one while
-// the other's 16-byte loads are in flight, and the address of the chunk after
-// next is formed while the current one is reduced.  Each chunk leaves one
-// partial: its largest logit as given and the sum of 2^(y - max y) (y = z T^-1
-// log2 e), every lane holding vectors lane + 32u of the chunk.  The partials
-// depend only on the values and the shapes, not on where the arrays sit.
+// the batch rows in order, so each batch row's chunks complete one after
+// another.  A warp keeps NBUF chunks in flight in its own shared-memory
+// buffers (cp.async, 16 bytes per lane and vector, no registers held while the
+// copies are in flight); lane l copies and later reads vectors l + 32u of a
+// chunk.  The address of each chunk comes from a cursor stepped by fixed
+// increments (no division in the loop).  Each chunk leaves one partial: its
+// largest logit as given and the sum of 2^(y - max y) (y = z T^-1 log2 e).  The
+// partials depend only on the values and the shapes, not on where the arrays
+// sit in memory.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -25,31 +27,13 @@
 
 namespace sv {
 
-// A partial as one 64-bit word that is never zero (a zeroed slot reads as "not
-// written yet"): the largest logit's bits low, the sum's bits with the sign bit
-// flipped high (a sum is never -0).
-__device__ __forceinline__ uint64_t part_word(float2 p) {
-  return ((uint64_t)(__float_as_uint(p.y) ^ 0x80000000u) << 32) | (uint64_t)__float_as_uint(p.x);
-}
-__device__ __forceinline__ float2 part_unword(uint64_t w) {
-  return make_float2(__uint_as_float((uint32_t)w), __uint_as_float((uint32_t)(w >> 32) ^ 0x80000000u));
-}
-
-__device__ __forceinline__ uint64_t ld_relaxed64(const uint64_t* p) {
-  uint64_t v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_relaxed64(uint64_t* p, uint64_t v) {
-  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
 // Where a chunk is and how it is reduced.
 struct UnitInfo {
   const uint4* p;
   int nv;     // 16-byte vectors in the chunk (256 for a full one)
   float c;    // the batch row's scale fl32(1/T) log2 e
   float tau;  // top-k threshold of the row (-inf: none)
+  int row;    // its logit row, b R1 + k
 };
 
 template <int DT, bool TOPK>
@@ -62,19 +46,27 @@ __device__ __forceinline__ UnitInfo unit_info(const SweepCtx& x, const UnitCurso
   r.p = reinterpret_cast<const uint4*>(row_ptr<DT>(x.zt, x.zd, u.b, u.k, x.gamma, x.V) + off);
   r.c = x.row_T ? log2_scale(inv_temperature(__ldg(x.row_T + u.b))) : c_all;
   r.tau = TOPK ? __ldg(x.thr + (int64_t)u.b * (2 * x.gamma + 1) + u.k) : -kInf;
+  r.row = u.b * (2 * x.gamma + 1) + u.k;
   return r;
 }
 
-__device__ __forceinline__ void unit_load(uint4 (&v)[8], const UnitInfo& u) {
+// One chunk into a warp's shared-memory buffer [8][32] of 16-byte vectors: lane
+// l copies vectors l + 32u (past the chunk's end: zero fill, nothing read).
+__device__ __forceinline__ void unit_copy(uint4* buf, const UnitInfo& u) {
   const int lane = threadIdx.x & 31;
-  if (u.nv == 256) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = ld_stream16(u.p + lane + 32 * q);
-  } else {
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      v[q] = (lane + 32 * q < u.nv) ? ld_stream16(u.p + lane + 32 * q) : make_uint4(0u, 0u, 0u, 0u);
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(buf + 32 * q + lane);
+    const bool in = lane + 32 * q < u.nv;  // past the end: the chunk's start, 0 bytes read
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+                 "l"(in ? u.p + lane + 32 * q : u.p), "r"(in ? 16 : 0)
+                 : "memory");
   }
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 template <int DT, bool TOPK>
@@ -87,16 +79,15 @@ __device__ __forceinline__ float2 unit_reduce(const uint4 (&v)[8], const UnitInf
   return warp_chunk_partial(zmax, mc, sacc, u.c);
 }
 
-// The loop of one warp over its chunks, and over the iterations after them up
-// to `it_end`.  After the chunk of iteration `it` (if any) is reduced, its
-// partial goes to `emit(g, partial)` and `tasks(it)` runs (the other chunk's
-// loads still in flight).
-template <int DT, bool TOPK, class Emit, class Tasks>
-__device__ __forceinline__ void unit_loop(const SweepCtx& x, int nck, int64_t it_end, Emit&& emit,
-                                          Tasks&& tasks) {
-  const int warp = threadIdx.x >> 5;
-  const int W = (int)gridDim.x * (int)(blockDim.x >> 5);
-  const int w = (int)blockIdx.x * (int)(blockDim.x >> 5) + warp;
+// The loop of sweep warp w of W over its chunks, and over the iterations after
+// them up to `it_end`.  `wbuf` is the warp's NBUF x 4 KB of shared memory.  At
+// iteration `it` the copies of chunk it + NBUF - 1 are issued, chunk it is
+// reduced (its partial goes to `emit(g, partial, logit row)`, and `tasks(it,
+// g)` runs with g its chunk or -1 when the warp has none left).
+template <int DT, bool TOPK, int NBUF, class Emit, class Tasks>
+__device__ __forceinline__ void unit_loop(const SweepCtx& x, int nck, int64_t it_end, uint4* wbuf,
+                                          int w, int W, Emit&& emit, Tasks&& tasks) {
+  const int lane = threadIdx.x & 31;
   const int R1 = 2 * x.gamma + 1;
   const int64_t NU = (int64_t)x.B * R1 * nck;
   const int64_t RB = x.V * ((DT == SV_F32) ? 4 : 2);
@@ -104,33 +95,42 @@ __device__ __forceinline__ void unit_loop(const SweepCtx& x, int nck, int64_t it
   UnitWalk walk;
   walk.init(R1, nck, W);
   UnitCursor cn = walk.at(w);
-  uint4 va[8], vb[8];
-  UnitInfo ia{}, inx{};
-  if (w < NU) {
-    ia = unit_info<DT, TOPK>(x, cn, RB, c_all);
-    unit_load(va, ia);
-  }
-  walk.step(cn);  // unit w + W
-  if (w + W < NU) inx = unit_info<DT, TOPK>(x, cn, RB, c_all);
-  walk.step(cn);  // unit w + 2W
-  // one iteration: the chunk in `cur` (described by ia), the next one's loads into `nxt`
-  auto iteration = [&](int64_t it, uint4 (&cur)[8], uint4 (&nxt)[8]) {
-    const int64_t g = w + it * W;
-    if (g < NU) {
-      if (g + W < NU) unit_load(nxt, inx);
-      UnitInfo after{};
-      if (g + 2 * (int64_t)W < NU) after = unit_info<DT, TOPK>(x, cn, RB, c_all);
-      walk.step(cn);
-      emit(g, unit_reduce<DT, TOPK>(cur, ia));
-      ia = inx;
-      inx = after;
+  UnitInfo info[NBUF];
+#pragma unroll
+  for (int i = 0; i < NBUF - 1; ++i) {
+    if (w + (int64_t)i * W < NU) {
+      info[i] = unit_info<DT, TOPK>(x, cn, RB, c_all);
+      unit_copy(wbuf + 256 * i, info[i]);
     }
-    tasks(it);
-  };
-  for (int64_t it = 0; it <= it_end; it += 2) {
-    iteration(it, va, vb);
-    if (it + 1 > it_end) break;
-    iteration(it + 1, vb, va);
+    cp_async_commit();
+    walk.step(cn);
+  }
+  for (int64_t it0 = 0; it0 <= it_end; it0 += NBUF) {
+#pragma unroll
+    for (int i = 0; i < NBUF; ++i) {
+      const int64_t it = it0 + i;
+      if (it > it_end) break;
+      const int64_t g = w + it * W;
+      // the chunk NBUF - 1 iterations ahead goes into the slot freed last iteration
+      constexpr int kAhead = NBUF - 1;
+      const int sl = (i + kAhead) % NBUF;
+      if (g + (int64_t)kAhead * W < NU) {
+        info[sl] = unit_info<DT, TOPK>(x, cn, RB, c_all);
+        unit_copy(wbuf + 256 * sl, info[sl]);
+      }
+      cp_async_commit();
+      walk.step(cn);
+      if (g < NU) {
+        cp_async_wait<NBUF - 1>();  // this chunk's copies (this lane's) have landed
+        uint4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = wbuf[256 * i + 32 * q + lane];
+        emit(g, unit_reduce<DT, TOPK>(v, info[i]), info[i].row);
+        tasks(it, g);
+      } else {
+        tasks(it, (int64_t)-1);
+      }
+    }
   }
 }
 
