@@ -3,10 +3,14 @@
 
 One step = one call of spec_verify on one round of the sample_b64 workload:
 B=64, gamma=4, V=128256, bf16 logits, T=0.8, draft noise sigma=1 (Zipf(1.1)
-target bias).  The call is one fused kernel (softmax sweep over all 2*gamma+1
-logit rows, accept test, Gumbel-max residual/bonus draw) after a small memset of
-its hand-over words.  Metric: verify rounds per second (whole job, all GPUs);
-the line also carries verified positions/s (B*gamma per round).
+target bias).  The call is two kernels: k_sweep_vec (online-softmax statistics
+of all 2*gamma+1 logit rows, 4 KB chunks) and k_race (per CTA the batch row's
+accept test, then the Gumbel-max residual/bonus draw over slices of the draw
+row, merged by the last CTA of the batch row).  Metric: verify rounds per
+second (whole job, all GPUs); the line also carries verified positions/s
+(B*gamma per round).  The roofline object is the verify sweep's (HBM-bound);
+the race, which takes a comparable time, is issue-bound and is reported beside
+it (race_ms, its share of the step).
 
 Timing: W untimed warm-up steps, then K steps between a barrier +
 cuda.synchronize() on both sides, CUDA events on the launching stream, max over
@@ -82,9 +86,9 @@ def tensor_peaks():
         return 1900.0, 1700.0, "fallback"
 
 
-# DRAM bytes per launch of the dominant kernel from an ncu capture of the same
+# DRAM bytes per launch of the verify sweep from an ncu capture of the same
 # workload (profiles/ holds the summary); None when the kernel changed since.
-ROUND_TRAFFIC_BYTES = None
+SWEEP_TRAFFIC_BYTES = None
 LMHEAD_PASS1_TRAFFIC_BYTES = 1580866592  # 1577.972 MB read + 2.895 MB written, profiles/k_lm_lmhead.md
 
 
@@ -284,8 +288,8 @@ def _rotation(make, per_bytes, dev):
 
 def measure_sampling(L, dev, stream, name, sets, B, gamma, V, dt, reps, extra_keys=None):
     """Back-to-back rounds/s of spec_verify on rotating input sets, the per-kernel
-    times from the library's events (the fused round: its memset and k_round),
-    and the HBM roofline of the round's kernel on the logit bytes."""
+    times from the library's events (the sweep, then the race), and the HBM
+    roofline of the sweep on the logit bytes."""
     import torch
     import speculative_decoding_verification_21_gb300 as sv
     tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
@@ -297,7 +301,7 @@ def measure_sampling(L, dev, stream, name, sets, B, gamma, V, dt, reps, extra_ke
     hbm, kind = peaks()
     esz = 4 if dt == 0 else 2
     nbytes = B * (2 * gamma + 1) * V * esz
-    gbs = nbytes / (kms[1] / 1000.0) / 1e9
+    gbs = nbytes / (kms[0] / 1000.0) / 1e9
     acc = 0
     for i in range(len(sets)):
         call(i)
@@ -305,14 +309,14 @@ def measure_sampling(L, dev, stream, name, sets, B, gamma, V, dt, reps, extra_ke
     out = {"workload": name, "B": B, "gamma": gamma, "V": V,
            "dtype": "f32" if dt == 0 else "bf16",
            "rounds_per_s": 1000.0 / ms, "positions_per_s": 1000.0 / ms * B * gamma,
-           "ms_per_round": ms, "kernel_ms": {"memset": kms[0], "k_round": kms[1]},
+           "ms_per_round": ms, "kernel_ms": {"sweep": kms[0], "k_race": kms[1]},
            "mean_accepted": acc / (len(sets) * B),
-           "roofline": {"bound": "hbm", "kernel": "k_round", "achieved": gbs, "peak": hbm,
+           "roofline": {"bound": "hbm", "kernel": "sweep", "achieved": gbs, "peak": hbm,
                         "peak_kind": kind, "unit": "GB/s", "frac": gbs / hbm,
                         "frac_of_8TBs": gbs / 8000.0, "algorithmic_bytes": nbytes,
                         "step_frac": nbytes / (ms / 1000.0) / 1e9 / hbm},
            "l2_policy": f"inputs rotate over {len(sets)} sets",
-           "gpu_launches_per_round": 1}
+           "gpu_launches_per_round": 2}
     if extra_keys:
         out.update(extra_keys)
     return out
@@ -364,10 +368,10 @@ def run_ours(args):
     reps = max(200, args.kernel_reps)
     with ClockSampler(local) as kclk:
         kms, call_ms = _kernel_times(L, stream, step, 2, reps)
-    kavg = {"memset": kms[0], "k_round": kms[1], "call": call_ms}
+    kavg = {"k_sweep_vec": kms[0], "k_race": kms[1], "call": call_ms}
     hbm, peak_kind = peaks()
     sweep_bytes = B * (2 * gamma + 1) * V * 2
-    round_gbs = sweep_bytes / (kms[1] / 1000.0) / 1e9
+    sweep_gbs = sweep_bytes / (kms[0] / 1000.0) / 1e9
 
     # end-to-end through the C ABI with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -451,13 +455,16 @@ def run_ours(args):
             "parallelism": f"replicas x{world}",
             "positions_per_s": rounds_per_s * B * gamma,
             "step_effective_gbs": sweep_bytes * args.steps / (ms / world / 1000.0) / 1e9 / world,
-            "roofline": {"bound": "hbm", "kernel": "k_round", "achieved": round_gbs,
+            "roofline": {"bound": "hbm", "kernel": "k_sweep_vec", "achieved": sweep_gbs,
                          "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": round_gbs / hbm, "frac_of_8TBs": round_gbs / 8000.0,
-                         "traffic": ROUND_TRAFFIC_BYTES, "algorithmic_bytes": sweep_bytes,
-                         "timing": f"CUDA events around k_round, {reps} calls"},
+                         "frac": sweep_gbs / hbm, "frac_of_8TBs": sweep_gbs / 8000.0,
+                         "traffic": SWEEP_TRAFFIC_BYTES, "algorithmic_bytes": sweep_bytes,
+                         "timing": f"CUDA events around k_sweep_vec, {reps} calls",
+                         "step_share": kms[0] / (kms[0] + kms[1])},
+            "race": {"kernel": "k_race", "ms": kms[1], "step_share": kms[1] / (kms[0] + kms[1]),
+                     "bound": "issue (Philox4x32-10 per entry; see profiles/k_race_sample_b64.md)"},
             "kernel_ms": kavg,
-            "gpu_launches": args.steps,  # k_round (plus a memset of its hand-over words)
+            "gpu_launches": 2 * args.steps,  # k_sweep_vec and k_race per step
             "clocks": clk.summary(),
             "clocks_kernel_loop": kclk.summary(),
             "e2e": e2e,
@@ -504,7 +511,7 @@ def measure_configs(L, dev, stream, rank, reps):
 def measure_options(L, stream, sets, tokens, counts, flags, ws, lenience=1.0, top_k=0,
                     top_p=1.0, reps=400):
     """spec_verify_opts on the same rotating sample_b64 sets.  Lenience l: the
-    comparison u <= p/(l q) runs in the same fused round and accepts more.
+    comparison u <= p/(l q) runs in the same two kernels and accepts more.
     top_k: a sweep, the threshold from the candidates at or above the k-th
     largest chunk maximum, and the race on the adjusted rows.  top_p: a sweep for
     the row maxima, the nucleus cut, the thresholded sweep and the race."""
@@ -544,7 +551,7 @@ def measure_options(L, stream, sets, tokens, counts, flags, ws, lenience=1.0, to
     ms = a.elapsed_time(b) / reps
     out = {"workload": "sample_b64", "rounds_per_s": 1000.0 / ms, "ms_per_round": ms,
            "mean_accepted": acc["variant"], "mean_accepted_plain": acc["plain"],
-           "gpu_launches_per_round": (1 if not (top_k or top_p < 1.0) else
+           "gpu_launches_per_round": (2 if not (top_k or top_p < 1.0) else
                                       2 + (1 if top_k else 0) + (2 if top_p < 1.0 else 0))}
     if lenience != 1.0:
         out["lenience"] = lenience

@@ -21,20 +21,25 @@
  * Randomness (no state): Philox4x32-10 (Salmon et al., SC'11), key = (lo32(seed),
  * hi32(seed)), counter = (c0, (tag<<24)|position, b, lo32(round)).  Tag 0 is the
  * acceptance uniform (c0 = 0, lane 0; u = (2*(x>>9)+1)*2^-24 in (0,1)).  Tag 1 at
- * the draw position n (c0 = 0) gives the uniform of the target's own token,
- * U = k 2^-53 in [0,1) with k = (x0>>11)*2^32 + x1, and the token is drawn by the
- * inverse transform: the smallest v, in vocabulary order, whose cumulative weight
- * exceeds U times the total weight (weights max(0, p_n - q_n), or p_n, formed
- * and summed in fp32 and fp64 on the GPU: the interval ends are exact up to
- * about 1e-6 of the total).  Same inputs at the same addresses and (seed, round)
- * give the same outputs on any stream, launch shape or GPU (the row sums are
- * split along 4 KB blocks of memory, so a copy at another address may round
- * their last bits differently).
+ * the draw position n draws the target's own token by Gumbel-max: entry v gets
+ * u_v from counter (v>>2, (1<<24)|n, b, lo32(round)), lane v&3 (same mapping to
+ * (0,1)), g_v = -ln(-ln u_v), and the token is the argmax over the entries of
+ * positive weight w_v (max(0, p_n - q_n), or p_n) of ln w_v + g_v, ties to the
+ * lowest index.  On the GPU the race runs in fp32 on w_v / (-log2 u_v) (the same
+ * argmax); when its two best keys lie within 2^-10 of each other they are
+ * re-decided in double from the logits, so the token can differ from an exact
+ * evaluation only where the two best exact keys are within the rounding of the
+ * row sums.  sv_options.sampler selects the inverse transform instead (see
+ * there).  Outputs depend only on the values, the shapes and (seed, round): not
+ * on the stream, the launch shape or where the arrays sit in memory (every row
+ * is cut into pieces counted from the row's own start).
  *
  * Conventions for every entry point:
  *   - All array arguments are DEVICE pointers, row-major and contiguous; the caller
  *     owns every buffer.  The library never allocates or frees device memory and
- *     keeps no state between calls except a per-device SM-count cache.
+ *     keeps no state between calls except per-device caches of launch facts (SM
+ *     count, resident CTAs per SM) and, for spec_verify_noalloc only, its one
+ *     static scratch array and that array's cached device address (see there).
  *   - Work is queued on `cuda_stream` (a cudaStream_t; NULL = legacy default stream)
  *     and the call returns at once.  The return value reports only errors the host
  *     can see: bad arguments, misalignment, a too-small workspace, a launch failure.
@@ -64,7 +69,8 @@ typedef enum {
   SV_ERR_ALIGN = -3,       /* pointer misaligned (see conventions)                       */
   SV_ERR_WORKSPACE = -4,   /* workspace null or smaller than sv_workspace_bytes()        */
   SV_ERR_CUDA = -5,        /* a CUDA runtime call or kernel launch failed                */
-  SV_ERR_UNSUPPORTED = -6  /* device is not sm_103 or shape outside the fused kernel's set */
+  SV_ERR_UNSUPPORTED = -6  /* device is not sm_103, or a size an entry point does not
+                              support (stated at that entry point)                     */
 } sv_status;
 
 typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
@@ -78,7 +84,9 @@ enum {
                                     outputs of the row are then in range but unspecified  */
   SV_FLAG_RESIDUAL_FALLBACK = 4, /* max(0, p_n - q_n) had no positive entry in floating
                                     point; the token was drawn from p_n                   */
-  SV_FLAG_TIMEOUT = 8,           /* reserved: a bounded device-side wait gave up           */
+  SV_FLAG_TIMEOUT = 8,           /* a bounded device-side wait of the fused LM head gave up
+                                    (a tile that never arrived); the row's outputs are then
+                                    unspecified                                          */
   SV_FLAG_BAD_TOKEN = 16         /* a draft token outside [0, V): treated as p = q = 0    */
 };
 
@@ -200,6 +208,10 @@ int spec_verify_opts(const void* target_logits, const void* draft_logits,
  *     call first resets, on its stream, the counters and markers it relies on.
  *     Calls that overlap on the GPU (different streams or host threads) race on
  *     it: serialise them.
+ *   - The cached address belongs to the CUDA context current at the first call.
+ *     Calling spec_verify_noalloc after that context was destroyed
+ *     (cudaDeviceReset, or a primary context released and re-created) is not
+ *     supported: the cache is not refreshed.
  */
 int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
                         const int32_t* draft_tokens, int B, int gamma, int64_t V, int dtype,
@@ -299,14 +311,26 @@ int spec_lmhead_verify_drafted(const void* h_target, const void* W_target, int H
                                void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /* Profiling aid (not thread-safe): when `events` is non-NULL, following calls
- * record events[0] on their stream before the first kernel and events[k] after
- * the k-th of their kernels: for spec_verify the softmax sweep and the draw
- * (with the decision at its start and the select at its end; n >= 3); for
- * spec_lmhead_verify the first GEMM pass, the decision, the recompute pass and
- * the merge (n >= 5).  Only events[0..n-1] are recorded (n >= 1; at most 8).
- * NULL switches recording off.  The events are cudaEvent_t created by the
- * caller; they change no result. */
+ * record events on their stream: for spec_verify events[0] before the first
+ * kernel, events[1] after the softmax sweep (and the top-k / top-p kernels
+ * before it) and events[2] after the draw kernel (which takes the decision at
+ * its start and merges at its end; n >= 3); for spec_lmhead_verify events[0]
+ * first and events[k] after the first GEMM pass, the decision, the recompute
+ * pass and the merge (n >= 5).  Only events[0..n-1] are recorded (n >= 1; at
+ * most 8).  NULL switches recording off.  The events are cudaEvent_t created by
+ * the caller; they change no result. */
 int sv_set_timing_events(void* const* events, int n);
+
+/* Test only: failure detection without a GPU fault.  The next spec_lmhead_verify
+ * and spec_lmhead_verify_drafted calls withhold, in the first CTA of the first
+ * GEMM pass, the hand-over of accumulator `job` to the epilogue (job < 0: none),
+ * so that the epilogue's bounded wait runs out; and every bounded wait of the
+ * fused LM head gives up after `wait_limit` tries (0: the default limit).  A wait
+ * that gives up ends the CTA's other roles, lets the copies it issued land (a
+ * bounded wait again), frees its tensor memory and returns; the call still
+ * returns SV_OK and the batch rows carry SV_FLAG_TIMEOUT.  The setting stays
+ * until changed; not thread-safe.  Returns 0. */
+int sv_test_lmhead_stall(int job, uint32_t wait_limit);
 
 /* Human-readable name of a status code. */
 const char* sv_status_string(int status);

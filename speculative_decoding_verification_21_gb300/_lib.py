@@ -21,7 +21,7 @@ FLAG_ZERO_MASS, FLAG_NONFINITE, FLAG_RESIDUAL_FALLBACK, FLAG_TIMEOUT, FLAG_BAD_T
 EXPORTS = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verify_opts",
            "spec_verify_greedy", "spec_lmhead_verify", "spec_lmhead_draft",
            "spec_lmhead_verify_drafted",
-           "sv_set_timing_events", "sv_status_string", "sv_version")
+           "sv_set_timing_events", "sv_test_lmhead_stall", "sv_status_string", "sv_version")
 
 
 class Options(ctypes.Structure):
@@ -83,12 +83,21 @@ def load(build_if_missing: bool = True):
         L.spec_lmhead_draft.restype = I
         L.sv_set_timing_events.argtypes = [P, I]
         L.sv_set_timing_events.restype = I
+        L.sv_test_lmhead_stall.argtypes = [I, ctypes.c_uint32]
+        L.sv_test_lmhead_stall.restype = I
         L.sv_status_string.argtypes = [I]
         L.sv_status_string.restype = ctypes.c_char_p
         L.sv_version.argtypes = []
         L.sv_version.restype = I
         _lib = L
         return _lib
+
+
+def test_lmhead_stall(job: int, wait_limit: int = 0) -> None:
+    """Test only: the next fused LM-head calls withhold one accumulator hand-over
+    (job < 0: none) and give up every bounded wait after `wait_limit` tries (0: the
+    default); see sv_test_lmhead_stall in include/specverify.h."""
+    load().sv_test_lmhead_stall(int(job), int(wait_limit))
 
 
 def status_string(status: int) -> str:

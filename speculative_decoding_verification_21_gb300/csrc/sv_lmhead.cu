@@ -64,6 +64,10 @@ constexpr int kEpiWarps = 8;     // two per tensor-memory lane quadrant, each ha
 constexpr int kLmThreads = 32 * (3 + kEpiWarps);  // W producer, MMA issuer, h producer, epilogue
 constexpr int kTmemCols = 512;   // two accumulators of 256 columns
 constexpr uint32_t kWaitLimit = 1u << 22;
+// The wait limit and the withheld hand-over of the next launches (a failure
+// test sets them through sv_test_lmhead_stall; host-side, not thread-safe).
+uint32_t g_lm_wait_limit = kWaitLimit;
+int g_lm_stall_job = -1;
 constexpr int kMaxWStages = 8;  // W-ring slots
 constexpr int kHStagesPass2 = 3;  // h-ring slots of the recompute pass (small h tiles)
 constexpr int kMaxRep = 2;      // copies of the compact rows in the recompute pass
@@ -107,6 +111,9 @@ struct LmArgs {
   float* out_p;
   float* out_q;
   uint8_t* out_flags;
+  uint32_t wait_limit;  // tries of every bounded wait (kWaitLimit unless a test set it)
+  int stall_job;        // test only: the job of CTA 0's first pass whose accumulator is
+                        // never handed to the epilogue (-1: none)
 };
 
 __device__ __forceinline__ bool cand_better(const LmCand& a, const LmCand& b) {
@@ -164,9 +171,11 @@ __device__ Cand2 block_cand2(Cand2 t, Cand2* sm /* [32] */) {
   return r;
 }
 
-// Bounded wait that also gives up when another role of the CTA has aborted.
-__device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+// Bounded wait (`limit` tries) that also gives up when another role of the CTA
+// has aborted.
+__device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                        uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 63u && *abort_flag) return false;
   }
@@ -176,9 +185,9 @@ __device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity, volatile
 
 // The same for a whole warp: lane 0 polls, the others wait at the shuffle.
 __device__ __forceinline__ bool lm_wait_warp(uint64_t* bar, uint32_t parity,
-                                             volatile int* abort_flag) {
+                                             volatile int* abort_flag, uint32_t limit) {
   bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = lm_wait(bar, parity, abort_flag);
+  if ((threadIdx.x & 31) == 0) ok = lm_wait(bar, parity, abort_flag, limit);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
@@ -298,12 +307,13 @@ struct Slot {
   }
 };
 
-// Wait (bounded) until every copy issued into a ring has landed.
-__device__ void drain_ring(uint64_t* full, uint32_t n, uint32_t issued) {
+// Wait (bounded, `limit` tries per slot) until every copy issued into a ring
+// has landed.
+__device__ void drain_ring(uint64_t* full, uint32_t n, uint32_t issued, uint32_t limit) {
   for (uint32_t s = 0; s < n; ++s) {
     if (issued <= s) continue;
     const uint32_t last = (issued - 1u) - ((issued - 1u - s) % n);
-    mbar_wait_bounded(full + s, (last / n) & 1u);
+    mbar_wait_bounded(full + s, (last / n) & 1u, limit);
   }
 }
 
@@ -757,7 +767,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
               const uint32_t ws = w.i;
               const int k0 = kb * kKBlock;  // spans past the hidden size read as zeros
               if (isw) {
-                if (!lm_wait(empty + ws, w.ph ^ 1u, abort_flag)) {
+                if (!lm_wait(empty + ws, w.ph ^ 1u, abort_flag, a.wait_limit)) {
                   ok = false;
                   break;
                 }
@@ -768,7 +778,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
               } else {
                 if (k >= nh) {
                   // stage k - nh, the last to use this h slot, is done
-                  if (!lm_wait(empty + lag.i, lag.ph, abort_flag)) {
+                  if (!lm_wait(empty + lag.i, lag.ph, abort_flag, a.wait_limit)) {
                     ok = false;
                     break;
                   }
@@ -794,7 +804,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           }
         }
       }
-      drain_ring(full, nw, k);  // every issued copy has landed before the CTA may exit
+      drain_ring(full, nw, k, a.wait_limit);  // every issued copy has landed before the CTA may exit
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -807,7 +817,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         for (int job = 0; ok && job < Jobs<PASS>::kPerTile; ++job, ++jobi) {
           const int buf = jobi & 1;
           const uint32_t ap = (uint32_t)(jobi >> 1) & 1u;
-          if (!lm_wait(acce + buf, ap ^ 1u, abort_flag)) {
+          if (!lm_wait(acce + buf, ap ^ 1u, abort_flag, a.wait_limit)) {
             ok = false;
             break;
           }
@@ -818,7 +828,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             for (int kb = 0; kb < q.kblocks; ++kb) {
               const uint32_t ws = w.i;
               // one wait per stage: the copies of both producers have landed
-              if (!lm_wait(full + ws, w.ph, abort_flag)) {
+              if (!lm_wait(full + ws, w.ph, abort_flag, a.wait_limit)) {
                 ok = false;
                 break;
               }
@@ -843,7 +853,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
               hs.next(nh);
             }
           }
-          if (ok) umma_commit(accf + buf);
+          // (a test may withhold one hand-over: the epilogue's wait then runs out)
+          if (ok && !(PASS == 1 && blockIdx.x == 0 && jobi == a.stall_job)) umma_commit(accf + buf);
         }
       }
       // all MMAs of this CTA complete before tensor memory is released
@@ -874,7 +885,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       for (int job = 0; job < Jobs<PASS>::kPerTile; ++job) {
         const int buf = (jobi + job) & 1;
         const uint32_t ap = (uint32_t)((jobi + job) >> 1) & 1u;
-        if (!lm_wait_warp(accf + buf, ap, abort_flag)) {
+        if (!lm_wait_warp(accf + buf, ap, abort_flag, a.wait_limit)) {
           ok = false;
           break;
         }
@@ -908,10 +919,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       pass3_flush(a, quad, half, cy3, hring);
   }
 
-  if (threadIdx.x == 0 && *abort_flag) atomicOr(a.ctl + ((PASS == 1 || PASS == 4) ? 1 : 2), 1u);
   tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // every role is done: an abort by any of them is in the flag
   tc_fence_after();
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(a.ctl + ((PASS == 1 || PASS == 4) ? 1 : 2), 1u);
   if (warp == 1) tmem_dealloc(tbase, kTmemCols);
 }
 
@@ -1250,6 +1261,8 @@ int lmhead_verify(const void* h_target, const void* W_target, int Ht, const void
 
   char* ws = reinterpret_cast<char*>(workspace);
   LmArgs a{};
+  a.wait_limit = g_lm_wait_limit;
+  a.stall_job = g_lm_stall_job;
   a.xt = draft_tokens;
   a.B = B;
   a.gamma = gamma;
@@ -1359,6 +1372,8 @@ int lmhead_draft(const void* h_draft, const void* W_draft, int Hd, int B, int64_
 
   char* ws = reinterpret_cast<char*>(workspace);
   LmArgs a{};
+  a.wait_limit = g_lm_wait_limit;
+  a.stall_job = g_lm_stall_job;
   a.B = B;
   a.gamma = 1;
   a.V = (int)V;
@@ -1401,3 +1416,13 @@ int lmhead_draft(const void* h_draft, const void* W_draft, int Hd, int B, int64_
 }
 
 }  // namespace sv
+
+// Test only: the next fused LM-head launches withhold the first pass's hand-over
+// of accumulator `job` in CTA 0 (job < 0: none), so that the epilogue's wait runs
+// out, and every bounded wait gives up after `wait_limit` tries (0: the default).
+extern "C" int sv_test_lmhead_stall(int job, uint32_t wait_limit) {
+  sv::g_lm_stall_job = job < 0 ? -1 : job;
+  sv::g_lm_wait_limit = wait_limit ? wait_limit : sv::kWaitLimit;
+  return 0;
+}
+

@@ -188,8 +188,8 @@ def test_outputs_do_not_depend_on_addresses(dtype, V):
     """The same logits at three places in memory (16-byte aligned views starting
     at different offsets within a 4 KB block) give bit-identical tokens, counts,
     p, q, alpha and flags: the sweep cuts every row from its own start, so no sum
-    depends on where the row sits.  V = 6001 (bf16) takes the separate-kernel
-    path, the others the fused round."""
+    depends on where the row sits.  V = 6001 (bf16) takes the generic sweep (rows
+    not a multiple of 16 bytes), the others the vector sweep."""
     B, g = 8, 3
     zt0, zd0, xt = rand_case(V, B=B, g=g, dtype=dtype, seed=V)
     esz = 4 if dtype == torch.float32 else 2
