@@ -88,8 +88,8 @@ def tensor_peaks():
 
 # DRAM bytes per launch of the verify sweep from an ncu capture of the same
 # workload (profiles/ holds the summary); None when the kernel changed since.
-SWEEP_TRAFFIC_BYTES = None
-LMHEAD_PASS1_TRAFFIC_BYTES = 1580866592  # 1577.972 MB read + 2.895 MB written, profiles/k_lm_lmhead.md
+SWEEP_TRAFFIC_BYTES = 150913024  # 147.793 MB read + 3.120 MB written (ncu, one launch)
+LMHEAD_PASS1_TRAFFIC_BYTES = 1580866592  # 1577.972 MB read + 2.895 MB written (ncu, one launch)
 
 
 def cpu_model() -> str:
@@ -462,7 +462,7 @@ def run_ours(args):
                          "timing": f"CUDA events around k_sweep_vec, {reps} calls",
                          "step_share": kms[0] / (kms[0] + kms[1])},
             "race": {"kernel": "k_race", "ms": kms[1], "step_share": kms[1] / (kms[0] + kms[1]),
-                     "bound": "issue (Philox4x32-10 per entry; see profiles/k_race_sample_b64.md)"},
+                     "bound": "issue and latency (a Philox4x32-10 block per four entries)"},
             "kernel_ms": kavg,
             "gpu_launches": 2 * args.steps,  # k_sweep_vec and k_race per step
             "clocks": clk.summary(),
