@@ -127,7 +127,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -271,8 +271,9 @@ def _verify_call(L, stream, sets, tokens, counts, flags, ws, B, gamma, V, dt):
             P(ws.data_ptr()), ctypes.c_size_t(ws.numel()), sh)
     fn = L.spec_verify
 
-    def call(i):
-        rc = fn(*argsets[i % len(argsets)], 0, i, *tail)
+    def call(i, h=None):
+        t = tail if h is None else tail[:-1] + (h,)
+        rc = fn(*argsets[i % len(argsets)], 0, i, *t)
         if rc != 0:
             raise RuntimeError(f"spec_verify failed: {sv.status_string(rc)}")
     return call
@@ -369,6 +370,8 @@ def run_ours(args):
     with ClockSampler(local) as kclk:
         kms, call_ms = _kernel_times(L, stream, step, 2, reps)
     kavg = {"k_sweep_vec": kms[0], "k_race": kms[1], "call": call_ms}
+    # the same calls captured into one CUDA graph (no host launch cost between them)
+    gms = _graph_ms(lambda h, i: step(i, h), 2 * nsets)
     hbm, peak_kind = peaks()
     sweep_bytes = B * (2 * gamma + 1) * V * 2
     sweep_gbs = sweep_bytes / (kms[0] / 1000.0) / 1e9
@@ -464,6 +467,8 @@ def run_ours(args):
             "race": {"kernel": "k_race", "ms": kms[1], "step_share": kms[1] / (kms[0] + kms[1]),
                      "bound": "issue and latency (a Philox4x32-10 block per four entries)"},
             "kernel_ms": kavg,
+            "graph": {"ms_per_step": gms, "rounds_per_s": 1000.0 / gms,
+                      "note": f"{2 * nsets} calls captured in one CUDA graph, replayed"},
             "gpu_launches": 2 * args.steps,  # k_sweep_vec and k_race per step
             "clocks": clk.summary(),
             "clocks_kernel_loop": kclk.summary(),
@@ -594,6 +599,36 @@ def _kernel_times(L, stream, call, nkern, reps, warm=3):
     return [a / reps for a in acc], s0.elapsed_time(s1) / reps
 
 
+def _graph_ms(call_on, n, replays=20):
+    """Average ms per call of `call_on(stream_handle, i)`, i = 0..n-1, captured once
+    into a CUDA graph on a side stream and replayed `replays` times (no host
+    launch cost between the calls)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(3):
+            call_on(ctypes.c_void_p(s.cuda_stream), i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        cs = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        for i in range(n):
+            call_on(cs, i)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(replays):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (replays * n)
+    del g
+    return ms
+
+
 def measure_greedy(L, dev, stream, rank, reps=400):
     """Greedy verify on greedy_b64 (B=64, gamma=5, V=32000, bf16); inputs rotate
     over >= 4x L2."""
@@ -614,19 +649,25 @@ def measure_greedy(L, dev, stream, rank, reps=400):
     P = ctypes.c_void_p
     sh = P(stream.cuda_stream)
 
-    def call(i):
+    def call_on(h, i):
         s = sets[i % nsets]
         rc = L.spec_verify_greedy(P(s.zt.data_ptr()), P(s.xt.data_ptr()), B, g, V, 1,
                                   P(tok.data_ptr()), P(cnt.data_ptr()), P(ws.data_ptr()),
-                                  ctypes.c_size_t(ws.numel()), sh)
+                                  ctypes.c_size_t(ws.numel()), h)
         if rc != 0:
             raise RuntimeError(sv.status_string(rc))
 
+    def call(i):
+        call_on(sh, i)
+
     kms, ms = _kernel_times(L, stream, call, 1, reps)
+    gms = _graph_ms(call_on, 4 * nsets)
     hbm, kind = peaks()
     gbs = per / (kms[0] / 1000.0) / 1e9
     return {"workload": "greedy_b64", "B": B, "gamma": g, "V": V, "dtype": "bf16",
             "rounds_per_s": 1000.0 / ms, "ms_per_round": ms, "kernel_ms": {"k_greedy": kms[0]},
+            "graph": {"ms_per_round": gms, "rounds_per_s": 1000.0 / gms,
+                      "note": f"{4 * nsets} calls captured in one CUDA graph, replayed"},
             "roofline": {"bound": "hbm", "kernel": "k_greedy", "achieved": gbs, "peak": hbm,
                          "peak_kind": kind, "unit": "GB/s", "frac": gbs / hbm,
                          "algorithmic_bytes": per},
