@@ -53,7 +53,7 @@ struct SweepCtx {
   const float* thr;      // [B][R1] top-k thresholds (logits below have weight 0) or null
   uint32_t* done;        // [B] arrival counters of the draw, zeroed by every sweep
   uint32_t* thw;         // [B] the race's shared lower bound on its second-best key (float
-                         // bits, 0: none yet), zeroed by every sweep and the fused round
+                         // bits, 0: none yet), zeroed by every sweep
 };
 
 // The partials of one logit row, in row order: [np] consecutive entries.  Each

@@ -263,7 +263,8 @@ struct RaceStage {
   static constexpr int kVecs = (DT == SV_F32) ? 2 : 1;
   static constexpr int kRound = kRuns * 2 * kVecs * 32;  // uint4 per round, both rows
 };
-constexpr size_t kRaceWarpSmem = 2 * 4 * 2 * 32 * sizeof(uint4);  // 8 KB, both types
+constexpr int kRaceStages = 3;  // rounds staged per warp: one raced, the others in flight
+constexpr size_t kRaceWarpSmem = kRaceStages * 4 * 2 * 32 * sizeof(uint4);  // 4 KB a round
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
@@ -279,23 +280,31 @@ __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// The race over entries [lo, hi) of row n (and of draft row n for a residual):
-// lane l takes the runs of eight at lo + 8 (l + 32 i), kRuns of them per
-// round of loads.  Whole 16-byte runs go through the warp's shared memory `sb`
-// (kRaceWarpSmem bytes) by cp.async, the next round's copies in flight while
-// this round is raced; a run cut by the row's end (or any run of rows that do
-// not start on 16-byte boundaries, !vec) is loaded directly.  Each lane reads
-// back only its own copies.  lo is a multiple of 8.  `th` (the same in every
-// lane) is the warp's bound on the second-best key, carried from one range to
-// the next; while it is unset, the largest-logit entry of each lane's first
-// run is keyed first to set it.  `thw` (or null) is a bound shared by every
-// warp racing the same draw: each round reads it and raises it to th
-// afterwards (any warp's bound holds for the union of their candidates).
-template <int DT, bool RESID, bool TOPK>
-__device__ __forceinline__ void race_range(const char* rt, const char* rd, int64_t lo, int64_t hi,
-                                           int64_t V, bool vec, const DrawState& st, float kd,
-                                           uint64_t seed, uint64_t round, int b, KeyTop2& t,
-                                           float& th, uint32_t* thw, uint4* sb) {
+// A round of the race: entries [lo, hi) of the draw row (hi <= lo: none; V <
+// 2^31, so entry indices fit in 32 bits).
+struct RaceRound {
+  int32_t lo, hi;
+};
+
+// The race over the rounds `next()` hands out (warp-uniform; once it returns an
+// empty round it returns no other) of row n (and of draft row n for a
+// residual): a round holds at most kRuns runs of eight per lane, lane l taking
+// the runs at lo + 8 (l + 32 u).  Whole 16-byte runs go through the warp's
+// shared memory `sb` (kRaceWarpSmem bytes) by cp.async, the next
+// kRaceStages - 1 rounds' copies in flight while one round is raced; a run cut
+// by the row's end (or any run of rows that do not start on 16-byte
+// boundaries, !vec) is loaded directly.  Each lane reads back only its own
+// copies.  Round starts are multiples of 8.  `th` (the same in every lane) is
+// the warp's bound on the second-best key, carried from one call to the next;
+// while it is unset, the largest-logit entry of each lane's first run is keyed
+// first to set it.  `thw` (or null) is a bound shared by every warp racing the
+// same draw: each round reads it and raises it to th afterwards (any warp's
+// bound holds for the union of their candidates).
+template <int DT, bool RESID, bool TOPK, class Next>
+__device__ __forceinline__ void race_rounds(const char* rt, const char* rd, int64_t V, bool vec,
+                                            const DrawState& st, float kd, uint64_t seed,
+                                            uint64_t round, int b, KeyTop2& t, float& th,
+                                            uint32_t* thw, uint4* sb, Next&& next) {
   using RS = RaceStage<DT>;
   constexpr int kRuns = RS::kRuns, kVecs = RS::kVecs;
   constexpr int kElem = (DT == SV_F32) ? 4 : 2;
@@ -309,48 +318,55 @@ __device__ __forceinline__ void race_range(const char* rt, const char* rd, int64
                    : "memory");
   };
   const uint32_t c1 = (1u << 24) | (uint32_t)st.pos, c2 = (uint32_t)b, c3 = (uint32_t)round;
-  const int nrun = (int)((hi - lo + 7) >> 3);
+  auto nruns = [](const RaceRound& q) { return q.hi > q.lo ? (int)((q.hi - q.lo + 7) >> 3) : 0; };
   // slot of (round buffer s, run u, row w, vector q) for this lane
   auto slot = [&](int s, int u, int w, int q) {
     return sb + s * RS::kRound + ((u * 2 + w) * kVecs + q) * 32 + lane;
   };
   auto whole = [&](int64_t v0) { return vec && v0 + 8 <= V; };
-  auto issue = [&](int r0, int s) {
+  auto issue = [&](const RaceRound& q, int s) {
+    const int n = nruns(q);
 #pragma unroll
     for (int u = 0; u < kRuns; ++u) {
-      const int r = r0 + lane + 32 * u;
-      const int64_t v0 = lo + 8 * (int64_t)r;
-      if (r < nrun && whole(v0)) {
+      const int r = lane + 32 * u;
+      const int64_t v0 = q.lo + 8 * (int64_t)r;
+      if (r < n && whole(v0)) {
 #pragma unroll
-        for (int q = 0; q < kVecs; ++q) {
-          cp_async16(slot(s, u, 0, q), rt + v0 * kElem + 16 * q);
-          if (RESID) cp_async16(slot(s, u, 1, q), rd + v0 * kElem + 16 * q);
+        for (int k = 0; k < kVecs; ++k) {
+          cp_async16(slot(s, u, 0, k), rt + v0 * kElem + 16 * k);
+          if (RESID) cp_async16(slot(s, u, 1, k), rd + v0 * kElem + 16 * k);
         }
       }
     }
-    cp_async_commit_group();
+    cp_async_commit_group();  // (possibly empty: the count of groups stays the same)
   };
-  issue(0, 0);
-  for (int r0 = 0, s = 0; r0 < nrun; r0 += 32 * kRuns, s ^= 1) {
+  // q[0] is raced from buffer s, q[k] is in flight in buffer (s + k) mod kRaceStages
+  RaceRound q[kRaceStages];
+#pragma unroll
+  for (int k = 0; k < kRaceStages - 1; ++k) {
+    q[k] = next();
+    issue(q[k], k);
+  }
+  for (int s = 0; q[0].hi > q[0].lo; s = (s + 1 == kRaceStages) ? 0 : s + 1) {
     uint32_t g = 0u;
     if (thw != nullptr && lane == 0)
       asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(g) : "l"(thw) : "memory");
-    if (r0 + 32 * kRuns < nrun)
-      issue(r0 + 32 * kRuns, s ^ 1);  // the next round, into the other buffer
-    else
-      cp_async_commit_group();        // (an empty group: the count stays the same)
-    cp_async_wait_group<1>();         // this round's copies have landed
+    q[kRaceStages - 1] = next();
+    issue(q[kRaceStages - 1], (s + kRaceStages - 1) % kRaceStages);  // the buffer raced last
+    cp_async_wait_group<kRaceStages - 1>();  // this round's copies have landed
+    const int64_t lo = q[0].lo;
+    const int nrun = nruns(q[0]);
     Raw8<DT> xt[kRuns], xd[kRuns];
 #pragma unroll
     for (int u = 0; u < kRuns; ++u) {
-      const int r = r0 + lane + 32 * u;
+      const int r = lane + 32 * u;
       const int64_t v0 = lo + 8 * (int64_t)r;
       if (r >= nrun) continue;
       if (whole(v0)) {
 #pragma unroll
-        for (int q = 0; q < kVecs; ++q) {
-          xt[u].v[q] = *slot(s, u, 0, q);
-          if (RESID) xd[u].v[q] = *slot(s, u, 1, q);
+        for (int k = 0; k < kVecs; ++k) {
+          xt[u].v[k] = *slot(s, u, 0, k);
+          if (RESID) xd[u].v[k] = *slot(s, u, 1, k);
         }
       } else {
         xt[u] = load_raw8<DT>(rt, v0, V, vec, -kInf);
@@ -360,11 +376,10 @@ __device__ __forceinline__ void race_range(const char* rt, const char* rd, int64
     g = __shfl_sync(0xffffffffu, g, 0);
     if (g != 0u) th = fmaxf(th, __uint_as_float(g));
     if (!(th > 0.0f)) {  // the same in every lane: seeds from each lane's first run
-      const int r = r0 + lane;
       float k = -kInf;
-      if (r < nrun)
-        k = run_seed_key<DT, RESID, TOPK>(xt[0], xd[0], run_max<DT>(xt[0]), lo + 8 * (int64_t)r, st,
-                                          kd, pk, c1, c2, c3);
+      if (lane < nrun)
+        k = run_seed_key<DT, RESID, TOPK>(xt[0], xd[0], run_max<DT>(xt[0]), lo + 8 * (int64_t)lane,
+                                          st, kd, pk, c1, c2, c3);
       // the second largest seed over the lanes (distinct entries)
       const float m1 = warp_max(k);
       const unsigned top = __ballot_sync(0xffffffffu, k == m1);
@@ -376,11 +391,11 @@ __device__ __forceinline__ void race_range(const char* rt, const char* rd, int64
     // entries left, in increasing order
     uint32_t rw[kRuns][8];
 #pragma unroll
-    for (int u = 0; u < kRuns; ++u) run_words(lo + 8 * (int64_t)(r0 + lane + 32 * u), c1, c2, c3, pk, rw[u]);
+    for (int u = 0; u < kRuns; ++u) run_words(lo + 8 * (int64_t)(lane + 32 * u), c1, c2, c3, pk, rw[u]);
     const float tau = prune_tau(fmaxf(th, t.b.k));
 #pragma unroll
     for (int u = 0; u < kRuns; ++u) {
-      const int r = r0 + lane + 32 * u;
+      const int r = lane + 32 * u;
       uint32_t live = 0u;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -400,29 +415,51 @@ __device__ __forceinline__ void race_range(const char* rt, const char* rd, int64
     }
     th = fmaxf(th, warp_second_bound(t));
     share();
+#pragma unroll
+    for (int k = 0; k < kRaceStages - 1; ++k) q[k] = q[k + 1];
   }
-  cp_async_wait_group<0>();  // nothing of this range left in flight
+  cp_async_wait_group<0>();  // nothing left in flight
 }
 
-// The race of a draw over [lo, hi) of its row in the mode the decision set
-// (residual, or p_n), into t.
-// thw: the bound shared by the warps racing this draw, or null; sb: the warp's
-// kRaceWarpSmem bytes of shared memory.
-template <int DT, bool TOPK>
-__device__ __forceinline__ void race_draw(const SweepCtx& x, int b, const DrawState& st, bool resid,
-                                          int64_t lo, int64_t hi, bool vec, KeyTop2& t,
-                                          float& th, uint32_t* thw, uint4* sb) {
+// Entries per round of the race (kRuns runs of eight per lane).
+template <int DT>
+constexpr int64_t race_round_entries() {
+  return (int64_t)32 * 8 * RaceStage<DT>::kRuns;
+}
+
+// The race of a draw in the mode the decision set (residual, or p_n), into t,
+// over the rounds `next()` hands out.  thw: the bound shared by the warps
+// racing this draw, or null; sb: the warp's kRaceWarpSmem bytes of shared
+// memory.
+template <int DT, bool TOPK, class Next>
+__device__ __forceinline__ void race_draw_rounds(const SweepCtx& x, int b, const DrawState& st,
+                                                 bool resid, bool vec, KeyTop2& t, float& th,
+                                                 uint32_t* thw, uint4* sb, Next&& next) {
   const int gamma = x.gamma;
   const int64_t V = x.V;
   const char* rt = row_ptr<DT>(x.zt, x.zd, b, st.pos, gamma, V);
   if (resid) {
     const char* rd = row_ptr<DT>(x.zt, x.zd, b, gamma + 1 + st.pos, gamma, V);
-    race_range<DT, true, TOPK>(rt, rd, lo, hi, V, vec, st, __fsub_rn(st.K, st.mct), x.seed,
-                               x.round, b, t, th, thw, sb);
+    race_rounds<DT, true, TOPK>(rt, rd, V, vec, st, __fsub_rn(st.K, st.mct), x.seed, x.round, b,
+                                t, th, thw, sb, next);
   } else {
-    race_range<DT, false, TOPK>(rt, rt, lo, hi, V, vec, st, 0.0f, x.seed, x.round, b, t, th, thw,
-                                sb);
+    race_rounds<DT, false, TOPK>(rt, rt, V, vec, st, 0.0f, x.seed, x.round, b, t, th, thw, sb,
+                                 next);
   }
+}
+
+// The same over the contiguous entries [lo, hi) (lo a multiple of 8).
+template <int DT, bool TOPK>
+__device__ __forceinline__ void race_draw(const SweepCtx& x, int b, const DrawState& st, bool resid,
+                                          int64_t lo, int64_t hi, bool vec, KeyTop2& t,
+                                          float& th, uint32_t* thw, uint4* sb) {
+  int64_t at = lo;
+  race_draw_rounds<DT, TOPK>(x, b, st, resid, vec, t, th, thw, sb, [&]() {
+    const int64_t e = at + race_round_entries<DT>() < hi ? at + race_round_entries<DT>() : hi;
+    const RaceRound q{(int32_t)at, (int32_t)e};
+    if (e > at) at = e;
+    return q;
+  });
 }
 
 // The token from the best two keys T over the whole row of the race that drew

@@ -741,21 +741,20 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
 
 // --------------------------------------------------------------------------
 // k_race: the target's own token by Gumbel-max (the default sampler) after a
-// separate sweep.  One CTA per (batch row, spc race slices of kRaceSlice
-// entries), one resident wave.  Every CTA takes its batch row's decision
-// (decide_in_cta); each warp races one eighth of the CTA's slices in one piece
-// (its rounds of loads staged in shared memory, the next round in flight while
-// one is raced), the CTA keeps the best two, and the CTA of the batch row that
-// finishes last (a per-batch-row counter the sweep zeroes) merges them and
-// emits.  The warps racing one draw share their bound on the second-best key
-// through a word per batch row (zeroed by the sweep).
+// separate sweep.  nsplit CTAs per batch row, one resident wave.  Every CTA
+// takes its batch row's decision (decide_in_cta); each warp then races one
+// eighth of the CTA's share of the slices (kRaceSlice entries each) in one
+// contiguous piece, its rounds of loads staged in shared memory with the next
+// rounds in flight.  The CTA keeps the best two, and the CTA of the batch row
+// that finishes last (a per-batch-row counter the sweep zeroes) merges them
+// and emits.  The warps racing one draw share their bound on the second-best
+// key through a word per batch row (zeroed by the sweep).
 // --------------------------------------------------------------------------
 struct RaceArgs {
   uint64_t* cword;        // [B][nsplit][2] the race's best two per CTA
   uint32_t* alpha_cnt;    // [B] counters of the optional overlap kernel, zeroed here
   uint32_t* done;         // [B] CTAs of the batch row that finished (zeroed by the sweep)
   int nsplit;             // CTAs per batch row
-  int spc;                // race slices per CTA
   bool vec;               // 16-byte loads of 8 entries are aligned in every row
 };
 constexpr size_t kRaceSmemBytes = (kThreads / 32) * kRaceWarpSmem;
@@ -778,10 +777,12 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) k_race(SweepCtx x, R
   const DrawState st = s_st;
   if (st.mode == kDrawDone) return;  // the same in every CTA of the batch row
   const bool resid = st.mode == kDrawResidual;
-  // the CTA's slices [clo, chi) in one piece per warp (a multiple of 8 entries
-  // each), so that a warp's rounds of loads follow one another
-  const int64_t clo = (int64_t)split * a.spc * kRaceSlice;
-  const int64_t chi = min(V, clo + (int64_t)a.spc * kRaceSlice);
+  // the CTA's share of the batch row's slices, one contiguous piece per warp (a
+  // multiple of 8 entries each), so that a warp's rounds follow one another
+  const int S = (int)race_slices(V);
+  const int spc = (S + a.nsplit - 1) / a.nsplit;
+  const int64_t clo = (int64_t)split * spc * kRaceSlice;
+  const int64_t chi = min(V, clo + (int64_t)spc * kRaceSlice);
   const int64_t wlen = ceil_div(ceil_div(chi - clo, (int64_t)kWarps), (int64_t)8) * 8;
   const int64_t wlo = clo + warp * wlen;
   const int64_t whi = min(chi, wlo + wlen);
@@ -1071,16 +1072,13 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
                             stream, sx, da);
   } else {
     // Gumbel-max: one resident wave of race CTAs (every CTA takes its batch
-    // row's decision, so a second wave would pay that latency again), at least
-    // two slices per warp of a CTA
+    // row's decision, so a second wave would pay that latency again), about two
+    // slices per warp at least
     const int64_t S = race_slices(V);
     const int64_t rslots = (int64_t)di->sms * max(1, di->race_ctas_per_sm[DT][masked ? 1 : 0]);
     int64_t nsplit = ceil_div(S, (int64_t)(2 * kThreads / 32));
     if ((int64_t)B * nsplit > rslots) nsplit = (rslots / B > 1) ? rslots / B : 1;
-    const int64_t spc = ceil_div(S, nsplit);
-    nsplit = ceil_div(S, spc);  // no CTA without slices
-    RaceArgs ra{reinterpret_cast<uint64_t*>(ws + pl.off_cword), alpha_cnt, done, (int)nsplit,
-                (int)spc, vec};
+    RaceArgs ra{reinterpret_cast<uint64_t*>(ws + pl.off_cword), alpha_cnt, done, (int)nsplit, vec};
     e = masked ? launch_pdl(k_race<DT, true>, dim3((unsigned)(nsplit * B)), dim3(kThreads),
                             kRaceSmemBytes, stream, sx, ra)
                : launch_pdl(k_race<DT, false>, dim3((unsigned)(nsplit * B)), dim3(kThreads),
