@@ -1072,11 +1072,11 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
                             stream, sx, da);
   } else {
     // Gumbel-max: one resident wave of race CTAs (every CTA takes its batch
-    // row's decision, so a second wave would pay that latency again), about two
-    // slices per warp at least
+    // row's decision, so a second wave would pay that latency again), at least
+    // one slice per warp
     const int64_t S = race_slices(V);
     const int64_t rslots = (int64_t)di->sms * max(1, di->race_ctas_per_sm[DT][masked ? 1 : 0]);
-    int64_t nsplit = ceil_div(S, (int64_t)(2 * kThreads / 32));
+    int64_t nsplit = ceil_div(S, (int64_t)(kThreads / 32));
     if ((int64_t)B * nsplit > rslots) nsplit = (rslots / B > 1) ? rslots / B : 1;
     RaceArgs ra{reinterpret_cast<uint64_t*>(ws + pl.off_cword), alpha_cnt, done, (int)nsplit, vec};
     e = masked ? launch_pdl(k_race<DT, true>, dim3((unsigned)(nsplit * B)), dim3(kThreads),
