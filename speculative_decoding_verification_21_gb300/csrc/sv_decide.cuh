@@ -29,7 +29,7 @@ __device__ __forceinline__ const char* row_ptr(const void* zt, const void* zd, i
 }
 
 // --------------------------------------------------------------------------
-// Row combine and decision (the start of k_draw; k_lm_finish on the fused path).
+// Row combine and decision (the start of k_race and k_draw; k_lm_finish on the fused path).
 // --------------------------------------------------------------------------
 struct SweepCtx {
   const void* zt;

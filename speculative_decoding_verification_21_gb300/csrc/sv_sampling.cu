@@ -161,10 +161,9 @@ __global__ void __launch_bounds__(kSweepWarps * 32, kSweepCtasPerSm) k_sweep_vec
   unit_loop<DT, TOPK, kSweepBufs>(
       x, x.np, (NU - 1) / W, sweep_buf + (threadIdx.x >> 5) * kSweepBufs * 256,
       (int)(blockIdx.x * kSweepWarps + (threadIdx.x >> 5)), (int)W,
-      [&](int64_t g, float2 p, int) {
+      [&](int64_t g, float2 p) {
         if ((threadIdx.x & 31) == 0) x.part[g] = p;
-      },
-      [](int64_t, int64_t) {});
+      });
 }
 
 // --------------------------------------------------------------------------

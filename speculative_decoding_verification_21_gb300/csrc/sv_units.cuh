@@ -5,11 +5,12 @@
 // row may be shorter.  Chunks are numbered in batch-row order, g = (b R1 + k)
 // nck + j, and warp w of W takes g = w, w + W, w + 2W, ...: the whole GPU walks
 // the batch rows in order, so each batch row's chunks complete one after
-// another.  A warp keeps NBUF chunks in flight in its own shared-memory
-// buffers (cp.async, 16 bytes per lane and vector, no registers held while the
-// copies are in flight); lane l copies and later reads vectors l + 32u of a
-// chunk.  The address of each chunk comes from a cursor stepped by fixed
-// increments (no division in the loop).  Each chunk leaves one partial: its
+// another.  A warp stages its chunks in NBUF shared-memory buffers of its own
+// (cp.async, 16 bytes per lane and vector, no registers held while the copies
+// are in flight): NBUF - 1 chunks in flight while one is reduced; lane l
+// copies and later reads vectors l + 32u of a chunk.  The address of each
+// chunk comes from a cursor stepped by fixed increments (no division in the
+// loop).  Each chunk leaves one partial: its
 // largest logit as given and the sum of 2^(y - max y) (y = z T^-1 log2 e).  The
 // partials depend only on the values and the shapes, not on where the arrays
 // sit in memory.
@@ -33,7 +34,6 @@ struct UnitInfo {
   int nv;     // 16-byte vectors in the chunk (256 for a full one)
   float c;    // the batch row's scale fl32(1/T) log2 e
   float tau;  // top-k threshold of the row (-inf: none)
-  int row;    // its logit row, b R1 + k
 };
 
 template <int DT, bool TOPK>
@@ -46,7 +46,6 @@ __device__ __forceinline__ UnitInfo unit_info(const SweepCtx& x, const UnitCurso
   r.p = reinterpret_cast<const uint4*>(row_ptr<DT>(x.zt, x.zd, u.b, u.k, x.gamma, x.V) + off);
   r.c = x.row_T ? log2_scale(inv_temperature(__ldg(x.row_T + u.b))) : c_all;
   r.tau = TOPK ? __ldg(x.thr + (int64_t)u.b * (2 * x.gamma + 1) + u.k) : -kInf;
-  r.row = u.b * (2 * x.gamma + 1) + u.k;
   return r;
 }
 
@@ -79,14 +78,14 @@ __device__ __forceinline__ float2 unit_reduce(const uint4 (&v)[8], const UnitInf
   return warp_chunk_partial(zmax, mc, sacc, u.c);
 }
 
-// The loop of sweep warp w of W over its chunks, and over the iterations after
-// them up to `it_end`.  `wbuf` is the warp's NBUF x 4 KB of shared memory.  At
-// iteration `it` the copies of chunk it + NBUF - 1 are issued, chunk it is
-// reduced (its partial goes to `emit(g, partial, logit row)`, and `tasks(it,
-// g)` runs with g its chunk or -1 when the warp has none left).
-template <int DT, bool TOPK, int NBUF, class Emit, class Tasks>
+// The loop of sweep warp w of W over its chunks g = w + it W, it = 0..it_end
+// (iterations past the last chunk only commit empty copy groups).  `wbuf` is
+// the warp's NBUF x 4 KB of shared memory.  At iteration `it` the copies of
+// chunk it + NBUF - 1 are issued and chunk it is reduced; its partial goes to
+// `emit(g, partial)`.
+template <int DT, bool TOPK, int NBUF, class Emit>
 __device__ __forceinline__ void unit_loop(const SweepCtx& x, int nck, int64_t it_end, uint4* wbuf,
-                                          int w, int W, Emit&& emit, Tasks&& tasks) {
+                                          int w, int W, Emit&& emit) {
   const int lane = threadIdx.x & 31;
   const int R1 = 2 * x.gamma + 1;
   const int64_t NU = (int64_t)x.B * R1 * nck;
@@ -125,10 +124,7 @@ __device__ __forceinline__ void unit_loop(const SweepCtx& x, int nck, int64_t it
         uint4 v[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) v[q] = wbuf[256 * i + 32 * q + lane];
-        emit(g, unit_reduce<DT, TOPK>(v, info[i]), info[i].row);
-        tasks(it, g);
-      } else {
-        tasks(it, (int64_t)-1);
+        emit(g, unit_reduce<DT, TOPK>(v, info[i]));
       }
     }
   }
