@@ -194,23 +194,19 @@ __device__ __forceinline__ void run_words(int64_t v0, uint32_t c1, uint32_t c2, 
   }
 }
 
-// The key of a run's largest-logit entry (the first of equal ones): a seed for
-// the pruning bound.  -inf when that entry has no weight.
+// The key of a run's largest-logit entry (the first of equal ones), from the
+// run's Philox words rw: a seed for the pruning bound.  -inf when that entry
+// has no weight.
 template <int DT, bool RESID, bool TOPK>
 __device__ __forceinline__ float run_seed_key(const Raw8<DT>& xt, const Raw8<DT>& xd, float zmax,
-                                              int64_t v0, const DrawState& st, float kd,
-                                              const PhiloxKeys& pk, uint32_t c1, uint32_t c2,
-                                              uint32_t c3) {
+                                              const uint32_t (&rw)[8], const DrawState& st,
+                                              float kd) {
   int es = 0;
   for (int e = 7; e >= 0; --e)
     if (run_at<DT>(xt, e) == zmax) es = e;
-  const int64_t v = v0 + es;
-  const uint4 x = philox_rk(make_uint4((uint32_t)(v >> 2), c1, c2, c3), pk);
-  const int l = (int)(v & 3);
-  const uint32_t r = (l == 0) ? x.x : (l == 1) ? x.y : (l == 2) ? x.z : x.w;
   return race_key(race_weight<RESID, TOPK>(run_at<DT>(xt, es), RESID ? run_at<DT>(xd, es) : 0.0f,
                                            st, kd),
-                  r);
+                  word_at(rw, es));
 }
 
 // Pruning of a block of four entries (one Philox block): their weights are at
@@ -353,63 +349,67 @@ __device__ __forceinline__ void race_rounds(const char* rt, const char* rd, int6
       asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(g) : "l"(thw) : "memory");
     q[kRaceStages - 1] = next();
     issue(q[kRaceStages - 1], (s + kRaceStages - 1) % kRaceStages);  // the buffer raced last
-    cp_async_wait_group<kRaceStages - 1>();  // this round's copies have landed
     const int64_t lo = q[0].lo;
     const int nrun = nruns(q[0]);
-    Raw8<DT> xt[kRuns], xd[kRuns];
+    // the Philox words of all runs first (independent chains, interleaved): they
+    // need neither this round's copies nor the shared bound, whose latencies
+    // they cover
+    uint32_t rw[kRuns][8];
 #pragma unroll
-    for (int u = 0; u < kRuns; ++u) {
-      const int r = lane + 32 * u;
-      const int64_t v0 = lo + 8 * (int64_t)r;
-      if (r >= nrun) continue;
+    for (int u = 0; u < kRuns; ++u) run_words(lo + 8 * (int64_t)(lane + 32 * u), c1, c2, c3, pk, rw[u]);
+    cp_async_wait_group<kRaceStages - 1>();  // this round's copies have landed
+    // run u of this lane (from its own copies; a ragged tail from global memory),
+    // read when it is pruned so that only one run's logits are held at a time
+    auto load_run = [&](int u, Raw8<DT>& a, Raw8<DT>& d) {
+      const int64_t v0 = lo + 8 * (int64_t)(lane + 32 * u);
       if (whole(v0)) {
 #pragma unroll
         for (int k = 0; k < kVecs; ++k) {
-          xt[u].v[k] = *slot(s, u, 0, k);
-          if (RESID) xd[u].v[k] = *slot(s, u, 1, k);
+          a.v[k] = *slot(s, u, 0, k);
+          if (RESID) d.v[k] = *slot(s, u, 1, k);
         }
       } else {
-        xt[u] = load_raw8<DT>(rt, v0, V, vec, -kInf);
-        if (RESID) xd[u] = load_raw8<DT>(rd, v0, V, vec, -kInf);
+        a = load_raw8<DT>(rt, v0, V, vec, -kInf);
+        if (RESID) d = load_raw8<DT>(rd, v0, V, vec, -kInf);
       }
-    }
+    };
     g = __shfl_sync(0xffffffffu, g, 0);
     if (g != 0u) th = fmaxf(th, __uint_as_float(g));
     if (!(th > 0.0f)) {  // the same in every lane: seeds from each lane's first run
       float k = -kInf;
-      if (lane < nrun)
-        k = run_seed_key<DT, RESID, TOPK>(xt[0], xd[0], run_max<DT>(xt[0]), lo + 8 * (int64_t)lane,
-                                          st, kd, pk, c1, c2, c3);
+      if (lane < nrun) {
+        Raw8<DT> a, d;
+        load_run(0, a, d);
+        k = run_seed_key<DT, RESID, TOPK>(a, d, run_max<DT>(a), rw[0], st, kd);
+      }
       // the second largest seed over the lanes (distinct entries)
       const float m1 = warp_max(k);
       const unsigned top = __ballot_sync(0xffffffffu, k == m1);
       th = fmaxf(th, (__popc(top) > 1) ? m1 : warp_max(k == m1 ? -kInf : k));
       share();
     }
-    // the Philox words of all runs first (independent chains, interleaved),
-    // then the pruning of each block of four against one bound, then the rare
+    // the pruning of each block of four against one bound, then the rare
     // entries left, in increasing order
-    uint32_t rw[kRuns][8];
-#pragma unroll
-    for (int u = 0; u < kRuns; ++u) run_words(lo + 8 * (int64_t)(lane + 32 * u), c1, c2, c3, pk, rw[u]);
     const float tau = prune_tau(fmaxf(th, t.b.k));
 #pragma unroll
     for (int u = 0; u < kRuns; ++u) {
       const int r = lane + 32 * u;
+      if (r >= nrun) continue;
+      Raw8<DT> xt, xd;
+      load_run(u, xt, xd);
       uint32_t live = 0u;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t R = prune_word(half_max<DT>(xt[u], h), st, tau);
+        const uint32_t R = prune_word(half_max<DT>(xt, h), st, tau);
 #pragma unroll
         for (int e = 4 * h; e < 4 * h + 4; ++e) live |= (rw[u][e] >= R ? 1u : 0u) << e;
       }
-      if (r >= nrun) live = 0u;
       const int64_t v0 = lo + 8 * (int64_t)r;
       while (live != 0u) {
         const int e = __ffs((int)live) - 1;
         live &= live - 1u;
-        const float w = race_weight<RESID, TOPK>(run_at<DT>(xt[u], e),
-                                                 RESID ? run_at<DT>(xd[u], e) : 0.0f, st, kd);
+        const float w = race_weight<RESID, TOPK>(run_at<DT>(xt, e),
+                                                 RESID ? run_at<DT>(xd, e) : 0.0f, st, kd);
         top2_push(t, race_key(w, word_at(rw[u], e)), (int)(v0 + e));
       }
     }
