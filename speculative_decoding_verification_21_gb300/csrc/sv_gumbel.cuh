@@ -306,12 +306,16 @@ __device__ __forceinline__ void race_rounds(const char* rt, const char* rd, int6
   constexpr int kElem = (DT == SV_F32) ? 4 : 2;
   const int lane = threadIdx.x & 31;
   const PhiloxKeys pk = philox_keys(seed);
-  // th into the shared bound (no reply waited for; keys are positive, so their
-  // bits order as integers)
+  // th into the shared bound when it is above what the word is known to hold
+  // (no reply waited for; keys are positive, so their bits order as integers)
+  float known = 0.0f;
   auto share = [&]() {
-    if (thw != nullptr && lane == 0 && th > 0.0f)
-      asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(thw), "r"(__float_as_uint(th))
-                   : "memory");
+    if (thw != nullptr && th > known) {
+      if (lane == 0)
+        asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(thw), "r"(__float_as_uint(th))
+                     : "memory");
+      known = th;
+    }
   };
   const uint32_t c1 = (1u << 24) | (uint32_t)st.pos, c2 = (uint32_t)b, c3 = (uint32_t)round;
   auto nruns = [](const RaceRound& q) { return q.hi > q.lo ? (int)((q.hi - q.lo + 7) >> 3) : 0; };
@@ -374,7 +378,10 @@ __device__ __forceinline__ void race_rounds(const char* rt, const char* rd, int6
       }
     };
     g = __shfl_sync(0xffffffffu, g, 0);
-    if (g != 0u) th = fmaxf(th, __uint_as_float(g));
+    if (g != 0u) {
+      th = fmaxf(th, __uint_as_float(g));
+      known = fmaxf(known, __uint_as_float(g));
+    }
     if (!(th > 0.0f)) {  // the same in every lane: seeds from each lane's first run
       float k = -kInf;
       if (lane < nrun) {

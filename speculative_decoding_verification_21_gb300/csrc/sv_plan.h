@@ -87,12 +87,17 @@ struct DrawState {
   float zmd;     // draft row n: largest logit as given (residual only)
 };
 
+// The race's shared bound of a batch row sits alone in a 128-byte line (every
+// warp racing the row adds to it and reads it each round; rows packed into one
+// line would make all warps of the GPU queue on the same L2 line).
+constexpr int kThwStride = 32;  // 32-bit words between the bounds of consecutive rows
+
 struct SamplePlan {
   int R1 = 0;          // logit rows per batch row, 2*gamma+1
   int npmax = 0;       // partials per row the workspace holds (one per 1024 logits)
   int nsplit3 = 0;     // most CTAs per batch row in the inverse-transform draw
   int nrace = 0;       // race slices per batch row (the most race CTAs per batch row)
-  // the race's shared bound per batch row [B] (zeroed by the sweep), the race
+  // the race's shared bound per batch row [B][kThwStride] (zeroed by the sweep), the race
   // candidates [B][nrace][2] (two per race CTA), then the sweep's partials
   // [B][R1][partials per row] as float2 pairs
   size_t off_thw = 0, off_cword = 0, off_part1 = 0;
@@ -110,8 +115,7 @@ inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
   p.nsplit3 = (int)ceil_div(V, kChunkDraw);
   p.nrace = (int)race_slices(V);
   size_t o = 0;
-  p.off_thw = o;      o += sizeof(uint32_t) * (size_t)B;
-  o = (o + 7) & ~(size_t)7;
+  p.off_thw = o;      o += sizeof(uint32_t) * kThwStride * (size_t)B;
   p.off_cword = o;    o += sizeof(uint64_t) * 2 * (size_t)B * p.nrace;
   p.off_part1 = o;    o = align_up(o + 8 * (size_t)B * p.R1 * (size_t)p.npmax);
   p.cnt_bytes = 2 * sizeof(uint32_t) * (size_t)B;

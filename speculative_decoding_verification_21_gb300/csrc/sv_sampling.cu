@@ -80,7 +80,7 @@ __device__ __forceinline__ void zero_draw_counters(const SweepCtx& x) {
   if (blockIdx.x == 0 && x.done)
     for (int i = threadIdx.x; i < x.B; i += blockDim.x) x.done[i] = 0u;
   if (blockIdx.x == 0 && x.thw)
-    for (int i = threadIdx.x; i < x.B; i += blockDim.x) x.thw[i] = 0u;
+    for (int i = threadIdx.x; i < x.B; i += blockDim.x) x.thw[(int64_t)i * kThwStride] = 0u;
 }
 
 template <int DT, bool TOPK>
@@ -787,7 +787,8 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) k_race(SweepCtx x, R
   const int64_t whi = min(chi, wlo + wlen);
   KeyTop2 t = key_top2_empty();
   float th = -kInf;
-  if (wlo < whi) race_draw<DT, TOPK>(x, b, st, resid, wlo, whi, a.vec, t, th, x.thw + b, sb);
+  if (wlo < whi) race_draw<DT, TOPK>(x, b, st, resid, wlo, whi, a.vec, t, th,
+                                       x.thw + (int64_t)b * kThwStride, sb);
   t = key_warp(t);
   if (lane == 0) s_t[warp] = t;
   __syncthreads();
