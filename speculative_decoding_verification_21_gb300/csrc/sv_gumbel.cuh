@@ -382,7 +382,8 @@ __device__ __forceinline__ void race_rounds(const char* rt, const char* rd, int6
       th = fmaxf(th, __uint_as_float(g));
       known = fmaxf(known, __uint_as_float(g));
     }
-    if (!(th > 0.0f)) {  // the same in every lane: seeds from each lane's first run
+    const bool seeded = !(th > 0.0f);  // this warp's first round: its bound is still loose
+    if (seeded) {  // the same in every lane: seeds from each lane's first run
       float k = -kInf;
       if (lane < nrun) {
         Raw8<DT> a, d;
@@ -410,6 +411,17 @@ __device__ __forceinline__ void race_rounds(const char* rt, const char* rd, int6
         const uint32_t R = prune_word(half_max<DT>(xt, h), st, tau);
 #pragma unroll
         for (int e = 4 * h; e < 4 * h + 4; ++e) live |= (rw[u][e] >= R ? 1u : 0u) << e;
+      }
+      if (RESID && !TOPK && seeded) {
+        // under the loose first bound, also drop the entries whose residual weight
+        // is certainly 0: 2^a below 2^d by far more than the error of ex2 (their
+        // key would be -inf, which never enters the best two)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float a = __fmaf_rn(run_at<DT>(xt, e), st.c, -st.mct);
+          const float d = __fmaf_rn(run_at<DT>(xd, e), st.c, kd);
+          if (a < d - 0x1p-6f) live &= ~(1u << e);
+        }
       }
       const int64_t v0 = lo + 8 * (int64_t)r;
       while (live != 0u) {
