@@ -88,7 +88,7 @@ def tensor_peaks():
 
 # DRAM bytes per launch of the verify sweep from an ncu capture of the same
 # workload (profiles/ holds the summary); None when the kernel changed since.
-SWEEP_TRAFFIC_BYTES = 150913024  # 147.793 MB read + 3.120 MB written (ncu, one launch)
+SWEEP_TRAFFIC_BYTES = 150702592  # 147.796 MB read + 2.907 MB written (ncu, one launch)
 LMHEAD_PASS1_TRAFFIC_BYTES = 1580866592  # 1577.972 MB read + 2.895 MB written (ncu, one launch)
 
 
