@@ -96,13 +96,11 @@ struct SamplePlan {
   int R1 = 0;          // logit rows per batch row, 2*gamma+1
   int npmax = 0;       // partials per row the workspace holds (one per 1024 logits)
   int nsplit3 = 0;     // most CTAs per batch row in the inverse-transform draw
-  int nrace = 0;       // race slices per batch row (the most race CTAs per batch row)
-  // the race's shared bound per batch row [B][kThwStride] (zeroed by the sweep), the race
-  // candidates [B][nrace][2] (two per race CTA), then the sweep's partials
-  // [B][R1][partials per row] as float2 pairs
-  size_t off_thw = 0, off_cword = 0, off_part1 = 0;
+  // the race's shared bound per batch row [B][kThwStride] (zeroed by the sweep), then the
+  // sweep's partials [B][R1][partials per row] as float2 pairs
+  size_t off_thw = 0, off_part1 = 0;
   // counters: [B] overlap CTAs (zeroed by the first draw CTA of each batch row),
-  // then [B] draw CTAs that finished (zeroed by the sweep)
+  // then [B] inverse-transform draw CTAs that finished (zeroed by the sweep)
   size_t off_cnt = 0, cnt_bytes = 0, off_rowstat = 0, off_state = 0, off_segsum = 0,
          off_ctot = 0, off_alpha = 0, off_thr = 0, total = 0;
 };
@@ -113,10 +111,8 @@ inline SamplePlan make_sample_plan(int B, int gamma, int64_t V) {
   p.R1 = 2 * gamma + 1;
   p.npmax = (int)max_row_partials(V);
   p.nsplit3 = (int)ceil_div(V, kChunkDraw);
-  p.nrace = (int)race_slices(V);
   size_t o = 0;
   p.off_thw = o;      o += sizeof(uint32_t) * kThwStride * (size_t)B;
-  p.off_cword = o;    o += sizeof(uint64_t) * 2 * (size_t)B * p.nrace;
   p.off_part1 = o;    o = align_up(o + 8 * (size_t)B * p.R1 * (size_t)p.npmax);
   p.cnt_bytes = 2 * sizeof(uint32_t) * (size_t)B;
   p.off_cnt = o;      o = align_up(o + p.cnt_bytes);

@@ -12,14 +12,16 @@
 //             sv_units.cuh.  k_sweep (any shape): one CTA per 8192-logit split.
 //   top-k / top-p thresholds (k_topk_cand, k_topk, k_topp), then a thresholded
 //             sweep where needed.
-//   k_race    the default draw: one CTA per (batch row, slices); every CTA takes
-//             its batch row's decision from the partials (accept test, first
-//             rejection by a warp ballot), races its slices by Gumbel-max
-//             (sv_gumbel.cuh), and the CTA of the batch row that finishes last
-//             merges the CTAs' best two and emits.
+//   k_race    the default draw: one thread-block cluster per batch row, one CTA
+//             per share of its slices; every CTA takes its batch row's decision
+//             from the partials (accept test, first rejection by a warp ballot),
+//             races its slices by Gumbel-max (sv_gumbel.cuh), and the cluster's
+//             first CTA merges the CTAs' best two over distributed shared memory
+//             and emits.
 //   k_draw    the opt-in inverse-transform draw (sv_draw.cuh), same structure.
 //   k_alpha   optional overlap sum_v min(p_i, q_i) ("The acceptance rate is the
 //             overlap of p and q").
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -36,6 +38,8 @@
 #include "sv_sweep.cuh"
 #include "sv_units.cuh"
 #include "sv_launch.h"
+
+namespace cg = cooperative_groups;
 
 namespace sv {
 
@@ -744,18 +748,20 @@ __global__ void __launch_bounds__(kThreads, kDrawCtasPerSm) k_draw(SweepCtx x, D
 // takes its batch row's decision (decide_in_cta); each warp then races one
 // eighth of the CTA's share of the slices (kRaceSlice entries each) in one
 // contiguous piece, its rounds of loads staged in shared memory with the next
-// rounds in flight.  The CTA keeps the best two, and the CTA of the batch row
-// that finishes last (a per-batch-row counter the sweep zeroes) merges them
-// and emits.  The warps racing one draw share their bound on the second-best
-// key through a word per batch row (zeroed by the sweep).
+// rounds in flight.  The warps racing one draw share their bound on the
+// second-best key through a word per batch row (zeroed by the sweep).  The
+// batch row's CTAs form one thread-block cluster: each keeps its best two in
+// shared memory, and after a cluster barrier the first reads the others' over
+// distributed shared memory, merges and emits (no global counter, fence or
+// candidate words on the way; a second barrier keeps the others resident while
+// it reads).
 // --------------------------------------------------------------------------
 struct RaceArgs {
-  uint64_t* cword;        // [B][nsplit][2] the race's best two per CTA
   uint32_t* alpha_cnt;    // [B] counters of the optional overlap kernel, zeroed here
-  uint32_t* done;         // [B] CTAs of the batch row that finished (zeroed by the sweep)
-  int nsplit;             // CTAs per batch row
+  int nsplit;             // CTAs per batch row: the cluster size, 1..kRaceMaxCluster
   bool vec;               // 16-byte loads of 8 entries are aligned in every row
 };
+constexpr int kRaceMaxCluster = 8;  // the portable cluster size
 constexpr size_t kRaceSmemBytes = (kThreads / 32) * kRaceWarpSmem;
 
 template <int DT, bool TOPK>
@@ -771,10 +777,11 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) k_race(SweepCtx x, R
   __shared__ DraftAt sda[32];
   __shared__ DrawState s_st;
   __shared__ KeyTop2 s_t[kWarps];
-  __shared__ int s_last;
+  __shared__ KeyTop2 s_best;  // the CTA's best two, read by the cluster's first CTA
   decide_in_cta<DT, TOPK>(x, b, split == 0, a.alpha_cnt, srs, sda, &s_st);
   const DrawState st = s_st;
-  if (st.mode == kDrawDone) return;  // the same in every CTA of the batch row
+  // the same in every CTA of the batch row, so the whole cluster leaves together
+  if (st.mode == kDrawDone) return;
   const bool resid = st.mode == kDrawResidual;
   // the CTA's share of the batch row's slices, one contiguous piece per warp (a
   // multiple of 8 entries each), so that a warp's rounds follow one another
@@ -795,26 +802,20 @@ __global__ void __launch_bounds__(kThreads, kRaceCtasPerSm) k_race(SweepCtx x, R
   if (warp == 0) {
     KeyTop2 r = (lane < kWarps) ? s_t[lane] : key_top2_empty();
     r = key_warp(r);
-    if (lane == 0) {
-      uint64_t* o = a.cword + ((int64_t)b * a.nsplit + split) * 2;
-      o[0] = key_word(r.a);
-      o[1] = key_word(r.b);
-      __threadfence();  // this CTA's candidates before its arrival
-      s_last = (atomicAdd(a.done + b, 1u) == (unsigned)(a.nsplit - 1)) ? 1 : 0;
-    }
+    if (lane == 0) s_best = r;
   }
-  __syncthreads();
-  if (!s_last || warp != 0) return;
-  __threadfence();  // every other CTA's candidates are visible from here
-  KeyTop2 T = key_top2_empty();
-  const unsigned long long* cw =
-      reinterpret_cast<const unsigned long long*>(a.cword) + (int64_t)b * a.nsplit * 2;
-  for (int j = lane; j < 2 * a.nsplit; j += 32) key_insert(T, key_unword(__ldcg(cw + j)));
-  T = key_warp(T);
-  if (resid && T.a.i < 0)
-    race_fallback_emit<DT, TOPK>(x, b, st, a.vec, st.flags, sb);
-  else
-    race_emit<DT>(x, b, st, T, resid, st.flags);
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();  // every CTA's best two are in its shared memory
+  if (split == 0 && warp == 0) {
+    // the batch row's best two over its CTAs (lane j: CTA j's), then the emit
+    KeyTop2 T = (lane < a.nsplit) ? *cluster.map_shared_rank(&s_best, lane) : key_top2_empty();
+    T = key_warp(T);
+    if (resid && T.a.i < 0)
+      race_fallback_emit<DT, TOPK>(x, b, st, a.vec, st.flags, sb);
+    else
+      race_emit<DT>(x, b, st, T, resid, st.flags);
+  }
+  cluster.sync();  // no CTA leaves while the first may still read its shared memory
 }
 
 // --------------------------------------------------------------------------
@@ -880,7 +881,8 @@ k_alpha(const void* __restrict__ zt, const void* __restrict__ zd, int gamma, int
 struct DeviceInfo {
   int sms = 0;
   int sweep_ctas_per_sm[2][2] = {{0, 0}, {0, 0}};  // by dtype, then top-k variant
-  int race_ctas_per_sm[2][2] = {{0, 0}, {0, 0}};   // the same for k_race
+  // k_race clusters of c CTAs that can be resident at once, c = 1..kRaceMaxCluster
+  int race_clusters[2][2][kRaceMaxCluster + 1] = {};
   bool ready = false;
 };
 
@@ -904,8 +906,23 @@ static cudaError_t sweep_setup(DeviceInfo& d) {
   e = cudaFuncSetAttribute(k_race<DT, TOPK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kRaceSmemBytes);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.race_ctas_per_sm[DT][TOPK ? 1 : 0],
-                                                       k_race<DT, TOPK>, kThreads, kRaceSmemBytes);
+  for (int c = 1; c <= kRaceMaxCluster; ++c) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)c);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kRaceSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&d.race_clusters[DT][TOPK ? 1 : 0][c], k_race<DT, TOPK>,
+                                       &cfg);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 static std::mutex g_dev_mu;
 static DeviceInfo g_dev[64];
@@ -1071,18 +1088,20 @@ static cudaError_t launch_sample_t(const void* zt, const void* zd, const int32_t
                : launch_pdl(k_draw<DT, false>, dim3((unsigned)(nsplit * B)), dim3(kThreads), 0,
                             stream, sx, da);
   } else {
-    // Gumbel-max: one resident wave of race CTAs (every CTA takes its batch
-    // row's decision, so a second wave would pay that latency again), at least
-    // one slice per warp
+    // Gumbel-max: one cluster of race CTAs per batch row, all clusters resident
+    // at once (every CTA takes its batch row's decision, so a second wave would
+    // pay that latency again), at most one slice per warp
     const int64_t S = race_slices(V);
-    const int64_t rslots = (int64_t)di->sms * max(1, di->race_ctas_per_sm[DT][masked ? 1 : 0]);
-    int64_t nsplit = ceil_div(S, (int64_t)(kThreads / 32));
-    if ((int64_t)B * nsplit > rslots) nsplit = (rslots / B > 1) ? rslots / B : 1;
-    RaceArgs ra{reinterpret_cast<uint64_t*>(ws + pl.off_cword), alpha_cnt, done, (int)nsplit, vec};
-    e = masked ? launch_pdl(k_race<DT, true>, dim3((unsigned)(nsplit * B)), dim3(kThreads),
-                            kRaceSmemBytes, stream, sx, ra)
-               : launch_pdl(k_race<DT, false>, dim3((unsigned)(nsplit * B)), dim3(kThreads),
-                            kRaceSmemBytes, stream, sx, ra);
+    const int* ncl = di->race_clusters[DT][masked ? 1 : 0];
+    int nsplit = (int)min((int64_t)kRaceMaxCluster, ceil_div(S, (int64_t)(kThreads / 32)));
+    while (nsplit > 1 && B > ncl[nsplit]) --nsplit;
+    RaceArgs ra{alpha_cnt, nsplit, vec};
+    e = masked ? launch_pdl_cluster(k_race<DT, true>, dim3((unsigned)(nsplit * B)),
+                                    dim3(kThreads), kRaceSmemBytes, (unsigned)nsplit, stream, sx,
+                                    ra)
+               : launch_pdl_cluster(k_race<DT, false>, dim3((unsigned)(nsplit * B)),
+                                    dim3(kThreads), kRaceSmemBytes, (unsigned)nsplit, stream, sx,
+                                    ra);
   }
   if (e != cudaSuccess) return e;
   mark(2, stream);
