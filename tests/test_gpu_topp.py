@@ -70,7 +70,10 @@ def test_sample_b64_topp(top_p, top_k):
                                                   (torch.float32, 1001, 0.6, False, 0.7),
                                                   (torch.bfloat16, 4099, 0.9, False, 1.0),
                                                   (torch.bfloat16, 2048, 0.7, True, 1.0),
-                                                  (torch.float32, 3000, 0.3, True, 1.3)])
+                                                  (torch.float32, 3000, 0.3, True, 1.3),
+                                                  (torch.bfloat16, 4099, 0.99, False, 1.0),
+                                                  (torch.float32, 3000, 0.999, False, 0.7),
+                                                  (torch.float32, 1000, 0.999, True, 1.0)])
 def test_topp_shapes_and_ties(dtype, V, top_p, ties, T):
     B, g = 24, 3
     zt, zd, xt = case(V, B, g, dtype, seed=V, ties=ties)
