@@ -6,7 +6,8 @@ B=64, gamma=4, V=128256, bf16 logits, T=0.8, draft noise sigma=1 (Zipf(1.1)
 target bias).  The call is two kernels: k_sweep_vec (online-softmax statistics
 of all 2*gamma+1 logit rows, 4 KB chunks) and k_race (per CTA the batch row's
 accept test, then the Gumbel-max residual/bonus draw over slices of the draw
-row, merged by the last CTA of the batch row).  Metric: verify rounds per
+row; the batch row's CTAs form one cluster whose first CTA merges their best
+keys over distributed shared memory).  Metric: verify rounds per
 second (whole job, all GPUs); the line also carries verified positions/s
 (B*gamma per round).  The roofline object is the verify sweep's (HBM-bound);
 the race, which takes a comparable time, is issue-bound and is reported beside

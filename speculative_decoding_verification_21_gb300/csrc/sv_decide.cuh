@@ -51,7 +51,8 @@ struct SweepCtx {
   uint8_t* out_flags;
   float inv_lenience;    // 1/l of the lenient comparison u <= p/(l q); 1: the exact round
   const float* thr;      // [B][R1] top-k thresholds (logits below have weight 0) or null
-  uint32_t* done;        // [B] arrival counters of the draw, zeroed by every sweep
+  uint32_t* done;        // [B] arrival counters of the inverse-transform draw, zeroed by
+                         // every sweep
   uint32_t* thw;         // [B][kThwStride] the race's shared lower bound on its second-best
                          // key (float bits, 0: none yet; word 0 of each row's line), zeroed
                          // by every sweep

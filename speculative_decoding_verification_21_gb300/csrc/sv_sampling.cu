@@ -78,8 +78,9 @@ __device__ __forceinline__ void for_each_in_chunk(const char* row, int64_t lo, i
   for (int64_t v = a1 + tid; v < hi; v += blockDim.x) f_one(v, load_logit<DT>(row, v));
 }
 
-// The draw's per-batch-row arrival counters start at 0 in every call; the draw
-// touches them only after this grid has completed.
+// The inverse-transform draw's per-batch-row arrival counters and the race's
+// shared bounds start at 0 in every call; the draw touches them only after this
+// grid has completed.
 __device__ __forceinline__ void zero_draw_counters(const SweepCtx& x) {
   if (blockIdx.x == 0 && x.done)
     for (int i = threadIdx.x; i < x.B; i += blockDim.x) x.done[i] = 0u;
