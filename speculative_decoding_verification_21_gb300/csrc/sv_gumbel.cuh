@@ -13,11 +13,12 @@
 // lane keeps its two largest keys w_v / E_v (a reciprocal and a product per
 // entry, the update by selects); the warp, then the merge, keep the best two of
 // those.  Most entries never reach the key: once a warp holds two candidates,
-// an entry whose Philox word shows an E_v too large for any weight of its run
-// to beat the second-best key is dropped by one integer compare.  When the two best keys lie within 2^-10 of each other,
-// they are re-decided in double precision from the logits (the key's
-// definition, log w + g), so that the winner differs from an exact evaluation
-// only where the exact keys themselves are within the rounding of the row sums.
+// an entry whose Philox word shows an E_v too large for any weight of its block
+// of four (one Philox block) to beat the second-best key is dropped by one
+// integer compare.  When the two best keys lie within 2^-10 of each other, they
+// are re-decided in double precision from the logits (the key's definition,
+// log w + g), so that the winner differs from an exact evaluation only where
+// the exact keys themselves are within the rounding of the row sums.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -290,12 +291,16 @@ struct RaceRound {
 // kRaceStages - 1 rounds' copies in flight while one round is raced; a run cut
 // by the row's end (or any run of rows that do not start on 16-byte
 // boundaries, !vec) is loaded directly.  Each lane reads back only its own
-// copies.  Round starts are multiples of 8.  `th` (the same in every lane) is
-// the warp's bound on the second-best key, carried from one call to the next;
-// while it is unset, the largest-logit entry of each lane's first run is keyed
-// first to set it.  `thw` (or null) is a bound shared by every warp racing the
-// same draw: each round reads it and raises it to th afterwards (any warp's
-// bound holds for the union of their candidates).
+// copies.  Round starts are multiples of 8.  A round computes its Philox words
+// first, then waits for its copies and for the shared bound (the words cover
+// both latencies).  `th` (the same in every lane) is the warp's bound on the
+// second-best key, carried from one call to the next; while it is unset, the
+// largest-logit entry of each lane's first run is keyed first to set it, and
+// in that first round residual entries of certainly zero weight are dropped
+// too.  `thw` (or null) is a bound shared by every warp racing the same draw:
+// each round reads it and raises it to th afterwards when th rose above what
+// it is known to hold (any warp's bound holds for the union of their
+// candidates).
 template <int DT, bool RESID, bool TOPK, class Next>
 __device__ __forceinline__ void race_rounds(const char* rt, const char* rd, int64_t V, bool vec,
                                             const DrawState& st, float kd, uint64_t seed,
