@@ -38,7 +38,8 @@
  *   - All array arguments are DEVICE pointers, row-major and contiguous; the caller
  *     owns every buffer.  The library never allocates or frees device memory and
  *     keeps no state between calls except per-device caches of launch facts (SM
- *     count, resident CTAs per SM) and, for spec_verify_noalloc only, its one
+ *     count, resident CTAs per SM, resident CTA clusters per cluster size) and, for
+ *     spec_verify_noalloc only, its one
  *     static scratch array and that array's cached device address (see there).
  *   - Work is queued on `cuda_stream` (a cudaStream_t; NULL = legacy default stream)
  *     and the call returns at once.  The return value reports only errors the host
